@@ -1,0 +1,193 @@
+/*
+ * sparsecos: exact bulk cosine similarity between two CSR batches of
+ * high-dimensional sparse embeddings, on one NVIDIA GB300 (sm_103a).
+ *
+ *   S[q, i] = (Q_q . I_i) / (|Q_q|_2 |I_i|_2)
+ *
+ * for every query row q of Q and every item row i of I, written as a dense
+ * row-major float32 matrix.  The operation is the one set out in the blog
+ * post "Engineering practice for bulk similarity calculation over sparse
+ * embeddings": section 2.3 (the full n_query x n_item float32 result, every
+ * entry exact, not a top-K), section 3.1 (cosine; the sparse dot product
+ * summed over the intersection of the two supports), section 5.2 (norms over
+ * the stored nonzeros only, computed once and passed in), section 2.2 and
+ * 4.4 (items streamed in chunks of 8,192 rows; normalise right after the
+ * product).
+ *
+ * Conventions for every call:
+ *  - Matrices are CSR: int64 indptr[n_rows + 1] with indptr[0] = 0 and
+ *    indptr non-decreasing, int32 indices[nnz] strictly increasing within a
+ *    row and in [0, dim), float32 values[nnz].  Explicit zero values are
+ *    allowed and count as ordinary entries.
+ *  - A row with no nonzeros (norm 0) has cosine 0 with every row.
+ *  - Device pointers are device memory of the handle's device, owned by the
+ *    caller, and must stay valid until the work queued on `stream` is done.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call that takes a stream only queues work on it and
+ *    returns; a fault in a kernel shows at the next synchronisation or via
+ *    ss_check_device.
+ *  - No call throws; each returns an ss_status.  A call that returns an error
+ *    before queueing work leaves the handle usable.  ss_last_error gives a
+ *    message for the last error on a handle.
+ *  - A handle is used by one host thread at a time and drives one GPU.
+ */
+#ifndef SPARSECOS_H
+#define SPARSECOS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t ss_status;
+
+#define SS_OK 0
+#define SS_ERR_INVALID_ARG 1  /* null pointer, bad size, mismatched shapes */
+#define SS_ERR_UNSORTED 2     /* indices not strictly increasing in a row */
+#define SS_ERR_OUT_OF_RANGE 3 /* an index outside [0, dim), or bad indptr */
+#define SS_ERR_OOM 4          /* a device or pinned-host allocation failed */
+#define SS_ERR_CUDA 5         /* a CUDA runtime call failed */
+#define SS_ERR_DEVICE_CHECK 6 /* a kernel found an input it could not use */
+#define SS_ERR_TIMEOUT 7      /* a host wait on the GPU ran out of time */
+#define SS_ERR_LIMIT 8        /* a size beyond a documented maximum */
+
+/* ss_create flags */
+#define SS_VALIDATE 0x1 /* check CSR inputs on the device (synchronises) */
+
+/* Largest chunk the index builder accepts (item numbers in a chunk are
+ * stored in 16 bits). */
+#define SS_MAX_CHUNK_ROWS 65536
+
+typedef struct ss_handle ss_handle;
+typedef struct ss_index ss_index;
+
+/* A CSR matrix.  For calls marked "device" the three arrays are device
+ * memory; for ss_bulk_cosine_host they are host memory. */
+typedef struct ss_csr {
+  const int64_t *indptr;  /* [n_rows + 1] */
+  const int32_t *indices; /* [nnz] */
+  const float *values;    /* [nnz] */
+  int64_t n_rows;
+  int64_t nnz; /* = indptr[n_rows] */
+  int64_t dim; /* number of dimensions d; indices lie in [0, d) */
+} ss_csr;
+
+/*
+ * Creates a handle on `device` for matrices of dimension `dim` whose items
+ * are streamed in chunks of `chunk_rows` rows (the post picks 8,192,
+ * section 3.3).  Allocates the handle's device workspace (the chunk index
+ * and its scratch).  chunk_rows must lie in [1, SS_MAX_CHUNK_ROWS].
+ * Errors: SS_ERR_INVALID_ARG, SS_ERR_LIMIT, SS_ERR_OOM, SS_ERR_CUDA.
+ */
+ss_status ss_create(ss_handle **out, int device, int64_t dim, int32_t chunk_rows,
+                    int32_t flags);
+
+/*
+ * Row norms (section 5.2, computed once, section 4.4): for every row r of m
+ * (device CSR), inv_norms[r] = 1 / sqrt(sum_j values[j]^2) over the row's
+ * stored values, or 0 when that sum is 0.  The sum of squares is taken in
+ * double precision and the reciprocal square root rounded once to float.
+ * inv_norms: device, float32[m->n_rows], written.
+ * With SS_VALIDATE the CSR is checked first (SS_ERR_UNSORTED,
+ * SS_ERR_OUT_OF_RANGE) and the call synchronises `stream`.
+ */
+ss_status ss_row_norms(ss_handle *h, const ss_csr *m, float *inv_norms, void *stream);
+
+/*
+ * Per-chunk inverted index (the chunk's CSR turned into lists by dimension):
+ * indexes item rows [row_begin, row_end) of `items` (device CSR), with
+ * 0 < row_end - row_begin <= chunk_rows.  The index is owned by the handle
+ * and stays valid until the next ss_build_item_index or ss_destroy on it;
+ * `*out` receives a pointer to it.  Work on `stream` must not overlap a
+ * score call still using the previous index (queue both on one stream).
+ * Errors: SS_ERR_INVALID_ARG, SS_ERR_LIMIT, SS_ERR_OOM, SS_ERR_CUDA.
+ */
+ss_status ss_build_item_index(ss_handle *h, const ss_csr *items, int64_t row_begin,
+                              int64_t row_end, ss_index **out, void *stream);
+
+/*
+ * Scores every query row against one indexed chunk and normalises in the
+ * same kernel (section 4.4):
+ *   out[q * ld_out + c] = dot(Q_q, I_{row_begin + c}) * inv_q[q] * inv_i[c]
+ * for q < queries->n_rows and c < row_end - row_begin.
+ * queries: device CSR; inv_q: device float32[n_q] from ss_row_norms;
+ * inv_i: device float32 pointer to the chunk's first item norm (the item
+ * norm array + row_begin); out: device float32, row-major with leading
+ * dimension ld_out >= chunk width.  Products and sums are float32.
+ * Errors: SS_ERR_INVALID_ARG, SS_ERR_CUDA.
+ */
+ss_status ss_score_chunk(ss_handle *h, const ss_csr *queries, const float *inv_q,
+                         const ss_index *idx, const float *inv_i, float *out, int64_t ld_out,
+                         void *stream);
+
+/*
+ * The whole device-resident pass: splits the items into chunks of the
+ * handle's chunk_rows (section 2.2, "streaming batch"), and for each chunk
+ * builds the index and scores it into
+ *   out[q * ld_out + i], i in [0, items->n_rows).
+ * inv_q / inv_i: device norms from ss_row_norms.  out: device float32 with
+ * ld_out >= items->n_rows.  Equivalent to calling ss_build_item_index and
+ * ss_score_chunk per chunk in order on `stream`.
+ */
+ss_status ss_score_all(ss_handle *h, const ss_csr *queries, const float *inv_q,
+                       const ss_csr *items, const float *inv_i, float *out, int64_t ld_out,
+                       void *stream);
+
+/*
+ * Receives one finished chunk of the result in host memory:
+ *   tile[q * ld + c] = S[q, item_begin + c], q < n_q, c < item_end - item_begin.
+ * The tile is only valid during the call.  A nonzero return stops the pass
+ * (ss_bulk_cosine_host then returns SS_ERR_INVALID_ARG).
+ */
+typedef int (*ss_chunk_consumer)(void *user, int64_t chunk, int64_t item_begin,
+                                 int64_t item_end, const float *tile, int64_t ld, int64_t n_q);
+
+/*
+ * End to end from host memory (sections 2.2 and 4.4): copies the host CSR
+ * batches to the device, computes both norm vectors, then for each item
+ * chunk builds the index, scores it, and streams the chunk's result back to
+ * the host through a ring of `ring_depth` (>= 2) pinned host buffers, with
+ * the device-to-host copies on a second stream so they overlap the next
+ * chunk's kernels.  Each finished chunk is copied into out_host (row-major,
+ * ld_out >= items->n_rows; may be NULL) and/or handed to `consumer` (may be
+ * NULL).  Blocks until the last chunk has been delivered.  Device buffers
+ * and pinned slots are allocated and freed by the call.
+ * timeout_ms bounds each host wait on the GPU (0 = 60000 ms);
+ * SS_ERR_TIMEOUT if one runs out.
+ */
+ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *queries_host,
+                              const ss_csr *items_host, float *out_host, int64_t ld_out,
+                              ss_chunk_consumer consumer, void *user, int32_t ring_depth,
+                              int32_t timeout_ms);
+
+/*
+ * Checks a device CSR on the device (indptr[0] = 0, indptr non-decreasing
+ * and ending at nnz, indices strictly increasing within rows and in
+ * [0, dim)).  Synchronises `stream`.  Returns SS_OK, SS_ERR_UNSORTED or
+ * SS_ERR_OUT_OF_RANGE.
+ */
+ss_status ss_validate_csr(ss_handle *h, const ss_csr *m, void *stream);
+
+/*
+ * Synchronises `stream` and reports whether a kernel of this handle flagged
+ * an input it could not use (SS_ERR_DEVICE_CHECK, e.g. a chunk whose nnz
+ * exceeds the index capacity), then clears the flag.
+ */
+ss_status ss_check_device(ss_handle *h, void *stream);
+
+/* Frees the handle and its device workspace (synchronises the device). */
+ss_status ss_destroy(ss_handle *h);
+
+/* Static text for a status code. */
+const char *ss_status_string(ss_status s);
+
+/* Message of the last error on the handle ("" if none); valid until the
+ * next call on the handle. */
+const char *ss_last_error(const ss_handle *h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSECOS_H */

@@ -1,0 +1,197 @@
+"""Exact bulk cosine similarity between CSR batches of sparse embeddings on GB300.
+
+A thin Python layer over the C ABI of ``include/sparsecos.h``: it turns torch
+tensors into pointers and sizes and calls the CUDA library.  Every step of the
+computation runs in the library's kernels; this package has no fallback path
+and raises if the library is missing.
+
+    S[q, i] = (Q_q . I_i) / (|Q_q|_2 |I_i|_2)
+
+The calls mirror the C ABI: ``row_norms``, ``build_item_index``,
+``score_chunk``, ``score_all`` (the device-resident chunk loop) and
+``bulk_cosine_host`` (host buffers in, result streamed back chunk by chunk).
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Callable, Optional
+
+import numpy as np
+import torch
+
+from . import _abi
+from ._abi import SparseCosError, SS_VALIDATE  # noqa: F401
+
+DEFAULT_CHUNK_ROWS = 8192
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+@dataclass
+class DeviceCsr:
+    """A CSR matrix in device memory (int64 indptr, int32 indices, float32 values)."""
+
+    indptr: torch.Tensor
+    indices: torch.Tensor
+    values: torch.Tensor
+    dim: int
+
+    @property
+    def n_rows(self) -> int:
+        return int(self.indptr.shape[0] - 1)
+
+    @property
+    def nnz(self) -> int:
+        return int(self.indices.shape[0])
+
+    def abi(self) -> _abi.ss_csr:
+        return _abi.ss_csr(self.indptr.data_ptr(), self.indices.data_ptr(), self.values.data_ptr(),
+                           self.n_rows, self.nnz, int(self.dim))
+
+    @staticmethod
+    def from_host(batch, device="cuda") -> "DeviceCsr":
+        """Copies a host CSR (anything with indptr/indices/values/dim arrays)."""
+        def dev(a, dt):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).to(device)
+        return DeviceCsr(dev(batch.indptr, np.int64), dev(batch.indices, np.int32),
+                         dev(batch.values, np.float32), int(batch.dim))
+
+
+def _host_csr(batch):
+    indptr = np.ascontiguousarray(batch.indptr, dtype=np.int64)
+    indices = np.ascontiguousarray(batch.indices, dtype=np.int32)
+    values = np.ascontiguousarray(batch.values, dtype=np.float32)
+    m = _abi.ss_csr(indptr.ctypes.data, indices.ctypes.data, values.ctypes.data,
+                    int(indptr.shape[0] - 1), int(indices.shape[0]), int(batch.dim))
+    return m, (indptr, indices, values)
+
+
+class SparseCosine:
+    """One library handle: a device, a dimension and a chunk size."""
+
+    def __init__(self, dim: int, chunk_rows: int = DEFAULT_CHUNK_ROWS, device: int = 0,
+                 validate: bool = False):
+        self._lib = _abi.load()
+        self.dim = int(dim)
+        self.chunk_rows = int(chunk_rows)
+        self.device = int(device)
+        h = ctypes.c_void_p()
+        st = self._lib.ss_create(ctypes.byref(h), self.device, self.dim, self.chunk_rows,
+                                 SS_VALIDATE if validate else 0)
+        if st != _abi.SS_OK:
+            raise SparseCosError(st, f"ss_create: {self._lib.ss_status_string(st).decode()}")
+        self._h = h
+
+    # -- plumbing
+    def _check(self, st: int, what: str):
+        if st != _abi.SS_OK:
+            msg = self._lib.ss_last_error(self._h).decode() if self._h else ""
+            raise SparseCosError(st, f"{what}: {self._lib.ss_status_string(st).decode()}: {msg}")
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.ss_destroy(self._h)
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- the calls
+    def row_norms(self, m: DeviceCsr, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty(m.n_rows, dtype=torch.float32, device=m.indptr.device)
+        c = m.abi()
+        self._check(self._lib.ss_row_norms(self._h, ctypes.byref(c), _ptr(out), _stream_ptr(stream)),
+                    "ss_row_norms")
+        return out
+
+    def build_item_index(self, items: DeviceCsr, row_begin: int, row_end: int, stream=None):
+        c = items.abi()
+        idx = ctypes.c_void_p()
+        self._check(self._lib.ss_build_item_index(self._h, ctypes.byref(c), int(row_begin),
+                                                  int(row_end), ctypes.byref(idx),
+                                                  _stream_ptr(stream)), "ss_build_item_index")
+        return idx
+
+    def score_chunk(self, queries: DeviceCsr, inv_q: torch.Tensor, index, inv_i_chunk: torch.Tensor,
+                    out: torch.Tensor, ld_out: int, stream=None):
+        c = queries.abi()
+        self._check(self._lib.ss_score_chunk(self._h, ctypes.byref(c), _ptr(inv_q), index,
+                                             _ptr(inv_i_chunk), _ptr(out), int(ld_out),
+                                             _stream_ptr(stream)), "ss_score_chunk")
+
+    def score_all(self, queries: DeviceCsr, inv_q: torch.Tensor, items: DeviceCsr,
+                  inv_i: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty((queries.n_rows, items.n_rows), dtype=torch.float32,
+                              device=queries.indptr.device)
+        cq, ci = queries.abi(), items.abi()
+        self._check(self._lib.ss_score_all(self._h, ctypes.byref(cq), _ptr(inv_q), ctypes.byref(ci),
+                                           _ptr(inv_i), _ptr(out), int(out.stride(0)),
+                                           _stream_ptr(stream)), "ss_score_all")
+        return out
+
+    def bulk_cosine_host(self, queries, items, out: Optional[np.ndarray] = None,
+                         consumer: Optional[Callable] = None, ring_depth: int = 3,
+                         timeout_ms: int = 0):
+        """Host CSR in, result streamed back chunk by chunk.
+
+        out: a float32 (n_q, n_i) host array (numpy or a CPU torch tensor,
+        ideally page-locked) or None; consumer(chunk, item_begin, item_end,
+        tile) receives each chunk as a (n_q, width) numpy view valid during
+        the call.
+        """
+        cq, keep_q = _host_csr(queries)
+        ci, keep_i = _host_csr(items)
+        out_ptr, ld = ctypes.c_void_p(0), 0
+        if out is not None:
+            if isinstance(out, torch.Tensor):
+                assert out.dtype == torch.float32 and out.device.type == "cpu" and out.stride(1) == 1
+                out_ptr, ld = ctypes.c_void_p(out.data_ptr()), out.stride(0)
+            else:
+                assert out.dtype == np.float32 and out.strides[1] == 4
+                out_ptr, ld = ctypes.c_void_p(out.ctypes.data), out.strides[0] // 4
+        cb = _abi.ss_chunk_consumer(0)
+        if consumer is not None:
+            def _cb(user, chunk, b, e, tile, ld_t, n_q):
+                try:
+                    arr = np.ctypeslib.as_array(tile, shape=(int(n_q), int(ld_t)))[:, : e - b]
+                    r = consumer(int(chunk), int(b), int(e), arr)
+                    return 0 if r is None else int(r)
+                except Exception:  # stop the pass; the error surfaces as a status
+                    return 1
+            cb = _abi.ss_chunk_consumer(_cb)
+        st = self._lib.ss_bulk_cosine_host(self._h, ctypes.byref(cq), ctypes.byref(ci), out_ptr, ld,
+                                           cb, None, int(ring_depth), int(timeout_ms))
+        del keep_q, keep_i
+        self._check(st, "ss_bulk_cosine_host")
+        return out
+
+    def validate_csr(self, m: DeviceCsr, stream=None):
+        c = m.abi()
+        self._check(self._lib.ss_validate_csr(self._h, ctypes.byref(c), _stream_ptr(stream)),
+                    "ss_validate_csr")
+
+    def check_device(self, stream=None):
+        self._check(self._lib.ss_check_device(self._h, _stream_ptr(stream)), "ss_check_device")
+
+
+def library_path() -> str:
+    return _abi.library_path()

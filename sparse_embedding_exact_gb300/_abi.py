@@ -1,0 +1,93 @@
+"""ctypes declarations of the C ABI in include/sparsecos.h.
+
+Loading fails loudly when the library has not been built: there is no
+fallback implementation anywhere in this package.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+SS_OK = 0
+SS_ERR_INVALID_ARG = 1
+SS_ERR_UNSORTED = 2
+SS_ERR_OUT_OF_RANGE = 3
+SS_ERR_OOM = 4
+SS_ERR_CUDA = 5
+SS_ERR_DEVICE_CHECK = 6
+SS_ERR_TIMEOUT = 7
+SS_ERR_LIMIT = 8
+SS_VALIDATE = 0x1
+SS_MAX_CHUNK_ROWS = 65536
+
+
+class ss_csr(ctypes.Structure):
+    _fields_ = [
+        ("indptr", ctypes.c_void_p),
+        ("indices", ctypes.c_void_p),
+        ("values", ctypes.c_void_p),
+        ("n_rows", ctypes.c_int64),
+        ("nnz", ctypes.c_int64),
+        ("dim", ctypes.c_int64),
+    ]
+
+
+ss_chunk_consumer = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.c_int64, ctypes.POINTER(ctypes.c_float), ctypes.c_int64,
+                                     ctypes.c_int64)
+
+_P = ctypes.c_void_p
+_CSR = ctypes.POINTER(ss_csr)
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+
+# name -> (restype, argtypes); one entry per function declared in the header.
+SIGNATURES = {
+    "ss_create": (_I32, [ctypes.POINTER(_P), ctypes.c_int, _I64, _I32, _I32]),
+    "ss_row_norms": (_I32, [_P, _CSR, _P, _P]),
+    "ss_build_item_index": (_I32, [_P, _CSR, _I64, _I64, ctypes.POINTER(_P), _P]),
+    "ss_score_chunk": (_I32, [_P, _CSR, _P, _P, _P, _P, _I64, _P]),
+    "ss_score_all": (_I32, [_P, _CSR, _P, _CSR, _P, _P, _I64, _P]),
+    "ss_bulk_cosine_host": (_I32, [_P, _CSR, _CSR, _P, _I64, ss_chunk_consumer, _P, _I32, _I32]),
+    "ss_validate_csr": (_I32, [_P, _CSR, _P]),
+    "ss_check_device": (_I32, [_P, _P]),
+    "ss_destroy": (_I32, [_P]),
+    "ss_status_string": (ctypes.c_char_p, [_I32]),
+    "ss_last_error": (ctypes.c_char_p, [_P]),
+}
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path) or not _build.up_to_date():
+        if build_if_missing:
+            _build.build()
+        elif not os.path.exists(path):
+            raise ImportError(
+                f"the sparsecos CUDA library is not built ({path} is missing); "
+                "run __graft_entry__.build() or python -m sparse_embedding_exact_gb300.build")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+class SparseCosError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} [status {status}]")
+        self.status = status

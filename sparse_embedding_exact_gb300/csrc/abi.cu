@@ -1,0 +1,281 @@
+// The C ABI: handle lifecycle, argument checks, the chunk loop and the
+// host-buffer streaming pass.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <chrono>
+#include <new>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "internal.cuh"
+
+namespace {
+
+ss_status fail(ss_handle *h, ss_status st, const char *fmt, ...) {
+  if (h) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    h->last_error = buf;
+  }
+  return st;
+}
+
+ss_status cuda_fail(ss_handle *h, cudaError_t e, const char *what) {
+  const ss_status st = (e == cudaErrorMemoryAllocation) ? SS_ERR_OOM : SS_ERR_CUDA;
+  return fail(h, st, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define SS_CUDA(h, call)                                  \
+  do {                                                    \
+    cudaError_t e_ = (call);                              \
+    if (e_ != cudaSuccess) return cuda_fail((h), e_, #call); \
+  } while (0)
+
+inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+ss_status check_csr_args(ss_handle *h, const ss_csr *m, const char *what) {
+  if (!m) return fail(h, SS_ERR_INVALID_ARG, "%s: null matrix", what);
+  if (m->n_rows < 0 || m->nnz < 0)
+    return fail(h, SS_ERR_INVALID_ARG, "%s: negative size", what);
+  if (!m->indptr) return fail(h, SS_ERR_INVALID_ARG, "%s: null indptr", what);
+  if (m->nnz > 0 && (!m->indices || !m->values))
+    return fail(h, SS_ERR_INVALID_ARG, "%s: null indices/values", what);
+  if (m->dim != h->dim)
+    return fail(h, SS_ERR_INVALID_ARG, "%s: dim %lld differs from the handle's %lld", what,
+                (long long)m->dim, (long long)h->dim);
+  if (m->nnz >= ((int64_t)1 << 31))
+    return fail(h, SS_ERR_LIMIT, "%s: nnz %lld exceeds 2^31 - 1", what, (long long)m->nnz);
+  return SS_OK;
+}
+
+ss_status set_device(ss_handle *h) {
+  SS_CUDA(h, cudaSetDevice(h->device));
+  return SS_OK;
+}
+
+ss_status read_status(ss_handle *h, cudaStream_t s, int32_t *code) {
+  SS_CUDA(h, cudaStreamSynchronize(s));
+  SS_CUDA(h, cudaMemcpy(code, h->d_status, sizeof(int32_t), cudaMemcpyDeviceToHost));
+  if (*code != DEV_OK) SS_CUDA(h, cudaMemset(h->d_status, 0, sizeof(int32_t)));
+  return SS_OK;
+}
+
+ss_status status_from_device(ss_handle *h, int32_t code, const char *what) {
+  switch (code) {
+    case DEV_OK:
+      return SS_OK;
+    case DEV_UNSORTED:
+      return fail(h, SS_ERR_UNSORTED, "%s: indices not strictly increasing within a row", what);
+    case DEV_OUT_OF_RANGE:
+      return fail(h, SS_ERR_OUT_OF_RANGE, "%s: index outside [0, dim) or bad indptr", what);
+    case DEV_CAPACITY:
+      return fail(h, SS_ERR_DEVICE_CHECK, "%s: chunk nnz exceeds the index capacity", what);
+    default:
+      return fail(h, SS_ERR_DEVICE_CHECK, "%s: device check code %d", what, code);
+  }
+}
+
+ss_status validate(ss_handle *h, const ss_csr &m, cudaStream_t s, const char *what) {
+  SS_CUDA(h, launch_validate_csr(m, h->d_status, h->sm_count, s));
+  int32_t code = 0;
+  ss_status st = read_status(h, s, &code);
+  if (st != SS_OK) return st;
+  return status_from_device(h, code, what);
+}
+
+// Grows the posting-list capacity to hold `need` entries (synchronises the
+// device when it has to reallocate).
+ss_status ensure_post_capacity(ss_handle *h, int64_t need) {
+  if (need <= h->post_cap) return SS_OK;
+  int64_t cap = std::max<int64_t>(need, h->post_cap + h->post_cap / 2);
+  SS_CUDA(h, cudaDeviceSynchronize());
+  cudaFree(h->post_item);
+  cudaFree(h->post_val);
+  h->post_item = nullptr;
+  h->post_val = nullptr;
+  h->post_cap = 0;
+  SS_CUDA(h, cudaMalloc(&h->post_item, sizeof(uint16_t) * (size_t)cap));
+  SS_CUDA(h, cudaMalloc(&h->post_val, sizeof(float) * (size_t)cap));
+  h->post_cap = cap;
+  return SS_OK;
+}
+
+void free_workspace(ss_handle *h) {
+  cudaFree(h->d_status);
+  cudaFree(h->col_cnt);
+  cudaFree(h->col_ptr);
+  cudaFree(h->scan_part);
+  cudaFree(h->post_item);
+  cudaFree(h->post_val);
+  h->d_status = nullptr;
+  h->col_cnt = h->col_ptr = h->scan_part = nullptr;
+  h->post_item = nullptr;
+  h->post_val = nullptr;
+  h->post_cap = 0;
+}
+
+ss_status build_chunk(ss_handle *h, const ss_csr &items, int64_t rb, int64_t re, cudaStream_t s) {
+  // The chunk holds at most items.nnz entries: size the lists for that.
+  ss_status st = ensure_post_capacity(h, std::max<int64_t>(items.nnz, 1));
+  if (st != SS_OK) return st;
+  SS_CUDA(h, launch_build_index(h, items, rb, re, s));
+  return SS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ss_status_string(ss_status s) {
+  switch (s) {
+    case SS_OK: return "ok";
+    case SS_ERR_INVALID_ARG: return "invalid argument";
+    case SS_ERR_UNSORTED: return "indices not strictly increasing within a row";
+    case SS_ERR_OUT_OF_RANGE: return "index out of range";
+    case SS_ERR_OOM: return "out of memory";
+    case SS_ERR_CUDA: return "CUDA error";
+    case SS_ERR_DEVICE_CHECK: return "device-side check failed";
+    case SS_ERR_TIMEOUT: return "timed out waiting for the GPU";
+    case SS_ERR_LIMIT: return "size beyond a documented limit";
+    default: return "unknown status";
+  }
+}
+
+const char *ss_last_error(const ss_handle *h) { return h ? h->last_error.c_str() : ""; }
+
+ss_status ss_create(ss_handle **out, int device, int64_t dim, int32_t chunk_rows, int32_t flags) {
+  if (!out) return SS_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (dim <= 0 || chunk_rows <= 0) return SS_ERR_INVALID_ARG;
+  if (chunk_rows > SS_MAX_CHUNK_ROWS || dim >= ((int64_t)1 << 31) - 1) return SS_ERR_LIMIT;
+  ss_handle *h = new (std::nothrow) ss_handle();
+  if (!h) return SS_ERR_OOM;
+  h->device = device;
+  h->dim = dim;
+  h->chunk_rows = chunk_rows;
+  h->flags = flags;
+  cudaError_t e = cudaSetDevice(device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, device);
+  h->scan_tiles = scan_tile_count(dim + 1);
+  if (e == cudaSuccess) e = cudaMalloc(&h->d_status, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMalloc(&h->col_cnt, sizeof(int32_t) * (size_t)(dim + 1));
+  if (e == cudaSuccess) e = cudaMalloc(&h->col_ptr, sizeof(int32_t) * (size_t)(dim + 1));
+  if (e == cudaSuccess) e = cudaMalloc(&h->scan_part, sizeof(int32_t) * (size_t)(h->scan_tiles + 1));
+  if (e != cudaSuccess) {
+    const ss_status st = (e == cudaErrorMemoryAllocation) ? SS_ERR_OOM : SS_ERR_CUDA;
+    free_workspace(h);
+    delete h;
+    return st;
+  }
+  *out = h;
+  return SS_OK;
+}
+
+ss_status ss_destroy(ss_handle *h) {
+  if (!h) return SS_ERR_INVALID_ARG;
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  free_workspace(h);
+  delete h;
+  return SS_OK;
+}
+
+ss_status ss_validate_csr(ss_handle *h, const ss_csr *m, void *stream) {
+  if (!h) return SS_ERR_INVALID_ARG;
+  ss_status st = check_csr_args(h, m, "ss_validate_csr");
+  if (st != SS_OK) return st;
+  if ((st = set_device(h)) != SS_OK) return st;
+  return validate(h, *m, as_stream(stream), "ss_validate_csr");
+}
+
+ss_status ss_check_device(ss_handle *h, void *stream) {
+  if (!h) return SS_ERR_INVALID_ARG;
+  ss_status st = set_device(h);
+  if (st != SS_OK) return st;
+  int32_t code = 0;
+  if ((st = read_status(h, as_stream(stream), &code)) != SS_OK) return st;
+  return status_from_device(h, code, "ss_check_device");
+}
+
+ss_status ss_row_norms(ss_handle *h, const ss_csr *m, float *inv_norms, void *stream) {
+  if (!h) return SS_ERR_INVALID_ARG;
+  ss_status st = check_csr_args(h, m, "ss_row_norms");
+  if (st != SS_OK) return st;
+  if (m->n_rows > 0 && !inv_norms) return fail(h, SS_ERR_INVALID_ARG, "ss_row_norms: null output");
+  if ((st = set_device(h)) != SS_OK) return st;
+  cudaStream_t s = as_stream(stream);
+  if (h->flags & SS_VALIDATE) {
+    if ((st = validate(h, *m, s, "ss_row_norms")) != SS_OK) return st;
+  }
+  SS_CUDA(h, launch_row_norms(*m, inv_norms, h->sm_count, s));
+  return SS_OK;
+}
+
+ss_status ss_build_item_index(ss_handle *h, const ss_csr *items, int64_t row_begin,
+                              int64_t row_end, ss_index **out, void *stream) {
+  if (!h) return SS_ERR_INVALID_ARG;
+  if (!out) return fail(h, SS_ERR_INVALID_ARG, "ss_build_item_index: null out");
+  *out = nullptr;
+  ss_status st = check_csr_args(h, items, "ss_build_item_index");
+  if (st != SS_OK) return st;
+  if (row_begin < 0 || row_end <= row_begin || row_end > items->n_rows)
+    return fail(h, SS_ERR_INVALID_ARG, "ss_build_item_index: bad row range [%lld, %lld)",
+                (long long)row_begin, (long long)row_end);
+  if (row_end - row_begin > h->chunk_rows)
+    return fail(h, SS_ERR_LIMIT, "ss_build_item_index: %lld rows exceed chunk_rows %d",
+                (long long)(row_end - row_begin), h->chunk_rows);
+  if ((st = set_device(h)) != SS_OK) return st;
+  if ((st = build_chunk(h, *items, row_begin, row_end, as_stream(stream))) != SS_OK) return st;
+  *out = &h->index;
+  return SS_OK;
+}
+
+ss_status ss_score_chunk(ss_handle *h, const ss_csr *queries, const float *inv_q,
+                         const ss_index *idx, const float *inv_i, float *out, int64_t ld_out,
+                         void *stream) {
+  if (!h) return SS_ERR_INVALID_ARG;
+  ss_status st = check_csr_args(h, queries, "ss_score_chunk");
+  if (st != SS_OK) return st;
+  if (!idx || idx != &h->index)
+    return fail(h, SS_ERR_INVALID_ARG, "ss_score_chunk: index does not belong to this handle");
+  if (queries->n_rows > 0 && (!inv_q || !inv_i || !out))
+    return fail(h, SS_ERR_INVALID_ARG, "ss_score_chunk: null norms or output");
+  if (ld_out < idx->n_items)
+    return fail(h, SS_ERR_INVALID_ARG, "ss_score_chunk: ld_out %lld < chunk width %d",
+                (long long)ld_out, idx->n_items);
+  if ((st = set_device(h)) != SS_OK) return st;
+  SS_CUDA(h, launch_score_chunk(h, *queries, inv_q, *idx, inv_i, out, ld_out, as_stream(stream)));
+  return SS_OK;
+}
+
+ss_status ss_score_all(ss_handle *h, const ss_csr *queries, const float *inv_q,
+                       const ss_csr *items, const float *inv_i, float *out, int64_t ld_out,
+                       void *stream) {
+  if (!h) return SS_ERR_INVALID_ARG;
+  ss_status st = check_csr_args(h, queries, "ss_score_all");
+  if (st == SS_OK) st = check_csr_args(h, items, "ss_score_all");
+  if (st != SS_OK) return st;
+  if (ld_out < items->n_rows)
+    return fail(h, SS_ERR_INVALID_ARG, "ss_score_all: ld_out < number of items");
+  if (queries->n_rows == 0 || items->n_rows == 0) return SS_OK;
+  if (!inv_q || !inv_i || !out) return fail(h, SS_ERR_INVALID_ARG, "ss_score_all: null pointer");
+  if ((st = set_device(h)) != SS_OK) return st;
+  cudaStream_t s = as_stream(stream);
+  for (int64_t rb = 0; rb < items->n_rows; rb += h->chunk_rows) {
+    const int64_t re = std::min<int64_t>(rb + h->chunk_rows, items->n_rows);
+    if ((st = build_chunk(h, *items, rb, re, s)) != SS_OK) return st;
+    SS_CUDA(h, launch_score_chunk(h, *queries, inv_q, h->index, inv_i + rb, out + rb, ld_out, s));
+  }
+  return SS_OK;
+}
+
+}  // extern "C"

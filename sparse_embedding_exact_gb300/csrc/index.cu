@@ -1,0 +1,188 @@
+// Per-chunk inverted index: the chunk's CSR rows turned into one posting list
+// per dimension (CSR -> CSC by dimension).
+//
+// The blog post ("Engineering practice for bulk similarity calculation over
+// sparse embeddings", section 3.1) computes u.v over supp(u) and supp(v);
+// the posting list of dimension k names every item of the chunk whose support
+// holds k, so a query nonzero at k meets exactly the items it multiplies.
+//
+// Steps (all on the device, queued on one stream):
+//   1. histogram: count[k] = number of chunk rows holding dimension k;
+//   2. exclusive scan of count[0..dim] -> col_ptr (tile sums, a scan of the
+//      tile sums, then the tiles again with warp-shuffle scans);
+//   3. scatter: every nonzero (row r, dim k, value v) takes the next slot of
+//      list k and stores (r - row_begin, v).
+#include <cuda_runtime.h>
+
+#include "internal.cuh"
+
+namespace {
+
+constexpr int kScanThreads = 256;
+constexpr int kScanItems = 16;  // per thread
+constexpr int kScanTile = kScanThreads * kScanItems;
+constexpr int kHistThreads = 256;
+
+__device__ __forceinline__ void flag(int32_t *status, int32_t code) {
+  atomicCAS(status, DEV_OK, code);
+}
+
+__global__ void __launch_bounds__(kHistThreads)
+    k_histogram(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
+                int64_t row_begin, int64_t row_end, int64_t dim, int32_t *__restrict__ count,
+                int32_t *status) {
+  const int64_t p0 = indptr[row_begin], p1 = indptr[row_end];
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t p = p0 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < p1; p += stride) {
+    const int32_t k = __ldg(indices + p);
+    if (k >= 0 && (int64_t)k < dim) {
+      atomicAdd(count + k, 1);
+    } else {
+      flag(status, DEV_OUT_OF_RANGE);
+    }
+  }
+}
+
+// Inclusive warp scan with shuffles.
+__device__ __forceinline__ int32_t warp_inclusive_scan(int32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// Exclusive block scan of one value per thread (warp-shuffle scans inside
+// each warp, then one warp scans the warp totals).  *total gets the sum.
+__device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t *total) {
+  constexpr int kWarps = kScanThreads / 32;
+  __shared__ int32_t warp_off[kWarps];
+  __shared__ int32_t block_total;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int32_t inc = warp_inclusive_scan(v);
+  if (lane == 31) warp_off[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int32_t w = (lane < kWarps) ? warp_off[lane] : 0;
+    const int32_t winc = warp_inclusive_scan(w);
+    if (lane < kWarps) warp_off[lane] = winc - w;
+    if (lane == kWarps - 1) block_total = winc;
+  }
+  __syncthreads();
+  const int32_t r = warp_off[warp] + inc - v;
+  *total = block_total;
+  __syncthreads();  // warp_off and block_total are reused by the next call
+  return r;
+}
+
+// Phase 1: sum of each tile of kScanTile counters.
+__global__ void __launch_bounds__(kScanThreads)
+    k_scan_tile_sums(const int32_t *__restrict__ count, int64_t n, int32_t *__restrict__ part) {
+  const int64_t base = (int64_t)blockIdx.x * kScanTile + (int64_t)threadIdx.x * kScanItems;
+  int32_t s = 0;
+#pragma unroll
+  for (int t = 0; t < kScanItems; ++t) s += (base + t < n) ? count[base + t] : 0;
+  int32_t total;
+  block_exclusive_scan(s, &total);
+  if (threadIdx.x == 0) part[blockIdx.x] = total;
+}
+
+// Phase 2: one block scans the tile sums (exclusive), carrying across passes.
+__global__ void __launch_bounds__(kScanThreads)
+    k_scan_partials(int32_t *__restrict__ part, int64_t n_tiles) {
+  int32_t carry = 0;
+  for (int64_t b = 0; b < n_tiles; b += kScanThreads) {
+    const int64_t i = b + threadIdx.x;
+    const int32_t v = (i < n_tiles) ? part[i] : 0;
+    int32_t total;
+    const int32_t ex = block_exclusive_scan(v, &total);
+    if (i < n_tiles) part[i] = carry + ex;
+    carry += total;
+  }
+  if (threadIdx.x == 0) part[n_tiles] = carry;
+}
+
+// Phase 3: exclusive scan inside each tile plus the tile offset; writes
+// col_ptr and resets the counters to the same values (scatter cursors).
+__global__ void __launch_bounds__(kScanThreads)
+    k_scan_apply(int32_t *__restrict__ count, int64_t n, const int32_t *__restrict__ part,
+                 int32_t *__restrict__ col_ptr) {
+  const int64_t base = (int64_t)blockIdx.x * kScanTile + (int64_t)threadIdx.x * kScanItems;
+  int32_t v[kScanItems];
+  int32_t s = 0;
+#pragma unroll
+  for (int t = 0; t < kScanItems; ++t) {
+    v[t] = (base + t < n) ? count[base + t] : 0;
+    s += v[t];
+  }
+  int32_t total;
+  int32_t run = block_exclusive_scan(s, &total) + part[blockIdx.x];
+#pragma unroll
+  for (int t = 0; t < kScanItems; ++t) {
+    if (base + t < n) {
+      col_ptr[base + t] = run;
+      count[base + t] = run;
+    }
+    run += v[t];
+  }
+}
+
+// One warp per chunk row: each nonzero claims the next slot of its list.
+__global__ void __launch_bounds__(kHistThreads)
+    k_scatter(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
+              const float *__restrict__ values, int64_t row_begin, int64_t row_end, int64_t dim,
+              int32_t *__restrict__ cursor, uint16_t *__restrict__ post_item,
+              float *__restrict__ post_val, int64_t capacity, int32_t *status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (kHistThreads / 32);
+  for (int64_t r = row_begin + (int64_t)blockIdx.x * (kHistThreads / 32) + (threadIdx.x >> 5);
+       r < row_end; r += warps) {
+    const int64_t b = indptr[r], e = indptr[r + 1];
+    for (int64_t j = b + lane; j < e; j += 32) {
+      const int32_t k = __ldg(indices + j);
+      if (k < 0 || (int64_t)k >= dim) continue;  // flagged by the histogram
+      const int32_t pos = atomicAdd(cursor + k, 1);
+      if (pos >= 0 && (int64_t)pos < capacity) {
+        post_item[pos] = (uint16_t)(r - row_begin);
+        post_val[pos] = __ldg(values + j);
+      } else {
+        flag(status, DEV_CAPACITY);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+int64_t scan_tile_count(int64_t n) { return (n + kScanTile - 1) / kScanTile; }
+
+cudaError_t launch_build_index(ss_handle *h, const ss_csr &items, int64_t row_begin,
+                               int64_t row_end, cudaStream_t s) {
+  const int64_t n = h->dim + 1;
+  cudaError_t e = cudaMemsetAsync(h->col_cnt, 0, sizeof(int32_t) * (size_t)n, s);
+  if (e != cudaSuccess) return e;
+  const int grid = h->sm_count * 8;
+  k_histogram<<<grid, kHistThreads, 0, s>>>(items.indptr, items.indices, row_begin, row_end,
+                                            h->dim, h->col_cnt, h->d_status);
+  const int64_t tiles = scan_tile_count(n);
+  k_scan_tile_sums<<<(unsigned)tiles, kScanThreads, 0, s>>>(h->col_cnt, n, h->scan_part);
+  k_scan_partials<<<1, kScanThreads, 0, s>>>(h->scan_part, tiles);
+  k_scan_apply<<<(unsigned)tiles, kScanThreads, 0, s>>>(h->col_cnt, n, h->scan_part, h->col_ptr);
+  k_scatter<<<grid, kHistThreads, 0, s>>>(items.indptr, items.indices, items.values, row_begin,
+                                          row_end, h->dim, h->col_cnt, h->post_item, h->post_val,
+                                          h->post_cap, h->d_status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ss_index &ix = h->index;
+  ix.row_begin = row_begin;
+  ix.row_end = row_end;
+  ix.n_items = (int32_t)(row_end - row_begin);
+  ix.dim = h->dim;
+  ix.col_ptr = h->col_ptr;
+  ix.post_item = h->post_item;
+  ix.post_val = h->post_val;
+  ix.capacity = h->post_cap;
+  return cudaSuccess;
+}
