@@ -176,6 +176,10 @@ ss_status ss_validate_csr(ss_handle *h, const ss_csr *m, void *stream);
  */
 ss_status ss_check_device(ss_handle *h, void *stream);
 
+/* Number of kernels this handle has launched so far (every call that
+ * queues kernels adds the number it queued).  Host-side count; no sync. */
+uint64_t ss_kernel_launches(const ss_handle *h);
+
 /* Frees the handle and its device workspace (synchronises the device). */
 ss_status ss_destroy(ss_handle *h);
 

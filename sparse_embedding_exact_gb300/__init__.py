@@ -189,6 +189,10 @@ class SparseCosine:
         self._check(self._lib.ss_validate_csr(self._h, ctypes.byref(c), _stream_ptr(stream)),
                     "ss_validate_csr")
 
+    def kernel_launches(self) -> int:
+        """Kernels this handle has queued so far (counted by the library)."""
+        return int(self._lib.ss_kernel_launches(self._h))
+
     def check_device(self, stream=None):
         self._check(self._lib.ss_check_device(self._h, _stream_ptr(stream)), "ss_check_device")
 

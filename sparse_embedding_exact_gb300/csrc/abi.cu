@@ -85,6 +85,7 @@ ss_status status_from_device(ss_handle *h, int32_t code, const char *what) {
 
 ss_status validate(ss_handle *h, const ss_csr &m, cudaStream_t s, const char *what) {
   SS_CUDA(h, launch_validate_csr(m, h->d_status, h->sm_count, s));
+  h->launches += 1;
   int32_t code = 0;
   ss_status st = read_status(h, s, &code);
   if (st != SS_OK) return st;
@@ -127,6 +128,7 @@ ss_status build_chunk(ss_handle *h, const ss_csr &items, int64_t rb, int64_t re,
   ss_status st = ensure_post_capacity(h, std::max<int64_t>(items.nnz, 1));
   if (st != SS_OK) return st;
   SS_CUDA(h, launch_build_index(h, items, rb, re, s));
+  h->launches += kIndexKernels;
   return SS_OK;
 }
 
@@ -150,6 +152,8 @@ const char *ss_status_string(ss_status s) {
 }
 
 const char *ss_last_error(const ss_handle *h) { return h ? h->last_error.c_str() : ""; }
+
+uint64_t ss_kernel_launches(const ss_handle *h) { return h ? h->launches : 0; }
 
 ss_status ss_create(ss_handle **out, int device, int64_t dim, int32_t chunk_rows, int32_t flags) {
   if (!out) return SS_ERR_INVALID_ARG;
@@ -217,6 +221,7 @@ ss_status ss_row_norms(ss_handle *h, const ss_csr *m, float *inv_norms, void *st
     if ((st = validate(h, *m, s, "ss_row_norms")) != SS_OK) return st;
   }
   SS_CUDA(h, launch_row_norms(*m, inv_norms, h->sm_count, s));
+  if (m->n_rows > 0) h->launches += 1;
   return SS_OK;
 }
 
@@ -254,6 +259,7 @@ ss_status ss_score_chunk(ss_handle *h, const ss_csr *queries, const float *inv_q
                 (long long)ld_out, idx->n_items);
   if ((st = set_device(h)) != SS_OK) return st;
   SS_CUDA(h, launch_score_chunk(h, *queries, inv_q, *idx, inv_i, out, ld_out, as_stream(stream)));
+  if (queries->n_rows > 0 && idx->n_items > 0) h->launches += 1;
   return SS_OK;
 }
 
@@ -274,6 +280,7 @@ ss_status ss_score_all(ss_handle *h, const ss_csr *queries, const float *inv_q,
     const int64_t re = std::min<int64_t>(rb + h->chunk_rows, items->n_rows);
     if ((st = build_chunk(h, *items, rb, re, s)) != SS_OK) return st;
     SS_CUDA(h, launch_score_chunk(h, *queries, inv_q, h->index, inv_i + rb, out + rb, ld_out, s));
+    h->launches += 1;
   }
   return SS_OK;
 }

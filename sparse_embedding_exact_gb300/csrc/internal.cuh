@@ -37,6 +37,7 @@ struct ss_handle {
   int32_t flags = 0;
   int sm_count = 0;
   std::string last_error;
+  uint64_t launches = 0;  // kernels queued by this handle
 
   // Device workspace, owned by the handle.
   int32_t *d_status = nullptr;   // one status word
@@ -59,6 +60,9 @@ cudaError_t launch_build_index(ss_handle *h, const ss_csr &items, int64_t row_be
 cudaError_t launch_score_chunk(const ss_handle *h, const ss_csr &queries, const float *inv_q,
                                const ss_index &idx, const float *inv_i, float *out,
                                int64_t ld_out, cudaStream_t s);
+
+// Kernels queued by one launch_build_index call.
+constexpr int kIndexKernels = 5;
 
 // Number of scan tiles needed for n counters.
 int64_t scan_tile_count(int64_t n);
