@@ -52,6 +52,10 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target seconds of oracle work for the CPU baseline sample")
+    p.add_argument("--n-queries", type=int, default=0,
+                   help="use only the first N query rows (small profiling captures)")
+    p.add_argument("--n-items", type=int, default=0,
+                   help="use only the first N item rows (small profiling captures)")
     return p.parse_args()
 
 
@@ -162,6 +166,13 @@ def cpu_baseline(cfg, Q, I, seconds: float):
                       f"{dt:.1f} s, {cores} threads)"}
 
 
+def item_shard(cfg, rank: int, world: int):
+    """Weak scaling: rank r scores item rows [r*n_i, (r+1)*n_i) of one seeded
+    item set of world*n_i rows against the same queries (no data exchange)."""
+    big = cfg.scaled(cfg.n_q, cfg.n_i * world, name=cfg.name)
+    return big, rank * cfg.n_i, (rank + 1) * cfg.n_i
+
+
 def dist_setup(n_gpus):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -228,11 +239,12 @@ def run_ours(args):
 
     build.build()
     cfg = CONFIGS[args.workload]
+    if args.n_queries or args.n_items:
+        cfg = cfg.scaled(args.n_queries or cfg.n_q, args.n_items or cfg.n_i)
     Q = generate_side(cfg, 0)
     if world > 1:
-        big = cfg.scaled(cfg.n_q, cfg.n_i * world, name=cfg.name)
-        I = generate_rows(big, 1, rank * cfg.n_i, (rank + 1) * cfg.n_i,
-                          workers=max(1, host_cores() // world))
+        big, b, e = item_shard(cfg, rank, world)
+        I = generate_rows(big, 1, b, e, workers=max(1, host_cores() // world))
     else:
         I = generate_side(cfg, 1)
 

@@ -54,6 +54,12 @@ typedef int32_t ss_status;
 
 /* ss_create flags */
 #define SS_VALIDATE 0x1 /* check CSR inputs on the device (synchronises) */
+/* Scoring algorithm.  The default splits dimensions into a few dense "hot"
+ * ones (multiplied as a small dense product) and the rest (hashed lists in
+ * shared memory).  SS_ALGO_POSTING_LISTS instead walks, for each query
+ * nonzero, the chunk's posting list of that dimension (one warp per query
+ * row).  Both give the same cosines up to float32 summation order. */
+#define SS_ALGO_POSTING_LISTS 0x2
 
 /* Largest chunk the index builder accepts (item numbers in a chunk are
  * stored in 16 bits). */

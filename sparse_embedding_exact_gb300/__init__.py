@@ -77,15 +77,24 @@ def _host_csr(batch):
 class SparseCosine:
     """One library handle: a device, a dimension and a chunk size."""
 
+    ALGORITHMS = ("hybrid", "posting")
+
     def __init__(self, dim: int, chunk_rows: int = DEFAULT_CHUNK_ROWS, device: int = 0,
-                 validate: bool = False):
+                 validate: bool = False, algorithm: str = "hybrid"):
+        """algorithm: "hybrid" (dense hot dimensions + hashed cold lists, the
+        default) or "posting" (one warp per query row walking posting lists)."""
         self._lib = _abi.load()
         self.dim = int(dim)
         self.chunk_rows = int(chunk_rows)
         self.device = int(device)
+        if algorithm not in self.ALGORITHMS:
+            raise ValueError(f"algorithm must be one of {self.ALGORITHMS}")
+        self.algorithm = algorithm
+        flags = (SS_VALIDATE if validate else 0)
+        if algorithm == "posting":
+            flags |= _abi.SS_ALGO_POSTING_LISTS
         h = ctypes.c_void_p()
-        st = self._lib.ss_create(ctypes.byref(h), self.device, self.dim, self.chunk_rows,
-                                 SS_VALIDATE if validate else 0)
+        st = self._lib.ss_create(ctypes.byref(h), self.device, self.dim, self.chunk_rows, flags)
         if st != _abi.SS_OK:
             raise SparseCosError(st, f"ss_create: {self._lib.ss_status_string(st).decode()}")
         self._h = h

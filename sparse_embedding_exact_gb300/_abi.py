@@ -20,6 +20,7 @@ SS_ERR_DEVICE_CHECK = 6
 SS_ERR_TIMEOUT = 7
 SS_ERR_LIMIT = 8
 SS_VALIDATE = 0x1
+SS_ALGO_POSTING_LISTS = 0x2
 SS_MAX_CHUNK_ROWS = 65536
 
 

@@ -92,44 +92,78 @@ ss_status validate(ss_handle *h, const ss_csr &m, cudaStream_t s, const char *wh
   return status_from_device(h, code, what);
 }
 
-// Grows the posting-list capacity to hold `need` entries (synchronises the
-// device when it has to reallocate).
-ss_status ensure_post_capacity(ss_handle *h, int64_t need) {
-  if (need <= h->post_cap) return SS_OK;
-  int64_t cap = std::max<int64_t>(need, h->post_cap + h->post_cap / 2);
+// Grows the per-chunk entry capacity (posting lists, or the hybrid path's
+// heavy-item list) to hold `need` entries; synchronises the device when it
+// has to reallocate.
+ss_status ensure_capacity(ss_handle *h, int64_t need) {
+  if (h->algo == ALGO_POSTING) {
+    if (need <= h->post_cap) return SS_OK;
+    const int64_t cap = std::max<int64_t>(need, h->post_cap + h->post_cap / 2);
+    SS_CUDA(h, cudaDeviceSynchronize());
+    cudaFree(h->post_item);
+    cudaFree(h->post_val);
+    h->post_item = nullptr;
+    h->post_val = nullptr;
+    h->post_cap = 0;
+    SS_CUDA(h, cudaMalloc(&h->post_item, sizeof(uint16_t) * (size_t)cap));
+    SS_CUDA(h, cudaMalloc(&h->post_val, sizeof(float) * (size_t)cap));
+    h->post_cap = cap;
+    return SS_OK;
+  }
+  if (need <= h->heavy_cap) return SS_OK;
+  const int64_t cap = std::max<int64_t>(need, h->heavy_cap + h->heavy_cap / 2);
   SS_CUDA(h, cudaDeviceSynchronize());
-  cudaFree(h->post_item);
-  cudaFree(h->post_val);
-  h->post_item = nullptr;
-  h->post_val = nullptr;
-  h->post_cap = 0;
-  SS_CUDA(h, cudaMalloc(&h->post_item, sizeof(uint16_t) * (size_t)cap));
-  SS_CUDA(h, cudaMalloc(&h->post_val, sizeof(float) * (size_t)cap));
-  h->post_cap = cap;
+  cudaFree(h->heavy_k);
+  cudaFree(h->heavy_v);
+  cudaFree(h->heavy_item);
+  h->heavy_k = nullptr;
+  h->heavy_v = nullptr;
+  h->heavy_item = nullptr;
+  h->heavy_cap = 0;
+  SS_CUDA(h, cudaMalloc(&h->heavy_k, sizeof(int32_t) * (size_t)cap));
+  SS_CUDA(h, cudaMalloc(&h->heavy_v, sizeof(float) * (size_t)cap));
+  SS_CUDA(h, cudaMalloc(&h->heavy_item, (size_t)cap));
+  h->heavy_cap = cap;
   return SS_OK;
 }
 
 void free_workspace(ss_handle *h) {
-  cudaFree(h->d_status);
-  cudaFree(h->col_cnt);
-  cudaFree(h->col_ptr);
-  cudaFree(h->scan_part);
-  cudaFree(h->post_item);
-  cudaFree(h->post_val);
+  void *ptrs[] = {h->d_status, h->col_cnt, h->col_ptr, h->scan_part, h->post_item, h->post_val,
+                  h->hot, h->slab, h->ell, h->meta, h->heavy_k, h->heavy_v, h->heavy_item,
+                  h->heavy_cursor};
+  for (void *p : ptrs) cudaFree(p);
   h->d_status = nullptr;
   h->col_cnt = h->col_ptr = h->scan_part = nullptr;
   h->post_item = nullptr;
   h->post_val = nullptr;
   h->post_cap = 0;
+  h->hot = h->meta = h->heavy_k = h->heavy_cursor = nullptr;
+  h->slab = h->heavy_v = nullptr;
+  h->ell = nullptr;
+  h->heavy_item = nullptr;
+  h->heavy_cap = 0;
 }
 
 ss_status build_chunk(ss_handle *h, const ss_csr &items, int64_t rb, int64_t re, cudaStream_t s) {
   // The chunk holds at most items.nnz entries: size the lists for that.
-  ss_status st = ensure_post_capacity(h, std::max<int64_t>(items.nnz, 1));
+  ss_status st = ensure_capacity(h, std::max<int64_t>(items.nnz, 1));
   if (st != SS_OK) return st;
-  SS_CUDA(h, launch_build_index(h, items, rb, re, s));
-  h->launches += kIndexKernels;
+  if (h->algo == ALGO_POSTING) {
+    SS_CUDA(h, launch_build_index(h, items, rb, re, s));
+    h->launches += kIndexKernels;
+    return SS_OK;
+  }
+  int queued = 0;
+  SS_CUDA(h, launch_hot_select(h, items, s, &queued));
+  SS_CUDA(h, launch_build_hybrid(h, items, rb, re, s));
+  h->launches += queued + 1;
   return SS_OK;
+}
+
+cudaError_t score(const ss_handle *h, const ss_csr &q, const float *inv_q, const ss_index &idx,
+                  const float *inv_i, float *out, int64_t ld_out, cudaStream_t s) {
+  if (idx.algo == ALGO_POSTING) return launch_score_chunk(h, q, inv_q, idx, inv_i, out, ld_out, s);
+  return launch_score_hybrid(h, q, inv_q, idx, inv_i, out, ld_out, s);
 }
 
 }  // namespace
@@ -166,14 +200,27 @@ ss_status ss_create(ss_handle **out, int device, int64_t dim, int32_t chunk_rows
   h->dim = dim;
   h->chunk_rows = chunk_rows;
   h->flags = flags;
+  h->algo = (flags & SS_ALGO_POSTING_LISTS) ? ALGO_POSTING : ALGO_HYBRID;
   cudaError_t e = cudaSetDevice(device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, device);
-  h->scan_tiles = scan_tile_count(dim + 1);
   if (e == cudaSuccess) e = cudaMalloc(&h->d_status, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int32_t));
-  if (e == cudaSuccess) e = cudaMalloc(&h->col_cnt, sizeof(int32_t) * (size_t)(dim + 1));
-  if (e == cudaSuccess) e = cudaMalloc(&h->col_ptr, sizeof(int32_t) * (size_t)(dim + 1));
-  if (e == cudaSuccess) e = cudaMalloc(&h->scan_part, sizeof(int32_t) * (size_t)(h->scan_tiles + 1));
+  if (h->algo == ALGO_POSTING) {
+    h->scan_tiles = scan_tile_count(dim + 1);
+    if (e == cudaSuccess) e = cudaMalloc(&h->col_cnt, sizeof(int32_t) * (size_t)(dim + 1));
+    if (e == cudaSuccess) e = cudaMalloc(&h->col_ptr, sizeof(int32_t) * (size_t)(dim + 1));
+    if (e == cudaSuccess) e = cudaMalloc(&h->scan_part, sizeof(int32_t) * (size_t)(h->scan_tiles + 1));
+  } else {
+    using namespace hyb;
+    h->max_tiles = (chunk_rows + kTI - 1) / kTI;
+    const size_t tiles = (size_t)h->max_tiles;
+    if (e == cudaSuccess) e = cudaMalloc(&h->hot, sizeof(int32_t) * (1 + kHotMax));
+    if (e == cudaSuccess) e = cudaMemset(h->hot, 0, sizeof(int32_t) * (1 + kHotMax));
+    if (e == cudaSuccess) e = cudaMalloc(&h->slab, sizeof(float) * tiles * kHotMax * kTI);
+    if (e == cudaSuccess) e = cudaMalloc(&h->ell, sizeof(int2) * tiles * kEllMaxW * kTI);
+    if (e == cudaSuccess) e = cudaMalloc(&h->meta, sizeof(int32_t) * tiles * kMetaInts);
+    if (e == cudaSuccess) e = cudaMalloc(&h->heavy_cursor, sizeof(int32_t));
+  }
   if (e != cudaSuccess) {
     const ss_status st = (e == cudaErrorMemoryAllocation) ? SS_ERR_OOM : SS_ERR_CUDA;
     free_workspace(h);
@@ -258,7 +305,7 @@ ss_status ss_score_chunk(ss_handle *h, const ss_csr *queries, const float *inv_q
     return fail(h, SS_ERR_INVALID_ARG, "ss_score_chunk: ld_out %lld < chunk width %d",
                 (long long)ld_out, idx->n_items);
   if ((st = set_device(h)) != SS_OK) return st;
-  SS_CUDA(h, launch_score_chunk(h, *queries, inv_q, *idx, inv_i, out, ld_out, as_stream(stream)));
+  SS_CUDA(h, score(h, *queries, inv_q, *idx, inv_i, out, ld_out, as_stream(stream)));
   if (queries->n_rows > 0 && idx->n_items > 0) h->launches += 1;
   return SS_OK;
 }
@@ -279,7 +326,7 @@ ss_status ss_score_all(ss_handle *h, const ss_csr *queries, const float *inv_q,
   for (int64_t rb = 0; rb < items->n_rows; rb += h->chunk_rows) {
     const int64_t re = std::min<int64_t>(rb + h->chunk_rows, items->n_rows);
     if ((st = build_chunk(h, *items, rb, re, s)) != SS_OK) return st;
-    SS_CUDA(h, launch_score_chunk(h, *queries, inv_q, h->index, inv_i + rb, out + rb, ld_out, s));
+    SS_CUDA(h, score(h, *queries, inv_q, h->index, inv_i + rb, out + rb, ld_out, s));
     h->launches += 1;
   }
   return SS_OK;

@@ -176,6 +176,7 @@ cudaError_t launch_build_index(ss_handle *h, const ss_csr &items, int64_t row_be
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ss_index &ix = h->index;
+  ix.algo = ALGO_POSTING;
   ix.row_begin = row_begin;
   ix.row_end = row_end;
   ix.n_items = (int32_t)(row_end - row_begin);

@@ -16,18 +16,53 @@ enum : int32_t {
   DEV_CAPACITY = 3,
 };
 
-// The per-chunk inverted index: for each dimension k of the chunk, the
-// posting list of (item number within the chunk, value), laid out CSC-style
-// by dimension.
+// Scoring algorithms.
+enum : int32_t {
+  ALGO_HYBRID = 0,   // dense hot dimensions in registers + sparse cold lists in shared memory
+  ALGO_POSTING = 1,  // one warp per query row walking the chunk's posting lists
+};
+
+// Geometry of the hybrid scorer (see hybrid.cu).
+namespace hyb {
+constexpr int kTQ = 64;                    // query rows per tile
+constexpr int kTI = 256;                   // items per tile (one thread per item)
+constexpr int kThreads = 256;              // threads per block (8 warps)
+constexpr int kHotMax = 48;                // dense ("hot") dimensions per item matrix
+constexpr int kEllMaxW = 1024;             // cold entries per item kept in the ELL block
+constexpr int kMetaInts = 16;              // per item tile: 8 warp lengths, heavy begin, count
+constexpr int kBatchEntries = 4096;        // cold query entries per hashed batch
+constexpr int kHashBits = 13;
+constexpr int kHashSlots = 1 << kHashBits; // load factor <= 1/2
+constexpr int kBitmapBits = 15;
+constexpr int kBitmapWords = (1 << kBitmapBits) / 32;
+constexpr int kHotSampleEntries = 8192;    // nonzeros sampled to choose the hot set
+constexpr int kHotMinPercent = 20;         // a dimension is hot if >= 20% of sampled rows hold it
+}  // namespace hyb
+
+// The per-chunk index.  ALGO_POSTING: one posting list of (item, value) per
+// dimension, CSC-style.  ALGO_HYBRID: per tile of kTI items, the hot
+// dimensions' posting lists stored dense (slab), every other nonzero in an
+// item-major ELL block (items with many of them in a separate list).
 struct ss_index {
+  int32_t algo = ALGO_HYBRID;
   int64_t row_begin = 0;
   int64_t row_end = 0;
   int32_t n_items = 0;
   int64_t dim = 0;
+  // ALGO_POSTING
   const int32_t *col_ptr = nullptr;    // [dim + 1], posting list k = [col_ptr[k], col_ptr[k+1])
   const uint16_t *post_item = nullptr; // [capacity]
   const float *post_val = nullptr;     // [capacity]
   int64_t capacity = 0;
+  // ALGO_HYBRID
+  int32_t n_tiles = 0;
+  const int32_t *hot = nullptr;        // [1 + kHotMax]: H, then the H hot dims ascending
+  const float *slab = nullptr;         // [tile][kHotMax][kTI]: value of hot dim h for item i (0 if absent)
+  const int2 *ell = nullptr;           // [tile][kEllMaxW][kTI]: (dim, value bits), dims ascending, -1 pads
+  const int32_t *meta = nullptr;       // [tile][kMetaInts]
+  const int32_t *heavy_k = nullptr;    // heavy items' cold entries: dim
+  const float *heavy_v = nullptr;      //   value
+  const uint8_t *heavy_item = nullptr; //   item within its tile
 };
 
 struct ss_handle {
@@ -35,12 +70,14 @@ struct ss_handle {
   int64_t dim = 0;
   int32_t chunk_rows = 0;
   int32_t flags = 0;
+  int32_t algo = ALGO_HYBRID;
   int sm_count = 0;
   std::string last_error;
   uint64_t launches = 0;  // kernels queued by this handle
 
   // Device workspace, owned by the handle.
-  int32_t *d_status = nullptr;   // one status word
+  int32_t *d_status = nullptr;  // one status word
+  // ALGO_POSTING
   int32_t *col_cnt = nullptr;    // [dim + 1]: histogram, then scatter cursors
   int32_t *col_ptr = nullptr;    // [dim + 1]
   int32_t *scan_part = nullptr;  // [scan tiles + 1]
@@ -48,6 +85,20 @@ struct ss_handle {
   uint16_t *post_item = nullptr; // [post_cap]
   float *post_val = nullptr;     // [post_cap]
   int64_t post_cap = 0;
+  // ALGO_HYBRID
+  int32_t *hot = nullptr;        // [1 + kHotMax]
+  float *slab = nullptr;         // [max tiles][kHotMax][kTI]
+  int2 *ell = nullptr;           // [max tiles][kEllMaxW][kTI]
+  int32_t *meta = nullptr;       // [max tiles][kMetaInts]
+  int32_t *heavy_k = nullptr;    // [heavy_cap]
+  float *heavy_v = nullptr;
+  uint8_t *heavy_item = nullptr;
+  int32_t *heavy_cursor = nullptr;
+  int64_t heavy_cap = 0;
+  int32_t max_tiles = 0;
+  // The hot set is chosen once per item matrix: the matrix it was chosen for.
+  const void *hot_src[3] = {nullptr, nullptr, nullptr};
+  int64_t hot_src_rows = -1, hot_src_nnz = -1;
 
   ss_index index;
 };
@@ -60,6 +111,13 @@ cudaError_t launch_build_index(ss_handle *h, const ss_csr &items, int64_t row_be
 cudaError_t launch_score_chunk(const ss_handle *h, const ss_csr &queries, const float *inv_q,
                                const ss_index &idx, const float *inv_i, float *out,
                                int64_t ld_out, cudaStream_t s);
+// Hybrid path.  launch_hot_select returns the number of kernels it queued.
+cudaError_t launch_hot_select(ss_handle *h, const ss_csr &items, cudaStream_t s, int *queued);
+cudaError_t launch_build_hybrid(ss_handle *h, const ss_csr &items, int64_t row_begin,
+                                int64_t row_end, cudaStream_t s);
+cudaError_t launch_score_hybrid(const ss_handle *h, const ss_csr &queries, const float *inv_q,
+                                const ss_index &idx, const float *inv_i, float *out,
+                                int64_t ld_out, cudaStream_t s);
 
 // Kernels queued by one launch_build_index call.
 constexpr int kIndexKernels = 5;

@@ -35,8 +35,11 @@ def _dev(sec, batch):
     return sec.DeviceCsr.from_host(batch, "cuda")
 
 
-def _gpu_cosine(sec, Q, I, chunk_rows=8192):
-    with sec.SparseCosine(Q.dim, chunk_rows=chunk_rows) as h:
+ALGOS = ["hybrid", "posting"]
+
+
+def _gpu_cosine(sec, Q, I, chunk_rows=8192, algorithm="hybrid"):
+    with sec.SparseCosine(Q.dim, chunk_rows=chunk_rows, algorithm=algorithm) as h:
         q, i = _dev(sec, Q), _dev(sec, I)
         inv_q, inv_i = h.row_norms(q), h.row_norms(i)
         S = h.score_all(q, inv_q, i, inv_i)
@@ -85,11 +88,12 @@ def test_row_norms_heavy_rows(sec):
 
 
 # ------------------------------------------------------------------ cosine
-def test_small_workload_full_matrix(sec):
+@pytest.mark.parametrize("algo", ALGOS)
+def test_small_workload_full_matrix(sec, algo):
     """1,000 x 10,000 at d = 65,536: two chunks (8,192 + 1,808), all entries."""
     cfg = CONFIGS["d65k_q1k_i10k"]
     Q, I = generate_side(cfg, 0), generate_side(cfg, 1)
-    got = _gpu_cosine(sec, Q, I)
+    got = _gpu_cosine(sec, Q, I, algorithm=algo)
     ref = oracle.cosine(Q, I)
     assert got.shape == (1000, 10000)
     assert np.isfinite(got).all()
@@ -108,12 +112,13 @@ EDGE = [
 ]
 
 
+@pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("case", EDGE, ids=lambda c: "x".join(map(str, c[:3])) + f"-{c[4]}-c{c[5]}")
-def test_edge_shapes(sec, case):
+def test_edge_shapes(sec, case, algo):
     nq, ni, d, dens, law, chunk = case
     Q, _ = random_csr(11 + nq, nq, d, dens, law, zero_rows=1 if nq > 3 else 0, explicit_zeros=3)
     I, _ = random_csr(23 + ni, ni, d, dens, law, zero_rows=2 if ni > 3 else 0, explicit_zeros=3)
-    got = _gpu_cosine(sec, Q, I, chunk_rows=chunk)
+    got = _gpu_cosine(sec, Q, I, chunk_rows=chunk, algorithm=algo)
     ref = oracle.cosine(Q, I)
     assert got.shape == ref.shape
     assert np.isfinite(got).all()
@@ -148,12 +153,15 @@ def test_closed_forms_on_gpu(sec):
     assert np.abs(got - exp).max() <= TOL
 
 
-def test_chunk_size_invariance_is_bitwise(sec):
+@pytest.mark.parametrize("algo", ALGOS)
+def test_chunk_size_invariance_is_bitwise(sec, algo):
+    """Each entry's sum runs in an order fixed by its own two rows, so the
+    chunk size cannot change a single bit."""
     cfg = CONFIGS["d65k_q1k_i10k"]
     Q, I = generate_rows(cfg, 0, 0, 300), generate_rows(cfg, 1, 0, 5000)
-    a = _gpu_cosine(sec, Q, I, chunk_rows=8192)
+    a = _gpu_cosine(sec, Q, I, chunk_rows=8192, algorithm=algo)
     for c in (1000, 333, 4096):
-        b = _gpu_cosine(sec, Q, I, chunk_rows=c)
+        b = _gpu_cosine(sec, Q, I, chunk_rows=c, algorithm=algo)
         assert np.array_equal(a.view(np.int32), b.view(np.int32)), c
 
 
@@ -224,6 +232,54 @@ def test_argument_errors(sec):
         with pytest.raises(SparseCosError) as e:
             h.row_norms(other)
         assert e.value.status == _abi.SS_ERR_INVALID_ARG
+
+
+def _rows_csr(rows, dim):
+    return csr_from_rows([(np.asarray(i), np.asarray(v, np.float32)) for i, v in rows], dim)
+
+
+def test_heavy_items_and_multibatch_queries(sec):
+    """A few rows far longer than the rest: long item rows take the heavy-item
+    path, long query rows force several hashed batches per query tile."""
+    rng = np.random.default_rng(3)
+    d = 50_000
+
+    def row(n):
+        idx = np.sort(rng.choice(d, size=n, replace=False))
+        return idx, rng.standard_normal(n).astype(np.float32)
+
+    q_rows = [row(int(rng.integers(5, 60))) for _ in range(150)]
+    q_rows[7] = row(6000)      # one tile holds > 4,096 cold query nonzeros
+    q_rows[100] = row(2500)
+    i_rows = [row(int(rng.integers(5, 60))) for _ in range(900)]
+    for j in (3, 300, 301, 899):
+        i_rows[j] = row(4000)  # items far above their tile's mean
+    Q, I = _rows_csr(q_rows, d), _rows_csr(i_rows, d)
+    ref = oracle.cosine(Q, I)
+    for algo in ALGOS:
+        got = _gpu_cosine(sec, Q, I, chunk_rows=512, algorithm=algo)
+        assert _max_err(got, ref) <= TOL, algo
+
+
+def test_hot_set_saturated_and_empty(sec):
+    # every one of 100 dims in half the rows: 48 of them hot, the rest cold
+    Q, _ = random_csr(5, 70, 100, 0.5, "normal")
+    I, _ = random_csr(6, 700, 100, 0.5, "normal")
+    assert _max_err(_gpu_cosine(sec, Q, I, chunk_rows=300), oracle.cosine(Q, I)) <= TOL
+    # uniform sparse dims: no dimension qualifies as hot
+    Q, _ = random_csr(7, 90, 20_000, 0.002, "lognormal")
+    I, _ = random_csr(8, 900, 20_000, 0.002, "lognormal")
+    assert _max_err(_gpu_cosine(sec, Q, I), oracle.cosine(Q, I)) <= TOL
+
+
+@pytest.mark.parametrize("name", ["d1.2m_q5k_i200k", "d1.2m_q20k_i1m_heavy"])
+def test_two_gpu_algorithms_agree(sec, name):
+    cfg = CONFIGS[name]
+    Q, I = generate_rows(cfg, 0, 0, 700), generate_rows(cfg, 1, 0, 9000)
+    a = _gpu_cosine(sec, Q, I, algorithm="hybrid")
+    b = _gpu_cosine(sec, Q, I, algorithm="posting")
+    assert _max_err(a, b) <= TOL
+    assert _max_err(a, oracle.cosine(Q, I)) <= TOL
 
 
 # ------------------------------------------------------------- host streaming
