@@ -182,6 +182,41 @@ ss_status ss_validate_csr(ss_handle *h, const ss_csr *m, void *stream);
  */
 ss_status ss_check_device(ss_handle *h, void *stream);
 
+/* Size of the fixed scratch array behind ss_cosine_chunk_noalloc. */
+#define SS_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * For callers that cannot allocate device memory (a host whose memory pool
+ * owns the whole GPU, a CUDA graph capture in progress, a plug-in with a
+ * fixed memory budget).  The paper has no counterpart: it is a packaging of
+ * the same computation.
+ *
+ *   out[q * ld_out + c] = cos(Q_q, I_{row_begin + c}),  c < row_end - row_begin
+ *
+ * for every query row, computed with the posting-list kernels.  Needs no
+ * handle and calls no cudaMalloc, cudaFree or allocating library routine:
+ * all scratch (both norm vectors, the chunk's per-dimension counters and
+ * list offsets, the posting lists) comes from one static device array of
+ * SS_NOALLOC_SCRATCH_BYTES that every GPU loading this library holds until
+ * the process exits.  The caller passes the inputs and the output, all in
+ * device memory of the current device; `stream` as in the other calls.
+ *   chunk_nnz: the number of nonzeros in item rows [row_begin, row_end)
+ *   (indptr[row_end] - indptr[row_begin]), known to the caller; the lists
+ *   are sized by it (a smaller value truncates them on the device).
+ * Returns SS_ERR_LIMIT, without queueing work, when the scratch needed
+ * (about 8 * (dim + 1) + 6 * chunk_nnz + 4 * (n_q + chunk rows) bytes)
+ * exceeds SS_NOALLOC_SCRATCH_BYTES or the chunk exceeds SS_MAX_CHUNK_ROWS.
+ * The first call on a device looks up the array's device address (no
+ * allocation); make that first call before any stream capture.  Every call
+ * shares the one array and it keeps the last call's contents (each call
+ * clears what must start at zero): calls that overlap on the GPU, on
+ * different streams or host threads, race and corrupt each other's results;
+ * order them on one stream.
+ */
+ss_status ss_cosine_chunk_noalloc(const ss_csr *queries, const ss_csr *items, int64_t row_begin,
+                                  int64_t row_end, int64_t chunk_nnz, float *out, int64_t ld_out,
+                                  void *stream);
+
 /* Number of kernels this handle has launched so far (every call that
  * queues kernels adds the number it queued).  Host-side count; no sync. */
 uint64_t ss_kernel_launches(const ss_handle *h);
