@@ -267,6 +267,9 @@ def run_ours(args):
           for _ in chunks]
 
     def step(record):
+        # Every step redoes the whole path: the hot set and the prepared
+        # queries are derived again, not reused from the previous step.
+        h.invalidate()
         h.row_norms(q, out=inv_q)
         h.row_norms(it, out=inv_i)
         for c, (b, e) in enumerate(chunks):
@@ -281,6 +284,7 @@ def run_ours(args):
         step(False)
     torch.cuda.synchronize()
     h.check_device()
+    index_stats = h.index_stats(h.build_item_index(it, *chunks[0]))
 
     def barrier():
         if world > 1:
@@ -386,6 +390,7 @@ def run_ours(args):
             "e2e": e2e,
             "gpu_launches": int(launches),
             "clocks": clocks,
+            "first_chunk_index": index_stats,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -182,6 +182,26 @@ ss_status ss_validate_csr(ss_handle *h, const ss_csr *m, void *stream);
  */
 ss_status ss_check_device(ss_handle *h, void *stream);
 
+/*
+ * Forgets what the handle derived from earlier inputs: the hot dimensions
+ * chosen for an item matrix and the prepared query matrix.  The handle keys
+ * both on the arrays' addresses and sizes, so call this after changing the
+ * contents of a matrix in place; the next calls recompute them.  No GPU work.
+ */
+ss_status ss_invalidate(ss_handle *h);
+
+/*
+ * Diagnostics for an index built by ss_build_item_index.  Synchronises
+ * `stream` and writes stats[0..7]:
+ *   [0] algorithm (0 = hybrid, 1 = posting lists)  [1] items in the chunk
+ *   [2] item tiles (hybrid)                         [3] hot dimensions H
+ *   [4] entries in the heavy-item list              [5] widest ELL column
+ *   [6] ELL entries stored, padding included        [7] item tiles without an
+ *                                                       inverted-index image
+ * Fields that do not apply to the algorithm are 0.
+ */
+ss_status ss_index_stats(ss_handle *h, const ss_index *idx, int64_t *stats, void *stream);
+
 /* Size of the fixed scratch array behind ss_cosine_chunk_noalloc. */
 #define SS_NOALLOC_SCRATCH_BYTES (32u << 20)
 

@@ -198,6 +198,19 @@ class SparseCosine:
         self._check(self._lib.ss_validate_csr(self._h, ctypes.byref(c), _stream_ptr(stream)),
                     "ss_validate_csr")
 
+    def index_stats(self, index, stream=None) -> dict:
+        """Diagnostics of the last built index (synchronises the stream)."""
+        out = (ctypes.c_int64 * 8)()
+        self._check(self._lib.ss_index_stats(self._h, index, out, _stream_ptr(stream)),
+                    "ss_index_stats")
+        keys = ("algorithm", "items", "tiles", "hot_dims", "heavy_entries", "ell_width_max",
+                "ell_entries", "tiles_without_image")
+        return {k: int(out[j]) for j, k in enumerate(keys)}
+
+    def invalidate(self):
+        """Forget the hot set and the prepared queries (after in-place edits)."""
+        self._check(self._lib.ss_invalidate(self._h), "ss_invalidate")
+
     def kernel_launches(self) -> int:
         """Kernels this handle has queued so far (counted by the library)."""
         return int(self._lib.ss_kernel_launches(self._h))

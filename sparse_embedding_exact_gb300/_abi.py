@@ -54,6 +54,8 @@ SIGNATURES = {
     "ss_bulk_cosine_host": (_I32, [_P, _CSR, _CSR, _P, _I64, ss_chunk_consumer, _P, _I32, _I32]),
     "ss_validate_csr": (_I32, [_P, _CSR, _P]),
     "ss_check_device": (_I32, [_P, _P]),
+    "ss_invalidate": (_I32, [_P]),
+    "ss_index_stats": (_I32, [_P, _P, ctypes.POINTER(ctypes.c_int64), _P]),
     "ss_cosine_chunk_noalloc": (_I32, [_CSR, _CSR, _I64, _I64, _I64, _P, _I64, _P]),
     "ss_kernel_launches": (ctypes.c_uint64, [_P]),
     "ss_destroy": (_I32, [_P]),

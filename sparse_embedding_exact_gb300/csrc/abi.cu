@@ -78,6 +78,8 @@ ss_status status_from_device(ss_handle *h, int32_t code, const char *what) {
       return fail(h, SS_ERR_OUT_OF_RANGE, "%s: index outside [0, dim) or bad indptr", what);
     case DEV_CAPACITY:
       return fail(h, SS_ERR_DEVICE_CHECK, "%s: chunk nnz exceeds the index capacity", what);
+    case DEV_STALL:
+      return fail(h, SS_ERR_DEVICE_CHECK, "%s: a kernel loop ran out of its iteration bound", what);
     default:
       return fail(h, SS_ERR_DEVICE_CHECK, "%s: device check code %d", what, code);
   }
@@ -130,14 +132,19 @@ ss_status ensure_capacity(ss_handle *h, int64_t need) {
 void free_workspace(ss_handle *h) {
   void *ptrs[] = {h->d_status, h->col_cnt, h->col_ptr, h->scan_part, h->post_item, h->post_val,
                   h->hot, h->slab, h->ell, h->meta, h->heavy_k, h->heavy_v, h->heavy_item,
-                  h->heavy_cursor};
+                  h->counters, h->image, h->qhot, h->qcold};
   for (void *p : ptrs) cudaFree(p);
+  h->counters = nullptr;
+  h->image = nullptr;
+  h->qhot = nullptr;
+  h->qcold = nullptr;
+  h->qhot_cap = h->qcold_cap = 0;
   h->d_status = nullptr;
   h->col_cnt = h->col_ptr = h->scan_part = nullptr;
   h->post_item = nullptr;
   h->post_val = nullptr;
   h->post_cap = 0;
-  h->hot = h->meta = h->heavy_k = h->heavy_cursor = nullptr;
+  h->hot = h->meta = h->heavy_k = nullptr;
   h->slab = h->heavy_v = nullptr;
   h->ell = nullptr;
   h->heavy_item = nullptr;
@@ -160,10 +167,17 @@ ss_status build_chunk(ss_handle *h, const ss_csr &items, int64_t rb, int64_t re,
   return SS_OK;
 }
 
-cudaError_t score(const ss_handle *h, const ss_csr &q, const float *inv_q, const ss_index &idx,
+cudaError_t score(ss_handle *h, const ss_csr &q, const float *inv_q, const ss_index &idx,
                   const float *inv_i, float *out, int64_t ld_out, cudaStream_t s) {
-  if (idx.algo == ALGO_POSTING) return launch_score_chunk(h, q, inv_q, idx, inv_i, out, ld_out, s);
-  return launch_score_hybrid(h, q, inv_q, idx, inv_i, out, ld_out, s);
+  if (idx.algo == ALGO_POSTING) {
+    const cudaError_t e = launch_score_chunk(h, q, inv_q, idx, inv_i, out, ld_out, s);
+    if (e == cudaSuccess && q.n_rows > 0 && idx.n_items > 0) h->launches += 1;
+    return e;
+  }
+  int queued = 0;
+  const cudaError_t e = launch_score_hybrid(h, q, inv_q, idx, inv_i, out, ld_out, s, &queued);
+  h->launches += queued;
+  return e;
 }
 
 }  // namespace
@@ -219,7 +233,8 @@ ss_status ss_create(ss_handle **out, int device, int64_t dim, int32_t chunk_rows
     if (e == cudaSuccess) e = cudaMalloc(&h->slab, sizeof(float) * tiles * kHotMax * kTI);
     if (e == cudaSuccess) e = cudaMalloc(&h->ell, sizeof(int2) * tiles * kEllMaxW * kTI);
     if (e == cudaSuccess) e = cudaMalloc(&h->meta, sizeof(int32_t) * tiles * kMetaInts);
-    if (e == cudaSuccess) e = cudaMalloc(&h->heavy_cursor, sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMalloc(&h->counters, sizeof(int32_t) * (2 + tiles));
+    if (e == cudaSuccess) e = cudaMalloc(&h->image, (size_t)kImgBytes * tiles);
   }
   if (e != cudaSuccess) {
     const ss_status st = (e == cudaErrorMemoryAllocation) ? SS_ERR_OOM : SS_ERR_CUDA;
@@ -246,6 +261,45 @@ ss_status ss_validate_csr(ss_handle *h, const ss_csr *m, void *stream) {
   if (st != SS_OK) return st;
   if ((st = set_device(h)) != SS_OK) return st;
   return validate(h, *m, as_stream(stream), "ss_validate_csr");
+}
+
+ss_status ss_invalidate(ss_handle *h) {
+  if (!h) return SS_ERR_INVALID_ARG;
+  for (int j = 0; j < 3; ++j) h->hot_src[j] = h->prep_src[j] = nullptr;
+  h->hot_src_rows = h->hot_src_nnz = h->prep_rows = h->prep_nnz = -1;
+  h->prep_generation = ~0ull;
+  return SS_OK;
+}
+
+ss_status ss_index_stats(ss_handle *h, const ss_index *idx, int64_t *stats, void *stream) {
+  if (!h) return SS_ERR_INVALID_ARG;
+  if (!idx || idx != &h->index || !stats)
+    return fail(h, SS_ERR_INVALID_ARG, "ss_index_stats: bad index or output");
+  ss_status st = set_device(h);
+  if (st != SS_OK) return st;
+  for (int j = 0; j < 8; ++j) stats[j] = 0;
+  stats[0] = idx->algo;
+  stats[1] = idx->n_items;
+  SS_CUDA(h, cudaStreamSynchronize(as_stream(stream)));
+  if (idx->algo != ALGO_HYBRID || idx->n_tiles == 0) return SS_OK;
+  stats[2] = idx->n_tiles;
+  int32_t hcount = 0;
+  SS_CUDA(h, cudaMemcpy(&hcount, idx->hot, sizeof(int32_t), cudaMemcpyDeviceToHost));
+  stats[3] = hcount;
+  int32_t n_ovf = 0;
+  SS_CUDA(h, cudaMemcpy(&n_ovf, idx->counters + 1, sizeof(int32_t), cudaMemcpyDeviceToHost));
+  stats[7] = n_ovf;
+  std::vector<int32_t> meta((size_t)idx->n_tiles * hyb::kMetaInts);
+  SS_CUDA(h, cudaMemcpy(meta.data(), idx->meta, sizeof(int32_t) * meta.size(), cudaMemcpyDeviceToHost));
+  for (int32_t t = 0; t < idx->n_tiles; ++t) {
+    const int32_t *m = meta.data() + (size_t)t * hyb::kMetaInts;
+    stats[4] += m[9];
+    for (int w = 0; w < 8; ++w) {
+      stats[5] = std::max<int64_t>(stats[5], m[w]);
+      stats[6] += (int64_t)m[w] * 32;
+    }
+  }
+  return SS_OK;
 }
 
 ss_status ss_check_device(ss_handle *h, void *stream) {
@@ -306,7 +360,6 @@ ss_status ss_score_chunk(ss_handle *h, const ss_csr *queries, const float *inv_q
                 (long long)ld_out, idx->n_items);
   if ((st = set_device(h)) != SS_OK) return st;
   SS_CUDA(h, score(h, *queries, inv_q, *idx, inv_i, out, ld_out, as_stream(stream)));
-  if (queries->n_rows > 0 && idx->n_items > 0) h->launches += 1;
   return SS_OK;
 }
 
@@ -327,7 +380,6 @@ ss_status ss_score_all(ss_handle *h, const ss_csr *queries, const float *inv_q,
     const int64_t re = std::min<int64_t>(rb + h->chunk_rows, items->n_rows);
     if ((st = build_chunk(h, *items, rb, re, s)) != SS_OK) return st;
     SS_CUDA(h, score(h, *queries, inv_q, h->index, inv_i + rb, out + rb, ld_out, s));
-    h->launches += 1;
   }
   return SS_OK;
 }

@@ -185,26 +185,60 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *red, int *total)
   return off + inc - v;
 }
 
-// One block per tile of kTI items, one thread per item.
+// Open-addressing insert / find in the image-building hash (kImgSlots).
+__device__ __forceinline__ int img_insert(int *keys, int32_t k) {
+  uint32_t s = hash_a(k, kImgSlotsBits);
+  for (int n = 0; n < kImgSlots; ++n) {
+    const int prev = atomicCAS(&keys[s], -1, k);
+    if (prev == -1 || prev == k) return (int)s;
+    s = (s + 1) & (kImgSlots - 1);
+  }
+  return -1;
+}
+__device__ __forceinline__ int img_find(const int *keys, int32_t k) {
+  uint32_t s = hash_a(k, kImgSlotsBits);
+  for (int n = 0; n < kImgSlots; ++n) {
+    const int key = keys[s];
+    if (key == k) return (int)s;
+    if (key == -1) return -1;
+    s = (s + 1) & (kImgSlots - 1);
+  }
+  return -1;
+}
+
+// Shared memory of the builder block (bytes).
+constexpr int kBldOffSlab = 0;
+constexpr int kBldOffKeys = kBldOffSlab + kHotMax * kTI * 4;
+constexpr int kBldOffCnt = kBldOffKeys + kImgSlots * 4;
+constexpr int kBuildSmem = kBldOffCnt + kImgSlots * 4;
+
+// One block per tile of kTI items, one thread per item.  Hot values go to
+// the tile's slab.  The cold nonzeros become the tile's image (dimension ->
+// segment of (item, value)) when they fit; otherwise they go to the ELL
+// block and the heavy list, and the tile joins the overflow list.
 __global__ void __launch_bounds__(kThreads)
     k_build_tiles(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
                   const float *__restrict__ values, int64_t row_begin, int64_t row_end,
                   const int32_t *__restrict__ hot, float *__restrict__ slab,
                   int2 *__restrict__ ell, int32_t *__restrict__ meta,
                   int32_t *__restrict__ heavy_k, float *__restrict__ heavy_v,
-                  uint8_t *__restrict__ heavy_item, int32_t *__restrict__ heavy_cursor,
-                  int64_t heavy_cap, int32_t *status) {
-  extern __shared__ float slab_s[];  // [kHotMax][kTI]
+                  uint8_t *__restrict__ heavy_item, int32_t *__restrict__ counters,
+                  int64_t heavy_cap, unsigned char *__restrict__ image, int32_t *status) {
+  extern __shared__ __align__(16) unsigned char bsm[];
+  float *slab_s = reinterpret_cast<float *>(bsm + kBldOffSlab);  // [kHotMax][kTI]
+  int *ikeys = reinterpret_cast<int *>(bsm + kBldOffKeys);
+  int *icnt = reinterpret_cast<int *>(bsm + kBldOffCnt);
   __shared__ int hkeys[kHotSlots];
   __shared__ int8_t hvals[kHotSlots];
   __shared__ int red[kThreads / 32];
-  __shared__ int heavy_base;
+  __shared__ int heavy_base, img_fail;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t = blockIdx.x;
   const int64_t item = row_begin + (int64_t)t * kTI + tid;
   const bool valid = item < row_end;
   const int H = hot[0];
   for (int s = tid; s < kHotSlots; s += kThreads) hkeys[s] = -1;
+  if (tid == 0) img_fail = 0;
   __syncthreads();
   if (tid < H) hot_insert(hkeys, hvals, hot[1 + tid], tid);
   for (int h = 0; h < H; ++h) slab_s[h * kTI + tid] = 0.0f;
@@ -223,38 +257,112 @@ __global__ void __launch_bounds__(kThreads)
   }
   const int n_valid = block_sum(valid ? 1 : 0, red);
   const int sum_cold = block_sum(cold, red);
-  const int mean = n_valid > 0 ? sum_cold / n_valid : 0;
-  const int thr = min(kEllMaxW, 2 * mean + 32);
-  const bool heavy = cold > thr;
-  const int reg_len = heavy ? 0 : cold;
-  int len_w = reg_len;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) len_w = max(len_w, __shfl_xor_sync(0xffffffffu, len_w, o));
-  int heavy_total = 0;
-  const int my_off = block_exclusive_scan(heavy ? cold : 0, red, &heavy_total);
-  if (tid == 0) heavy_base = heavy_total > 0 ? atomicAdd(heavy_cursor, heavy_total) : 0;
-  __syncthreads();
-  const int64_t hbase = heavy_base;
-  const bool heavy_ok = hbase + heavy_total <= heavy_cap;
-  if (tid == 0 && !heavy_ok) flag(status, DEV_CAPACITY);
+  unsigned char *img = image + (size_t)t * kImgBytes;
+  int32_t *hdr = reinterpret_cast<int32_t *>(img);
 
-  int2 *col = ell + (size_t)t * kEllMaxW * kTI + tid;
-  int s = 0;
-  for (int64_t p = pb; p < pe; ++p) {
-    const int32_t k = indices[p];
-    if (hot_find(hkeys, hvals, k) >= 0) continue;
-    const float v = values[p];
-    if (!heavy) {
-      col[(size_t)s * kTI] = make_int2(k, __float_as_int(v));
-    } else if (heavy_ok) {
-      const int64_t e = hbase + my_off + s;
-      heavy_k[e] = k;
-      heavy_v[e] = v;
-      heavy_item[e] = (uint8_t)tid;
+  // ---- image path
+  bool fits = sum_cold <= kImgECap;
+  if (fits) {
+    for (int s = tid; s < kImgSlots; s += kThreads) {
+      ikeys[s] = -1;
+      icnt[s] = 0;
     }
-    ++s;
+    __syncthreads();
+    for (int64_t p = pb; p < pe; ++p) {
+      const int32_t k = indices[p];
+      if (hot_find(hkeys, hvals, k) >= 0) continue;
+      const int slot = img_insert(ikeys, k);
+      if (slot < 0) img_fail = 1;
+      else atomicAdd(&icnt[slot], 1);
+    }
+    __syncthreads();
+    constexpr int kPer = kImgSlots / kThreads;
+    int occ = 0, ent = 0;
+    for (int j = 0; j < kPer; ++j) {
+      const int s = tid * kPer + j;
+      occ += ikeys[s] >= 0;
+      ent += icnt[s];
+    }
+    int D = 0, E = 0;
+    int d_run = block_exclusive_scan(occ, red, &D);
+    int e_run = block_exclusive_scan(ent, red, &E);
+    fits = !img_fail && D <= kImgDCap && E <= kImgECap;
+    if (fits) {
+      uint2 *gslot = reinterpret_cast<uint2 *>(img + kImgOffSlots);
+      for (int j = 0; j < kPer; ++j) {
+        const int s = tid * kPer + j;
+        if (ikeys[s] >= 0) {
+          const int c = icnt[s];
+          gslot[s] = make_uint2((uint32_t)ikeys[s], (uint32_t)e_run | ((uint32_t)(e_run + c) << 16));
+          icnt[s] = e_run;  // now the fill cursor of this segment
+          e_run += c;
+        } else {
+          gslot[s] = make_uint2(0xffffffffu, 0u);
+        }
+      }
+      (void)d_run;
+      if (tid == 0) {
+        hdr[0] = D;
+        hdr[1] = E;
+        hdr[2] = 1;
+        hdr[3] = 0;
+      }
+      __syncthreads();
+      uint8_t *gitem = img + kImgOffItem;
+      float *gval = reinterpret_cast<float *>(img + kImgOffVal);
+      for (int64_t p = pb; p < pe; ++p) {
+        const int32_t k = indices[p];
+        if (hot_find(hkeys, hvals, k) >= 0) continue;
+        const int slot = img_find(ikeys, k);
+        const int pos = atomicAdd(&icnt[slot], 1);
+        gitem[pos] = (uint8_t)tid;
+        gval[pos] = values[p];
+      }
+    }
   }
-  for (int j = reg_len; j < len_w; ++j) col[(size_t)j * kTI] = make_int2(-1, 0);
+
+  // ---- ELL path for tiles whose cold part does not fit an image
+  int len_w = 0;
+  int64_t hbase = 0;
+  int heavy_total = 0;
+  bool heavy_ok = true;
+  if (!fits) {
+    const int mean = n_valid > 0 ? sum_cold / n_valid : 0;
+    const int thr = min(kEllMaxW, 2 * mean + 32);
+    const bool heavy = cold > thr;
+    const int reg_len = heavy ? 0 : cold;
+    len_w = reg_len;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) len_w = max(len_w, __shfl_xor_sync(0xffffffffu, len_w, o));
+    const int my_off = block_exclusive_scan(heavy ? cold : 0, red, &heavy_total);
+    if (tid == 0) {
+      heavy_base = heavy_total > 0 ? atomicAdd(&counters[0], heavy_total) : 0;
+      hdr[2] = 0;
+      const int c = atomicAdd(&counters[1], 1);
+      counters[2 + c] = t;
+    }
+    __syncthreads();
+    hbase = heavy_base;
+    heavy_ok = hbase + heavy_total <= heavy_cap;
+    if (tid == 0 && !heavy_ok) flag(status, DEV_CAPACITY);
+    int2 *col = ell + (size_t)t * kEllMaxW * kTI + tid;
+    int s = 0;
+    for (int64_t p = pb; p < pe; ++p) {
+      const int32_t k = indices[p];
+      if (hot_find(hkeys, hvals, k) >= 0) continue;
+      const float v = values[p];
+      if (!heavy) {
+        col[(size_t)s * kTI] = make_int2(k, __float_as_int(v));
+      } else if (heavy_ok) {
+        const int64_t e = hbase + my_off + s;
+        heavy_k[e] = k;
+        heavy_v[e] = v;
+        heavy_item[e] = (uint8_t)tid;
+      }
+      ++s;
+    }
+    for (int j = reg_len; j < len_w; ++j) col[(size_t)j * kTI] = make_int2(-1, 0);
+  }
   float *dst = slab + (size_t)t * kHotMax * kTI + tid;
   for (int h = 0; h < H; ++h) dst[(size_t)h * kTI] = slab_s[h * kTI + tid];
   int32_t *m = meta + (size_t)t * kMetaInts;
@@ -262,6 +370,7 @@ __global__ void __launch_bounds__(kThreads)
   if (tid == 0) {
     m[8] = (int32_t)hbase;
     m[9] = heavy_ok ? heavy_total : 0;
+    m[kMetaFits] = fits ? 1 : 0;
   }
 }
 
@@ -282,12 +391,15 @@ struct HybridArgs {
   const float *inv_i;
   int32_t n_items;
   int32_t n_tiles;
-  int64_t n_units;
+  int64_t n_qtiles;
+  const int32_t *counters;  // [1] tiles without an image, [2..] their ids
   float *out;
   int64_t ld_out;
   int32_t vec_ok;
   int32_t dim;
 };
+
+constexpr int kQueue = 8;  // cold entries probed per step; their hits queue per thread
 
 // Shared-memory layout of the scoring block (bytes).
 constexpr int kOffAcc = 0;
@@ -295,20 +407,22 @@ constexpr int kOffSlab = kOffAcc + kTQ * kTI * 4;
 constexpr int kOffQhot = kOffSlab + kHotMax * kTI * 4;
 constexpr int kOffKeys = kOffQhot + kHotMax * kTQ * 4;
 constexpr int kOffMeta = kOffKeys + kHashSlots * 4;
-constexpr int kOffLv = kOffMeta + kHashSlots * 4;
-constexpr int kOffBits = kOffLv + kBatchEntries * 4;
+constexpr int kOffLists = kOffMeta + kHashSlots * 4;
+constexpr int kOffQueue = kOffLists + kBatchEntries * 8;
+constexpr int kOffBits = kOffQueue + kQueue * kThreads * 8;
 constexpr int kOffHist = kOffBits + kBitmapWords * 4;
 constexpr int kOffHotK = kOffHist + 256 * 4;
 constexpr int kOffMisc = kOffHotK + kHotSlots * 4;
-constexpr int kOffLq = kOffMisc + 64 * 4;
-constexpr int kOffHotV = kOffLq + kBatchEntries;
+constexpr int kOffHotV = kOffMisc + 64 * 4;
 constexpr int kScoreSmem = kOffHotV + kHotSlots;
+static_assert(kScoreSmem <= 232448, "scoring block exceeds 227 KB of shared memory");
 
 struct Smem {
-  float *acc, *slab, *qhot, *lv;
+  float *acc, *slab, *qhot;
   int *keys, *hist, *hotk, *misc;
   uint32_t *hmeta, *bits;
-  uint8_t *lq;
+  uint2 *lists;  // query lists: {row * kTI, value bits}
+  uint2 *queue;  // per-thread hit queue: entry j of thread t at [j * kThreads + t]
   int8_t *hotv;
 };
 
@@ -410,10 +524,7 @@ __device__ void build_batch(const Smem &sm, const HybridArgs &a, int64_t q0, int
     }
     if (!found) return;
     const uint32_t pos = atomicAdd(&sm.hmeta[s], 1u << 16) >> 16;
-    if (pos < (uint32_t)kBatchEntries) {
-      sm.lq[pos] = (uint8_t)r;
-      sm.lv[pos] = v;
-    }
+    if (pos < (uint32_t)kBatchEntries) sm.lists[pos] = make_uint2((uint32_t)(r * kTI), __float_as_uint(v));
   });
   __syncthreads();
   // The fill advanced each start by its count: move it back.
@@ -495,8 +606,27 @@ __device__ __forceinline__ void hot_product(const Smem &sm, int H) {
   }
 }
 
+// Slot of dimension k in the batch hash, resolved past the first probe.
+__device__ __noinline__ uint32_t batch_find_slow(const Smem &sm, int32_t k, uint32_t s) {
+  for (int n = 1; n < kHashSlots; ++n) {
+    s = (s + 1) & (kHashSlots - 1);
+    const int key = sm.keys[s];
+    if (key == k) return sm.hmeta[s];
+    if (key == -1) return 0;
+  }
+  return 0;
+}
+
 // Cold nonzeros of item tile t with dims in [lo, hi).  `cursor` is this
 // thread's position in its item's ELL column (kept across batches).
+//
+// Thread i owns item i (column i of the accumulator tile).  It takes its
+// ELL entries kQueue at a time: the loads of the next group are in flight
+// while the current one is probed, the kQueue probes are independent, and
+// the hits go into the thread's queue.  The thread then walks all queued
+// query lists in one loop, so a warp waits for its busiest lane's total,
+// not for the longest list at every step.  Hits are queued and walked in
+// ascending dimension order, which fixes the order of each entry's sum.
 __device__ __forceinline__ void cold_pass(const Smem &sm, const HybridArgs &a, int t, int32_t lo,
                                           int32_t hi, int &cursor) {
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -504,19 +634,73 @@ __device__ __forceinline__ void cold_pass(const Smem &sm, const HybridArgs &a, i
   const int len = m[warp];
   const int2 *col = a.ell + (size_t)t * kEllMaxW * kTI + tid;
   float *accc = sm.acc + tid;
+  uint2 *queue = sm.queue + tid;
   int s = cursor;
-  while (s < len) {
-    const int2 x = __ldg(col + (size_t)s * kTI);
-    if (x.x < 0 || x.x >= hi) break;
-    ++s;
-    const uint32_t hm = batch_find(sm, x.x);
-    const uint32_t cnt = hm & 0xffffu;
-    if (!cnt) continue;
-    const float v = __int_as_float(x.y);
-    const uint32_t st = hm >> 16;
-    for (uint32_t e = st; e < st + cnt; ++e) {
-      float *dst = accc + sm.lq[e] * kTI;
-      *dst = fmaf(sm.lv[e], v, *dst);
+  bool active = s < len;
+  int2 x[kQueue];
+#pragma unroll
+  for (int j = 0; j < kQueue; ++j)
+    x[j] = (active && s + j < len) ? __ldg(col + (size_t)(s + j) * kTI) : make_int2(-1, 0);
+  while (__any_sync(0xffffffffu, active)) {
+    // Probe: entries are a prefix of valid dims (< hi), then pads / later dims.
+    bool in[kQueue];
+    uint32_t bit[kQueue], slot[kQueue];
+    int consumed = 0;
+#pragma unroll
+    for (int j = 0; j < kQueue; ++j) {
+      in[j] = active && x[j].x >= 0 && x[j].x < hi;
+      if (in[j]) consumed = j + 1;
+      const uint32_t b = hash_b(x[j].x, kBitmapBits);
+      bit[j] = in[j] ? ((sm.bits[b >> 5] >> (b & 31)) & 1u) : 0u;
+      slot[j] = hash_a(x[j].x, kHashBits);
+    }
+    uint32_t hm[kQueue];
+#pragma unroll
+    for (int j = 0; j < kQueue; ++j) {
+      hm[j] = 0;
+      if (bit[j]) {
+        const int key = sm.keys[slot[j]];
+        if (key == x[j].x) hm[j] = sm.hmeta[slot[j]];
+        else if (key != -1) hm[j] = batch_find_slow(sm, x[j].x, slot[j]);
+      }
+    }
+    int nh = 0;
+#pragma unroll
+    for (int j = 0; j < kQueue; ++j) {
+      if (hm[j] & 0xffffu) {
+        queue[nh * kThreads] = make_uint2(hm[j], (uint32_t)x[j].y);
+        ++nh;
+      }
+    }
+    s += consumed;
+    if (consumed < kQueue || s >= len) active = false;
+#pragma unroll
+    for (int j = 0; j < kQueue; ++j)
+      x[j] = (active && s + j < len) ? __ldg(col + (size_t)(s + j) * kTI) : make_int2(-1, 0);
+    // Walk the queued lists: acc[q][i] += q_k * v_ik.
+    int h = 0;
+    uint32_t st = 0, end = 0;
+    float v = 0.f;
+    if (nh > 0) {
+      const uint2 e0 = queue[0];
+      st = e0.x >> 16;
+      end = st + (e0.x & 0xffffu);
+      v = __uint_as_float(e0.y);
+    }
+    while (__any_sync(0xffffffffu, h < nh)) {
+      if (h < nh) {
+        const uint2 e = sm.lists[st];
+        float *d = accc + e.x;
+        *d = fmaf(__uint_as_float(e.y), v, *d);
+        if (++st == end) {
+          if (++h < nh) {
+            const uint2 en = queue[h * kThreads];
+            st = en.x >> 16;
+            end = st + (en.x & 0xffffu);
+            v = __uint_as_float(en.y);
+          }
+        }
+      }
     }
   }
   cursor = s;
@@ -532,7 +716,10 @@ __device__ __forceinline__ void cold_pass(const Smem &sm, const HybridArgs &a, i
     const float v = __ldg(a.heavy_v + e);
     const int it = __ldg(a.heavy_item + e);
     const uint32_t st = hm >> 16;
-    for (uint32_t j = st; j < st + cnt; ++j) atomicAdd(sm.acc + sm.lq[j] * kTI + it, sm.lv[j] * v);
+    for (uint32_t j = st; j < st + cnt; ++j) {
+      const uint2 l = sm.lists[j];
+      atomicAdd(sm.acc + l.x + it, __uint_as_float(l.y) * v);
+    }
   }
 }
 
@@ -569,12 +756,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_hybrid(const HybridArgs a
   sm.qhot = reinterpret_cast<float *>(smem_raw + kOffQhot);
   sm.keys = reinterpret_cast<int *>(smem_raw + kOffKeys);
   sm.hmeta = reinterpret_cast<uint32_t *>(smem_raw + kOffMeta);
-  sm.lv = reinterpret_cast<float *>(smem_raw + kOffLv);
+  sm.lists = reinterpret_cast<uint2 *>(smem_raw + kOffLists);
+  sm.queue = reinterpret_cast<uint2 *>(smem_raw + kOffQueue);
   sm.bits = reinterpret_cast<uint32_t *>(smem_raw + kOffBits);
   sm.hist = reinterpret_cast<int *>(smem_raw + kOffHist);
   sm.hotk = reinterpret_cast<int *>(smem_raw + kOffHotK);
   sm.misc = reinterpret_cast<int *>(smem_raw + kOffMisc);
-  sm.lq = smem_raw + kOffLq;
   sm.hotv = reinterpret_cast<int8_t *>(smem_raw + kOffHotV);
   const int tid = threadIdx.x;
 
@@ -584,14 +771,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_hybrid(const HybridArgs a
   if (tid < H) hot_insert(sm.hotk, sm.hotv, a.hot[1 + tid], tid);
   __syncthreads();
 
-  const int64_t u0 = (int64_t)blockIdx.x * a.n_units / gridDim.x;
-  const int64_t u1 = (int64_t)(blockIdx.x + 1) * a.n_units / gridDim.x;
+  // Only the item tiles that have no image (the builder's overflow list).
+  const int n_ovf = a.counters[1];
+  const int32_t *ovf = a.counters + 2;
+  const int64_t n_units = a.n_qtiles * n_ovf;
+  const int64_t u0 = (int64_t)blockIdx.x * n_units / gridDim.x;
+  const int64_t u1 = (int64_t)(blockIdx.x + 1) * n_units / gridDim.x;
   int64_t cur_g = -1;
   bool single = false;
-  if (H > 0 && u0 < u1) slab_prefetch(sm, a, (int)(u0 % a.n_tiles), H);
+  if (H > 0 && u0 < u1) slab_prefetch(sm, a, ovf[u0 % n_ovf], H);
   for (int64_t u = u0; u < u1; ++u) {
-    const int64_t g = u / a.n_tiles;
-    const int t = (int)(u % a.n_tiles);
+    const int64_t g = u / n_ovf;
+    const int t = ovf[u % n_ovf];
     const int64_t q0 = g * kTQ;
     const int nq = (int)(a.n_q - q0 < kTQ ? a.n_q - q0 : kTQ);
     if (g != cur_g) {
@@ -621,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_hybrid(const HybridArgs a
       for (int j = tid; j < kTQ * kTI / 4; j += kThreads) acc4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     __syncthreads();
-    if (H > 0 && u + 1 < u1) slab_prefetch(sm, a, (int)((u + 1) % a.n_tiles), H);
+    if (H > 0 && u + 1 < u1) slab_prefetch(sm, a, ovf[(u + 1) % n_ovf], H);
     // 2. cold dims through the hashed query lists
     int cursor = 0;
     if (single) {
@@ -638,6 +829,338 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_hybrid(const HybridArgs a
     __syncthreads();
     // 3. normalise and store
     store_tile(sm, a, q0, nq, t);
+    __syncthreads();
+  }
+  cp_async_wait_all();
+}
+
+// ---------------------------------------------------------------- fast path
+// One warp per query row: the row's hot values into its column of the query
+// tile's hot block ([tile][kHotMax][kTQ], zero where absent), and the row's
+// indices with the hot dimensions replaced by -1.  Rows past n_q in the last
+// tile get a zero column.
+__global__ void __launch_bounds__(kThreads)
+    k_prep_queries(const int64_t *__restrict__ indptr, const int32_t *__restrict__ idx,
+                   const float *__restrict__ val, int64_t n_q, int64_t n_rows_padded,
+                   const int32_t *__restrict__ hot, float *__restrict__ qhot,
+                   int32_t *__restrict__ qcold) {
+  __shared__ int hkeys[kHotSlots];
+  __shared__ int8_t hvals[kHotSlots];
+  const int lane = threadIdx.x & 31;
+  const int H = hot[0];
+  for (int s = threadIdx.x; s < kHotSlots; s += kThreads) hkeys[s] = -1;
+  __syncthreads();
+  if ((int)threadIdx.x < H) hot_insert(hkeys, hvals, hot[1 + threadIdx.x], threadIdx.x);
+  __syncthreads();
+  const int64_t warps = (int64_t)gridDim.x * (kThreads / 32);
+  for (int64_t q = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); q < n_rows_padded;
+       q += warps) {
+    float *col = qhot + (q / kTQ) * kHotMax * kTQ + (q % kTQ);
+    for (int h = lane; h < kHotMax; h += 32) col[h * kTQ] = 0.f;
+    __syncwarp();
+    if (q >= n_q) continue;
+    for (int64_t p = indptr[q] + lane; p < indptr[q + 1]; p += 32) {
+      const int32_t k = idx[p];
+      const int h = hot_find(hkeys, hvals, k);
+      if (h >= 0) col[h * kTQ] = val[p];
+      qcold[p] = h >= 0 ? -1 : k;
+    }
+  }
+}
+
+struct TileArgs {
+  const int64_t *q_indptr;
+  const int32_t *qcold;
+  const float *q_val;
+  int64_t n_q;
+  const float *inv_q;
+  const float *qhot;
+  const int32_t *hot;
+  const float *slab;
+  const int32_t *meta;
+  const unsigned char *image;
+  const float *inv_i;
+  int32_t n_items;
+  int32_t n_tiles;
+  int64_t n_qtiles;
+  int64_t n_units;
+  float *out;
+  int64_t ld_out;
+  int32_t vec_ok;
+  int32_t *status;
+};
+
+constexpr int kFThreads = 512;  // fast scorer: 16 warps, 4 query rows each
+constexpr int kRowsPerWarp = kTQ / (kFThreads / 32);
+constexpr int kGroup = 32 / kRowsPerWarp;  // lanes walking one row's segments
+constexpr int kHitCap = 24;  // hits of one query row walked per round
+constexpr int kMaxRounds = 1 << 20;  // far above any row's entry count
+constexpr int kFOffAcc = 0;
+constexpr int kFOffImg = kFOffAcc + kTQ * kTI * 4;
+constexpr int kFOffSlab = kFOffImg + kImgBytes;
+constexpr int kFOffQhot = kFOffSlab + kHotMax * kTI * 4;
+constexpr int kFOffHits = kFOffQhot + kHotMax * kTQ * 4;
+constexpr int kFOffInvQ = kFOffHits + kTQ * kHitCap * 8;
+constexpr int kFOffInvI = kFOffInvQ + kTQ * 4;
+constexpr int kFOffNh = kFOffInvI + kTI * 4;
+constexpr int kFastSmem = kFOffNh + kTQ * 4;
+static_assert(kFastSmem <= 232448, "fast scoring block exceeds 227 KB of shared memory");
+static_assert(kFOffSlab % 16 == 0 && kFOffQhot % 16 == 0 && kFOffHits % 16 == 0 &&
+                  kFOffInvI % 16 == 0,
+              "fast scorer shared sections must stay 16-byte aligned");
+
+// Copies n bytes (a multiple of 16, both addresses 16-byte aligned).
+__device__ __forceinline__ void cp_bytes(unsigned char *dst, const unsigned char *src, int n) {
+  for (int j = threadIdx.x * 16; j < n; j += kFThreads * 16) cp_async16(dst + j, src + j);
+}
+
+__device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
+
+// Looks dimension k up in the item tile's image: one 8-byte load per probe.
+// Returns the segment [start, end) packed as start | end << 16 (0 if absent).
+__device__ __forceinline__ uint32_t image_find(const uint2 *slots, int32_t k) {
+  uint32_t s = hash_a(k, kImgSlotsBits);
+  for (int n = 0; n < kImgSlots; ++n) {
+    const uint2 sl = slots[s];
+    if ((int32_t)sl.x == k) return sl.y;
+    if (sl.x == 0xffffffffu) return 0;
+    s = (s + 1) & (kImgSlots - 1);
+  }
+  return 0;
+}
+
+// Dense product over the hot dims for 512 threads: thread (lq, li) of warp
+// (wq, wi) owns queries wq*16 + lq*4 + [0, 4) and items wi*64 + li*8 + [0, 8).
+__device__ __forceinline__ void hot_product512(float *acc, const float *qhot, const float *slab,
+                                               int H) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int qb = (warp & 3) * 16 + (lane >> 3) * 4;
+  const int ib = (warp >> 2) * 64 + (lane & 7) * 8;
+  float2 c[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c[r][j] = make_float2(0.f, 0.f);
+  for (int h = 0; h < H; ++h) {
+    const float4 qa = *reinterpret_cast<const float4 *>(qhot + h * kTQ + qb);
+    const float4 ia = *reinterpret_cast<const float4 *>(slab + h * kTI + ib);
+    const float4 ic = *reinterpret_cast<const float4 *>(slab + h * kTI + ib + 4);
+    const float qv[4] = {qa.x, qa.y, qa.z, qa.w};
+    const float2 i0 = make_float2(ia.x, ia.y), i1 = make_float2(ia.z, ia.w);
+    const float2 i2 = make_float2(ic.x, ic.y), i3 = make_float2(ic.z, ic.w);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float2 qq = make_float2(qv[r], qv[r]);
+      c[r][0] = __ffma2_rn(qq, i0, c[r][0]);
+      c[r][1] = __ffma2_rn(qq, i1, c[r][1]);
+      c[r][2] = __ffma2_rn(qq, i2, c[r][2]);
+      c[r][3] = __ffma2_rn(qq, i3, c[r][3]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    float4 *d = reinterpret_cast<float4 *>(acc + (qb + r) * kTI + ib);
+    d[0] = make_float4(c[r][0].x, c[r][0].y, c[r][1].x, c[r][1].y);
+    d[1] = make_float4(c[r][2].x, c[r][2].y, c[r][3].x, c[r][3].y);
+  }
+}
+
+// The persistent fast scorer for item tiles that have an image.  Units are
+// (item tile, query tile) pairs, item-tile major, so a block loads an item
+// tile's image and slab once and runs every query tile of its range on it.
+// Per unit: the hot product writes acc; then warp w takes query rows
+// 4w..4w+3, looks up each row's cold nonzeros in the image, and walks the
+// hit segments with one 8-lane group per row (a group only touches its own
+// row, and within one segment every item is distinct, so no accumulator is
+// shared); then the normalised tile is stored.
+__global__ void __launch_bounds__(kFThreads, 1) k_score_tiles(const TileArgs a) {
+  extern __shared__ __align__(16) unsigned char fsm[];
+  float *acc = reinterpret_cast<float *>(fsm + kFOffAcc);
+  unsigned char *img = fsm + kFOffImg;
+  float *slab = reinterpret_cast<float *>(fsm + kFOffSlab);
+  float *qhot = reinterpret_cast<float *>(fsm + kFOffQhot);
+  uint2 *hits = reinterpret_cast<uint2 *>(fsm + kFOffHits);
+  float *invq = reinterpret_cast<float *>(fsm + kFOffInvQ);
+  float *invi = reinterpret_cast<float *>(fsm + kFOffInvI);
+  int *nh = reinterpret_cast<int *>(fsm + kFOffNh);
+  const uint2 *slots = reinterpret_cast<const uint2 *>(img + kImgOffSlots);
+  const uint8_t *seg_item = img + kImgOffItem;
+  const float *seg_val = reinterpret_cast<const float *>(img + kImgOffVal);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int H = a.hot[0];
+
+  const int64_t u0 = (int64_t)blockIdx.x * a.n_units / gridDim.x;
+  const int64_t u1 = (int64_t)(blockIdx.x + 1) * a.n_units / gridDim.x;
+  int cur_t = -1;
+  bool tile_ok = false;
+  for (int64_t u = u0; u < u1; ++u) {
+    const int t = (int)(u / a.n_qtiles);
+    const int64_t g = u % a.n_qtiles;
+    if (t != cur_t) {
+      cur_t = t;
+      tile_ok = a.meta[(size_t)t * kMetaInts + kMetaFits] != 0;
+      if (tile_ok) {
+        const unsigned char *src = a.image + (size_t)t * kImgBytes;
+        const int32_t E = reinterpret_cast<const int32_t *>(src)[1];
+        cp_bytes(img, src, kImgOffItem);  // header + slots
+        cp_bytes(img + kImgOffItem, src + kImgOffItem, round16(E));
+        cp_bytes(img + kImgOffVal, src + kImgOffVal, round16(4 * E));
+        cp_bytes(reinterpret_cast<unsigned char *>(slab),
+                 reinterpret_cast<const unsigned char *>(a.slab + (size_t)t * kHotMax * kTI),
+                 H * kTI * 4);
+        if (tid < kTI) {
+          const int i = t * kTI + tid;
+          invi[tid] = i < a.n_items ? __ldg(a.inv_i + i) : 0.f;
+        }
+      }
+    }
+    if (!tile_ok) continue;
+    const int64_t q0 = g * kTQ;
+    const int nq = (int)(a.n_q - q0 < kTQ ? a.n_q - q0 : kTQ);
+    cp_bytes(reinterpret_cast<unsigned char *>(qhot),
+             reinterpret_cast<const unsigned char *>(a.qhot + (size_t)g * kHotMax * kTQ),
+             H * kTQ * 4);
+    cp_async_commit();
+    if (tid < kTQ) invq[tid] = tid < nq ? __ldg(a.inv_q + q0 + tid) : 0.f;
+    // This warp's query rows: bounds and their first two 32-entry chunks,
+    // loaded now so that the wait hides behind the hot product.
+    int32_t p[kRowsPerWarp], e[kRowsPerWarp], ch[kRowsPerWarp], pk0[kRowsPerWarp], pk1[kRowsPerWarp];
+    float pv0[kRowsPerWarp], pv1[kRowsPerWarp];
+#pragma unroll
+    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+      const int r = warp * kRowsPerWarp + rr;
+      p[rr] = r < nq ? (int32_t)__ldg(a.q_indptr + q0 + r) : 0;
+      e[rr] = r < nq ? (int32_t)__ldg(a.q_indptr + q0 + r + 1) : 0;
+      ch[rr] = 0;
+    }
+#pragma unroll
+    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+      const int32_t p0 = p[rr] + lane, p1 = p0 + 32;
+      pk0[rr] = p0 < e[rr] ? __ldg(a.qcold + p0) : -1;
+      pv0[rr] = p0 < e[rr] ? __ldg(a.q_val + p0) : 0.f;
+      pk1[rr] = p1 < e[rr] ? __ldg(a.qcold + p1) : -1;
+      pv1[rr] = p1 < e[rr] ? __ldg(a.q_val + p1) : 0.f;
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    // 1. hot dims
+    if (H > 0) {
+      hot_product512(acc, qhot, slab, H);
+    } else {
+      float4 *acc4 = reinterpret_cast<float4 *>(acc);
+      for (int j = tid; j < kTQ * kTI / 4; j += kFThreads) acc4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+    // 2. cold dims: lookups row by row, then one lane group per row walks.
+    // Every round consumes at least one entry of some row; the round count is
+    // bounded anyway, and running out of rounds raises the status flag.
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int round = 0;; ++round) {
+      if (round == kMaxRounds) {
+        if (lane == 0) flag(a.status, DEV_STALL);
+        break;
+      }
+      bool left = false;
+#pragma unroll
+      for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+        uint2 *hrow = hits + (warp * kRowsPerWarp + rr) * kHitCap;
+        int n = 0;
+        while (p[rr] < e[rr]) {
+          const int32_t pp = p[rr] + lane;
+          int32_t k;
+          float v;
+          if (ch[rr] == 0) {
+            k = pk0[rr];
+            v = pv0[rr];
+          } else if (ch[rr] == 1) {
+            k = pk1[rr];
+            v = pv1[rr];
+          } else {
+            k = pp < e[rr] ? __ldg(a.qcold + pp) : -1;
+            v = pp < e[rr] ? __ldg(a.q_val + pp) : 0.f;
+          }
+          const uint32_t se = k >= 0 ? image_find(slots, k) : 0u;
+          const bool hit = (se >> 16) > (se & 0xffffu);
+          const unsigned mask = __ballot_sync(0xffffffffu, hit);
+          const int c = __popc(mask);
+          const int room = kHitCap - n;
+          const int rank = __popc(mask & lt_mask);
+          if (c <= room) {
+            if (hit) hrow[n + rank] = make_uint2(se, __float_as_uint(v));
+            n += c;
+            p[rr] = pp - lane + 32 < e[rr] ? pp - lane + 32 : e[rr];
+            ++ch[rr];
+            continue;
+          }
+          // More hits than room: keep the first `room` (room >= 1 whenever
+          // n == 0, since kHitCap >= 1, so every round makes progress) and
+          // resume right after the last one kept.
+          if (room > 0) {
+            if (hit && rank < room) hrow[n + rank] = make_uint2(se, __float_as_uint(v));
+            unsigned m = mask;
+            for (int j = 1; j < room; ++j) m &= m - 1u;  // drop the lowest room-1 hits
+            p[rr] = pp - lane + __ffs(m);                 // one past the room-th hit's lane
+            ch[rr] = 2;  // later chunks no longer line up with the prefetched ones
+            n += room;
+          }
+          break;
+        }
+        if (lane == 0) nh[warp * kRowsPerWarp + rr] = n;
+        left |= p[rr] < e[rr];
+      }
+      __syncwarp();
+      const int grp = lane / kGroup, li = lane % kGroup;
+      const int row = warp * kRowsPerWarp + grp;
+      const int my_n = nh[row];
+      const uint2 *hrow = hits + row * kHitCap;
+      float *arow = acc + row * kTI;
+      for (int h = 0; h < my_n; ++h) {
+        const uint2 hh = hrow[h];
+        const float qv = __uint_as_float(hh.y);
+        const int end = (int)(hh.x >> 16);
+        // Two entries of the segment per step (distinct items, so the two
+        // read-modify-writes are independent).
+        int j = (int)(hh.x & 0xffffu) + li;
+        for (; j + kGroup < end; j += 2 * kGroup) {
+          float *d0 = arow + seg_item[j];
+          float *d1 = arow + seg_item[j + kGroup];
+          const float v0 = seg_val[j], v1 = seg_val[j + kGroup];
+          const float a0 = *d0, a1 = *d1;
+          *d0 = fmaf(qv, v0, a0);
+          *d1 = fmaf(qv, v1, a1);
+        }
+        if (j < end) {
+          float *d = arow + seg_item[j];
+          *d = fmaf(qv, seg_val[j], *d);
+        }
+      }
+      __syncwarp();
+      if (!__any_sync(0xffffffffu, left)) break;
+    }
+    __syncthreads();
+    // 3. normalise and store
+    {
+      const int i0 = t * kTI;
+      const int ni = min(kTI, a.n_items - i0);
+      const int c = (tid & 63) * 4;
+      if (c < ni) {
+        const float4 n4 = *reinterpret_cast<const float4 *>(invi + c);
+        const bool vec = a.vec_ok && (c + 4 <= ni);
+        for (int r = tid >> 6; r < nq; r += kFThreads / 64) {
+          const float4 v = *reinterpret_cast<const float4 *>(acc + r * kTI + c);
+          const float iq = invq[r];
+          float *dst = a.out + (q0 + r) * a.ld_out + i0 + c;
+          const float o0 = v.x * iq * n4.x, o1 = v.y * iq * n4.y, o2 = v.z * iq * n4.z,
+                      o3 = v.w * iq * n4.w;
+          if (vec) {
+            __stcs(reinterpret_cast<float4 *>(dst), make_float4(o0, o1, o2, o3));
+          } else {
+            const float o[4] = {o0, o1, o2, o3};
+            for (int j = 0; j < 4 && c + j < ni; ++j) dst[j] = o[j];
+          }
+        }
+      }
+    }
     __syncthreads();
   }
   cp_async_wait_all();
@@ -679,6 +1202,7 @@ cudaError_t launch_hot_select(ss_handle *h, const ss_csr &items, cudaStream_t s,
   h->hot_src[2] = items.values;
   h->hot_src_rows = items.n_rows;
   h->hot_src_nnz = items.nnz;
+  ++h->hot_generation;
   return cudaSuccess;
 }
 
@@ -686,18 +1210,18 @@ cudaError_t launch_build_hybrid(ss_handle *h, const ss_csr &items, int64_t row_b
                                 int64_t row_end, cudaStream_t s) {
   const int n_items = (int)(row_end - row_begin);
   const int n_tiles = (n_items + kTI - 1) / kTI;
-  cudaError_t e = cudaMemsetAsync(h->heavy_cursor, 0, sizeof(int32_t), s);
+  cudaError_t e = cudaMemsetAsync(h->counters, 0, 2 * sizeof(int32_t), s);
   if (e != cudaSuccess) return e;
-  const size_t smem = sizeof(float) * kHotMax * kTI;
   static bool configured = false;
   if (!configured) {
-    e = cudaFuncSetAttribute(k_build_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(k_build_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize, kBuildSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  k_build_tiles<<<n_tiles, kThreads, smem, s>>>(
+  k_build_tiles<<<n_tiles, kThreads, kBuildSmem, s>>>(
       items.indptr, items.indices, items.values, row_begin, row_end, h->hot, h->slab, h->ell,
-      h->meta, h->heavy_k, h->heavy_v, h->heavy_item, h->heavy_cursor, h->heavy_cap, h->d_status);
+      h->meta, h->heavy_k, h->heavy_v, h->heavy_item, h->counters, h->heavy_cap, h->image,
+      h->d_status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ss_index &ix = h->index;
@@ -714,20 +1238,104 @@ cudaError_t launch_build_hybrid(ss_handle *h, const ss_csr &items, int64_t row_b
   ix.heavy_k = h->heavy_k;
   ix.heavy_v = h->heavy_v;
   ix.heavy_item = h->heavy_item;
+  ix.image = h->image;
+  ix.counters = h->counters;
   return cudaSuccess;
 }
 
-cudaError_t launch_score_hybrid(const ss_handle *h, const ss_csr &queries, const float *inv_q,
+// Hot values per query tile and the cold index view, for the current hot
+// set; redone when the query matrix or the hot set changes.
+static cudaError_t prepare_queries(ss_handle *h, const ss_csr &q, cudaStream_t s, int *queued) {
+  *queued = 0;
+  if (h->prep_src[0] == q.indptr && h->prep_src[1] == q.indices && h->prep_src[2] == q.values &&
+      h->prep_rows == q.n_rows && h->prep_nnz == q.nnz && h->prep_generation == h->hot_generation)
+    return cudaSuccess;
+  const int64_t n_qtiles = (q.n_rows + kTQ - 1) / kTQ;
+  const int64_t need_hot = std::max<int64_t>(1, n_qtiles * kHotMax * kTQ);
+  const int64_t need_cold = std::max<int64_t>(1, q.nnz);
+  if (need_hot > h->qhot_cap || need_cold > h->qcold_cap) {
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    if (need_hot > h->qhot_cap) {
+      cudaFree(h->qhot);
+      h->qhot = nullptr;
+      h->qhot_cap = 0;
+      e = cudaMalloc(&h->qhot, sizeof(float) * (size_t)need_hot);
+      if (e != cudaSuccess) return e;
+      h->qhot_cap = need_hot;
+    }
+    if (need_cold > h->qcold_cap) {
+      cudaFree(h->qcold);
+      h->qcold = nullptr;
+      h->qcold_cap = 0;
+      e = cudaMalloc(&h->qcold, sizeof(int32_t) * (size_t)need_cold);
+      if (e != cudaSuccess) return e;
+      h->qcold_cap = need_cold;
+    }
+  }
+  const int64_t rows_padded = n_qtiles * kTQ;
+  const int64_t blocks_needed = (rows_padded + kThreads / 32 - 1) / (kThreads / 32);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(blocks_needed, (int64_t)h->sm_count * 8));
+  k_prep_queries<<<grid, kThreads, 0, s>>>(q.indptr, q.indices, q.values, q.n_rows, rows_padded,
+                                           h->hot, h->qhot, h->qcold);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  *queued = 1;
+  h->prep_src[0] = q.indptr;
+  h->prep_src[1] = q.indices;
+  h->prep_src[2] = q.values;
+  h->prep_rows = q.n_rows;
+  h->prep_nnz = q.nnz;
+  h->prep_generation = h->hot_generation;
+  return cudaSuccess;
+}
+
+cudaError_t launch_score_hybrid(ss_handle *h, const ss_csr &queries, const float *inv_q,
                                 const ss_index &idx, const float *inv_i, float *out,
-                                int64_t ld_out, cudaStream_t s) {
+                                int64_t ld_out, cudaStream_t s, int *queued) {
+  *queued = 0;
   if (queries.n_rows == 0 || idx.n_items == 0) return cudaSuccess;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(k_score_hybrid, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kScoreSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_score_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize, kFastSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  int prep = 0;
+  cudaError_t e = prepare_queries(h, queries, s, &prep);
+  if (e != cudaSuccess) return e;
+  const int64_t n_qtiles = (queries.n_rows + kTQ - 1) / kTQ;
+  const int vec_ok = ((reinterpret_cast<uintptr_t>(out) % 16) == 0) && (ld_out % 4 == 0);
+  const int sms = h->sm_count > 0 ? h->sm_count : 148;
+
+  TileArgs f;
+  f.q_indptr = queries.indptr;
+  f.qcold = h->qcold;
+  f.q_val = queries.values;
+  f.n_q = queries.n_rows;
+  f.inv_q = inv_q;
+  f.qhot = h->qhot;
+  f.hot = idx.hot;
+  f.slab = idx.slab;
+  f.meta = idx.meta;
+  f.image = idx.image;
+  f.inv_i = inv_i;
+  f.n_items = idx.n_items;
+  f.n_tiles = idx.n_tiles;
+  f.n_qtiles = n_qtiles;
+  f.n_units = n_qtiles * idx.n_tiles;
+  f.out = out;
+  f.ld_out = ld_out;
+  f.vec_ok = vec_ok;
+  f.status = h->d_status;
+  const int grid_f = (int)std::min<int64_t>(f.n_units, sms);
+  k_score_tiles<<<grid_f, kFThreads, kFastSmem, s>>>(f);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
   HybridArgs a;
   a.q_indptr = queries.indptr;
   a.q_idx = queries.indices;
@@ -744,14 +1352,15 @@ cudaError_t launch_score_hybrid(const ss_handle *h, const ss_csr &queries, const
   a.inv_i = inv_i;
   a.n_items = idx.n_items;
   a.n_tiles = idx.n_tiles;
-  const int64_t n_qtiles = (queries.n_rows + kTQ - 1) / kTQ;
-  a.n_units = n_qtiles * idx.n_tiles;
-  if (a.n_units == 0) return cudaSuccess;
+  a.n_qtiles = n_qtiles;
+  a.counters = idx.counters;
   a.out = out;
   a.ld_out = ld_out;
-  a.vec_ok = ((reinterpret_cast<uintptr_t>(out) % 16) == 0) && (ld_out % 4 == 0);
+  a.vec_ok = vec_ok;
   a.dim = (int32_t)idx.dim;
-  const int grid = (int)std::min<int64_t>(a.n_units, h->sm_count > 0 ? h->sm_count : 148);
-  k_score_hybrid<<<grid, kThreads, kScoreSmem, s>>>(a);
-  return cudaGetLastError();
+  k_score_hybrid<<<sms, kThreads, kScoreSmem, s>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  *queued = prep + 2;
+  return cudaSuccess;
 }

@@ -14,6 +14,7 @@ enum : int32_t {
   DEV_UNSORTED = 1,
   DEV_OUT_OF_RANGE = 2,
   DEV_CAPACITY = 3,
+  DEV_STALL = 4,  // a bounded loop ran out of iterations
 };
 
 // Scoring algorithms.
@@ -27,7 +28,7 @@ namespace hyb {
 constexpr int kTQ = 64;                    // query rows per tile
 constexpr int kTI = 256;                   // items per tile (one thread per item)
 constexpr int kThreads = 256;              // threads per block (8 warps)
-constexpr int kHotMax = 48;                // dense ("hot") dimensions per item matrix
+constexpr int kHotMax = 24;                // dense ("hot") dimensions per item matrix
 constexpr int kEllMaxW = 1024;             // cold entries per item kept in the ELL block
 constexpr int kMetaInts = 16;              // per item tile: 8 warp lengths, heavy begin, count
 constexpr int kBatchEntries = 4096;        // cold query entries per hashed batch
@@ -37,6 +38,21 @@ constexpr int kBitmapBits = 15;
 constexpr int kBitmapWords = (1 << kBitmapBits) / 32;
 constexpr int kHotSampleEntries = 8192;    // nonzeros sampled to choose the hot set
 constexpr int kHotMinPercent = 20;         // a dimension is hot if >= 20% of sampled rows hold it
+
+// Per item tile, the cold nonzeros as an inverted index (an "image" that the
+// scoring block copies into shared memory as is): dimension -> segment of
+// (item, value).  Tiles whose cold part does not fit keep the ELL format.
+constexpr int kImgSlotsBits = 13;
+constexpr int kImgSlots = 1 << kImgSlotsBits;      // {dim or -1, start | end << 16}
+constexpr int kImgDCap = 6144;                     // distinct cold dims per tile (load <= 3/4)
+constexpr int kImgECap = 10240;                    // cold nonzeros per tile
+constexpr int kImgOffSlots = 16;                   // after the header {D, E, fits, 0}
+constexpr int kImgOffItem = kImgOffSlots + kImgSlots * 8;       // u8 item[E]
+constexpr int kImgOffVal = kImgOffItem + kImgECap;              // float value[E]
+constexpr int kImgBytes = kImgOffVal + kImgECap * 4;
+static_assert(kImgOffItem % 16 == 0 && kImgOffVal % 16 == 0 && kImgBytes % 16 == 0,
+              "image sections must stay 16-byte aligned");
+constexpr int kMetaFits = 10;              // meta slot: 1 if the tile has an image
 }  // namespace hyb
 
 // The per-chunk index.  ALGO_POSTING: one posting list of (item, value) per
@@ -63,6 +79,8 @@ struct ss_index {
   const int32_t *heavy_k = nullptr;    // heavy items' cold entries: dim
   const float *heavy_v = nullptr;      //   value
   const uint8_t *heavy_item = nullptr; //   item within its tile
+  const unsigned char *image = nullptr; // [tile][kImgBytes]
+  const int32_t *counters = nullptr;   // [0] heavy cursor, [1] tiles without an image, [2..] their ids
 };
 
 struct ss_handle {
@@ -93,12 +111,24 @@ struct ss_handle {
   int32_t *heavy_k = nullptr;    // [heavy_cap]
   float *heavy_v = nullptr;
   uint8_t *heavy_item = nullptr;
-  int32_t *heavy_cursor = nullptr;
+  int32_t *counters = nullptr;   // [2 + max tiles]: heavy cursor, overflow count, overflow ids
   int64_t heavy_cap = 0;
   int32_t max_tiles = 0;
-  // The hot set is chosen once per item matrix: the matrix it was chosen for.
+  unsigned char *image = nullptr; // [max tiles][kImgBytes]
+  // Queries prepared for the current hot set: hot values per query tile
+  // ([tile][kHotMax][kTQ]) and the indices with hot dims replaced by -1.
+  float *qhot = nullptr;
+  int32_t *qcold = nullptr;
+  int64_t qhot_cap = 0, qcold_cap = 0;
+  // The hot set is chosen once per item matrix: the matrix it was chosen for,
+  // and a counter that changes whenever it is chosen again.
   const void *hot_src[3] = {nullptr, nullptr, nullptr};
   int64_t hot_src_rows = -1, hot_src_nnz = -1;
+  uint64_t hot_generation = 0;
+  // The query matrix (and hot generation) qhot / qcold were prepared for.
+  const void *prep_src[3] = {nullptr, nullptr, nullptr};
+  int64_t prep_rows = -1, prep_nnz = -1;
+  uint64_t prep_generation = ~0ull;
 
   ss_index index;
 };
@@ -115,9 +145,11 @@ cudaError_t launch_score_chunk(const ss_handle *h, const ss_csr &queries, const 
 cudaError_t launch_hot_select(ss_handle *h, const ss_csr &items, cudaStream_t s, int *queued);
 cudaError_t launch_build_hybrid(ss_handle *h, const ss_csr &items, int64_t row_begin,
                                 int64_t row_end, cudaStream_t s);
-cudaError_t launch_score_hybrid(const ss_handle *h, const ss_csr &queries, const float *inv_q,
+// Queues the query preparation (when needed), the fast tile scorer and the
+// fallback scorer; *queued gets the number of kernels queued.
+cudaError_t launch_score_hybrid(ss_handle *h, const ss_csr &queries, const float *inv_q,
                                 const ss_index &idx, const float *inv_i, float *out,
-                                int64_t ld_out, cudaStream_t s);
+                                int64_t ld_out, cudaStream_t s, int *queued);
 
 // Kernels queued by one launch_build_index call.
 constexpr int kIndexKernels = 5;

@@ -272,6 +272,28 @@ def test_hot_set_saturated_and_empty(sec):
     assert _max_err(_gpu_cosine(sec, Q, I), oracle.cosine(Q, I)) <= TOL
 
 
+def test_index_stats_hot_set(sec):
+    """The hot set holds the dimensions in >= 20% of sampled rows: about two
+    dozen on the Zipf(1.1) workload, none on the uniform one."""
+    cfg = CONFIGS["d1.2m_q5k_i200k"]
+    I = generate_rows(cfg, 1, 0, 20_000)
+    # expected hot count from the data itself: dims in >= 20% of rows
+    frac = np.bincount(I.indices, minlength=cfg.dim) / I.n_rows
+    expect = int((frac >= 0.2).sum())
+    with sec.SparseCosine(cfg.dim) as h:
+        i = _dev(sec, I)
+        st = h.index_stats(h.build_item_index(i, 0, 8192))
+    assert st["algorithm"] == 0 and st["items"] == 8192 and st["tiles"] == 32
+    assert abs(st["hot_dims"] - expect) <= 3, (st, expect)
+    assert st["tiles_without_image"] == 0  # every tile takes the inverted-index path
+    cfg3 = CONFIGS["d500k_q50k_i500k_uniform"]
+    U = generate_rows(cfg3, 1, 0, 3000)
+    with sec.SparseCosine(cfg3.dim) as h:
+        st = h.index_stats(h.build_item_index(_dev(sec, U), 0, 3000))
+    assert st["hot_dims"] == 0 and st["ell_width_max"] >= 400
+    assert st["tiles_without_image"] == st["tiles"]  # 500 nonzeros a row: no tile fits an image
+
+
 @pytest.mark.parametrize("name", ["d1.2m_q5k_i200k", "d1.2m_q20k_i1m_heavy"])
 def test_two_gpu_algorithms_agree(sec, name):
     cfg = CONFIGS[name]
