@@ -132,13 +132,14 @@ ss_status ensure_capacity(ss_handle *h, int64_t need) {
 void free_workspace(ss_handle *h) {
   void *ptrs[] = {h->d_status, h->col_cnt, h->col_ptr, h->scan_part, h->post_item, h->post_val,
                   h->hot, h->slab, h->ell, h->meta, h->heavy_k, h->heavy_v, h->heavy_item,
-                  h->counters, h->image, h->qhot, h->qcold};
+                  h->counters, h->image, h->qhot, h->qcold, h->qcold_n};
   for (void *p : ptrs) cudaFree(p);
   h->counters = nullptr;
   h->image = nullptr;
   h->qhot = nullptr;
   h->qcold = nullptr;
-  h->qhot_cap = h->qcold_cap = 0;
+  h->qcold_n = nullptr;
+  h->qhot_cap = h->qcold_cap = h->qcold_n_cap = 0;
   h->d_status = nullptr;
   h->col_cnt = h->col_ptr = h->scan_part = nullptr;
   h->post_item = nullptr;

@@ -151,19 +151,6 @@ __global__ void __launch_bounds__(kSelThreads)
 }
 
 // ---------------------------------------------------------------- builder
-__device__ __forceinline__ int block_sum(int v, int *red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  int t = 0;
-#pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) t += red[w];
-  __syncthreads();
-  return t;
-}
-
 __device__ __forceinline__ int block_exclusive_scan(int v, int *red, int *total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int inc = v;
@@ -207,16 +194,53 @@ __device__ __forceinline__ int img_find(const int *keys, int32_t k) {
 }
 
 // Shared memory of the builder block (bytes).
+constexpr int kBThreads = 1024;  // builder: 32 warps, one item row per warp at a time
 constexpr int kBldOffSlab = 0;
 constexpr int kBldOffKeys = kBldOffSlab + kHotMax * kTI * 4;
 constexpr int kBldOffCnt = kBldOffKeys + kImgSlots * 4;
-constexpr int kBuildSmem = kBldOffCnt + kImgSlots * 4;
+constexpr int kBldOffCold = kBldOffCnt + kImgSlots * 4;  // cold nonzeros per item
+constexpr int kBuildSmem = kBldOffCold + kTI * 4;
 
-// One block per tile of kTI items, one thread per item.  Hot values go to
-// the tile's slab.  The cold nonzeros become the tile's image (dimension ->
-// segment of (item, value)) when they fit; otherwise they go to the ELL
+__device__ __forceinline__ int bblock_sum(int v, int *red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  int t = 0;
+#pragma unroll
+  for (int w = 0; w < kBThreads / 32; ++w) t += red[w];
+  __syncthreads();
+  return t;
+}
+
+__device__ __forceinline__ int bblock_exclusive_scan(int v, int *red, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += t;
+  }
+  if (lane == 31) red[warp] = inc;
+  __syncthreads();
+  int off = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kBThreads / 32; ++w) {
+    off += (w < warp) ? red[w] : 0;
+    tot += red[w];
+  }
+  __syncthreads();
+  *total = tot;
+  return off + inc - v;
+}
+
+// One block per tile of kTI items; warp w handles items w, w + 32, ..., its
+// lanes taking the row's nonzeros 32 at a time (coalesced).  Hot values go
+// to the tile's slab.  The cold nonzeros become the tile's image (dimension
+// -> segment of (item, value)) when they fit; otherwise they go to the ELL
 // block and the heavy list, and the tile joins the overflow list.
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kBThreads, 1)
     k_build_tiles(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
                   const float *__restrict__ values, int64_t row_begin, int64_t row_end,
                   const int32_t *__restrict__ hot, float *__restrict__ slab,
@@ -228,113 +252,120 @@ __global__ void __launch_bounds__(kThreads)
   float *slab_s = reinterpret_cast<float *>(bsm + kBldOffSlab);  // [kHotMax][kTI]
   int *ikeys = reinterpret_cast<int *>(bsm + kBldOffKeys);
   int *icnt = reinterpret_cast<int *>(bsm + kBldOffCnt);
+  int *cold_n = reinterpret_cast<int *>(bsm + kBldOffCold);
   __shared__ int hkeys[kHotSlots];
   __shared__ int8_t hvals[kHotSlots];
-  __shared__ int red[kThreads / 32];
+  __shared__ int red[kBThreads / 32];
   __shared__ int heavy_base, img_fail;
+  __shared__ int heavy_off[kTI];
+  __shared__ uint32_t bits_s[(1 << kImgBitsLog2) / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int w = tid; w < (1 << kImgBitsLog2) / 32; w += kBThreads) bits_s[w] = 0u;
   const int t = blockIdx.x;
-  const int64_t item = row_begin + (int64_t)t * kTI + tid;
-  const bool valid = item < row_end;
+  const int64_t item0 = row_begin + (int64_t)t * kTI;
+  const int n_items = (int)min((int64_t)kTI, row_end - item0);
   const int H = hot[0];
-  for (int s = tid; s < kHotSlots; s += kThreads) hkeys[s] = -1;
+  for (int s = tid; s < kHotSlots; s += kBThreads) hkeys[s] = -1;
+  for (int s = tid; s < kImgSlots; s += kBThreads) {
+    ikeys[s] = -1;
+    icnt[s] = 0;
+  }
+  for (int j = tid; j < H * kTI; j += kBThreads) slab_s[j] = 0.0f;
   if (tid == 0) img_fail = 0;
   __syncthreads();
   if (tid < H) hot_insert(hkeys, hvals, hot[1 + tid], tid);
-  for (int h = 0; h < H; ++h) slab_s[h * kTI + tid] = 0.0f;
   __syncthreads();
 
-  int64_t pb = 0, pe = 0;
-  if (valid) {
-    pb = indptr[item];
-    pe = indptr[item + 1];
+  // Pass 1: hot values into the slab; cold dims into the image hash.
+  for (int it = warp; it < kTI; it += kBThreads / 32) {
+    int cold = 0;
+    if (it < n_items) {
+      const int64_t pb = indptr[item0 + it], pe = indptr[item0 + it + 1];
+      for (int64_t p = pb + lane; p < pe; p += 32) {
+        const int32_t k = __ldg(indices + p);
+        const int h = hot_find(hkeys, hvals, k);
+        if (h >= 0) {
+          slab_s[h * kTI + it] = __ldg(values + p);
+        } else {
+          ++cold;
+          const int slot = img_insert(ikeys, k);
+          if (slot < 0) img_fail = 1;
+          else atomicAdd(&icnt[slot], 1);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cold += __shfl_xor_sync(0xffffffffu, cold, o);
+    if (lane == 0) cold_n[it] = cold;
   }
-  int cold = 0;
-  for (int64_t p = pb; p < pe; ++p) {
-    const int h = hot_find(hkeys, hvals, indices[p]);
-    if (h >= 0) slab_s[h * kTI + tid] = values[p];
-    else ++cold;
-  }
-  const int n_valid = block_sum(valid ? 1 : 0, red);
-  const int sum_cold = block_sum(cold, red);
+  __syncthreads();
+  const int my_cold = tid < kTI ? cold_n[tid] : 0;
+  const int sum_cold = bblock_sum(my_cold, red);
   unsigned char *img = image + (size_t)t * kImgBytes;
   int32_t *hdr = reinterpret_cast<int32_t *>(img);
 
   // ---- image path
-  bool fits = sum_cold <= kImgECap;
+  constexpr int kPer = kImgSlots / kBThreads;
+  int occ = 0, ent = 0;
+  for (int j = 0; j < kPer; ++j) {
+    const int s = tid * kPer + j;
+    occ += ikeys[s] >= 0;
+    ent += icnt[s];
+  }
+  int D = 0, E = 0;
+  (void)bblock_exclusive_scan(occ, red, &D);
+  int e_run = bblock_exclusive_scan(ent, red, &E);
+  const bool fits = !img_fail && sum_cold <= kImgECap && D <= kImgDCap && E == sum_cold;
   if (fits) {
-    for (int s = tid; s < kImgSlots; s += kThreads) {
-      ikeys[s] = -1;
-      icnt[s] = 0;
-    }
-    __syncthreads();
-    for (int64_t p = pb; p < pe; ++p) {
-      const int32_t k = indices[p];
-      if (hot_find(hkeys, hvals, k) >= 0) continue;
-      const int slot = img_insert(ikeys, k);
-      if (slot < 0) img_fail = 1;
-      else atomicAdd(&icnt[slot], 1);
-    }
-    __syncthreads();
-    constexpr int kPer = kImgSlots / kThreads;
-    int occ = 0, ent = 0;
+    uint2 *gslot = reinterpret_cast<uint2 *>(img + kImgOffSlots);
     for (int j = 0; j < kPer; ++j) {
       const int s = tid * kPer + j;
-      occ += ikeys[s] >= 0;
-      ent += icnt[s];
+      if (ikeys[s] >= 0) {
+        const int c = icnt[s];
+        gslot[s] = make_uint2((uint32_t)ikeys[s], (uint32_t)e_run | ((uint32_t)(e_run + c) << 16));
+        icnt[s] = e_run;  // now the fill cursor of this segment
+        e_run += c;
+        const uint32_t bb = hash_b(ikeys[s], kImgBitsLog2);
+        atomicOr(&bits_s[bb >> 5], 1u << (bb & 31));
+      } else {
+        gslot[s] = make_uint2(0xffffffffu, 0u);
+      }
     }
-    int D = 0, E = 0;
-    int d_run = block_exclusive_scan(occ, red, &D);
-    int e_run = block_exclusive_scan(ent, red, &E);
-    fits = !img_fail && D <= kImgDCap && E <= kImgECap;
-    if (fits) {
-      uint2 *gslot = reinterpret_cast<uint2 *>(img + kImgOffSlots);
-      for (int j = 0; j < kPer; ++j) {
-        const int s = tid * kPer + j;
-        if (ikeys[s] >= 0) {
-          const int c = icnt[s];
-          gslot[s] = make_uint2((uint32_t)ikeys[s], (uint32_t)e_run | ((uint32_t)(e_run + c) << 16));
-          icnt[s] = e_run;  // now the fill cursor of this segment
-          e_run += c;
-        } else {
-          gslot[s] = make_uint2(0xffffffffu, 0u);
-        }
-      }
-      (void)d_run;
-      if (tid == 0) {
-        hdr[0] = D;
-        hdr[1] = E;
-        hdr[2] = 1;
-        hdr[3] = 0;
-      }
-      __syncthreads();
-      uint8_t *gitem = img + kImgOffItem;
-      float *gval = reinterpret_cast<float *>(img + kImgOffVal);
-      for (int64_t p = pb; p < pe; ++p) {
-        const int32_t k = indices[p];
+    if (tid == 0) {
+      hdr[0] = D;
+      hdr[1] = E;
+      hdr[2] = 1;
+      hdr[3] = 0;
+    }
+    __syncthreads();
+    uint32_t *gbits = reinterpret_cast<uint32_t *>(img + kImgOffBits);
+    for (int w = tid; w < (1 << kImgBitsLog2) / 32; w += kBThreads) gbits[w] = bits_s[w];
+    uint8_t *gitem = img + kImgOffItem;
+    float *gval = reinterpret_cast<float *>(img + kImgOffVal);
+    for (int it = warp; it < n_items; it += kBThreads / 32) {
+      const int64_t pb = indptr[item0 + it], pe = indptr[item0 + it + 1];
+      for (int64_t p = pb + lane; p < pe; p += 32) {
+        const int32_t k = __ldg(indices + p);
         if (hot_find(hkeys, hvals, k) >= 0) continue;
-        const int slot = img_find(ikeys, k);
-        const int pos = atomicAdd(&icnt[slot], 1);
-        gitem[pos] = (uint8_t)tid;
-        gval[pos] = values[p];
+        const int pos = atomicAdd(&icnt[img_find(ikeys, k)], 1);
+        gitem[pos] = (uint8_t)it;
+        gval[pos] = __ldg(values + p);
       }
     }
   }
 
   // ---- ELL path for tiles whose cold part does not fit an image
-  int len_w = 0;
-  int64_t hbase = 0;
+  int32_t *m = meta + (size_t)t * kMetaInts;
   int heavy_total = 0;
   bool heavy_ok = true;
   if (!fits) {
-    const int mean = n_valid > 0 ? sum_cold / n_valid : 0;
+    // Items far above the tile's mean go to the heavy list.
+    const int mean = n_items > 0 ? sum_cold / n_items : 0;
     const int thr = min(kEllMaxW, 2 * mean + 32);
-    const bool heavy = cold > thr;
-    const int reg_len = heavy ? 0 : cold;
-    len_w = reg_len;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) len_w = max(len_w, __shfl_xor_sync(0xffffffffu, len_w, o));
-    const int my_off = block_exclusive_scan(heavy ? cold : 0, red, &heavy_total);
+    const bool my_heavy = tid < n_items && my_cold > thr;
+    const int off = bblock_exclusive_scan(my_heavy ? my_cold : 0, red, &heavy_total);
+    if (tid < kTI) heavy_off[tid] = my_heavy ? off : -1;
     if (tid == 0) {
       heavy_base = heavy_total > 0 ? atomicAdd(&counters[0], heavy_total) : 0;
       hdr[2] = 0;
@@ -342,34 +373,62 @@ __global__ void __launch_bounds__(kThreads)
       counters[2 + c] = t;
     }
     __syncthreads();
-    hbase = heavy_base;
+    const int64_t hbase = heavy_base;
     heavy_ok = hbase + heavy_total <= heavy_cap;
     if (tid == 0 && !heavy_ok) flag(status, DEV_CAPACITY);
-    int2 *col = ell + (size_t)t * kEllMaxW * kTI + tid;
-    int s = 0;
-    for (int64_t p = pb; p < pe; ++p) {
-      const int32_t k = indices[p];
-      if (hot_find(hkeys, hvals, k) >= 0) continue;
-      const float v = values[p];
-      if (!heavy) {
-        col[(size_t)s * kTI] = make_int2(k, __float_as_int(v));
-      } else if (heavy_ok) {
-        const int64_t e = hbase + my_off + s;
-        heavy_k[e] = k;
-        heavy_v[e] = v;
-        heavy_item[e] = (uint8_t)tid;
-      }
-      ++s;
+    // ELL width of each warp group of 32 items: the longest regular row.
+    if (tid < kTI) {
+      int len = heavy_off[tid] < 0 ? cold_n[tid] : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) len = max(len, __shfl_xor_sync(0xffffffffu, len, o));
+      if (lane == 0) m[warp] = len;
+      if (lane == 0) red[warp] = len;
     }
-    for (int j = reg_len; j < len_w; ++j) col[(size_t)j * kTI] = make_int2(-1, 0);
+    __syncthreads();
+    for (int it = warp; it < kTI; it += kBThreads / 32) {
+      const int hoff = heavy_off[it];
+      const int len_w = red[it >> 5];
+      int2 *col = ell + (size_t)t * kEllMaxW * kTI + it;
+      int s = 0;
+      if (it < n_items) {
+        const int64_t pb = indptr[item0 + it], pe = indptr[item0 + it + 1];
+        for (int64_t p = pb; p < pe; p += 32) {
+          const int64_t pp = p + lane;
+          int32_t k = -1;
+          bool is_cold = false;
+          if (pp < pe) {
+            k = __ldg(indices + pp);
+            is_cold = hot_find(hkeys, hvals, k) < 0;
+          }
+          const unsigned cm = __ballot_sync(0xffffffffu, is_cold);
+          const int pos = s + __popc(cm & lt_mask);
+          if (is_cold) {
+            const float v = __ldg(values + pp);
+            if (hoff < 0) {
+              col[(size_t)pos * kTI] = make_int2(k, __float_as_int(v));
+            } else if (heavy_ok) {
+              const int64_t e = hbase + hoff + pos;
+              heavy_k[e] = k;
+              heavy_v[e] = v;
+              heavy_item[e] = (uint8_t)it;
+            }
+          }
+          s += __popc(cm);
+        }
+      }
+      const int reg_len = hoff < 0 ? s : 0;
+      for (int j = reg_len + lane; j < len_w; j += 32) col[(size_t)j * kTI] = make_int2(-1, 0);
+    }
+    if (tid == 0) m[8] = (int32_t)hbase;
+  } else if (tid < 8) {
+    m[tid] = 0;
   }
-  float *dst = slab + (size_t)t * kHotMax * kTI + tid;
-  for (int h = 0; h < H; ++h) dst[(size_t)h * kTI] = slab_s[h * kTI + tid];
-  int32_t *m = meta + (size_t)t * kMetaInts;
-  if (lane == 0) m[warp] = len_w;
+  __syncthreads();
+  float *dst = slab + (size_t)t * kHotMax * kTI;
+  for (int j = tid; j < H * kTI; j += kBThreads) dst[j] = slab_s[j];
   if (tid == 0) {
-    m[8] = (int32_t)hbase;
-    m[9] = heavy_ok ? heavy_total : 0;
+    if (fits) m[8] = 0;
+    m[9] = (!fits && heavy_ok) ? heavy_total : 0;
     m[kMetaFits] = fits ? 1 : 0;
   }
 }
@@ -837,16 +896,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_hybrid(const HybridArgs a
 // ---------------------------------------------------------------- fast path
 // One warp per query row: the row's hot values into its column of the query
 // tile's hot block ([tile][kHotMax][kTQ], zero where absent), and the row's
-// indices with the hot dimensions replaced by -1.  Rows past n_q in the last
-// tile get a zero column.
+// cold nonzeros as {dim, value bits}, in their original (ascending) order,
+// moved to the front of the row's own range, with their count.  Rows past
+// n_q in the last tile get a zero column.
 __global__ void __launch_bounds__(kThreads)
     k_prep_queries(const int64_t *__restrict__ indptr, const int32_t *__restrict__ idx,
                    const float *__restrict__ val, int64_t n_q, int64_t n_rows_padded,
                    const int32_t *__restrict__ hot, float *__restrict__ qhot,
-                   int32_t *__restrict__ qcold) {
+                   int2 *__restrict__ qcold, int32_t *__restrict__ qcold_n) {
   __shared__ int hkeys[kHotSlots];
   __shared__ int8_t hvals[kHotSlots];
   const int lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
   const int H = hot[0];
   for (int s = threadIdx.x; s < kHotSlots; s += kThreads) hkeys[s] = -1;
   __syncthreads();
@@ -859,19 +920,32 @@ __global__ void __launch_bounds__(kThreads)
     for (int h = lane; h < kHotMax; h += 32) col[h * kTQ] = 0.f;
     __syncwarp();
     if (q >= n_q) continue;
-    for (int64_t p = indptr[q] + lane; p < indptr[q + 1]; p += 32) {
-      const int32_t k = idx[p];
-      const int h = hot_find(hkeys, hvals, k);
-      if (h >= 0) col[h * kTQ] = val[p];
-      qcold[p] = h >= 0 ? -1 : k;
+    const int64_t b = indptr[q], e = indptr[q + 1];
+    int n = 0;
+    for (int64_t p0 = b; p0 < e; p0 += 32) {
+      const int64_t p = p0 + lane;
+      int32_t k = -1;
+      float v = 0.f;
+      int h = -1;
+      if (p < e) {
+        k = idx[p];
+        v = val[p];
+        h = hot_find(hkeys, hvals, k);
+        if (h >= 0) col[h * kTQ] = v;
+      }
+      const bool cold = p < e && h < 0;
+      const unsigned m = __ballot_sync(0xffffffffu, cold);
+      if (cold) qcold[b + n + __popc(m & lt_mask)] = make_int2(k, __float_as_int(v));
+      n += __popc(m);
     }
+    if (lane == 0) qcold_n[q] = n;
   }
 }
 
 struct TileArgs {
   const int64_t *q_indptr;
-  const int32_t *qcold;
-  const float *q_val;
+  const int2 *qcold;
+  const int32_t *qcold_n;
   int64_t n_q;
   const float *inv_q;
   const float *qhot;
@@ -909,6 +983,25 @@ static_assert(kFOffSlab % 16 == 0 && kFOffQhot % 16 == 0 && kFOffHits % 16 == 0 
                   kFOffInvI % 16 == 0,
               "fast scorer shared sections must stay 16-byte aligned");
 
+// Read-only global loads kept where they are written: the compiler may move
+// plain __ldg loads past barriers to their first use, which would defeat
+// issuing them early so their latency hides behind other work.
+__device__ __forceinline__ int32_t ld_early_s32(const int32_t *p) {
+  int32_t v;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ int64_t ld_early_s64(const int64_t *p) {
+  int64_t v;
+  asm volatile("ld.global.nc.s64 %0, [%1];" : "=l"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ int2 ld_early_s64_as_int2(const int2 *p) {
+  int2 v;
+  asm volatile("ld.global.nc.v2.s32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
 // Copies n bytes (a multiple of 16, both addresses 16-byte aligned).
 __device__ __forceinline__ void cp_bytes(unsigned char *dst, const unsigned char *src, int n) {
   for (int j = threadIdx.x * 16; j < n; j += kFThreads * 16) cp_async16(dst + j, src + j);
@@ -916,15 +1009,35 @@ __device__ __forceinline__ void cp_bytes(unsigned char *dst, const unsigned char
 
 __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
 
-// Looks dimension k up in the item tile's image: one 8-byte load per probe.
-// Returns the segment [start, end) packed as start | end << 16 (0 if absent).
-__device__ __forceinline__ uint32_t image_find(const uint2 *slots, int32_t k) {
-  uint32_t s = hash_a(k, kImgSlotsBits);
-  for (int n = 0; n < kImgSlots; ++n) {
-    const uint2 sl = slots[s];
-    if ((int32_t)sl.x == k) return sl.y;
-    if (sl.x == 0xffffffffu) return 0;
-    s = (s + 1) & (kImgSlots - 1);
+// Looks dimension k up in the item tile's image (linear probing from the
+// home slot).  Reads the aligned group of four slots around the probe point
+// with two 16-byte loads and checks the four at once, so a long probe
+// sequence costs a quarter as many dependent loads.  Returns the segment
+// [start, end) packed as start | end << 16 (0 if absent).
+__device__ __forceinline__ uint32_t image_find(const uint2 *slots, const uint32_t *bits, int32_t k) {
+  // About half of a query row's cold dims are absent from a given item tile;
+  // the tile's membership bitmap turns most of those misses into one load.
+  const uint32_t bb = hash_b(k, kImgBitsLog2);
+  if (!((bits[bb >> 5] >> (bb & 31)) & 1u)) return 0;
+  const uint32_t s = hash_a(k, kImgSlotsBits);
+  uint32_t base = s & ~3u;
+  const int first = (int)(s & 3u);
+  const uint32_t ku = (uint32_t)k, empty = 0xffffffffu;
+  uint32_t valid = 0xfu << first;  // slots of the first group before the home slot do not count
+  for (int n = 0; n < kImgSlots / 4; ++n) {
+    const uint4 a = *reinterpret_cast<const uint4 *>(slots + base);
+    const uint4 b = *reinterpret_cast<const uint4 *>(slots + base + 2);
+    const uint32_t eq = ((a.x == ku) | ((a.z == ku) << 1) | ((b.x == ku) << 2) | ((b.z == ku) << 3)) & valid;
+    const uint32_t em =
+        ((a.x == empty) | ((a.z == empty) << 1) | ((b.x == empty) << 2) | ((b.z == empty) << 3)) & valid;
+    const uint32_t stop = eq | em;
+    if (stop) {
+      const uint32_t j = __ffs(stop) - 1;  // the first slot that is k or empty
+      if (!((eq >> j) & 1u)) return 0;
+      return j == 0 ? a.y : j == 1 ? a.w : j == 2 ? b.y : b.w;
+    }
+    valid = 0xfu;
+    base = (base + 4) & (kImgSlots - 1);
   }
   return 0;
 }
@@ -941,10 +1054,18 @@ __device__ __forceinline__ void hot_product512(float *acc, const float *qhot, co
   for (int r = 0; r < 4; ++r)
 #pragma unroll
     for (int j = 0; j < 4; ++j) c[r][j] = make_float2(0.f, 0.f);
+  // Operands of dim h + 1 are loaded while dim h is multiplied.
+  float4 qa = make_float4(0.f, 0.f, 0.f, 0.f), ia = qa, ic = qa;
+  if (H > 0) {
+    qa = *reinterpret_cast<const float4 *>(qhot + qb);
+    ia = *reinterpret_cast<const float4 *>(slab + ib);
+    ic = *reinterpret_cast<const float4 *>(slab + ib + 4);
+  }
   for (int h = 0; h < H; ++h) {
-    const float4 qa = *reinterpret_cast<const float4 *>(qhot + h * kTQ + qb);
-    const float4 ia = *reinterpret_cast<const float4 *>(slab + h * kTI + ib);
-    const float4 ic = *reinterpret_cast<const float4 *>(slab + h * kTI + ib + 4);
+    const int hn = h + 1 < H ? h + 1 : h;
+    const float4 qn = *reinterpret_cast<const float4 *>(qhot + hn * kTQ + qb);
+    const float4 in = *reinterpret_cast<const float4 *>(slab + hn * kTI + ib);
+    const float4 cn = *reinterpret_cast<const float4 *>(slab + hn * kTI + ib + 4);
     const float qv[4] = {qa.x, qa.y, qa.z, qa.w};
     const float2 i0 = make_float2(ia.x, ia.y), i1 = make_float2(ia.z, ia.w);
     const float2 i2 = make_float2(ic.x, ic.y), i3 = make_float2(ic.z, ic.w);
@@ -956,6 +1077,9 @@ __device__ __forceinline__ void hot_product512(float *acc, const float *qhot, co
       c[r][2] = __ffma2_rn(qq, i2, c[r][2]);
       c[r][3] = __ffma2_rn(qq, i3, c[r][3]);
     }
+    qa = qn;
+    ia = in;
+    ic = cn;
   }
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
@@ -984,6 +1108,7 @@ __global__ void __launch_bounds__(kFThreads, 1) k_score_tiles(const TileArgs a) 
   float *invi = reinterpret_cast<float *>(fsm + kFOffInvI);
   int *nh = reinterpret_cast<int *>(fsm + kFOffNh);
   const uint2 *slots = reinterpret_cast<const uint2 *>(img + kImgOffSlots);
+  const uint32_t *bits = reinterpret_cast<const uint32_t *>(img + kImgOffBits);
   const uint8_t *seg_item = img + kImgOffItem;
   const float *seg_val = reinterpret_cast<const float *>(img + kImgOffVal);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1022,24 +1147,28 @@ __global__ void __launch_bounds__(kFThreads, 1) k_score_tiles(const TileArgs a) 
              H * kTQ * 4);
     cp_async_commit();
     if (tid < kTQ) invq[tid] = tid < nq ? __ldg(a.inv_q + q0 + tid) : 0.f;
-    // This warp's query rows: bounds and their first two 32-entry chunks,
-    // loaded now so that the wait hides behind the hot product.
-    int32_t p[kRowsPerWarp], e[kRowsPerWarp], ch[kRowsPerWarp], pk0[kRowsPerWarp], pk1[kRowsPerWarp];
-    float pv0[kRowsPerWarp], pv1[kRowsPerWarp];
+    // This warp's query rows: their cold ranges [indptr[q], indptr[q] +
+    // cold count) and the first 32 cold entries of each, loaded now so that
+    // the wait hides behind the hot product.
+    int32_t p[kRowsPerWarp], e[kRowsPerWarp], ch[kRowsPerWarp];
+    int2 pk[kRowsPerWarp];
 #pragma unroll
     for (int rr = 0; rr < kRowsPerWarp; ++rr) {
       const int r = warp * kRowsPerWarp + rr;
-      p[rr] = r < nq ? (int32_t)__ldg(a.q_indptr + q0 + r) : 0;
-      e[rr] = r < nq ? (int32_t)__ldg(a.q_indptr + q0 + r + 1) : 0;
+      const int rc = r < nq ? r : 0;  // rows past n_q read row 0's range, then drop it
+      p[rr] = (int32_t)ld_early_s64(a.q_indptr + q0 + rc);
+      e[rr] = p[rr] + ld_early_s32(a.qcold_n + q0 + rc);
+      if (r >= nq) p[rr] = e[rr] = 0;
       ch[rr] = 0;
     }
 #pragma unroll
     for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-      const int32_t p0 = p[rr] + lane, p1 = p0 + 32;
-      pk0[rr] = p0 < e[rr] ? __ldg(a.qcold + p0) : -1;
-      pv0[rr] = p0 < e[rr] ? __ldg(a.q_val + p0) : 0.f;
-      pk1[rr] = p1 < e[rr] ? __ldg(a.qcold + p1) : -1;
-      pv1[rr] = p1 < e[rr] ? __ldg(a.q_val + p1) : 0.f;
+      const int32_t p0 = p[rr] + lane;
+      pk[rr] = make_int2(-1, 0);
+      if (p[rr] < e[rr]) {  // warp-uniform; the load is clamped inside the range, masked after
+        const int2 x = ld_early_s64_as_int2(a.qcold + (p0 < e[rr] ? p0 : e[rr] - 1));
+        if (p0 < e[rr]) pk[rr] = x;
+      }
     }
     cp_async_wait_all();
     __syncthreads();
@@ -1067,19 +1196,12 @@ __global__ void __launch_bounds__(kFThreads, 1) k_score_tiles(const TileArgs a) 
         int n = 0;
         while (p[rr] < e[rr]) {
           const int32_t pp = p[rr] + lane;
-          int32_t k;
-          float v;
-          if (ch[rr] == 0) {
-            k = pk0[rr];
-            v = pv0[rr];
-          } else if (ch[rr] == 1) {
-            k = pk1[rr];
-            v = pv1[rr];
-          } else {
-            k = pp < e[rr] ? __ldg(a.qcold + pp) : -1;
-            v = pp < e[rr] ? __ldg(a.q_val + pp) : 0.f;
-          }
-          const uint32_t se = k >= 0 ? image_find(slots, k) : 0u;
+          int2 x = make_int2(-1, 0);
+          if (ch[rr] == 0) x = pk[rr];
+          else if (pp < e[rr]) x = __ldg(a.qcold + pp);
+          const int32_t k = x.x;
+          const float v = __int_as_float(x.y);
+          const uint32_t se = k >= 0 ? image_find(slots, bits, k) : 0u;
           const bool hit = (se >> 16) > (se & 0xffffu);
           const unsigned mask = __ballot_sync(0xffffffffu, hit);
           const int c = __popc(mask);
@@ -1100,7 +1222,7 @@ __global__ void __launch_bounds__(kFThreads, 1) k_score_tiles(const TileArgs a) 
             unsigned m = mask;
             for (int j = 1; j < room; ++j) m &= m - 1u;  // drop the lowest room-1 hits
             p[rr] = pp - lane + __ffs(m);                 // one past the room-th hit's lane
-            ch[rr] = 2;  // later chunks no longer line up with the prefetched ones
+            ch[rr] = 1;  // later chunks no longer line up with the prefetched one
             n += room;
           }
           break;
@@ -1218,7 +1340,7 @@ cudaError_t launch_build_hybrid(ss_handle *h, const ss_csr &items, int64_t row_b
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  k_build_tiles<<<n_tiles, kThreads, kBuildSmem, s>>>(
+  k_build_tiles<<<n_tiles, kBThreads, kBuildSmem, s>>>(
       items.indptr, items.indices, items.values, row_begin, row_end, h->hot, h->slab, h->ell,
       h->meta, h->heavy_k, h->heavy_v, h->heavy_item, h->counters, h->heavy_cap, h->image,
       h->d_status);
@@ -1253,7 +1375,8 @@ static cudaError_t prepare_queries(ss_handle *h, const ss_csr &q, cudaStream_t s
   const int64_t n_qtiles = (q.n_rows + kTQ - 1) / kTQ;
   const int64_t need_hot = std::max<int64_t>(1, n_qtiles * kHotMax * kTQ);
   const int64_t need_cold = std::max<int64_t>(1, q.nnz);
-  if (need_hot > h->qhot_cap || need_cold > h->qcold_cap) {
+  const int64_t need_n = std::max<int64_t>(1, q.n_rows);
+  if (need_hot > h->qhot_cap || need_cold > h->qcold_cap || need_n > h->qcold_n_cap) {
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return e;
     if (need_hot > h->qhot_cap) {
@@ -1268,16 +1391,24 @@ static cudaError_t prepare_queries(ss_handle *h, const ss_csr &q, cudaStream_t s
       cudaFree(h->qcold);
       h->qcold = nullptr;
       h->qcold_cap = 0;
-      e = cudaMalloc(&h->qcold, sizeof(int32_t) * (size_t)need_cold);
+      e = cudaMalloc(&h->qcold, sizeof(int2) * (size_t)need_cold);
       if (e != cudaSuccess) return e;
       h->qcold_cap = need_cold;
+    }
+    if (need_n > h->qcold_n_cap) {
+      cudaFree(h->qcold_n);
+      h->qcold_n = nullptr;
+      h->qcold_n_cap = 0;
+      e = cudaMalloc(&h->qcold_n, sizeof(int32_t) * (size_t)need_n);
+      if (e != cudaSuccess) return e;
+      h->qcold_n_cap = need_n;
     }
   }
   const int64_t rows_padded = n_qtiles * kTQ;
   const int64_t blocks_needed = (rows_padded + kThreads / 32 - 1) / (kThreads / 32);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(blocks_needed, (int64_t)h->sm_count * 8));
   k_prep_queries<<<grid, kThreads, 0, s>>>(q.indptr, q.indices, q.values, q.n_rows, rows_padded,
-                                           h->hot, h->qhot, h->qcold);
+                                           h->hot, h->qhot, h->qcold, h->qcold_n);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   *queued = 1;
@@ -1314,7 +1445,7 @@ cudaError_t launch_score_hybrid(ss_handle *h, const ss_csr &queries, const float
   TileArgs f;
   f.q_indptr = queries.indptr;
   f.qcold = h->qcold;
-  f.q_val = queries.values;
+  f.qcold_n = h->qcold_n;
   f.n_q = queries.n_rows;
   f.inv_q = inv_q;
   f.qhot = h->qhot;

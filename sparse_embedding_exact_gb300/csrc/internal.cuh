@@ -47,7 +47,9 @@ constexpr int kImgSlots = 1 << kImgSlotsBits;      // {dim or -1, start | end <<
 constexpr int kImgDCap = 6144;                     // distinct cold dims per tile (load <= 3/4)
 constexpr int kImgECap = 10240;                    // cold nonzeros per tile
 constexpr int kImgOffSlots = 16;                   // after the header {D, E, fits, 0}
-constexpr int kImgOffItem = kImgOffSlots + kImgSlots * 8;       // u8 item[E]
+constexpr int kImgBitsLog2 = 15;                   // membership bitmap of the tile's cold dims
+constexpr int kImgOffBits = kImgOffSlots + kImgSlots * 8;       // u32 bits[2^15 / 32]
+constexpr int kImgOffItem = kImgOffBits + (1 << kImgBitsLog2) / 8;  // u8 item[E]
 constexpr int kImgOffVal = kImgOffItem + kImgECap;              // float value[E]
 constexpr int kImgBytes = kImgOffVal + kImgECap * 4;
 static_assert(kImgOffItem % 16 == 0 && kImgOffVal % 16 == 0 && kImgBytes % 16 == 0,
@@ -116,10 +118,12 @@ struct ss_handle {
   int32_t max_tiles = 0;
   unsigned char *image = nullptr; // [max tiles][kImgBytes]
   // Queries prepared for the current hot set: hot values per query tile
-  // ([tile][kHotMax][kTQ]) and the indices with hot dims replaced by -1.
+  // ([tile][kHotMax][kTQ]); each row's cold nonzeros as {dim, value bits},
+  // moved to the front of the row's own range; and each row's cold count.
   float *qhot = nullptr;
-  int32_t *qcold = nullptr;
-  int64_t qhot_cap = 0, qcold_cap = 0;
+  int2 *qcold = nullptr;
+  int32_t *qcold_n = nullptr;
+  int64_t qhot_cap = 0, qcold_cap = 0, qcold_n_cap = 0;
   // The hot set is chosen once per item matrix: the matrix it was chosen for,
   // and a counter that changes whenever it is chosen again.
   const void *hot_src[3] = {nullptr, nullptr, nullptr};
