@@ -173,8 +173,11 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *red, int *total)
 }
 
 // Open-addressing insert / find in the image-building hash (kImgSlots).
+// Probing starts at the first slot of the key's aligned group of four, so a
+// reader that loads whole groups finds most keys in the first one.
+__device__ __forceinline__ uint32_t img_home(int32_t k) { return hash_a(k, kImgSlotsBits) & ~3u; }
 __device__ __forceinline__ int img_insert(int *keys, int32_t k) {
-  uint32_t s = hash_a(k, kImgSlotsBits);
+  uint32_t s = img_home(k);
   for (int n = 0; n < kImgSlots; ++n) {
     const int prev = atomicCAS(&keys[s], -1, k);
     if (prev == -1 || prev == k) return (int)s;
@@ -183,7 +186,7 @@ __device__ __forceinline__ int img_insert(int *keys, int32_t k) {
   return -1;
 }
 __device__ __forceinline__ int img_find(const int *keys, int32_t k) {
-  uint32_t s = hash_a(k, kImgSlotsBits);
+  uint32_t s = img_home(k);
   for (int n = 0; n < kImgSlots; ++n) {
     const int key = keys[s];
     if (key == k) return (int)s;
@@ -894,11 +897,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_hybrid(const HybridArgs a
 }
 
 // ---------------------------------------------------------------- fast path
-// One warp per query row: the row's hot values into its column of the query
-// tile's hot block ([tile][kHotMax][kTQ], zero where absent), and the row's
-// cold nonzeros as {dim, value bits}, in their original (ascending) order,
-// moved to the front of the row's own range, with their count.  Rows past
-// n_q in the last tile get a zero column.
+// One warp per group of kQGroup query rows.  Each row's hot values go into
+// its column of the query tile's hot block ([tile][kHotMax][kTQ], zero where
+// absent).  The group's cold nonzeros, as {dim, value bits}, are packed row
+// after row (each row's in its original, ascending order) from the group's
+// first CSR position, so a group's cold list is contiguous; each row's cold
+// count is kept.  Rows past n_q in the last tile get a zero column.
 __global__ void __launch_bounds__(kThreads)
     k_prep_queries(const int64_t *__restrict__ indptr, const int32_t *__restrict__ idx,
                    const float *__restrict__ val, int64_t n_q, int64_t n_rows_padded,
@@ -913,32 +917,41 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   if ((int)threadIdx.x < H) hot_insert(hkeys, hvals, hot[1 + threadIdx.x], threadIdx.x);
   __syncthreads();
+  // One warp per group of kQGroup rows; the group's cold entries are packed
+  // row after row from the group's first CSR position.
   const int64_t warps = (int64_t)gridDim.x * (kThreads / 32);
-  for (int64_t q = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); q < n_rows_padded;
-       q += warps) {
-    float *col = qhot + (q / kTQ) * kHotMax * kTQ + (q % kTQ);
-    for (int h = lane; h < kHotMax; h += 32) col[h * kTQ] = 0.f;
-    __syncwarp();
-    if (q >= n_q) continue;
-    const int64_t b = indptr[q], e = indptr[q + 1];
+  for (int64_t j = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+       j < n_rows_padded / kQGroup; j += warps) {
+    const int64_t q_first = j * kQGroup;
+    const int64_t base = indptr[q_first < n_q ? q_first : n_q];
     int n = 0;
-    for (int64_t p0 = b; p0 < e; p0 += 32) {
-      const int64_t p = p0 + lane;
-      int32_t k = -1;
-      float v = 0.f;
-      int h = -1;
-      if (p < e) {
-        k = idx[p];
-        v = val[p];
-        h = hot_find(hkeys, hvals, k);
-        if (h >= 0) col[h * kTQ] = v;
+    for (int r = 0; r < kQGroup; ++r) {
+      const int64_t q = q_first + r;
+      float *col = qhot + (q / kTQ) * kHotMax * kTQ + (q % kTQ);
+      for (int h = lane; h < kHotMax; h += 32) col[h * kTQ] = 0.f;
+      __syncwarp();
+      if (q >= n_q) continue;
+      const int64_t b = indptr[q], e = indptr[q + 1];
+      int n_row = 0;
+      for (int64_t p0 = b; p0 < e; p0 += 32) {
+        const int64_t p = p0 + lane;
+        int32_t k = -1;
+        float v = 0.f;
+        int h = -1;
+        if (p < e) {
+          k = idx[p];
+          v = val[p];
+          h = hot_find(hkeys, hvals, k);
+          if (h >= 0) col[h * kTQ] = v;
+        }
+        const bool cold = p < e && h < 0;
+        const unsigned m = __ballot_sync(0xffffffffu, cold);
+        if (cold) qcold[base + n + __popc(m & lt_mask)] = make_int2(k, __float_as_int(v));
+        n += __popc(m);
+        n_row += __popc(m);
       }
-      const bool cold = p < e && h < 0;
-      const unsigned m = __ballot_sync(0xffffffffu, cold);
-      if (cold) qcold[b + n + __popc(m & lt_mask)] = make_int2(k, __float_as_int(v));
-      n += __popc(m);
+      if (lane == 0) qcold_n[q] = n_row;
     }
-    if (lane == 0) qcold_n[q] = n;
   }
 }
 
@@ -947,6 +960,7 @@ struct TileArgs {
   const int2 *qcold;
   const int32_t *qcold_n;
   int64_t n_q;
+  int64_t q_nnz;  // qcold entries: indptr[n_q]
   const float *inv_q;
   const float *qhot;
   const int32_t *hot;
@@ -964,31 +978,38 @@ struct TileArgs {
   int32_t *status;
 };
 
-constexpr int kFThreads = 512;  // fast scorer: 16 warps, 4 query rows each
-constexpr int kRowsPerWarp = kTQ / (kFThreads / 32);
-constexpr int kGroup = 32 / kRowsPerWarp;  // lanes walking one row's segments
-constexpr int kHitCap = 24;  // hits of one query row walked per round
-constexpr int kMaxRounds = 1 << 20;  // far above any row's entry count
-constexpr int kFOffAcc = 0;
-constexpr int kFOffImg = kFOffAcc + kTQ * kTI * 4;
-constexpr int kFOffSlab = kFOffImg + kImgBytes;
-constexpr int kFOffQhot = kFOffSlab + kHotMax * kTI * 4;
-constexpr int kFOffHits = kFOffQhot + kHotMax * kTQ * 4;
-constexpr int kFOffInvQ = kFOffHits + kTQ * kHitCap * 8;
-constexpr int kFOffInvI = kFOffInvQ + kTQ * 4;
-constexpr int kFOffNh = kFOffInvI + kTI * 4;
-constexpr int kFastSmem = kFOffNh + kTQ * 4;
+constexpr int kFThreads = 512;                   // fast scorer: 16 warps
+constexpr int kFWarps = kFThreads / 32;
+constexpr int kGroup = 32 / kQGroup;             // lanes walking one row's segments
+constexpr int kHitCap = 112;                     // hits of one row group held per round
+constexpr int kPasses = 4;                       // lookup passes of 32 entries in flight
+constexpr int kMaxRounds = 1 << 20;              // far above any group's entry count
+constexpr int kGroupsPerQTile = kTQ / kQGroup;
+constexpr int kFOffAcc = 0;                                          // [warp][kQGroup][kTI] f32
+constexpr int kFOffImg = kFOffAcc + kFWarps * kQGroup * kTI * 4;
+constexpr int kFOffSlab = kFOffImg + kImgBytes;                      // [kHotMax][kTI] f32
+constexpr int kFOffQh = kFOffSlab + kHotMax * kTI * 4;               // [warp][kHotMax][kQGroup] f32
+constexpr int kFOffHits = kFOffQh + kFWarps * kHotMax * kQGroup * 4; // [warp][kHitCap] {segment, value}
+constexpr int kFOffCtl = kFOffHits + kFWarps * kHitCap * 8;          // next row group of the tile
+constexpr int kFastSmem = kFOffCtl + 16;
 static_assert(kFastSmem <= 232448, "fast scoring block exceeds 227 KB of shared memory");
-static_assert(kFOffSlab % 16 == 0 && kFOffQhot % 16 == 0 && kFOffHits % 16 == 0 &&
-                  kFOffInvI % 16 == 0,
+static_assert(kFOffImg % 16 == 0 && kFOffSlab % 16 == 0 && kFOffQh % 16 == 0 &&
+                  kFOffHits % 16 == 0 && kFOffCtl % 16 == 0,
               "fast scorer shared sections must stay 16-byte aligned");
+static_assert(kQGroup == 4 && kTI == 256 && kGroup == 8,
+              "the fast scorer's lane mapping assumes 4 rows x 256 items per warp");
 
 // Read-only global loads kept where they are written: the compiler may move
-// plain __ldg loads past barriers to their first use, which would defeat
-// issuing them early so their latency hides behind other work.
+// plain __ldg loads past other work to their first use, which would defeat
+// issuing them early so their latency hides behind that work.
 __device__ __forceinline__ int32_t ld_early_s32(const int32_t *p) {
   int32_t v;
   asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_early_f32(const float *p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
   return v;
 }
 __device__ __forceinline__ int64_t ld_early_s64(const int64_t *p) {
@@ -1001,6 +1022,13 @@ __device__ __forceinline__ int2 ld_early_s64_as_int2(const int2 *p) {
   asm volatile("ld.global.nc.v2.s32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
   return v;
 }
+__device__ __forceinline__ float4 ld_early_f4(const float *p) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
 
 // Copies n bytes (a multiple of 16, both addresses 16-byte aligned).
 __device__ __forceinline__ void cp_bytes(unsigned char *dst, const unsigned char *src, int n) {
@@ -1009,281 +1037,342 @@ __device__ __forceinline__ void cp_bytes(unsigned char *dst, const unsigned char
 
 __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
 
-// Looks dimension k up in the item tile's image (linear probing from the
-// home slot).  Reads the aligned group of four slots around the probe point
-// with two 16-byte loads and checks the four at once, so a long probe
-// sequence costs a quarter as many dependent loads.  Returns the segment
-// [start, end) packed as start | end << 16 (0 if absent).
-__device__ __forceinline__ uint32_t image_find(const uint2 *slots, const uint32_t *bits, int32_t k) {
-  // About half of a query row's cold dims are absent from a given item tile;
-  // the tile's membership bitmap turns most of those misses into one load.
-  const uint32_t bb = hash_b(k, kImgBitsLog2);
-  if (!((bits[bb >> 5] >> (bb & 31)) & 1u)) return 0;
-  const uint32_t s = hash_a(k, kImgSlotsBits);
-  uint32_t base = s & ~3u;
-  const int first = (int)(s & 3u);
+// Lanes [0, x) of a warp (x clamped to [0, 32]).
+__device__ __forceinline__ unsigned lanes_below(int x) {
+  return x <= 0 ? 0u : x >= 32 ? 0xffffffffu : (1u << x) - 1u;
+}
+
+// The rest of a lookup whose home group of four slots held neither the key
+// nor an empty slot: linear probing over the following groups.
+__device__ __forceinline__ uint32_t image_find_rest(const uint2 *slots, int32_t k, uint32_t base) {
   const uint32_t ku = (uint32_t)k, empty = 0xffffffffu;
-  uint32_t valid = 0xfu << first;  // slots of the first group before the home slot do not count
-  for (int n = 0; n < kImgSlots / 4; ++n) {
+  for (int n = 1; n < kImgSlots / 4; ++n) {
+    base = (base + 4) & (kImgSlots - 1);
     const uint4 a = *reinterpret_cast<const uint4 *>(slots + base);
     const uint4 b = *reinterpret_cast<const uint4 *>(slots + base + 2);
-    const uint32_t eq = ((a.x == ku) | ((a.z == ku) << 1) | ((b.x == ku) << 2) | ((b.z == ku) << 3)) & valid;
-    const uint32_t em =
-        ((a.x == empty) | ((a.z == empty) << 1) | ((b.x == empty) << 2) | ((b.z == empty) << 3)) & valid;
-    const uint32_t stop = eq | em;
-    if (stop) {
-      const uint32_t j = __ffs(stop) - 1;  // the first slot that is k or empty
-      if (!((eq >> j) & 1u)) return 0;
-      return j == 0 ? a.y : j == 1 ? a.w : j == 2 ? b.y : b.w;
-    }
-    valid = 0xfu;
-    base = (base + 4) & (kImgSlots - 1);
+    if (a.x == ku) return a.y;
+    if (a.z == ku) return a.w;
+    if (b.x == ku) return b.y;
+    if (b.z == ku) return b.w;
+    if (a.x == empty || a.z == empty || b.x == empty || b.z == empty) return 0;
   }
   return 0;
 }
 
-// Dense product over the hot dims for 512 threads: thread (lq, li) of warp
-// (wq, wi) owns queries wq*16 + lq*4 + [0, 4) and items wi*64 + li*8 + [0, 8).
-__device__ __forceinline__ void hot_product512(float *acc, const float *qhot, const float *slab,
-                                               int H) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int qb = (warp & 3) * 16 + (lane >> 3) * 4;
-  const int ib = (warp >> 2) * 64 + (lane & 7) * 8;
-  float2 c[4][4];
+// Looks up kPasses dimensions per lane (k < 0: none) in the item tile's
+// image and returns each one's segment [start, end) packed as start |
+// end << 16 (0 if absent).  About half of a query row's cold dimensions are
+// absent from a given tile; the membership bitmap turns most of those misses
+// into one load.  The others read their home group of four slots (every key
+// between the home slot and a key's own slot is occupied, so a key missing
+// from a group that holds an empty slot is absent).  All passes' loads are
+// issued before any result is used.
+__device__ __forceinline__ void image_lookups(const uint2 *slots, const uint32_t *bits,
+                                              const int2 (&x)[kPasses], uint32_t (&se)[kPasses]) {
+  bool cand[kPasses];
 #pragma unroll
-  for (int r = 0; r < 4; ++r)
+  for (int p = 0; p < kPasses; ++p) {
+    const uint32_t bb = hash_b(x[p].x, kImgBitsLog2);
+    cand[p] = x[p].x >= 0 && ((bits[bb >> 5] >> (bb & 31)) & 1u);
+  }
+  uint4 ga[kPasses], gb[kPasses];
+#pragma unroll
+  for (int p = 0; p < kPasses; ++p) {
+    ga[p] = make_uint4(0u, 0u, 0u, 0u);
+    gb[p] = ga[p];
+    if (cand[p]) {
+      const uint32_t base = img_home(x[p].x);
+      ga[p] = *reinterpret_cast<const uint4 *>(slots + base);
+      gb[p] = *reinterpret_cast<const uint4 *>(slots + base + 2);
+    }
+  }
+  const uint32_t empty = 0xffffffffu;
+#pragma unroll
+  for (int p = 0; p < kPasses; ++p) {
+    const uint32_t ku = (uint32_t)x[p].x;
+    const uint4 a = ga[p], b = gb[p];
+    se[p] = 0u;
+    if (cand[p]) {
+      if (a.x == ku) se[p] = a.y;
+      else if (a.z == ku) se[p] = a.w;
+      else if (b.x == ku) se[p] = b.y;
+      else if (b.z == ku) se[p] = b.w;
+      else if (a.x != empty && a.z != empty && b.x != empty && b.z != empty)
+        se[p] = image_find_rest(slots, x[p].x, img_home(x[p].x));
+    }
+  }
+}
+
+// Dense product over the hot dims for one warp's row group: lane l owns
+// items 4l + [0, 4) and 128 + 4l + [0, 4) of all kQGroup rows.  Operands of
+// dim h + 1 are loaded while dim h is multiplied.  Writes the group's
+// accumulator rows (zeros when there are no hot dims).
+__device__ __forceinline__ void hot_product_group(float *acc, const float *qh, const float *slab,
+                                                  int H, int lane) {
+  const int ia = 4 * lane, ib = 128 + 4 * lane;
+  float2 c[kQGroup][4];
+#pragma unroll
+  for (int r = 0; r < kQGroup; ++r)
 #pragma unroll
     for (int j = 0; j < 4; ++j) c[r][j] = make_float2(0.f, 0.f);
-  // Operands of dim h + 1 are loaded while dim h is multiplied.
-  float4 qa = make_float4(0.f, 0.f, 0.f, 0.f), ia = qa, ic = qa;
+  float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f), sa = q4, sb = q4;
   if (H > 0) {
-    qa = *reinterpret_cast<const float4 *>(qhot + qb);
-    ia = *reinterpret_cast<const float4 *>(slab + ib);
-    ic = *reinterpret_cast<const float4 *>(slab + ib + 4);
+    q4 = *reinterpret_cast<const float4 *>(qh);
+    sa = *reinterpret_cast<const float4 *>(slab + ia);
+    sb = *reinterpret_cast<const float4 *>(slab + ib);
   }
   for (int h = 0; h < H; ++h) {
     const int hn = h + 1 < H ? h + 1 : h;
-    const float4 qn = *reinterpret_cast<const float4 *>(qhot + hn * kTQ + qb);
-    const float4 in = *reinterpret_cast<const float4 *>(slab + hn * kTI + ib);
-    const float4 cn = *reinterpret_cast<const float4 *>(slab + hn * kTI + ib + 4);
-    const float qv[4] = {qa.x, qa.y, qa.z, qa.w};
-    const float2 i0 = make_float2(ia.x, ia.y), i1 = make_float2(ia.z, ia.w);
-    const float2 i2 = make_float2(ic.x, ic.y), i3 = make_float2(ic.z, ic.w);
+    const float4 qn = *reinterpret_cast<const float4 *>(qh + hn * kQGroup);
+    const float4 an = *reinterpret_cast<const float4 *>(slab + hn * kTI + ia);
+    const float4 bn = *reinterpret_cast<const float4 *>(slab + hn * kTI + ib);
+    const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+    const float2 i0 = make_float2(sa.x, sa.y), i1 = make_float2(sa.z, sa.w);
+    const float2 i2 = make_float2(sb.x, sb.y), i3 = make_float2(sb.z, sb.w);
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < kQGroup; ++r) {
       const float2 qq = make_float2(qv[r], qv[r]);
       c[r][0] = __ffma2_rn(qq, i0, c[r][0]);
       c[r][1] = __ffma2_rn(qq, i1, c[r][1]);
       c[r][2] = __ffma2_rn(qq, i2, c[r][2]);
       c[r][3] = __ffma2_rn(qq, i3, c[r][3]);
     }
-    qa = qn;
-    ia = in;
-    ic = cn;
+    q4 = qn;
+    sa = an;
+    sb = bn;
   }
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    float4 *d = reinterpret_cast<float4 *>(acc + (qb + r) * kTI + ib);
-    d[0] = make_float4(c[r][0].x, c[r][0].y, c[r][1].x, c[r][1].y);
-    d[1] = make_float4(c[r][2].x, c[r][2].y, c[r][3].x, c[r][3].y);
+  for (int r = 0; r < kQGroup; ++r) {
+    *reinterpret_cast<float4 *>(acc + r * kTI + ia) =
+        make_float4(c[r][0].x, c[r][0].y, c[r][1].x, c[r][1].y);
+    *reinterpret_cast<float4 *>(acc + r * kTI + ib) =
+        make_float4(c[r][2].x, c[r][2].y, c[r][3].x, c[r][3].y);
   }
 }
 
-// The persistent fast scorer for item tiles that have an image.  Units are
-// (item tile, query tile) pairs, item-tile major, so a block loads an item
-// tile's image and slab once and runs every query tile of its range on it.
-// Per unit: the hot product writes acc; then warp w takes query rows
-// 4w..4w+3, looks up each row's cold nonzeros in the image, and walks the
-// hit segments with one 8-lane group per row (a group only touches its own
-// row, and within one segment every item is distinct, so no accumulator is
-// shared); then the normalised tile is stored.
+// Adds q * value over one image segment into a row's accumulator: the lanes
+// of a group take every kGroup-th entry, two entries per step (the items of
+// one segment are distinct, so the read-modify-writes are independent).
+__device__ __forceinline__ void walk_segment(float *arow, const uint8_t *seg_item,
+                                             const float *seg_val, uint2 hh, int li) {
+  const float qv = __uint_as_float(hh.y);
+  const int end = (int)(hh.x >> 16);
+  int j = (int)(hh.x & 0xffffu) + li;
+  for (; j + kGroup < end; j += 2 * kGroup) {
+    float *d0 = arow + seg_item[j];
+    float *d1 = arow + seg_item[j + kGroup];
+    const float v0 = seg_val[j], v1 = seg_val[j + kGroup];
+    const float a0 = *d0, a1 = *d1;
+    *d0 = fmaf(qv, v0, a0);
+    *d1 = fmaf(qv, v1, a1);
+  }
+  if (j < end) {
+    float *d = arow + seg_item[j];
+    *d = fmaf(qv, seg_val[j], *d);
+  }
+}
+
+// The persistent fast scorer for item tiles that have an image.  A block's
+// range of (item tile, query tile) units is item-tile major: for each item
+// tile in it, the block loads the tile's image, hot slab and item norms
+// once, then its warps take groups of kQGroup query rows from a shared
+// counter.  A warp scores its group against the tile on its own, with no
+// block barrier: the hot product writes the group's accumulator rows; the
+// group's cold nonzeros (contiguous, row after row) are looked up in the
+// image 32 x kPasses at a time and the hits kept in order; one lane group
+// per row walks that row's hit segments (a group only touches its own row,
+// so no accumulator is shared, and each row's cold terms are added in
+// ascending dimension order); then the normalised rows are stored.
 __global__ void __launch_bounds__(kFThreads, 1) k_score_tiles(const TileArgs a) {
   extern __shared__ __align__(16) unsigned char fsm[];
-  float *acc = reinterpret_cast<float *>(fsm + kFOffAcc);
   unsigned char *img = fsm + kFOffImg;
   float *slab = reinterpret_cast<float *>(fsm + kFOffSlab);
-  float *qhot = reinterpret_cast<float *>(fsm + kFOffQhot);
-  uint2 *hits = reinterpret_cast<uint2 *>(fsm + kFOffHits);
-  float *invq = reinterpret_cast<float *>(fsm + kFOffInvQ);
-  float *invi = reinterpret_cast<float *>(fsm + kFOffInvI);
-  int *nh = reinterpret_cast<int *>(fsm + kFOffNh);
+  int *next_group = reinterpret_cast<int *>(fsm + kFOffCtl);
   const uint2 *slots = reinterpret_cast<const uint2 *>(img + kImgOffSlots);
   const uint32_t *bits = reinterpret_cast<const uint32_t *>(img + kImgOffBits);
   const uint8_t *seg_item = img + kImgOffItem;
   const float *seg_val = reinterpret_cast<const float *>(img + kImgOffVal);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float *acc = reinterpret_cast<float *>(fsm + kFOffAcc) + warp * kQGroup * kTI;
+  float *qh = reinterpret_cast<float *>(fsm + kFOffQh) + warp * kHotMax * kQGroup;
+  uint2 *hits = reinterpret_cast<uint2 *>(fsm + kFOffHits) + warp * kHitCap;
+  const int grp = lane / kGroup, li = lane % kGroup;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const int ia = 4 * lane, ib = 128 + 4 * lane;
   const int H = a.hot[0];
+  const int64_t n_groups = (a.n_q + kQGroup - 1) / kQGroup;
 
   const int64_t u0 = (int64_t)blockIdx.x * a.n_units / gridDim.x;
   const int64_t u1 = (int64_t)(blockIdx.x + 1) * a.n_units / gridDim.x;
-  int cur_t = -1;
-  bool tile_ok = false;
-  for (int64_t u = u0; u < u1; ++u) {
+  for (int64_t u = u0; u < u1;) {
     const int t = (int)(u / a.n_qtiles);
-    const int64_t g = u % a.n_qtiles;
-    if (t != cur_t) {
-      cur_t = t;
-      tile_ok = a.meta[(size_t)t * kMetaInts + kMetaFits] != 0;
-      if (tile_ok) {
-        const unsigned char *src = a.image + (size_t)t * kImgBytes;
-        const int32_t E = reinterpret_cast<const int32_t *>(src)[1];
-        cp_bytes(img, src, kImgOffItem);  // header + slots
-        cp_bytes(img + kImgOffItem, src + kImgOffItem, round16(E));
-        cp_bytes(img + kImgOffVal, src + kImgOffVal, round16(4 * E));
-        cp_bytes(reinterpret_cast<unsigned char *>(slab),
-                 reinterpret_cast<const unsigned char *>(a.slab + (size_t)t * kHotMax * kTI),
-                 H * kTI * 4);
-        if (tid < kTI) {
-          const int i = t * kTI + tid;
-          invi[tid] = i < a.n_items ? __ldg(a.inv_i + i) : 0.f;
-        }
-      }
+    const int64_t g_lo = u % a.n_qtiles;
+    const int64_t u_end = u1 < (int64_t)(t + 1) * a.n_qtiles ? u1 : (int64_t)(t + 1) * a.n_qtiles;
+    const int64_t g_hi = g_lo + (u_end - u);
+    u = u_end;
+    if (a.meta[(size_t)t * kMetaInts + kMetaFits] == 0) continue;  // same for the whole block
+    __syncthreads();  // every warp is done with the previous tile
+    {
+      const unsigned char *src = a.image + (size_t)t * kImgBytes;
+      const int32_t E = reinterpret_cast<const int32_t *>(src)[1];
+      cp_bytes(img, src, kImgOffItem);  // header, slots, bitmap
+      cp_bytes(img + kImgOffItem, src + kImgOffItem, round16(E));
+      cp_bytes(img + kImgOffVal, src + kImgOffVal, round16(4 * E));
+      cp_bytes(reinterpret_cast<unsigned char *>(slab),
+               reinterpret_cast<const unsigned char *>(a.slab + (size_t)t * kHotMax * kTI),
+               H * kTI * 4);
+      cp_async_commit();
+      if (tid == 0) *next_group = 0;
     }
-    if (!tile_ok) continue;
-    const int64_t q0 = g * kTQ;
-    const int nq = (int)(a.n_q - q0 < kTQ ? a.n_q - q0 : kTQ);
-    cp_bytes(reinterpret_cast<unsigned char *>(qhot),
-             reinterpret_cast<const unsigned char *>(a.qhot + (size_t)g * kHotMax * kTQ),
-             H * kTQ * 4);
-    cp_async_commit();
-    if (tid < kTQ) invq[tid] = tid < nq ? __ldg(a.inv_q + q0 + tid) : 0.f;
-    // This warp's query rows: their cold ranges [indptr[q], indptr[q] +
-    // cold count) and the first 32 cold entries of each, loaded now so that
-    // the wait hides behind the hot product.
-    int32_t p[kRowsPerWarp], e[kRowsPerWarp], ch[kRowsPerWarp];
-    int2 pk[kRowsPerWarp];
+    const int i0 = t * kTI;
+    const int ni = a.n_items - i0 < kTI ? a.n_items - i0 : kTI;
+    float na[4], nb[4];  // inverse norms of this lane's items (0 past the chunk)
 #pragma unroll
-    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-      const int r = warp * kRowsPerWarp + rr;
-      const int rc = r < nq ? r : 0;  // rows past n_q read row 0's range, then drop it
-      p[rr] = (int32_t)ld_early_s64(a.q_indptr + q0 + rc);
-      e[rr] = p[rr] + ld_early_s32(a.qcold_n + q0 + rc);
-      if (r >= nq) p[rr] = e[rr] = 0;
-      ch[rr] = 0;
-    }
-#pragma unroll
-    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-      const int32_t p0 = p[rr] + lane;
-      pk[rr] = make_int2(-1, 0);
-      if (p[rr] < e[rr]) {  // warp-uniform; the load is clamped inside the range, masked after
-        const int2 x = ld_early_s64_as_int2(a.qcold + (p0 < e[rr] ? p0 : e[rr] - 1));
-        if (p0 < e[rr]) pk[rr] = x;
-      }
+    for (int c = 0; c < 4; ++c) {
+      na[c] = ia + c < ni ? __ldg(a.inv_i + i0 + ia + c) : 0.f;
+      nb[c] = ib + c < ni ? __ldg(a.inv_i + i0 + ib + c) : 0.f;
     }
     cp_async_wait_all();
     __syncthreads();
-    // 1. hot dims
-    if (H > 0) {
-      hot_product512(acc, qhot, slab, H);
-    } else {
-      float4 *acc4 = reinterpret_cast<float4 *>(acc);
-      for (int j = tid; j < kTQ * kTI / 4; j += kFThreads) acc4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    __syncthreads();
-    // 2. cold dims: lookups row by row, then one lane group per row walks.
-    // Every round consumes at least one entry of some row; the round count is
-    // bounded anyway, and running out of rounds raises the status flag.
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int round = 0;; ++round) {
-      if (round == kMaxRounds) {
-        if (lane == 0) flag(a.status, DEV_STALL);
-        break;
+
+    const int64_t j_lo = g_lo * kGroupsPerQTile;
+    const int64_t j_hi =
+        g_hi * kGroupsPerQTile < n_groups ? g_hi * kGroupsPerQTile : n_groups;
+    for (;;) {
+      int jj = 0;
+      if (lane == 0) jj = atomicAdd(next_group, 1);
+      jj = __shfl_sync(0xffffffffu, jj, 0);
+      const int64_t j = j_lo + jj;
+      if (j >= j_hi) break;
+      const int64_t q_first = j * kQGroup;
+      const int nr = a.n_q - q_first < kQGroup ? (int)(a.n_q - q_first) : kQGroup;
+
+      // Group metadata, hot values and the first cold entries, issued before
+      // the hot product so their latency hides behind it.
+      int cn = 0;
+      float iq = 0.f;
+      if (lane < nr) {
+        cn = ld_early_s32(a.qcold_n + q_first + lane);
+        iq = ld_early_f32(a.inv_q + q_first + lane);
       }
-      bool left = false;
+      const int64_t base = ld_early_s64(a.q_indptr + q_first);
+      if (lane < H) {
+        const float4 v = ld_early_f4(a.qhot + (size_t)(j / kGroupsPerQTile) * kHotMax * kTQ +
+                                     lane * kTQ + (int)(j % kGroupsPerQTile) * kQGroup);
+        *reinterpret_cast<float4 *>(qh + lane * kQGroup) = v;
+      }
+      int2 pf[kPasses];
 #pragma unroll
-      for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-        uint2 *hrow = hits + (warp * kRowsPerWarp + rr) * kHitCap;
-        int n = 0;
-        while (p[rr] < e[rr]) {
-          const int32_t pp = p[rr] + lane;
-          int2 x = make_int2(-1, 0);
-          if (ch[rr] == 0) x = pk[rr];
-          else if (pp < e[rr]) x = __ldg(a.qcold + pp);
-          const int32_t k = x.x;
-          const float v = __int_as_float(x.y);
-          const uint32_t se = k >= 0 ? image_find(slots, bits, k) : 0u;
-          const bool hit = (se >> 16) > (se & 0xffffu);
-          const unsigned mask = __ballot_sync(0xffffffffu, hit);
-          const int c = __popc(mask);
-          const int room = kHitCap - n;
-          const int rank = __popc(mask & lt_mask);
-          if (c <= room) {
-            if (hit) hrow[n + rank] = make_uint2(se, __float_as_uint(v));
-            n += c;
-            p[rr] = pp - lane + 32 < e[rr] ? pp - lane + 32 : e[rr];
-            ++ch[rr];
-            continue;
-          }
-          // More hits than room: keep the first `room` (room >= 1 whenever
-          // n == 0, since kHitCap >= 1, so every round makes progress) and
-          // resume right after the last one kept.
-          if (room > 0) {
-            if (hit && rank < room) hrow[n + rank] = make_uint2(se, __float_as_uint(v));
-            unsigned m = mask;
-            for (int j = 1; j < room; ++j) m &= m - 1u;  // drop the lowest room-1 hits
-            p[rr] = pp - lane + __ffs(m);                 // one past the room-th hit's lane
-            ch[rr] = 1;  // later chunks no longer line up with the prefetched one
-            n += room;
-          }
+      for (int p = 0; p < kPasses; ++p) {
+        pf[p] = make_int2(-1, 0);
+        if (base + p * 32 + lane < a.q_nnz) pf[p] = ld_early_s64_as_int2(a.qcold + base + p * 32 + lane);
+      }
+      const int b1 = __shfl_sync(0xffffffffu, cn, 0);
+      const int b2 = b1 + __shfl_sync(0xffffffffu, cn, 1);
+      const int b3 = b2 + __shfl_sync(0xffffffffu, cn, 2);
+      const int N = b3 + __shfl_sync(0xffffffffu, cn, 3);
+      __syncwarp();
+
+      // 1. hot dims
+      hot_product_group(acc, qh, slab, H, lane);
+      __syncwarp();
+
+      // 2. cold dims, in rounds of at most kHitCap hits.  Every round starts
+      // with room for 32 hits, so it consumes at least one pass of entries.
+      int pos = 0;
+      bool from_pf = true;
+      for (int round = 0; pos < N; ++round) {
+        if (round == kMaxRounds) {
+          if (lane == 0) flag(a.status, DEV_STALL);
           break;
         }
-        if (lane == 0) nh[warp * kRowsPerWarp + rr] = n;
-        left |= p[rr] < e[rr];
-      }
-      __syncwarp();
-      const int grp = lane / kGroup, li = lane % kGroup;
-      const int row = warp * kRowsPerWarp + grp;
-      const int my_n = nh[row];
-      const uint2 *hrow = hits + row * kHitCap;
-      float *arow = acc + row * kTI;
-      for (int h = 0; h < my_n; ++h) {
-        const uint2 hh = hrow[h];
-        const float qv = __uint_as_float(hh.y);
-        const int end = (int)(hh.x >> 16);
-        // Two entries of the segment per step (distinct items, so the two
-        // read-modify-writes are independent).
-        int j = (int)(hh.x & 0xffffu) + li;
-        for (; j + kGroup < end; j += 2 * kGroup) {
-          float *d0 = arow + seg_item[j];
-          float *d1 = arow + seg_item[j + kGroup];
-          const float v0 = seg_val[j], v1 = seg_val[j + kGroup];
-          const float a0 = *d0, a1 = *d1;
-          *d0 = fmaf(qv, v0, a0);
-          *d1 = fmaf(qv, v1, a1);
-        }
-        if (j < end) {
-          float *d = arow + seg_item[j];
-          *d = fmaf(qv, seg_val[j], *d);
-        }
-      }
-      __syncwarp();
-      if (!__any_sync(0xffffffffu, left)) break;
-    }
-    __syncthreads();
-    // 3. normalise and store
-    {
-      const int i0 = t * kTI;
-      const int ni = min(kTI, a.n_items - i0);
-      const int c = (tid & 63) * 4;
-      if (c < ni) {
-        const float4 n4 = *reinterpret_cast<const float4 *>(invi + c);
-        const bool vec = a.vec_ok && (c + 4 <= ni);
-        for (int r = tid >> 6; r < nq; r += kFThreads / 64) {
-          const float4 v = *reinterpret_cast<const float4 *>(acc + r * kTI + c);
-          const float iq = invq[r];
-          float *dst = a.out + (q0 + r) * a.ld_out + i0 + c;
-          const float o0 = v.x * iq * n4.x, o1 = v.y * iq * n4.y, o2 = v.z * iq * n4.z,
-                      o3 = v.w * iq * n4.w;
-          if (vec) {
-            __stcs(reinterpret_cast<float4 *>(dst), make_float4(o0, o1, o2, o3));
-          } else {
-            const float o[4] = {o0, o1, o2, o3};
-            for (int j = 0; j < 4 && c + j < ni; ++j) dst[j] = o[j];
+        int nh = 0, h1 = 0, h2 = 0, h3 = 0;  // hits kept; of them, from rows before 1, 2, 3
+        bool full = false;
+        while (!full && pos < N) {
+          int2 x[kPasses];
+#pragma unroll
+          for (int p = 0; p < kPasses; ++p) {
+            const int e = pos + p * 32 + lane;
+            if (from_pf) {
+              x[p] = pf[p];
+            } else {
+              x[p] = make_int2(-1, 0);
+              if (e < N) x[p] = __ldg(a.qcold + base + e);
+            }
+            if (e >= N) x[p].x = -1;
           }
+          from_pf = false;
+          uint32_t se[kPasses];
+          image_lookups(slots, bits, x, se);
+          int next = pos + kPasses * 32 < N ? pos + kPasses * 32 : N;
+#pragma unroll
+          for (int p = 0; p < kPasses; ++p) {
+            const int P = pos + p * 32;
+            if (P >= N || full) continue;
+            const bool hit = (se[p] >> 16) > (se[p] & 0xffffu);
+            const unsigned mask = __ballot_sync(0xffffffffu, hit);
+            const int room = kHitCap - nh;
+            unsigned keep = mask;
+            if (__popc(mask) > room) {
+              // Keep the first `room` hits; the next round resumes at the
+              // first hit not kept.
+              unsigned rest = mask;
+              for (int i = 0; i < room; ++i) rest &= rest - 1u;
+              keep = mask & ~rest;
+              next = P + __ffs(rest) - 1;
+              full = true;
+            }
+            if ((keep >> lane) & 1u)
+              hits[nh + __popc(keep & lt_mask)] = make_uint2(se[p], (uint32_t)x[p].y);  // value bits
+            h1 += __popc(keep & lanes_below(b1 - P));
+            h2 += __popc(keep & lanes_below(b2 - P));
+            h3 += __popc(keep & lanes_below(b3 - P));
+            nh += __popc(keep);
+          }
+          pos = next;
+        }
+        __syncwarp();
+        // One lane group per row walks the row's hits, the next hit's record
+        // loaded while the current segment is walked.
+        const int hs = grp == 0 ? 0 : grp == 1 ? h1 : grp == 2 ? h2 : h3;
+        const int he = grp == 0 ? h1 : grp == 1 ? h2 : grp == 2 ? h3 : nh;
+        float *arow = acc + grp * kTI;
+        uint2 hh = hits[hs < he ? hs : 0];
+        for (int h = hs; h < he; ++h) {
+          const uint2 nx = hits[h + 1 < he ? h + 1 : h];
+          walk_segment(arow, seg_item, seg_val, hh, li);
+          hh = nx;
+        }
+        __syncwarp();
+      }
+
+      // 3. normalise and store the group's rows
+#pragma unroll
+      for (int r = 0; r < kQGroup; ++r) {
+        const float iqr = __shfl_sync(0xffffffffu, iq, r);
+        if (r >= nr) continue;
+        float *dst = a.out + (q_first + r) * a.ld_out + i0;
+        const float4 va = *reinterpret_cast<const float4 *>(acc + r * kTI + ia);
+        const float4 vb = *reinterpret_cast<const float4 *>(acc + r * kTI + ib);
+        const float oa[4] = {va.x * iqr * na[0], va.y * iqr * na[1], va.z * iqr * na[2],
+                             va.w * iqr * na[3]};
+        const float ob[4] = {vb.x * iqr * nb[0], vb.y * iqr * nb[1], vb.z * iqr * nb[2],
+                             vb.w * iqr * nb[3]};
+        if (a.vec_ok && ia + 4 <= ni) {
+          __stcs(reinterpret_cast<float4 *>(dst + ia), make_float4(oa[0], oa[1], oa[2], oa[3]));
+        } else {
+          for (int c = 0; c < 4; ++c)
+            if (ia + c < ni) dst[ia + c] = oa[c];
+        }
+        if (a.vec_ok && ib + 4 <= ni) {
+          __stcs(reinterpret_cast<float4 *>(dst + ib), make_float4(ob[0], ob[1], ob[2], ob[3]));
+        } else {
+          for (int c = 0; c < 4; ++c)
+            if (ib + c < ni) dst[ib + c] = ob[c];
         }
       }
+      __syncwarp();
     }
-    __syncthreads();
   }
   cp_async_wait_all();
 }
@@ -1447,6 +1536,7 @@ cudaError_t launch_score_hybrid(ss_handle *h, const ss_csr &queries, const float
   f.qcold = h->qcold;
   f.qcold_n = h->qcold_n;
   f.n_q = queries.n_rows;
+  f.q_nnz = queries.nnz;
   f.inv_q = inv_q;
   f.qhot = h->qhot;
   f.hot = idx.hot;

@@ -26,6 +26,7 @@ enum : int32_t {
 // Geometry of the hybrid scorer (see hybrid.cu).
 namespace hyb {
 constexpr int kTQ = 64;                    // query rows per tile
+constexpr int kQGroup = 4;                 // query rows scored together by one warp
 constexpr int kTI = 256;                   // items per tile (one thread per item)
 constexpr int kThreads = 256;              // threads per block (8 warps)
 constexpr int kHotMax = 24;                // dense ("hot") dimensions per item matrix
@@ -55,6 +56,7 @@ constexpr int kImgBytes = kImgOffVal + kImgECap * 4;
 static_assert(kImgOffItem % 16 == 0 && kImgOffVal % 16 == 0 && kImgBytes % 16 == 0,
               "image sections must stay 16-byte aligned");
 constexpr int kMetaFits = 10;              // meta slot: 1 if the tile has an image
+static_assert(kTQ % kQGroup == 0, "query tiles hold whole row groups");
 }  // namespace hyb
 
 // The per-chunk index.  ALGO_POSTING: one posting list of (item, value) per
