@@ -196,13 +196,50 @@ __device__ __forceinline__ int img_find(const int *keys, int32_t k) {
   return -1;
 }
 
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async4(void *smem_dst, const void *gmem_src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(gmem_src) : "memory");
+}
+
+__device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
+
+// Copies elements [b, e) of a 4-byte array to dst[0, e - a), where a = b
+// rounded down to a multiple of 4 (so dst[p - a] holds element p): 16-byte
+// copies for whole aligned groups inside [a, e) when the array itself is
+// 16-byte aligned, 4-byte copies for the rest.  Elements [a, b) are copied
+// too; they lie inside the array.
+__device__ __forceinline__ void stage_words(void *dst, const void *src_array, int64_t b, int64_t e,
+                                            int nthreads) {
+  const int64_t a = b & ~(int64_t)3;
+  const bool vec = (reinterpret_cast<uintptr_t>(src_array) & 15u) == 0;
+  const int64_t e4 = vec ? (e & ~(int64_t)3) : a;
+  const uint32_t *src = reinterpret_cast<const uint32_t *>(src_array);
+  uint32_t *d = reinterpret_cast<uint32_t *>(dst);
+  for (int64_t p = a + 4 * (int64_t)threadIdx.x; p < e4; p += 4 * (int64_t)nthreads)
+    cp_async16(d + (p - a), src + p);
+  const int64_t tail0 = e4 > a ? e4 : a;
+  for (int64_t p = tail0 + threadIdx.x; p < e; p += nthreads) cp_async4(d + (p - a), src + p);
+}
+
 // Shared memory of the builder block (bytes).
 constexpr int kBThreads = 1024;  // builder: 32 warps, one item row per warp at a time
 constexpr int kBldOffSlab = 0;
 constexpr int kBldOffKeys = kBldOffSlab + kHotMax * kTI * 4;
 constexpr int kBldOffCnt = kBldOffKeys + kImgSlots * 4;
 constexpr int kBldOffCold = kBldOffCnt + kImgSlots * 4;  // cold nonzeros per item
-constexpr int kBuildSmem = kBldOffCold + kTI * 4;
+constexpr int kBldOffPtr = kBldOffCold + kTI * 4;         // the tile's row offsets (int64)
+constexpr int kBldStage = 12288;                          // nonzeros of a tile staged on chip
+constexpr int kBldOffIdx = kBldOffPtr + ((kTI + 1) * 8 + 15) / 16 * 16;
+constexpr int kBldOffVal = kBldOffIdx + kBldStage * 4;
+constexpr int kBuildSmem = kBldOffVal + kBldStage * 4;
+static_assert(kBldOffIdx % 16 == 0 && kBldOffVal % 16 == 0, "staging buffers must stay 16-byte aligned");
+static_assert(kImgECap <= kHotMax * kTI * 4, "segment items are staged in the slab's space");
 
 __device__ __forceinline__ int bblock_sum(int v, int *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -238,11 +275,14 @@ __device__ __forceinline__ int bblock_exclusive_scan(int v, int *red, int *total
   return off + inc - v;
 }
 
-// One block per tile of kTI items; warp w handles items w, w + 32, ..., its
-// lanes taking the row's nonzeros 32 at a time (coalesced).  Hot values go
-// to the tile's slab.  The cold nonzeros become the tile's image (dimension
-// -> segment of (item, value)) when they fit; otherwise they go to the ELL
-// block and the heavy list, and the tile joins the overflow list.
+// One block per tile of kTI items.  The tile's row offsets, and its
+// nonzeros when they fit (kBldStage), are first copied on chip with
+// asynchronous copies, so the two passes below read shared memory instead of
+// waiting on dependent global loads.  Warp w handles items w, w + 32, ...,
+// its lanes taking the row's nonzeros 32 at a time.  Hot values go to the
+// tile's slab.  The cold nonzeros become the tile's image (dimension ->
+// segment of (item, value)) when they fit; otherwise they go to the ELL block
+// and the heavy list, and the tile joins the overflow list.
 __global__ void __launch_bounds__(kBThreads, 1)
     k_build_tiles(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
                   const float *__restrict__ values, int64_t row_begin, int64_t row_end,
@@ -253,9 +293,13 @@ __global__ void __launch_bounds__(kBThreads, 1)
                   int64_t heavy_cap, unsigned char *__restrict__ image, int32_t *status) {
   extern __shared__ __align__(16) unsigned char bsm[];
   float *slab_s = reinterpret_cast<float *>(bsm + kBldOffSlab);  // [kHotMax][kTI]
+  uint8_t *item_s = bsm + kBldOffSlab;  // segment items, once the slab has been written out
   int *ikeys = reinterpret_cast<int *>(bsm + kBldOffKeys);
   int *icnt = reinterpret_cast<int *>(bsm + kBldOffCnt);
   int *cold_n = reinterpret_cast<int *>(bsm + kBldOffCold);
+  int64_t *ptr_s = reinterpret_cast<int64_t *>(bsm + kBldOffPtr);
+  const int32_t *idx_s = reinterpret_cast<const int32_t *>(bsm + kBldOffIdx);
+  const float *val_s = reinterpret_cast<const float *>(bsm + kBldOffVal);
   __shared__ int hkeys[kHotSlots];
   __shared__ int8_t hvals[kHotSlots];
   __shared__ int red[kBThreads / 32];
@@ -264,11 +308,12 @@ __global__ void __launch_bounds__(kBThreads, 1)
   __shared__ uint32_t bits_s[(1 << kImgBitsLog2) / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int w = tid; w < (1 << kImgBitsLog2) / 32; w += kBThreads) bits_s[w] = 0u;
   const int t = blockIdx.x;
   const int64_t item0 = row_begin + (int64_t)t * kTI;
   const int n_items = (int)min((int64_t)kTI, row_end - item0);
   const int H = hot[0];
+  if (tid <= n_items) ptr_s[tid] = indptr[item0 + tid];
+  for (int w = tid; w < (1 << kImgBitsLog2) / 32; w += kBThreads) bits_s[w] = 0u;
   for (int s = tid; s < kHotSlots; s += kBThreads) hkeys[s] = -1;
   for (int s = tid; s < kImgSlots; s += kBThreads) {
     ikeys[s] = -1;
@@ -277,19 +322,30 @@ __global__ void __launch_bounds__(kBThreads, 1)
   for (int j = tid; j < H * kTI; j += kBThreads) slab_s[j] = 0.0f;
   if (tid == 0) img_fail = 0;
   __syncthreads();
+  const int64_t p0 = ptr_s[0], p1 = ptr_s[n_items];
+  const int64_t pa = p0 & ~(int64_t)3;  // staged element p sits at [p - pa]
+  const bool staged = p1 - pa <= kBldStage;
+  if (staged) {
+    stage_words(bsm + kBldOffIdx, indices, p0, p1, kBThreads);
+    stage_words(bsm + kBldOffVal, values, p0, p1, kBThreads);
+  }
+  cp_async_commit();
   if (tid < H) hot_insert(hkeys, hvals, hot[1 + tid], tid);
+  cp_async_wait_all();
   __syncthreads();
+  auto key_at = [&](int64_t p) -> int32_t { return staged ? idx_s[p - pa] : __ldg(indices + p); };
+  auto val_at = [&](int64_t p) -> float { return staged ? val_s[p - pa] : __ldg(values + p); };
 
   // Pass 1: hot values into the slab; cold dims into the image hash.
   for (int it = warp; it < kTI; it += kBThreads / 32) {
     int cold = 0;
     if (it < n_items) {
-      const int64_t pb = indptr[item0 + it], pe = indptr[item0 + it + 1];
+      const int64_t pb = ptr_s[it], pe = ptr_s[it + 1];
       for (int64_t p = pb + lane; p < pe; p += 32) {
-        const int32_t k = __ldg(indices + p);
+        const int32_t k = key_at(p);
         const int h = hot_find(hkeys, hvals, k);
         if (h >= 0) {
-          slab_s[h * kTI + it] = __ldg(values + p);
+          slab_s[h * kTI + it] = val_at(p);
         } else {
           ++cold;
           const int slot = img_insert(ikeys, k);
@@ -303,8 +359,12 @@ __global__ void __launch_bounds__(kBThreads, 1)
     if (lane == 0) cold_n[it] = cold;
   }
   __syncthreads();
+  {
+    float *dst = slab + (size_t)t * kHotMax * kTI;
+    for (int j = tid; j < H * kTI; j += kBThreads) dst[j] = slab_s[j];
+  }
   const int my_cold = tid < kTI ? cold_n[tid] : 0;
-  const int sum_cold = bblock_sum(my_cold, red);
+  const int sum_cold = bblock_sum(my_cold, red);  // its barriers also end the slab's reads
   unsigned char *img = image + (size_t)t * kImgBytes;
   int32_t *hdr = reinterpret_cast<int32_t *>(img);
 
@@ -344,18 +404,21 @@ __global__ void __launch_bounds__(kBThreads, 1)
     __syncthreads();
     uint32_t *gbits = reinterpret_cast<uint32_t *>(img + kImgOffBits);
     for (int w = tid; w < (1 << kImgBitsLog2) / 32; w += kBThreads) gbits[w] = bits_s[w];
-    uint8_t *gitem = img + kImgOffItem;
     float *gval = reinterpret_cast<float *>(img + kImgOffVal);
     for (int it = warp; it < n_items; it += kBThreads / 32) {
-      const int64_t pb = indptr[item0 + it], pe = indptr[item0 + it + 1];
+      const int64_t pb = ptr_s[it], pe = ptr_s[it + 1];
       for (int64_t p = pb + lane; p < pe; p += 32) {
-        const int32_t k = __ldg(indices + p);
+        const int32_t k = key_at(p);
         if (hot_find(hkeys, hvals, k) >= 0) continue;
         const int pos = atomicAdd(&icnt[img_find(ikeys, k)], 1);
-        gitem[pos] = (uint8_t)it;
-        gval[pos] = __ldg(values + p);
+        item_s[pos] = (uint8_t)it;
+        gval[pos] = val_at(p);
       }
     }
+    __syncthreads();
+    uint4 *gitem = reinterpret_cast<uint4 *>(img + kImgOffItem);
+    const uint4 *sitem = reinterpret_cast<const uint4 *>(item_s);
+    for (int j = tid; j < round16(E) / 16; j += kBThreads) gitem[j] = sitem[j];
   }
 
   // ---- ELL path for tiles whose cold part does not fit an image
@@ -394,19 +457,19 @@ __global__ void __launch_bounds__(kBThreads, 1)
       int2 *col = ell + (size_t)t * kEllMaxW * kTI + it;
       int s = 0;
       if (it < n_items) {
-        const int64_t pb = indptr[item0 + it], pe = indptr[item0 + it + 1];
+        const int64_t pb = ptr_s[it], pe = ptr_s[it + 1];
         for (int64_t p = pb; p < pe; p += 32) {
           const int64_t pp = p + lane;
           int32_t k = -1;
           bool is_cold = false;
           if (pp < pe) {
-            k = __ldg(indices + pp);
+            k = key_at(pp);
             is_cold = hot_find(hkeys, hvals, k) < 0;
           }
           const unsigned cm = __ballot_sync(0xffffffffu, is_cold);
           const int pos = s + __popc(cm & lt_mask);
           if (is_cold) {
-            const float v = __ldg(values + pp);
+            const float v = val_at(pp);
             if (hoff < 0) {
               col[(size_t)pos * kTI] = make_int2(k, __float_as_int(v));
             } else if (heavy_ok) {
@@ -426,9 +489,6 @@ __global__ void __launch_bounds__(kBThreads, 1)
   } else if (tid < 8) {
     m[tid] = 0;
   }
-  __syncthreads();
-  float *dst = slab + (size_t)t * kHotMax * kTI;
-  for (int j = tid; j < H * kTI; j += kBThreads) dst[j] = slab_s[j];
   if (tid == 0) {
     if (fits) m[8] = 0;
     m[9] = (!fits && heavy_ok) ? heavy_total : 0;
@@ -488,12 +548,6 @@ struct Smem {
   int8_t *hotv;
 };
 
-__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
-  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gmem_src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 // Queues the copy of one item tile's hot slab (H rows of kTI floats).
 __device__ __forceinline__ void slab_prefetch(const Smem &sm, const HybridArgs &a, int t, int H) {
@@ -1034,8 +1088,6 @@ __device__ __forceinline__ float4 ld_early_f4(const float *p) {
 __device__ __forceinline__ void cp_bytes(unsigned char *dst, const unsigned char *src, int n) {
   for (int j = threadIdx.x * 16; j < n; j += kFThreads * 16) cp_async16(dst + j, src + j);
 }
-
-__device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
 
 // Lanes [0, x) of a warp (x clamped to [0, 32]).
 __device__ __forceinline__ unsigned lanes_below(int x) {

@@ -73,6 +73,27 @@ def test_row_norms_zero_rows_and_explicit_zeros(sec):
     assert inv[2] == np.float32(0.2) and inv[3] == np.float32(1.0 / 3.0)
 
 
+def test_row_norms_extreme_magnitudes(sec):
+    # Rows whose squares underflow or overflow float: tiny values, float
+    # subnormals, values near the top of the float range, and mixed scales.
+    rng = np.random.default_rng(11)
+    rows = []
+    for scale, n in [(1e-25, 40), (1e-39, 100), (4e-39, 200), (1e30, 50), (3e37, 3),
+                     (1.0, 60), (1e-20, 5)]:
+        idx = np.sort(rng.choice(4096, size=n, replace=False))
+        rows.append((idx, (rng.standard_normal(n) * scale).astype(np.float32)))
+    idx = np.arange(0, 4096, 512)
+    rows.append((idx, np.array([1e-30, 1e20, 3.0, 1e-40, 2e19, 0.0, 5e-3, 1e10], np.float32)))
+    X = csr_from_rows(rows, 4096)
+    with sec.SparseCosine(X.dim) as h:
+        inv = h.row_norms(_dev(sec, X)).cpu().numpy()
+    with np.errstate(divide="ignore", over="ignore"):
+        ref = (1.0 / oracle.row_norms(X)).astype(np.float32)
+    assert np.all(np.isfinite(ref))
+    ulps = np.abs(inv.view(np.int32).astype(np.int64) - ref.view(np.int32).astype(np.int64))
+    assert ulps.max() <= 1, (inv, ref)
+
+
 def test_row_norms_heavy_rows(sec):
     # rows of 20,000 nonzeros, the largest the heavy-tailed workload allows
     rng = np.random.default_rng(7)
