@@ -1037,6 +1037,7 @@ constexpr int kFWarps = kFThreads / 32;
 constexpr int kGroup = 32 / kQGroup;             // lanes walking one row's segments
 constexpr int kHitCap = 112;                     // hits of one row group held per round
 constexpr int kPasses = 4;                       // lookup passes of 32 entries in flight
+static_assert(kPasses == 4, "the lookup dispatch instantiates 1 to 4 passes");
 constexpr int kMaxRounds = 1 << 20;              // far above any group's entry count
 constexpr int kGroupsPerQTile = kTQ / kQGroup;
 constexpr int kFOffAcc = 0;                                          // [warp][kQGroup][kTI] f32
@@ -1111,7 +1112,7 @@ __device__ __forceinline__ uint32_t image_find_rest(const uint2 *slots, int32_t 
   return 0;
 }
 
-// Looks up kPasses dimensions per lane (k < 0: none) in the item tile's
+// Looks up P <= kPasses dimensions per lane (k < 0: none) in the item tile's
 // image and returns each one's segment [start, end) packed as start |
 // end << 16 (0 if absent).  About half of a query row's cold dimensions are
 // absent from a given tile; the membership bitmap turns most of those misses
@@ -1119,17 +1120,18 @@ __device__ __forceinline__ uint32_t image_find_rest(const uint2 *slots, int32_t 
 // between the home slot and a key's own slot is occupied, so a key missing
 // from a group that holds an empty slot is absent).  All passes' loads are
 // issued before any result is used.
+template <int P>
 __device__ __forceinline__ void image_lookups(const uint2 *slots, const uint32_t *bits,
                                               const int2 (&x)[kPasses], uint32_t (&se)[kPasses]) {
-  bool cand[kPasses];
+  bool cand[P];
 #pragma unroll
-  for (int p = 0; p < kPasses; ++p) {
+  for (int p = 0; p < P; ++p) {
     const uint32_t bb = hash_b(x[p].x, kImgBitsLog2);
     cand[p] = x[p].x >= 0 && ((bits[bb >> 5] >> (bb & 31)) & 1u);
   }
-  uint4 ga[kPasses], gb[kPasses];
+  uint4 ga[P], gb[P];
 #pragma unroll
-  for (int p = 0; p < kPasses; ++p) {
+  for (int p = 0; p < P; ++p) {
     ga[p] = make_uint4(0u, 0u, 0u, 0u);
     gb[p] = ga[p];
     if (cand[p]) {
@@ -1140,7 +1142,7 @@ __device__ __forceinline__ void image_lookups(const uint2 *slots, const uint32_t
   }
   const uint32_t empty = 0xffffffffu;
 #pragma unroll
-  for (int p = 0; p < kPasses; ++p) {
+  for (int p = 0; p < P; ++p) {
     const uint32_t ku = (uint32_t)x[p].x;
     const uint4 a = ga[p], b = gb[p];
     se[p] = 0u;
@@ -1203,24 +1205,28 @@ __device__ __forceinline__ void hot_product_group(float *acc, const float *qh, c
 }
 
 // Adds q * value over one image segment into a row's accumulator: the lanes
-// of a group take every kGroup-th entry, two entries per step (the items of
-// one segment are distinct, so the read-modify-writes are independent).
+// of a group take every kGroup-th entry, two entries per step, the second
+// one predicated (the items of one segment are distinct, so the two
+// read-modify-writes are independent, and one loop body serves every length
+// without a separate tail for the group to diverge on).
 __device__ __forceinline__ void walk_segment(float *arow, const uint8_t *seg_item,
                                              const float *seg_val, uint2 hh, int li) {
   const float qv = __uint_as_float(hh.y);
   const int end = (int)(hh.x >> 16);
-  int j = (int)(hh.x & 0xffffu) + li;
-  for (; j + kGroup < end; j += 2 * kGroup) {
-    float *d0 = arow + seg_item[j];
-    float *d1 = arow + seg_item[j + kGroup];
-    const float v0 = seg_val[j], v1 = seg_val[j + kGroup];
-    const float a0 = *d0, a1 = *d1;
-    *d0 = fmaf(qv, v0, a0);
-    *d1 = fmaf(qv, v1, a1);
-  }
-  if (j < end) {
-    float *d = arow + seg_item[j];
-    *d = fmaf(qv, seg_val[j], *d);
+  for (int j = (int)(hh.x & 0xffffu) + li; j < end; j += 2 * kGroup) {
+    const bool two = j + kGroup < end;
+    const int i0 = seg_item[j];
+    const float v0 = seg_val[j];
+    int i1 = 0;
+    float v1 = 0.f;
+    if (two) {
+      i1 = seg_item[j + kGroup];
+      v1 = seg_val[j + kGroup];
+    }
+    const float a0 = arow[i0];
+    const float a1 = two ? arow[i1] : 0.f;
+    arow[i0] = fmaf(qv, v0, a0);
+    if (two) arow[i1] = fmaf(qv, v1, a1);
   }
 }
 
@@ -1354,8 +1360,13 @@ __global__ void __launch_bounds__(kFThreads, 1) k_score_tiles(const TileArgs a) 
             if (e >= N) x[p].x = -1;
           }
           from_pf = false;
-          uint32_t se[kPasses];
-          image_lookups(slots, bits, x, se);
+          // Only the passes that still hold entries are looked up.
+          uint32_t se[kPasses] = {};
+          const int live = (N - pos + 31) / 32;
+          if (live >= kPasses) image_lookups<kPasses>(slots, bits, x, se);
+          else if (live == 3) image_lookups<3>(slots, bits, x, se);
+          else if (live == 2) image_lookups<2>(slots, bits, x, se);
+          else image_lookups<1>(slots, bits, x, se);
           int next = pos + kPasses * 32 < N ? pos + kPasses * 32 : N;
 #pragma unroll
           for (int p = 0; p < kPasses; ++p) {
