@@ -1038,6 +1038,7 @@ constexpr int kGroup = 32 / kQGroup;             // lanes walking one row's segm
 constexpr int kHitCap = 112;                     // hits of one row group held per round
 constexpr int kPasses = 4;                       // lookup passes of 32 entries in flight
 static_assert(kPasses == 4, "the lookup dispatch instantiates 1 to 4 passes");
+static_assert(kHotMax % 4 == 0, "hot dims are padded to a multiple of 4 inside the slab");
 constexpr int kMaxRounds = 1 << 20;              // far above any group's entry count
 constexpr int kGroupsPerQTile = kTQ / kQGroup;
 constexpr int kFOffAcc = 0;                                          // [warp][kQGroup][kTI] f32
@@ -1158,9 +1159,11 @@ __device__ __forceinline__ void image_lookups(const uint2 *slots, const uint32_t
 }
 
 // Dense product over the hot dims for one warp's row group: lane l owns
-// items 4l + [0, 4) and 128 + 4l + [0, 4) of all kQGroup rows.  Operands of
-// dim h + 1 are loaded while dim h is multiplied.  Writes the group's
-// accumulator rows (zeros when there are no hot dims).
+// items 4l + [0, 4) and 128 + 4l + [0, 4) of all kQGroup rows.  The dims run
+// four at a time (H rounded up to a multiple of 4; the slab and hot values
+// hold zeros past H), their twelve operand loads issued before the packed
+// multiply-adds.  Writes the group's accumulator rows (zeros when there are
+// no hot dims).
 __device__ __forceinline__ void hot_product_group(float *acc, const float *qh, const float *slab,
                                                   int H, int lane) {
   const int ia = 4 * lane, ib = 128 + 4 * lane;
@@ -1169,31 +1172,29 @@ __device__ __forceinline__ void hot_product_group(float *acc, const float *qh, c
   for (int r = 0; r < kQGroup; ++r)
 #pragma unroll
     for (int j = 0; j < 4; ++j) c[r][j] = make_float2(0.f, 0.f);
-  float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f), sa = q4, sb = q4;
-  if (H > 0) {
-    q4 = *reinterpret_cast<const float4 *>(qh);
-    sa = *reinterpret_cast<const float4 *>(slab + ia);
-    sb = *reinterpret_cast<const float4 *>(slab + ib);
-  }
-  for (int h = 0; h < H; ++h) {
-    const int hn = h + 1 < H ? h + 1 : h;
-    const float4 qn = *reinterpret_cast<const float4 *>(qh + hn * kQGroup);
-    const float4 an = *reinterpret_cast<const float4 *>(slab + hn * kTI + ia);
-    const float4 bn = *reinterpret_cast<const float4 *>(slab + hn * kTI + ib);
-    const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
-    const float2 i0 = make_float2(sa.x, sa.y), i1 = make_float2(sa.z, sa.w);
-    const float2 i2 = make_float2(sb.x, sb.y), i3 = make_float2(sb.z, sb.w);
+  const int Hp = (H + 3) & ~3;
+  for (int h0 = 0; h0 < Hp; h0 += 4) {
+    float4 q4[4], sa[4], sb[4];
 #pragma unroll
-    for (int r = 0; r < kQGroup; ++r) {
-      const float2 qq = make_float2(qv[r], qv[r]);
-      c[r][0] = __ffma2_rn(qq, i0, c[r][0]);
-      c[r][1] = __ffma2_rn(qq, i1, c[r][1]);
-      c[r][2] = __ffma2_rn(qq, i2, c[r][2]);
-      c[r][3] = __ffma2_rn(qq, i3, c[r][3]);
+    for (int u = 0; u < 4; ++u) {
+      q4[u] = *reinterpret_cast<const float4 *>(qh + (h0 + u) * kQGroup);
+      sa[u] = *reinterpret_cast<const float4 *>(slab + (h0 + u) * kTI + ia);
+      sb[u] = *reinterpret_cast<const float4 *>(slab + (h0 + u) * kTI + ib);
     }
-    q4 = qn;
-    sa = an;
-    sb = bn;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float qv[4] = {q4[u].x, q4[u].y, q4[u].z, q4[u].w};
+      const float2 i0 = make_float2(sa[u].x, sa[u].y), i1 = make_float2(sa[u].z, sa[u].w);
+      const float2 i2 = make_float2(sb[u].x, sb[u].y), i3 = make_float2(sb[u].z, sb[u].w);
+#pragma unroll
+      for (int r = 0; r < kQGroup; ++r) {
+        const float2 qq = make_float2(qv[r], qv[r]);
+        c[r][0] = __ffma2_rn(qq, i0, c[r][0]);
+        c[r][1] = __ffma2_rn(qq, i1, c[r][1]);
+        c[r][2] = __ffma2_rn(qq, i2, c[r][2]);
+        c[r][3] = __ffma2_rn(qq, i3, c[r][3]);
+      }
+    }
   }
 #pragma unroll
   for (int r = 0; r < kQGroup; ++r) {
@@ -1280,6 +1281,7 @@ __global__ void __launch_bounds__(kFThreads, 1) k_score_tiles(const TileArgs a) 
                reinterpret_cast<const unsigned char *>(a.slab + (size_t)t * kHotMax * kTI),
                H * kTI * 4);
       cp_async_commit();
+      for (int z = H * kTI + tid; z < ((H + 3) & ~3) * kTI; z += kFThreads) slab[z] = 0.f;  // pad rows
       if (tid == 0) *next_group = 0;
     }
     const int i0 = t * kTI;
@@ -1314,6 +1316,8 @@ __global__ void __launch_bounds__(kFThreads, 1) k_score_tiles(const TileArgs a) 
         iq = ld_early_f32(a.inv_q + q_first + lane);
       }
       const int64_t base = ld_early_s64(a.q_indptr + q_first);
+      if (lane >= H && lane < ((H + 3) & ~3))  // pad rows of the hot values
+        *reinterpret_cast<float4 *>(qh + lane * kQGroup) = make_float4(0.f, 0.f, 0.f, 0.f);
       if (lane < H) {
         const float4 v = ld_early_f4(a.qhot + (size_t)(j / kGroupsPerQTile) * kHotMax * kTQ +
                                      lane * kTQ + (int)(j % kGroupsPerQTile) * kQGroup);
