@@ -152,15 +152,21 @@ typedef int (*ss_chunk_consumer)(void *user, int64_t chunk, int64_t item_begin,
 /*
  * End to end from host memory (sections 2.2 and 4.4): copies the host CSR
  * batches to the device, computes both norm vectors, then for each item
- * chunk builds the index, scores it, and streams the chunk's result back to
- * the host through a ring of `ring_depth` (>= 2) pinned host buffers, with
- * the device-to-host copies on a second stream so they overlap the next
- * chunk's kernels.  Each finished chunk is copied into out_host (row-major,
- * ld_out >= items->n_rows; may be NULL) and/or handed to `consumer` (may be
- * NULL).  Blocks until the last chunk has been delivered.  Device buffers
- * and pinned slots are allocated and freed by the call.
- * timeout_ms bounds each host wait on the GPU (0 = 60000 ms);
- * SS_ERR_TIMEOUT if one runs out.
+ * chunk builds the index, scores it, and delivers the chunk's result to the
+ * host.  out_host (row-major, ld_out >= items->n_rows) may be NULL;
+ * `consumer` may be NULL; not both.
+ *  - out_host page-locked (cudaHostAlloc, or registered as mapped) and no
+ *    consumer: the scoring kernel stores each chunk straight into out_host
+ *    through the buffer's device address; nothing is staged.
+ *  - otherwise: each chunk is scored into one of two device buffers and
+ *    copied, on a second stream that overlaps the next chunk's kernels, into
+ *    a ring of `ring_depth` (>= 2) page-locked host buffers; from there its
+ *    rows are copied into out_host (if given) and the tile is handed to
+ *    `consumer` (if given).
+ * Blocks until the last chunk has been delivered.  Streams, device buffers
+ * and ring buffers belong to the handle and are kept (grown when needed)
+ * between calls; ss_destroy frees them.  timeout_ms bounds each host wait
+ * on the GPU (0 = 60000 ms); SS_ERR_TIMEOUT if one runs out.
  */
 ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *queries_host,
                               const ss_csr *items_host, float *out_host, int64_t ld_out,

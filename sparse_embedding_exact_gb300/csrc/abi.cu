@@ -130,6 +130,7 @@ ss_status ensure_capacity(ss_handle *h, int64_t need) {
 }
 
 void free_workspace(ss_handle *h) {
+  free_host_pass(h->host);
   void *ptrs[] = {h->d_status, h->col_cnt, h->col_ptr, h->scan_part, h->post_item, h->post_val,
                   h->hot, h->slab, h->ell, h->meta, h->heavy_k, h->heavy_v, h->heavy_item,
                   h->counters, h->image, h->qhot, h->qcold, h->qcold_n};

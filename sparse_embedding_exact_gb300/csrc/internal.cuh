@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <vector>
 
 #include "sparsecos.h"
 
@@ -87,6 +88,23 @@ struct ss_index {
   const int32_t *counters = nullptr;   // [0] heavy cursor, [1] tiles without an image, [2..] their ids
 };
 
+// Workspace of the host-buffer pass (ss_bulk_cosine_host), kept between
+// calls and grown on demand: its streams and events, the device copies of the
+// two CSR matrices and their inverse norms, two chunk output buffers, and the
+// page-locked ring used when results cannot be written straight to the
+// caller's memory.
+struct ss_host_pass {
+  enum { kQPtr, kQIdx, kQVal, kIPtr, kIIdx, kIVal, kInvQ, kInvI, kOut0, kOut1, kBuffers };
+  cudaStream_t comp = nullptr, copy = nullptr;
+  cudaEvent_t done[2] = {nullptr, nullptr}, out_free[2] = {nullptr, nullptr}, finished = nullptr;
+  std::vector<cudaEvent_t> copied;  // one per ring slot
+  void *buf[kBuffers] = {};
+  size_t cap[kBuffers] = {};
+  std::vector<float *> slots;
+  size_t slot_bytes = 0;
+};
+void free_host_pass(ss_host_pass &hp);
+
 struct ss_handle {
   int device = 0;
   int64_t dim = 0;
@@ -137,6 +155,7 @@ struct ss_handle {
   uint64_t prep_generation = ~0ull;
 
   ss_index index;
+  ss_host_pass host;
 };
 
 // Launchers (all asynchronous on `s`).

@@ -1,16 +1,20 @@
 // Host-buffer streaming pass: the "streaming batch" pipeline of the blog post
 // ("Engineering practice for bulk similarity calculation over sparse
-// embeddings", sections 2.2 and 4.4): items are scored chunk by chunk and each
-// chunk's slice of the result goes back to host memory while the next chunk
-// is computed.
+// embeddings", sections 2.2 and 4.4): items are scored chunk by chunk and
+// each chunk's slice of the result reaches host memory.
 //
-// Two device output buffers alternate between chunks.  The compute stream
-// builds the index and scores chunk c into buffer c % 2; the copy stream
-// waits for that, then copies the buffer to the host: straight into the
-// caller's output when that is page-locked, otherwise into slot c % R of a
-// ring of page-locked buffers, from which the host thread copies rows out or
-// hands the tile to the caller's consumer.  Events order buffer and slot
-// reuse; every host wait polls its event with a deadline.
+// When the caller's output is page-locked host memory that the device can
+// address, each chunk's scoring kernel stores its normalised tile straight
+// into it (device stores cross to host memory at the same rate as the copy
+// engines, and a pitched store costs no more than a contiguous one, while a
+// pitched copy-engine transfer of the chunk's rows runs at about half that
+// rate).  Otherwise two device output buffers alternate between chunks: the
+// compute stream builds the index and scores chunk c into buffer c % 2, the
+// copy stream then copies the buffer into slot c % R of a ring of
+// page-locked buffers, from which the host copies rows out or hands the tile
+// to the caller's consumer.  Events order buffer and slot reuse; every host
+// wait polls its event with a deadline.  Streams, events and buffers stay
+// with the handle between calls.
 #include <cuda_runtime.h>
 #include <stdarg.h>
 #include <stdio.h>
@@ -46,33 +50,6 @@ ss_status scuda(ss_handle *h, cudaError_t e, const char *what) {
     cudaError_t e_ = (call);                            \
     if (e_ != cudaSuccess) return scuda(h, e_, #call);  \
   } while (0)
-
-// Everything the pass allocates; the destructor drains the streams and frees.
-struct Pass {
-  cudaStream_t comp = nullptr, copy = nullptr;
-  int64_t *q_indptr = nullptr, *i_indptr = nullptr;
-  int32_t *q_idx = nullptr, *i_idx = nullptr;
-  float *q_val = nullptr, *i_val = nullptr, *inv_q = nullptr, *inv_i = nullptr;
-  float *dbuf[2] = {nullptr, nullptr};
-  std::vector<float *> slots;
-  cudaEvent_t done[2] = {nullptr, nullptr}, dbuf_free[2] = {nullptr, nullptr};
-  std::vector<cudaEvent_t> copied;
-  ~Pass() {
-    if (comp) cudaStreamSynchronize(comp);
-    if (copy) cudaStreamSynchronize(copy);
-    for (float *p : slots) cudaFreeHost(p);
-    for (cudaEvent_t e : copied) cudaEventDestroy(e);
-    for (int b = 0; b < 2; ++b) {
-      if (done[b]) cudaEventDestroy(done[b]);
-      if (dbuf_free[b]) cudaEventDestroy(dbuf_free[b]);
-      cudaFree(dbuf[b]);
-    }
-    cudaFree(q_indptr); cudaFree(i_indptr); cudaFree(q_idx); cudaFree(i_idx);
-    cudaFree(q_val); cudaFree(i_val); cudaFree(inv_q); cudaFree(inv_i);
-    if (comp) cudaStreamDestroy(comp);
-    if (copy) cudaStreamDestroy(copy);
-  }
-};
 
 ss_status wait_event(ss_handle *h, cudaEvent_t ev, int32_t timeout_ms, const char *what) {
   const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms);
@@ -117,14 +94,100 @@ ss_status check_host_csr(ss_handle *h, const ss_csr *m, const char *what) {
   return SS_OK;
 }
 
+// Grows device buffer `role` of the pass to at least `bytes` (its contents
+// are not kept).  The previous pass has finished: every call waits for its
+// own work before returning, and drains the streams before starting.
+ss_status ensure_buf(ss_handle *h, int role, size_t bytes) {
+  ss_host_pass &hp = h->host;
+  bytes = std::max<size_t>(bytes, 16);
+  if (hp.cap[role] >= bytes) return SS_OK;
+  cudaFree(hp.buf[role]);
+  hp.buf[role] = nullptr;
+  hp.cap[role] = 0;
+  S_CUDA(cudaMalloc(&hp.buf[role], bytes));
+  hp.cap[role] = bytes;
+  return SS_OK;
+}
+
 template <typename T>
-ss_status upload(ss_handle *h, T **dst, const T *src, int64_t n, cudaStream_t s) {
-  S_CUDA(cudaMalloc(dst, sizeof(T) * (size_t)std::max<int64_t>(n, 1)));
-  if (n > 0) S_CUDA(cudaMemcpyAsync(*dst, src, sizeof(T) * (size_t)n, cudaMemcpyHostToDevice, s));
+ss_status upload(ss_handle *h, int role, const T *src, int64_t n) {
+  ss_status st = ensure_buf(h, role, sizeof(T) * (size_t)n);
+  if (st != SS_OK) return st;
+  if (n > 0)
+    S_CUDA(cudaMemcpyAsync(h->host.buf[role], src, sizeof(T) * (size_t)n, cudaMemcpyHostToDevice,
+                           h->host.comp));
+  return SS_OK;
+}
+
+// Waits (with the deadline) until everything queued on the pass's streams has run.
+ss_status drain(ss_handle *h, int32_t timeout_ms) {
+  ss_host_pass &hp = h->host;
+  for (cudaStream_t s : {hp.comp, hp.copy}) {
+    S_CUDA(cudaEventRecord(hp.finished, s));
+    const ss_status st = wait_event(h, hp.finished, timeout_ms, "ss_bulk_cosine_host");
+    if (st != SS_OK) return st;
+  }
+  return SS_OK;
+}
+
+ss_status ensure_sync_objects(ss_handle *h, int ring) {
+  ss_host_pass &hp = h->host;
+  if (!hp.comp) S_CUDA(cudaStreamCreateWithFlags(&hp.comp, cudaStreamNonBlocking));
+  if (!hp.copy) S_CUDA(cudaStreamCreateWithFlags(&hp.copy, cudaStreamNonBlocking));
+  if (!hp.finished) S_CUDA(cudaEventCreateWithFlags(&hp.finished, cudaEventDisableTiming));
+  for (int b = 0; b < 2; ++b) {
+    if (!hp.done[b]) S_CUDA(cudaEventCreateWithFlags(&hp.done[b], cudaEventDisableTiming));
+    if (!hp.out_free[b]) S_CUDA(cudaEventCreateWithFlags(&hp.out_free[b], cudaEventDisableTiming));
+  }
+  while ((int)hp.copied.size() < ring) {
+    cudaEvent_t e = nullptr;
+    S_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    hp.copied.push_back(e);
+  }
+  return SS_OK;
+}
+
+ss_status ensure_ring(ss_handle *h, int ring, size_t bytes) {
+  ss_host_pass &hp = h->host;
+  if (hp.slot_bytes < bytes) {
+    for (float *p : hp.slots) cudaFreeHost(p);
+    hp.slots.clear();
+    hp.slot_bytes = bytes;
+  }
+  while ((int)hp.slots.size() < ring) {
+    float *p = nullptr;
+    S_CUDA(cudaHostAlloc(&p, hp.slot_bytes, cudaHostAllocDefault));
+    hp.slots.push_back(p);
+  }
   return SS_OK;
 }
 
 }  // namespace
+
+void free_host_pass(ss_host_pass &hp) {
+  if (hp.comp) cudaStreamSynchronize(hp.comp);
+  if (hp.copy) cudaStreamSynchronize(hp.copy);
+  for (float *p : hp.slots) cudaFreeHost(p);
+  hp.slots.clear();
+  hp.slot_bytes = 0;
+  for (cudaEvent_t e : hp.copied) cudaEventDestroy(e);
+  hp.copied.clear();
+  for (int b = 0; b < 2; ++b) {
+    if (hp.done[b]) cudaEventDestroy(hp.done[b]);
+    if (hp.out_free[b]) cudaEventDestroy(hp.out_free[b]);
+    hp.done[b] = hp.out_free[b] = nullptr;
+  }
+  if (hp.finished) cudaEventDestroy(hp.finished);
+  hp.finished = nullptr;
+  for (int r = 0; r < ss_host_pass::kBuffers; ++r) {
+    cudaFree(hp.buf[r]);
+    hp.buf[r] = nullptr;
+    hp.cap[r] = 0;
+  }
+  if (hp.comp) cudaStreamDestroy(hp.comp);
+  if (hp.copy) cudaStreamDestroy(hp.copy);
+  hp.comp = hp.copy = nullptr;
+}
 
 extern "C" ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *qh, const ss_csr *ih,
                                          float *out_host, int64_t ld_out,
@@ -143,80 +206,89 @@ extern "C" ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *qh, const s
   const int64_t n_q = qh->n_rows, n_i = ih->n_rows, C = h->chunk_rows;
   if (n_q == 0 || n_i == 0) return SS_OK;
   S_CUDA(cudaSetDevice(h->device));
+  const int R = ring_depth;
+  if ((st = ensure_sync_objects(h, R)) != SS_OK) return st;
+  if ((st = drain(h, timeout_ms)) != SS_OK) return st;
+  ss_host_pass &hp = h->host;
 
-  Pass p;
-  S_CUDA(cudaStreamCreateWithFlags(&p.comp, cudaStreamNonBlocking));
-  S_CUDA(cudaStreamCreateWithFlags(&p.copy, cudaStreamNonBlocking));
-  if ((st = upload(h, &p.q_indptr, qh->indptr, n_q + 1, p.comp)) != SS_OK) return st;
-  if ((st = upload(h, &p.q_idx, qh->indices, qh->nnz, p.comp)) != SS_OK) return st;
-  if ((st = upload(h, &p.q_val, qh->values, qh->nnz, p.comp)) != SS_OK) return st;
-  if ((st = upload(h, &p.i_indptr, ih->indptr, n_i + 1, p.comp)) != SS_OK) return st;
-  if ((st = upload(h, &p.i_idx, ih->indices, ih->nnz, p.comp)) != SS_OK) return st;
-  if ((st = upload(h, &p.i_val, ih->values, ih->nnz, p.comp)) != SS_OK) return st;
-  S_CUDA(cudaMalloc(&p.inv_q, sizeof(float) * (size_t)n_q));
-  S_CUDA(cudaMalloc(&p.inv_i, sizeof(float) * (size_t)n_i));
-  const ss_csr qd = {p.q_indptr, p.q_idx, p.q_val, n_q, qh->nnz, h->dim};
-  const ss_csr id = {p.i_indptr, p.i_idx, p.i_val, n_i, ih->nnz, h->dim};
-  void *vs = reinterpret_cast<void *>(p.comp);
-  if ((st = ss_row_norms(h, &qd, p.inv_q, vs)) != SS_OK) return st;
-  if ((st = ss_row_norms(h, &id, p.inv_i, vs)) != SS_OK) return st;
-
-  // Direct copies when the caller's output is page-locked and nobody else
-  // needs the tile; otherwise go through the pinned ring.
-  bool direct = false;
+  // Direct stores when the caller's output is page-locked, the device can
+  // address it, and nobody else needs the tile; otherwise the ring.
+  float *out_dev = nullptr;
   if (out_host && !consumer) {
     cudaPointerAttributes attr;
-    if (cudaPointerGetAttributes(&attr, out_host) == cudaSuccess && attr.type == cudaMemoryTypeHost)
-      direct = true;
+    if (cudaPointerGetAttributes(&attr, out_host) == cudaSuccess && attr.type == cudaMemoryTypeHost &&
+        attr.devicePointer)
+      out_dev = static_cast<float *>(attr.devicePointer);
     cudaGetLastError();
   }
-  const int64_t width_max = std::min<int64_t>(C, n_i);
-  const int R = ring_depth;
-  for (int b = 0; b < 2; ++b) {
-    S_CUDA(cudaMalloc(&p.dbuf[b], sizeof(float) * (size_t)(n_q * width_max)));
-    S_CUDA(cudaEventCreateWithFlags(&p.done[b], cudaEventDisableTiming));
-    S_CUDA(cudaEventCreateWithFlags(&p.dbuf_free[b], cudaEventDisableTiming));
-  }
-  p.copied.assign(R, nullptr);
-  for (int r = 0; r < R; ++r) S_CUDA(cudaEventCreateWithFlags(&p.copied[r], cudaEventDisableTiming));
-  if (!direct) {
-    p.slots.assign(R, nullptr);
-    for (int r = 0; r < R; ++r)
-      S_CUDA(cudaHostAlloc(&p.slots[r], sizeof(float) * (size_t)(n_q * width_max), cudaHostAllocDefault));
+
+  using HP = ss_host_pass;
+  if ((st = upload(h, HP::kQPtr, qh->indptr, n_q + 1)) != SS_OK) return st;
+  if ((st = upload(h, HP::kQIdx, qh->indices, qh->nnz)) != SS_OK) return st;
+  if ((st = upload(h, HP::kQVal, qh->values, qh->nnz)) != SS_OK) return st;
+  if ((st = upload(h, HP::kIPtr, ih->indptr, n_i + 1)) != SS_OK) return st;
+  if ((st = upload(h, HP::kIIdx, ih->indices, ih->nnz)) != SS_OK) return st;
+  if ((st = upload(h, HP::kIVal, ih->values, ih->nnz)) != SS_OK) return st;
+  if ((st = ensure_buf(h, HP::kInvQ, sizeof(float) * (size_t)n_q)) != SS_OK) return st;
+  if ((st = ensure_buf(h, HP::kInvI, sizeof(float) * (size_t)n_i)) != SS_OK) return st;
+  float *inv_q = static_cast<float *>(hp.buf[HP::kInvQ]);
+  float *inv_i = static_cast<float *>(hp.buf[HP::kInvI]);
+  const ss_csr qd = {static_cast<const int64_t *>(hp.buf[HP::kQPtr]),
+                     static_cast<const int32_t *>(hp.buf[HP::kQIdx]),
+                     static_cast<const float *>(hp.buf[HP::kQVal]), n_q, qh->nnz, h->dim};
+  const ss_csr id = {static_cast<const int64_t *>(hp.buf[HP::kIPtr]),
+                     static_cast<const int32_t *>(hp.buf[HP::kIIdx]),
+                     static_cast<const float *>(hp.buf[HP::kIVal]), n_i, ih->nnz, h->dim};
+  void *vs = reinterpret_cast<void *>(hp.comp);
+  if ((st = ss_row_norms(h, &qd, inv_q, vs)) != SS_OK) return st;
+  if ((st = ss_row_norms(h, &id, inv_i, vs)) != SS_OK) return st;
+  const int64_t n_chunks = (n_i + C - 1) / C;
+
+  if (out_dev) {
+    for (int64_t c = 0; c < n_chunks; ++c) {
+      const int64_t rb = c * C, re = std::min(rb + C, n_i);
+      ss_index *idx = nullptr;
+      if ((st = ss_build_item_index(h, &id, rb, re, &idx, vs)) != SS_OK) return st;
+      if ((st = ss_score_chunk(h, &qd, inv_q, idx, inv_i + rb, out_dev + rb, ld_out, vs)) != SS_OK)
+        return st;
+    }
+    if ((st = drain(h, timeout_ms)) != SS_OK) return st;
+    return ss_check_device(h, vs);
   }
 
-  const int64_t n_chunks = (n_i + C - 1) / C;
+  const int64_t width_max = std::min<int64_t>(C, n_i);
+  const size_t tile_bytes = sizeof(float) * (size_t)(n_q * width_max);
+  if ((st = ensure_buf(h, HP::kOut0, tile_bytes)) != SS_OK) return st;
+  if ((st = ensure_buf(h, HP::kOut1, tile_bytes)) != SS_OK) return st;
+  if ((st = ensure_ring(h, R, tile_bytes)) != SS_OK) return st;
+  float *dbuf[2] = {static_cast<float *>(hp.buf[HP::kOut0]), static_cast<float *>(hp.buf[HP::kOut1])};
+
   int64_t delivered = 0;
   auto deliver = [&](int64_t c) -> ss_status {
     const int64_t rb = c * C, re = std::min(rb + C, n_i), w = re - rb;
-    ss_status s2 = wait_event(h, p.copied[c % R], timeout_ms, "ss_bulk_cosine_host copy");
+    ss_status s2 = wait_event(h, hp.copied[c % R], timeout_ms, "ss_bulk_cosine_host copy");
     if (s2 != SS_OK) return s2;
-    if (!direct) {
-      const float *slot = p.slots[c % R];
-      if (out_host) scatter_rows(out_host, ld_out, rb, slot, w, w, n_q);
-      if (consumer && consumer(user, c, rb, re, slot, w, n_q) != 0)
-        return sfail(h, SS_ERR_INVALID_ARG, "ss_bulk_cosine_host: consumer stopped the pass");
-    }
+    const float *slot = hp.slots[c % R];
+    if (out_host) scatter_rows(out_host, ld_out, rb, slot, w, w, n_q);
+    if (consumer && consumer(user, c, rb, re, slot, w, n_q) != 0)
+      return sfail(h, SS_ERR_INVALID_ARG, "ss_bulk_cosine_host: consumer stopped the pass");
     return SS_OK;
   };
 
   for (int64_t c = 0; c < n_chunks; ++c) {
     const int b = (int)(c & 1);
     const int64_t rb = c * C, re = std::min(rb + C, n_i), w = re - rb;
-    if (c >= 2) S_CUDA(cudaStreamWaitEvent(p.comp, p.dbuf_free[b], 0));
+    if (c >= 2) S_CUDA(cudaStreamWaitEvent(hp.comp, hp.out_free[b], 0));
     ss_index *idx = nullptr;
     if ((st = ss_build_item_index(h, &id, rb, re, &idx, vs)) != SS_OK) return st;
-    if ((st = ss_score_chunk(h, &qd, p.inv_q, idx, p.inv_i + rb, p.dbuf[b], w, vs)) != SS_OK)
-      return st;
-    S_CUDA(cudaEventRecord(p.done[b], p.comp));
-    S_CUDA(cudaStreamWaitEvent(p.copy, p.done[b], 0));
+    if ((st = ss_score_chunk(h, &qd, inv_q, idx, inv_i + rb, dbuf[b], w, vs)) != SS_OK) return st;
+    S_CUDA(cudaEventRecord(hp.done[b], hp.comp));
+    S_CUDA(cudaStreamWaitEvent(hp.copy, hp.done[b], 0));
     // Slot c % R was last used by chunk c - R, delivered before this point.
-    float *dst = direct ? out_host + rb : p.slots[c % R];
-    const int64_t dld = direct ? ld_out : w;
-    S_CUDA(cudaMemcpy2DAsync(dst, sizeof(float) * (size_t)dld, p.dbuf[b], sizeof(float) * (size_t)w,
-                             sizeof(float) * (size_t)w, (size_t)n_q, cudaMemcpyDeviceToHost, p.copy));
-    S_CUDA(cudaEventRecord(p.copied[c % R], p.copy));
-    S_CUDA(cudaEventRecord(p.dbuf_free[b], p.copy));
+    S_CUDA(cudaMemcpyAsync(hp.slots[c % R], dbuf[b], sizeof(float) * (size_t)(n_q * w),
+                           cudaMemcpyDeviceToHost, hp.copy));
+    S_CUDA(cudaEventRecord(hp.copied[c % R], hp.copy));
+    S_CUDA(cudaEventRecord(hp.out_free[b], hp.copy));
     // Keep R - 1 chunks in flight; deliver the oldest.
     while (delivered <= c - (R - 1)) {
       if ((st = deliver(delivered)) != SS_OK) return st;

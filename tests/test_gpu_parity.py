@@ -349,6 +349,24 @@ def test_bulk_cosine_host_paths_agree(sec):
     assert _max_err(ref, oracle.cosine(Q, I)) <= TOL
 
 
+def test_bulk_cosine_host_reuses_workspace_across_sizes(sec):
+    # The pass keeps its buffers between calls: shrink, grow and shrink again,
+    # once into an unaligned window of a larger page-locked array (direct
+    # stores through an interior device address, 4-byte stores).
+    cfg = CONFIGS["d65k_q1k_i10k"]
+    small = (generate_rows(cfg, 0, 0, 37), generate_rows(cfg, 1, 0, 1500))
+    large = (generate_rows(cfg, 0, 100, 260), generate_rows(cfg, 1, 2000, 6100))
+    with sec.SparseCosine(cfg.dim, chunk_rows=1024) as h:
+        for Q, I in (small, large, small):
+            ref = _gpu_cosine(sec, Q, I, chunk_rows=1024)
+            big = torch.full((Q.n_rows, I.n_rows + 9), float("nan"), dtype=torch.float32).pin_memory()
+            window = big[:, 5:5 + I.n_rows]
+            h.bulk_cosine_host(Q, I, out=window, ring_depth=2)
+            got = big.numpy()
+            assert np.array_equal(got[:, 5:5 + I.n_rows].view(np.int32), ref.view(np.int32))
+            assert np.isnan(got[:, :5]).all() and np.isnan(got[:, 5 + I.n_rows:]).all()
+
+
 def test_bulk_cosine_host_consumer_can_stop(sec):
     from sparse_embedding_exact_gb300 import SparseCosError
 
