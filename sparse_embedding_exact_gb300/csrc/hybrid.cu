@@ -174,24 +174,36 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *red, int *total)
 
 // Open-addressing insert / find in the image-building hash (kImgSlots).
 // Probing starts at the first slot of the key's aligned group of four, so a
-// reader that loads whole groups finds most keys in the first one.
+// reader that loads whole groups finds most keys in the first one.  Insert
+// claims slots with compare-and-swap; find reads a group with one 16-byte
+// load.  Every slot between a key's home and the key is occupied (slots go
+// from empty to a key once and never change again), so a group that lacks
+// the key but has an empty slot ends a search.
 __device__ __forceinline__ uint32_t img_home(int32_t k) { return hash_a(k, kImgSlotsBits) & ~3u; }
-__device__ __forceinline__ int img_insert(int *keys, int32_t k) {
+__device__ __forceinline__ int img_insert(int *keys, uint32_t *bits, int32_t k) {
   uint32_t s = img_home(k);
   for (int n = 0; n < kImgSlots; ++n) {
     const int prev = atomicCAS(&keys[s], -1, k);
-    if (prev == -1 || prev == k) return (int)s;
+    if (prev == -1) {  // this thread added k: mark it in the membership bitmap
+      const uint32_t bb = hash_b(k, kImgBitsLog2);
+      atomicOr(&bits[bb >> 5], 1u << (bb & 31));
+      return (int)s;
+    }
+    if (prev == k) return (int)s;
     s = (s + 1) & (kImgSlots - 1);
   }
   return -1;
 }
 __device__ __forceinline__ int img_find(const int *keys, int32_t k) {
-  uint32_t s = img_home(k);
-  for (int n = 0; n < kImgSlots; ++n) {
-    const int key = keys[s];
-    if (key == k) return (int)s;
-    if (key == -1) return -1;
-    s = (s + 1) & (kImgSlots - 1);
+  uint32_t base = img_home(k);
+  for (int n = 0; n < kImgSlots / 4; ++n) {
+    const int4 g = *reinterpret_cast<const int4 *>(keys + base);
+    if (g.x == k) return (int)base;
+    if (g.y == k) return (int)base + 1;
+    if (g.z == k) return (int)base + 2;
+    if (g.w == k) return (int)base + 3;
+    if (g.x == -1 || g.y == -1 || g.z == -1 || g.w == -1) return -1;
+    base = (base + 4) & (kImgSlots - 1);
   }
   return -1;
 }
@@ -240,6 +252,9 @@ constexpr int kBldOffVal = kBldOffIdx + kBldStage * 4;
 constexpr int kBuildSmem = kBldOffVal + kBldStage * 4;
 static_assert(kBldOffIdx % 16 == 0 && kBldOffVal % 16 == 0, "staging buffers must stay 16-byte aligned");
 static_assert(kImgECap <= kHotMax * kTI * 4, "segment items are staged in the slab's space");
+constexpr int kItemsPerWarp = kTI / (kBThreads / 32);  // builder: consecutive items per warp
+static_assert(kItemsPerWarp * (kBThreads / 32) == kTI, "warps cover the tile's items exactly");
+constexpr int32_t kCodeHot = -1;  // code of a hot (or unplaced) nonzero in the builder
 
 __device__ __forceinline__ int bblock_sum(int v, int *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -306,6 +321,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
   __shared__ int heavy_base, img_fail;
   __shared__ int heavy_off[kTI];
   __shared__ uint32_t bits_s[(1 << kImgBitsLog2) / 32];
+  __shared__ int cum_s[kBThreads / 32][kItemsPerWarp + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
   const int t = blockIdx.x;
@@ -336,39 +352,58 @@ __global__ void __launch_bounds__(kBThreads, 1)
   auto key_at = [&](int64_t p) -> int32_t { return staged ? idx_s[p - pa] : __ldg(indices + p); };
   auto val_at = [&](int64_t p) -> float { return staged ? val_s[p - pa] : __ldg(values + p); };
 
-  // Pass 1: hot values into the slab; cold dims into the image hash.
-  for (int it = warp; it < kTI; it += kBThreads / 32) {
-    int cold = 0;
-    if (it < n_items) {
-      const int64_t pb = ptr_s[it], pe = ptr_s[it + 1];
-      for (int64_t p = pb + lane; p < pe; p += 32) {
-        const int32_t k = key_at(p);
-        const int h = hot_find(hkeys, hvals, k);
-        if (h >= 0) {
-          slab_s[h * kTI + it] = val_at(p);
-        } else {
-          ++cold;
-          const int slot = img_insert(ikeys, k);
-          if (slot < 0) img_fail = 1;
-          else atomicAdd(&icnt[slot], 1);
-        }
-      }
-    }
+  // Pass 1: hot values into the slab; cold dims into the image hash.  The
+  // atomic that counts a cold entry's dimension also gives the entry's rank
+  // within that dimension's segment; on a staged tile the entry's staged key
+  // is replaced by its code (slot | rank << 16, or kCodeHot), so the scatter
+  // needs neither lookups nor atomics.  Warp w takes items w, w + 32, ...,
+  // whose rows its lanes run through as one list, 32 entries at a time (so
+  // the block works through the items roughly in ascending order, and each
+  // segment lists its items roughly ascending, which spreads the scorer's
+  // accumulator accesses over the banks).
+  int32_t *code_s = reinterpret_cast<int32_t *>(bsm + kBldOffIdx);
+  int *cum = cum_s[warp];  // cum[m]: entries of the warp's items before item w + 32 m
+  {
+    const int item = warp + 32 * lane;
+    int len = (lane < kItemsPerWarp && item < n_items) ? (int)(ptr_s[item + 1] - ptr_s[item]) : 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cold += __shfl_xor_sync(0xffffffffu, cold, o);
-    if (lane == 0) cold_n[it] = cold;
+    for (int o = 1; o < kItemsPerWarp; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, len, o);
+      if (lane >= o) len += v;
+    }
+    if (lane < kItemsPerWarp) cum[lane + 1] = len;
+    if (lane == 0) cum[0] = 0;
+    __syncwarp();
+  }
+  const int warp_entries = cum[kItemsPerWarp];
+  {
+    int m = 0;
+    for (int f = lane; f < warp_entries; f += 32) {
+      while (cum[m + 1] <= f) ++m;  // ends below kItemsPerWarp, since f < cum[kItemsPerWarp]
+      const int it = warp + 32 * m;
+      const int64_t p = ptr_s[it] + (f - cum[m]);
+      const int32_t k = key_at(p);
+      const int h = hot_find(hkeys, hvals, k);
+      int32_t code = kCodeHot;
+      if (h >= 0) {
+        slab_s[h * kTI + it] = val_at(p);
+      } else {
+        const int slot = img_insert(ikeys, bits_s, k);
+        if (slot < 0) img_fail = 1;
+        else code = slot | (atomicAdd(&icnt[slot], 1) << 16);
+      }
+      if (staged) code_s[p - pa] = code;
+    }
   }
   __syncthreads();
   {
     float *dst = slab + (size_t)t * kHotMax * kTI;
     for (int j = tid; j < H * kTI; j += kBThreads) dst[j] = slab_s[j];
   }
-  const int my_cold = tid < kTI ? cold_n[tid] : 0;
-  const int sum_cold = bblock_sum(my_cold, red);  // its barriers also end the slab's reads
   unsigned char *img = image + (size_t)t * kImgBytes;
   int32_t *hdr = reinterpret_cast<int32_t *>(img);
 
-  // ---- image path
+  // ---- image path (the scans' barriers also end the slab's reads above)
   constexpr int kPer = kImgSlots / kBThreads;
   int occ = 0, ent = 0;
   for (int j = 0; j < kPer; ++j) {
@@ -379,7 +414,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
   int D = 0, E = 0;
   (void)bblock_exclusive_scan(occ, red, &D);
   int e_run = bblock_exclusive_scan(ent, red, &E);
-  const bool fits = !img_fail && sum_cold <= kImgECap && D <= kImgDCap && E == sum_cold;
+  const bool fits = !img_fail && E <= kImgECap && D <= kImgDCap;
   if (fits) {
     uint2 *gslot = reinterpret_cast<uint2 *>(img + kImgOffSlots);
     for (int j = 0; j < kPer; ++j) {
@@ -387,10 +422,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
       if (ikeys[s] >= 0) {
         const int c = icnt[s];
         gslot[s] = make_uint2((uint32_t)ikeys[s], (uint32_t)e_run | ((uint32_t)(e_run + c) << 16));
-        icnt[s] = e_run;  // now the fill cursor of this segment
+        icnt[s] = e_run;  // now the segment's start (the fill cursor on the unstaged path)
         e_run += c;
-        const uint32_t bb = hash_b(ikeys[s], kImgBitsLog2);
-        atomicOr(&bits_s[bb >> 5], 1u << (bb & 31));
       } else {
         gslot[s] = make_uint2(0xffffffffu, 0u);
       }
@@ -405,14 +438,28 @@ __global__ void __launch_bounds__(kBThreads, 1)
     uint32_t *gbits = reinterpret_cast<uint32_t *>(img + kImgOffBits);
     for (int w = tid; w < (1 << kImgBitsLog2) / 32; w += kBThreads) gbits[w] = bits_s[w];
     float *gval = reinterpret_cast<float *>(img + kImgOffVal);
-    for (int it = warp; it < n_items; it += kBThreads / 32) {
-      const int64_t pb = ptr_s[it], pe = ptr_s[it + 1];
-      for (int64_t p = pb + lane; p < pe; p += 32) {
-        const int32_t k = key_at(p);
-        if (hot_find(hkeys, hvals, k) >= 0) continue;
-        const int pos = atomicAdd(&icnt[img_find(ikeys, k)], 1);
+    if (staged) {
+      int m = 0;
+      for (int f = lane; f < warp_entries; f += 32) {
+        while (cum[m + 1] <= f) ++m;
+        const int it = warp + 32 * m;
+        const int64_t p = ptr_s[it] + (f - cum[m]);
+        const int32_t code = code_s[p - pa];
+        if (code == kCodeHot) continue;
+        const int pos = icnt[code & 0xffff] + (code >> 16);
         item_s[pos] = (uint8_t)it;
-        gval[pos] = val_at(p);
+        gval[pos] = val_s[p - pa];
+      }
+    } else {
+      for (int it = warp; it < n_items; it += kBThreads / 32) {
+        const int64_t pb = ptr_s[it], pe = ptr_s[it + 1];
+        for (int64_t p = pb + lane; p < pe; p += 32) {
+          const int32_t k = __ldg(indices + p);
+          if (hot_find(hkeys, hvals, k) >= 0) continue;
+          const int pos = atomicAdd(&icnt[img_find(ikeys, k)], 1);
+          item_s[pos] = (uint8_t)it;
+          gval[pos] = __ldg(values + p);
+        }
       }
     }
     __syncthreads();
@@ -426,6 +473,20 @@ __global__ void __launch_bounds__(kBThreads, 1)
   int heavy_total = 0;
   bool heavy_ok = true;
   if (!fits) {
+    // Cold nonzeros per item (keys read from the CSR itself: a staged tile's
+    // keys have been replaced by codes).
+    for (int it = warp; it < kTI; it += kBThreads / 32) {
+      int cold = 0;
+      if (it < n_items)
+        for (int64_t p = ptr_s[it] + lane; p < ptr_s[it + 1]; p += 32)
+          cold += hot_find(hkeys, hvals, __ldg(indices + p)) < 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cold += __shfl_xor_sync(0xffffffffu, cold, o);
+      if (lane == 0) cold_n[it] = cold;
+    }
+    __syncthreads();
+    const int my_cold = tid < kTI ? cold_n[tid] : 0;
+    const int sum_cold = bblock_sum(my_cold, red);
     // Items far above the tile's mean go to the heavy list.
     const int mean = n_items > 0 ? sum_cold / n_items : 0;
     const int thr = min(kEllMaxW, 2 * mean + 32);
@@ -463,7 +524,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
           int32_t k = -1;
           bool is_cold = false;
           if (pp < pe) {
-            k = key_at(pp);
+            k = __ldg(indices + pp);
             is_cold = hot_find(hkeys, hvals, k) < 0;
           }
           const unsigned cm = __ballot_sync(0xffffffffu, is_cold);
