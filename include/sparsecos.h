@@ -92,8 +92,10 @@ ss_status ss_create(ss_handle **out, int device, int64_t dim, int32_t chunk_rows
 /*
  * Row norms (section 5.2, computed once, section 4.4): for every row r of m
  * (device CSR), inv_norms[r] = 1 / sqrt(sum_j values[j]^2) over the row's
- * stored values, or 0 when that sum is 0.  The sum of squares is taken in
- * double precision and the reciprocal square root rounded once to float.
+ * stored values, or 0 when that sum is 0.  The squares are summed exactly
+ * split into pairs of floats (about 48 significant bits), so the result is
+ * within one unit in the last place of the correctly rounded value; rows
+ * whose squares leave the float range are rescaled by a power of two.
  * inv_norms: device, float32[m->n_rows], written.
  * With SS_VALIDATE the CSR is checked first (SS_ERR_UNSORTED,
  * SS_ERR_OUT_OF_RANGE) and the call synchronises `stream`.
@@ -104,7 +106,8 @@ ss_status ss_row_norms(ss_handle *h, const ss_csr *m, float *inv_norms, void *st
  * Per-chunk inverted index (the chunk's CSR turned into lists by dimension):
  * indexes item rows [row_begin, row_end) of `items` (device CSR), with
  * 0 < row_end - row_begin <= chunk_rows.  The index is owned by the handle
- * and stays valid until the next ss_build_item_index or ss_destroy on it;
+ * and stays valid until the next build (ss_build_item_index or
+ * ss_build_item_indexes) or ss_destroy on it;
  * `*out` receives a pointer to it.  Work on `stream` must not overlap a
  * score call still using the previous index (queue both on one stream).
  * Errors: SS_ERR_INVALID_ARG, SS_ERR_LIMIT, SS_ERR_OOM, SS_ERR_CUDA.
@@ -126,6 +129,28 @@ ss_status ss_build_item_index(ss_handle *h, const ss_csr *items, int64_t row_beg
 ss_status ss_score_chunk(ss_handle *h, const ss_csr *queries, const float *inv_q,
                          const ss_index *idx, const float *inv_i, float *out, int64_t ld_out,
                          void *stream);
+
+/*
+ * Number of chunks one ss_build_item_indexes call can build: enough that the
+ * builder's blocks (one per 256-item tile) cover the GPU's SMs, at most 8;
+ * always 1 with SS_ALGO_POSTING_LISTS.  Fixed at ss_create.
+ */
+int32_t ss_build_batch(const ss_handle *h);
+
+/*
+ * Builds, in one launch, the indexes of the consecutive chunks that split
+ * [row_begin, row_end) into pieces of chunk_rows items starting at row_begin
+ * (the last may be shorter); at most ss_build_batch(h) chunks, else
+ * SS_ERR_LIMIT.  out (host array of at least ss_build_batch(h) pointers)
+ * receives one handle-owned index per chunk, in order, and *n_out their
+ * number; each is scored with ss_score_chunk exactly as one from
+ * ss_build_item_index, and all stay valid until the next build on this
+ * handle or ss_destroy.  Results equal those of building the chunks one by
+ * one.  Errors: SS_ERR_INVALID_ARG (bad range, null pointers), SS_ERR_LIMIT,
+ * SS_ERR_CUDA.
+ */
+ss_status ss_build_item_indexes(ss_handle *h, const ss_csr *items, int64_t row_begin,
+                                int64_t row_end, ss_index **out, int32_t *n_out, void *stream);
 
 /*
  * The whole device-resident pass: splits the items into chunks of the

@@ -139,6 +139,27 @@ class SparseCosine:
                                                   _stream_ptr(stream)), "ss_build_item_index")
         return idx
 
+    @property
+    def build_batch(self) -> int:
+        """How many chunks one ``build_item_indexes`` call can build."""
+        return int(self._lib.ss_build_batch(self._h))
+
+    def build_item_indexes(self, items: DeviceCsr, row_begin: int, row_end: int, stream=None):
+        """Indexes of the chunks of ``chunk_rows`` items that split
+        [row_begin, row_end) (at most ``build_batch`` of them), built in one
+        launch; a list of (chunk_row_begin, chunk_row_end, index)."""
+        c = items.abi()
+        arr = (ctypes.c_void_p * max(1, self.build_batch))()
+        n = ctypes.c_int32(0)
+        self._check(self._lib.ss_build_item_indexes(self._h, ctypes.byref(c), int(row_begin),
+                                                    int(row_end), arr, ctypes.byref(n),
+                                                    _stream_ptr(stream)), "ss_build_item_indexes")
+        out = []
+        for k in range(n.value):
+            b = int(row_begin) + k * self.chunk_rows
+            out.append((b, min(b + self.chunk_rows, int(row_end)), ctypes.c_void_p(arr[k])))
+        return out
+
     def score_chunk(self, queries: DeviceCsr, inv_q: torch.Tensor, index, inv_i_chunk: torch.Tensor,
                     out: torch.Tensor, ld_out: int, stream=None):
         c = queries.abi()

@@ -49,6 +49,8 @@ SIGNATURES = {
     "ss_create": (_I32, [ctypes.POINTER(_P), ctypes.c_int, _I64, _I32, _I32]),
     "ss_row_norms": (_I32, [_P, _CSR, _P, _P]),
     "ss_build_item_index": (_I32, [_P, _CSR, _I64, _I64, ctypes.POINTER(_P), _P]),
+    "ss_build_batch": (_I32, [_P]),
+    "ss_build_item_indexes": (_I32, [_P, _CSR, _I64, _I64, ctypes.POINTER(_P), ctypes.POINTER(_I32), _P]),
     "ss_score_chunk": (_I32, [_P, _CSR, _P, _P, _P, _P, _I64, _P]),
     "ss_score_all": (_I32, [_P, _CSR, _P, _CSR, _P, _P, _I64, _P]),
     "ss_bulk_cosine_host": (_I32, [_P, _CSR, _CSR, _P, _I64, ss_chunk_consumer, _P, _I32, _I32]),

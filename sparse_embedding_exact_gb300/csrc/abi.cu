@@ -182,6 +182,13 @@ cudaError_t score(ss_handle *h, const ss_csr &q, const float *inv_q, const ss_in
   return e;
 }
 
+// Whether idx is one of the handle's current chunk indexes.
+bool owns_index(const ss_handle *h, const ss_index *idx) {
+  for (int k = 0; k < h->n_views; ++k)
+    if (idx == &h->views[k]) return true;
+  return false;
+}
+
 }  // namespace
 
 extern "C" {
@@ -228,14 +235,21 @@ ss_status ss_create(ss_handle **out, int device, int64_t dim, int32_t chunk_rows
     if (e == cudaSuccess) e = cudaMalloc(&h->scan_part, sizeof(int32_t) * (size_t)(h->scan_tiles + 1));
   } else {
     using namespace hyb;
-    h->max_tiles = (chunk_rows + kTI - 1) / kTI;
+    // One build launch covers enough chunks to give every SM a tile (a
+    // chunk alone has only chunk_rows / 256 tiles, one block each).
+    h->chunk_tiles = (chunk_rows + kTI - 1) / kTI;
+    const int sms = h->sm_count > 0 ? h->sm_count : 1;
+    h->build_batch = std::max(1, std::min(kMaxBuildBatch, (sms + h->chunk_tiles - 1) / h->chunk_tiles));
+    h->max_tiles = h->build_batch * h->chunk_tiles;
     const size_t tiles = (size_t)h->max_tiles;
     if (e == cudaSuccess) e = cudaMalloc(&h->hot, sizeof(int32_t) * (1 + kHotMax));
     if (e == cudaSuccess) e = cudaMemset(h->hot, 0, sizeof(int32_t) * (1 + kHotMax));
     if (e == cudaSuccess) e = cudaMalloc(&h->slab, sizeof(float) * tiles * kHotMax * kTI);
     if (e == cudaSuccess) e = cudaMalloc(&h->ell, sizeof(int2) * tiles * kEllMaxW * kTI);
     if (e == cudaSuccess) e = cudaMalloc(&h->meta, sizeof(int32_t) * tiles * kMetaInts);
-    if (e == cudaSuccess) e = cudaMalloc(&h->counters, sizeof(int32_t) * (2 + tiles));
+    const size_t n_counters = 1 + (size_t)h->build_batch * (1 + h->chunk_tiles);
+    if (e == cudaSuccess) e = cudaMalloc(&h->counters, sizeof(int32_t) * n_counters);
+    if (e == cudaSuccess) e = cudaMemset(h->counters, 0, sizeof(int32_t) * n_counters);
     if (e == cudaSuccess) e = cudaMalloc(&h->image, (size_t)kImgBytes * tiles);
   }
   if (e != cudaSuccess) {
@@ -275,7 +289,7 @@ ss_status ss_invalidate(ss_handle *h) {
 
 ss_status ss_index_stats(ss_handle *h, const ss_index *idx, int64_t *stats, void *stream) {
   if (!h) return SS_ERR_INVALID_ARG;
-  if (!idx || idx != &h->index || !stats)
+  if (!idx || !owns_index(h, idx) || !stats)
     return fail(h, SS_ERR_INVALID_ARG, "ss_index_stats: bad index or output");
   ss_status st = set_device(h);
   if (st != SS_OK) return st;
@@ -343,7 +357,30 @@ ss_status ss_build_item_index(ss_handle *h, const ss_csr *items, int64_t row_beg
                 (long long)(row_end - row_begin), h->chunk_rows);
   if ((st = set_device(h)) != SS_OK) return st;
   if ((st = build_chunk(h, *items, row_begin, row_end, as_stream(stream))) != SS_OK) return st;
-  *out = &h->index;
+  *out = &h->views[0];
+  return SS_OK;
+}
+
+int32_t ss_build_batch(const ss_handle *h) { return h ? h->build_batch : 0; }
+
+ss_status ss_build_item_indexes(ss_handle *h, const ss_csr *items, int64_t row_begin,
+                                int64_t row_end, ss_index **out, int32_t *n_out, void *stream) {
+  if (!h) return SS_ERR_INVALID_ARG;
+  if (!out || !n_out) return fail(h, SS_ERR_INVALID_ARG, "ss_build_item_indexes: null out");
+  *n_out = 0;
+  ss_status st = check_csr_args(h, items, "ss_build_item_indexes");
+  if (st != SS_OK) return st;
+  if (row_begin < 0 || row_end <= row_begin || row_end > items->n_rows)
+    return fail(h, SS_ERR_INVALID_ARG, "ss_build_item_indexes: bad row range [%lld, %lld)",
+                (long long)row_begin, (long long)row_end);
+  const int64_t n_chunks = (row_end - row_begin + h->chunk_rows - 1) / h->chunk_rows;
+  if (n_chunks > h->build_batch)
+    return fail(h, SS_ERR_LIMIT, "ss_build_item_indexes: %lld chunks exceed the build batch %d",
+                (long long)n_chunks, h->build_batch);
+  if ((st = set_device(h)) != SS_OK) return st;
+  if ((st = build_chunk(h, *items, row_begin, row_end, as_stream(stream))) != SS_OK) return st;
+  for (int k = 0; k < h->n_views; ++k) out[k] = &h->views[k];
+  *n_out = h->n_views;
   return SS_OK;
 }
 
@@ -353,7 +390,7 @@ ss_status ss_score_chunk(ss_handle *h, const ss_csr *queries, const float *inv_q
   if (!h) return SS_ERR_INVALID_ARG;
   ss_status st = check_csr_args(h, queries, "ss_score_chunk");
   if (st != SS_OK) return st;
-  if (!idx || idx != &h->index)
+  if (!idx || !owns_index(h, idx))
     return fail(h, SS_ERR_INVALID_ARG, "ss_score_chunk: index does not belong to this handle");
   if (queries->n_rows > 0 && (!inv_q || !inv_i || !out))
     return fail(h, SS_ERR_INVALID_ARG, "ss_score_chunk: null norms or output");
@@ -378,10 +415,15 @@ ss_status ss_score_all(ss_handle *h, const ss_csr *queries, const float *inv_q,
   if (!inv_q || !inv_i || !out) return fail(h, SS_ERR_INVALID_ARG, "ss_score_all: null pointer");
   if ((st = set_device(h)) != SS_OK) return st;
   cudaStream_t s = as_stream(stream);
-  for (int64_t rb = 0; rb < items->n_rows; rb += h->chunk_rows) {
-    const int64_t re = std::min<int64_t>(rb + h->chunk_rows, items->n_rows);
-    if ((st = build_chunk(h, *items, rb, re, s)) != SS_OK) return st;
-    SS_CUDA(h, score(h, *queries, inv_q, h->index, inv_i + rb, out + rb, ld_out, s));
+  // One build per batch of chunks, then each chunk scored on its own.
+  const int64_t span = (int64_t)h->chunk_rows * h->build_batch;
+  for (int64_t bb = 0; bb < items->n_rows; bb += span) {
+    const int64_t be = std::min<int64_t>(bb + span, items->n_rows);
+    if ((st = build_chunk(h, *items, bb, be, s)) != SS_OK) return st;
+    for (int k = 0; k < h->n_views; ++k) {
+      const ss_index &v = h->views[k];
+      SS_CUDA(h, score(h, *queries, inv_q, v, inv_i + v.row_begin, out + v.row_begin, ld_out, s));
+    }
   }
   return SS_OK;
 }

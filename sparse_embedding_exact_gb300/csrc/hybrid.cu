@@ -305,7 +305,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
                   int2 *__restrict__ ell, int32_t *__restrict__ meta,
                   int32_t *__restrict__ heavy_k, float *__restrict__ heavy_v,
                   uint8_t *__restrict__ heavy_item, int32_t *__restrict__ counters,
-                  int64_t heavy_cap, unsigned char *__restrict__ image, int32_t *status) {
+                  int64_t heavy_cap, unsigned char *__restrict__ image, int32_t *status,
+                  int32_t chunk_rows, int32_t chunk_tiles, int32_t n_chunks) {
   extern __shared__ __align__(16) unsigned char bsm[];
   float *slab_s = reinterpret_cast<float *>(bsm + kBldOffSlab);  // [kHotMax][kTI]
   uint8_t *item_s = bsm + kBldOffSlab;  // segment items, once the slab has been written out
@@ -324,9 +325,17 @@ __global__ void __launch_bounds__(kBThreads, 1)
   __shared__ int cum_s[kBThreads / 32][kItemsPerWarp + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
+  // Block t builds tile tl of chunk kc of the build (chunks of chunk_rows
+  // items from row_begin; only the last may be shorter).  Images, slabs,
+  // meta and ELL blocks are indexed by t; the chunk's overflow list is ovf.
   const int t = blockIdx.x;
-  const int64_t item0 = row_begin + (int64_t)t * kTI;
-  const int n_items = (int)min((int64_t)kTI, row_end - item0);
+  const int kc = min(t / chunk_tiles, n_chunks - 1);
+  const int tl = t - kc * chunk_tiles;
+  const int64_t chunk_begin = row_begin + (int64_t)kc * chunk_rows;
+  const int64_t chunk_end = min(chunk_begin + (int64_t)chunk_rows, row_end);
+  const int64_t item0 = chunk_begin + (int64_t)tl * kTI;
+  const int n_items = (int)min((int64_t)kTI, chunk_end - item0);
+  int32_t *ovf = counters + 1 + (size_t)kc * (1 + chunk_tiles);  // [0] count, [1..] tile numbers
   const int H = hot[0];
   if (tid <= n_items) ptr_s[tid] = indptr[item0 + tid];
   for (int w = tid; w < (1 << kImgBitsLog2) / 32; w += kBThreads) bits_s[w] = 0u;
@@ -496,8 +505,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
     if (tid == 0) {
       heavy_base = heavy_total > 0 ? atomicAdd(&counters[0], heavy_total) : 0;
       hdr[2] = 0;
-      const int c = atomicAdd(&counters[1], 1);
-      counters[2 + c] = t;
+      const int c = atomicAdd(&ovf[0], 1);
+      ovf[1 + c] = tl;
     }
     __syncthreads();
     const int64_t hbase = heavy_base;
@@ -1547,9 +1556,14 @@ cudaError_t launch_hot_select(ss_handle *h, const ss_csr &items, cudaStream_t s,
 
 cudaError_t launch_build_hybrid(ss_handle *h, const ss_csr &items, int64_t row_begin,
                                 int64_t row_end, cudaStream_t s) {
-  const int n_items = (int)(row_end - row_begin);
-  const int n_tiles = (n_items + kTI - 1) / kTI;
-  cudaError_t e = cudaMemsetAsync(h->counters, 0, 2 * sizeof(int32_t), s);
+  const int64_t C = h->chunk_rows;
+  const int T = h->chunk_tiles;
+  const int n_chunks = (int)((row_end - row_begin + C - 1) / C);
+  const int64_t last_len = row_end - (row_begin + (int64_t)(n_chunks - 1) * C);
+  const int n_tiles = (n_chunks - 1) * T + (int)((last_len + kTI - 1) / kTI);
+  h->n_views = 0;
+  if (n_chunks < 1 || n_chunks > h->build_batch || n_tiles > h->max_tiles) return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(h->counters, 0, sizeof(int32_t) * (1 + (size_t)n_chunks * (1 + T)), s);
   if (e != cudaSuccess) return e;
   static bool configured = false;
   if (!configured) {
@@ -1560,25 +1574,30 @@ cudaError_t launch_build_hybrid(ss_handle *h, const ss_csr &items, int64_t row_b
   k_build_tiles<<<n_tiles, kBThreads, kBuildSmem, s>>>(
       items.indptr, items.indices, items.values, row_begin, row_end, h->hot, h->slab, h->ell,
       h->meta, h->heavy_k, h->heavy_v, h->heavy_item, h->counters, h->heavy_cap, h->image,
-      h->d_status);
+      h->d_status, (int32_t)C, T, n_chunks);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  ss_index &ix = h->index;
-  ix.algo = ALGO_HYBRID;
-  ix.row_begin = row_begin;
-  ix.row_end = row_end;
-  ix.n_items = n_items;
-  ix.dim = h->dim;
-  ix.n_tiles = n_tiles;
-  ix.hot = h->hot;
-  ix.slab = h->slab;
-  ix.ell = h->ell;
-  ix.meta = h->meta;
-  ix.heavy_k = h->heavy_k;
-  ix.heavy_v = h->heavy_v;
-  ix.heavy_item = h->heavy_item;
-  ix.image = h->image;
-  ix.counters = h->counters;
+  for (int k = 0; k < n_chunks; ++k) {
+    ss_index &ix = h->views[k];
+    const size_t t0 = (size_t)k * T;
+    ix = ss_index();
+    ix.algo = ALGO_HYBRID;
+    ix.row_begin = row_begin + (int64_t)k * C;
+    ix.row_end = std::min<int64_t>(ix.row_begin + C, row_end);
+    ix.n_items = (int32_t)(ix.row_end - ix.row_begin);
+    ix.dim = h->dim;
+    ix.n_tiles = (ix.n_items + kTI - 1) / kTI;
+    ix.hot = h->hot;
+    ix.slab = h->slab + t0 * kHotMax * kTI;
+    ix.ell = h->ell + t0 * kEllMaxW * kTI;
+    ix.meta = h->meta + t0 * kMetaInts;
+    ix.heavy_k = h->heavy_k;
+    ix.heavy_v = h->heavy_v;
+    ix.heavy_item = h->heavy_item;
+    ix.image = h->image + t0 * kImgBytes;
+    ix.counters = h->counters + (size_t)k * (1 + T);  // [1] the chunk's overflow count, [2..] its tiles
+  }
+  h->n_views = n_chunks;
   return cudaSuccess;
 }
 

@@ -175,7 +175,8 @@ cudaError_t launch_build_index(ss_handle *h, const ss_csr &items, int64_t row_be
                                           h->post_cap, h->d_status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  ss_index &ix = h->index;
+  ss_index &ix = h->views[0];
+  h->n_views = 1;
   ix.algo = ALGO_POSTING;
   ix.row_begin = row_begin;
   ix.row_end = row_end;

@@ -85,8 +85,11 @@ struct ss_index {
   const float *heavy_v = nullptr;      //   value
   const uint8_t *heavy_item = nullptr; //   item within its tile
   const unsigned char *image = nullptr; // [tile][kImgBytes]
-  const int32_t *counters = nullptr;   // [0] heavy cursor, [1] tiles without an image, [2..] their ids
+  const int32_t *counters = nullptr;   // [1] tiles without an image, [2..] their ids ([0] unused)
 };
+
+// Most chunks one hybrid index build covers (one launch, one view per chunk).
+constexpr int kMaxBuildBatch = 8;
 
 // Workspace of the host-buffer pass (ss_bulk_cosine_host), kept between
 // calls and grown on demand: its streams and events, the device copies of the
@@ -133,9 +136,13 @@ struct ss_handle {
   int32_t *heavy_k = nullptr;    // [heavy_cap]
   float *heavy_v = nullptr;
   uint8_t *heavy_item = nullptr;
-  int32_t *counters = nullptr;   // [2 + max tiles]: heavy cursor, overflow count, overflow ids
+  // counters: [0] heavy cursor, then per chunk k of a build, at 1 + k * (1 +
+  // chunk_tiles): the count of its tiles without an image and their ids.
+  int32_t *counters = nullptr;
   int64_t heavy_cap = 0;
-  int32_t max_tiles = 0;
+  int32_t max_tiles = 0;        // build_batch * chunk_tiles
+  int32_t chunk_tiles = 0;      // item tiles per full chunk
+  int32_t build_batch = 1;      // chunks one build covers
   unsigned char *image = nullptr; // [max tiles][kImgBytes]
   // Queries prepared for the current hot set: hot values per query tile
   // ([tile][kHotMax][kTQ]); each row's cold nonzeros as {dim, value bits},
@@ -154,7 +161,9 @@ struct ss_handle {
   int64_t prep_rows = -1, prep_nnz = -1;
   uint64_t prep_generation = ~0ull;
 
-  ss_index index;
+  // The last build's chunk indexes (views into the workspace above).
+  ss_index views[kMaxBuildBatch];
+  int32_t n_views = 0;
   ss_host_pass host;
 };
 
@@ -168,6 +177,8 @@ cudaError_t launch_score_chunk(const ss_handle *h, const ss_csr &queries, const 
                                int64_t ld_out, cudaStream_t s);
 // Hybrid path.  launch_hot_select returns the number of kernels it queued.
 cudaError_t launch_hot_select(ss_handle *h, const ss_csr &items, cudaStream_t s, int *queued);
+// Builds the chunks of h->chunk_rows items that split [row_begin, row_end)
+// (at most h->build_batch of them) in one launch, into h->views[0..n).
 cudaError_t launch_build_hybrid(ss_handle *h, const ss_csr &items, int64_t row_begin,
                                 int64_t row_end, cudaStream_t s);
 // Queues the query preparation (when needed), the fast tile scorer and the

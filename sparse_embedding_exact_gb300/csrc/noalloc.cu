@@ -119,7 +119,7 @@ extern "C" ss_status ss_cosine_chunk_noalloc(const ss_csr *queries, const ss_csr
   chunk_rows.n_rows = width;
   if (launch_row_norms(chunk_rows, inv_i, sm_count, s) != cudaSuccess) return SS_ERR_CUDA;
   if (launch_build_index(&view, *items, row_begin, row_end, s) != cudaSuccess) return SS_ERR_CUDA;
-  if (launch_score_chunk(&view, *queries, inv_q, view.index, inv_i, out, ld_out, s) != cudaSuccess)
+  if (launch_score_chunk(&view, *queries, inv_q, view.views[0], inv_i, out, ld_out, s) != cudaSuccess)
     return SS_ERR_CUDA;
   return SS_OK;
 }

@@ -244,13 +244,19 @@ extern "C" ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *qh, const s
   if ((st = ss_row_norms(h, &id, inv_i, vs)) != SS_OK) return st;
   const int64_t n_chunks = (n_i + C - 1) / C;
 
+  // The chunks' indexes are built h->build_batch at a time (one launch).
+  const int64_t span = C * h->build_batch;
+  ss_index *views[kMaxBuildBatch];
+  int32_t n_views = 0;
   if (out_dev) {
-    for (int64_t c = 0; c < n_chunks; ++c) {
-      const int64_t rb = c * C, re = std::min(rb + C, n_i);
-      ss_index *idx = nullptr;
-      if ((st = ss_build_item_index(h, &id, rb, re, &idx, vs)) != SS_OK) return st;
-      if ((st = ss_score_chunk(h, &qd, inv_q, idx, inv_i + rb, out_dev + rb, ld_out, vs)) != SS_OK)
+    for (int64_t bb = 0; bb < n_i; bb += span) {
+      if ((st = ss_build_item_indexes(h, &id, bb, std::min(bb + span, n_i), views, &n_views, vs)) != SS_OK)
         return st;
+      for (int k = 0; k < n_views; ++k) {
+        const int64_t rb = views[k]->row_begin;
+        if ((st = ss_score_chunk(h, &qd, inv_q, views[k], inv_i + rb, out_dev + rb, ld_out, vs)) != SS_OK)
+          return st;
+      }
     }
     if ((st = drain(h, timeout_ms)) != SS_OK) return st;
     return ss_check_device(h, vs);
@@ -278,9 +284,12 @@ extern "C" ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *qh, const s
   for (int64_t c = 0; c < n_chunks; ++c) {
     const int b = (int)(c & 1);
     const int64_t rb = c * C, re = std::min(rb + C, n_i), w = re - rb;
+    if (rb % span == 0) {  // first chunk of a build batch
+      if ((st = ss_build_item_indexes(h, &id, rb, std::min(rb + span, n_i), views, &n_views, vs)) != SS_OK)
+        return st;
+    }
     if (c >= 2) S_CUDA(cudaStreamWaitEvent(hp.comp, hp.out_free[b], 0));
-    ss_index *idx = nullptr;
-    if ((st = ss_build_item_index(h, &id, rb, re, &idx, vs)) != SS_OK) return st;
+    ss_index *idx = views[(rb % span) / C];
     if ((st = ss_score_chunk(h, &qd, inv_q, idx, inv_i + rb, dbuf[b], w, vs)) != SS_OK) return st;
     S_CUDA(cudaEventRecord(hp.done[b], hp.comp));
     S_CUDA(cudaStreamWaitEvent(hp.copy, hp.done[b], 0));

@@ -205,6 +205,65 @@ def test_score_chunk_calls_match_score_all(sec):
     assert (got[:, I.n_rows:] == -7.0).all()
 
 
+@pytest.mark.parametrize("name,n_q,n_i,chunk", [
+    ("d500k_q50k_i500k_uniform", 40, 12000, 4096),  # every tile takes the ELL / fallback path
+    ("d1.2m_q20k_i1m_heavy", 60, 9000, 2048),       # heavy rows: the batch-wide heavy list
+    ("d65k_q1k_i10k", 50, 4000, 333),               # chunks that end inside a 256-item tile
+])
+def test_batched_builds_match_single_builds(sec, name, n_q, n_i, chunk):
+    cfg = CONFIGS[name]
+    Q, I = generate_rows(cfg, 0, 0, n_q), generate_rows(cfg, 1, 0, n_i)
+    with sec.SparseCosine(cfg.dim, chunk_rows=chunk) as h:
+        q, i = _dev(sec, Q), _dev(sec, I)
+        inv_q, inv_i = h.row_norms(q), h.row_norms(i)
+        single = torch.empty((n_q, n_i), device="cuda")
+        for b in range(0, n_i, chunk):
+            e = min(b + chunk, n_i)
+            h.score_chunk(q, inv_q, h.build_item_index(i, b, e), inv_i[b:], single[:, b:], n_i)
+        batched = torch.empty((n_q, n_i), device="cuda")
+        span = chunk * h.build_batch
+        assert h.build_batch > 1
+        seen, tiles_without_image = [], 0
+        for bb in range(0, n_i, span):
+            views = h.build_item_indexes(i, bb, min(bb + span, n_i))
+            for b, e, idx in views:
+                seen.append((b, e))
+                tiles_without_image += h.index_stats(idx)["tiles_without_image"]
+            for b, e, idx in views:
+                h.score_chunk(q, inv_q, idx, inv_i[b:], batched[:, b:], n_i)
+        h.check_device()
+        a, c = single.cpu().numpy(), batched.cpu().numpy()
+    assert seen == [(b, min(b + chunk, n_i)) for b in range(0, n_i, chunk)]
+    if name.endswith("heavy"):
+        # Rows far above their tile's mean take the fallback scorer's heavy
+        # list, whose products land with shared-memory atomics in no fixed
+        # order: equal up to float32 rounding, not bit for bit.
+        assert _max_err(a, c) <= 1e-6
+    else:
+        assert np.array_equal(a.view(np.int32), c.view(np.int32))
+    if name.endswith("uniform"):
+        assert tiles_without_image == sum((min(chunk, n_i - b) + 255) // 256 for b in range(0, n_i, chunk))
+    assert _max_err(c, oracle.cosine(Q, I)) <= TOL
+
+
+def test_build_item_indexes_limits(sec):
+    from sparse_embedding_exact_gb300 import SparseCosError
+
+    cfg = CONFIGS["d65k_q1k_i10k"]
+    I = generate_rows(cfg, 1, 0, 3000)
+    with sec.SparseCosine(cfg.dim, chunk_rows=256) as h:
+        i = _dev(sec, I)
+        n = h.build_batch
+        with pytest.raises(SparseCosError):
+            h.build_item_indexes(i, 0, min(I.n_rows, 256 * n + 1))
+        with pytest.raises(SparseCosError):
+            h.build_item_indexes(i, 10, 10)
+        views = h.build_item_indexes(i, 5, 5 + 256 * n)
+        assert [(b, e) for b, e, _ in views] == [(5 + 256 * k, 5 + 256 * (k + 1)) for k in range(n)]
+    with sec.SparseCosine(cfg.dim, chunk_rows=256, algorithm="posting") as h:
+        assert h.build_batch == 1
+
+
 def test_self_similarity_invariants(sec):
     cfg = CONFIGS["d1.2m_q5k_i200k"]
     X = generate_rows(cfg, 1, 0, 2000)
