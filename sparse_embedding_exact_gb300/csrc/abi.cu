@@ -133,9 +133,10 @@ void free_workspace(ss_handle *h) {
   free_host_pass(h->host);
   void *ptrs[] = {h->d_status, h->col_cnt, h->col_ptr, h->scan_part, h->post_item, h->post_val,
                   h->hot, h->slab, h->ell, h->meta, h->heavy_k, h->heavy_v, h->heavy_item,
-                  h->counters, h->image, h->qhot, h->qcold, h->qcold_n};
+                  h->counters, h->image, h->qhot, h->qcold, h->qcold_n, h->heavy_tbl};
   for (void *p : ptrs) cudaFree(p);
   h->counters = nullptr;
+  h->heavy_tbl = nullptr;
   h->image = nullptr;
   h->qhot = nullptr;
   h->qcold = nullptr;
@@ -247,6 +248,7 @@ ss_status ss_create(ss_handle **out, int device, int64_t dim, int32_t chunk_rows
     if (e == cudaSuccess) e = cudaMalloc(&h->slab, sizeof(float) * tiles * kHotMax * kTI);
     if (e == cudaSuccess) e = cudaMalloc(&h->ell, sizeof(int2) * tiles * kEllMaxW * kTI);
     if (e == cudaSuccess) e = cudaMalloc(&h->meta, sizeof(int32_t) * tiles * kMetaInts);
+    if (e == cudaSuccess) e = cudaMalloc(&h->heavy_tbl, sizeof(int4) * tiles * kTI);
     const size_t n_counters = 1 + (size_t)h->build_batch * (1 + h->chunk_tiles);
     if (e == cudaSuccess) e = cudaMalloc(&h->counters, sizeof(int32_t) * n_counters);
     if (e == cudaSuccess) e = cudaMemset(h->counters, 0, sizeof(int32_t) * n_counters);

@@ -306,7 +306,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
                   int32_t *__restrict__ heavy_k, float *__restrict__ heavy_v,
                   uint8_t *__restrict__ heavy_item, int32_t *__restrict__ counters,
                   int64_t heavy_cap, unsigned char *__restrict__ image, int32_t *status,
-                  int32_t chunk_rows, int32_t chunk_tiles, int32_t n_chunks) {
+                  int32_t chunk_rows, int32_t chunk_tiles, int32_t n_chunks,
+                  int4 *__restrict__ heavy_tbl) {
   extern __shared__ __align__(16) unsigned char bsm[];
   float *slab_s = reinterpret_cast<float *>(bsm + kBldOffSlab);  // [kHotMax][kTI]
   uint8_t *item_s = bsm + kBldOffSlab;  // segment items, once the slab has been written out
@@ -479,7 +480,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
 
   // ---- ELL path for tiles whose cold part does not fit an image
   int32_t *m = meta + (size_t)t * kMetaInts;
-  int heavy_total = 0;
+  int heavy_total = 0, n_heavy_items = 0;
   bool heavy_ok = true;
   if (!fits) {
     // Cold nonzeros per item (keys read from the CSR itself: a staged tile's
@@ -502,6 +503,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
     const bool my_heavy = tid < n_items && my_cold > thr;
     const int off = bblock_exclusive_scan(my_heavy ? my_cold : 0, red, &heavy_total);
     if (tid < kTI) heavy_off[tid] = my_heavy ? off : -1;
+    // The heavy items in item order, for the fallback scorer.
+    const int hslot = bblock_exclusive_scan(my_heavy ? 1 : 0, red, &n_heavy_items);
+    if (my_heavy) heavy_tbl[(size_t)t * kTI + hslot] = make_int4(tid, off, my_cold, 0);
     if (tid == 0) {
       heavy_base = heavy_total > 0 ? atomicAdd(&counters[0], heavy_total) : 0;
       hdr[2] = 0;
@@ -562,6 +566,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
   if (tid == 0) {
     if (fits) m[8] = 0;
     m[9] = (!fits && heavy_ok) ? heavy_total : 0;
+    m[kMetaHeavyItems] = (!fits && heavy_ok) ? n_heavy_items : 0;
     m[kMetaFits] = fits ? 1 : 0;
   }
 }
@@ -580,6 +585,7 @@ struct HybridArgs {
   const int32_t *heavy_k;
   const float *heavy_v;
   const uint8_t *heavy_item;
+  const int4 *heavy_tbl;
   const float *inv_i;
   int32_t n_items;
   int32_t n_tiles;
@@ -890,21 +896,42 @@ __device__ __forceinline__ void cold_pass(const Smem &sm, const HybridArgs &a, i
     }
   }
   cursor = s;
-  // Heavy items: their nonzeros are spread over all threads; several
-  // threads may add into one accumulator, hence the atomics.
-  const int hb = m[8], hc = m[9];
-  for (int e = hb + tid; e < hb + hc; e += kThreads) {
-    const int32_t k = __ldg(a.heavy_k + e);
-    if (k < lo || k >= hi) continue;
-    const uint32_t hm = batch_find(sm, k);
-    const uint32_t cnt = hm & 0xffffu;
-    if (!cnt) continue;
-    const float v = __ldg(a.heavy_v + e);
-    const int it = __ldg(a.heavy_item + e);
-    const uint32_t st = hm >> 16;
-    for (uint32_t j = st; j < st + cnt; ++j) {
-      const uint2 l = sm.lists[j];
-      atomicAdd(sm.acc + l.x + it, __uint_as_float(l.y) * v);
+  // Heavy items: one warp per item.  Its lanes look up 32 of the item's
+  // nonzeros (ascending dims) at a time; then the query lists of the hits
+  // are applied one after another in lane order, all lanes sharing each
+  // list (whose rows are distinct).  Only this warp writes the item's
+  // column, and every entry's cold terms keep ascending dimension order, as
+  // on the regular path, so the result does not depend on which items a
+  // tile's layout makes heavy.
+  const int hb = m[8], n_hv = m[kMetaHeavyItems];
+  const int lane = tid & 31;
+  for (int g = warp; g < n_hv; g += kThreads / 32) {
+    const int4 hv = __ldg(a.heavy_tbl + (size_t)t * kTI + g);
+    const int64_t e0 = (int64_t)hb + hv.y;
+    float *acol = sm.acc + hv.x;
+    for (int base = 0; base < hv.z; base += 32) {
+      const int e = base + lane;
+      int32_t k = -1;
+      float v = 0.f;
+      if (e < hv.z) {
+        k = __ldg(a.heavy_k + e0 + e);
+        v = __ldg(a.heavy_v + e0 + e);
+      }
+      const uint32_t hm = (k >= lo && k < hi) ? batch_find(sm, k) : 0u;
+      unsigned pending = __ballot_sync(0xffffffffu, (hm & 0xffffu) != 0u);
+      while (pending) {
+        const int j = __ffs(pending) - 1;
+        pending &= pending - 1u;
+        const uint32_t hj = __shfl_sync(0xffffffffu, hm, j);
+        const float vj = __shfl_sync(0xffffffffu, v, j);
+        const uint32_t st = hj >> 16, cnt = hj & 0xffffu;
+        for (uint32_t x = lane; x < cnt; x += 32) {
+          const uint2 l = sm.lists[st + x];
+          float *d = acol + l.x;
+          *d = fmaf(__uint_as_float(l.y), vj, *d);
+        }
+        __syncwarp();
+      }
     }
   }
 }
@@ -1574,7 +1601,7 @@ cudaError_t launch_build_hybrid(ss_handle *h, const ss_csr &items, int64_t row_b
   k_build_tiles<<<n_tiles, kBThreads, kBuildSmem, s>>>(
       items.indptr, items.indices, items.values, row_begin, row_end, h->hot, h->slab, h->ell,
       h->meta, h->heavy_k, h->heavy_v, h->heavy_item, h->counters, h->heavy_cap, h->image,
-      h->d_status, (int32_t)C, T, n_chunks);
+      h->d_status, (int32_t)C, T, n_chunks, h->heavy_tbl);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   for (int k = 0; k < n_chunks; ++k) {
@@ -1594,6 +1621,7 @@ cudaError_t launch_build_hybrid(ss_handle *h, const ss_csr &items, int64_t row_b
     ix.heavy_k = h->heavy_k;
     ix.heavy_v = h->heavy_v;
     ix.heavy_item = h->heavy_item;
+    ix.heavy_tbl = h->heavy_tbl + t0 * kTI;
     ix.image = h->image + t0 * kImgBytes;
     ix.counters = h->counters + (size_t)k * (1 + T);  // [1] the chunk's overflow count, [2..] its tiles
   }
@@ -1717,6 +1745,7 @@ cudaError_t launch_score_hybrid(ss_handle *h, const ss_csr &queries, const float
   a.heavy_k = idx.heavy_k;
   a.heavy_v = idx.heavy_v;
   a.heavy_item = idx.heavy_item;
+  a.heavy_tbl = idx.heavy_tbl;
   a.inv_i = inv_i;
   a.n_items = idx.n_items;
   a.n_tiles = idx.n_tiles;

@@ -57,6 +57,7 @@ constexpr int kImgBytes = kImgOffVal + kImgECap * 4;
 static_assert(kImgOffItem % 16 == 0 && kImgOffVal % 16 == 0 && kImgBytes % 16 == 0,
               "image sections must stay 16-byte aligned");
 constexpr int kMetaFits = 10;              // meta slot: 1 if the tile has an image
+constexpr int kMetaHeavyItems = 11;        // meta slot: heavy items of the tile (entries in heavy_tbl)
 static_assert(kTQ % kQGroup == 0, "query tiles hold whole row groups");
 }  // namespace hyb
 
@@ -84,6 +85,7 @@ struct ss_index {
   const int32_t *heavy_k = nullptr;    // heavy items' cold entries: dim
   const float *heavy_v = nullptr;      //   value
   const uint8_t *heavy_item = nullptr; //   item within its tile
+  const int4 *heavy_tbl = nullptr;     // [tile][kTI]: heavy items {item, first entry - tile's heavy base, count, 0}
   const unsigned char *image = nullptr; // [tile][kImgBytes]
   const int32_t *counters = nullptr;   // [1] tiles without an image, [2..] their ids ([0] unused)
 };
@@ -136,6 +138,7 @@ struct ss_handle {
   int32_t *heavy_k = nullptr;    // [heavy_cap]
   float *heavy_v = nullptr;
   uint8_t *heavy_item = nullptr;
+  int4 *heavy_tbl = nullptr;     // [max tiles][kTI]
   // counters: [0] heavy cursor, then per chunk k of a build, at 1 + k * (1 +
   // chunk_tiles): the count of its tiles without an image and their ids.
   int32_t *counters = nullptr;
