@@ -1132,7 +1132,7 @@ struct TileArgs {
 constexpr int kFThreads = 512;                   // fast scorer: 16 warps
 constexpr int kFWarps = kFThreads / 32;
 constexpr int kGroup = 32 / kQGroup;             // lanes walking one row's segments
-constexpr int kHitCap = 112;                     // hits of one row group held per round
+constexpr int kHitCap = 78;                      // hits of one row group held per round
 constexpr int kPasses = 4;                       // lookup passes of 32 entries in flight
 static_assert(kPasses == 4, "the lookup dispatch instantiates 1 to 4 passes");
 static_assert(kHotMax % 4 == 0, "hot dims are padded to a multiple of 4 inside the slab");

@@ -30,7 +30,7 @@ constexpr int kTQ = 64;                    // query rows per tile
 constexpr int kQGroup = 4;                 // query rows scored together by one warp
 constexpr int kTI = 256;                   // items per tile (one thread per item)
 constexpr int kThreads = 256;              // threads per block (8 warps)
-constexpr int kHotMax = 24;                // dense ("hot") dimensions per item matrix
+constexpr int kHotMax = 32;                // dense ("hot") dimensions per item matrix
 constexpr int kEllMaxW = 1024;             // cold entries per item kept in the ELL block
 constexpr int kMetaInts = 16;              // per item tile: 8 warp lengths, heavy begin, count
 constexpr int kBatchEntries = 4096;        // cold query entries per hashed batch
@@ -39,7 +39,7 @@ constexpr int kHashSlots = 1 << kHashBits; // load factor <= 1/2
 constexpr int kBitmapBits = 15;
 constexpr int kBitmapWords = (1 << kBitmapBits) / 32;
 constexpr int kHotSampleEntries = 8192;    // nonzeros sampled to choose the hot set
-constexpr int kHotMinPercent = 20;         // a dimension is hot if >= 20% of sampled rows hold it
+constexpr int kHotMinPercent = 14;         // a dimension is hot if >= 14% of sampled rows hold it
 
 // Per item tile, the cold nonzeros as an inverted index (an "image" that the
 // scoring block copies into shared memory as is): dimension -> segment of
@@ -47,7 +47,7 @@ constexpr int kHotMinPercent = 20;         // a dimension is hot if >= 20% of sa
 constexpr int kImgSlotsBits = 13;
 constexpr int kImgSlots = 1 << kImgSlotsBits;      // {dim or -1, start | end << 16}
 constexpr int kImgDCap = 6144;                     // distinct cold dims per tile (load <= 3/4)
-constexpr int kImgECap = 10240;                    // cold nonzeros per tile
+constexpr int kImgECap = 9216;                     // cold nonzeros per tile
 constexpr int kImgOffSlots = 16;                   // after the header {D, E, fits, 0}
 constexpr int kImgBitsLog2 = 15;                   // membership bitmap of the tile's cold dims
 constexpr int kImgOffBits = kImgOffSlots + kImgSlots * 8;       // u32 bits[2^15 / 32]

@@ -363,19 +363,26 @@ def test_hot_set_saturated_and_empty(sec):
     assert _max_err(_gpu_cosine(sec, Q, I), oracle.cosine(Q, I)) <= TOL
 
 
+HOT_MIN_FRACTION = 0.14  # the library's hot-set threshold (share of sampled rows)
+HOT_MAX = 32             # and its cap
+
+
 def test_index_stats_hot_set(sec):
-    """The hot set holds the dimensions in >= 20% of sampled rows: about two
-    dozen on the Zipf(1.1) workload, none on the uniform one."""
+    """The hot set holds the dimensions in >= 14% of about 190 sampled rows
+    (at most 32): about thirty on the Zipf(1.1) workload, none on the uniform
+    one.  The sample's frequency estimates carry a standard error of about
+    2.5 points, so the count is checked against dims clearly above and
+    clearly below the threshold."""
     cfg = CONFIGS["d1.2m_q5k_i200k"]
     I = generate_rows(cfg, 1, 0, 20_000)
-    # expected hot count from the data itself: dims in >= 20% of rows
     frac = np.bincount(I.indices, minlength=cfg.dim) / I.n_rows
-    expect = int((frac >= 0.2).sum())
+    surely_in = int((frac >= HOT_MIN_FRACTION + 0.05).sum())
+    maybe_in = min(HOT_MAX, int((frac >= HOT_MIN_FRACTION - 0.05).sum()))
     with sec.SparseCosine(cfg.dim) as h:
         i = _dev(sec, I)
         st = h.index_stats(h.build_item_index(i, 0, 8192))
     assert st["algorithm"] == 0 and st["items"] == 8192 and st["tiles"] == 32
-    assert abs(st["hot_dims"] - expect) <= 3, (st, expect)
+    assert surely_in <= st["hot_dims"] <= maybe_in, (st, surely_in, maybe_in)
     assert st["tiles_without_image"] == 0  # every tile takes the inverted-index path
     cfg3 = CONFIGS["d500k_q50k_i500k_uniform"]
     U = generate_rows(cfg3, 1, 0, 3000)
