@@ -50,6 +50,9 @@ def parse_args():
     p.add_argument("--workload", default=WORKLOAD, choices=sorted(CONFIGS))
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--topk", type=int, default=0,
+                   help="also time the same step with the top-k epilogue (per query row, the k best items) "
+                        "in place of storing the full matrix; reported under 'topk'")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target seconds of oracle work for the CPU baseline sample")
     p.add_argument("--n-queries", type=int, default=0,
@@ -363,6 +366,42 @@ def run_ours(args):
             "index_build_ms_per_launch": statistics.mean(build_ms),
             "index_build_chunks_per_launch": h.build_batch}
 
+    topk = None
+    if args.topk:
+        # The same step (norms, hot set, builds, scoring) with the top-k
+        # epilogue: every score is computed, only each row's k best are kept.
+        def step_topk():
+            h.invalidate()
+            h.row_norms(q, out=inv_q)
+            h.row_norms(it, out=inv_i)
+            return h.topk_all(q, inv_q, it, inv_i, args.topk)
+
+        for _ in range(args.warmup):
+            step_topk()
+        torch.cuda.synchronize()
+        h.check_device()
+        tk_ms = []
+        for _ in range(args.steps):
+            flush.fill_(1.0)
+            torch.cuda.synchronize()
+            barrier()
+            torch.cuda.synchronize()
+            t_start.record(stream)
+            step_topk()
+            t_end.record(stream)
+            torch.cuda.synchronize()
+            tk_ms.append(t_start.elapsed_time(t_end))
+        h.check_device()
+        tms = statistics.mean(tk_ms)
+        if world > 1:
+            import torch.distributed as dist
+
+            t = torch.tensor([tms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            tms = float(t.item())
+        topk = {"k": args.topk, "value": world * n_q * n_i / (tms / 1e3), "unit": UNIT,
+                "ms_per_step": tms, "api": "ss_topk_all"}
+
     e2e = None
     if not args.no_e2e:
         import torch as _t
@@ -417,6 +456,7 @@ def run_ours(args):
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "topk": topk,
             "gpu_launches": int(launches),
             "clocks": clocks,
             "first_chunk_index": index_stats,

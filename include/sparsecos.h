@@ -166,6 +166,40 @@ ss_status ss_score_all(ss_handle *h, const ss_csr *queries, const float *inv_q,
                        void *stream);
 
 /*
+ * Top-k epilogue (the post's downstream uses are ranking and threshold
+ * filtering of the scores, section 2.3): instead of storing a chunk's
+ * scores, keep for every query row q the k items of largest cosine seen so
+ * far, larger score first and equal scores by smaller item number, in
+ *   best_val[q * k + r], best_item[q * k + r], r < k
+ * (device float32 and int64, row-major; -INFINITY and -1 where fewer than k
+ * items have been seen).  The scores are the very values ss_score_chunk
+ * would store.  Needs the default (hybrid) algorithm; 1 <= k <=
+ * SS_TOPK_MAX and k * (ceil(chunk_rows / 256) + 1) <= 8192, else
+ * SS_ERR_LIMIT.
+ *
+ * ss_topk_reset: starts a pass for n_q query rows (fills best_val with
+ * -INFINITY and best_item with -1, and sizes the handle's candidate
+ * workspace; may synchronise the device when that grows).
+ * ss_score_chunk_topk: scores one chunk (an index from ss_build_item_index
+ * or ss_build_item_indexes) and merges its best items into the running
+ * result; chunks may come in any order, each once per pass.
+ * ss_topk_all: reset, then every chunk of `items` (built chunk_rows at a
+ * time, ss_build_batch chunks per build).
+ * All are asynchronous on `stream`.  Errors: SS_ERR_INVALID_ARG (null
+ * pointers, an index of another handle, no reset for these rows and k),
+ * SS_ERR_LIMIT, SS_ERR_OOM, SS_ERR_CUDA.
+ */
+#define SS_TOPK_MAX 64
+ss_status ss_topk_reset(ss_handle *h, int64_t n_q, int32_t k, float *best_val, int64_t *best_item,
+                        void *stream);
+ss_status ss_score_chunk_topk(ss_handle *h, const ss_csr *queries, const float *inv_q,
+                              const ss_index *idx, const float *inv_i, int32_t k, float *best_val,
+                              int64_t *best_item, void *stream);
+ss_status ss_topk_all(ss_handle *h, const ss_csr *queries, const float *inv_q, const ss_csr *items,
+                      const float *inv_i, int32_t k, float *best_val, int64_t *best_item,
+                      void *stream);
+
+/*
  * Receives one finished chunk of the result in host memory:
  *   tile[q * ld + c] = S[q, item_begin + c], q < n_q, c < item_end - item_begin.
  * The tile is only valid during the call.  A nonzero return stops the pass

@@ -178,6 +178,40 @@ class SparseCosine:
                                            _stream_ptr(stream)), "ss_score_all")
         return out
 
+    def topk_reset(self, n_q: int, k: int, device=None, stream=None):
+        """A fresh running top-k for n_q query rows: (best_val float32, best_item
+        int64) device tensors of shape (n_q, k), filled with -inf and -1."""
+        dev = device if device is not None else torch.device("cuda", self.device)
+        best_val = torch.empty((n_q, k), dtype=torch.float32, device=dev)
+        best_item = torch.empty((n_q, k), dtype=torch.int64, device=dev)
+        self._check(self._lib.ss_topk_reset(self._h, int(n_q), int(k), _ptr(best_val),
+                                            _ptr(best_item), _stream_ptr(stream)), "ss_topk_reset")
+        return best_val, best_item
+
+    def score_chunk_topk(self, queries: DeviceCsr, inv_q: torch.Tensor, index,
+                         inv_i_chunk: torch.Tensor, best_val: torch.Tensor,
+                         best_item: torch.Tensor, stream=None):
+        """Scores one chunk and merges its best items into (best_val, best_item)."""
+        c = queries.abi()
+        k = int(best_val.shape[1])
+        self._check(self._lib.ss_score_chunk_topk(self._h, ctypes.byref(c), _ptr(inv_q), index,
+                                                  _ptr(inv_i_chunk), k, _ptr(best_val),
+                                                  _ptr(best_item), _stream_ptr(stream)),
+                    "ss_score_chunk_topk")
+
+    def topk_all(self, queries: DeviceCsr, inv_q: torch.Tensor, items: DeviceCsr,
+                 inv_i: torch.Tensor, k: int, stream=None):
+        """Per query row, the k items of largest cosine (larger first, ties to
+        the smaller item): (values float32, items int64), shape (n_q, k)."""
+        dev = queries.indptr.device
+        best_val = torch.empty((queries.n_rows, k), dtype=torch.float32, device=dev)
+        best_item = torch.empty((queries.n_rows, k), dtype=torch.int64, device=dev)
+        cq, ci = queries.abi(), items.abi()
+        self._check(self._lib.ss_topk_all(self._h, ctypes.byref(cq), _ptr(inv_q), ctypes.byref(ci),
+                                          _ptr(inv_i), int(k), _ptr(best_val), _ptr(best_item),
+                                          _stream_ptr(stream)), "ss_topk_all")
+        return best_val, best_item
+
     def bulk_cosine_host(self, queries, items, out: Optional[np.ndarray] = None,
                          consumer: Optional[Callable] = None, ring_depth: int = 3,
                          timeout_ms: int = 0):

@@ -131,6 +131,13 @@ ss_status ensure_capacity(ss_handle *h, int64_t need) {
 
 void free_workspace(ss_handle *h) {
   free_host_pass(h->host);
+  cudaFree(h->cand_val);
+  cudaFree(h->cand_item);
+  cudaFree(h->cand_n);
+  h->cand_val = nullptr;
+  h->cand_item = nullptr;
+  h->cand_n = nullptr;
+  h->cand_elems = h->cand_rows = 0;
   void *ptrs[] = {h->d_status, h->col_cnt, h->col_ptr, h->scan_part, h->post_item, h->post_val,
                   h->hot, h->slab, h->ell, h->meta, h->heavy_k, h->heavy_v, h->heavy_item,
                   h->counters, h->image, h->qhot, h->qcold, h->qcold_n, h->heavy_tbl};
@@ -171,16 +178,51 @@ ss_status build_chunk(ss_handle *h, const ss_csr &items, int64_t rb, int64_t re,
 }
 
 cudaError_t score(ss_handle *h, const ss_csr &q, const float *inv_q, const ss_index &idx,
-                  const float *inv_i, float *out, int64_t ld_out, cudaStream_t s) {
+                  const float *inv_i, float *out, int64_t ld_out, cudaStream_t s,
+                  const ss_topk *topk = nullptr) {
   if (idx.algo == ALGO_POSTING) {
     const cudaError_t e = launch_score_chunk(h, q, inv_q, idx, inv_i, out, ld_out, s);
     if (e == cudaSuccess && q.n_rows > 0 && idx.n_items > 0) h->launches += 1;
     return e;
   }
   int queued = 0;
-  const cudaError_t e = launch_score_hybrid(h, q, inv_q, idx, inv_i, out, ld_out, s, &queued);
+  const cudaError_t e = launch_score_hybrid(h, q, inv_q, idx, inv_i, out, ld_out, s, &queued, topk);
   h->launches += queued;
   return e;
+}
+
+// Top-k candidate workspace for n_q rows of `cap` entries; synchronises the
+// device when it has to grow.
+ss_status ensure_topk_space(ss_handle *h, int64_t n_q, int64_t cap) {
+  const int64_t elems = std::max<int64_t>(1, n_q * cap);
+  if (elems <= h->cand_elems && n_q <= h->cand_rows) return SS_OK;
+  SS_CUDA(h, cudaDeviceSynchronize());
+  cudaFree(h->cand_val);
+  cudaFree(h->cand_item);
+  cudaFree(h->cand_n);
+  h->cand_val = nullptr;
+  h->cand_item = nullptr;
+  h->cand_n = nullptr;
+  h->cand_elems = h->cand_rows = 0;
+  SS_CUDA(h, cudaMalloc(&h->cand_val, sizeof(float) * (size_t)elems));
+  SS_CUDA(h, cudaMalloc(&h->cand_item, sizeof(int32_t) * (size_t)elems));
+  SS_CUDA(h, cudaMalloc(&h->cand_n, sizeof(int32_t) * (size_t)std::max<int64_t>(1, n_q)));
+  SS_CUDA(h, cudaMemset(h->cand_n, 0, sizeof(int32_t) * (size_t)std::max<int64_t>(1, n_q)));
+  h->cand_elems = elems;
+  h->cand_rows = n_q;
+  return SS_OK;
+}
+
+ss_status check_topk_args(ss_handle *h, int32_t k, const float *best_val, const int64_t *best_item,
+                          int64_t n_q, const char *what) {
+  if (h->algo != ALGO_HYBRID)
+    return fail(h, SS_ERR_INVALID_ARG, "%s: the top-k epilogue needs the default (hybrid) algorithm", what);
+  if (k < 1 || k > kTopkMax) return fail(h, SS_ERR_LIMIT, "%s: k = %d outside [1, %d]", what, k, kTopkMax);
+  if ((int64_t)k * (h->chunk_tiles + 1) > kTopkEntries)
+    return fail(h, SS_ERR_LIMIT, "%s: k = %d too large for chunks of %d rows (k * (chunk_rows / 256 + 1) <= %d)",
+                what, k, h->chunk_rows, kTopkEntries);
+  if (n_q > 0 && (!best_val || !best_item)) return fail(h, SS_ERR_INVALID_ARG, "%s: null output", what);
+  return SS_OK;
 }
 
 // Whether idx is one of the handle's current chunk indexes.
@@ -425,6 +467,73 @@ ss_status ss_score_all(ss_handle *h, const ss_csr *queries, const float *inv_q,
     for (int k = 0; k < h->n_views; ++k) {
       const ss_index &v = h->views[k];
       SS_CUDA(h, score(h, *queries, inv_q, v, inv_i + v.row_begin, out + v.row_begin, ld_out, s));
+    }
+  }
+  return SS_OK;
+}
+
+ss_status ss_topk_reset(ss_handle *h, int64_t n_q, int32_t k, float *best_val, int64_t *best_item,
+                        void *stream) {
+  if (!h) return SS_ERR_INVALID_ARG;
+  if (n_q < 0) return fail(h, SS_ERR_INVALID_ARG, "ss_topk_reset: n_q < 0");
+  ss_status st = check_topk_args(h, k, best_val, best_item, n_q, "ss_topk_reset");
+  if (st != SS_OK) return st;
+  if ((st = set_device(h)) != SS_OK) return st;
+  if ((st = ensure_topk_space(h, n_q, (int64_t)h->chunk_tiles * k)) != SS_OK) return st;
+  SS_CUDA(h, launch_topk_reset(n_q, k, best_val, best_item, h->cand_n, h->sm_count, as_stream(stream)));
+  if (n_q > 0) h->launches += 1;
+  return SS_OK;
+}
+
+ss_status ss_score_chunk_topk(ss_handle *h, const ss_csr *queries, const float *inv_q,
+                              const ss_index *idx, const float *inv_i, int32_t k, float *best_val,
+                              int64_t *best_item, void *stream) {
+  if (!h) return SS_ERR_INVALID_ARG;
+  ss_status st = check_csr_args(h, queries, "ss_score_chunk_topk");
+  if (st != SS_OK) return st;
+  if ((st = check_topk_args(h, k, best_val, best_item, queries->n_rows, "ss_score_chunk_topk")) != SS_OK)
+    return st;
+  if (!idx || !owns_index(h, idx))
+    return fail(h, SS_ERR_INVALID_ARG, "ss_score_chunk_topk: index does not belong to this handle");
+  if (queries->n_rows == 0 || idx->n_items == 0) return SS_OK;
+  if (!inv_q || !inv_i) return fail(h, SS_ERR_INVALID_ARG, "ss_score_chunk_topk: null norms");
+  if (queries->n_rows > h->cand_rows || (int64_t)h->chunk_tiles * k * queries->n_rows > h->cand_elems)
+    return fail(h, SS_ERR_INVALID_ARG, "ss_score_chunk_topk: call ss_topk_reset for these rows and k first");
+  if ((st = set_device(h)) != SS_OK) return st;
+  cudaStream_t s = as_stream(stream);
+  ss_topk t;
+  t.k = k;
+  t.best_val = best_val;
+  t.cand_val = h->cand_val;
+  t.cand_item = h->cand_item;
+  t.cand_n = h->cand_n;
+  t.cand_cap = h->chunk_tiles * k;
+  SS_CUDA(h, score(h, *queries, inv_q, *idx, inv_i, nullptr, idx->n_items, s, &t));
+  SS_CUDA(h, launch_topk_merge(t, queries->n_rows, idx->row_begin, best_val, best_item, h->sm_count, s));
+  h->launches += 1;
+  return SS_OK;
+}
+
+ss_status ss_topk_all(ss_handle *h, const ss_csr *queries, const float *inv_q, const ss_csr *items,
+                      const float *inv_i, int32_t k, float *best_val, int64_t *best_item,
+                      void *stream) {
+  if (!h) return SS_ERR_INVALID_ARG;
+  ss_status st = check_csr_args(h, queries, "ss_topk_all");
+  if (st == SS_OK) st = check_csr_args(h, items, "ss_topk_all");
+  if (st != SS_OK) return st;
+  if ((st = ss_topk_reset(h, queries->n_rows, k, best_val, best_item, stream)) != SS_OK) return st;
+  if (queries->n_rows == 0 || items->n_rows == 0) return SS_OK;
+  if (!inv_q || !inv_i) return fail(h, SS_ERR_INVALID_ARG, "ss_topk_all: null norms");
+  cudaStream_t s = as_stream(stream);
+  const int64_t span = (int64_t)h->chunk_rows * h->build_batch;
+  for (int64_t bb = 0; bb < items->n_rows; bb += span) {
+    const int64_t be = std::min<int64_t>(bb + span, items->n_rows);
+    if ((st = build_chunk(h, *items, bb, be, s)) != SS_OK) return st;
+    for (int v = 0; v < h->n_views; ++v) {
+      const ss_index *ix = &h->views[v];
+      if ((st = ss_score_chunk_topk(h, queries, inv_q, ix, inv_i + ix->row_begin, k, best_val,
+                                    best_item, stream)) != SS_OK)
+        return st;
     }
   }
   return SS_OK;

@@ -36,6 +36,7 @@
 // For each (q, i) the sum runs over hot dims ascending, then cold dims
 // ascending (heavy items excepted: their cold adds are atomic).
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include <algorithm>
@@ -571,6 +572,98 @@ __global__ void __launch_bounds__(kBThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- top-k
+// Order of the top-k epilogue: larger score first, equal scores by smaller
+// item number.
+__device__ __forceinline__ bool topk_before(float v, int64_t i, float w, int64_t j) {
+  return v > w || (v == w && i < j);
+}
+
+// How many of query row q's scores in one item tile (8 per lane) are >= thr
+// (the row's current k-th best score).
+__device__ __forceinline__ int topk_count(float thr, const float (&v)[8], const bool (&valid)[8]) {
+  int count = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) count += __popc(__ballot_sync(0xffffffffu, valid[j] && v[j] >= thr));
+  return count;
+}
+
+// Writes a tile's offer for query row q at slots [base, base + min(count,
+// k)) of the row's candidates: the scores >= thr, or when more than k pass,
+// the k best in the top-k order (k rounds of warp arg-best).  Items are
+// chunk-relative.
+__device__ __forceinline__ void topk_emit(const ss_topk &t, int64_t q, float thr, const float (&v)[8],
+                                          const int (&item)[8], const bool (&valid)[8], int base,
+                                          int count, int lane) {
+  bool pass[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) pass[j] = valid[j] && v[j] >= thr;
+  float *cv = t.cand_val + q * t.cand_cap + base;
+  int32_t *ci = t.cand_item + q * t.cand_cap + base;
+  if (count <= t.k) {
+    const unsigned lt = (1u << lane) - 1u;
+    int off = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const unsigned m = __ballot_sync(0xffffffffu, pass[j]);
+      if (pass[j]) {
+        const int pos = off + __popc(m & lt);
+        cv[pos] = v[j];
+        ci[pos] = item[j];
+      }
+      off += __popc(m);
+    }
+    return;
+  }
+  for (int r = 0; r < t.k; ++r) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff, bj = -1;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (pass[j] && topk_before(v[j], item[j], bv, bi)) {
+        bv = v[j];
+        bi = item[j];
+        bj = j;
+      }
+    float wv = bv;
+    int wi = bi;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
+      if (topk_before(ov, oi, wv, wi)) {
+        wv = ov;
+        wi = oi;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)  // items are distinct: one lane holds the winner
+      if (j == bj && bi == wi) pass[j] = false;
+    if (lane == 0) {
+      cv[r] = wv;
+      ci[r] = wi;
+    }
+  }
+}
+
+// Offers query row q's scores of one item tile to the row's candidates
+// (reserving the slots with one atomic).
+__device__ __forceinline__ void topk_offer(const ss_topk &t, int64_t q, float thr, const float (&v)[8],
+                                           const int (&item)[8], const bool (&valid)[8], int lane,
+                                           int32_t *status) {
+  const int count = topk_count(thr, v, valid);
+  if (count == 0) return;
+  const int n_emit = count < t.k ? count : t.k;
+  int base = 0;
+  if (lane == 0) base = atomicAdd(t.cand_n + q, n_emit);
+  base = __shfl_sync(0xffffffffu, base, 0);
+  if (base + n_emit > t.cand_cap) {  // cannot happen: a chunk's tiles offer at most k each
+    if (lane == 0) flag(status, DEV_CAPACITY);
+    return;
+  }
+  topk_emit(t, q, thr, v, item, valid, base, count, lane);
+}
+
 // ---------------------------------------------------------------- scorer
 struct HybridArgs {
   const int64_t *q_indptr;
@@ -595,6 +688,8 @@ struct HybridArgs {
   int64_t ld_out;
   int32_t vec_ok;
   int32_t dim;
+  ss_topk topk;     // k > 0: offer top-k candidates instead of storing the tile
+  int32_t *status;
 };
 
 constexpr int kQueue = 8;  // cold entries probed per step; their hits queue per thread
@@ -941,6 +1036,30 @@ __device__ __forceinline__ void store_tile(const Smem &sm, const HybridArgs &a, 
   const int tid = threadIdx.x;
   const int i0 = t * kTI;
   const int ni = min(kTI, a.n_items - i0);
+  if (a.topk.k > 0) {  // one warp per row: lane l holds items 4l + [0, 4) and 128 + 4l + [0, 4)
+    const int lane = tid & 31, warp = tid >> 5;
+    const int ia = 4 * lane, ib = 128 + 4 * lane;
+    float n[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      n[j] = ia + j < ni ? __ldg(a.inv_i + i0 + ia + j) : 0.f;
+      n[4 + j] = ib + j < ni ? __ldg(a.inv_i + i0 + ib + j) : 0.f;
+    }
+    for (int r = warp; r < nq; r += kThreads / 32) {
+      const float iq = __ldg(a.inv_q + q0 + r);
+      const float4 va = *reinterpret_cast<const float4 *>(sm.acc + r * kTI + ia);
+      const float4 vb = *reinterpret_cast<const float4 *>(sm.acc + r * kTI + ib);
+      const float v[8] = {va.x * iq * n[0], va.y * iq * n[1], va.z * iq * n[2], va.w * iq * n[3],
+                          vb.x * iq * n[4], vb.y * iq * n[5], vb.z * iq * n[6], vb.w * iq * n[7]};
+      const int it[8] = {i0 + ia, i0 + ia + 1, i0 + ia + 2, i0 + ia + 3,
+                         i0 + ib, i0 + ib + 1, i0 + ib + 2, i0 + ib + 3};
+      const bool ok[8] = {ia < ni, ia + 1 < ni, ia + 2 < ni, ia + 3 < ni,
+                          ib < ni, ib + 1 < ni, ib + 2 < ni, ib + 3 < ni};
+      const float thr = __ldg(a.topk.best_val + (q0 + r) * a.topk.k + (a.topk.k - 1));
+      topk_offer(a.topk, q0 + r, thr, v, it, ok, lane, a.status);
+    }
+    return;
+  }
   const int c = (tid & 63) * 4;
   if (c >= ni) return;
   float n[4];
@@ -1127,6 +1246,7 @@ struct TileArgs {
   int64_t ld_out;
   int32_t vec_ok;
   int32_t *status;
+  ss_topk topk;  // k > 0: offer top-k candidates instead of storing the tile
 };
 
 constexpr int kFThreads = 512;                   // fast scorer: 16 warps
@@ -1339,6 +1459,9 @@ __device__ __forceinline__ void walk_segment(float *arow, const uint8_t *seg_ite
 // per row walks that row's hit segments (a group only touches its own row,
 // so no accumulator is shared, and each row's cold terms are added in
 // ascending dimension order); then the normalised rows are stored.
+// kTopk: offer top-k candidates (a.topk) instead of storing the tile; a
+// separate instantiation, so the plain store path keeps its registers.
+template <bool kTopk>
 __global__ void __launch_bounds__(kFThreads, 1) k_score_tiles(const TileArgs a) {
   extern __shared__ __align__(16) unsigned char fsm[];
   unsigned char *img = fsm + kFOffImg;
@@ -1407,10 +1530,11 @@ __global__ void __launch_bounds__(kFThreads, 1) k_score_tiles(const TileArgs a) 
       // Group metadata, hot values and the first cold entries, issued before
       // the hot product so their latency hides behind it.
       int cn = 0;
-      float iq = 0.f;
+      float iq = 0.f, thr = 0.f;  // thr: the row's current k-th best (top-k epilogue)
       if (lane < nr) {
         cn = ld_early_s32(a.qcold_n + q_first + lane);
         iq = ld_early_f32(a.inv_q + q_first + lane);
+        if (kTopk) thr = ld_early_f32(a.topk.best_val + (q_first + lane) * a.topk.k + (a.topk.k - 1));
       }
       const int64_t base = ld_early_s64(a.q_indptr + q_first);
       if (lane >= H && lane < ((H + 3) & ~3))  // pad rows of the hot values
@@ -1510,7 +1634,55 @@ __global__ void __launch_bounds__(kFThreads, 1) k_score_tiles(const TileArgs a) 
         __syncwarp();
       }
 
-      // 3. normalise and store the group's rows
+      // 3. normalise and store the group's rows (or offer them to the top-k)
+      if constexpr (kTopk) {
+        // Scores of row r of the group, normalised as the store path does.
+        auto row_scores = [&](int r, float (&v)[8]) {
+          const float iqr = __shfl_sync(0xffffffffu, iq, r);
+          const float4 va = *reinterpret_cast<const float4 *>(acc + r * kTI + ia);
+          const float4 vb = *reinterpret_cast<const float4 *>(acc + r * kTI + ib);
+          v[0] = va.x * iqr * na[0];
+          v[1] = va.y * iqr * na[1];
+          v[2] = va.z * iqr * na[2];
+          v[3] = va.w * iqr * na[3];
+          v[4] = vb.x * iqr * nb[0];
+          v[5] = vb.y * iqr * nb[1];
+          v[6] = vb.z * iqr * nb[2];
+          v[7] = vb.w * iqr * nb[3];
+        };
+        const int it[8] = {i0 + ia, i0 + ia + 1, i0 + ia + 2, i0 + ia + 3,
+                           i0 + ib, i0 + ib + 1, i0 + ib + 2, i0 + ib + 3};
+        const bool ok[8] = {ia < ni, ia + 1 < ni, ia + 2 < ni, ia + 3 < ni,
+                            ib < ni, ib + 1 < ni, ib + 2 < ni, ib + 3 < ni};
+        // Counts first, then lanes 0..3 reserve their rows' slots together,
+        // then each row's offer is written.
+        int mine = 0;
+#pragma unroll
+        for (int r = 0; r < kQGroup; ++r) {
+          float v[8];
+          row_scores(r, v);
+          const int c = r < nr ? topk_count(__shfl_sync(0xffffffffu, thr, r), v, ok) : 0;
+          if (lane == r) mine = c;
+        }
+        const int n_emit = mine < a.topk.k ? mine : a.topk.k;
+        int base = 0;
+        if (n_emit > 0) base = atomicAdd(a.topk.cand_n + q_first + lane, n_emit);
+        if (n_emit > 0 && base + n_emit > a.topk.cand_cap) {  // cannot happen: at most k per tile
+          flag(a.status, DEV_CAPACITY);
+          mine = 0;
+        }
+#pragma unroll
+        for (int r = 0; r < kQGroup; ++r) {
+          const int c = __shfl_sync(0xffffffffu, mine, r);
+          const int b = __shfl_sync(0xffffffffu, base, r);
+          if (c == 0) continue;
+          float v[8];
+          row_scores(r, v);
+          topk_emit(a.topk, q_first + r, __shfl_sync(0xffffffffu, thr, r), v, it, ok, b, c, lane);
+        }
+        __syncwarp();
+        continue;
+      }
 #pragma unroll
       for (int r = 0; r < kQGroup; ++r) {
         const float iqr = __shfl_sync(0xffffffffu, iq, r);
@@ -1687,7 +1859,7 @@ static cudaError_t prepare_queries(ss_handle *h, const ss_csr &q, cudaStream_t s
 
 cudaError_t launch_score_hybrid(ss_handle *h, const ss_csr &queries, const float *inv_q,
                                 const ss_index &idx, const float *inv_i, float *out,
-                                int64_t ld_out, cudaStream_t s, int *queued) {
+                                int64_t ld_out, cudaStream_t s, int *queued, const ss_topk *topk) {
   *queued = 0;
   if (queries.n_rows == 0 || idx.n_items == 0) return cudaSuccess;
   static bool configured = false;
@@ -1695,7 +1867,9 @@ cudaError_t launch_score_hybrid(ss_handle *h, const ss_csr &queries, const float
     cudaError_t e = cudaFuncSetAttribute(k_score_hybrid, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kScoreSmem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_score_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize, kFastSmem);
+      e = cudaFuncSetAttribute(k_score_tiles<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFastSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_score_tiles<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFastSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -1727,8 +1901,10 @@ cudaError_t launch_score_hybrid(ss_handle *h, const ss_csr &queries, const float
   f.ld_out = ld_out;
   f.vec_ok = vec_ok;
   f.status = h->d_status;
+  f.topk = topk ? *topk : ss_topk();
   const int grid_f = (int)std::min<int64_t>(f.n_units, sms);
-  k_score_tiles<<<grid_f, kFThreads, kFastSmem, s>>>(f);
+  if (f.topk.k > 0) k_score_tiles<true><<<grid_f, kFThreads, kFastSmem, s>>>(f);
+  else k_score_tiles<false><<<grid_f, kFThreads, kFastSmem, s>>>(f);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -1755,9 +1931,113 @@ cudaError_t launch_score_hybrid(ss_handle *h, const ss_csr &queries, const float
   a.ld_out = ld_out;
   a.vec_ok = vec_ok;
   a.dim = (int32_t)idx.dim;
+  a.topk = topk ? *topk : ss_topk();
+  a.status = h->d_status;
   k_score_hybrid<<<sms, kThreads, kScoreSmem, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   *queued = prep + 2;
   return cudaSuccess;
+}
+
+// ---------------------------------------------------------------- top-k merge
+namespace {
+
+__global__ void __launch_bounds__(256)
+    k_topk_reset(int64_t n_q, int32_t k, float *best_val, int64_t *best_item, int32_t *cand_n) {
+  const int64_t n = n_q * k;
+  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    best_val[e] = -INFINITY;
+    best_item[e] = -1;
+  }
+  for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < n_q;
+       q += (int64_t)gridDim.x * blockDim.x)
+    cand_n[q] = 0;
+}
+
+// One warp per query row: the row's running best k and its candidates of
+// the chunk (items item_base + chunk-relative number) go through k rounds
+// of warp arg-best in the top-k order; then the candidates are cleared.
+__global__ void __launch_bounds__(256)
+    k_topk_merge(const ss_topk t, int64_t n_q, int64_t item_base, float *best_val,
+                 int64_t *best_item) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t q = blockIdx.x * (int64_t)(blockDim.x / 32) + (threadIdx.x >> 5); q < n_q;
+       q += warps) {
+    const int m = t.cand_n[q];
+    if (m == 0) continue;
+    const int k = t.k, total = k + m;  // at most kTopkEntries (checked by the caller)
+    float *bv = best_val + q * k;
+    int64_t *bi = best_item + q * k;
+    const float *cv = t.cand_val + q * t.cand_cap;
+    const int32_t *ci = t.cand_item + q * t.cand_cap;
+    float res_v[2] = {-INFINITY, -INFINITY};
+    int64_t res_i[2] = {-1, -1};
+    {
+      uint32_t taken[kTopkEntries / 1024] = {};  // entries lane + 32 j
+      for (int r = 0; r < k; ++r) {
+        float lv = -INFINITY;
+        int64_t li = INT64_MAX;
+        int lj = -1;
+        for (int j = 0; lane + 32 * j < total; ++j) {
+          if ((taken[j >> 5] >> (j & 31)) & 1u) continue;
+          const int e = lane + 32 * j;
+          const float v = e < k ? bv[e] : cv[e - k];
+          const int64_t it = e < k ? bi[e] : item_base + ci[e - k];
+          if (topk_before(v, it, lv, li)) {
+            lv = v;
+            li = it;
+            lj = j;
+          }
+        }
+        float wv = lv;
+        int64_t wi = li;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
+          const int64_t oi = __shfl_xor_sync(0xffffffffu, wi, o);
+          if (topk_before(ov, oi, wv, wi)) {
+            wv = ov;
+            wi = oi;
+          }
+        }
+        if (lj >= 0 && lv == wv && li == wi) taken[lj >> 5] |= 1u << (lj & 31);
+        if ((r & 31) == lane) {
+          res_v[r >> 5] = wv;
+          res_i[r >> 5] = wi < 0 || wi == INT64_MAX ? -1 : wi;
+        }
+      }
+    }
+    __syncwarp();
+    for (int rr = 0; rr < 2; ++rr) {
+      const int r = lane + 32 * rr;
+      if (r < k) {
+        bv[r] = res_v[rr];
+        bi[r] = res_i[rr];
+      }
+    }
+    if (lane == 0) t.cand_n[q] = 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_topk_reset(int64_t n_q, int32_t k, float *best_val, int64_t *best_item,
+                              int32_t *cand_n, int sm_count, cudaStream_t s) {
+  if (n_q == 0) return cudaSuccess;
+  const int64_t need = (n_q * k + 255) / 256;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count * 8));
+  k_topk_reset<<<grid, 256, 0, s>>>(n_q, k, best_val, best_item, cand_n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_merge(const ss_topk &t, int64_t n_q, int64_t item_base, float *best_val,
+                              int64_t *best_item, int sm_count, cudaStream_t s) {
+  if (n_q == 0) return cudaSuccess;
+  const int64_t need = (n_q + 7) / 8;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sm_count * 16));
+  k_topk_merge<<<grid, 256, 0, s>>>(t, n_q, item_base, best_val, best_item);
+  return cudaGetLastError();
 }

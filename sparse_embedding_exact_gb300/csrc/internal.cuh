@@ -93,6 +93,22 @@ struct ss_index {
 // Most chunks one hybrid index build covers (one launch, one view per chunk).
 constexpr int kMaxBuildBatch = 8;
 
+// Largest k of the top-k epilogue, and the most entries (k running plus a
+// chunk's candidates, at most k per item tile) one row's merge handles.
+constexpr int kTopkMax = 64;
+constexpr int kTopkEntries = 8192;
+
+// Top-k epilogue: the running best k of every query row, and per row the
+// candidates one chunk's tiles offer before they are merged in.
+struct ss_topk {
+  int32_t k = 0;           // 0: the scorers store full tiles instead
+  const float *best_val = nullptr;  // [n_q][k], descending; -inf where fewer than k seen
+  float *cand_val = nullptr;        // [n_q][cand_cap]
+  int32_t *cand_item = nullptr;     // [n_q][cand_cap]: item within the chunk
+  int32_t *cand_n = nullptr;        // [n_q]
+  int32_t cand_cap = 0;             // tiles of the chunk * k
+};
+
 // Workspace of the host-buffer pass (ss_bulk_cosine_host), kept between
 // calls and grown on demand: its streams and events, the device copies of the
 // two CSR matrices and their inverse norms, two chunk output buffers, and the
@@ -168,6 +184,11 @@ struct ss_handle {
   ss_index views[kMaxBuildBatch];
   int32_t n_views = 0;
   ss_host_pass host;
+  // Top-k candidate workspace, grown on demand.
+  float *cand_val = nullptr;
+  int32_t *cand_item = nullptr;
+  int32_t *cand_n = nullptr;
+  int64_t cand_elems = 0, cand_rows = 0;
 };
 
 // Launchers (all asynchronous on `s`).
@@ -188,7 +209,14 @@ cudaError_t launch_build_hybrid(ss_handle *h, const ss_csr &items, int64_t row_b
 // fallback scorer; *queued gets the number of kernels queued.
 cudaError_t launch_score_hybrid(ss_handle *h, const ss_csr &queries, const float *inv_q,
                                 const ss_index &idx, const float *inv_i, float *out,
-                                int64_t ld_out, cudaStream_t s, int *queued);
+                                int64_t ld_out, cudaStream_t s, int *queued,
+                                const ss_topk *topk = nullptr);
+// Top-k: fills best_val with -inf and best_item with -1; merges one chunk's
+// candidates (items numbered from item_base) into the running best.
+cudaError_t launch_topk_reset(int64_t n_q, int32_t k, float *best_val, int64_t *best_item,
+                              int32_t *cand_n, int sm_count, cudaStream_t s);
+cudaError_t launch_topk_merge(const ss_topk &t, int64_t n_q, int64_t item_base, float *best_val,
+                              int64_t *best_item, int sm_count, cudaStream_t s);
 
 // Kernels queued by one launch_build_index call.
 constexpr int kIndexKernels = 5;

@@ -1,0 +1,130 @@
+"""GPU top-k epilogue: per query row, the k items of largest cosine (larger
+first, equal scores by smaller item number).
+
+The top-k path keeps exactly the scores the full path stores, so it must pick
+the top k of the GPU's own full matrix bit for bit; against the oracle, each
+picked score is within the 2e-6 bar and no better item was missed by more
+than twice that.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from workload import CONFIGS, generate_rows  # noqa: E402
+from workload.tiny import csr_from_rows  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-6
+
+
+@pytest.fixture(scope="module")
+def sec():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sparse_embedding_exact_gb300 as sec
+    from sparse_embedding_exact_gb300 import build
+
+    build.build()
+    sec._abi.load()
+    return sec
+
+
+def _dev(sec, batch):
+    return sec.DeviceCsr.from_host(batch, "cuda")
+
+
+def _top_order(S, k):
+    """Per row, the item numbers of the k best by (score desc, item asc)."""
+    items = np.arange(S.shape[1])
+    return np.stack([np.lexsort((items, -S[q]))[:k] for q in range(S.shape[0])])
+
+
+def _topk_and_full(sec, Q, I, k, chunk):
+    with sec.SparseCosine(Q.dim, chunk_rows=chunk) as h:
+        q, i = _dev(sec, Q), _dev(sec, I)
+        inv_q, inv_i = h.row_norms(q), h.row_norms(i)
+        vals, items = h.topk_all(q, inv_q, i, inv_i, k)
+        full = h.score_all(q, inv_q, i, inv_i)
+        h.check_device()
+        return vals.cpu().numpy(), items.cpu().numpy(), full.cpu().numpy()
+
+
+CASES = [
+    # (workload, n_q, n_i, k, chunk_rows)
+    ("d65k_q1k_i10k", 60, 7000, 10, 2048),
+    ("d65k_q1k_i10k", 30, 9000, 64, 8192),
+    ("d65k_q1k_i10k", 25, 3000, 1, 333),
+    ("d1.2m_q5k_i200k", 50, 12000, 20, 8192),
+    ("d1.2m_q20k_i1m_heavy", 40, 6000, 16, 2048),  # heavy rows on the fallback path
+    ("d500k_q50k_i500k_uniform", 20, 5000, 8, 4096),  # every tile on the fallback path
+]
+
+
+@pytest.mark.parametrize("name,n_q,n_i,k,chunk", CASES)
+def test_topk_is_the_top_of_the_full_matrix(sec, name, n_q, n_i, k, chunk):
+    cfg = CONFIGS[name]
+    Q, I = generate_rows(cfg, 0, 0, n_q), generate_rows(cfg, 1, 0, n_i)
+    vals, items, full = _topk_and_full(sec, Q, I, k, chunk)
+    expect = _top_order(full, k)
+    assert np.array_equal(items, expect)
+    assert np.array_equal(vals.view(np.int32), np.take_along_axis(full, expect, 1).view(np.int32))
+    ref = oracle.cosine(Q, I, f64=True)
+    picked = np.take_along_axis(ref, items, 1)
+    assert np.abs(vals.astype(np.float64) - picked).max() <= TOL
+    kth = np.sort(ref, axis=1)[:, -k]
+    assert (picked >= kth[:, None] - 2 * TOL).all()
+
+
+def test_topk_short_rows_ties_and_padding(sec):
+    # 3 query rows (one all zero: every score 0, ties broken by item number),
+    # 5 items, k = 8 > 5: the last 3 slots stay (-inf, -1).
+    Q = csr_from_rows([([1, 3], [1.0, 2.0]), ([], []), ([0, 3, 5], [0.5, -1.0, 2.0])], 8)
+    I = csr_from_rows([([3], [1.0]), ([1, 3], [2.0, 4.0]), ([0], [-1.0]), ([5, 7], [1.0, 1.0]), ([], [])], 8)
+    with sec.SparseCosine(8, chunk_rows=2) as h:
+        q, i = _dev(sec, Q), _dev(sec, I)
+        inv_q, inv_i = h.row_norms(q), h.row_norms(i)
+        vals, items = (t.cpu().numpy() for t in h.topk_all(q, inv_q, i, inv_i, 8))
+        full = h.score_all(q, inv_q, i, inv_i).cpu().numpy()
+    assert np.isneginf(vals[:, 5:]).all() and (items[:, 5:] == -1).all()
+    assert np.array_equal(items[:, :5], _top_order(full, 5))
+    assert np.array_equal(items[1, :5], np.arange(5)) and (vals[1, :5] == 0).all()
+
+
+def test_topk_chunks_in_any_order_match_topk_all(sec):
+    cfg = CONFIGS["d65k_q1k_i10k"]
+    Q, I = generate_rows(cfg, 0, 0, 40), generate_rows(cfg, 1, 0, 5000)
+    with sec.SparseCosine(cfg.dim, chunk_rows=1024) as h:
+        q, i = _dev(sec, Q), _dev(sec, I)
+        inv_q, inv_i = h.row_norms(q), h.row_norms(i)
+        want_v, want_i = h.topk_all(q, inv_q, i, inv_i, 12)
+        want_v, want_i = want_v.cpu().numpy(), want_i.cpu().numpy()
+        best_v, best_i = h.topk_reset(Q.n_rows, 12)
+        span = 1024 * h.build_batch
+        for bb in reversed(range(0, I.n_rows, span)):
+            for b, e, idx in reversed(h.build_item_indexes(i, bb, min(bb + span, I.n_rows))):
+                h.score_chunk_topk(q, inv_q, idx, inv_i[b:], best_v, best_i)
+        h.check_device()
+        got_v, got_i = best_v.cpu().numpy(), best_i.cpu().numpy()
+    assert np.array_equal(got_i, want_i)
+    assert np.array_equal(got_v.view(np.int32), want_v.view(np.int32))
+
+
+def test_topk_limits(sec):
+    from sparse_embedding_exact_gb300 import SparseCosError
+
+    cfg = CONFIGS["d65k_q1k_i10k"]
+    Q, I = generate_rows(cfg, 0, 0, 4), generate_rows(cfg, 1, 0, 300)
+    with sec.SparseCosine(cfg.dim, chunk_rows=256) as h:
+        q, i = _dev(sec, Q), _dev(sec, I)
+        inv_q, inv_i = h.row_norms(q), h.row_norms(i)
+        for k in (0, 65):
+            with pytest.raises(SparseCosError):
+                h.topk_all(q, inv_q, i, inv_i, k)
+        h.topk_all(q, inv_q, i, inv_i, 64)  # still usable
+    with sec.SparseCosine(cfg.dim, chunk_rows=256, algorithm="posting") as h:
+        q, i = _dev(sec, Q), _dev(sec, I)
+        with pytest.raises(SparseCosError):
+            h.topk_all(q, h.row_norms(q), i, h.row_norms(i), 4)
