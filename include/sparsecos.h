@@ -60,6 +60,10 @@ typedef int32_t ss_status;
  * nonzero, the chunk's posting list of that dimension (one warp per query
  * row).  Both give the same cosines up to float32 summation order. */
 #define SS_ALGO_POSTING_LISTS 0x2
+/* ss_bulk_cosine_host verifies every streamed chunk: its checksum (see
+ * ss_tile_checksum) is taken on the device before the copy and on the host
+ * after it, and must agree; the pass then always goes through the ring. */
+#define SS_VERIFY_STREAM 0x4
 
 /* Largest chunk the index builder accepts (item numbers in a chunk are
  * stored in 16 bits). */
@@ -231,6 +235,32 @@ ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *queries_host,
                               const ss_csr *items_host, float *out_host, int64_t ld_out,
                               ss_chunk_consumer consumer, void *user, int32_t ring_depth,
                               int32_t timeout_ms);
+
+/*
+ * Checksums of a row-major float32 tile of n_rows x n_cols with leading
+ * dimension ld (the integrity check of a streamed result):
+ *   bits_sum  = sum of the values' 32-bit patterns read as unsigned integers,
+ *               modulo 2^64 (exact and order-independent: two copies of a
+ *               tile agree exactly when, as a rule, they are bit-identical);
+ *   value_sum = sum of the values in double, for reporting (its last bits
+ *               depend on the summation order).
+ * ss_tile_checksum: tile, bits_sum and value_sum are device pointers; the
+ * sums are ADDED to *bits_sum / *value_sum (zero them first; several tiles
+ * may add up), asynchronously on `stream`.  ss_tile_checksum_host: host
+ * pointers, results written.  Errors: SS_ERR_INVALID_ARG, SS_ERR_CUDA.
+ */
+ss_status ss_tile_checksum(ss_handle *h, const float *tile, int64_t n_rows, int64_t n_cols,
+                           int64_t ld, uint64_t *bits_sum, double *value_sum, void *stream);
+ss_status ss_tile_checksum_host(const float *tile, int64_t n_rows, int64_t n_cols, int64_t ld,
+                                uint64_t *bits_sum, double *value_sum);
+
+/*
+ * Checksums of chunk `chunk` of the last ss_bulk_cosine_host pass run with
+ * SS_VERIFY_STREAM (as found on the host copy, equal to the device's).
+ * Errors: SS_ERR_INVALID_ARG (no such chunk, or no verified pass).
+ */
+ss_status ss_stream_checksum(const ss_handle *h, int64_t chunk, uint64_t *bits_sum,
+                             double *value_sum);
 
 /*
  * Checks a device CSR on the device (indptr[0] = 0, indptr non-decreasing

@@ -80,9 +80,11 @@ class SparseCosine:
     ALGORITHMS = ("hybrid", "posting")
 
     def __init__(self, dim: int, chunk_rows: int = DEFAULT_CHUNK_ROWS, device: int = 0,
-                 validate: bool = False, algorithm: str = "hybrid"):
+                 validate: bool = False, algorithm: str = "hybrid", verify_stream: bool = False):
         """algorithm: "hybrid" (dense hot dimensions + hashed cold lists, the
-        default) or "posting" (one warp per query row walking posting lists)."""
+        default) or "posting" (one warp per query row walking posting lists).
+        verify_stream: bulk_cosine_host checks every chunk's checksum on the
+        device against its host copy (and records them, see stream_checksums)."""
         self._lib = _abi.load()
         self.dim = int(dim)
         self.chunk_rows = int(chunk_rows)
@@ -93,6 +95,8 @@ class SparseCosine:
         flags = (SS_VALIDATE if validate else 0)
         if algorithm == "posting":
             flags |= _abi.SS_ALGO_POSTING_LISTS
+        if verify_stream:
+            flags |= _abi.SS_VERIFY_STREAM
         h = ctypes.c_void_p()
         st = self._lib.ss_create(ctypes.byref(h), self.device, self.dim, self.chunk_rows, flags)
         if st != _abi.SS_OK:
@@ -212,6 +216,29 @@ class SparseCosine:
                                           _stream_ptr(stream)), "ss_topk_all")
         return best_val, best_item
 
+    def tile_checksum(self, tile: torch.Tensor, stream=None):
+        """(bits_sum, value_sum) of a 2-D float32 device tile (rows contiguous):
+        the sum of the values' bit patterns as unsigned 32-bit integers modulo
+        2**64, and the sum of the values in double.  Synchronises."""
+        assert tile.dtype == torch.float32 and tile.dim() == 2 and tile.stride(1) == 1
+        sums = torch.zeros(2, dtype=torch.int64, device=tile.device)
+        self._check(self._lib.ss_tile_checksum(self._h, _ptr(tile), int(tile.shape[0]),
+                                               int(tile.shape[1]), int(tile.stride(0)),
+                                               ctypes.c_void_p(sums.data_ptr()),
+                                               ctypes.c_void_p(sums.data_ptr() + 8),
+                                               _stream_ptr(stream)), "ss_tile_checksum")
+        host = sums.cpu().numpy()
+        return int(host[:1].view(np.uint64)[0]), float(host[1:].view(np.float64)[0])
+
+    def stream_checksums(self):
+        """Per chunk of the last verified bulk_cosine_host pass: (bits_sum, value_sum)."""
+        out, c = [], 0
+        b, v = ctypes.c_uint64(0), ctypes.c_double(0.0)
+        while self._lib.ss_stream_checksum(self._h, c, ctypes.byref(b), ctypes.byref(v)) == _abi.SS_OK:
+            out.append((int(b.value), float(v.value)))
+            c += 1
+        return out
+
     def bulk_cosine_host(self, queries, items, out: Optional[np.ndarray] = None,
                          consumer: Optional[Callable] = None, ring_depth: int = 3,
                          timeout_ms: int = 0):
@@ -276,3 +303,19 @@ class SparseCosine:
 
 def library_path() -> str:
     return _abi.library_path()
+
+
+def tile_checksum_host(tile: np.ndarray):
+    """(bits_sum, value_sum) of a 2-D float32 host array (rows contiguous),
+    computed by the library's host routine (the counterpart of
+    SparseCosine.tile_checksum)."""
+    assert tile.dtype == np.float32 and tile.ndim == 2
+    empty = tile.size == 0
+    assert empty or tile.strides[1] == 4
+    ld = int(tile.shape[1]) if empty else int(tile.strides[0] // 4)
+    b, v = ctypes.c_uint64(0), ctypes.c_double(0.0)
+    st = _abi.load().ss_tile_checksum_host(ctypes.c_void_p(tile.ctypes.data), int(tile.shape[0]),
+                                           int(tile.shape[1]), ld, ctypes.byref(b), ctypes.byref(v))
+    if st != _abi.SS_OK:
+        raise SparseCosError(st, "ss_tile_checksum_host: bad arguments")
+    return int(b.value), float(v.value)

@@ -21,6 +21,7 @@ SS_ERR_TIMEOUT = 7
 SS_ERR_LIMIT = 8
 SS_VALIDATE = 0x1
 SS_TOPK_MAX = 64
+SS_VERIFY_STREAM = 0x4
 SS_ALGO_POSTING_LISTS = 0x2
 SS_MAX_CHUNK_ROWS = 65536
 
@@ -57,6 +58,9 @@ SIGNATURES = {
     "ss_topk_reset": (_I32, [_P, _I64, _I32, _P, _P, _P]),
     "ss_score_chunk_topk": (_I32, [_P, _CSR, _P, _P, _P, _I32, _P, _P, _P]),
     "ss_topk_all": (_I32, [_P, _CSR, _P, _CSR, _P, _I32, _P, _P, _P]),
+    "ss_tile_checksum": (_I32, [_P, _P, _I64, _I64, _I64, _P, _P, _P]),
+    "ss_tile_checksum_host": (_I32, [_P, _I64, _I64, _I64, _P, _P]),
+    "ss_stream_checksum": (_I32, [_P, _I64, _P, _P]),
     "ss_bulk_cosine_host": (_I32, [_P, _CSR, _CSR, _P, _I64, ss_chunk_consumer, _P, _I32, _I32]),
     "ss_validate_csr": (_I32, [_P, _CSR, _P]),
     "ss_check_device": (_I32, [_P, _P]),

@@ -514,6 +514,38 @@ ss_status ss_score_chunk_topk(ss_handle *h, const ss_csr *queries, const float *
   return SS_OK;
 }
 
+ss_status ss_tile_checksum(ss_handle *h, const float *tile, int64_t n_rows, int64_t n_cols,
+                           int64_t ld, uint64_t *bits_sum, double *value_sum, void *stream) {
+  if (!h) return SS_ERR_INVALID_ARG;
+  if (n_rows < 0 || n_cols < 0 || ld < n_cols || !bits_sum || !value_sum ||
+      (n_rows > 0 && n_cols > 0 && !tile))
+    return fail(h, SS_ERR_INVALID_ARG, "ss_tile_checksum: bad arguments");
+  ss_status st = set_device(h);
+  if (st != SS_OK) return st;
+  SS_CUDA(h, launch_tile_checksum(tile, n_rows, n_cols, ld, bits_sum, value_sum, h->sm_count,
+                                  as_stream(stream)));
+  if (n_rows > 0 && n_cols > 0) h->launches += 1;
+  return SS_OK;
+}
+
+ss_status ss_tile_checksum_host(const float *tile, int64_t n_rows, int64_t n_cols, int64_t ld,
+                                uint64_t *bits_sum, double *value_sum) {
+  if (n_rows < 0 || n_cols < 0 || ld < n_cols || !bits_sum || !value_sum ||
+      (n_rows > 0 && n_cols > 0 && !tile))
+    return SS_ERR_INVALID_ARG;
+  tile_checksum_host(tile, n_rows, n_cols, ld, bits_sum, value_sum);
+  return SS_OK;
+}
+
+ss_status ss_stream_checksum(const ss_handle *h, int64_t chunk, uint64_t *bits_sum,
+                             double *value_sum) {
+  if (!h || !bits_sum || !value_sum || chunk < 0 || chunk >= (int64_t)h->host.log_bits.size())
+    return SS_ERR_INVALID_ARG;
+  *bits_sum = h->host.log_bits[(size_t)chunk];
+  *value_sum = h->host.log_values[(size_t)chunk];
+  return SS_OK;
+}
+
 ss_status ss_topk_all(ss_handle *h, const ss_csr *queries, const float *inv_q, const ss_csr *items,
                       const float *inv_i, int32_t k, float *best_val, int64_t *best_item,
                       void *stream) {

@@ -123,6 +123,14 @@ struct ss_host_pass {
   size_t cap[kBuffers] = {};
   std::vector<float *> slots;
   size_t slot_bytes = 0;
+  // Stream verification: per ring slot, the device checksum {bits, value}
+  // copied to page-locked host memory with the tile; per chunk of the last
+  // pass, the checksums found on the host.
+  void *dev_sums = nullptr;             // [ring][2] x 8 bytes, device
+  void *host_sums = nullptr;            // [ring][2] x 8 bytes, page-locked
+  int32_t sums_slots = 0;
+  std::vector<uint64_t> log_bits;
+  std::vector<double> log_values;
 };
 void free_host_pass(ss_host_pass &hp);
 
@@ -217,6 +225,14 @@ cudaError_t launch_topk_reset(int64_t n_q, int32_t k, float *best_val, int64_t *
                               int32_t *cand_n, int sm_count, cudaStream_t s);
 cudaError_t launch_topk_merge(const ss_topk &t, int64_t n_q, int64_t item_base, float *best_val,
                               int64_t *best_item, int sm_count, cudaStream_t s);
+
+// Checksums of a row-major float tile (see checksum.cu): the device version
+// adds into *bits_sum / *value_sum (device), the host version writes them.
+cudaError_t launch_tile_checksum(const float *tile, int64_t n_rows, int64_t n_cols, int64_t ld,
+                                 uint64_t *bits_sum, double *value_sum, int sm_count,
+                                 cudaStream_t s);
+void tile_checksum_host(const float *tile, int64_t n_rows, int64_t n_cols, int64_t ld,
+                        uint64_t *bits_sum, double *value_sum);
 
 // Kernels queued by one launch_build_index call.
 constexpr int kIndexKernels = 5;

@@ -50,6 +50,12 @@ ss_status scuda(ss_handle *h, cudaError_t e, const char *what) {
     cudaError_t e_ = (call);                            \
     if (e_ != cudaSuccess) return scuda(h, e_, #call);  \
   } while (0)
+#define SS_CUDA_LAUNCH(call)                            \
+  do {                                                  \
+    cudaError_t e_ = (call);                            \
+    if (e_ != cudaSuccess) return scuda(h, e_, #call);  \
+    h->launches += 1;                                   \
+  } while (0)
 
 ss_status wait_event(ss_handle *h, cudaEvent_t ev, int32_t timeout_ms, const char *what) {
   const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms);
@@ -184,6 +190,10 @@ void free_host_pass(ss_host_pass &hp) {
     hp.buf[r] = nullptr;
     hp.cap[r] = 0;
   }
+  cudaFree(hp.dev_sums);
+  cudaFreeHost(hp.host_sums);
+  hp.dev_sums = hp.host_sums = nullptr;
+  hp.sums_slots = 0;
   if (hp.comp) cudaStreamDestroy(hp.comp);
   if (hp.copy) cudaStreamDestroy(hp.copy);
   hp.comp = hp.copy = nullptr;
@@ -213,8 +223,11 @@ extern "C" ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *qh, const s
 
   // Direct stores when the caller's output is page-locked, the device can
   // address it, and nobody else needs the tile; otherwise the ring.
+  const bool verify = (h->flags & SS_VERIFY_STREAM) != 0;
+  hp.log_bits.clear();
+  hp.log_values.clear();
   float *out_dev = nullptr;
-  if (out_host && !consumer) {
+  if (out_host && !consumer && !verify) {
     cudaPointerAttributes attr;
     if (cudaPointerGetAttributes(&attr, out_host) == cudaSuccess && attr.type == cudaMemoryTypeHost &&
         attr.devicePointer)
@@ -268,6 +281,18 @@ extern "C" ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *qh, const s
   if ((st = ensure_buf(h, HP::kOut1, tile_bytes)) != SS_OK) return st;
   if ((st = ensure_ring(h, R, tile_bytes)) != SS_OK) return st;
   float *dbuf[2] = {static_cast<float *>(hp.buf[HP::kOut0]), static_cast<float *>(hp.buf[HP::kOut1])};
+  if (verify && hp.sums_slots < R) {
+    cudaFree(hp.dev_sums);
+    cudaFreeHost(hp.host_sums);
+    hp.dev_sums = hp.host_sums = nullptr;
+    hp.sums_slots = 0;
+    S_CUDA(cudaMalloc(&hp.dev_sums, 16 * (size_t)R));
+    S_CUDA(cudaHostAlloc(&hp.host_sums, 16 * (size_t)R, cudaHostAllocDefault));
+    hp.sums_slots = R;
+  }
+  // Slot r of the checksum buffers: {bits_sum (u64), value_sum (double)}.
+  auto dev_sum_slot = [&](int64_t c) { return static_cast<unsigned char *>(hp.dev_sums) + 16 * (c % R); };
+  auto host_sum_slot = [&](int64_t c) { return static_cast<unsigned char *>(hp.host_sums) + 16 * (c % R); };
 
   int64_t delivered = 0;
   auto deliver = [&](int64_t c) -> ss_status {
@@ -275,6 +300,18 @@ extern "C" ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *qh, const s
     ss_status s2 = wait_event(h, hp.copied[c % R], timeout_ms, "ss_bulk_cosine_host copy");
     if (s2 != SS_OK) return s2;
     const float *slot = hp.slots[c % R];
+    if (verify) {
+      uint64_t hb = 0, db = 0;
+      double hv = 0.0;
+      tile_checksum_host(slot, n_q, w, w, &hb, &hv);
+      memcpy(&db, host_sum_slot(c), sizeof(db));
+      if (hb != db)
+        return sfail(h, SS_ERR_DEVICE_CHECK,
+                     "ss_bulk_cosine_host: chunk %lld checksum differs between device (%llu) and host copy (%llu)",
+                     (long long)c, (unsigned long long)db, (unsigned long long)hb);
+      hp.log_bits.push_back(hb);
+      hp.log_values.push_back(hv);
+    }
     if (out_host) scatter_rows(out_host, ld_out, rb, slot, w, w, n_q);
     if (consumer && consumer(user, c, rb, re, slot, w, n_q) != 0)
       return sfail(h, SS_ERR_INVALID_ARG, "ss_bulk_cosine_host: consumer stopped the pass");
@@ -291,11 +328,21 @@ extern "C" ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *qh, const s
     if (c >= 2) S_CUDA(cudaStreamWaitEvent(hp.comp, hp.out_free[b], 0));
     ss_index *idx = views[(rb % span) / C];
     if ((st = ss_score_chunk(h, &qd, inv_q, idx, inv_i + rb, dbuf[b], w, vs)) != SS_OK) return st;
+    if (verify) {
+      // The checksum slot of chunk c - R was copied out before this chunk's
+      // buffer became free (same copy stream, earlier).
+      S_CUDA(cudaMemsetAsync(dev_sum_slot(c), 0, 16, hp.comp));
+      unsigned char *ds = dev_sum_slot(c);
+      SS_CUDA_LAUNCH(launch_tile_checksum(dbuf[b], n_q, w, w, reinterpret_cast<uint64_t *>(ds),
+                                          reinterpret_cast<double *>(ds + 8), h->sm_count, hp.comp));
+    }
     S_CUDA(cudaEventRecord(hp.done[b], hp.comp));
     S_CUDA(cudaStreamWaitEvent(hp.copy, hp.done[b], 0));
     // Slot c % R was last used by chunk c - R, delivered before this point.
     S_CUDA(cudaMemcpyAsync(hp.slots[c % R], dbuf[b], sizeof(float) * (size_t)(n_q * w),
                            cudaMemcpyDeviceToHost, hp.copy));
+    if (verify)
+      S_CUDA(cudaMemcpyAsync(host_sum_slot(c), dev_sum_slot(c), 16, cudaMemcpyDeviceToHost, hp.copy));
     S_CUDA(cudaEventRecord(hp.copied[c % R], hp.copy));
     S_CUDA(cudaEventRecord(hp.out_free[b], hp.copy));
     // Keep R - 1 chunks in flight; deliver the oldest.

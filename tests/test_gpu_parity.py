@@ -454,3 +454,36 @@ def test_bulk_cosine_host_consumer_can_stop(sec):
             h.bulk_cosine_host(Q, I, consumer=lambda c, b, e, t: 1 if c == 2 else 0)
         # still usable
         h.bulk_cosine_host(Q, I, consumer=lambda c, b, e, t: 0)
+
+
+# ------------------------------------------------------------- checksums
+def test_device_checksum_matches_host_checksum(sec):
+    rng = np.random.default_rng(9)
+    big = rng.standard_normal((777, 3000)).astype(np.float32)
+    win = big[:, 5:2905]
+    with sec.SparseCosine(64) as h:
+        d = torch.from_numpy(big).cuda()[:, 5:2905]
+        db, dv = h.tile_checksum(d)
+    hb, hv = sec.tile_checksum_host(win)
+    nb = int(np.ascontiguousarray(win).view(np.uint32).astype(np.uint64).sum(dtype=np.uint64))
+    assert db == hb == nb
+    assert abs(dv - hv) <= 1e-6 * max(1.0, abs(hv))
+
+
+def test_verified_stream_pass(sec):
+    # With SS_VERIFY_STREAM the pass checks each chunk's device checksum
+    # against its host copy and records them; the result is unchanged.
+    cfg = CONFIGS["d65k_q1k_i10k"]
+    Q, I = generate_rows(cfg, 0, 0, 150), generate_rows(cfg, 1, 0, 5000)
+    ref = _gpu_cosine(sec, Q, I, chunk_rows=2048)
+    with sec.SparseCosine(cfg.dim, chunk_rows=2048, verify_stream=True) as h:
+        pinned = torch.empty((Q.n_rows, I.n_rows), dtype=torch.float32).pin_memory()
+        h.bulk_cosine_host(Q, I, out=pinned, ring_depth=3)
+        sums = h.stream_checksums()
+    got = pinned.numpy()
+    assert np.array_equal(got.view(np.int32), ref.view(np.int32))
+    assert len(sums) == 3
+    for c, (bits, value) in enumerate(sums):
+        tile = np.ascontiguousarray(got[:, c * 2048:(c + 1) * 2048])
+        assert bits == int(tile.view(np.uint32).astype(np.uint64).sum(dtype=np.uint64))
+        assert abs(value - float(tile.astype(np.float64).sum())) <= 1e-6 * max(1.0, abs(value))
