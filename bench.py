@@ -133,21 +133,26 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def captured_traffic():
-    """DRAM bytes per scoring launch from the committed ncu capture, or None
-    when the kernel source has changed since the counters were taken."""
+def captured_traffic(workload, kernel):
+    """DRAM bytes per scoring launch from a committed ncu capture of this
+    workload and kernel, or None when there is none or the kernel's source
+    has changed since the counters were taken."""
     import hashlib
 
     path = os.path.join(ROOT, "profiles", "score_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        rec = json.load(f)
-    src = os.path.join(ROOT, rec["source"])
-    with open(src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
-            return None
-    return int(rec["dram_bytes_read"]) + int(rec["dram_bytes_write"])
+        recs = json.load(f)["records"]
+    for rec in recs:
+        if rec["workload"] != workload or rec["kernel"] != kernel:
+            continue
+        src = os.path.join(ROOT, rec["source"])
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
+                return None
+        return int(rec["dram_bytes_read"]) + int(rec["dram_bytes_write"])
+    return None
 
 
 def chunk_algorithmic_bytes(Q, I):
@@ -366,9 +371,11 @@ def run_ours(args):
     per_launch_s = statistics.mean(score_ms) / 1e3
     achieved = per_launch_bytes / per_launch_s / 1e9
     peak, peak_kind = measured_peaks()
+    kernel = "k_score_lists" if index_stats["algorithm"] == 1 else "k_score_tiles"
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": captured_traffic(),
-            "kernel": "k_score_tiles (ss_score_chunk)",
+            "frac": achieved / peak, "traffic": captured_traffic(cfg.name, kernel),
+            "kernel": kernel + (" (posting lists" if kernel == "k_score_lists" else " (item tiles")
+                      + ", ss_score_chunk)",
             "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
             "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
             "bytes_per_launch": per_launch_bytes, "launch_ms": 1e3 * per_launch_s,

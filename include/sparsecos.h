@@ -54,12 +54,27 @@ typedef int32_t ss_status;
 
 /* ss_create flags */
 #define SS_VALIDATE 0x1 /* check CSR inputs on the device (synchronises) */
-/* Scoring algorithm.  The default splits dimensions into a few dense "hot"
- * ones (multiplied as a small dense product) and the rest (hashed lists in
- * shared memory).  SS_ALGO_POSTING_LISTS instead walks, for each query
- * nonzero, the chunk's posting list of that dimension (one warp per query
- * row).  Both give the same cosines up to float32 summation order. */
+/* Scoring algorithm of the chunk indexes.
+ *  - item tiles ("hybrid"): a few dense "hot" dimensions multiplied as a
+ *    small dense product, the rest through per-tile inverted indexes in
+ *    shared memory; float32 products summed in ascending dimension order,
+ *    then scaled by inv_q * inv_i.  Best for short rows with a skewed
+ *    (Zipf-like) dimension distribution.
+ *  - posting lists: per query row, the chunk's posting list of each of its
+ *    dimensions is walked and the products of the normalised values
+ *    (q_k inv_q)(v_ik inv_i) are summed exactly in fixed point (resolution
+ *    2^-38), then rounded to float32 once.  Best for long or evenly spread
+ *    rows.  Needs inverse norms whose products bound the scores by 1 (those
+ *    of ss_row_norms); larger normalised products end the call with
+ *    SS_ERR_DEVICE_CHECK.
+ * With neither flag the handle chooses per item matrix: its first build is a
+ * tiled one, and if more than half of the item tiles found no room for their
+ * inverted index the matrix is rebuilt, and afterwards always built, as
+ * posting lists (one synchronisation per item matrix).  Both give the
+ * cosines within a few float32 roundings; each is bitwise deterministic.
+ * Setting both flags is SS_ERR_INVALID_ARG. */
 #define SS_ALGO_POSTING_LISTS 0x2
+#define SS_ALGO_TILES 0x8
 /* ss_bulk_cosine_host verifies every streamed chunk: its checksum (see
  * ss_tile_checksum) is taken on the device before the copy and on the host
  * after it, and must agree; the pass then always goes through the ring. */
@@ -127,7 +142,9 @@ ss_status ss_build_item_index(ss_handle *h, const ss_csr *items, int64_t row_beg
  * queries: device CSR; inv_q: device float32[n_q] from ss_row_norms;
  * inv_i: device float32 pointer to the chunk's first item norm (the item
  * norm array + row_begin); out: device float32, row-major with leading
- * dimension ld_out >= chunk width.  Products and sums are float32.
+ * dimension ld_out >= chunk width.  Tiled indexes: float32 products and
+ * sums; posting-list indexes: exact fixed-point sums of float32 products of
+ * the normalised values (see SS_ALGO_POSTING_LISTS).
  * Errors: SS_ERR_INVALID_ARG, SS_ERR_CUDA.
  */
 ss_status ss_score_chunk(ss_handle *h, const ss_csr *queries, const float *inv_q,
@@ -136,8 +153,8 @@ ss_status ss_score_chunk(ss_handle *h, const ss_csr *queries, const float *inv_q
 
 /*
  * Number of chunks one ss_build_item_indexes call can build: enough that the
- * builder's blocks (one per 256-item tile) cover the GPU's SMs, at most 8;
- * always 1 with SS_ALGO_POSTING_LISTS.  Fixed at ss_create.
+ * builder's blocks (one per 256-item tile) cover the GPU's SMs, at most 8.
+ * The same for both algorithms.  Fixed at ss_create.
  */
 int32_t ss_build_batch(const ss_handle *h);
 
@@ -177,8 +194,7 @@ ss_status ss_score_all(ss_handle *h, const ss_csr *queries, const float *inv_q,
  *   best_val[q * k + r], best_item[q * k + r], r < k
  * (device float32 and int64, row-major; -INFINITY and -1 where fewer than k
  * items have been seen).  The scores are the very values ss_score_chunk
- * would store.  Needs the default (hybrid) algorithm; 1 <= k <=
- * SS_TOPK_MAX and k * (ceil(chunk_rows / 256) + 1) <= 8192, else
+ * would store (either algorithm); 1 <= k <= SS_TOPK_MAX and k * (ceil(chunk_rows / 256) + 1) <= 8192, else
  * SS_ERR_LIMIT.
  *
  * ss_topk_reset: starts a pass for n_q query rows (fills best_val with
@@ -292,7 +308,7 @@ ss_status ss_invalidate(ss_handle *h);
  *   [2] item tiles (hybrid)                         [3] hot dimensions H
  *   [4] entries in the heavy-item list              [5] widest ELL column
  *   [6] ELL entries stored, padding included        [7] item tiles without an
- *                                                       inverted-index image
+ *       (posting lists: entries in the chunk)           inverted-index image
  * Fields that do not apply to the algorithm are 0.
  */
 ss_status ss_index_stats(ss_handle *h, const ss_index *idx, int64_t *stats, void *stream);
@@ -319,7 +335,7 @@ ss_status ss_index_stats(ss_handle *h, const ss_index *idx, int64_t *stats, void
  *   (indptr[row_end] - indptr[row_begin]), known to the caller; the lists
  *   are sized by it (a smaller value truncates them on the device).
  * Returns SS_ERR_LIMIT, without queueing work, when the scratch needed
- * (about 8 * (dim + 1) + 6 * chunk_nnz + 4 * (n_q + chunk rows) bytes)
+ * (about 8 * (dim + 1) + 14 * chunk_nnz + 4 * (n_q + chunk rows) bytes)
  * exceeds SS_NOALLOC_SCRATCH_BYTES or the chunk exceeds SS_MAX_CHUNK_ROWS.
  * The first call on a device looks up the array's device address (no
  * allocation); make that first call before any stream capture.  Every call

@@ -77,12 +77,15 @@ def _host_csr(batch):
 class SparseCosine:
     """One library handle: a device, a dimension and a chunk size."""
 
-    ALGORITHMS = ("hybrid", "posting")
+    ALGORITHMS = ("auto", "hybrid", "posting")
 
     def __init__(self, dim: int, chunk_rows: int = DEFAULT_CHUNK_ROWS, device: int = 0,
-                 validate: bool = False, algorithm: str = "hybrid", verify_stream: bool = False):
-        """algorithm: "hybrid" (dense hot dimensions + hashed cold lists, the
-        default) or "posting" (one warp per query row walking posting lists).
+                 validate: bool = False, algorithm: str = "auto", verify_stream: bool = False):
+        """algorithm: "hybrid" (item tiles: dense hot dimensions + per-tile
+        inverted indexes in shared memory), "posting" (per query row, the
+        chunk's posting lists of its dimensions, summed exactly in fixed
+        point), or "auto" (the default: per item matrix, posting lists when
+        most item tiles of its first build overflow).
         verify_stream: bulk_cosine_host checks every chunk's checksum on the
         device against its host copy (and records them, see stream_checksums)."""
         self._lib = _abi.load()
@@ -95,6 +98,8 @@ class SparseCosine:
         flags = (SS_VALIDATE if validate else 0)
         if algorithm == "posting":
             flags |= _abi.SS_ALGO_POSTING_LISTS
+        elif algorithm == "hybrid":
+            flags |= _abi.SS_ALGO_TILES
         if verify_stream:
             flags |= _abi.SS_VERIFY_STREAM
         h = ctypes.c_void_p()
@@ -281,7 +286,9 @@ class SparseCosine:
                     "ss_validate_csr")
 
     def index_stats(self, index, stream=None) -> dict:
-        """Diagnostics of the last built index (synchronises the stream)."""
+        """Diagnostics of the last built index (synchronises the stream).
+        "algorithm" is 0 for item tiles, 1 for posting lists; for posting
+        lists "ell_entries" holds the chunk's entries."""
         out = (ctypes.c_int64 * 8)()
         self._check(self._lib.ss_index_stats(self._h, index, out, _stream_ptr(stream)),
                     "ss_index_stats")

@@ -23,6 +23,7 @@ SS_VALIDATE = 0x1
 SS_TOPK_MAX = 64
 SS_VERIFY_STREAM = 0x4
 SS_ALGO_POSTING_LISTS = 0x2
+SS_ALGO_TILES = 0x8
 SS_MAX_CHUNK_ROWS = 65536
 
 

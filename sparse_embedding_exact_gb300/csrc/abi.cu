@@ -80,6 +80,9 @@ ss_status status_from_device(ss_handle *h, int32_t code, const char *what) {
       return fail(h, SS_ERR_DEVICE_CHECK, "%s: chunk nnz exceeds the index capacity", what);
     case DEV_STALL:
       return fail(h, SS_ERR_DEVICE_CHECK, "%s: a kernel loop ran out of its iteration bound", what);
+    case DEV_RANGE:
+      return fail(h, SS_ERR_DEVICE_CHECK,
+                  "%s: a product of normalised values exceeded 1 (inverse norms not those of the rows)", what);
     default:
       return fail(h, SS_ERR_DEVICE_CHECK, "%s: device check code %d", what, code);
   }
@@ -94,21 +97,37 @@ ss_status validate(ss_handle *h, const ss_csr &m, cudaStream_t s, const char *wh
   return status_from_device(h, code, what);
 }
 
-// Grows the per-chunk entry capacity (posting lists, or the hybrid path's
-// heavy-item list) to hold `need` entries; synchronises the device when it
-// has to reallocate.
-ss_status ensure_capacity(ss_handle *h, int64_t need) {
-  if (h->algo == ALGO_POSTING) {
+// Posting-list workspace (column counters and pointers for a build batch,
+// the scorer's row counter); allocated on first use.
+ss_status ensure_posting_workspace(ss_handle *h) {
+  if (h->col_ptr) return SS_OK;
+  const size_t n = (size_t)h->build_batch * (size_t)(h->dim + 1);
+  h->scan_tiles = scan_tile_count((int64_t)n);
+  SS_CUDA(h, cudaDeviceSynchronize());
+  SS_CUDA(h, cudaMalloc(&h->col_cnt, sizeof(int32_t) * n));
+  SS_CUDA(h, cudaMalloc(&h->scan_part, sizeof(int32_t) * (size_t)(h->scan_tiles + 1)));
+  SS_CUDA(h, cudaMalloc(&h->col_ptr, sizeof(int32_t) * n));
+  return SS_OK;
+}
+
+// Grows the entry capacity of one build (posting lists, or the hybrid
+// path's heavy-item list) to hold `need` entries; synchronises the device
+// when it has to reallocate.
+ss_status ensure_capacity(ss_handle *h, int32_t algo, int64_t need) {
+  if (algo == ALGO_POSTING) {
     if (need <= h->post_cap) return SS_OK;
     const int64_t cap = std::max<int64_t>(need, h->post_cap + h->post_cap / 2);
     SS_CUDA(h, cudaDeviceSynchronize());
     cudaFree(h->post_item);
     cudaFree(h->post_val);
+    cudaFree(h->post_hat);
     h->post_item = nullptr;
     h->post_val = nullptr;
+    h->post_hat = nullptr;
     h->post_cap = 0;
     SS_CUDA(h, cudaMalloc(&h->post_item, sizeof(uint16_t) * (size_t)cap));
     SS_CUDA(h, cudaMalloc(&h->post_val, sizeof(float) * (size_t)cap));
+    SS_CUDA(h, cudaMalloc(&h->post_hat, sizeof(int2) * (size_t)cap));
     h->post_cap = cap;
     return SS_OK;
   }
@@ -139,9 +158,13 @@ void free_workspace(ss_handle *h) {
   h->cand_n = nullptr;
   h->cand_elems = h->cand_rows = 0;
   void *ptrs[] = {h->d_status, h->col_cnt, h->col_ptr, h->scan_part, h->post_item, h->post_val,
-                  h->hot, h->slab, h->ell, h->meta, h->heavy_k, h->heavy_v, h->heavy_item,
-                  h->counters, h->image, h->qhot, h->qcold, h->qcold_n, h->heavy_tbl};
+                  h->post_hat, h->row_next, h->probe, h->hot, h->slab, h->ell, h->meta, h->heavy_k,
+                  h->heavy_v, h->heavy_item, h->counters, h->image, h->qhot, h->qcold,
+                  h->qcold_n, h->heavy_tbl};
   for (void *p : ptrs) cudaFree(p);
+  h->post_hat = nullptr;
+  h->row_next = nullptr;
+  h->probe = nullptr;
   h->counters = nullptr;
   h->heavy_tbl = nullptr;
   h->image = nullptr;
@@ -161,11 +184,14 @@ void free_workspace(ss_handle *h) {
   h->heavy_cap = 0;
 }
 
-ss_status build_chunk(ss_handle *h, const ss_csr &items, int64_t rb, int64_t re, cudaStream_t s) {
-  // The chunk holds at most items.nnz entries: size the lists for that.
-  ss_status st = ensure_capacity(h, std::max<int64_t>(items.nnz, 1));
+ss_status build_algo(ss_handle *h, int32_t algo, const ss_csr &items, int64_t rb, int64_t re,
+                     cudaStream_t s) {
+  // A build holds at most items.nnz entries: size the lists for that.
+  ss_status st = ensure_capacity(h, algo, std::max<int64_t>(items.nnz, 1));
   if (st != SS_OK) return st;
-  if (h->algo == ALGO_POSTING) {
+  h->algo = algo;
+  if (algo == ALGO_POSTING) {
+    if ((st = ensure_posting_workspace(h)) != SS_OK) return st;
     SS_CUDA(h, launch_build_index(h, items, rb, re, s));
     h->launches += kIndexKernels;
     return SS_OK;
@@ -177,15 +203,47 @@ ss_status build_chunk(ss_handle *h, const ss_csr &items, int64_t rb, int64_t re,
   return SS_OK;
 }
 
+bool same_auto_source(const ss_handle *h, const ss_csr &m) {
+  return h->auto_src[0] == m.indptr && h->auto_src[1] == m.indices && h->auto_src[2] == m.values &&
+         h->auto_src_rows == m.n_rows && h->auto_src_nnz == m.nnz;
+}
+
+// Builds the chunk indexes of [rb, re).  MODE_AUTO: for a new item matrix,
+// the hot set is chosen and every item tile of this first build is probed:
+// when more than kAutoOverflowShare of them hold more cold entries than a
+// shared-memory image takes (rows too long or too spread for item tiles),
+// the matrix is built as posting lists from then on, else as item tiles.
+// Reading the probe synchronises the stream once per item matrix.
+ss_status build_chunk(ss_handle *h, const ss_csr &items, int64_t rb, int64_t re, cudaStream_t s) {
+  if (h->mode == MODE_POSTING) return build_algo(h, ALGO_POSTING, items, rb, re, s);
+  if (h->mode == MODE_TILES) return build_algo(h, ALGO_HYBRID, items, rb, re, s);
+  if (!same_auto_source(h, items)) {
+    int queued = 0;
+    SS_CUDA(h, launch_hot_select(h, items, s, &queued));
+    SS_CUDA(h, launch_auto_probe(h, items, rb, re, h->probe, s));
+    h->launches += queued + 1;
+    int32_t counts[2] = {0, 0};
+    SS_CUDA(h, cudaMemcpyAsync(counts, h->probe, sizeof(counts), cudaMemcpyDeviceToHost, s));
+    SS_CUDA(h, cudaStreamSynchronize(s));
+    h->auto_algo = ((double)counts[1] > kAutoOverflowShare * (double)counts[0]) ? ALGO_POSTING : ALGO_HYBRID;
+    h->auto_src[0] = items.indptr;
+    h->auto_src[1] = items.indices;
+    h->auto_src[2] = items.values;
+    h->auto_src_rows = items.n_rows;
+    h->auto_src_nnz = items.nnz;
+  }
+  return build_algo(h, h->auto_algo, items, rb, re, s);
+}
+
 cudaError_t score(ss_handle *h, const ss_csr &q, const float *inv_q, const ss_index &idx,
                   const float *inv_i, float *out, int64_t ld_out, cudaStream_t s,
                   const ss_topk *topk = nullptr) {
+  int queued = 0;
   if (idx.algo == ALGO_POSTING) {
-    const cudaError_t e = launch_score_chunk(h, q, inv_q, idx, inv_i, out, ld_out, s);
-    if (e == cudaSuccess && q.n_rows > 0 && idx.n_items > 0) h->launches += 1;
+    const cudaError_t e = launch_score_lists(h, q, inv_q, idx, inv_i, out, ld_out, s, &queued, topk);
+    h->launches += queued;
     return e;
   }
-  int queued = 0;
   const cudaError_t e = launch_score_hybrid(h, q, inv_q, idx, inv_i, out, ld_out, s, &queued, topk);
   h->launches += queued;
   return e;
@@ -215,8 +273,6 @@ ss_status ensure_topk_space(ss_handle *h, int64_t n_q, int64_t cap) {
 
 ss_status check_topk_args(ss_handle *h, int32_t k, const float *best_val, const int64_t *best_item,
                           int64_t n_q, const char *what) {
-  if (h->algo != ALGO_HYBRID)
-    return fail(h, SS_ERR_INVALID_ARG, "%s: the top-k epilogue needs the default (hybrid) algorithm", what);
   if (k < 1 || k > kTopkMax) return fail(h, SS_ERR_LIMIT, "%s: k = %d outside [1, %d]", what, k, kTopkMax);
   if ((int64_t)k * (h->chunk_tiles + 1) > kTopkEntries)
     return fail(h, SS_ERR_LIMIT, "%s: k = %d too large for chunks of %d rows (k * (chunk_rows / 256 + 1) <= %d)",
@@ -266,24 +322,36 @@ ss_status ss_create(ss_handle **out, int device, int64_t dim, int32_t chunk_rows
   h->dim = dim;
   h->chunk_rows = chunk_rows;
   h->flags = flags;
-  h->algo = (flags & SS_ALGO_POSTING_LISTS) ? ALGO_POSTING : ALGO_HYBRID;
+  if ((flags & SS_ALGO_POSTING_LISTS) && (flags & SS_ALGO_TILES)) {
+    delete h;
+    return SS_ERR_INVALID_ARG;
+  }
+  h->mode = (flags & SS_ALGO_POSTING_LISTS) ? MODE_POSTING : (flags & SS_ALGO_TILES) ? MODE_TILES : MODE_AUTO;
+  h->algo = (h->mode == MODE_POSTING) ? ALGO_POSTING : ALGO_HYBRID;
   cudaError_t e = cudaSetDevice(device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, device);
   if (e == cudaSuccess) e = cudaMalloc(&h->d_status, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int32_t));
-  if (h->algo == ALGO_POSTING) {
-    h->scan_tiles = scan_tile_count(dim + 1);
-    if (e == cudaSuccess) e = cudaMalloc(&h->col_cnt, sizeof(int32_t) * (size_t)(dim + 1));
-    if (e == cudaSuccess) e = cudaMalloc(&h->col_ptr, sizeof(int32_t) * (size_t)(dim + 1));
-    if (e == cudaSuccess) e = cudaMalloc(&h->scan_part, sizeof(int32_t) * (size_t)(h->scan_tiles + 1));
-  } else {
+  if (e == cudaSuccess) e = cudaMalloc(&h->row_next, 2 * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(h->row_next, 0, 2 * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMalloc(&h->probe, 2 * sizeof(int32_t));
+  {
     using namespace hyb;
-    // One build launch covers enough chunks to give every SM a tile (a
-    // chunk alone has only chunk_rows / 256 tiles, one block each).
+    // One build covers enough chunks to give every SM a tile (a chunk alone
+    // has only chunk_rows / 256 tiles, one block each).
     h->chunk_tiles = (chunk_rows + kTI - 1) / kTI;
     const int sms = h->sm_count > 0 ? h->sm_count : 1;
     h->build_batch = std::max(1, std::min(kMaxBuildBatch, (sms + h->chunk_tiles - 1) / h->chunk_tiles));
     h->max_tiles = h->build_batch * h->chunk_tiles;
+  }
+  if (e == cudaSuccess && h->mode == MODE_POSTING) {
+    const size_t n = (size_t)h->build_batch * (size_t)(dim + 1);
+    h->scan_tiles = scan_tile_count((int64_t)n);
+    e = cudaMalloc(&h->col_cnt, sizeof(int32_t) * n);
+    if (e == cudaSuccess) e = cudaMalloc(&h->col_ptr, sizeof(int32_t) * n);
+    if (e == cudaSuccess) e = cudaMalloc(&h->scan_part, sizeof(int32_t) * (size_t)(h->scan_tiles + 1));
+  } else if (e == cudaSuccess) {
+    using namespace hyb;
     const size_t tiles = (size_t)h->max_tiles;
     if (e == cudaSuccess) e = cudaMalloc(&h->hot, sizeof(int32_t) * (1 + kHotMax));
     if (e == cudaSuccess) e = cudaMemset(h->hot, 0, sizeof(int32_t) * (1 + kHotMax));
@@ -325,8 +393,9 @@ ss_status ss_validate_csr(ss_handle *h, const ss_csr *m, void *stream) {
 
 ss_status ss_invalidate(ss_handle *h) {
   if (!h) return SS_ERR_INVALID_ARG;
-  for (int j = 0; j < 3; ++j) h->hot_src[j] = h->prep_src[j] = nullptr;
+  for (int j = 0; j < 3; ++j) h->hot_src[j] = h->prep_src[j] = h->auto_src[j] = nullptr;
   h->hot_src_rows = h->hot_src_nnz = h->prep_rows = h->prep_nnz = -1;
+  h->auto_src_rows = h->auto_src_nnz = -1;
   h->prep_generation = ~0ull;
   return SS_OK;
 }
@@ -341,7 +410,14 @@ ss_status ss_index_stats(ss_handle *h, const ss_index *idx, int64_t *stats, void
   stats[0] = idx->algo;
   stats[1] = idx->n_items;
   SS_CUDA(h, cudaStreamSynchronize(as_stream(stream)));
-  if (idx->algo != ALGO_HYBRID || idx->n_tiles == 0) return SS_OK;
+  if (idx->algo == ALGO_POSTING) {
+    int32_t ends[2] = {0, 0};
+    SS_CUDA(h, cudaMemcpy(&ends[0], idx->col_ptr, sizeof(int32_t), cudaMemcpyDeviceToHost));
+    SS_CUDA(h, cudaMemcpy(&ends[1], idx->col_ptr + idx->dim, sizeof(int32_t), cudaMemcpyDeviceToHost));
+    stats[6] = ends[1] - ends[0];
+    return SS_OK;
+  }
+  if (idx->n_tiles == 0) return SS_OK;
   stats[2] = idx->n_tiles;
   int32_t hcount = 0;
   SS_CUDA(h, cudaMemcpy(&hcount, idx->hot, sizeof(int32_t), cudaMemcpyDeviceToHost));

@@ -42,10 +42,12 @@
 #include <algorithm>
 
 #include "internal.cuh"
+#include "topk.cuh"
 
 namespace {
 
 using namespace hyb;
+using namespace topk_dev;
 
 constexpr int kSelThreads = 1024;
 constexpr int kSelSlotsBits = 14;
@@ -570,98 +572,6 @@ __global__ void __launch_bounds__(kBThreads, 1)
     m[kMetaHeavyItems] = (!fits && heavy_ok) ? n_heavy_items : 0;
     m[kMetaFits] = fits ? 1 : 0;
   }
-}
-
-// ---------------------------------------------------------------- top-k
-// Order of the top-k epilogue: larger score first, equal scores by smaller
-// item number.
-__device__ __forceinline__ bool topk_before(float v, int64_t i, float w, int64_t j) {
-  return v > w || (v == w && i < j);
-}
-
-// How many of query row q's scores in one item tile (8 per lane) are >= thr
-// (the row's current k-th best score).
-__device__ __forceinline__ int topk_count(float thr, const float (&v)[8], const bool (&valid)[8]) {
-  int count = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) count += __popc(__ballot_sync(0xffffffffu, valid[j] && v[j] >= thr));
-  return count;
-}
-
-// Writes a tile's offer for query row q at slots [base, base + min(count,
-// k)) of the row's candidates: the scores >= thr, or when more than k pass,
-// the k best in the top-k order (k rounds of warp arg-best).  Items are
-// chunk-relative.
-__device__ __forceinline__ void topk_emit(const ss_topk &t, int64_t q, float thr, const float (&v)[8],
-                                          const int (&item)[8], const bool (&valid)[8], int base,
-                                          int count, int lane) {
-  bool pass[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) pass[j] = valid[j] && v[j] >= thr;
-  float *cv = t.cand_val + q * t.cand_cap + base;
-  int32_t *ci = t.cand_item + q * t.cand_cap + base;
-  if (count <= t.k) {
-    const unsigned lt = (1u << lane) - 1u;
-    int off = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const unsigned m = __ballot_sync(0xffffffffu, pass[j]);
-      if (pass[j]) {
-        const int pos = off + __popc(m & lt);
-        cv[pos] = v[j];
-        ci[pos] = item[j];
-      }
-      off += __popc(m);
-    }
-    return;
-  }
-  for (int r = 0; r < t.k; ++r) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff, bj = -1;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (pass[j] && topk_before(v[j], item[j], bv, bi)) {
-        bv = v[j];
-        bi = item[j];
-        bj = j;
-      }
-    float wv = bv;
-    int wi = bi;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
-      if (topk_before(ov, oi, wv, wi)) {
-        wv = ov;
-        wi = oi;
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j)  // items are distinct: one lane holds the winner
-      if (j == bj && bi == wi) pass[j] = false;
-    if (lane == 0) {
-      cv[r] = wv;
-      ci[r] = wi;
-    }
-  }
-}
-
-// Offers query row q's scores of one item tile to the row's candidates
-// (reserving the slots with one atomic).
-__device__ __forceinline__ void topk_offer(const ss_topk &t, int64_t q, float thr, const float (&v)[8],
-                                           const int (&item)[8], const bool (&valid)[8], int lane,
-                                           int32_t *status) {
-  const int count = topk_count(thr, v, valid);
-  if (count == 0) return;
-  const int n_emit = count < t.k ? count : t.k;
-  int base = 0;
-  if (lane == 0) base = atomicAdd(t.cand_n + q, n_emit);
-  base = __shfl_sync(0xffffffffu, base, 0);
-  if (base + n_emit > t.cand_cap) {  // cannot happen: a chunk's tiles offer at most k each
-    if (lane == 0) flag(status, DEV_CAPACITY);
-    return;
-  }
-  topk_emit(t, q, thr, v, item, valid, base, count, lane);
 }
 
 // ---------------------------------------------------------------- scorer
@@ -1713,7 +1623,54 @@ __global__ void __launch_bounds__(kFThreads, 1) k_score_tiles(const TileArgs a) 
   cp_async_wait_all();
 }
 
+// The automatic choice between item tiles and posting lists: per item tile of
+// a build, the cold entries (those outside the hot set) against the image's
+// entry capacity kImgECap, the builder's own rule for a tile without an
+// image.  probe[0] += tiles, probe[1] += tiles above the capacity.
+__global__ void __launch_bounds__(256)
+    k_auto_probe(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
+                 int64_t row_begin, int64_t row_end, const int32_t *__restrict__ hot,
+                 int32_t *__restrict__ probe) {
+  __shared__ int hkeys[kHotSlots];
+  __shared__ int8_t hvals[kHotSlots];
+  __shared__ int red[8];
+  const int tid = threadIdx.x;
+  const int64_t i0 = row_begin + (int64_t)blockIdx.x * kTI;
+  const int64_t i1 = min(i0 + kTI, row_end);
+  for (int j = tid; j < kHotSlots; j += 256) hkeys[j] = -1;
+  __syncthreads();
+  const int H = hot[0];
+  if (tid < H) hot_insert(hkeys, hvals, hot[1 + tid], tid);
+  __syncthreads();
+  const int64_t p0 = indptr[i0], p1 = indptr[i1];
+  int cold = 0;
+  for (int64_t p = p0 + tid; p < p1; p += 256) cold += hot_find(hkeys, hvals, __ldg(indices + p)) < 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cold += __shfl_xor_sync(0xffffffffu, cold, o);
+  if ((tid & 31) == 0) red[tid >> 5] = cold;
+  __syncthreads();
+  if (tid == 0) {
+    int e = 0;
+    for (int w = 0; w < 8; ++w) e += red[w];
+    atomicAdd(probe, 1);
+    if (e > kImgECap) atomicAdd(probe + 1, 1);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_auto_probe(ss_handle *h, const ss_csr &items, int64_t row_begin, int64_t row_end,
+                              int32_t *probe, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(probe, 0, 2 * sizeof(int32_t), s);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = (row_end - row_begin + kTI - 1) / kTI;
+  if (tiles <= 0) return cudaSuccess;
+  k_auto_probe<<<(unsigned)tiles, 256, 0, s>>>(items.indptr, items.indices, row_begin, row_end,
+                                               h->hot, probe);
+  return cudaGetLastError();
+}
+
+
 
 cudaError_t launch_hot_select(ss_handle *h, const ss_csr &items, cudaStream_t s, int *queued) {
   *queued = 0;

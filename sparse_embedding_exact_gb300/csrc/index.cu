@@ -6,13 +6,19 @@
 // the posting list of dimension k names every item of the chunk whose support
 // holds k, so a query nonzero at k meets exactly the items it multiplies.
 //
-// Steps (all on the device, queued on one stream):
-//   1. histogram: count[k] = number of chunk rows holding dimension k;
-//   2. exclusive scan of count[0..dim] -> col_ptr (tile sums, a scan of the
-//      tile sums, then the tiles again with warp-shuffle scans);
-//   3. scatter: every nonzero (row r, dim k, value v) takes the next slot of
-//      list k and stores (r - row_begin, v).
+// One build covers up to B chunks of C rows (B counter arrays of dim + 1 laid
+// end to end).  Steps (all on the device, queued on one stream):
+//   1. histogram: count[c][k] = number of rows of chunk c holding dimension k;
+//   2. exclusive scan of the B * (dim + 1) counters as one array -> col_ptr
+//      (tile sums, a scan of the tile sums, then the tiles again with
+//      warp-shuffle scans).  Chunk c's lists thus follow chunk c-1's, and
+//      col_ptr[c][k] is an absolute position in the build's entry arrays;
+//   3. scatter: every nonzero (row r of chunk c, dim k, value v) takes the
+//      next slot of list (c, k) and stores (item r - first row of c, v).
+// A list's entries are in no particular order; the scorer does not need one.
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "internal.cuh"
 
@@ -29,14 +35,23 @@ __device__ __forceinline__ void flag(int32_t *status, int32_t code) {
 
 __global__ void __launch_bounds__(kHistThreads)
     k_histogram(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
-                int64_t row_begin, int64_t row_end, int64_t dim, int32_t *__restrict__ count,
-                int32_t *status) {
-  const int64_t p0 = indptr[row_begin], p1 = indptr[row_end];
+                int64_t row_begin, int64_t row_end, int64_t chunk_rows, int n_chunks, int64_t dim,
+                int32_t *__restrict__ count, int32_t *status) {
+  // First entry of each chunk of the build, then the build's end.
+  __shared__ int64_t bound[kMaxBuildBatch + 1];
+  if (threadIdx.x <= n_chunks) {
+    const int64_t r = min(row_begin + (int64_t)threadIdx.x * chunk_rows, row_end);
+    bound[threadIdx.x] = indptr[r];
+  }
+  __syncthreads();
+  const int64_t p0 = bound[0], p1 = bound[n_chunks];
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t p = p0 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < p1; p += stride) {
     const int32_t k = __ldg(indices + p);
+    int c = 0;
+    while (c + 1 < n_chunks && p >= bound[c + 1]) ++c;
     if (k >= 0 && (int64_t)k < dim) {
-      atomicAdd(count + k, 1);
+      atomicAdd(count + (int64_t)c * (dim + 1) + k, 1);
     } else {
       flag(status, DEV_OUT_OF_RANGE);
     }
@@ -129,23 +144,27 @@ __global__ void __launch_bounds__(kScanThreads)
   }
 }
 
-// One warp per chunk row: each nonzero claims the next slot of its list.
+// One warp per row: each nonzero claims the next slot of its list.
 __global__ void __launch_bounds__(kHistThreads)
     k_scatter(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
-              const float *__restrict__ values, int64_t row_begin, int64_t row_end, int64_t dim,
-              int32_t *__restrict__ cursor, uint16_t *__restrict__ post_item,
-              float *__restrict__ post_val, int64_t capacity, int32_t *status) {
+              const float *__restrict__ values, int64_t row_begin, int64_t row_end,
+              int64_t chunk_rows, int64_t dim, int32_t *__restrict__ cursor,
+              uint16_t *__restrict__ post_item, float *__restrict__ post_val, int64_t capacity,
+              int32_t *status) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (kHistThreads / 32);
   for (int64_t r = row_begin + (int64_t)blockIdx.x * (kHistThreads / 32) + (threadIdx.x >> 5);
        r < row_end; r += warps) {
     const int64_t b = indptr[r], e = indptr[r + 1];
+    const int64_t c = (r - row_begin) / chunk_rows;
+    int32_t *cur = cursor + c * (dim + 1);
+    const uint16_t item = (uint16_t)(r - row_begin - c * chunk_rows);
     for (int64_t j = b + lane; j < e; j += 32) {
       const int32_t k = __ldg(indices + j);
       if (k < 0 || (int64_t)k >= dim) continue;  // flagged by the histogram
-      const int32_t pos = atomicAdd(cursor + k, 1);
+      const int32_t pos = atomicAdd(cur + k, 1);
       if (pos >= 0 && (int64_t)pos < capacity) {
-        post_item[pos] = (uint16_t)(r - row_begin);
+        post_item[pos] = item;
         post_val[pos] = __ldg(values + j);
       } else {
         flag(status, DEV_CAPACITY);
@@ -160,31 +179,39 @@ int64_t scan_tile_count(int64_t n) { return (n + kScanTile - 1) / kScanTile; }
 
 cudaError_t launch_build_index(ss_handle *h, const ss_csr &items, int64_t row_begin,
                                int64_t row_end, cudaStream_t s) {
-  const int64_t n = h->dim + 1;
+  const int64_t C = h->chunk_rows;
+  const int n_chunks = (int)((row_end - row_begin + C - 1) / C);
+  h->n_views = 0;
+  if (n_chunks < 1 || n_chunks > h->build_batch) return cudaErrorInvalidValue;
+  const int64_t stride = h->dim + 1;
+  const int64_t n = stride * n_chunks;
   cudaError_t e = cudaMemsetAsync(h->col_cnt, 0, sizeof(int32_t) * (size_t)n, s);
   if (e != cudaSuccess) return e;
   const int grid = h->sm_count * 8;
-  k_histogram<<<grid, kHistThreads, 0, s>>>(items.indptr, items.indices, row_begin, row_end,
-                                            h->dim, h->col_cnt, h->d_status);
+  k_histogram<<<grid, kHistThreads, 0, s>>>(items.indptr, items.indices, row_begin, row_end, C,
+                                            n_chunks, h->dim, h->col_cnt, h->d_status);
   const int64_t tiles = scan_tile_count(n);
   k_scan_tile_sums<<<(unsigned)tiles, kScanThreads, 0, s>>>(h->col_cnt, n, h->scan_part);
   k_scan_partials<<<1, kScanThreads, 0, s>>>(h->scan_part, tiles);
   k_scan_apply<<<(unsigned)tiles, kScanThreads, 0, s>>>(h->col_cnt, n, h->scan_part, h->col_ptr);
   k_scatter<<<grid, kHistThreads, 0, s>>>(items.indptr, items.indices, items.values, row_begin,
-                                          row_end, h->dim, h->col_cnt, h->post_item, h->post_val,
-                                          h->post_cap, h->d_status);
+                                          row_end, C, h->dim, h->col_cnt, h->post_item,
+                                          h->post_val, h->post_cap, h->d_status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  ss_index &ix = h->views[0];
-  h->n_views = 1;
-  ix.algo = ALGO_POSTING;
-  ix.row_begin = row_begin;
-  ix.row_end = row_end;
-  ix.n_items = (int32_t)(row_end - row_begin);
-  ix.dim = h->dim;
-  ix.col_ptr = h->col_ptr;
-  ix.post_item = h->post_item;
-  ix.post_val = h->post_val;
-  ix.capacity = h->post_cap;
+  for (int k = 0; k < n_chunks; ++k) {
+    ss_index &ix = h->views[k];
+    ix = ss_index();
+    ix.algo = ALGO_POSTING;
+    ix.row_begin = row_begin + (int64_t)k * C;
+    ix.row_end = std::min<int64_t>(ix.row_begin + C, row_end);
+    ix.n_items = (int32_t)(ix.row_end - ix.row_begin);
+    ix.dim = h->dim;
+    ix.col_ptr = h->col_ptr + (size_t)k * stride;
+    ix.post_item = h->post_item;
+    ix.post_val = h->post_val;
+    ix.capacity = h->post_cap;
+  }
+  h->n_views = n_chunks;
   return cudaSuccess;
 }

@@ -16,13 +16,24 @@ enum : int32_t {
   DEV_OUT_OF_RANGE = 2,
   DEV_CAPACITY = 3,
   DEV_STALL = 4,  // a bounded loop ran out of iterations
+  DEV_RANGE = 5,  // a normalised product above 1: inverse norms that are not the rows' own
 };
 
 // Scoring algorithms.
 enum : int32_t {
   ALGO_HYBRID = 0,   // dense hot dimensions in registers + sparse cold lists in shared memory
-  ALGO_POSTING = 1,  // one warp per query row walking the chunk's posting lists
+  ALGO_POSTING = 1,  // one block per query row walking the chunk's posting lists
 };
+
+// How a handle picks the algorithm of its chunk indexes.
+enum : int32_t {
+  MODE_AUTO = 0,     // per item matrix, from the tile overflow of its first build
+  MODE_TILES = 1,    // always ALGO_HYBRID
+  MODE_POSTING = 2,  // always ALGO_POSTING
+};
+// The automatic choice takes posting lists when more than this share of the
+// first build's item tiles have more cold entries than an image holds.
+constexpr double kAutoOverflowShare = 0.5;
 
 // Geometry of the hybrid scorer (see hybrid.cu).
 namespace hyb {
@@ -72,8 +83,9 @@ struct ss_index {
   int32_t n_items = 0;
   int64_t dim = 0;
   // ALGO_POSTING
-  const int32_t *col_ptr = nullptr;    // [dim + 1], posting list k = [col_ptr[k], col_ptr[k+1])
-  const uint16_t *post_item = nullptr; // [capacity]
+  const int32_t *col_ptr = nullptr;    // [dim + 1], posting list k = [col_ptr[k], col_ptr[k+1]),
+                                       // positions into the build's entry arrays
+  const uint16_t *post_item = nullptr; // [capacity]: item within the chunk
   const float *post_val = nullptr;     // [capacity]
   int64_t capacity = 0;
   // ALGO_HYBRID
@@ -139,21 +151,29 @@ struct ss_handle {
   int64_t dim = 0;
   int32_t chunk_rows = 0;
   int32_t flags = 0;
-  int32_t algo = ALGO_HYBRID;
+  int32_t algo = ALGO_HYBRID;   // algorithm of the current item matrix's indexes
+  int32_t mode = MODE_AUTO;
   int sm_count = 0;
   std::string last_error;
   uint64_t launches = 0;  // kernels queued by this handle
 
   // Device workspace, owned by the handle.
   int32_t *d_status = nullptr;  // one status word
-  // ALGO_POSTING
-  int32_t *col_cnt = nullptr;    // [dim + 1]: histogram, then scatter cursors
-  int32_t *col_ptr = nullptr;    // [dim + 1]
+  // ALGO_POSTING (allocated when first needed)
+  int32_t *col_cnt = nullptr;    // [build_batch][dim + 1]: histogram, then scatter cursors
+  int32_t *col_ptr = nullptr;    // [build_batch][dim + 1]
   int32_t *scan_part = nullptr;  // [scan tiles + 1]
   int64_t scan_tiles = 0;
   uint16_t *post_item = nullptr; // [post_cap]
   float *post_val = nullptr;     // [post_cap]
+  int2 *post_hat = nullptr;      // [post_cap]: {item, value * inv_i}, rewritten per scoring call
   int64_t post_cap = 0;
+  int32_t *row_next = nullptr;   // [2]: the posting scorer's row counter and finished blocks
+  int32_t *probe = nullptr;      // [2]: tiles probed, tiles above the image capacity
+  // The automatic choice, made once per item matrix (same identity as hot_src).
+  const void *auto_src[3] = {nullptr, nullptr, nullptr};
+  int64_t auto_src_rows = -1, auto_src_nnz = -1;
+  int32_t auto_algo = ALGO_HYBRID;
   // ALGO_HYBRID
   int32_t *hot = nullptr;        // [1 + kHotMax]
   float *slab = nullptr;         // [max tiles][kHotMax][kTI]
@@ -202,17 +222,25 @@ struct ss_handle {
 // Launchers (all asynchronous on `s`).
 cudaError_t launch_row_norms(const ss_csr &m, float *inv_norms, int sm_count, cudaStream_t s);
 cudaError_t launch_validate_csr(const ss_csr &m, int32_t *d_status, int sm_count, cudaStream_t s);
+// Builds the posting lists of the chunks of h->chunk_rows items that split
+// [row_begin, row_end) (at most h->build_batch of them), into h->views[0..n).
 cudaError_t launch_build_index(ss_handle *h, const ss_csr &items, int64_t row_begin,
                                int64_t row_end, cudaStream_t s);
-cudaError_t launch_score_chunk(const ss_handle *h, const ss_csr &queries, const float *inv_q,
-                               const ss_index &idx, const float *inv_i, float *out,
-                               int64_t ld_out, cudaStream_t s);
+// Posting-list scorer: normalises the chunk's entries into h->post_hat, then
+// scores (or offers top-k candidates); *queued gets the kernels queued.
+cudaError_t launch_score_lists(ss_handle *h, const ss_csr &queries, const float *inv_q,
+                               const ss_index &idx, const float *inv_i, float *out, int64_t ld_out,
+                               cudaStream_t s, int *queued, const ss_topk *topk = nullptr);
 // Hybrid path.  launch_hot_select returns the number of kernels it queued.
 cudaError_t launch_hot_select(ss_handle *h, const ss_csr &items, cudaStream_t s, int *queued);
 // Builds the chunks of h->chunk_rows items that split [row_begin, row_end)
 // (at most h->build_batch of them) in one launch, into h->views[0..n).
 cudaError_t launch_build_hybrid(ss_handle *h, const ss_csr &items, int64_t row_begin,
                                 int64_t row_end, cudaStream_t s);
+// Counts the item tiles of [row_begin, row_end) and those whose cold entries
+// exceed an image's capacity (for the hot set in h->hot) into probe[0..1].
+cudaError_t launch_auto_probe(ss_handle *h, const ss_csr &items, int64_t row_begin, int64_t row_end,
+                              int32_t *probe, cudaStream_t s);
 // Queues the query preparation (when needed), the fast tile scorer and the
 // fallback scorer; *queued gets the number of kernels queued.
 cudaError_t launch_score_hybrid(ss_handle *h, const ss_csr &queries, const float *inv_q,

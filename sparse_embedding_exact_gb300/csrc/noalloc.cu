@@ -80,6 +80,8 @@ extern "C" ss_status ss_cosine_chunk_noalloc(const ss_csr *queries, const ss_csr
   const size_t o_part = off;   off = align256(off + sizeof(int32_t) * (size_t)(tiles + 1));
   const size_t o_item = off;   off = align256(off + sizeof(uint16_t) * (size_t)chunk_nnz);
   const size_t o_val = off;    off = align256(off + sizeof(float) * (size_t)chunk_nnz);
+  const size_t o_hat = off;    off = align256(off + sizeof(int2) * (size_t)chunk_nnz);
+  const size_t o_rows = off;   off = align256(off + 2 * sizeof(int32_t));
   if (off > (size_t)SS_NOALLOC_SCRATCH_BYTES) return SS_ERR_LIMIT;
 
   int device = 0;
@@ -98,6 +100,8 @@ extern "C" ss_status ss_cosine_chunk_noalloc(const ss_csr *queries, const ss_csr
   view.dim = dim;
   view.chunk_rows = (int32_t)width;
   view.algo = ALGO_POSTING;
+  view.mode = MODE_POSTING;
+  view.build_batch = 1;
   view.sm_count = sm_count;
   view.d_status = reinterpret_cast<int32_t *>(b + o_status);
   view.col_cnt = reinterpret_cast<int32_t *>(b + o_cnt);
@@ -106,20 +110,26 @@ extern "C" ss_status ss_cosine_chunk_noalloc(const ss_csr *queries, const ss_csr
   view.scan_tiles = tiles;
   view.post_item = reinterpret_cast<uint16_t *>(b + o_item);
   view.post_val = reinterpret_cast<float *>(b + o_val);
+  view.post_hat = reinterpret_cast<int2 *>(b + o_hat);
   view.post_cap = chunk_nnz;
+  view.row_next = reinterpret_cast<int32_t *>(b + o_rows);
   float *inv_q = reinterpret_cast<float *>(b + o_inv_q);
   float *inv_i = reinterpret_cast<float *>(b + o_inv_i);
 
-  // The scratch keeps the previous call's contents: the status word starts
-  // at zero here, and the index builder clears its own counters.
+  // The scratch keeps the previous call's contents: the status word and the
+  // scorer's row counter start at zero here, and the index builder clears
+  // its own counters.
   if (cudaMemsetAsync(view.d_status, 0, sizeof(int32_t), s) != cudaSuccess) return SS_ERR_CUDA;
+  if (cudaMemsetAsync(view.row_next, 0, 2 * sizeof(int32_t), s) != cudaSuccess) return SS_ERR_CUDA;
   if (launch_row_norms(*queries, inv_q, sm_count, s) != cudaSuccess) return SS_ERR_CUDA;
   ss_csr chunk_rows = *items;
   chunk_rows.indptr = items->indptr + row_begin;
   chunk_rows.n_rows = width;
   if (launch_row_norms(chunk_rows, inv_i, sm_count, s) != cudaSuccess) return SS_ERR_CUDA;
   if (launch_build_index(&view, *items, row_begin, row_end, s) != cudaSuccess) return SS_ERR_CUDA;
-  if (launch_score_chunk(&view, *queries, inv_q, view.views[0], inv_i, out, ld_out, s) != cudaSuccess)
+  int queued = 0;
+  if (launch_score_lists(&view, *queries, inv_q, view.views[0], inv_i, out, ld_out, s, &queued) !=
+      cudaSuccess)
     return SS_ERR_CUDA;
   return SS_OK;
 }

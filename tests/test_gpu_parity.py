@@ -196,7 +196,7 @@ def test_chunk_size_invariance_with_heavy_rows_is_bitwise(sec):
     for c in (2048, 777):
         b = _gpu_cosine(sec, Q, I, chunk_rows=c)
         assert np.array_equal(a.view(np.int32), b.view(np.int32)), c
-    with sec.SparseCosine(cfg.dim, chunk_rows=2048) as h:
+    with sec.SparseCosine(cfg.dim, chunk_rows=2048, algorithm="hybrid") as h:
         i = _dev(sec, I)
         heavy = sum(h.index_stats(idx)["heavy_entries"] for _, _, idx in h.build_item_indexes(i, 0, 2048 * min(h.build_batch, 3)))
     assert heavy > 0  # the heavy path really ran
@@ -222,15 +222,16 @@ def test_score_chunk_calls_match_score_all(sec):
     assert (got[:, I.n_rows:] == -7.0).all()
 
 
+@pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("name,n_q,n_i,chunk", [
-    ("d500k_q50k_i500k_uniform", 40, 12000, 4096),  # every tile takes the ELL / fallback path
+    ("d500k_q50k_i500k_uniform", 40, 12000, 4096),  # hybrid: every tile takes the ELL / fallback path
     ("d1.2m_q20k_i1m_heavy", 60, 9000, 2048),       # heavy rows: the batch-wide heavy list
     ("d65k_q1k_i10k", 50, 4000, 333),               # chunks that end inside a 256-item tile
 ])
-def test_batched_builds_match_single_builds(sec, name, n_q, n_i, chunk):
+def test_batched_builds_match_single_builds(sec, name, n_q, n_i, chunk, algo):
     cfg = CONFIGS[name]
     Q, I = generate_rows(cfg, 0, 0, n_q), generate_rows(cfg, 1, 0, n_i)
-    with sec.SparseCosine(cfg.dim, chunk_rows=chunk) as h:
+    with sec.SparseCosine(cfg.dim, chunk_rows=chunk, algorithm=algo) as h:
         q, i = _dev(sec, Q), _dev(sec, I)
         inv_q, inv_i = h.row_norms(q), h.row_norms(i)
         single = torch.empty((n_q, n_i), device="cuda")
@@ -252,7 +253,7 @@ def test_batched_builds_match_single_builds(sec, name, n_q, n_i, chunk):
         a, c = single.cpu().numpy(), batched.cpu().numpy()
     assert seen == [(b, min(b + chunk, n_i)) for b in range(0, n_i, chunk)]
     assert np.array_equal(a.view(np.int32), c.view(np.int32))
-    if name.endswith("uniform"):
+    if name.endswith("uniform") and algo == "hybrid":
         assert tiles_without_image == sum((min(chunk, n_i - b) + 255) // 256 for b in range(0, n_i, chunk))
     assert _max_err(c, oracle.cosine(Q, I)) <= TOL
 
@@ -272,7 +273,11 @@ def test_build_item_indexes_limits(sec):
         views = h.build_item_indexes(i, 5, 5 + 256 * n)
         assert [(b, e) for b, e, _ in views] == [(5 + 256 * k, 5 + 256 * (k + 1)) for k in range(n)]
     with sec.SparseCosine(cfg.dim, chunk_rows=256, algorithm="posting") as h:
-        assert h.build_batch == 1
+        assert h.build_batch == n  # the same batch for both algorithms
+        i = _dev(sec, I)
+        views = h.build_item_indexes(i, 5, 5 + 256 * n)
+        assert [(b, e) for b, e, _ in views] == [(5 + 256 * k, 5 + 256 * (k + 1)) for k in range(n)]
+        assert all(h.index_stats(idx)["algorithm"] == 1 for _, _, idx in views)
 
 
 def test_self_similarity_invariants(sec):
@@ -347,7 +352,7 @@ def test_heavy_items_and_multibatch_queries(sec):
         i_rows[j] = row(4000)  # items far above their tile's mean
     Q, I = _rows_csr(q_rows, d), _rows_csr(i_rows, d)
     ref = oracle.cosine(Q, I)
-    for algo in ALGOS:
+    for algo in ALGOS + ["auto"]:
         got = _gpu_cosine(sec, Q, I, chunk_rows=512, algorithm=algo)
         assert _max_err(got, ref) <= TOL, algo
 
@@ -386,7 +391,7 @@ def test_index_stats_hot_set(sec):
     assert st["tiles_without_image"] == 0  # every tile takes the inverted-index path
     cfg3 = CONFIGS["d500k_q50k_i500k_uniform"]
     U = generate_rows(cfg3, 1, 0, 3000)
-    with sec.SparseCosine(cfg3.dim) as h:
+    with sec.SparseCosine(cfg3.dim, algorithm="hybrid") as h:
         st = h.index_stats(h.build_item_index(_dev(sec, U), 0, 3000))
     assert st["hot_dims"] == 0 and st["ell_width_max"] >= 400
     assert st["tiles_without_image"] == st["tiles"]  # 500 nonzeros a row: no tile fits an image
@@ -399,6 +404,76 @@ def test_two_gpu_algorithms_agree(sec, name):
     a = _gpu_cosine(sec, Q, I, algorithm="hybrid")
     b = _gpu_cosine(sec, Q, I, algorithm="posting")
     assert _max_err(a, b) <= TOL
+    assert _max_err(a, oracle.cosine(Q, I)) <= TOL
+
+
+# ------------------------------------------------------------- posting lists
+def test_auto_choice_follows_tile_overflow(sec):
+    """Without an algorithm flag the handle builds an item matrix's first
+    batch as tiles and switches to posting lists when most tiles overflow:
+    the uniform workload (500 nonzeros a row) switches, the Zipf one stays.
+    Either way the result is that of the chosen algorithm, bit for bit."""
+    for name, want in (("d500k_q50k_i500k_uniform", 1), ("d1.2m_q5k_i200k", 0)):
+        cfg = CONFIGS[name]
+        Q, I = generate_rows(cfg, 0, 0, 50), generate_rows(cfg, 1, 0, 9000)
+        with sec.SparseCosine(cfg.dim) as h:
+            i = _dev(sec, I)
+            algos = {h.index_stats(idx)["algorithm"] for _, _, idx in h.build_item_indexes(i, 0, 9000)}
+        assert algos == {want}, name
+        auto = _gpu_cosine(sec, Q, I, algorithm="auto")
+        forced = _gpu_cosine(sec, Q, I, algorithm="posting" if want else "hybrid")
+        assert np.array_equal(auto.view(np.int32), forced.view(np.int32)), name
+        assert _max_err(auto, oracle.cosine(Q, I)) <= TOL
+
+
+def test_posting_fold_over_many_shared_dims(sec):
+    """Rows sharing more than 16,384 dimensions: the fixed-point low parts are
+    folded into the high parts between segments, and the sums stay exact."""
+    rng = np.random.default_rng(21)
+    d = 60_000
+    base = np.sort(rng.choice(d, size=40_000, replace=False))
+    rows = []
+    for n in (40_000, 39_000, 25_000, 17_000, 3):
+        idx = np.sort(rng.choice(base, size=n, replace=False))
+        rows.append((idx, rng.standard_normal(n).astype(np.float32)))
+    rows.append((base, np.abs(rng.standard_normal(base.size)).astype(np.float32)))
+    X = _rows_csr(rows, d)
+    got = _gpu_cosine(sec, X, X, chunk_rows=4, algorithm="posting")
+    ref = oracle.cosine(X, X)
+    assert _max_err(got, ref) <= TOL
+    assert np.abs(np.diag(got) - 1.0).max() <= TOL
+
+
+def test_posting_rejects_inverse_norms_of_other_rows(sec):
+    """Exact fixed-point sums need normalised products (|p| <= 1); inverse
+    norms that are not the rows' own are reported, and the handle stays
+    usable."""
+    from sparse_embedding_exact_gb300 import SparseCosError, _abi
+
+    X = _rows_csr([([1, 4], [30.0, 40.0]), ([4, 9], [2.0, 1.0])], 16)
+    with sec.SparseCosine(16, algorithm="posting") as h:
+        x = _dev(sec, X)
+        ones = torch.ones(2, dtype=torch.float32, device="cuda")
+        h.score_all(x, ones, x, ones)
+        with pytest.raises(SparseCosError) as e:
+            h.check_device()
+        assert e.value.status == _abi.SS_ERR_DEVICE_CHECK
+        inv = h.row_norms(x)
+        S = h.score_all(x, inv, x, inv).cpu().numpy()
+        h.check_device()
+    assert _max_err(S, oracle.cosine(X, X)) <= TOL
+
+
+@pytest.mark.parametrize("name", ["d1.2m_q20k_i1m_heavy", "d500k_q50k_i500k_uniform"])
+def test_posting_chunk_size_invariance_is_bitwise(sec, name):
+    """Fixed-point sums do not depend on their order: any chunking, any
+    batch of builds, the same bits."""
+    cfg = CONFIGS[name]
+    Q, I = generate_rows(cfg, 0, 0, 60), generate_rows(cfg, 1, 0, 6000)
+    a = _gpu_cosine(sec, Q, I, chunk_rows=8192, algorithm="posting")
+    for c in (2048, 777, 100):
+        b = _gpu_cosine(sec, Q, I, chunk_rows=c, algorithm="posting")
+        assert np.array_equal(a.view(np.int32), b.view(np.int32)), c
     assert _max_err(a, oracle.cosine(Q, I)) <= TOL
 
 

@@ -42,8 +42,8 @@ def _top_order(S, k):
     return np.stack([np.lexsort((items, -S[q]))[:k] for q in range(S.shape[0])])
 
 
-def _topk_and_full(sec, Q, I, k, chunk):
-    with sec.SparseCosine(Q.dim, chunk_rows=chunk) as h:
+def _topk_and_full(sec, Q, I, k, chunk, algo="auto"):
+    with sec.SparseCosine(Q.dim, chunk_rows=chunk, algorithm=algo) as h:
         q, i = _dev(sec, Q), _dev(sec, I)
         inv_q, inv_i = h.row_norms(q), h.row_norms(i)
         vals, items = h.topk_all(q, inv_q, i, inv_i, k)
@@ -58,16 +58,17 @@ CASES = [
     ("d65k_q1k_i10k", 30, 9000, 64, 8192),
     ("d65k_q1k_i10k", 25, 3000, 1, 333),
     ("d1.2m_q5k_i200k", 50, 12000, 20, 8192),
-    ("d1.2m_q20k_i1m_heavy", 40, 6000, 16, 2048),  # heavy rows on the fallback path
-    ("d500k_q50k_i500k_uniform", 20, 5000, 8, 4096),  # every tile on the fallback path
+    ("d1.2m_q20k_i1m_heavy", 40, 6000, 16, 2048),  # hybrid: heavy rows on the fallback path
+    ("d500k_q50k_i500k_uniform", 20, 5000, 8, 4096),  # hybrid: every tile on the fallback path
 ]
 
 
+@pytest.mark.parametrize("algo", ["hybrid", "posting"])
 @pytest.mark.parametrize("name,n_q,n_i,k,chunk", CASES)
-def test_topk_is_the_top_of_the_full_matrix(sec, name, n_q, n_i, k, chunk):
+def test_topk_is_the_top_of_the_full_matrix(sec, name, n_q, n_i, k, chunk, algo):
     cfg = CONFIGS[name]
     Q, I = generate_rows(cfg, 0, 0, n_q), generate_rows(cfg, 1, 0, n_i)
-    vals, items, full = _topk_and_full(sec, Q, I, k, chunk)
+    vals, items, full = _topk_and_full(sec, Q, I, k, chunk, algo)
     expect = _top_order(full, k)
     assert np.array_equal(items, expect)
     assert np.array_equal(vals.view(np.int32), np.take_along_axis(full, expect, 1).view(np.int32))
@@ -78,12 +79,13 @@ def test_topk_is_the_top_of_the_full_matrix(sec, name, n_q, n_i, k, chunk):
     assert (picked >= kth[:, None] - 2 * TOL).all()
 
 
-def test_topk_short_rows_ties_and_padding(sec):
+@pytest.mark.parametrize("algo", ["hybrid", "posting"])
+def test_topk_short_rows_ties_and_padding(sec, algo):
     # 3 query rows (one all zero: every score 0, ties broken by item number),
     # 5 items, k = 8 > 5: the last 3 slots stay (-inf, -1).
     Q = csr_from_rows([([1, 3], [1.0, 2.0]), ([], []), ([0, 3, 5], [0.5, -1.0, 2.0])], 8)
     I = csr_from_rows([([3], [1.0]), ([1, 3], [2.0, 4.0]), ([0], [-1.0]), ([5, 7], [1.0, 1.0]), ([], [])], 8)
-    with sec.SparseCosine(8, chunk_rows=2) as h:
+    with sec.SparseCosine(8, chunk_rows=2, algorithm=algo) as h:
         q, i = _dev(sec, Q), _dev(sec, I)
         inv_q, inv_i = h.row_norms(q), h.row_norms(i)
         vals, items = (t.cpu().numpy() for t in h.topk_all(q, inv_q, i, inv_i, 8))
@@ -93,10 +95,11 @@ def test_topk_short_rows_ties_and_padding(sec):
     assert np.array_equal(items[1, :5], np.arange(5)) and (vals[1, :5] == 0).all()
 
 
-def test_topk_chunks_in_any_order_match_topk_all(sec):
+@pytest.mark.parametrize("algo", ["hybrid", "posting"])
+def test_topk_chunks_in_any_order_match_topk_all(sec, algo):
     cfg = CONFIGS["d65k_q1k_i10k"]
     Q, I = generate_rows(cfg, 0, 0, 40), generate_rows(cfg, 1, 0, 5000)
-    with sec.SparseCosine(cfg.dim, chunk_rows=1024) as h:
+    with sec.SparseCosine(cfg.dim, chunk_rows=1024, algorithm=algo) as h:
         q, i = _dev(sec, Q), _dev(sec, I)
         inv_q, inv_i = h.row_norms(q), h.row_norms(i)
         want_v, want_i = h.topk_all(q, inv_q, i, inv_i, 12)
@@ -127,4 +130,5 @@ def test_topk_limits(sec):
     with sec.SparseCosine(cfg.dim, chunk_rows=256, algorithm="posting") as h:
         q, i = _dev(sec, Q), _dev(sec, I)
         with pytest.raises(SparseCosError):
-            h.topk_all(q, h.row_norms(q), i, h.row_norms(i), 4)
+            h.topk_all(q, h.row_norms(q), i, h.row_norms(i), 65)
+        h.topk_all(q, h.row_norms(q), i, h.row_norms(i), 4)  # both algorithms have the epilogue
