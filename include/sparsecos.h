@@ -305,7 +305,8 @@ ss_status ss_invalidate(ss_handle *h);
  * Diagnostics for an index built by ss_build_item_index.  Synchronises
  * `stream` and writes stats[0..7]:
  *   [0] algorithm (0 = hybrid, 1 = posting lists)  [1] items in the chunk
- *   [2] item tiles (hybrid)                         [3] hot dimensions H
+ *   [2] item tiles (hybrid)                         [3] hot dimensions H (posting
+ *                                                       lists: those split off)
  *   [4] entries in the heavy-item list              [5] widest ELL column
  *   [6] ELL entries stored, padding included        [7] item tiles without an
  *       (posting lists: entries in the chunk)           inverted-index image

@@ -106,6 +106,8 @@ ss_status ensure_posting_workspace(ss_handle *h) {
   SS_CUDA(h, cudaDeviceSynchronize());
   SS_CUDA(h, cudaMalloc(&h->col_cnt, sizeof(int32_t) * n));
   SS_CUDA(h, cudaMalloc(&h->scan_part, sizeof(int32_t) * (size_t)(h->scan_tiles + 1)));
+  SS_CUDA(h, cudaMalloc(&h->slab_post, sizeof(float) * (size_t)h->build_batch * hyb::kHotMax *
+                                           (size_t)h->chunk_rows));
   SS_CUDA(h, cudaMalloc(&h->col_ptr, sizeof(int32_t) * n));
   return SS_OK;
 }
@@ -158,13 +160,18 @@ void free_workspace(ss_handle *h) {
   h->cand_n = nullptr;
   h->cand_elems = h->cand_rows = 0;
   void *ptrs[] = {h->d_status, h->col_cnt, h->col_ptr, h->scan_part, h->post_item, h->post_val,
-                  h->post_hat, h->row_next, h->probe, h->hot, h->slab, h->ell, h->meta, h->heavy_k,
+                  h->post_hat, h->row_next, h->probe, h->slab_post, h->qhot_dense,
+                  h->hot_scratch, h->hot, h->slab, h->ell, h->meta, h->heavy_k,
                   h->heavy_v, h->heavy_item, h->counters, h->image, h->qhot, h->qcold,
                   h->qcold_n, h->heavy_tbl};
   for (void *p : ptrs) cudaFree(p);
   h->post_hat = nullptr;
   h->row_next = nullptr;
   h->probe = nullptr;
+  h->slab_post = nullptr;
+  h->qhot_dense = nullptr;
+  h->hot_scratch = nullptr;
+  h->qhot_dense_cap = h->hot_scratch_cap = 0;
   h->counters = nullptr;
   h->heavy_tbl = nullptr;
   h->image = nullptr;
@@ -190,14 +197,14 @@ ss_status build_algo(ss_handle *h, int32_t algo, const ss_csr &items, int64_t rb
   ss_status st = ensure_capacity(h, algo, std::max<int64_t>(items.nnz, 1));
   if (st != SS_OK) return st;
   h->algo = algo;
+  int queued = 0;
+  SS_CUDA(h, launch_hot_select(h, items, s, &queued));
   if (algo == ALGO_POSTING) {
     if ((st = ensure_posting_workspace(h)) != SS_OK) return st;
     SS_CUDA(h, launch_build_index(h, items, rb, re, s));
-    h->launches += kIndexKernels;
+    h->launches += queued + kIndexKernels;
     return SS_OK;
   }
-  int queued = 0;
-  SS_CUDA(h, launch_hot_select(h, items, s, &queued));
   SS_CUDA(h, launch_build_hybrid(h, items, rb, re, s));
   h->launches += queued + 1;
   return SS_OK;
@@ -335,6 +342,8 @@ ss_status ss_create(ss_handle **out, int device, int64_t dim, int32_t chunk_rows
   if (e == cudaSuccess) e = cudaMalloc(&h->row_next, 2 * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(h->row_next, 0, 2 * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMalloc(&h->probe, 2 * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMalloc(&h->hot, sizeof(int32_t) * (1 + hyb::kHotMax));
+  if (e == cudaSuccess) e = cudaMemset(h->hot, 0, sizeof(int32_t) * (1 + hyb::kHotMax));
   {
     using namespace hyb;
     // One build covers enough chunks to give every SM a tile (a chunk alone
@@ -344,17 +353,11 @@ ss_status ss_create(ss_handle **out, int device, int64_t dim, int32_t chunk_rows
     h->build_batch = std::max(1, std::min(kMaxBuildBatch, (sms + h->chunk_tiles - 1) / h->chunk_tiles));
     h->max_tiles = h->build_batch * h->chunk_tiles;
   }
-  if (e == cudaSuccess && h->mode == MODE_POSTING) {
-    const size_t n = (size_t)h->build_batch * (size_t)(dim + 1);
-    h->scan_tiles = scan_tile_count((int64_t)n);
-    e = cudaMalloc(&h->col_cnt, sizeof(int32_t) * n);
-    if (e == cudaSuccess) e = cudaMalloc(&h->col_ptr, sizeof(int32_t) * n);
-    if (e == cudaSuccess) e = cudaMalloc(&h->scan_part, sizeof(int32_t) * (size_t)(h->scan_tiles + 1));
-  } else if (e == cudaSuccess) {
+  // The posting-list workspace is allocated by the first posting build; the
+  // tile workspace unless the handle only ever builds posting lists.
+  if (e == cudaSuccess && h->mode != MODE_POSTING) {
     using namespace hyb;
     const size_t tiles = (size_t)h->max_tiles;
-    if (e == cudaSuccess) e = cudaMalloc(&h->hot, sizeof(int32_t) * (1 + kHotMax));
-    if (e == cudaSuccess) e = cudaMemset(h->hot, 0, sizeof(int32_t) * (1 + kHotMax));
     if (e == cudaSuccess) e = cudaMalloc(&h->slab, sizeof(float) * tiles * kHotMax * kTI);
     if (e == cudaSuccess) e = cudaMalloc(&h->ell, sizeof(int2) * tiles * kEllMaxW * kTI);
     if (e == cudaSuccess) e = cudaMalloc(&h->meta, sizeof(int32_t) * tiles * kMetaInts);
@@ -393,9 +396,10 @@ ss_status ss_validate_csr(ss_handle *h, const ss_csr *m, void *stream) {
 
 ss_status ss_invalidate(ss_handle *h) {
   if (!h) return SS_ERR_INVALID_ARG;
-  for (int j = 0; j < 3; ++j) h->hot_src[j] = h->prep_src[j] = h->auto_src[j] = nullptr;
+  for (int j = 0; j < 3; ++j) h->hot_src[j] = h->prep_src[j] = h->auto_src[j] = h->qd_src[j] = nullptr;
   h->hot_src_rows = h->hot_src_nnz = h->prep_rows = h->prep_nnz = -1;
-  h->auto_src_rows = h->auto_src_nnz = -1;
+  h->auto_src_rows = h->auto_src_nnz = h->qd_rows = h->qd_nnz = -1;
+  h->qd_generation = ~0ull;
   h->prep_generation = ~0ull;
   return SS_OK;
 }
@@ -415,6 +419,11 @@ ss_status ss_index_stats(ss_handle *h, const ss_index *idx, int64_t *stats, void
     SS_CUDA(h, cudaMemcpy(&ends[0], idx->col_ptr, sizeof(int32_t), cudaMemcpyDeviceToHost));
     SS_CUDA(h, cudaMemcpy(&ends[1], idx->col_ptr + idx->dim, sizeof(int32_t), cudaMemcpyDeviceToHost));
     stats[6] = ends[1] - ends[0];
+    if (idx->hot) {  // hot dimensions split off into the dense slab (0 when too few)
+      int32_t hcount = 0;
+      SS_CUDA(h, cudaMemcpy(&hcount, idx->hot, sizeof(int32_t), cudaMemcpyDeviceToHost));
+      stats[3] = hcount >= kSplitMinHot ? hcount : 0;
+    }
     return SS_OK;
   }
   if (idx->n_tiles == 0) return SS_OK;

@@ -42,52 +42,21 @@
 #include <algorithm>
 
 #include "internal.cuh"
+#include "hotset.cuh"
 #include "topk.cuh"
 
 namespace {
 
 using namespace hyb;
 using namespace topk_dev;
+using namespace hotset;
 
 constexpr int kSelThreads = 1024;
 constexpr int kSelSlotsBits = 14;
 constexpr int kSelSlots = 1 << kSelSlotsBits;
 constexpr int kSelCand = 1024;
-constexpr int kHotSlots = 128;
-
 __device__ __forceinline__ void flag(int32_t *status, int32_t code) {
   atomicCAS(status, DEV_OK, code);
-}
-
-__device__ __forceinline__ uint32_t hash_a(int32_t k, int bits) {
-  return ((uint32_t)k * 0x9E3779B1u) >> (32 - bits);
-}
-__device__ __forceinline__ uint32_t hash_b(int32_t k, int bits) {
-  return ((uint32_t)k * 0x85EBCA77u) >> (32 - bits);
-}
-
-// ---------------------------------------------------------------- hot set
-// Small open-addressing table of the hot dimensions (<= kHotMax keys in
-// kHotSlots slots): dimension -> position in the ascending hot list.
-__device__ __forceinline__ void hot_insert(int *keys, int8_t *vals, int32_t k, int h) {
-  uint32_t s = hash_a(k, 7);
-  for (int n = 0; n < kHotSlots; ++n) {
-    if (atomicCAS(&keys[s], -1, k) == -1) {
-      vals[s] = (int8_t)h;
-      return;
-    }
-    s = (s + 1) & (kHotSlots - 1);
-  }
-}
-__device__ __forceinline__ int hot_find(const int *keys, const int8_t *vals, int32_t k) {
-  uint32_t s = hash_a(k, 7);
-  for (int n = 0; n < kHotSlots; ++n) {
-    const int key = keys[s];
-    if (key == k) return vals[s];
-    if (key == -1) return -1;
-    s = (s + 1) & (kHotSlots - 1);
-  }
-  return -1;
 }
 
 // One block: counts the dimensions of `n_sample` evenly spaced rows in a

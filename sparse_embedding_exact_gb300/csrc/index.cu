@@ -16,10 +16,17 @@
 //   3. scatter: every nonzero (row r of chunk c, dim k, value v) takes the
 //      next slot of list (c, k) and stores (item r - first row of c, v).
 // A list's entries are in no particular order; the scorer does not need one.
+//
+// Hot dimensions.  When the item matrix has at least kSplitMinHot hot
+// dimensions (a Zipf-like head held by a large share of the rows), their
+// values go to a dense slab per chunk, slab[c][h][item], and not into the
+// lists: the scorer multiplies them as a small dense product and walks the
+// lists of the other ("cold") dimensions only.
 #include <cuda_runtime.h>
 
 #include <algorithm>
 
+#include "hotset.cuh"
 #include "internal.cuh"
 
 namespace {
@@ -36,9 +43,12 @@ __device__ __forceinline__ void flag(int32_t *status, int32_t code) {
 __global__ void __launch_bounds__(kHistThreads)
     k_histogram(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
                 int64_t row_begin, int64_t row_end, int64_t chunk_rows, int n_chunks, int64_t dim,
-                int32_t *__restrict__ count, int32_t *status) {
+                const int32_t *__restrict__ hot, int32_t *__restrict__ count, int32_t *status) {
   // First entry of each chunk of the build, then the build's end.
   __shared__ int64_t bound[kMaxBuildBatch + 1];
+  __shared__ int hkeys[hotset::kHotSlots];
+  __shared__ int8_t hvals[hotset::kHotSlots];
+  const bool split = hotset::load_hot_set(hot, hkeys, hvals) >= kSplitMinHot;
   if (threadIdx.x <= n_chunks) {
     const int64_t r = min(row_begin + (int64_t)threadIdx.x * chunk_rows, row_end);
     bound[threadIdx.x] = indptr[r];
@@ -51,6 +61,7 @@ __global__ void __launch_bounds__(kHistThreads)
     int c = 0;
     while (c + 1 < n_chunks && p >= bound[c + 1]) ++c;
     if (k >= 0 && (int64_t)k < dim) {
+      if (split && hotset::hot_find(hkeys, hvals, k) >= 0) continue;  // goes to the slab
       atomicAdd(count + (int64_t)c * (dim + 1) + k, 1);
     } else {
       flag(status, DEV_OUT_OF_RANGE);
@@ -148,9 +159,13 @@ __global__ void __launch_bounds__(kScanThreads)
 __global__ void __launch_bounds__(kHistThreads)
     k_scatter(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
               const float *__restrict__ values, int64_t row_begin, int64_t row_end,
-              int64_t chunk_rows, int64_t dim, int32_t *__restrict__ cursor,
-              uint16_t *__restrict__ post_item, float *__restrict__ post_val, int64_t capacity,
+              int64_t chunk_rows, int64_t dim, const int32_t *__restrict__ hot,
+              int32_t *__restrict__ cursor, uint16_t *__restrict__ post_item,
+              float *__restrict__ post_val, float *__restrict__ slab, int64_t capacity,
               int32_t *status) {
+  __shared__ int hkeys[hotset::kHotSlots];
+  __shared__ int8_t hvals[hotset::kHotSlots];
+  const bool split = hotset::load_hot_set(hot, hkeys, hvals) >= kSplitMinHot;
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (kHistThreads / 32);
   for (int64_t r = row_begin + (int64_t)blockIdx.x * (kHistThreads / 32) + (threadIdx.x >> 5);
@@ -162,6 +177,13 @@ __global__ void __launch_bounds__(kHistThreads)
     for (int64_t j = b + lane; j < e; j += 32) {
       const int32_t k = __ldg(indices + j);
       if (k < 0 || (int64_t)k >= dim) continue;  // flagged by the histogram
+      if (split) {
+        const int hh = hotset::hot_find(hkeys, hvals, k);
+        if (hh >= 0) {
+          slab[(c * hyb::kHotMax + hh) * chunk_rows + item] = __ldg(values + j);
+          continue;
+        }
+      }
       const int32_t pos = atomicAdd(cur + k, 1);
       if (pos >= 0 && (int64_t)pos < capacity) {
         post_item[pos] = item;
@@ -187,16 +209,22 @@ cudaError_t launch_build_index(ss_handle *h, const ss_csr &items, int64_t row_be
   const int64_t n = stride * n_chunks;
   cudaError_t e = cudaMemsetAsync(h->col_cnt, 0, sizeof(int32_t) * (size_t)n, s);
   if (e != cudaSuccess) return e;
+  // The hot slab (used only when the hot set is large enough to split off).
+  const int32_t *hot = h->slab_post ? h->hot : nullptr;
+  if (hot) {
+    e = cudaMemsetAsync(h->slab_post, 0, sizeof(float) * (size_t)n_chunks * hyb::kHotMax * (size_t)C, s);
+    if (e != cudaSuccess) return e;
+  }
   const int grid = h->sm_count * 8;
   k_histogram<<<grid, kHistThreads, 0, s>>>(items.indptr, items.indices, row_begin, row_end, C,
-                                            n_chunks, h->dim, h->col_cnt, h->d_status);
+                                            n_chunks, h->dim, hot, h->col_cnt, h->d_status);
   const int64_t tiles = scan_tile_count(n);
   k_scan_tile_sums<<<(unsigned)tiles, kScanThreads, 0, s>>>(h->col_cnt, n, h->scan_part);
   k_scan_partials<<<1, kScanThreads, 0, s>>>(h->scan_part, tiles);
   k_scan_apply<<<(unsigned)tiles, kScanThreads, 0, s>>>(h->col_cnt, n, h->scan_part, h->col_ptr);
   k_scatter<<<grid, kHistThreads, 0, s>>>(items.indptr, items.indices, items.values, row_begin,
-                                          row_end, C, h->dim, h->col_cnt, h->post_item,
-                                          h->post_val, h->post_cap, h->d_status);
+                                          row_end, C, h->dim, hot, h->col_cnt, h->post_item,
+                                          h->post_val, h->slab_post, h->post_cap, h->d_status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   for (int k = 0; k < n_chunks; ++k) {
@@ -211,6 +239,9 @@ cudaError_t launch_build_index(ss_handle *h, const ss_csr &items, int64_t row_be
     ix.post_item = h->post_item;
     ix.post_val = h->post_val;
     ix.capacity = h->post_cap;
+    ix.hot = hot;
+    ix.slab = hot ? h->slab_post + (size_t)k * hyb::kHotMax * (size_t)C : nullptr;
+    ix.slab_ld = (int32_t)C;
   }
   h->n_views = n_chunks;
   return cudaSuccess;

@@ -31,6 +31,10 @@ enum : int32_t {
   MODE_TILES = 1,    // always ALGO_HYBRID
   MODE_POSTING = 2,  // always ALGO_POSTING
 };
+// Posting lists split off the hot dimensions (dense slab and dense product)
+// when the item matrix has at least this many of them.
+constexpr int kSplitMinHot = 8;
+
 // The automatic choice takes posting lists when more than this share of the
 // first build's item tiles have more cold entries than an image holds.
 constexpr double kAutoOverflowShare = 0.5;
@@ -88,10 +92,12 @@ struct ss_index {
   const uint16_t *post_item = nullptr; // [capacity]: item within the chunk
   const float *post_val = nullptr;     // [capacity]
   int64_t capacity = 0;
+  int32_t slab_ld = 0;                 // the hot slab's item stride (posting lists: chunk_rows)
   // ALGO_HYBRID
   int32_t n_tiles = 0;
   const int32_t *hot = nullptr;        // [1 + kHotMax]: H, then the H hot dims ascending
-  const float *slab = nullptr;         // [tile][kHotMax][kTI]: value of hot dim h for item i (0 if absent)
+  const float *slab = nullptr;         // hybrid: [tile][kHotMax][kTI]; posting lists: [kHotMax][slab_ld];
+                                       // value of hot dim h for item i (0 if absent)
   const int2 *ell = nullptr;           // [tile][kEllMaxW][kTI]: (dim, value bits), dims ascending, -1 pads
   const int32_t *meta = nullptr;       // [tile][kMetaInts]
   const int32_t *heavy_k = nullptr;    // heavy items' cold entries: dim
@@ -170,6 +176,17 @@ struct ss_handle {
   int64_t post_cap = 0;
   int32_t *row_next = nullptr;   // [2]: the posting scorer's row counter and finished blocks
   int32_t *probe = nullptr;      // [2]: tiles probed, tiles above the image capacity
+  float *slab_post = nullptr;    // [build_batch][kHotMax][chunk_rows]: hot values (split lists)
+  // Dense hot values of the query matrix ([n_q][kHotMax]) for the posting
+  // path's split, for the current hot set; and the matrix they were made for.
+  float *qhot_dense = nullptr;
+  int64_t qhot_dense_cap = 0;
+  const void *qd_src[3] = {nullptr, nullptr, nullptr};
+  int64_t qd_rows = -1, qd_nnz = -1;
+  uint64_t qd_generation = ~0ull;
+  // Top-k with split lists: the chunk's dense hot scores ([n_q][chunk_rows]).
+  float *hot_scratch = nullptr;
+  int64_t hot_scratch_cap = 0;
   // The automatic choice, made once per item matrix (same identity as hot_src).
   const void *auto_src[3] = {nullptr, nullptr, nullptr};
   int64_t auto_src_rows = -1, auto_src_nnz = -1;

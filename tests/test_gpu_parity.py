@@ -426,6 +426,22 @@ def test_auto_choice_follows_tile_overflow(sec):
         assert _max_err(auto, oracle.cosine(Q, I)) <= TOL
 
 
+def test_posting_split_of_hot_dimensions(sec):
+    """With a large hot set (the heavy-tailed Zipf(1.3) workload) the posting
+    lists leave the hot dimensions to a dense product; with none (uniform)
+    nothing is split.  Both match the oracle, and a split handle agrees with
+    the tile path within the tolerance."""
+    for name, split in (("d1.2m_q20k_i1m_heavy", True), ("d500k_q50k_i500k_uniform", False)):
+        cfg = CONFIGS[name]
+        Q, I = generate_rows(cfg, 0, 0, 90), generate_rows(cfg, 1, 0, 5000)
+        with sec.SparseCosine(cfg.dim, algorithm="posting") as h:
+            st = h.index_stats(h.build_item_index(_dev(sec, I), 0, 5000))
+        assert (st["hot_dims"] >= 8) == split, (name, st)
+        got = _gpu_cosine(sec, Q, I, chunk_rows=2048, algorithm="posting")
+        assert _max_err(got, oracle.cosine(Q, I)) <= TOL, name
+        assert _max_err(got, _gpu_cosine(sec, Q, I, chunk_rows=2048, algorithm="hybrid")) <= TOL, name
+
+
 def test_posting_fold_over_many_shared_dims(sec):
     """Rows sharing more than 16,384 dimensions: the fixed-point low parts are
     folded into the high parts between segments, and the sums stay exact."""
@@ -462,6 +478,19 @@ def test_posting_rejects_inverse_norms_of_other_rows(sec):
         S = h.score_all(x, inv, x, inv).cpu().numpy()
         h.check_device()
     assert _max_err(S, oracle.cosine(X, X)) <= TOL
+
+
+@pytest.mark.parametrize("name,n_i,chunk", [("d65k_q1k_i10k", 10000, 10000),
+                                             ("d500k_q50k_i500k_uniform", 20000, 20000)])
+def test_posting_chunks_wider_than_one_window(sec, name, n_i, chunk):
+    """Chunks of more than 8,192 items: the accumulator covers 8,192 items at
+    a time and every list is walked once per window."""
+    cfg = CONFIGS[name]
+    Q, I = generate_rows(cfg, 0, 0, 70), generate_rows(cfg, 1, 0, n_i)
+    got = _gpu_cosine(sec, Q, I, chunk_rows=chunk, algorithm="posting")
+    ref = _gpu_cosine(sec, Q, I, chunk_rows=4096, algorithm="posting")
+    assert np.array_equal(got.view(np.int32), ref.view(np.int32))
+    assert _max_err(got, oracle.cosine(Q, I)) <= TOL
 
 
 @pytest.mark.parametrize("name", ["d1.2m_q20k_i1m_heavy", "d500k_q50k_i500k_uniform"])
