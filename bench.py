@@ -51,6 +51,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=WORKLOAD, choices=sorted(CONFIGS))
+    p.add_argument("--algorithm", default="auto", choices=["auto", "hybrid", "posting", "tensor"],
+                   help="scoring algorithm of the handle (auto: the library's choice per item matrix)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--topk", type=int, default=0,
@@ -281,7 +283,7 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg, Q, I, args.cpu_seconds)
 
-    h = sec.SparseCosine(cfg.dim, chunk_rows=CHUNK, device=local)
+    h = sec.SparseCosine(cfg.dim, chunk_rows=CHUNK, device=local, algorithm=args.algorithm)
     q = sec.DeviceCsr.from_host(Q, dev)
     it = sec.DeviceCsr.from_host(I, dev)
     n_q, n_i = Q.n_rows, I.n_rows
@@ -371,11 +373,13 @@ def run_ours(args):
     per_launch_s = statistics.mean(score_ms) / 1e3
     achieved = per_launch_bytes / per_launch_s / 1e9
     peak, peak_kind = measured_peaks()
-    kernel = "k_score_lists" if index_stats["algorithm"] == 1 else "k_score_tiles"
+    kernel = {0: "k_score_tiles", 1: "k_score_lists", 2: "k_tc_score"}[index_stats["algorithm"]]
+    label = {0: " (item tiles, ss_score_chunk)", 1: " (posting lists, ss_score_chunk)",
+             2: " (tensor cores; timed: the whole ss_score_chunk call = k_tc_prep_items + "
+                "k_tc_norm_lists + k_tc_records + k_tc_score)"}[index_stats["algorithm"]]
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "traffic": captured_traffic(cfg.name, kernel),
-            "kernel": kernel + (" (posting lists" if kernel == "k_score_lists" else " (item tiles")
-                      + ", ss_score_chunk)",
+            "kernel": kernel + label,
             "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
             "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
             "bytes_per_launch": per_launch_bytes, "launch_ms": 1e3 * per_launch_s,

@@ -75,6 +75,24 @@ typedef int32_t ss_status;
  * Setting both flags is SS_ERR_INVALID_ARG. */
 #define SS_ALGO_POSTING_LISTS 0x2
 #define SS_ALGO_TILES 0x8
+/* Tensor-core path: the (at most 128) dimensions held by the largest share of
+ * a row sample of the item matrix are multiplied on the tensor cores as a
+ * dense product of the normalised values, each split into two fp16 parts
+ * (hi = fp16(x), lo = fp16(x - hi)) so that hi*hi + hi*lo + lo*hi carries
+ * about 22 bits, accumulated in float32; the other ("cold") dimensions'
+ * products are summed exactly in fixed point (resolution 2^-28) and added
+ * once.  The cosines are within 2e-6 of the exact ones and bitwise the same
+ * for any chunking.  Best when the rows share a Zipf-like head of frequent
+ * dimensions (BM25/TF-IDF text).  Needs inverse norms of the rows (those of
+ * ss_row_norms): a normalised value above 1 + 2^-10 or a normalised row whose
+ * squares sum above 1 + 2^-6 ends the call with SS_ERR_DEVICE_CHECK.  The
+ * cold products of one scoring call are kept on the device in a buffer
+ * sized from the row sample (2.5 times the estimated count plus 4M); a call
+ * that needs more reports SS_ERR_DEVICE_CHECK at the next status read.
+ * The query side is prepared once per query matrix, inverse-norm array and
+ * item matrix: changing the contents of either array under the same
+ * pointers needs ss_invalidate.  Exclusive with the two flags above. */
+#define SS_ALGO_TENSOR 0x10
 /* ss_bulk_cosine_host verifies every streamed chunk: its checksum (see
  * ss_tile_checksum) is taken on the device before the copy and on the host
  * after it, and must agree; the pass then always goes through the ring. */

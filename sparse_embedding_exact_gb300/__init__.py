@@ -77,15 +77,17 @@ def _host_csr(batch):
 class SparseCosine:
     """One library handle: a device, a dimension and a chunk size."""
 
-    ALGORITHMS = ("auto", "hybrid", "posting")
+    ALGORITHMS = ("auto", "hybrid", "posting", "tensor")
 
     def __init__(self, dim: int, chunk_rows: int = DEFAULT_CHUNK_ROWS, device: int = 0,
                  validate: bool = False, algorithm: str = "auto", verify_stream: bool = False):
         """algorithm: "hybrid" (item tiles: dense hot dimensions + per-tile
         inverted indexes in shared memory), "posting" (per query row, the
         chunk's posting lists of its dimensions, summed exactly in fixed
-        point), or "auto" (the default: per item matrix, posting lists when
-        most item tiles of its first build overflow).
+        point), "tensor" (up to 128 frequent dimensions as a split-fp16
+        dense product on the tensor cores, the others summed exactly in
+        fixed point), or "auto" (the default: per item matrix, posting lists
+        when most item tiles of its first build overflow).
         verify_stream: bulk_cosine_host checks every chunk's checksum on the
         device against its host copy (and records them, see stream_checksums)."""
         self._lib = _abi.load()
@@ -100,6 +102,8 @@ class SparseCosine:
             flags |= _abi.SS_ALGO_POSTING_LISTS
         elif algorithm == "hybrid":
             flags |= _abi.SS_ALGO_TILES
+        elif algorithm == "tensor":
+            flags |= _abi.SS_ALGO_TENSOR
         if verify_stream:
             flags |= _abi.SS_VERIFY_STREAM
         h = ctypes.c_void_p()
@@ -287,8 +291,9 @@ class SparseCosine:
 
     def index_stats(self, index, stream=None) -> dict:
         """Diagnostics of the last built index (synchronises the stream).
-        "algorithm" is 0 for item tiles, 1 for posting lists; for posting
-        lists "ell_entries" holds the chunk's entries."""
+        "algorithm" is 0 for item tiles, 1 for posting lists, 2 for the
+        tensor path; for posting lists and the tensor path "ell_entries"
+        holds the chunk's list entries."""
         out = (ctypes.c_int64 * 8)()
         self._check(self._lib.ss_index_stats(self._h, index, out, _stream_ptr(stream)),
                     "ss_index_stats")

@@ -24,6 +24,7 @@ SS_TOPK_MAX = 64
 SS_VERIFY_STREAM = 0x4
 SS_ALGO_POSTING_LISTS = 0x2
 SS_ALGO_TILES = 0x8
+SS_ALGO_TENSOR = 0x10
 SS_MAX_CHUNK_ROWS = 65536
 
 

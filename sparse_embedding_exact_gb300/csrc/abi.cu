@@ -116,7 +116,7 @@ ss_status ensure_posting_workspace(ss_handle *h) {
 // path's heavy-item list) to hold `need` entries; synchronises the device
 // when it has to reallocate.
 ss_status ensure_capacity(ss_handle *h, int32_t algo, int64_t need) {
-  if (algo == ALGO_POSTING) {
+  if (algo == ALGO_POSTING || algo == ALGO_TENSOR) {
     if (need <= h->post_cap) return SS_OK;
     const int64_t cap = std::max<int64_t>(need, h->post_cap + h->post_cap / 2);
     SS_CUDA(h, cudaDeviceSynchronize());
@@ -163,8 +163,15 @@ void free_workspace(ss_handle *h) {
                   h->post_hat, h->row_next, h->probe, h->slab_post, h->qhot_dense,
                   h->hot_scratch, h->hot, h->slab, h->ell, h->meta, h->heavy_k,
                   h->heavy_v, h->heavy_item, h->counters, h->image, h->qhot, h->qcold,
-                  h->qcold_n, h->heavy_tbl};
+                  h->qcold_n, h->heavy_tbl, h->tc_hot, h->tc_sel, h->tc_stats, h->tc_A,
+                  h->tc_qcold, h->tc_qcold_n, h->tc_B, h->tc_rec, h->tc_rec_off,
+                  h->tc_slab, h->tc_sq};
   for (void *p : ptrs) cudaFree(p);
+  h->tc_hot = h->tc_sel = h->tc_qcold_n = h->tc_rec_off = nullptr;
+  h->tc_stats = h->tc_slab = h->tc_sq = nullptr;
+  h->tc_A = h->tc_B = nullptr;
+  h->tc_qcold = h->tc_rec = nullptr;
+  h->tc_A_cap = h->tc_qcold_cap = h->tc_qcold_n_cap = h->tc_B_cap = h->tc_rec_cap = h->tc_rec_off_cap = 0;
   h->post_hat = nullptr;
   h->row_next = nullptr;
   h->probe = nullptr;
@@ -198,6 +205,14 @@ ss_status build_algo(ss_handle *h, int32_t algo, const ss_csr &items, int64_t rb
   if (st != SS_OK) return st;
   h->algo = algo;
   int queued = 0;
+  if (algo == ALGO_TENSOR) {
+    if ((st = ensure_posting_workspace(h)) != SS_OK) return st;
+    SS_CUDA(h, launch_tc_hot_select(h, items, s, &queued));
+    h->launches += queued;
+    SS_CUDA(h, launch_build_tc(h, items, rb, re, s, &queued));
+    h->launches += queued;
+    return SS_OK;
+  }
   SS_CUDA(h, launch_hot_select(h, items, s, &queued));
   if (algo == ALGO_POSTING) {
     if ((st = ensure_posting_workspace(h)) != SS_OK) return st;
@@ -224,6 +239,7 @@ bool same_auto_source(const ss_handle *h, const ss_csr &m) {
 ss_status build_chunk(ss_handle *h, const ss_csr &items, int64_t rb, int64_t re, cudaStream_t s) {
   if (h->mode == MODE_POSTING) return build_algo(h, ALGO_POSTING, items, rb, re, s);
   if (h->mode == MODE_TILES) return build_algo(h, ALGO_HYBRID, items, rb, re, s);
+  if (h->mode == MODE_TENSOR) return build_algo(h, ALGO_TENSOR, items, rb, re, s);
   if (!same_auto_source(h, items)) {
     int queued = 0;
     SS_CUDA(h, launch_hot_select(h, items, s, &queued));
@@ -248,6 +264,11 @@ cudaError_t score(ss_handle *h, const ss_csr &q, const float *inv_q, const ss_in
   int queued = 0;
   if (idx.algo == ALGO_POSTING) {
     const cudaError_t e = launch_score_lists(h, q, inv_q, idx, inv_i, out, ld_out, s, &queued, topk);
+    h->launches += queued;
+    return e;
+  }
+  if (idx.algo == ALGO_TENSOR) {
+    const cudaError_t e = launch_score_tc(h, q, inv_q, idx, inv_i, out, ld_out, s, &queued, topk);
     h->launches += queued;
     return e;
   }
@@ -329,12 +350,17 @@ ss_status ss_create(ss_handle **out, int device, int64_t dim, int32_t chunk_rows
   h->dim = dim;
   h->chunk_rows = chunk_rows;
   h->flags = flags;
-  if ((flags & SS_ALGO_POSTING_LISTS) && (flags & SS_ALGO_TILES)) {
+  const int n_algo_flags = ((flags & SS_ALGO_POSTING_LISTS) != 0) + ((flags & SS_ALGO_TILES) != 0) +
+                           ((flags & SS_ALGO_TENSOR) != 0);
+  if (n_algo_flags > 1) {
     delete h;
     return SS_ERR_INVALID_ARG;
   }
-  h->mode = (flags & SS_ALGO_POSTING_LISTS) ? MODE_POSTING : (flags & SS_ALGO_TILES) ? MODE_TILES : MODE_AUTO;
-  h->algo = (h->mode == MODE_POSTING) ? ALGO_POSTING : ALGO_HYBRID;
+  h->mode = (flags & SS_ALGO_POSTING_LISTS) ? MODE_POSTING
+            : (flags & SS_ALGO_TILES)       ? MODE_TILES
+            : (flags & SS_ALGO_TENSOR)      ? MODE_TENSOR
+                                            : MODE_AUTO;
+  h->algo = (h->mode == MODE_POSTING) ? ALGO_POSTING : (h->mode == MODE_TENSOR) ? ALGO_TENSOR : ALGO_HYBRID;
   cudaError_t e = cudaSetDevice(device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, device);
   if (e == cudaSuccess) e = cudaMalloc(&h->d_status, sizeof(int32_t));
@@ -355,7 +381,7 @@ ss_status ss_create(ss_handle **out, int device, int64_t dim, int32_t chunk_rows
   }
   // The posting-list workspace is allocated by the first posting build; the
   // tile workspace unless the handle only ever builds posting lists.
-  if (e == cudaSuccess && h->mode != MODE_POSTING) {
+  if (e == cudaSuccess && h->mode != MODE_POSTING && h->mode != MODE_TENSOR) {
     using namespace hyb;
     const size_t tiles = (size_t)h->max_tiles;
     if (e == cudaSuccess) e = cudaMalloc(&h->slab, sizeof(float) * tiles * kHotMax * kTI);
@@ -397,6 +423,10 @@ ss_status ss_validate_csr(ss_handle *h, const ss_csr *m, void *stream) {
 ss_status ss_invalidate(ss_handle *h) {
   if (!h) return SS_ERR_INVALID_ARG;
   for (int j = 0; j < 3; ++j) h->hot_src[j] = h->prep_src[j] = h->auto_src[j] = h->qd_src[j] = nullptr;
+  for (int j = 0; j < 3; ++j) h->tc_hot_src[j] = nullptr;
+  for (int j = 0; j < 4; ++j) h->tcq_src[j] = nullptr;
+  h->tc_hot_rows = h->tc_hot_nnz = h->tcq_rows = h->tcq_nnz = -1;
+  h->tcq_generation = ~0ull;
   h->hot_src_rows = h->hot_src_nnz = h->prep_rows = h->prep_nnz = -1;
   h->auto_src_rows = h->auto_src_nnz = h->qd_rows = h->qd_nnz = -1;
   h->qd_generation = ~0ull;
@@ -414,6 +444,16 @@ ss_status ss_index_stats(ss_handle *h, const ss_index *idx, int64_t *stats, void
   stats[0] = idx->algo;
   stats[1] = idx->n_items;
   SS_CUDA(h, cudaStreamSynchronize(as_stream(stream)));
+  if (idx->algo == ALGO_TENSOR) {
+    int32_t ends[2] = {0, 0};
+    SS_CUDA(h, cudaMemcpy(&ends[0], idx->col_ptr, sizeof(int32_t), cudaMemcpyDeviceToHost));
+    SS_CUDA(h, cudaMemcpy(&ends[1], idx->col_ptr + idx->dim, sizeof(int32_t), cudaMemcpyDeviceToHost));
+    stats[6] = ends[1] - ends[0];
+    int32_t hcount = 0;
+    SS_CUDA(h, cudaMemcpy(&hcount, idx->hot, sizeof(int32_t), cudaMemcpyDeviceToHost));
+    stats[3] = hcount;
+    return SS_OK;
+  }
   if (idx->algo == ALGO_POSTING) {
     int32_t ends[2] = {0, 0};
     SS_CUDA(h, cudaMemcpy(&ends[0], idx->col_ptr, sizeof(int32_t), cudaMemcpyDeviceToHost));

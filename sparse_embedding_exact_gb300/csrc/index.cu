@@ -199,6 +199,15 @@ __global__ void __launch_bounds__(kHistThreads)
 
 int64_t scan_tile_count(int64_t n) { return (n + kScanTile - 1) / kScanTile; }
 
+cudaError_t launch_count_scan(int32_t *count, int64_t n, int32_t *part, int32_t *col_ptr,
+                              cudaStream_t s) {
+  const int64_t tiles = scan_tile_count(n);
+  k_scan_tile_sums<<<(unsigned)tiles, kScanThreads, 0, s>>>(count, n, part);
+  k_scan_partials<<<1, kScanThreads, 0, s>>>(part, tiles);
+  k_scan_apply<<<(unsigned)tiles, kScanThreads, 0, s>>>(count, n, part, col_ptr);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_build_index(ss_handle *h, const ss_csr &items, int64_t row_begin,
                                int64_t row_end, cudaStream_t s) {
   const int64_t C = h->chunk_rows;

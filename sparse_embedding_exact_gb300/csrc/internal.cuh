@@ -23,6 +23,7 @@ enum : int32_t {
 enum : int32_t {
   ALGO_HYBRID = 0,   // dense hot dimensions in registers + sparse cold lists in shared memory
   ALGO_POSTING = 1,  // one block per query row walking the chunk's posting lists
+  ALGO_TENSOR = 2,   // up to 128 hot dimensions on the tensor cores + exact cold records
 };
 
 // How a handle picks the algorithm of its chunk indexes.
@@ -30,6 +31,7 @@ enum : int32_t {
   MODE_AUTO = 0,     // per item matrix, from the tile overflow of its first build
   MODE_TILES = 1,    // always ALGO_HYBRID
   MODE_POSTING = 2,  // always ALGO_POSTING
+  MODE_TENSOR = 3,   // always ALGO_TENSOR
 };
 // Posting lists split off the hot dimensions (dense slab and dense product)
 // when the item matrix has at least this many of them.
@@ -106,7 +108,22 @@ struct ss_index {
   const int4 *heavy_tbl = nullptr;     // [tile][kTI]: heavy items {item, first entry - tile's heavy base, count, 0}
   const unsigned char *image = nullptr; // [tile][kImgBytes]
   const int32_t *counters = nullptr;   // [1] tiles without an image, [2..] their ids ([0] unused)
+  // ALGO_TENSOR (also col_ptr / post_item / post_val / capacity: the cold
+  // dimensions' lists; hot: the tensor hot set; slab: [item][tcp::kHotMax]
+  // raw hot values, 0 if absent)
+  const float *sq = nullptr;           // [n_items]: each item's raw sum of squares
 };
+
+// Tensor-core path (see tensor.cu).
+namespace tcp {
+constexpr int kHotMax = 128;   // hot dimensions multiplied on the tensor cores
+constexpr int kM = 128;        // query rows per tile (MMA M)
+constexpr int kN = 256;        // items per tile (MMA N)
+constexpr int kColBlock = 32;  // items per cold-record bucket
+// The automatic choice takes the tensor path when the estimated cold
+// overlap (expected shared cold dimensions per pair) is at most this.
+constexpr double kAutoMaxCold = 0.25;
+}  // namespace tcp
 
 // Most chunks one hybrid index build covers (one launch, one view per chunk).
 constexpr int kMaxBuildBatch = 8;
@@ -225,6 +242,43 @@ struct ss_handle {
   int64_t prep_rows = -1, prep_nnz = -1;
   uint64_t prep_generation = ~0ull;
 
+  // ALGO_TENSOR: the tensor hot set ([1 + tcp::kHotMax]: H, dims ascending),
+  // its selection table, and {estimated cold overlap per pair, H} on the
+  // device and as read back once per item matrix.
+  int32_t *tc_hot = nullptr;
+  int32_t *tc_sel = nullptr;
+  float *tc_stats = nullptr;
+  double tc_est_cold = 0.0;
+  int32_t tc_H = 0;
+  const void *tc_hot_src[3] = {nullptr, nullptr, nullptr};
+  int64_t tc_hot_rows = -1, tc_hot_nnz = -1;
+  uint64_t tc_hot_generation = 0;
+  // Query operand ([query tiles][kM x 2Hp] fp16) and cold entries ({dim,
+  // normalised value bits} at the row's own CSR positions; counts per row),
+  // for the query matrix, inverse norms and hot set they were made for.
+  uint16_t *tc_A = nullptr;
+  int64_t tc_A_cap = 0;
+  int2 *tc_qcold = nullptr;
+  int64_t tc_qcold_cap = 0;
+  int32_t *tc_qcold_n = nullptr;
+  int64_t tc_qcold_n_cap = 0;
+  const void *tcq_src[4] = {nullptr, nullptr, nullptr, nullptr};
+  int64_t tcq_rows = -1, tcq_nnz = -1;
+  uint64_t tcq_generation = ~0ull;
+  // Per chunk of a build: raw hot values [chunk_rows][kHotMax] and sums of
+  // squares [chunk_rows].
+  float *tc_slab = nullptr;
+  float *tc_sq = nullptr;
+  // Item operand of the chunk being scored ([item tiles][kN x 2Hp] fp16).
+  uint16_t *tc_B = nullptr;
+  int64_t tc_B_cap = 0;
+  // Cold records of one scoring call: fixed-size buckets per (32 query
+  // rows, 32 items) and their counts (-1: the bucket did not fit).
+  int2 *tc_rec = nullptr;
+  int64_t tc_rec_cap = 0;
+  int32_t *tc_rec_off = nullptr;
+  int64_t tc_rec_off_cap = 0;
+
   // The last build's chunk indexes (views into the workspace above).
   ss_index views[kMaxBuildBatch];
   int32_t n_views = 0;
@@ -278,6 +332,19 @@ cudaError_t launch_tile_checksum(const float *tile, int64_t n_rows, int64_t n_co
                                  cudaStream_t s);
 void tile_checksum_host(const float *tile, int64_t n_rows, int64_t n_cols, int64_t ld,
                         uint64_t *bits_sum, double *value_sum);
+
+// Tensor-core path (tensor.cu).  The hot set is chosen once per item matrix
+// (reads back its statistics: synchronises the stream then).
+cudaError_t launch_tc_hot_select(ss_handle *h, const ss_csr &items, cudaStream_t s, int *queued);
+cudaError_t launch_build_tc(ss_handle *h, const ss_csr &items, int64_t row_begin, int64_t row_end,
+                            cudaStream_t s, int *queued);
+cudaError_t launch_score_tc(ss_handle *h, const ss_csr &queries, const float *inv_q,
+                            const ss_index &idx, const float *inv_i, float *out, int64_t ld_out,
+                            cudaStream_t s, int *queued, const ss_topk *topk = nullptr);
+// Exclusive scan of n counters (three kernels): col_ptr gets the scan, and
+// count is reset to the same values (scatter cursors).
+cudaError_t launch_count_scan(int32_t *count, int64_t n, int32_t *part, int32_t *col_ptr,
+                              cudaStream_t s);
 
 // Kernels queued by one launch_build_index call.
 constexpr int kIndexKernels = 5;

@@ -253,6 +253,9 @@ extern "C" ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *qh, const s
                      static_cast<const int32_t *>(hp.buf[HP::kIIdx]),
                      static_cast<const float *>(hp.buf[HP::kIVal]), n_i, ih->nnz, h->dim};
   void *vs = reinterpret_cast<void *>(hp.comp);
+  // The device copies above reuse the pass's buffers: whatever the handle
+  // prepared from an earlier pass's matrices at these addresses is stale.
+  ss_invalidate(h);
   if ((st = ss_row_norms(h, &qd, inv_q, vs)) != SS_OK) return st;
   if ((st = ss_row_norms(h, &id, inv_i, vs)) != SS_OK) return st;
   const int64_t n_chunks = (n_i + C - 1) / C;

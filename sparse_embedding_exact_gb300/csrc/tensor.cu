@@ -1,0 +1,1354 @@
+// Tensor-core scoring path: the hot dimensions as a dense product on the
+// fifth-generation tensor cores (tcgen05, accumulators in tensor memory),
+// the cold dimensions as exact fixed-point records added in the epilogue.
+//
+// What is computed is the sparse dot product of the blog post "Engineering
+// practice for bulk similarity calculation over sparse embeddings", section
+// 3.1 (u.v over the shared support), of rows normalised first (section 4.4
+// normalises right after the product; here the inputs are normalised, which
+// is the same cosine and keeps every operand in [-1, 1]).
+//
+// In BM25/TF-IDF data the head of the dictionary (section 3.2) is held by a
+// large share of the rows: on a Zipf(1.1) law over 1.2M words, the 128 most
+// frequent dimensions carry 98% of the expected 6.8 shared dimensions of a
+// pair.  Those dimensions are multiplied as a dense [128 queries x 256 items
+// x H] product per tile pair.  The tensor cores take 16-bit operands, so
+// each normalised value x (|x| <= 1) is split as x = hi + lo with hi =
+// fp16(x) and lo = fp16(x - hi) (the split of Dekker / Ogita-Rump-Oishi
+// used for extended-precision dot products), and the tile accumulates
+// hi_q lo_v + lo_q hi_v (first, while the sum is small) then hi_q hi_v in
+// FP32: the dropped lo_q lo_v and the splitting error are below 2^-22 |x|
+// (2^-25 absolute for values in fp16's subnormal range).
+//
+// The remaining ("cold") dimensions are few per pair (0.11 expected on the
+// 1.2M-word workload).  A records kernel walks, for every block of 32 query
+// rows, each row's cold nonzeros against the chunk's posting lists (CSC by
+// dimension, the cold dimensions only) and writes one record per product,
+// bucketed by (32 query rows, 32 items): the position inside the bucket and
+// the product rounded to a fixed-point integer of resolution 2^-28.  The
+// scorer's epilogue adds a bucket's records into a 32 x 32 integer tile in
+// shared memory (integer sums do not depend on order, so the result is the
+// same bit for bit for any launch shape and chunking), adds that to the
+// tensor result and stores the tile.
+//
+// Scorer (k_tc_score): persistent, one block per SM, 6 warps.  Warp 0 loads
+// operand tiles with bulk asynchronous copies (an item tile's operand stays
+// while the block works through its query tiles); warp 1 allocates tensor
+// memory and one of its threads issues the MMAs into one of two
+// accumulators; warps 2-5 each own a quarter of the 128 accumulator lanes
+// and run the epilogue of one tile pair while the MMAs of the next run.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <cmath>
+
+#include <string.h>
+
+#include <algorithm>
+
+#include "internal.cuh"
+#include "topk.cuh"
+
+namespace {
+
+using namespace tcp;
+
+constexpr int kHotSlotsBits = 9;
+constexpr int kHotSlots = 1 << kHotSlotsBits;  // <= 128 keys: load <= 1/4
+constexpr int kSelSlotsBits = 16;
+constexpr int kSelSlots = 1 << kSelSlotsBits;  // selection table (global memory)
+constexpr int64_t kSampleEntries = 32768;      // nonzeros sampled to choose the hot set
+constexpr int kSelThreads = 1024;
+constexpr float kFixScale = 268435456.0f;      // 2^28: cold records' fixed point
+constexpr float kFixInv = 1.0f / 268435456.0f;
+constexpr float kMaxNormalised = 1.0f + 1.0f / 1024.0f;  // |x| of a normalised value
+constexpr float kMaxSquareSum = 1.0f + 1.0f / 64.0f;     // sum of x^2 of a normalised row
+constexpr int kStgInts = 32 * 32;              // one staging tile: 32 rows x 32 ints, 128-byte swizzle
+constexpr int kEpiWarps = 8;                   // two per quarter of the accumulator lanes
+constexpr int kSThreads = 64 + 32 * kEpiWarps; // producer, MMA, epilogue warps
+constexpr int kStgBytes = kEpiWarps * kStgInts * 4 + 1024;  // one tile per warp, 1024-byte aligned
+constexpr int kRThreads = 1024;         // records: one warp per query row of the block
+constexpr int kPrepThreads = 256;
+constexpr int kWalkUnroll = 4;          // list entries per lane loaded before use
+constexpr int kRecPerLane = 4;          // epilogue: records of a block held per lane (128 per block)
+constexpr long long kWaitNs = 2000000000ll;    // bounded waits: 2 s
+
+__device__ __forceinline__ void flag(int32_t *status, int32_t code) { atomicCAS(status, DEV_OK, code); }
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ long long global_ns() {
+  long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase of `parity` to complete, for at most kWaitNs; false
+// (and a DEV_STALL flag) when it runs out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t *status) {
+  if (mbar_try(bar, parity)) return true;
+  const long long t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitNs) {
+      flag(status, DEV_STALL);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// Bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16),
+// completing as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// Shared-memory matrix descriptor: K-major operand without swizzle, made of
+// core matrices of 8 rows x 16 bytes (128 contiguous bytes); lbo = bytes
+// between core matrices adjacent in K, sbo = bytes between adjacent groups
+// of 8 rows.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (fp16 inputs, fp32 accumulate).
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t da, uint64_t db, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(da), "l"(db), "r"(idesc), "r"(accumulate));
+}
+// Arrives on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+// Element (r, c) of a 32 x 32 int staging tile with 16-byte chunk j of row r
+// stored at chunk j ^ (r % 8): both the row-per-lane and the
+// chunk-per-lane accesses of the epilogue are then free of bank conflicts.
+__device__ __forceinline__ int stg_index(int r, int c) { return r * 32 + ((((c >> 2) ^ (r & 7)) << 2) | (c & 3)); }
+// The fixed-point cold product of a normalised query value and a
+// normalised list value (the records and the scorer's direct path agree on
+// it bit for bit).
+__device__ __forceinline__ int cold_fix(float qv, float vv) { return __float2int_rn((qv * vv) * kFixScale); }
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Read-only loads issued exactly where they are written: the compiler may
+// otherwise sink a plain load to its first use, which defeats a prefetch.
+__device__ __forceinline__ int2 ld_keep_int2(const int2 *p) {
+  int2 v;
+  asm volatile("ld.global.nc.v2.s32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ int ld_keep_int(const int32_t *p) {
+  int v;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// ---------------------------------------------------------------- hot table
+// Dimension -> position in the ascending hot list, for <= kHotMax keys.
+__device__ __forceinline__ uint32_t hot_hash(int32_t k) {
+  return ((uint32_t)k * 0x9E3779B1u) >> (32 - kHotSlotsBits);
+}
+__device__ __forceinline__ int load_hot(const int32_t *hot, int *keys, uint8_t *vals) {
+  for (int j = threadIdx.x; j < kHotSlots; j += blockDim.x) keys[j] = -1;
+  __syncthreads();
+  const int H = hot[0];
+  for (int j = threadIdx.x; j < H; j += blockDim.x) {
+    const int32_t k = hot[1 + j];
+    uint32_t s = hot_hash(k);
+    for (int n = 0; n < kHotSlots; ++n) {
+      if (atomicCAS(&keys[s], -1, k) == -1) {
+        vals[s] = (uint8_t)j;
+        break;
+      }
+      s = (s + 1) & (kHotSlots - 1);
+    }
+  }
+  __syncthreads();
+  return H;
+}
+__device__ __forceinline__ int find_hot(const int *keys, const uint8_t *vals, int32_t k) {
+  uint32_t s = hot_hash(k);
+  for (int n = 0; n < kHotSlots; ++n) {
+    const int key = keys[s];
+    if (key == k) return vals[s];
+    if (key == -1) return -1;
+    s = (s + 1) & (kHotSlots - 1);
+  }
+  return -1;
+}
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// ---------------------------------------------------------------- hot set
+// Counts the dimensions of n_sample evenly spaced item rows in a global
+// open-addressing table (keys then counts, kSelSlots each).
+__global__ void __launch_bounds__(256)
+    k_tc_sel_insert(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
+                    int64_t n_rows, int64_t n_sample, int32_t *__restrict__ tab) {
+  int32_t *keys = tab, *cnts = tab + kSelSlots;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * 8;
+  for (int64_t j = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); j < n_sample; j += warps) {
+    const int64_t r = j * n_rows / n_sample;
+    for (int64_t p = indptr[r] + lane; p < indptr[r + 1]; p += 32) {
+      const int32_t k = indices[p];
+      uint32_t s = ((uint32_t)k * 0x9E3779B1u) >> (32 - kSelSlotsBits);
+      for (int n = 0; n < 256; ++n) {  // a full neighbourhood drops the sample
+        const int prev = atomicCAS(&keys[s], -1, k);
+        if (prev == -1 || prev == k) {
+          atomicAdd(&cnts[s], 1);
+          break;
+        }
+        s = (s + 1) & (kSelSlots - 1);
+      }
+    }
+  }
+}
+
+// Ascending bitonic sort of n (a power of two) 64-bit keys in shared memory
+// by the whole block.
+__device__ void block_sort(unsigned long long *v, int n) {
+  for (int k = 2; k <= n; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const bool up = (i & k) == 0;
+          const unsigned long long x = v[i], y = v[ixj];
+          if ((x > y) == up) {
+            v[i] = y;
+            v[ixj] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+}
+
+// Visits the selection table's slots [64 t, 64 t + 64) as f(key, count),
+// their loads issued 32 slots at a time (the table lives in global memory).
+template <typename F>
+__device__ __forceinline__ void for_my_slots(const int32_t *keys, const int32_t *cnts, int t, F f) {
+  static_assert(kSelSlots == 64 * kSelThreads, "one run of 64 slots per thread");
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {
+    int4 k4[8], c4[8];
+    const int base = 64 * t + 32 * h;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      k4[q] = *reinterpret_cast<const int4 *>(keys + base + 4 * q);
+      c4[q] = *reinterpret_cast<const int4 *>(cnts + base + 4 * q);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      f(k4[q].x, c4[q].x);
+      f(k4[q].y, c4[q].y);
+      f(k4[q].z, c4[q].z);
+      f(k4[q].w, c4[q].w);
+    }
+  }
+}
+
+constexpr int kCountBins = 1024;  // sampled counts at or above the last bin share it
+constexpr int kTieCap = 4096;     // dimensions tied at the threshold count that are ranked
+
+// One block.  The hot set: the (at most kHotMax) most frequent sampled
+// dimensions held by at least max(2, 0.2% of the sampled rows), ties to the
+// lower dimension (counts of kCountBins - 1 or more count as equal); hot[0]
+// = H, hot[1..H] ascending.  The threshold comes from a histogram of the
+// counts; the dimensions tied at it are sorted, and when more than kTieCap
+// are tied none of them is taken.  stats[0]: the sampled rows' expected
+// number of shared dimensions outside the hot set per pair of rows, sum
+// c (c - 1) / (n (n - 1)) over the other dimensions' counts c (an unbiased
+// estimate of their sum of squared frequencies); stats[1] = H.
+__global__ void __launch_bounds__(kSelThreads)
+    k_tc_sel_pick(const int32_t *__restrict__ tab, int64_t n_sample, int32_t *__restrict__ hot,
+                  float *__restrict__ stats) {
+  const int32_t *keys = tab, *cnts = tab + kSelSlots;
+  __shared__ int hist[kCountBins];
+  __shared__ unsigned long long ties[kTieCap];
+  __shared__ unsigned long long sel[2 * kHotMax];
+  __shared__ int n_above, n_ties, thr_sh, take_ties;
+  __shared__ unsigned long long pairs_all, pairs_hot;
+  const int tid = threadIdx.x;
+  for (int j = tid; j < kCountBins; j += kSelThreads) hist[j] = 0;
+  for (int j = tid; j < 2 * kHotMax; j += kSelThreads) sel[j] = ~0ull;
+  for (int j = tid; j < kTieCap; j += kSelThreads) ties[j] = ~0ull;
+  if (tid == 0) {
+    n_above = n_ties = 0;
+    pairs_all = pairs_hot = 0ull;
+  }
+  __syncthreads();
+  const int floor_c = min(kCountBins - 1, max(2, (int)((n_sample * 2 + 999) / 1000)));
+  unsigned long long my_pairs = 0;
+  for_my_slots(keys, cnts, tid, [&](int key, int c) {
+    if (key < 0) return;
+    my_pairs += (unsigned long long)c * (unsigned long long)(c - 1);
+    if (c >= floor_c) atomicAdd(&hist[min(c, kCountBins - 1)], 1);
+  });
+  atomicAdd(&pairs_all, my_pairs);
+  __syncthreads();
+  if (tid == 0) {
+    // Largest bin t where the dimensions in bins > t are fewer than kHotMax
+    // and those in bins >= t reach it; -1 when all of them fit.
+    int above = 0, thr = -1;
+    for (int c = kCountBins - 1; c >= floor_c; --c) {
+      if (above + hist[c] >= kHotMax) {
+        thr = c;
+        break;
+      }
+      above += hist[c];
+    }
+    thr_sh = thr;
+    take_ties = thr >= 0 && hist[thr] <= kTieCap;
+  }
+  __syncthreads();
+  const int thr = thr_sh;
+  for_my_slots(keys, cnts, tid, [&](int kd, int c) {
+    if (kd < 0 || c < floor_c) return;
+    const int cc = min(c, kCountBins - 1);
+    const unsigned long long key = ((unsigned long long)(uint32_t)kd << 32) | (uint32_t)c;
+    if (thr < 0 || cc > thr) {
+      sel[atomicAdd(&n_above, 1)] = key;  // fewer than kHotMax of them
+    } else if (cc == thr && take_ties) {
+      ties[atomicAdd(&n_ties, 1)] = key;
+    }
+  });
+  __syncthreads();
+  int nt = 1;
+  while (nt < n_ties) nt <<= 1;
+  block_sort(ties, nt);  // lower dimensions first
+  const int above = n_above;
+  const int need = min(kHotMax - above, n_ties);
+  for (int j = tid; j < need; j += kSelThreads) sel[above + j] = ties[j];
+  __syncthreads();
+  block_sort(sel, 2 * kHotMax);
+  const int H = above + max(need, 0);
+  unsigned long long hp = 0;
+  for (int j = tid; j < H; j += kSelThreads) {
+    hot[1 + j] = (int32_t)(sel[j] >> 32);
+    const unsigned long long c = sel[j] & 0xffffffffull;
+    hp += c * (c - 1);
+  }
+  atomicAdd(&pairs_hot, hp);
+  __syncthreads();
+  if (tid == 0) {
+    hot[0] = H;
+    const double ns = (double)n_sample;
+    stats[0] = ns > 1.0 ? (float)((double)(pairs_all - pairs_hot) / (ns * (ns - 1.0))) : 0.f;
+    stats[1] = (float)H;
+  }
+}
+
+// ---------------------------------------------------------------- build
+// Posting lists of the cold dimensions (the hot ones are left out): the
+// histogram and scatter of a counting sort by dimension, per chunk of the
+// build, as the posting-list path builds them.
+__global__ void __launch_bounds__(256)
+    k_tc_hist(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
+              int64_t row_begin, int64_t row_end, int64_t chunk_rows, int n_chunks, int64_t dim,
+              const int32_t *__restrict__ hot, int32_t *__restrict__ count, int32_t *status) {
+  __shared__ int64_t bound[kMaxBuildBatch + 1];
+  __shared__ int hkeys[kHotSlots];
+  __shared__ uint8_t hvals[kHotSlots];
+  load_hot(hot, hkeys, hvals);
+  if (threadIdx.x <= n_chunks) {
+    const int64_t r = min(row_begin + (int64_t)threadIdx.x * chunk_rows, row_end);
+    bound[threadIdx.x] = indptr[r];
+  }
+  __syncthreads();
+  const int64_t p0 = bound[0], p1 = bound[n_chunks];
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t p = p0 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < p1; p += stride) {
+    const int32_t k = __ldg(indices + p);
+    int c = 0;
+    while (c + 1 < n_chunks && p >= bound[c + 1]) ++c;
+    if (k >= 0 && (int64_t)k < dim) {
+      if (find_hot(hkeys, hvals, k) >= 0) continue;
+      atomicAdd(count + (int64_t)c * (dim + 1) + k, 1);
+    } else {
+      flag(status, DEV_OUT_OF_RANGE);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256)
+    k_tc_scatter(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
+                 const float *__restrict__ values, int64_t row_begin, int64_t row_end,
+                 int64_t chunk_rows, int64_t dim, const int32_t *__restrict__ hot,
+                 int32_t *__restrict__ cursor, uint16_t *__restrict__ post_item,
+                 float *__restrict__ post_val, int64_t capacity, float *__restrict__ slab,
+                 float *__restrict__ sq, int32_t *status) {
+  __shared__ int hkeys[kHotSlots];
+  __shared__ uint8_t hvals[kHotSlots];
+  load_hot(hot, hkeys, hvals);
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * 8;
+  for (int64_t r = row_begin + (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < row_end; r += warps) {
+    const int64_t b = indptr[r], e = indptr[r + 1];
+    const int64_t c = (r - row_begin) / chunk_rows;
+    int32_t *cur = cursor + c * (dim + 1);
+    const int64_t item = r - row_begin - c * chunk_rows;
+    float ss = 0.f;
+    for (int64_t j = b + lane; j < e; j += 32) {
+      const int32_t k = __ldg(indices + j);
+      const float v = __ldg(values + j);
+      ss = fmaf(v, v, ss);
+      if (k < 0 || (int64_t)k >= dim) continue;  // flagged by the histogram
+      const int h = find_hot(hkeys, hvals, k);
+      if (h >= 0) {
+        slab[(c * chunk_rows + item) * kHotMax + h] = v;
+        continue;
+      }
+      const int32_t pos = atomicAdd(cur + k, 1);
+      if (pos >= 0 && (int64_t)pos < capacity) {
+        post_item[pos] = (uint16_t)item;
+        post_val[pos] = v;
+      } else {
+        flag(status, DEV_CAPACITY);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) sq[c * chunk_rows + item] = ss;
+  }
+}
+
+// ---------------------------------------------------------------- operands
+// An operand tile of R rows (R = kM queries or kN items) with Hp hot columns
+// is stored as two parts, hi then lo, each in the no-swizzle K-major layout:
+// 8-row groups of Hp / 8 core matrices (8 rows x 8 halves, 128 bytes), so a
+// part is R * Hp halves and element (r, k) of a part sits at
+// (r / 8) * 8 Hp + (k / 8) * 64 + (r % 8) * 8 + k % 8.
+__device__ __forceinline__ int core_off(int r8, int k) { return (k >> 3) * 64 + r8 * 8 + (k & 7); }
+
+struct PrepArgs {
+  const int64_t *indptr;  // queries: the CSR
+  const int32_t *idx;
+  const float *val;
+  const float *slab;      // items: [item][kHotMax] raw hot values of the chunk
+  const float *sq;        // items: raw sum of squares per item
+  int64_t n_rows;         // rows of the matrix (queries) or of the chunk (items)
+  int64_t n_groups;       // 8-row groups to write (whole tiles)
+  const float *inv;       // inverse norms of those rows
+  const int32_t *hot;
+  int32_t Hp;
+  int32_t gpt;            // 8-row groups per tile (kM / 8 or kN / 8)
+  uint16_t *op;           // operand tiles (hi part, lo part)
+  int2 *qcold;            // queries: {dim, normalised value bits} at the row's CSR positions
+  int32_t *qcold_n;       // queries: cold entries per row
+  int32_t *status;
+};
+
+// The warp's group buffer holds the group's hi part ([0, 8 Hp) halves) then
+// its lo part.
+__device__ __forceinline__ void put_split(uint16_t *gs, int rr, int h, int Hp, float x) {
+  const __half hi = __float2half_rn(x);
+  const __half lo = __float2half_rn(x - __half2float(hi));
+  gs[core_off(rr, h)] = __half_as_ushort(hi);
+  gs[8 * Hp + core_off(rr, h)] = __half_as_ushort(lo);
+}
+
+// Writes a group buffer (hi and lo parts, 8 Hp halves each) to group g of an
+// operand whose tiles hold `gpt` groups.
+__device__ __forceinline__ void store_group(uint16_t *op, const uint16_t *gs, int64_t g, int gpt, int Hp,
+                                            int lane) {
+  const int64_t t = g / gpt, gl = g % gpt;
+  const int P = 8 * Hp;  // halves of one group part
+  uint16_t *hi = op + (t * 2 * gpt + gl) * P;
+  uint16_t *lo = hi + (int64_t)gpt * P;
+  for (int o = lane * 8; o < P; o += 256) {
+    *reinterpret_cast<uint4 *>(hi + o) = *reinterpret_cast<const uint4 *>(gs + o);
+    *reinterpret_cast<uint4 *>(lo + o) = *reinterpret_cast<const uint4 *>(gs + P + o);
+  }
+}
+
+// One warp per group of 8 query rows: the rows' normalised hot values split
+// into fp16 hi (K columns [0, Hp)) and lo (columns [Hp, 2 Hp)), zero
+// elsewhere, and the cold nonzeros in CSR order.  Checks that the inverse
+// norms are the rows' own (every |x| <= 1 + 2^-10, sum x^2 <= 1 + 2^-6).
+__global__ void __launch_bounds__(kPrepThreads) k_tc_prep_queries(const PrepArgs a) {
+  __shared__ int hkeys[kHotSlots];
+  __shared__ uint8_t hvals[kHotSlots];
+  __shared__ __align__(16) uint16_t grp[kPrepThreads / 32][8 * 2 * kHotMax];
+  load_hot(a.hot, hkeys, hvals);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+  const int Hp = a.Hp, G = 16 * Hp;  // halves per group
+  uint16_t *gs = grp[warp];
+  bool bad = false;
+  for (int64_t g = (int64_t)blockIdx.x * (kPrepThreads / 32) + warp; g < a.n_groups;
+       g += (int64_t)gridDim.x * (kPrepThreads / 32)) {
+    for (int o = lane * 8; o < G; o += 256) *reinterpret_cast<uint4 *>(gs + o) = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    for (int rr = 0; rr < 8; ++rr) {
+      const int64_t r = g * 8 + rr;
+      if (r >= a.n_rows) break;
+      const int64_t b = a.indptr[r], e = a.indptr[r + 1];
+      const float iv = a.inv[r];
+      float ss = 0.f;
+      int nc = 0;
+      for (int64_t p0 = b; p0 < e; p0 += 32) {
+        const int64_t p = p0 + lane;
+        const bool have = p < e;
+        int32_t k = -1;
+        float x = 0.f;
+        int h = -1;
+        if (have) {
+          k = __ldg(a.idx + p);
+          x = __ldg(a.val + p) * iv;
+          ss = fmaf(x, x, ss);
+          bad |= !(fabsf(x) <= kMaxNormalised);
+          h = find_hot(hkeys, hvals, k);
+          if (h >= 0) put_split(gs, rr, h, Hp, x);
+        }
+        const bool cold = have && h < 0;
+        const unsigned m = __ballot_sync(0xffffffffu, cold);
+        if (cold) a.qcold[b + nc + __popc(m & lt)] = make_int2(k, __float_as_int(x));
+        nc += __popc(m);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      bad |= !(ss <= kMaxSquareSum);
+      if (lane == 0) a.qcold_n[r] = nc;
+    }
+    __syncwarp();
+    store_group(a.op, gs, g, a.gpt, Hp, lane);
+    __syncwarp();
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) flag(a.status, DEV_RANGE);
+}
+
+// The item operand of a chunk from its hot slab: one warp per group of 8
+// items, every K column written (zeros past the chunk).  Checks the inverse
+// norms against the items' sums of squares.
+__global__ void __launch_bounds__(kPrepThreads) k_tc_prep_items(const PrepArgs a) {
+  __shared__ __align__(16) uint16_t grp[kPrepThreads / 32][8 * 2 * kHotMax];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int Hp = a.Hp;
+  uint16_t *gs = grp[warp];
+  bool bad = false;
+  for (int64_t g = (int64_t)blockIdx.x * (kPrepThreads / 32) + warp; g < a.n_groups;
+       g += (int64_t)gridDim.x * (kPrepThreads / 32)) {
+    for (int rr = 0; rr < 8; ++rr) {
+      const int64_t r = g * 8 + rr;
+      const bool in = r < a.n_rows;
+      const float iv = in ? __ldg(a.inv + r) : 0.f;
+      if (in && lane == 0) bad |= !(__ldg(a.sq + r) * iv * iv <= kMaxSquareSum);
+      for (int h = lane; h < Hp; h += 32) {
+        const float v = (in && h < kHotMax) ? __ldg(a.slab + r * kHotMax + h) : 0.f;
+        const float x = v * iv;
+        bad |= !(fabsf(x) <= kMaxNormalised);
+        put_split(gs, rr, h, Hp, x);
+      }
+    }
+    __syncwarp();
+    store_group(a.op, gs, g, a.gpt, Hp, lane);
+    __syncwarp();
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) flag(a.status, DEV_RANGE);
+}
+
+// Normalised copy of a chunk's posting entries: {item, value * inv_i[item]}.
+__global__ void __launch_bounds__(256)
+    k_tc_norm_lists(const int32_t *__restrict__ col_ptr, int32_t dim, int64_t capacity,
+                    const uint16_t *__restrict__ post_item, const float *__restrict__ post_val,
+                    const float *__restrict__ inv_i, int2 *__restrict__ post_hat) {
+  const int64_t p0 = __ldg(col_ptr), p1 = min((int64_t)__ldg(col_ptr + dim), capacity);
+  for (int64_t p = p0 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < p1;
+       p += (int64_t)gridDim.x * blockDim.x) {
+    const int it = post_item[p];
+    post_hat[p] = make_int2(it, __float_as_int(post_val[p] * __ldg(inv_i + it)));
+  }
+}
+
+// ---------------------------------------------------------------- records
+struct RecArgs {
+  const int64_t *q_indptr;
+  const int2 *qcold;
+  const int32_t *qcold_n;
+  int64_t n_q;
+  const int32_t *col_ptr;  // the chunk's [dim + 1]
+  const int2 *post_hat;
+  int32_t n_cb;            // column blocks of the chunk
+  int32_t bucket_cap;      // records a bucket holds
+  int2 *rec;               // [quarter][column block][bucket_cap]: {position in the 32 x 32
+                           // swizzled staging tile, fixed-point product}
+  int32_t *rec_n;          // [quarter][column block]: records in the bucket, -1 if they did not fit
+  int32_t *status;
+};
+
+// Calls f(item, product) for every cold product of query row r with the
+// chunk: one warp takes the row's cold entries 32 at a time, and their
+// posting lists, laid end to end, 32 entries at a time (lane -> list by a
+// binary search over the lists' running lengths).
+template <typename F>
+__device__ __forceinline__ void walk_row(const RecArgs &a, int64_t r, int lane, int4 *slots, F f) {
+  const int64_t qb = a.q_indptr[r];
+  const int cn = a.qcold_n[r];
+  const unsigned lt = (1u << lane) - 1u;
+  for (int b0 = 0; b0 < cn; b0 += 32) {
+    int s = 0, len = 0;
+    float qv = 0.f;
+    if (b0 + lane < cn) {
+      const int2 e = __ldg(a.qcold + qb + b0 + lane);
+      qv = __int_as_float(e.y);
+      s = __ldg(a.col_ptr + e.x);
+      len = __ldg(a.col_ptr + e.x + 1) - s;
+    }
+    // The non-empty lists move to the first lanes, in order.
+    const unsigned nz = __ballot_sync(0xffffffffu, len > 0);
+    if (len > 0) slots[__popc(nz & lt)] = make_int4(s, len, __float_as_int(qv), 0);
+    __syncwarp();
+    if (lane < __popc(nz)) {
+      const int4 v = slots[lane];
+      s = v.x;
+      len = v.y;
+      qv = __int_as_float(v.z);
+    } else {
+      s = 0;
+      len = 0;
+      qv = 0.f;
+    }
+    __syncwarp();
+    const int incl = warp_incl_scan(len, lane);
+    const int excl = incl - len;
+    const int L = __shfl_sync(0xffffffffu, incl, 31);
+    // Lists that start inside a window of 32 entries set their start bit;
+    // a lane's list is the last one starting at or before it.
+    const unsigned lt_eq = (2u << lane) - 1u;
+    for (int f0 = 0; f0 < L; f0 += 32 * kWalkUnroll) {
+      int pos[kWalkUnroll];
+      float pq[kWalkUnroll];
+      bool ok[kWalkUnroll];
+#pragma unroll
+      for (int u = 0; u < kWalkUnroll; ++u) {
+        const int w0 = f0 + 32 * u, fi = w0 + lane;
+        const unsigned before = __ballot_sync(0xffffffffu, incl <= w0);  // lists ending at or before w0
+        const bool starts = len > 0 && excl >= w0 && excl < w0 + 32;
+        const unsigned m = __reduce_or_sync(0xffffffffu, starts ? (1u << ((excl - w0) & 31)) : 0u);
+        const int first = __popc(before);  // the list holding entry w0 (if any entry is left)
+        const int starts_before = __popc(m & lt_eq);
+        // If no list starts at w0 itself, entry w0 continues list `first`.
+        const int j = first + starts_before - ((m & 1u) ? 1 : 0);
+        const int jj = j < 31 ? j : 31;
+        const int sj = __shfl_sync(0xffffffffu, s, jj);
+        const int ej = __shfl_sync(0xffffffffu, excl, jj);
+        pq[u] = __shfl_sync(0xffffffffu, qv, jj);
+        ok[u] = fi < L;
+        pos[u] = sj + (fi - ej);
+      }
+      int2 ph[kWalkUnroll];
+#pragma unroll
+      for (int u = 0; u < kWalkUnroll; ++u) {
+        ph[u] = make_int2(0, 0);
+        if (ok[u]) ph[u] = ld_keep_int2(a.post_hat + pos[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < kWalkUnroll; ++u)
+        if (ok[u]) f(ph[u].x, cold_fix(pq[u], __int_as_float(ph[u].y)));
+    }
+  }
+}
+
+// One block per 32 query rows (one warp per row): every cold product of
+// the rows with the chunk becomes a record in the bucket of its 32-item
+// column block, in a slot taken from the block's own counter (the order
+// inside a bucket does not matter: the epilogue sums integers).  A bucket
+// that fills up is marked (count -1); the scorer then takes that block's
+// cold products straight from the lists.
+__global__ void __launch_bounds__(kRThreads, 2) k_tc_records(const RecArgs a) {
+  extern __shared__ int rsm[];
+  int *cnt = rsm;  // [n_cb]
+  __shared__ int4 slots_all[kRThreads / 32][32];
+  int4 *slots = slots_all[threadIdx.x >> 5];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t Q = blockIdx.x;
+  const int64_t row0 = Q * 32;
+  const int nrows = (int)(a.n_q - row0 < 32 ? a.n_q - row0 : 32);
+  const int ncb = a.n_cb, cap = a.bucket_cap;
+  for (int c = tid; c < ncb; c += kRThreads) cnt[c] = 0;
+  __syncthreads();
+  int2 *rq = a.rec + Q * ncb * (int64_t)cap;
+  for (int rl = warp; rl < nrows; rl += kRThreads / 32)
+    walk_row(a, row0 + rl, lane, slots, [&](int item, int p) {
+      const int cb = item >> 5;
+      const int slot = atomicAdd(&cnt[cb], 1);
+      if (slot < cap) rq[(int64_t)cb * cap + slot] = make_int2(stg_index(rl, item & 31), p);
+    });
+  __syncthreads();
+  for (int c = tid; c < ncb; c += kRThreads) a.rec_n[Q * ncb + c] = cnt[c] <= cap ? cnt[c] : -1;
+}
+
+// ---------------------------------------------------------------- scorer
+struct ScoreArgs {
+  const uint16_t *A;       // query operand tiles
+  const uint16_t *B;       // item operand tiles
+  const int2 *rec;
+  const int32_t *rec_n;
+  // For buckets that did not fit: the queries' cold entries and the chunk's
+  // normalised lists.
+  const int64_t *q_indptr;
+  const int2 *qcold;
+  const int32_t *qcold_n;
+  const int32_t *col_ptr;
+  const int2 *post_hat;
+  int64_t n_quarters;
+  int32_t n_cb;
+  int32_t bucket_cap;
+  float *out;
+  int64_t ld_out;
+  int64_t n_q;
+  int32_t n_items;
+  int64_t n_qtiles;
+  int64_t n_units;         // item tiles x query tiles
+  int32_t Hp;
+  int32_t vec_ok;          // 16-byte aligned output rows: vector stores
+  int32_t *status;
+};
+
+// Bytes of the scorer's dynamic shared memory for Hp hot columns: the item
+// tile (hi, lo: 1024 Hp), the query tile's lo and hi parts (256 Hp each,
+// separate so one can load while the other is read), the epilogue staging.
+size_t score_smem_bytes(int Hp) { return (size_t)1536 * Hp + kStgBytes; }
+
+// Ties registers just loaded from tensor memory to the wait that completes
+// the load, so that no use of them is scheduled before it.
+__device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                 "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                 "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
+__global__ void __launch_bounds__(kSThreads, 1)
+    k_tc_score(const ScoreArgs a) {
+  extern __shared__ __align__(1024) unsigned char sm[];
+  __shared__ __align__(8) uint64_t bars[10];
+  __shared__ uint32_t tmem_slot;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Hp = a.Hp;
+  const uint32_t bytesB = 1024u * (uint32_t)Hp, bytesApart = 256u * (uint32_t)Hp;
+  unsigned char *sB = sm;                          // hi part, then lo part
+  unsigned char *sAlo = sm + bytesB;
+  unsigned char *sAhi = sAlo + bytesApart;
+  int *stg_all = reinterpret_cast<int *>(
+      (reinterpret_cast<uintptr_t>(sAhi + bytesApart) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t b_full = smem_u32(&bars[0]), b_free = smem_u32(&bars[1]);
+  const uint32_t lo_full = smem_u32(&bars[2]), lo_free = smem_u32(&bars[3]);
+  const uint32_t hi_full = smem_u32(&bars[4]), hi_free = smem_u32(&bars[5]);
+  // bars[6..7]: accumulator b written (MMA commit); bars[8..9]: accumulator b
+  // read out (one arrival per epilogue warp).
+  const uint32_t acc_full0 = smem_u32(&bars[6]), acc_full1 = smem_u32(&bars[7]);
+  const uint32_t acc_free0 = smem_u32(&bars[8]), acc_free1 = smem_u32(&bars[9]);
+  if (tid == 0) {
+    for (int i = 0; i < 8; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    mbar_init(acc_free0, kEpiWarps);
+    mbar_init(acc_free1, kEpiWarps);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  const int64_t u0 = (int64_t)blockIdx.x * a.n_units / gridDim.x;
+  const int64_t u1 = (int64_t)(blockIdx.x + 1) * a.n_units / gridDim.x;
+  const int64_t nj = u1 - u0;
+
+  if (warp == 0) {
+    // ---- producer: the item tile when it changes, then per unit the query
+    // tile's lo part and hi part, each once the MMAs have released it.
+    if (lane == 0) {
+      int64_t prev_t = -1;
+      int nb = 0;
+      bool ok = true;
+      for (int64_t j = 0; j < nj && ok; ++j) {
+        const int64_t u = u0 + j, t = u / a.n_qtiles, g = u % a.n_qtiles;
+        if (t != prev_t) {
+          if (nb > 0) ok = mbar_wait(b_free, (uint32_t)((nb - 1) & 1), a.status);
+          if (!ok) break;
+          mbar_expect_tx(b_full, bytesB);
+          bulk_g2s(smem_u32(sB), a.B + (size_t)t * (bytesB / 2), bytesB, b_full);
+          ++nb;
+          prev_t = t;
+        }
+        const uint16_t *At = a.A + (size_t)g * (bytesApart);  // tile: hi part, lo part (halves)
+        if (j > 0) ok = mbar_wait(lo_free, (uint32_t)((j - 1) & 1), a.status);
+        if (!ok) break;
+        mbar_expect_tx(lo_full, bytesApart);
+        bulk_g2s(smem_u32(sAlo), At + bytesApart / 2, bytesApart, lo_full);
+        if (j > 0) ok = mbar_wait(hi_free, (uint32_t)((j - 1) & 1), a.status);
+        if (!ok) break;
+        mbar_expect_tx(hi_full, bytesApart);
+        bulk_g2s(smem_u32(sAhi), At, bytesApart, hi_full);
+      }
+      // Copies still in flight land before the block exits.
+      if (nj > 0) {
+        mbar_wait(lo_full, (uint32_t)((nj - 1) & 1), a.status);
+        mbar_wait(hi_full, (uint32_t)((nj - 1) & 1), a.status);
+      }
+      if (nb > 0) mbar_wait(b_full, (uint32_t)((nb - 1) & 1), a.status);
+    }
+  } else if (warp == 1) {
+    // ---- MMA issue: lo_q x hi_v (as soon as the lo part is in), then
+    // hi_q x lo_v and hi_q x hi_v.
+    if (lane == 0) {
+      const uint32_t idesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
+      const uint32_t sbo = 16u * (uint32_t)Hp, lbo = 128u;
+      const uint32_t bhi = smem_u32(sB), blo = bhi + bytesB / 2;
+      const uint32_t alo = smem_u32(sAlo), ahi = smem_u32(sAhi);
+      int64_t prev_t = -1;
+      int nb = 0;
+      bool ok = true;
+      for (int64_t j = 0; j < nj && ok; ++j) {
+        const int64_t t = (u0 + j) / a.n_qtiles;
+        if (t != prev_t) {
+          if (prev_t >= 0) mma_commit(b_free);  // the previous item tile is no longer read
+          ok = mbar_wait(b_full, (uint32_t)(nb & 1), a.status);
+          ++nb;
+          prev_t = t;
+        }
+        const int b = (int)(j & 1);
+        if (ok && j >= 2) ok = mbar_wait(b ? acc_free1 : acc_free0, (uint32_t)(((j - 2) >> 1) & 1), a.status);
+        if (ok) ok = mbar_wait(lo_full, (uint32_t)(j & 1), a.status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(b * kN);
+        for (int k = 0; k < Hp; k += 16)
+          mma_f16(d, smem_desc(alo + (uint32_t)(k / 8) * 128u, lbo, sbo),
+                  smem_desc(bhi + (uint32_t)(k / 8) * 128u, lbo, sbo), idesc, k > 0 ? 1u : 0u);
+        mma_commit(lo_free);
+        if (!mbar_wait(hi_full, (uint32_t)(j & 1), a.status)) break;
+        tc_fence_after();
+        for (int k = 0; k < Hp; k += 16)
+          mma_f16(d, smem_desc(ahi + (uint32_t)(k / 8) * 128u, lbo, sbo),
+                  smem_desc(blo + (uint32_t)(k / 8) * 128u, lbo, sbo), idesc, 1u);
+        for (int k = 0; k < Hp; k += 16)
+          mma_f16(d, smem_desc(ahi + (uint32_t)(k / 8) * 128u, lbo, sbo),
+                  smem_desc(bhi + (uint32_t)(k / 8) * 128u, lbo, sbo), idesc, 1u);
+        mma_commit(hi_free);
+        mma_commit(b ? acc_full1 : acc_full0);
+      }
+      // Every MMA has completed before the accumulators are freed.
+      if (nj > 0) mbar_wait((nj - 1) & 1 ? acc_full1 : acc_full0, (uint32_t)(((nj - 1) >> 1) & 1), a.status);
+    }
+  } else {
+    // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31, i.e. the
+    // unit's query rows 32 (w % 4) .. + 31, in 8 blocks of 32 columns.  The
+    // records of a block are fetched two blocks ahead (across units), the
+    // next block's accumulator columns one block ahead.
+    const int qd = warp & 3;
+    const int half = (warp - 2) >> 2;                 // 0: even column blocks, 1: odd ones
+    int *stg = stg_all + (warp - 2) * kStgInts;       // this warp's staging tile (swizzled)
+    const bool vec = a.vec_ok != 0;
+    const int sw = lane & 7;
+    int *row = stg + lane * 32;
+    // Lanes 0..7: record counts of the unit's 8 column blocks (0 past the
+    // chunk or the queries).
+    auto load_bnd = [&](int64_t u) -> int {
+      const int64_t t = u / a.n_qtiles, g = u % a.n_qtiles;
+      const int64_t Q = g * 4 + qd;
+      const int cb = (int)t * 8 + lane;
+      int v = 0;
+      if (Q < a.n_quarters && lane < 8 && cb < a.n_cb) v = ld_keep_int(a.rec_n + Q * a.n_cb + cb);
+      return v;
+    };
+    // Bucket of column block 0 of unit u (block c follows at c * bucket_cap).
+    auto bucket0 = [&](int64_t u) -> const int2 * {
+      const int64_t t = u / a.n_qtiles, g = u % a.n_qtiles;
+      const int64_t Q = g * 4 + qd;
+      return a.rec + (Q * a.n_cb + t * 8) * (int64_t)a.bucket_cap;
+    };
+    const int bcap = a.bucket_cap;
+    auto fetch = [&](int bnd, const int2 *bk, int c, int2(&dst)[kRecPerLane]) {
+      const int n = __shfl_sync(0xffffffffu, bnd, c);
+#pragma unroll
+      for (int m = 0; m < kRecPerLane; ++m) {
+        const int p = 32 * m + lane;
+        dst[m] = make_int2(0, 0);
+        if (p < n) dst[m] = ld_keep_int2(bk + p);
+      }
+    };
+    // This warp's blocks c = 2 i + half, i = 0..3; the records of its i-th
+    // block live in register slot i, fetched two of its blocks ahead
+    // (across units), so no copy waits on a load in flight.
+    constexpr int kMine = kN / kColBlock / 2;
+    int bnd = nj > 0 ? load_bnd(u0) : 0, bnd_n = 0;
+    int2 R[kMine][kRecPerLane];
+    const int2 *bk = nj > 0 ? bucket0(u0) : a.rec, *bk_n = bk;
+    if (nj > 0) {
+      fetch(bnd, bk + half * bcap, half, R[0]);
+      fetch(bnd, bk + (2 + half) * bcap, 2 + half, R[1]);
+    }
+    for (int64_t j = 0; j < nj; ++j) {
+      const int64_t u = u0 + j, t = u / a.n_qtiles, g = u % a.n_qtiles;
+      const int b = (int)(j & 1);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(b ? acc_full1 : acc_full0, (uint32_t)((j >> 1) & 1), a.status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      __syncwarp();
+      if (!ok) break;
+      tc_fence_after();
+      if (j + 1 < nj) {
+        bnd_n = load_bnd(u + 1);
+        bk_n = bucket0(u + 1);
+      }
+      const int64_t qrow0 = (g * 4 + qd) * 32;
+      const int item0 = (int)t * kN;
+      const uint32_t tbase = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(b * kN);
+#pragma unroll
+      for (int i = 0; i < kMine; ++i) {
+        const int c = 2 * i + half;
+        uint32_t rc[32];
+        tmem_ld32(tbase + (uint32_t)(c * kColBlock), rc);
+        if (i + 2 < kMine) fetch(bnd, bk + (c + 4) * bcap, c + 4, R[(i + 2) & 3]);
+        else if (j + 1 < nj) fetch(bnd_n, bk_n + (c + 4 - 2 * kMine) * bcap, c + 4 - 2 * kMine, R[(i + 2) & 3]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) *reinterpret_cast<int4 *>(row + 4 * (k ^ sw)) = make_int4(0, 0, 0, 0);
+        __syncwarp();
+#pragma unroll
+        for (int m = 0; m < kRecPerLane; ++m)
+          if (R[i & 3][m].y != 0) atomicAdd(stg + R[i & 3][m].x, R[i & 3][m].y);
+        {
+          const int n = __shfl_sync(0xffffffffu, bnd, c);
+          const int2 *bc = bk + c * bcap;
+          for (int p = 32 * kRecPerLane + lane; p < n; p += 32) {
+            const int2 rr = __ldg(bc + p);
+            atomicAdd(stg + rr.x, rr.y);
+          }
+          if (n < 0) {
+            // The bucket did not fit: each lane walks its row's cold lists
+            // and keeps the items of this block (rare; exact, same sums).
+            const int64_t q = qrow0 + lane;
+            const int lo = (int)t * kN + c * kColBlock;
+            if (q < a.n_q) {
+              const int64_t qb = a.q_indptr[q];
+              const int cn = a.qcold_n[q];
+              for (int e = 0; e < cn; ++e) {
+                const int2 qe = __ldg(a.qcold + qb + e);
+                const float qv = __int_as_float(qe.y);
+                const int p1 = __ldg(a.col_ptr + qe.x + 1);
+                for (int p = __ldg(a.col_ptr + qe.x); p < p1; ++p) {
+                  const int2 ph = __ldg(a.post_hat + p);
+                  const int d = ph.x - lo;
+                  if ((unsigned)d < (unsigned)kColBlock)
+                    atomicAdd(stg + stg_index(lane, d), cold_fix(qv, __int_as_float(ph.y)));
+                }
+              }
+            }
+          }
+        }
+        __syncwarp();
+        tmem_wait_ld();
+        tmem_regs_ready(rc);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          int *chunk = row + 4 * (k ^ sw);
+          const int4 ci = *reinterpret_cast<const int4 *>(chunk);
+          float4 o;
+          o.x = fmaf((float)ci.x, kFixInv, __uint_as_float(rc[4 * k + 0]));
+          o.y = fmaf((float)ci.y, kFixInv, __uint_as_float(rc[4 * k + 1]));
+          o.z = fmaf((float)ci.z, kFixInv, __uint_as_float(rc[4 * k + 2]));
+          o.w = fmaf((float)ci.w, kFixInv, __uint_as_float(rc[4 * k + 3]));
+          *reinterpret_cast<float4 *>(chunk) = o;
+        }
+        __syncwarp();
+        // Row-contiguous stores: lane l writes items 4 (l % 8) .. + 3 of
+        // rows 4 s + l / 8 (chunk l % 8 of the row, found through the swizzle).
+        const int it = item0 + c * kColBlock + 4 * (lane & 7);
+#pragma unroll
+        for (int sidx = 0; sidx < 8; ++sidx) {
+          const int rl = 4 * sidx + (lane >> 3);
+          const float4 v = *reinterpret_cast<const float4 *>(stg + rl * 32 + 4 * ((lane & 7) ^ (rl & 7)));
+          const int64_t q = qrow0 + rl;
+          if (q < a.n_q && it < a.n_items) {
+            float *dst = a.out + q * a.ld_out + it;
+            if (vec && it + 4 <= a.n_items) {
+              __stcs(reinterpret_cast<float4 *>(dst), v);
+            } else {
+              const float vv[4] = {v.x, v.y, v.z, v.w};
+              for (int e2 = 0; e2 < 4 && it + e2 < a.n_items; ++e2) dst[e2] = vv[e2];
+            }
+          }
+        }
+        __syncwarp();
+      }
+      bnd = bnd_n;
+      bk = bk_n;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b ? acc_free1 : acc_free0);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
+  }
+}
+
+// Top-k on the tensor path: offers one row's scores of one 256-item slice
+// of a dense score matrix (the chunk's scores, written by the scorer).
+__global__ void __launch_bounds__(256)
+    k_tc_topk_offer(const float *__restrict__ scores, int64_t n_q, int32_t n_items, ss_topk t,
+                    int32_t *status) {
+  using namespace topk_dev;
+  const int lane = threadIdx.x & 31;
+  const int n_sl = (n_items + kN - 1) / kN;
+  const int64_t n_jobs = n_q * n_sl;
+  for (int64_t jb = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); jb < n_jobs;
+       jb += (int64_t)gridDim.x * 8) {
+    const int64_t q = jb / n_sl;
+    const int sl = (int)(jb % n_sl);
+    const float thr = t.best_val[q * t.k + (t.k - 1)];
+    float v[8];
+    int item[8];
+    bool ok[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int it = sl * kN + (j < 4 ? 4 * lane + j : 128 + 4 * lane + (j - 4));
+      ok[j] = it < n_items;
+      item[j] = it;
+      v[j] = ok[j] ? scores[q * n_items + it] : -INFINITY;
+    }
+    topk_offer(t, q, thr, v, item, ok, lane, status);
+  }
+}
+
+template <typename T>
+cudaError_t grow(T **p, int64_t *cap, int64_t need, cudaStream_t s) {
+  if (need <= *cap) return cudaSuccess;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  cudaFree(*p);
+  *p = nullptr;
+  *cap = 0;
+  const int64_t n = std::max<int64_t>(need, *cap + *cap / 2);
+  e = cudaMalloc(p, sizeof(T) * (size_t)n);
+  if (e != cudaSuccess) return e;
+  *cap = n;
+  return cudaSuccess;
+}
+
+int padded_hot(int H) { return std::max(16, (H + 15) / 16 * 16); }
+
+}  // namespace
+
+cudaError_t launch_tc_hot_select(ss_handle *h, const ss_csr &items, cudaStream_t s, int *queued) {
+  *queued = 0;
+  if (h->tc_hot_src[0] == items.indptr && h->tc_hot_src[1] == items.indices &&
+      h->tc_hot_src[2] == items.values && h->tc_hot_rows == items.n_rows && h->tc_hot_nnz == items.nnz)
+    return cudaSuccess;
+  cudaError_t e = cudaSuccess;
+  if (!h->tc_hot) {
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
+    if ((e = cudaMalloc(&h->tc_hot, sizeof(int32_t) * (1 + kHotMax))) != cudaSuccess) return e;
+    if ((e = cudaMalloc(&h->tc_sel, sizeof(int32_t) * 2 * kSelSlots)) != cudaSuccess) return e;
+    if ((e = cudaMalloc(&h->tc_stats, sizeof(float) * 2)) != cudaSuccess) return e;
+  }
+  const int64_t n = items.n_rows;
+  int64_t n_sample = 0;
+  if (n > 0 && items.nnz > 0) {
+    n_sample = (int64_t)((double)kSampleEntries * (double)n / (double)items.nnz);
+    n_sample = std::max<int64_t>(16, std::min<int64_t>(n, n_sample));
+  }
+  float stats[2] = {0.f, 0.f};
+  if (n_sample == 0) {
+    if ((e = cudaMemsetAsync(h->tc_hot, 0, sizeof(int32_t), s)) != cudaSuccess) return e;
+  } else {
+    if ((e = cudaMemsetAsync(h->tc_sel, 0xFF, sizeof(int32_t) * kSelSlots, s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(h->tc_sel + kSelSlots, 0, sizeof(int32_t) * kSelSlots, s)) != cudaSuccess)
+      return e;
+    const int sms = h->sm_count > 0 ? h->sm_count : 148;
+    k_tc_sel_insert<<<sms * 2, 256, 0, s>>>(items.indptr, items.indices, n, n_sample, h->tc_sel);
+    k_tc_sel_pick<<<1, kSelThreads, 0, s>>>(h->tc_sel, n_sample, h->tc_hot, h->tc_stats);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    *queued = 2;
+    if ((e = cudaMemcpyAsync(stats, h->tc_stats, sizeof(stats), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+      return e;
+  }
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
+  h->tc_est_cold = stats[0];
+  h->tc_H = (int32_t)stats[1];
+  h->tc_hot_src[0] = items.indptr;
+  h->tc_hot_src[1] = items.indices;
+  h->tc_hot_src[2] = items.values;
+  h->tc_hot_rows = items.n_rows;
+  h->tc_hot_nnz = items.nnz;
+  ++h->tc_hot_generation;
+  return cudaSuccess;
+}
+
+cudaError_t launch_build_tc(ss_handle *h, const ss_csr &items, int64_t row_begin, int64_t row_end,
+                            cudaStream_t s, int *queued) {
+  *queued = 0;
+  const int64_t C = h->chunk_rows;
+  const int n_chunks = (int)((row_end - row_begin + C - 1) / C);
+  h->n_views = 0;
+  if (n_chunks < 1 || n_chunks > h->build_batch) return cudaErrorInvalidValue;
+  cudaError_t e = cudaSuccess;
+  if (!h->tc_slab) {
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
+    if ((e = cudaMalloc(&h->tc_slab, sizeof(float) * (size_t)h->build_batch * C * kHotMax)) != cudaSuccess)
+      return e;
+    if ((e = cudaMalloc(&h->tc_sq, sizeof(float) * (size_t)h->build_batch * C)) != cudaSuccess) return e;
+  }
+  const int64_t stride = h->dim + 1;
+  const int64_t n = stride * n_chunks;
+  if ((e = cudaMemsetAsync(h->col_cnt, 0, sizeof(int32_t) * (size_t)n, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(h->tc_slab, 0, sizeof(float) * (size_t)n_chunks * C * kHotMax, s)) != cudaSuccess)
+    return e;
+  const int grid = (h->sm_count > 0 ? h->sm_count : 148) * 8;
+  k_tc_hist<<<grid, 256, 0, s>>>(items.indptr, items.indices, row_begin, row_end, C, n_chunks, h->dim,
+                                 h->tc_hot, h->col_cnt, h->d_status);
+  if ((e = launch_count_scan(h->col_cnt, n, h->scan_part, h->col_ptr, s)) != cudaSuccess) return e;
+  k_tc_scatter<<<grid, 256, 0, s>>>(items.indptr, items.indices, items.values, row_begin, row_end, C,
+                                    h->dim, h->tc_hot, h->col_cnt, h->post_item, h->post_val,
+                                    h->post_cap, h->tc_slab, h->tc_sq, h->d_status);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  *queued = 5;
+  for (int k = 0; k < n_chunks; ++k) {
+    ss_index &ix = h->views[k];
+    ix = ss_index();
+    ix.algo = ALGO_TENSOR;
+    ix.row_begin = row_begin + (int64_t)k * C;
+    ix.row_end = std::min<int64_t>(ix.row_begin + C, row_end);
+    ix.n_items = (int32_t)(ix.row_end - ix.row_begin);
+    ix.dim = h->dim;
+    ix.col_ptr = h->col_ptr + (size_t)k * stride;
+    ix.post_item = h->post_item;
+    ix.post_val = h->post_val;
+    ix.capacity = h->post_cap;
+    ix.hot = h->tc_hot;
+    ix.slab = h->tc_slab + (size_t)k * C * kHotMax;
+    ix.slab_ld = kHotMax;
+    ix.sq = h->tc_sq + (size_t)k * C;
+  }
+  h->n_views = n_chunks;
+  return cudaSuccess;
+}
+
+cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, const ss_index &idx,
+                            const float *inv_i, float *out, int64_t ld_out, cudaStream_t s,
+                            int *queued, const ss_topk *topk) {
+  *queued = 0;
+  if (q.n_rows == 0 || idx.n_items == 0) return cudaSuccess;
+  const int sms = h->sm_count > 0 ? h->sm_count : 148;
+  const int Hp = padded_hot(h->tc_H);
+  const int64_t n_q = q.n_rows;
+  const int64_t n_qtiles = (n_q + kM - 1) / kM;
+  const int32_t n_items = idx.n_items;
+  const int64_t n_tiles = (n_items + kN - 1) / kN;
+  cudaError_t e = cudaSuccess;
+  int nq = 0;
+
+  // Query operand and cold entries, once per query matrix, inverse norms and hot set.
+  if (!(h->tcq_src[0] == q.indptr && h->tcq_src[1] == q.indices && h->tcq_src[2] == q.values &&
+        h->tcq_src[3] == inv_q && h->tcq_rows == q.n_rows && h->tcq_nnz == q.nnz &&
+        h->tcq_generation == h->tc_hot_generation)) {
+    if ((e = grow(&h->tc_A, &h->tc_A_cap, n_qtiles * kM * 2 * Hp, s)) != cudaSuccess) return e;
+    if ((e = grow(&h->tc_qcold, &h->tc_qcold_cap, std::max<int64_t>(1, q.nnz), s)) != cudaSuccess) return e;
+    if ((e = grow(&h->tc_qcold_n, &h->tc_qcold_n_cap, n_q, s)) != cudaSuccess) return e;
+    PrepArgs pa;
+    pa.indptr = q.indptr;
+    pa.idx = q.indices;
+    pa.val = q.values;
+    pa.slab = nullptr;
+    pa.sq = nullptr;
+    pa.n_rows = n_q;
+    pa.n_groups = n_qtiles * (kM / 8);
+    pa.inv = inv_q;
+    pa.hot = idx.hot;
+    pa.Hp = Hp;
+    pa.gpt = kM / 8;
+    pa.op = h->tc_A;
+    pa.qcold = h->tc_qcold;
+    pa.qcold_n = h->tc_qcold_n;
+    pa.status = h->d_status;
+    const int64_t blocks = std::min<int64_t>((pa.n_groups + 7) / 8, (int64_t)sms * 8);
+    k_tc_prep_queries<<<(unsigned)blocks, kPrepThreads, 0, s>>>(pa);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    ++nq;
+    h->tcq_src[0] = q.indptr;
+    h->tcq_src[1] = q.indices;
+    h->tcq_src[2] = q.values;
+    h->tcq_src[3] = inv_q;
+    h->tcq_rows = q.n_rows;
+    h->tcq_nnz = q.nnz;
+    h->tcq_generation = h->tc_hot_generation;
+  }
+
+  // Item operand and the normalised posting entries of this chunk.
+  if ((e = grow(&h->tc_B, &h->tc_B_cap, n_tiles * kN * 2 * Hp, s)) != cudaSuccess) return e;
+  {
+    PrepArgs pa;
+    pa.indptr = nullptr;
+    pa.idx = nullptr;
+    pa.val = nullptr;
+    pa.slab = idx.slab;
+    pa.sq = idx.sq;
+    pa.n_rows = n_items;
+    pa.n_groups = n_tiles * (kN / 8);
+    pa.inv = inv_i;
+    pa.hot = idx.hot;
+    pa.Hp = Hp;
+    pa.gpt = kN / 8;
+    pa.op = h->tc_B;
+    pa.qcold = nullptr;
+    pa.qcold_n = nullptr;
+    pa.status = h->d_status;
+    const int64_t blocks = std::min<int64_t>((pa.n_groups + 7) / 8, (int64_t)sms * 8);
+    k_tc_prep_items<<<(unsigned)blocks, kPrepThreads, 0, s>>>(pa);
+    k_tc_norm_lists<<<sms * 4, 256, 0, s>>>(idx.col_ptr, (int32_t)idx.dim, idx.capacity, idx.post_item,
+                                           idx.post_val, inv_i, h->post_hat);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    nq += 2;
+  }
+
+  // Cold records: a bucket per (32 query rows, 32 items) holding 3 times
+  // the sample's estimate of its records (at least 64, at most 1024); the
+  // scorer computes the blocks of fuller buckets from the lists.
+  const int64_t n_quarters = (n_q + 31) / 32;
+  const int32_t n_cb = (n_items + kColBlock - 1) / kColBlock;
+  const double est = std::max(0.0, h->tc_est_cold);
+  const int32_t cap = (int32_t)std::min<double>(1024.0, std::max<double>(64.0, std::ceil((3.0 * est * 1024.0 + 64.0) / 32.0) * 32.0));
+  if ((e = grow(&h->tc_rec_off, &h->tc_rec_off_cap, n_quarters * n_cb, s)) != cudaSuccess) return e;
+  if ((e = grow(&h->tc_rec, &h->tc_rec_cap, n_quarters * n_cb * (int64_t)cap, s)) != cudaSuccess) return e;
+  {
+    RecArgs ra;
+    ra.q_indptr = q.indptr;
+    ra.qcold = h->tc_qcold;
+    ra.qcold_n = h->tc_qcold_n;
+    ra.n_q = n_q;
+    ra.col_ptr = idx.col_ptr;
+    ra.post_hat = h->post_hat;
+    ra.n_cb = n_cb;
+    ra.bucket_cap = cap;
+    ra.rec = h->tc_rec;
+    ra.rec_n = h->tc_rec_off;
+    ra.status = h->d_status;
+    const size_t smem = sizeof(int) * (size_t)n_cb;
+    k_tc_records<<<(unsigned)n_quarters, kRThreads, smem, s>>>(ra);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    ++nq;
+  }
+
+  // Scores (full chunk, or the dense scratch the top-k offers read).
+  float *dst = out;
+  int64_t ld_dst = ld_out;
+  if (topk && topk->k > 0) {
+    if ((e = grow(&h->hot_scratch, &h->hot_scratch_cap, n_q * (int64_t)n_items, s)) != cudaSuccess) return e;
+    dst = h->hot_scratch;
+    ld_dst = n_items;
+  }
+  {
+    static bool configured = false;
+    const size_t smem = score_smem_bytes(kHotMax);
+    if (!configured) {
+      if ((e = cudaFuncSetAttribute(k_tc_score, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+          cudaSuccess)
+        return e;
+      configured = true;
+    }
+    ScoreArgs sa;
+    sa.A = h->tc_A;
+    sa.B = h->tc_B;
+    sa.rec = h->tc_rec;
+    sa.rec_n = h->tc_rec_off;
+    sa.q_indptr = q.indptr;
+    sa.qcold = h->tc_qcold;
+    sa.qcold_n = h->tc_qcold_n;
+    sa.col_ptr = idx.col_ptr;
+    sa.post_hat = h->post_hat;
+    sa.n_quarters = n_quarters;
+    sa.n_cb = n_cb;
+    sa.bucket_cap = cap;
+    sa.out = dst;
+    sa.ld_out = ld_dst;
+    sa.n_q = n_q;
+    sa.n_items = n_items;
+    sa.n_qtiles = n_qtiles;
+    sa.n_units = n_tiles * n_qtiles;
+    sa.Hp = Hp;
+    sa.vec_ok = ((reinterpret_cast<uintptr_t>(dst) % 16) == 0) && (ld_dst % 4 == 0);
+    sa.status = h->d_status;
+    const int64_t grid = std::min<int64_t>(sms, sa.n_units);
+    k_tc_score<<<(unsigned)grid, kSThreads, score_smem_bytes(Hp), s>>>(sa);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    ++nq;
+  }
+  if (topk && topk->k > 0) {
+    const int64_t jobs = n_q * n_tiles;
+    const int64_t blocks = std::min<int64_t>((jobs + 7) / 8, (int64_t)sms * 16);
+    k_tc_topk_offer<<<(unsigned)blocks, 256, 0, s>>>(dst, n_q, n_items, *topk, h->d_status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    ++nq;
+  }
+  *queued = nq;
+  return cudaSuccess;
+}

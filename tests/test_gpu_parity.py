@@ -35,7 +35,7 @@ def _dev(sec, batch):
     return sec.DeviceCsr.from_host(batch, "cuda")
 
 
-ALGOS = ["hybrid", "posting"]
+ALGOS = ["hybrid", "posting", "tensor"]
 
 
 def _gpu_cosine(sec, Q, I, chunk_rows=8192, algorithm="hybrid"):
@@ -478,6 +478,69 @@ def test_posting_rejects_inverse_norms_of_other_rows(sec):
         S = h.score_all(x, inv, x, inv).cpu().numpy()
         h.check_device()
     assert _max_err(S, oracle.cosine(X, X)) <= TOL
+
+
+def test_tensor_rejects_inverse_norms_of_other_rows(sec):
+    """The tensor path splits normalised values (|x| <= 1) into fp16 parts and
+    sums cold products in fixed point: inverse norms that are not the rows'
+    own are reported, and the handle stays usable."""
+    from sparse_embedding_exact_gb300 import SparseCosError, _abi
+
+    X = _rows_csr([([1, 4], [30.0, 40.0]), ([4, 9], [2.0, 1.0])], 16)
+    with sec.SparseCosine(16, algorithm="tensor") as h:
+        x = _dev(sec, X)
+        ones = torch.ones(2, dtype=torch.float32, device="cuda")
+        h.score_all(x, ones, x, ones)
+        with pytest.raises(SparseCosError) as e:
+            h.check_device()
+        assert e.value.status == _abi.SS_ERR_DEVICE_CHECK
+        inv = h.row_norms(x)
+        S = h.score_all(x, inv, x, inv).cpu().numpy()
+        h.check_device()
+    assert _max_err(S, oracle.cosine(X, X)) <= TOL
+
+
+@pytest.mark.parametrize("name,n_q,n_i,chunk", [
+    ("d1.2m_q5k_i200k", 300, 9000, 8192),   # 3 query tiles (the last ragged), 2 chunks (the last ragged)
+    ("d1.2m_q20k_i1m_heavy", 150, 5000, 2048),
+    ("d65k_q1k_i10k", 257, 3000, 1000),
+])
+def test_tensor_path_spans_tiles_and_ragged_tails(sec, name, n_q, n_i, chunk):
+    """Several 128 x 256 tile pairs per chunk, ragged in both directions: every
+    entry within the bar; the index reports the tensor path and its hot set."""
+    cfg = CONFIGS[name]
+    Q, I = generate_rows(cfg, 0, 0, n_q), generate_rows(cfg, 1, 0, n_i)
+    with sec.SparseCosine(cfg.dim, chunk_rows=chunk, algorithm="tensor") as h:
+        q, i = _dev(sec, Q), _dev(sec, I)
+        inv_q, inv_i = h.row_norms(q), h.row_norms(i)
+        st = h.index_stats(h.build_item_index(i, 0, min(chunk, n_i)))
+        S = h.score_all(q, inv_q, i, inv_i)
+        h.check_device()
+        got = S.cpu().numpy()
+    assert st["algorithm"] == 2 and 0 < st["hot_dims"] <= 128
+    assert _max_err(got, oracle.cosine(Q, I)) <= TOL
+
+
+def test_tensor_hot_part_alone_and_cold_part_alone(sec):
+    """Rows whose support lies wholly in the hot set (no cold records) and rows
+    with no hot dimension at all (only cold records), against the oracle."""
+    rng = np.random.default_rng(5)
+    d = 5000
+    rows = []
+    for r in range(300):
+        if r % 3 == 0:   # the first 40 dims: frequent, hence hot
+            idx = np.sort(rng.choice(40, size=12, replace=False))
+        elif r % 3 == 1:  # rare dims only
+            idx = np.sort(rng.choice(np.arange(1000, d), size=15, replace=False))
+        else:
+            idx = np.sort(np.concatenate([rng.choice(40, size=5, replace=False),
+                                          rng.choice(np.arange(1000, d), size=8, replace=False)]))
+        rows.append((idx, rng.standard_normal(idx.size).astype(np.float32)))
+    X = _rows_csr(rows, d)
+    got = _gpu_cosine(sec, X, X, chunk_rows=256, algorithm="tensor")
+    ref = oracle.cosine(X, X)
+    assert _max_err(got, ref) <= TOL
+    assert np.abs(np.diag(got) - 1.0).max() <= TOL
 
 
 @pytest.mark.parametrize("name,n_i,chunk", [("d65k_q1k_i10k", 10000, 10000),

@@ -63,7 +63,7 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("algo", ["hybrid", "posting"])
+@pytest.mark.parametrize("algo", ["hybrid", "posting", "tensor"])
 @pytest.mark.parametrize("name,n_q,n_i,k,chunk", CASES)
 def test_topk_is_the_top_of_the_full_matrix(sec, name, n_q, n_i, k, chunk, algo):
     cfg = CONFIGS[name]
@@ -79,7 +79,7 @@ def test_topk_is_the_top_of_the_full_matrix(sec, name, n_q, n_i, k, chunk, algo)
     assert (picked >= kth[:, None] - 2 * TOL).all()
 
 
-@pytest.mark.parametrize("algo", ["hybrid", "posting"])
+@pytest.mark.parametrize("algo", ["hybrid", "posting", "tensor"])
 def test_topk_short_rows_ties_and_padding(sec, algo):
     # 3 query rows (one all zero: every score 0, ties broken by item number),
     # 5 items, k = 8 > 5: the last 3 slots stay (-inf, -1).
@@ -95,7 +95,7 @@ def test_topk_short_rows_ties_and_padding(sec, algo):
     assert np.array_equal(items[1, :5], np.arange(5)) and (vals[1, :5] == 0).all()
 
 
-@pytest.mark.parametrize("algo", ["hybrid", "posting"])
+@pytest.mark.parametrize("algo", ["hybrid", "posting", "tensor"])
 def test_topk_chunks_in_any_order_match_topk_all(sec, algo):
     cfg = CONFIGS["d65k_q1k_i10k"]
     Q, I = generate_rows(cfg, 0, 0, 40), generate_rows(cfg, 1, 0, 5000)
