@@ -371,6 +371,18 @@ ss_status ss_cosine_chunk_noalloc(const ss_csr *queries, const ss_csr *items, in
  * queues kernels adds the number it queued).  Host-side count; no sync. */
 uint64_t ss_kernel_launches(const ss_handle *h);
 
+/* Timing of the scoring kernel itself (k_tc_score, k_score_tiles or
+ * k_score_lists, whichever the index uses).  While on, every scoring call
+ * records a CUDA event just before and just after its scoring kernel, on
+ * the caller's stream; the other kernels of the call (operand preparation,
+ * cold records, query preparation) fall outside the pair.  Turning it on or
+ * off forgets the pairs recorded so far.  No synchronisation. */
+ss_status ss_profile_scorer(ss_handle *h, int32_t on);
+
+/* Sum of the recorded pairs' elapsed times in milliseconds and their count,
+ * then forgets them.  Synchronises on the last recorded event. */
+ss_status ss_scorer_time(ss_handle *h, double *total_ms, int64_t *launches);
+
 /* Frees the handle and its device workspace (synchronises the device). */
 ss_status ss_destroy(ss_handle *h);
 

@@ -289,6 +289,19 @@ class SparseCosine:
         self._check(self._lib.ss_validate_csr(self._h, ctypes.byref(c), _stream_ptr(stream)),
                     "ss_validate_csr")
 
+    def profile_scorer(self, on: bool = True) -> None:
+        """Record CUDA events around each launch of the scoring kernel
+        (not the call's other kernels) on the caller's stream."""
+        self._check(self._lib.ss_profile_scorer(self._h, 1 if on else 0), "ss_profile_scorer")
+
+    def scorer_time(self):
+        """(total milliseconds, launches) of the scoring-kernel launches
+        recorded since profiling was turned on or last read; synchronises."""
+        ms = ctypes.c_double()
+        n = ctypes.c_int64()
+        self._check(self._lib.ss_scorer_time(self._h, ctypes.byref(ms), ctypes.byref(n)), "ss_scorer_time")
+        return ms.value, n.value
+
     def index_stats(self, index, stream=None) -> dict:
         """Diagnostics of the last built index (synchronises the stream).
         "algorithm" is 0 for item tiles, 1 for posting lists, 2 for the

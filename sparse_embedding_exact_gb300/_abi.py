@@ -70,6 +70,8 @@ SIGNATURES = {
     "ss_index_stats": (_I32, [_P, _P, ctypes.POINTER(ctypes.c_int64), _P]),
     "ss_cosine_chunk_noalloc": (_I32, [_CSR, _CSR, _I64, _I64, _I64, _P, _I64, _P]),
     "ss_kernel_launches": (ctypes.c_uint64, [_P]),
+    "ss_profile_scorer": (_I32, [_P, _I32]),
+    "ss_scorer_time": (_I32, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I64)]),
     "ss_destroy": (_I32, [_P]),
     "ss_status_string": (ctypes.c_char_p, [_I32]),
     "ss_last_error": (ctypes.c_char_p, [_P]),

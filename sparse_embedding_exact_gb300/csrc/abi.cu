@@ -152,6 +152,9 @@ ss_status ensure_capacity(ss_handle *h, int32_t algo, int64_t need) {
 
 void free_workspace(ss_handle *h) {
   free_host_pass(h->host);
+  for (cudaEvent_t e : h->prof_ev) cudaEventDestroy(e);
+  h->prof_ev.clear();
+  h->prof_used = 0;
   cudaFree(h->cand_val);
   cudaFree(h->cand_item);
   cudaFree(h->cand_n);
@@ -318,6 +321,19 @@ bool owns_index(const ss_handle *h, const ss_index *idx) {
 
 }  // namespace
 
+void prof_mark(ss_handle *h, cudaStream_t s) {
+  if (!h->prof_on) return;
+  if (h->prof_used == h->prof_ev.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      h->prof_on = false;
+      return;
+    }
+    h->prof_ev.push_back(e);
+  }
+  cudaEventRecord(h->prof_ev[h->prof_used++], s);
+}
+
 extern "C" {
 
 const char *ss_status_string(ss_status s) {
@@ -338,6 +354,31 @@ const char *ss_status_string(ss_status s) {
 const char *ss_last_error(const ss_handle *h) { return h ? h->last_error.c_str() : ""; }
 
 uint64_t ss_kernel_launches(const ss_handle *h) { return h ? h->launches : 0; }
+
+ss_status ss_profile_scorer(ss_handle *h, int32_t on) {
+  if (!h) return SS_ERR_INVALID_ARG;
+  h->prof_on = on != 0;
+  h->prof_used = 0;
+  return SS_OK;
+}
+
+ss_status ss_scorer_time(ss_handle *h, double *total_ms, int64_t *launches) {
+  if (!h || !total_ms || !launches) return SS_ERR_INVALID_ARG;
+  *total_ms = 0.0;
+  *launches = 0;
+  ss_status st = set_device(h);
+  if (st != SS_OK) return st;
+  const size_t pairs = h->prof_used / 2;
+  if (pairs > 0) SS_CUDA(h, cudaEventSynchronize(h->prof_ev[2 * pairs - 1]));
+  for (size_t k = 0; k < pairs; ++k) {
+    float ms = 0.f;
+    SS_CUDA(h, cudaEventElapsedTime(&ms, h->prof_ev[2 * k], h->prof_ev[2 * k + 1]));
+    *total_ms += ms;
+  }
+  *launches = (int64_t)pairs;
+  h->prof_used = 0;
+  return SS_OK;
+}
 
 ss_status ss_create(ss_handle **out, int device, int64_t dim, int32_t chunk_rows, int32_t flags) {
   if (!out) return SS_ERR_INVALID_ARG;

@@ -1829,8 +1829,10 @@ cudaError_t launch_score_hybrid(ss_handle *h, const ss_csr &queries, const float
   f.status = h->d_status;
   f.topk = topk ? *topk : ss_topk();
   const int grid_f = (int)std::min<int64_t>(f.n_units, sms);
+  prof_mark(h, s);
   if (f.topk.k > 0) k_score_tiles<true><<<grid_f, kFThreads, kFastSmem, s>>>(f);
   else k_score_tiles<false><<<grid_f, kFThreads, kFastSmem, s>>>(f);
+  prof_mark(h, s);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

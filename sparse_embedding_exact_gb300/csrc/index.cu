@@ -103,13 +103,39 @@ __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t *tota
   return r;
 }
 
+// A tile of kScanTile counters is read as kScanItems / 4 slices of
+// kScanThreads int4 vectors: thread t holds counters [4 t, 4 t + 4) of each
+// slice, so every warp access covers 512 contiguous bytes.  Vectors that
+// run past n are read and written element by element.
+__device__ __forceinline__ int4 load4(const int32_t *a, int64_t i, int64_t n) {
+  if (i + 4 <= n) return *reinterpret_cast<const int4 *>(a + i);
+  int4 v = make_int4(0, 0, 0, 0);
+  if (i < n) v.x = a[i];
+  if (i + 1 < n) v.y = a[i + 1];
+  if (i + 2 < n) v.z = a[i + 2];
+  return v;
+}
+__device__ __forceinline__ void store4(int32_t *a, int64_t i, int64_t n, int4 v) {
+  if (i + 4 <= n) {
+    *reinterpret_cast<int4 *>(a + i) = v;
+    return;
+  }
+  if (i < n) a[i] = v.x;
+  if (i + 1 < n) a[i + 1] = v.y;
+  if (i + 2 < n) a[i + 2] = v.z;
+}
+constexpr int kScanSlices = kScanItems / 4;
+
 // Phase 1: sum of each tile of kScanTile counters.
 __global__ void __launch_bounds__(kScanThreads)
     k_scan_tile_sums(const int32_t *__restrict__ count, int64_t n, int32_t *__restrict__ part) {
-  const int64_t base = (int64_t)blockIdx.x * kScanTile + (int64_t)threadIdx.x * kScanItems;
+  const int64_t tile = (int64_t)blockIdx.x * kScanTile;
+  int4 v[kScanSlices];
+#pragma unroll
+  for (int sl = 0; sl < kScanSlices; ++sl) v[sl] = load4(count, tile + 4 * ((int64_t)sl * kScanThreads + threadIdx.x), n);
   int32_t s = 0;
 #pragma unroll
-  for (int t = 0; t < kScanItems; ++t) s += (base + t < n) ? count[base + t] : 0;
+  for (int sl = 0; sl < kScanSlices; ++sl) s += v[sl].x + v[sl].y + v[sl].z + v[sl].w;
   int32_t total;
   block_exclusive_scan(s, &total);
   if (threadIdx.x == 0) part[blockIdx.x] = total;
@@ -130,28 +156,27 @@ __global__ void __launch_bounds__(kScanThreads)
   if (threadIdx.x == 0) part[n_tiles] = carry;
 }
 
-// Phase 3: exclusive scan inside each tile plus the tile offset; writes
-// col_ptr and resets the counters to the same values (scatter cursors).
+// Phase 3: exclusive scan inside each tile plus the tile offset, slice by
+// slice; writes col_ptr and resets the counters to the same values (scatter
+// cursors).
 __global__ void __launch_bounds__(kScanThreads)
     k_scan_apply(int32_t *__restrict__ count, int64_t n, const int32_t *__restrict__ part,
                  int32_t *__restrict__ col_ptr) {
-  const int64_t base = (int64_t)blockIdx.x * kScanTile + (int64_t)threadIdx.x * kScanItems;
-  int32_t v[kScanItems];
-  int32_t s = 0;
+  const int64_t tile = (int64_t)blockIdx.x * kScanTile;
+  int4 v[kScanSlices];
 #pragma unroll
-  for (int t = 0; t < kScanItems; ++t) {
-    v[t] = (base + t < n) ? count[base + t] : 0;
-    s += v[t];
-  }
-  int32_t total;
-  int32_t run = block_exclusive_scan(s, &total) + part[blockIdx.x];
+  for (int sl = 0; sl < kScanSlices; ++sl) v[sl] = load4(count, tile + 4 * ((int64_t)sl * kScanThreads + threadIdx.x), n);
+  int32_t carry = part[blockIdx.x];
 #pragma unroll
-  for (int t = 0; t < kScanItems; ++t) {
-    if (base + t < n) {
-      col_ptr[base + t] = run;
-      count[base + t] = run;
-    }
-    run += v[t];
+  for (int sl = 0; sl < kScanSlices; ++sl) {
+    const int32_t s = v[sl].x + v[sl].y + v[sl].z + v[sl].w;
+    int32_t total;
+    const int32_t run = block_exclusive_scan(s, &total) + carry;
+    const int4 o = make_int4(run, run + v[sl].x, run + v[sl].x + v[sl].y, run + v[sl].x + v[sl].y + v[sl].z);
+    const int64_t i = tile + 4 * ((int64_t)sl * kScanThreads + threadIdx.x);
+    store4(col_ptr, i, n, o);
+    store4(count, i, n, o);
+    carry += total;
   }
 }
 

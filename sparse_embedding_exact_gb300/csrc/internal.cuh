@@ -179,6 +179,11 @@ struct ss_handle {
   int sm_count = 0;
   std::string last_error;
   uint64_t launches = 0;  // kernels queued by this handle
+  // Timing of the scoring kernel (ss_profile_scorer): events recorded in
+  // pairs around each scoring-kernel launch while on.
+  bool prof_on = false;
+  std::vector<cudaEvent_t> prof_ev;
+  size_t prof_used = 0;
 
   // Device workspace, owned by the handle.
   int32_t *d_status = nullptr;  // one status word
@@ -289,6 +294,10 @@ struct ss_handle {
   int32_t *cand_n = nullptr;
   int64_t cand_elems = 0, cand_rows = 0;
 };
+
+// Records the next timing event on s when the scoring kernel is being timed
+// (called just before and just after each scoring-kernel launch).
+void prof_mark(ss_handle *h, cudaStream_t s);
 
 // Launchers (all asynchronous on `s`).
 cudaError_t launch_row_norms(const ss_csr &m, float *inv_norms, int sm_count, cudaStream_t s);

@@ -749,7 +749,9 @@ cudaError_t launch_score_lists(ss_handle *h, const ss_csr &queries, const float 
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kPThreads, smem);
   if (e != cudaSuccess) return e;
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(queries.n_rows, (int64_t)sms * std::max(per_sm, 1)));
+  prof_mark(h, s);
   kernel<<<(unsigned)grid, kPThreads, smem, s>>>(a);
+  prof_mark(h, s);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   *queued = 2 + queued_prep + queued_dense;

@@ -1338,7 +1338,9 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     sa.vec_ok = ((reinterpret_cast<uintptr_t>(dst) % 16) == 0) && (ld_dst % 4 == 0);
     sa.status = h->d_status;
     const int64_t grid = std::min<int64_t>(sms, sa.n_units);
+    prof_mark(h, s);
     k_tc_score<<<(unsigned)grid, kSThreads, score_smem_bytes(Hp), s>>>(sa);
+    prof_mark(h, s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ++nq;
   }
