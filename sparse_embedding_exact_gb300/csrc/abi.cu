@@ -240,6 +240,7 @@ bool same_auto_source(const ss_handle *h, const ss_csr &m) {
 // the matrix is built as posting lists from then on, else as item tiles.
 // Reading the probe synchronises the stream once per item matrix.
 ss_status build_chunk(ss_handle *h, const ss_csr &items, int64_t rb, int64_t re, cudaStream_t s) {
+  ss_status st = SS_OK;
   if (h->mode == MODE_POSTING) return build_algo(h, ALGO_POSTING, items, rb, re, s);
   if (h->mode == MODE_TILES) return build_algo(h, ALGO_HYBRID, items, rb, re, s);
   if (h->mode == MODE_TENSOR) return build_algo(h, ALGO_TENSOR, items, rb, re, s);
@@ -252,6 +253,15 @@ ss_status build_chunk(ss_handle *h, const ss_csr &items, int64_t rb, int64_t re,
     SS_CUDA(h, cudaMemcpyAsync(counts, h->probe, sizeof(counts), cudaMemcpyDeviceToHost, s));
     SS_CUDA(h, cudaStreamSynchronize(s));
     h->auto_algo = ((double)counts[1] > kAutoOverflowShare * (double)counts[0]) ? ALGO_POSTING : ALGO_HYBRID;
+    if (h->auto_algo == ALGO_HYBRID) {
+      // Rows short enough for item tiles: the tensor path when the matrix
+      // has a strong head (at least kAutoMinHot hot dimensions leaving at
+      // most kAutoMaxCold expected shared cold dimensions per pair).
+      if ((st = ensure_posting_workspace(h)) != SS_OK) return st;
+      SS_CUDA(h, launch_tc_hot_select(h, items, s, &queued));
+      h->launches += queued;
+      if (h->tc_H >= tcp::kAutoMinHot && h->tc_est_cold <= tcp::kAutoMaxCold) h->auto_algo = ALGO_TENSOR;
+    }
     h->auto_src[0] = items.indptr;
     h->auto_src[1] = items.indices;
     h->auto_src[2] = items.values;

@@ -123,6 +123,7 @@ constexpr int kColBlock = 32;  // items per cold-record bucket
 // The automatic choice takes the tensor path when the estimated cold
 // overlap (expected shared cold dimensions per pair) is at most this.
 constexpr double kAutoMaxCold = 0.25;
+constexpr int kAutoMinHot = 64;
 }  // namespace tcp
 
 // Most chunks one hybrid index build covers (one launch, one view per chunk).

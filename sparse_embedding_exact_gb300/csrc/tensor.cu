@@ -445,6 +445,10 @@ __global__ void __launch_bounds__(256)
     const int64_t c = (r - row_begin) / chunk_rows;
     int32_t *cur = cursor + c * (dim + 1);
     const int64_t item = r - row_begin - c * chunk_rows;
+    float *srow = slab + (c * chunk_rows + item) * kHotMax;  // this item's hot values, zero if absent
+    static_assert(kHotMax == 128, "one float4 per lane clears an item's hot values");
+    *reinterpret_cast<float4 *>(srow + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
+    __syncwarp();
     float ss = 0.f;
     for (int64_t j = b + lane; j < e; j += 32) {
       const int32_t k = __ldg(indices + j);
@@ -453,7 +457,7 @@ __global__ void __launch_bounds__(256)
       if (k < 0 || (int64_t)k >= dim) continue;  // flagged by the histogram
       const int h = find_hot(hkeys, hvals, k);
       if (h >= 0) {
-        slab[(c * chunk_rows + item) * kHotMax + h] = v;
+        srow[h] = v;
         continue;
       }
       const int32_t pos = atomicAdd(cur + k, 1);
@@ -960,12 +964,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
       const int64_t qrow0 = (g * 4 + qd) * 32;
       const int item0 = (int)t * kN;
+      // Lane l stores items 4 (l % 8) .. + 3 of rows 4 s + l / 8 of each block.
+      float *my_row = a.out + (qrow0 + (lane >> 3)) * a.ld_out + item0 + 4 * (lane & 7);
+      const bool rows_whole = qrow0 + 32 <= a.n_q;
       const uint32_t tbase = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(b * kN);
 #pragma unroll
       for (int i = 0; i < kMine; ++i) {
         const int c = 2 * i + half;
         uint32_t rc[32];
-        tmem_ld32(tbase + (uint32_t)(c * kColBlock), rc);
+        tmem_ld32(tbase + (uint32_t)(c * kColBlock), rc);  // lands during the record phase
         if (i + 2 < kMine) fetch(bnd, bk + (c + 4) * bcap, c + 4, R[(i + 2) & 3]);
         else if (j + 1 < nj) fetch(bnd_n, bk_n + (c + 4 - 2 * kMine) * bcap, c + 4 - 2 * kMine, R[(i + 2) & 3]);
 #pragma unroll
@@ -1021,18 +1028,27 @@ __global__ void __launch_bounds__(kSThreads, 1)
         // Row-contiguous stores: lane l writes items 4 (l % 8) .. + 3 of
         // rows 4 s + l / 8 (chunk l % 8 of the row, found through the swizzle).
         const int it = item0 + c * kColBlock + 4 * (lane & 7);
+        if (vec && rows_whole && item0 + (c + 1) * kColBlock <= a.n_items) {
 #pragma unroll
-        for (int sidx = 0; sidx < 8; ++sidx) {
-          const int rl = 4 * sidx + (lane >> 3);
-          const float4 v = *reinterpret_cast<const float4 *>(stg + rl * 32 + 4 * ((lane & 7) ^ (rl & 7)));
-          const int64_t q = qrow0 + rl;
-          if (q < a.n_q && it < a.n_items) {
-            float *dst = a.out + q * a.ld_out + it;
-            if (vec && it + 4 <= a.n_items) {
-              __stcs(reinterpret_cast<float4 *>(dst), v);
-            } else {
-              const float vv[4] = {v.x, v.y, v.z, v.w};
-              for (int e2 = 0; e2 < 4 && it + e2 < a.n_items; ++e2) dst[e2] = vv[e2];
+          for (int sidx = 0; sidx < 8; ++sidx) {
+            const int rl = 4 * sidx + (lane >> 3);
+            const float4 v = *reinterpret_cast<const float4 *>(stg + rl * 32 + 4 * ((lane & 7) ^ (rl & 7)));
+            __stcs(reinterpret_cast<float4 *>(my_row + (int64_t)(4 * sidx) * a.ld_out + c * kColBlock), v);
+          }
+        } else {
+#pragma unroll
+          for (int sidx = 0; sidx < 8; ++sidx) {
+            const int rl = 4 * sidx + (lane >> 3);
+            const float4 v = *reinterpret_cast<const float4 *>(stg + rl * 32 + 4 * ((lane & 7) ^ (rl & 7)));
+            const int64_t q = qrow0 + rl;
+            if (q < a.n_q && it < a.n_items) {
+              float *dst = a.out + q * a.ld_out + it;
+              if (vec && it + 4 <= a.n_items) {
+                __stcs(reinterpret_cast<float4 *>(dst), v);
+              } else {
+                const float vv[4] = {v.x, v.y, v.z, v.w};
+                for (int e2 = 0; e2 < 4 && it + e2 < a.n_items; ++e2) dst[e2] = vv[e2];
+              }
             }
           }
         }
@@ -1161,8 +1177,6 @@ cudaError_t launch_build_tc(ss_handle *h, const ss_csr &items, int64_t row_begin
   const int64_t stride = h->dim + 1;
   const int64_t n = stride * n_chunks;
   if ((e = cudaMemsetAsync(h->col_cnt, 0, sizeof(int32_t) * (size_t)n, s)) != cudaSuccess) return e;
-  if ((e = cudaMemsetAsync(h->tc_slab, 0, sizeof(float) * (size_t)n_chunks * C * kHotMax, s)) != cudaSuccess)
-    return e;
   const int grid = (h->sm_count > 0 ? h->sm_count : 148) * 8;
   k_tc_hist<<<grid, 256, 0, s>>>(items.indptr, items.indices, row_begin, row_end, C, n_chunks, h->dim,
                                  h->tc_hot, h->col_cnt, h->d_status);

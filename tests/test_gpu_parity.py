@@ -383,7 +383,7 @@ def test_index_stats_hot_set(sec):
     frac = np.bincount(I.indices, minlength=cfg.dim) / I.n_rows
     surely_in = int((frac >= HOT_MIN_FRACTION + 0.05).sum())
     maybe_in = min(HOT_MAX, int((frac >= HOT_MIN_FRACTION - 0.05).sum()))
-    with sec.SparseCosine(cfg.dim) as h:
+    with sec.SparseCosine(cfg.dim, algorithm="hybrid") as h:
         i = _dev(sec, I)
         st = h.index_stats(h.build_item_index(i, 0, 8192))
     assert st["algorithm"] == 0 and st["items"] == 8192 and st["tiles"] == 32
@@ -403,17 +403,22 @@ def test_two_gpu_algorithms_agree(sec, name):
     Q, I = generate_rows(cfg, 0, 0, 700), generate_rows(cfg, 1, 0, 9000)
     a = _gpu_cosine(sec, Q, I, algorithm="hybrid")
     b = _gpu_cosine(sec, Q, I, algorithm="posting")
-    assert _max_err(a, b) <= TOL
-    assert _max_err(a, oracle.cosine(Q, I)) <= TOL
+    c = _gpu_cosine(sec, Q, I, algorithm="tensor")
+    assert _max_err(a, b) <= TOL and _max_err(a, c) <= TOL
+    ref = oracle.cosine(Q, I)
+    assert _max_err(a, ref) <= TOL and _max_err(c, ref) <= TOL
 
 
 # ------------------------------------------------------------- posting lists
 def test_auto_choice_follows_tile_overflow(sec):
-    """Without an algorithm flag the handle builds an item matrix's first
-    batch as tiles and switches to posting lists when most tiles overflow:
-    the uniform workload (500 nonzeros a row) switches, the Zipf one stays.
-    Either way the result is that of the chosen algorithm, bit for bit."""
-    for name, want in (("d500k_q50k_i500k_uniform", 1), ("d1.2m_q5k_i200k", 0)):
+    """Without an algorithm flag the handle probes an item matrix's first
+    batch: posting lists when most item tiles overflow (the uniform workload,
+    500 nonzeros a row), else the tensor path when the matrix has a strong
+    head (the Zipf workloads: 128 hot dimensions leave about 0.11 shared cold
+    dimensions per pair).  Either way the result is that of the chosen
+    algorithm, bit for bit."""
+    names = {0: "hybrid", 1: "posting", 2: "tensor"}
+    for name, want in (("d500k_q50k_i500k_uniform", 1), ("d1.2m_q5k_i200k", 2), ("d65k_q1k_i10k", 2)):
         cfg = CONFIGS[name]
         Q, I = generate_rows(cfg, 0, 0, 50), generate_rows(cfg, 1, 0, 9000)
         with sec.SparseCosine(cfg.dim) as h:
@@ -421,7 +426,7 @@ def test_auto_choice_follows_tile_overflow(sec):
             algos = {h.index_stats(idx)["algorithm"] for _, _, idx in h.build_item_indexes(i, 0, 9000)}
         assert algos == {want}, name
         auto = _gpu_cosine(sec, Q, I, algorithm="auto")
-        forced = _gpu_cosine(sec, Q, I, algorithm="posting" if want else "hybrid")
+        forced = _gpu_cosine(sec, Q, I, algorithm=names[want])
         assert np.array_equal(auto.view(np.int32), forced.view(np.int32)), name
         assert _max_err(auto, oracle.cosine(Q, I)) <= TOL
 
@@ -573,7 +578,7 @@ def test_posting_chunk_size_invariance_is_bitwise(sec, name):
 def test_bulk_cosine_host_paths_agree(sec):
     cfg = CONFIGS["d65k_q1k_i10k"]
     Q, I = generate_rows(cfg, 0, 0, 200), generate_rows(cfg, 1, 0, 7000)
-    ref = _gpu_cosine(sec, Q, I, chunk_rows=2048)
+    ref = _gpu_cosine(sec, Q, I, chunk_rows=2048, algorithm="auto")  # the pass's own choice
     with sec.SparseCosine(cfg.dim, chunk_rows=2048) as h:
         pageable = np.full((Q.n_rows, I.n_rows), np.nan, np.float32)
         h.bulk_cosine_host(Q, I, out=pageable, ring_depth=2)
@@ -602,7 +607,7 @@ def test_bulk_cosine_host_reuses_workspace_across_sizes(sec):
     large = (generate_rows(cfg, 0, 100, 260), generate_rows(cfg, 1, 2000, 6100))
     with sec.SparseCosine(cfg.dim, chunk_rows=1024) as h:
         for Q, I in (small, large, small):
-            ref = _gpu_cosine(sec, Q, I, chunk_rows=1024)
+            ref = _gpu_cosine(sec, Q, I, chunk_rows=1024, algorithm="auto")
             big = torch.full((Q.n_rows, I.n_rows + 9), float("nan"), dtype=torch.float32).pin_memory()
             window = big[:, 5:5 + I.n_rows]
             h.bulk_cosine_host(Q, I, out=window, ring_depth=2)
@@ -642,7 +647,7 @@ def test_verified_stream_pass(sec):
     # against its host copy and records them; the result is unchanged.
     cfg = CONFIGS["d65k_q1k_i10k"]
     Q, I = generate_rows(cfg, 0, 0, 150), generate_rows(cfg, 1, 0, 5000)
-    ref = _gpu_cosine(sec, Q, I, chunk_rows=2048)
+    ref = _gpu_cosine(sec, Q, I, chunk_rows=2048, algorithm="auto")
     with sec.SparseCosine(cfg.dim, chunk_rows=2048, verify_stream=True) as h:
         pinned = torch.empty((Q.n_rows, I.n_rows), dtype=torch.float32).pin_memory()
         h.bulk_cosine_host(Q, I, out=pinned, ring_depth=3)
