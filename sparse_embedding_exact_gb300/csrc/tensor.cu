@@ -282,21 +282,21 @@ __device__ void block_sort(unsigned long long *v, int n) {
 }
 
 // Visits the selection table's slots [64 t, 64 t + 64) as f(key, count),
-// their loads issued 32 slots at a time (the table lives in global memory).
+// their loads issued 16 slots at a time (the table lives in global memory).
 template <typename F>
 __device__ __forceinline__ void for_my_slots(const int32_t *keys, const int32_t *cnts, int t, F f) {
   static_assert(kSelSlots == 64 * kSelThreads, "one run of 64 slots per thread");
 #pragma unroll 1
-  for (int h = 0; h < 2; ++h) {
-    int4 k4[8], c4[8];
-    const int base = 64 * t + 32 * h;
+  for (int h = 0; h < 4; ++h) {
+    int4 k4[4], c4[4];
+    const int base = 64 * t + 16 * h;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < 4; ++q) {
       k4[q] = *reinterpret_cast<const int4 *>(keys + base + 4 * q);
       c4[q] = *reinterpret_cast<const int4 *>(cnts + base + 4 * q);
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < 4; ++q) {
       f(k4[q].x, c4[q].x);
       f(k4[q].y, c4[q].y);
       f(k4[q].z, c4[q].z);
@@ -337,12 +337,18 @@ __global__ void __launch_bounds__(kSelThreads)
   __syncthreads();
   const int floor_c = min(kCountBins - 1, max(2, (int)((n_sample * 2 + 999) / 1000)));
   unsigned long long my_pairs = 0;
+  // Most sampled dimensions share a few small counts: the histogram adds
+  // are combined per warp (one atomic per distinct bin of the warp).
   for_my_slots(keys, cnts, tid, [&](int key, int c) {
-    if (key < 0) return;
-    my_pairs += (unsigned long long)c * (unsigned long long)(c - 1);
-    if (c >= floor_c) atomicAdd(&hist[min(c, kCountBins - 1)], 1);
+    const bool in = key >= 0 && c >= floor_c;
+    if (key >= 0) my_pairs += (unsigned long long)c * (unsigned long long)(c - 1);
+    const int bin = in ? min(c, kCountBins - 1) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, bin);
+    if (in && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
   });
-  atomicAdd(&pairs_all, my_pairs);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) my_pairs += __shfl_xor_sync(0xffffffffu, my_pairs, o);
+  if ((tid & 31) == 0) atomicAdd(&pairs_all, my_pairs);
   __syncthreads();
   if (tid == 0) {
     // Largest bin t where the dimensions in bins > t are fewer than kHotMax
