@@ -71,7 +71,7 @@ constexpr int kSThreads = 64 + 32 * kEpiWarps; // producer, MMA, epilogue warps
 constexpr int kStgBytes = kEpiWarps * kStgInts * 4 + 1024;  // one tile per warp, 1024-byte aligned
 constexpr int kRThreads = 1024;         // records: one warp per query row of the block
 constexpr int kPrepThreads = 256;
-constexpr int kWalkUnroll = 4;          // list entries per lane loaded before use
+constexpr int kWalkUnroll = 8;          // list entries per lane loaded before use
 constexpr int kRecPerLane = 4;          // epilogue: records of a block held per lane (128 per block)
 constexpr long long kWaitNs = 2000000000ll;    // bounded waits: 2 s
 
@@ -723,7 +723,7 @@ __device__ __forceinline__ void walk_row(const RecArgs &a, int64_t r, int lane, 
 // inside a bucket does not matter: the epilogue sums integers).  A bucket
 // that fills up is marked (count -1); the scorer then takes that block's
 // cold products straight from the lists.
-__global__ void __launch_bounds__(kRThreads, 2) k_tc_records(const RecArgs a) {
+__global__ void __launch_bounds__(kRThreads, 1) k_tc_records(const RecArgs a) {
   extern __shared__ int rsm[];
   int *cnt = rsm;  // [n_cb]
   __shared__ int4 slots_all[kRThreads / 32][32];
