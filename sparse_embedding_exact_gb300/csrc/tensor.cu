@@ -585,27 +585,62 @@ __global__ void __launch_bounds__(kPrepThreads) k_tc_prep_queries(const PrepArgs
   if (__any_sync(0xffffffffu, bad) && lane == 0) flag(a.status, DEV_RANGE);
 }
 
-// The item operand of a chunk from its hot slab: one warp per group of 8
-// items, every K column written (zeros past the chunk).  Checks the inverse
-// norms against the items' sums of squares.
-__global__ void __launch_bounds__(kPrepThreads) k_tc_prep_items(const PrepArgs a) {
+// The item operand of a chunk from its hot slab, and the normalised copy
+// of the chunk's list entries, in one launch: the first `prep_blocks`
+// blocks take groups of 8 items (one warp a group; lane l reads row l / 4,
+// hot columns 32 (l % 4) .. + 31 as eight float4 loads issued together;
+// every K column written, zeros past the chunk; the inverse norms are
+// checked against the items' sums of squares), the other blocks rewrite the
+// list entries as {item, v * inv_i[item]}.
+struct ItemPrepArgs {
+  PrepArgs p;
+  int64_t prep_blocks;
+  const int32_t *col_ptr;  // the chunk's [dim + 1]
+  int32_t dim;
+  int64_t capacity;
+  const uint16_t *post_item;
+  const float *post_val;
+  int2 *post_hat;
+};
+
+__global__ void __launch_bounds__(kPrepThreads) k_tc_prep_items(const ItemPrepArgs ia) {
+  const PrepArgs &a = ia.p;
+  if ((int64_t)blockIdx.x >= ia.prep_blocks) {
+    const int64_t nb = gridDim.x - ia.prep_blocks, b = blockIdx.x - ia.prep_blocks;
+    const int64_t p0 = __ldg(ia.col_ptr), p1 = min((int64_t)__ldg(ia.col_ptr + ia.dim), ia.capacity);
+    for (int64_t p = p0 + b * kPrepThreads + threadIdx.x; p < p1; p += nb * kPrepThreads) {
+      const int it = ia.post_item[p];
+      ia.post_hat[p] = make_int2(it, __float_as_int(ia.post_val[p] * __ldg(a.inv + it)));
+    }
+    return;
+  }
   __shared__ __align__(16) uint16_t grp[kPrepThreads / 32][8 * 2 * kHotMax];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int Hp = a.Hp;
+  const int rr = lane >> 2, h0 = 32 * (lane & 3);
   uint16_t *gs = grp[warp];
   bool bad = false;
   for (int64_t g = (int64_t)blockIdx.x * (kPrepThreads / 32) + warp; g < a.n_groups;
-       g += (int64_t)gridDim.x * (kPrepThreads / 32)) {
-    for (int rr = 0; rr < 8; ++rr) {
-      const int64_t r = g * 8 + rr;
-      const bool in = r < a.n_rows;
-      const float iv = in ? __ldg(a.inv + r) : 0.f;
-      if (in && lane == 0) bad |= !(__ldg(a.sq + r) * iv * iv <= kMaxSquareSum);
-      for (int h = lane; h < Hp; h += 32) {
-        const float v = (in && h < kHotMax) ? __ldg(a.slab + r * kHotMax + h) : 0.f;
-        const float x = v * iv;
-        bad |= !(fabsf(x) <= kMaxNormalised);
-        put_split(gs, rr, h, Hp, x);
+       g += ia.prep_blocks * (kPrepThreads / 32)) {
+    const int64_t r = g * 8 + rr;
+    const bool in = r < a.n_rows;
+    const float iv = in ? __ldg(a.inv + r) : 0.f;
+    if (in && (lane & 3) == 0) bad |= !(__ldg(a.sq + r) * iv * iv <= kMaxSquareSum);
+    float4 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (in && h0 + 4 * q < Hp) v[q] = __ldg(reinterpret_cast<const float4 *>(a.slab + r * kHotMax + h0) + q);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int h = h0 + 4 * q;
+      if (h >= Hp) continue;
+      const float x[4] = {v[q].x * iv, v[q].y * iv, v[q].z * iv, v[q].w * iv};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        bad |= !(fabsf(x[e]) <= kMaxNormalised);
+        put_split(gs, rr, h + e, Hp, x[e]);
       }
     }
     __syncwarp();
@@ -613,19 +648,6 @@ __global__ void __launch_bounds__(kPrepThreads) k_tc_prep_items(const PrepArgs a
     __syncwarp();
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) flag(a.status, DEV_RANGE);
-}
-
-// Normalised copy of a chunk's posting entries: {item, value * inv_i[item]}.
-__global__ void __launch_bounds__(256)
-    k_tc_norm_lists(const int32_t *__restrict__ col_ptr, int32_t dim, int64_t capacity,
-                    const uint16_t *__restrict__ post_item, const float *__restrict__ post_val,
-                    const float *__restrict__ inv_i, int2 *__restrict__ post_hat) {
-  const int64_t p0 = __ldg(col_ptr), p1 = min((int64_t)__ldg(col_ptr + dim), capacity);
-  for (int64_t p = p0 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < p1;
-       p += (int64_t)gridDim.x * blockDim.x) {
-    const int it = post_item[p];
-    post_hat[p] = make_int2(it, __float_as_int(post_val[p] * __ldg(inv_i + it)));
-  }
 }
 
 // ---------------------------------------------------------------- records
@@ -1282,12 +1304,19 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     pa.qcold = nullptr;
     pa.qcold_n = nullptr;
     pa.status = h->d_status;
-    const int64_t blocks = std::min<int64_t>((pa.n_groups + 7) / 8, (int64_t)sms * 8);
-    k_tc_prep_items<<<(unsigned)blocks, kPrepThreads, 0, s>>>(pa);
-    k_tc_norm_lists<<<sms * 4, 256, 0, s>>>(idx.col_ptr, (int32_t)idx.dim, idx.capacity, idx.post_item,
-                                           idx.post_val, inv_i, h->post_hat);
+    ItemPrepArgs ia;
+    ia.p = pa;
+    ia.prep_blocks = std::min<int64_t>((pa.n_groups + 7) / 8, (int64_t)sms * 8);
+    ia.col_ptr = idx.col_ptr;
+    ia.dim = (int32_t)idx.dim;
+    ia.capacity = idx.capacity;
+    ia.post_item = idx.post_item;
+    ia.post_val = idx.post_val;
+    ia.post_hat = h->post_hat;
+    const int64_t norm_blocks = (int64_t)sms * 2;
+    k_tc_prep_items<<<(unsigned)(ia.prep_blocks + norm_blocks), kPrepThreads, 0, s>>>(ia);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    nq += 2;
+    ++nq;
   }
 
   // Cold records: a bucket per (32 query rows, 32 items) holding 3 times
