@@ -548,6 +548,20 @@ def test_tensor_hot_part_alone_and_cold_part_alone(sec):
     assert np.abs(np.diag(got) - 1.0).max() <= TOL
 
 
+@pytest.mark.parametrize("name,n_q,n_i,chunk", [("d1.2m_q5k_i200k", 70, 20000, 20000),
+                                                 ("d65k_q1k_i10k", 45, 10000, 9000)])
+def test_tensor_chunks_wider_than_8192_items(sec, name, n_q, n_i, chunk):
+    """Chunks of more than 8,192 items on the tensor path: more than 256
+    record buckets per block of 32 rows, several item tiles per chunk, and
+    the same bits as with small chunks (integer sums of the cold part)."""
+    cfg = CONFIGS[name]
+    Q, I = generate_rows(cfg, 0, 0, n_q), generate_rows(cfg, 1, 0, n_i)
+    got = _gpu_cosine(sec, Q, I, chunk_rows=chunk, algorithm="tensor")
+    small = _gpu_cosine(sec, Q, I, chunk_rows=1000, algorithm="tensor")
+    assert np.array_equal(got.view(np.int32), small.view(np.int32))
+    assert _max_err(got, oracle.cosine(Q, I)) <= TOL
+
+
 @pytest.mark.parametrize("name,n_i,chunk", [("d65k_q1k_i10k", 10000, 10000),
                                              ("d500k_q50k_i500k_uniform", 20000, 20000)])
 def test_posting_chunks_wider_than_one_window(sec, name, n_i, chunk):
