@@ -64,6 +64,9 @@ def parse_args():
                    help="use only the first N query rows (small profiling captures)")
     p.add_argument("--n-items", type=int, default=0,
                    help="use only the first N item rows (small profiling captures)")
+    p.add_argument("--device-limit", type=int, default=0,
+                   help="device bytes the e2e host pass may hold for input copies and output tiles "
+                        "(0: no limit); above it the pass streams item batches and tiles the queries")
     return p.parse_args()
 
 
@@ -448,6 +451,7 @@ def run_ours(args):
             return o
 
         Qh, Ih = pin_csr(Q), pin_csr(I)
+        h.set_device_limit(args.device_limit)
         if resident:  # the whole matrix lands in one page-locked host array
             out_h = _t.empty((n_q, n_i), dtype=_t.float32).pin_memory()
             api = "ss_bulk_cosine_host (pinned host CSR in, pinned host matrix out)"
@@ -477,6 +481,10 @@ def run_ours(args):
         e2e = {"value": world * n_q * n_i / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(4 * n_q * n_i), "steps": e2e_steps,
                "api": api}
+        if args.device_limit:
+            qb, ib = sec.plan_host_pass(Q.indptr, I.indptr, CHUNK, args.device_limit, resident)
+            e2e["device_limit"] = {"bytes": args.device_limit, "query_tiles": len(qb) - 1,
+                                   "item_batches": len(ib) - 1}
 
     h.close()
     if rank == 0:

@@ -264,11 +264,60 @@ typedef int (*ss_chunk_consumer)(void *user, int64_t chunk, int64_t item_begin,
  * and ring buffers belong to the handle and are kept (grown when needed)
  * between calls; ss_destroy frees them.  timeout_ms bounds each host wait
  * on the GPU (0 = 60000 ms); SS_ERR_TIMEOUT if one runs out.
+ *
+ * Under a device limit (ss_set_device_limit) that the whole pass does not
+ * fit, the items are copied in batches of rows (the next batch on a third
+ * stream while the current one is scored, two batch buffers) and, where the
+ * queries and their output tiles do not fit half the limit, the queries in
+ * tiles of rows; each chunk of a batch is then scored against each query
+ * tile, and the tiles reach out_host at their own rows.  Per batch the
+ * norms, the choice of algorithm and the hot dimensions are taken from the
+ * batch alone, so the values agree with the unlimited pass within the
+ * stated accuracy, not bit for bit.  A consumer receives whole columns of
+ * the result: with more than one query tile the call returns SS_ERR_LIMIT
+ * before any work.  With SS_VERIFY_STREAM one checksum is logged per
+ * delivered tile (chunk x query tile, in delivery order).  The ranges come
+ * from ss_plan_host_pass.
  */
 ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *queries_host,
                               const ss_csr *items_host, float *out_host, int64_t ld_out,
                               ss_chunk_consumer consumer, void *user, int32_t ring_depth,
                               int32_t timeout_ms);
+
+/*
+ * Caps the device memory ss_bulk_cosine_host holds for its copies of the
+ * inputs, their inverse norms and its output tiles at `bytes` (0 = no cap,
+ * the default).  The chunk indexes and the scoring workspace are sized by a
+ * chunk, not by the matrices, and are not counted.  Errors:
+ * SS_ERR_INVALID_ARG (null handle, negative bytes).
+ */
+ss_status ss_set_device_limit(ss_handle *h, int64_t bytes);
+
+/*
+ * How ss_bulk_cosine_host splits a pass under a device limit (host only; no
+ * device is touched).  q_indptr[n_q + 1] and i_indptr[n_i + 1] are the host
+ * CSR row pointers; direct_output != 0 when the output is page-locked and
+ * written in place (no output tiles on the device).  On return *n_q_tiles
+ * query tiles and *n_i_batches item batches, with boundaries
+ * q_bounds[0..*n_q_tiles] (0, ..., n_q) and i_bounds[0..*n_i_batches]
+ * (0, ..., n_i) when those arrays are given (NULL: counts only).  Rules: no
+ * limit, or a pass that fits it whole: one tile and one batch.  Otherwise
+ * the queries stay whole if their copy (8 bytes per row pointer, 8 per
+ * nonzero, 4 per row for the norms) and their two output tiles of
+ * rows x min(chunk_rows, n_i) floats take at most half the limit; else
+ * tiles whose copy takes at most a quarter of the limit and whose output
+ * tiles at most another quarter.  What the query side leaves is halved into
+ * two item batch slots; each batch is the longest run of rows whose copy
+ * fits a slot, cut to a multiple of chunk_rows when it holds at least one
+ * chunk.  Every tile and batch has fewer than 2^31 nonzeros.  Errors:
+ * SS_ERR_INVALID_ARG (null pointers, negative sizes, chunk_rows < 1, a
+ * bounds array too short: counts are still written), SS_ERR_LIMIT (one row
+ * does not fit its share).
+ */
+ss_status ss_plan_host_pass(const int64_t *q_indptr, int64_t n_q, const int64_t *i_indptr, int64_t n_i,
+                            int32_t chunk_rows, int64_t device_limit, int32_t direct_output,
+                            int64_t *q_bounds, int64_t q_cap, int64_t *n_q_tiles, int64_t *i_bounds,
+                            int64_t i_cap, int64_t *n_i_batches);
 
 /*
  * Checksums of a row-major float32 tile of n_rows x n_cols with leading

@@ -284,6 +284,12 @@ class SparseCosine:
         self._check(st, "ss_bulk_cosine_host")
         return out
 
+    def set_device_limit(self, nbytes: int) -> None:
+        """Caps the device bytes bulk_cosine_host holds for input copies, norms
+        and output tiles (0: no cap); above it the pass streams item batches
+        and tiles the queries (ss_plan_host_pass)."""
+        self._check(self._lib.ss_set_device_limit(self._h, int(nbytes)), "ss_set_device_limit")
+
     def validate_csr(self, m: DeviceCsr, stream=None):
         c = m.abi()
         self._check(self._lib.ss_validate_csr(self._h, ctypes.byref(c), _stream_ptr(stream)),
@@ -328,6 +334,28 @@ class SparseCosine:
 
 def library_path() -> str:
     return _abi.library_path()
+
+
+def plan_host_pass(q_indptr, i_indptr, chunk_rows: int, device_limit: int, direct_output: bool = False):
+    """Query-tile and item-batch boundaries of a bulk_cosine_host pass under
+    a device limit (host only: runs without a GPU)."""
+    lib = _abi.load()
+    qp = np.ascontiguousarray(q_indptr, dtype=np.int64)
+    ip = np.ascontiguousarray(i_indptr, dtype=np.int64)
+    nq, ni = ctypes.c_int64(0), ctypes.c_int64(0)
+    st = lib.ss_plan_host_pass(qp.ctypes.data, len(qp) - 1, ip.ctypes.data, len(ip) - 1, int(chunk_rows),
+                               int(device_limit), int(bool(direct_output)), None, 0, ctypes.byref(nq),
+                               None, 0, ctypes.byref(ni))
+    if st != _abi.SS_OK:
+        raise _abi.SparseCosError(st, "ss_plan_host_pass: " + lib.ss_status_string(st).decode())
+    qb = np.zeros(nq.value + 1, dtype=np.int64)
+    ib = np.zeros(ni.value + 1, dtype=np.int64)
+    st = lib.ss_plan_host_pass(qp.ctypes.data, len(qp) - 1, ip.ctypes.data, len(ip) - 1, int(chunk_rows),
+                               int(device_limit), int(bool(direct_output)), qb.ctypes.data, len(qb),
+                               ctypes.byref(nq), ib.ctypes.data, len(ib), ctypes.byref(ni))
+    if st != _abi.SS_OK:
+        raise _abi.SparseCosError(st, "ss_plan_host_pass: " + lib.ss_status_string(st).decode())
+    return qb, ib
 
 
 def tile_checksum_host(tile: np.ndarray):

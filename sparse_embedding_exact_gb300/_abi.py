@@ -64,6 +64,9 @@ SIGNATURES = {
     "ss_tile_checksum_host": (_I32, [_P, _I64, _I64, _I64, _P, _P]),
     "ss_stream_checksum": (_I32, [_P, _I64, _P, _P]),
     "ss_bulk_cosine_host": (_I32, [_P, _CSR, _CSR, _P, _I64, ss_chunk_consumer, _P, _I32, _I32]),
+    "ss_set_device_limit": (_I32, [_P, _I64]),
+    "ss_plan_host_pass": (_I32, [_P, _I64, _P, _I64, _I32, _I64, _I32, _P, _I64,
+                                 ctypes.POINTER(_I64), _P, _I64, ctypes.POINTER(_I64)]),
     "ss_validate_csr": (_I32, [_P, _CSR, _P]),
     "ss_check_device": (_I32, [_P, _P]),
     "ss_invalidate": (_I32, [_P]),

@@ -473,15 +473,10 @@ ss_status ss_validate_csr(ss_handle *h, const ss_csr *m, void *stream) {
 
 ss_status ss_invalidate(ss_handle *h) {
   if (!h) return SS_ERR_INVALID_ARG;
-  for (int j = 0; j < 3; ++j) h->hot_src[j] = h->prep_src[j] = h->auto_src[j] = h->qd_src[j] = nullptr;
-  for (int j = 0; j < 3; ++j) h->tc_hot_src[j] = nullptr;
-  for (int j = 0; j < 4; ++j) h->tcq_src[j] = nullptr;
-  h->tc_hot_rows = h->tc_hot_nnz = h->tcq_rows = h->tcq_nnz = -1;
-  h->tcq_generation = ~0ull;
-  h->hot_src_rows = h->hot_src_nnz = h->prep_rows = h->prep_nnz = -1;
-  h->auto_src_rows = h->auto_src_nnz = h->qd_rows = h->qd_nnz = -1;
-  h->qd_generation = ~0ull;
-  h->prep_generation = ~0ull;
+  invalidate_queries(h);
+  for (int j = 0; j < 3; ++j) h->hot_src[j] = h->auto_src[j] = h->tc_hot_src[j] = nullptr;
+  h->tc_hot_rows = h->tc_hot_nnz = h->hot_src_rows = h->hot_src_nnz = -1;
+  h->auto_src_rows = h->auto_src_nnz = -1;
   return SS_OK;
 }
 

@@ -151,9 +151,18 @@ struct ss_topk {
 // page-locked ring used when results cannot be written straight to the
 // caller's memory.
 struct ss_host_pass {
-  enum { kQPtr, kQIdx, kQVal, kIPtr, kIIdx, kIVal, kInvQ, kInvI, kOut0, kOut1, kBuffers };
-  cudaStream_t comp = nullptr, copy = nullptr;
+  // Device buffers: the query tile (indptr, indices, values, inverse norms),
+  // two item batch slots (the same four each), two output tiles.
+  enum { kQPtr, kQIdx, kQVal, kInvQ, kIPtr0, kIIdx0, kIVal0, kInvI0, kIPtr1, kIIdx1, kIVal1, kInvI1,
+         kOut0, kOut1, kBuffers };
+  static constexpr int kSlotRoles = 4;  // kIPtr1 - kIPtr0
+  // comp: norms, builds, scoring; copy: results to the host ring; up: item
+  // batches to the device (the next batch while the current one is scored).
+  cudaStream_t comp = nullptr, copy = nullptr, up = nullptr;
   cudaEvent_t done[2] = {nullptr, nullptr}, out_free[2] = {nullptr, nullptr}, finished = nullptr;
+  cudaEvent_t batch_ready[2] = {nullptr, nullptr}, batch_free[2] = {nullptr, nullptr};
+  // Device bytes the pass may hold for its buffers above (0: no limit).
+  int64_t device_limit = 0;
   std::vector<cudaEvent_t> copied;  // one per ring slot
   void *buf[kBuffers] = {};
   size_t cap[kBuffers] = {};
@@ -295,6 +304,10 @@ struct ss_handle {
   int32_t *cand_n = nullptr;
   int64_t cand_elems = 0, cand_rows = 0;
 };
+
+// Forgets what was prepared from the current query matrix (its caches are
+// keyed on the arrays' addresses, which a host pass reuses for new contents).
+void invalidate_queries(ss_handle *h);
 
 // Records the next timing event on s when the scoring kernel is being timed
 // (called just before and just after each scoring-kernel launch).

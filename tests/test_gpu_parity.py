@@ -642,6 +642,87 @@ def test_bulk_cosine_host_consumer_can_stop(sec):
         h.bulk_cosine_host(Q, I, consumer=lambda c, b, e, t: 0)
 
 
+# --------------------------------------------- host streaming under a device limit
+def _limit_case(sec):
+    cfg = CONFIGS["d65k_q1k_i10k"]
+    Q, I = generate_rows(cfg, 0, 0, 300), generate_rows(cfg, 1, 0, 7000)
+    return cfg, Q, I, oracle.cosine(Q, I)
+
+
+@pytest.mark.parametrize("limit,direct,shape", [
+    (32 * 100 * 512, False, (4, 6)),   # query tiles of 100 rows, item batches of 3 chunks
+    (3_371_936, False, (2, 4)),        # queries whole, item batches of 5 chunks
+    (200_000, True, (4, 35)),          # in place; batches shorter than a chunk
+])
+def test_bulk_cosine_host_under_device_limit(sec, limit, direct, shape):
+    cfg, Q, I, ref = _limit_case(sec)
+    qb, ib = sec.plan_host_pass(Q.indptr, I.indptr, 512, limit, direct)
+    assert (len(qb), len(ib)) == shape
+    free = _gpu_cosine(sec, Q, I, chunk_rows=512, algorithm="auto")
+    with sec.SparseCosine(cfg.dim, chunk_rows=512) as h:
+        h.set_device_limit(limit)
+        if direct:
+            out = torch.full((Q.n_rows, I.n_rows), float("nan"), dtype=torch.float32).pin_memory()
+            h.bulk_cosine_host(Q, I, out=out, ring_depth=2)
+            got = out.numpy()
+        else:
+            got = np.full((Q.n_rows, I.n_rows), np.nan, np.float32)
+            h.bulk_cosine_host(Q, I, out=got, ring_depth=3)
+        # the handle stays usable without the limit, and then matches the free pass bit for bit
+        h.set_device_limit(0)
+        again = np.full_like(got, np.nan)
+        h.bulk_cosine_host(Q, I, out=again, ring_depth=2)
+    assert not np.isnan(got).any()
+    assert _max_err(got, ref) <= TOL
+    assert _max_err(got, free) <= 2 * TOL
+    assert np.array_equal(again.view(np.int32), free.view(np.int32))
+
+
+def test_bulk_cosine_host_limit_with_consumer_and_checksums(sec):
+    from sparse_embedding_exact_gb300 import SparseCosError
+
+    cfg, Q, I, ref = _limit_case(sec)
+    with sec.SparseCosine(cfg.dim, chunk_rows=512) as h:
+        # queries whole, items in batches of whole chunks: the consumer sees every chunk once, in order
+        h.set_device_limit(3_371_936)
+        seen = np.full((Q.n_rows, I.n_rows), np.nan, np.float32)
+        chunks = []
+
+        def consume(c, b, e, tile):
+            chunks.append((c, b, e))
+            seen[:, b:e] = tile
+
+        h.bulk_cosine_host(Q, I, consumer=consume, ring_depth=3)
+        assert chunks == [(c, 512 * c, min(512 * (c + 1), 7000)) for c in range(14)]
+        assert _max_err(seen, ref) <= TOL
+        # query tiles cannot go to a consumer: refused before any work
+        h.set_device_limit(32 * 100 * 512)
+        with pytest.raises(SparseCosError) as e:
+            h.bulk_cosine_host(Q, I, consumer=consume, ring_depth=3)
+        assert e.value.status == sec._abi.SS_ERR_LIMIT
+        assert len(chunks) == 14
+        # a limit no row fits
+        h.set_device_limit(64)
+        with pytest.raises(SparseCosError) as e:
+            h.bulk_cosine_host(Q, I, out=seen, ring_depth=2)
+        assert e.value.status == sec._abi.SS_ERR_LIMIT
+    with sec.SparseCosine(cfg.dim, chunk_rows=512, verify_stream=True) as h:
+        h.set_device_limit(32 * 100 * 512)
+        got = np.full((Q.n_rows, I.n_rows), np.nan, np.float32)
+        h.bulk_cosine_host(Q, I, out=got, ring_depth=4)
+        sums = h.stream_checksums()
+    assert _max_err(got, ref) <= TOL
+    # one checksum per delivered tile: per batch, per query tile, per chunk
+    qb, ib = sec.plan_host_pass(Q.indptr, I.indptr, 512, 32 * 100 * 512, False)
+    tiles = [(q0, q1, c0, min(c0 + 512, b1))
+             for b0, b1 in zip(ib[:-1], ib[1:]) for q0, q1 in zip(qb[:-1], qb[1:])
+             for c0 in range(b0, b1, 512)]
+    assert len(sums) == len(tiles)
+    for (bits, _), (q0, q1, c0, c1) in zip(sums, tiles):
+        t = np.ascontiguousarray(got[q0:q1, c0:c1])
+        assert bits == int(t.view(np.uint32).astype(np.uint64).sum(dtype=np.uint64))
+
+
 # ------------------------------------------------------------- checksums
 def test_device_checksum_matches_host_checksum(sec):
     rng = np.random.default_rng(9)
