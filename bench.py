@@ -64,6 +64,9 @@ def parse_args():
                    help="use only the first N query rows (small profiling captures)")
     p.add_argument("--n-items", type=int, default=0,
                    help="use only the first N item rows (small profiling captures)")
+    p.add_argument("--host-values", default="f32", choices=["f32", "bf16", "f16"],
+                   help="value type of the host CSRs of the e2e leg (16-bit values are rounded from the "
+                        "float32 workload, sent at 2 bytes a value and widened on the device)")
     p.add_argument("--device-limit", type=int, default=0,
                    help="device bytes the e2e host pass may hold for input copies and output tiles "
                         "(0: no limit); above it the pass streams item batches and tiles the queries")
@@ -443,11 +446,20 @@ def run_ours(args):
         class Host:
             pass
 
+        def host_values(v):
+            if args.host_values == "bf16":
+                from workload.halfprec import to_bf16_bits
+                return pinned(to_bf16_bits(v), np.uint16)
+            if args.host_values == "f16":
+                from workload.halfprec import to_f16_bits
+                return pinned(to_f16_bits(v), np.uint16)
+            return pinned(v, np.float32)
+
         def pin_csr(m):
             o = Host()
             o.indptr, o.indices, o.values, o.dim = (pinned(m.indptr, np.int64),
                                                   pinned(m.indices, np.int32),
-                                                  pinned(m.values, np.float32), m.dim)
+                                                  host_values(m.values), m.dim)
             return o
 
         Qh, Ih = pin_csr(Q), pin_csr(I)
@@ -457,12 +469,13 @@ def run_ours(args):
             api = "ss_bulk_cosine_host (pinned host CSR in, pinned host matrix out)"
 
             def host_pass():
-                h.bulk_cosine_host(Qh, Ih, out=out_h)
+                h.bulk_cosine_host(Qh, Ih, out=out_h, host_values=args.host_values)
         else:  # too large to keep: each chunk reaches the pinned ring, is handed over, dropped
             api = "ss_bulk_cosine_host (pinned host CSR in, each chunk to the pinned host ring)"
 
             def host_pass():
-                h.bulk_cosine_host(Qh, Ih, consumer=lambda c, b, e, tile: 0, ring_depth=3)
+                h.bulk_cosine_host(Qh, Ih, consumer=lambda c, b, e, tile: 0, ring_depth=3,
+                                   host_values=args.host_values)
         host_pass()  # warm-up
         e2e_steps = max(1, min(args.steps, 3))
         barrier()
@@ -476,13 +489,15 @@ def run_ours(args):
             t = torch.tensor([dt], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             dt = float(t.item())
-        h2d = (Q.indptr.nbytes + Q.indices.nbytes + Q.values.nbytes + I.indptr.nbytes
-               + I.indices.nbytes + I.values.nbytes)
+        h2d = sum(a.nbytes for m in (Qh, Ih) for a in (m.indptr, m.indices, m.values))
         e2e = {"value": world * n_q * n_i / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(4 * n_q * n_i), "steps": e2e_steps,
                "api": api}
+        if args.host_values != "f32":
+            e2e["host_values"] = args.host_values
         if args.device_limit:
-            qb, ib = sec.plan_host_pass(Q.indptr, I.indptr, CHUNK, args.device_limit, resident)
+            qb, ib = sec.plan_host_pass(Q.indptr, I.indptr, CHUNK, args.device_limit, resident,
+                                        args.host_values)
             e2e["device_limit"] = {"bytes": args.device_limit, "query_tiles": len(qb) - 1,
                                    "item_batches": len(ib) - 1}
 

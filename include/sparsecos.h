@@ -285,6 +285,28 @@ ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *queries_host,
                               int32_t timeout_ms);
 
 /*
+ * Reduced-precision input values for ss_bulk_cosine_host (the post's
+ * suggestion of 16-bit values to halve memory and transfers, section 5.3):
+ * after ss_set_host_values(h, SS_VALUES_BF16 or SS_VALUES_F16) the `values`
+ * arrays of the host CSRs given to ss_bulk_cosine_host hold 2-byte values
+ * of that type (the pointer is read as const uint16_t *: bfloat16 or IEEE
+ * binary16 bit patterns).  They cross to the device at 2 bytes a value and
+ * are widened there to float32, exactly; from then on the pass is the
+ * float32 one, so the scores are bit for bit those of the float32 pass on
+ * the widened values when both passes split alike (no device limit; under
+ * one the 2-byte staging copies can change the item batches, and each batch
+ * takes its own hot dimensions: equal within 2e-6 then).  Against the cosines of the unrounded values the
+ * input rounding adds at most 2 asin(u) (u = 2^-9 for bfloat16, 2^-11 for
+ * binary16, round-to-nearest inputs).  Values must be finite.  The setting
+ * stays with the handle; SS_VALUES_F32 (the default) restores float32.
+ * Errors: SS_ERR_INVALID_ARG (null handle, unknown type).
+ */
+#define SS_VALUES_F32 0
+#define SS_VALUES_BF16 1
+#define SS_VALUES_F16 2
+ss_status ss_set_host_values(ss_handle *h, int32_t value_type);
+
+/*
  * Caps the device memory ss_bulk_cosine_host holds for its copies of the
  * inputs, their inverse norms and its output tiles at `bytes` (0 = no cap,
  * the default).  The chunk indexes and the scoring workspace are sized by a
@@ -297,7 +319,9 @@ ss_status ss_set_device_limit(ss_handle *h, int64_t bytes);
  * How ss_bulk_cosine_host splits a pass under a device limit (host only; no
  * device is touched).  q_indptr[n_q + 1] and i_indptr[n_i + 1] are the host
  * CSR row pointers; direct_output != 0 when the output is page-locked and
- * written in place (no output tiles on the device).  On return *n_q_tiles
+ * written in place (no output tiles on the device); value_type is the host
+ * values' SS_VALUES_* type (16-bit values add a 2-byte staging copy per
+ * nonzero to the device copy).  On return *n_q_tiles
  * query tiles and *n_i_batches item batches, with boundaries
  * q_bounds[0..*n_q_tiles] (0, ..., n_q) and i_bounds[0..*n_i_batches]
  * (0, ..., n_i) when those arrays are given (NULL: counts only).  Rules: no
@@ -310,14 +334,14 @@ ss_status ss_set_device_limit(ss_handle *h, int64_t bytes);
  * two item batch slots; each batch is the longest run of rows whose copy
  * fits a slot, cut to a multiple of chunk_rows when it holds at least one
  * chunk.  Every tile and batch has fewer than 2^31 nonzeros.  Errors:
- * SS_ERR_INVALID_ARG (null pointers, negative sizes, chunk_rows < 1, a
- * bounds array too short: counts are still written), SS_ERR_LIMIT (one row
- * does not fit its share).
+ * SS_ERR_INVALID_ARG (null pointers, negative sizes, chunk_rows < 1, an
+ * unknown value type, a bounds array too short: counts are still written),
+ * SS_ERR_LIMIT (one row does not fit its share).
  */
 ss_status ss_plan_host_pass(const int64_t *q_indptr, int64_t n_q, const int64_t *i_indptr, int64_t n_i,
                             int32_t chunk_rows, int64_t device_limit, int32_t direct_output,
-                            int64_t *q_bounds, int64_t q_cap, int64_t *n_q_tiles, int64_t *i_bounds,
-                            int64_t i_cap, int64_t *n_i_batches);
+                            int32_t value_type, int64_t *q_bounds, int64_t q_cap, int64_t *n_q_tiles,
+                            int64_t *i_bounds, int64_t i_cap, int64_t *n_i_batches);
 
 /*
  * Checksums of a row-major float32 tile of n_rows x n_cols with leading

@@ -65,10 +65,20 @@ class DeviceCsr:
                          dev(batch.values, np.float32), int(batch.dim))
 
 
-def _host_csr(batch):
+_HOST_VALUES = {"f32": _abi.SS_VALUES_F32, "bf16": _abi.SS_VALUES_BF16, "f16": _abi.SS_VALUES_F16}
+
+
+def _host_csr(batch, host_values="f32"):
     indptr = np.ascontiguousarray(batch.indptr, dtype=np.int64)
     indices = np.ascontiguousarray(batch.indices, dtype=np.int32)
-    values = np.ascontiguousarray(batch.values, dtype=np.float32)
+    if host_values == "f32":
+        values = np.ascontiguousarray(batch.values, dtype=np.float32)
+    else:  # 2-byte bit patterns, passed through untouched
+        v = np.asarray(batch.values)
+        if v.dtype not in (np.uint16, np.int16, np.float16) or (host_values == "bf16" and v.dtype == np.float16):
+            raise TypeError(f"host_values={host_values!r} wants 16-bit values (uint16 bit patterns"
+                            f"{'' if host_values == 'bf16' else ' or float16'}), got {v.dtype}")
+        values = np.ascontiguousarray(v).view(np.uint16)
     m = _abi.ss_csr(indptr.ctypes.data, indices.ctypes.data, values.ctypes.data,
                     int(indptr.shape[0] - 1), int(indices.shape[0]), int(batch.dim))
     return m, (indptr, indices, values)
@@ -250,16 +260,21 @@ class SparseCosine:
 
     def bulk_cosine_host(self, queries, items, out: Optional[np.ndarray] = None,
                          consumer: Optional[Callable] = None, ring_depth: int = 3,
-                         timeout_ms: int = 0):
+                         timeout_ms: int = 0, host_values: str = "f32"):
         """Host CSR in, result streamed back chunk by chunk.
 
         out: a float32 (n_q, n_i) host array (numpy or a CPU torch tensor,
         ideally page-locked) or None; consumer(chunk, item_begin, item_end,
         tile) receives each chunk as a (n_q, width) numpy view valid during
-        the call.
+        the call.  host_values: "f32", or "bf16" / "f16" for 16-bit values
+        (uint16 bit patterns, or float16 for "f16"), sent to the device at
+        2 bytes a value and widened there exactly (ss_set_host_values).
         """
-        cq, keep_q = _host_csr(queries)
-        ci, keep_i = _host_csr(items)
+        if host_values not in _HOST_VALUES:
+            raise ValueError(f"host_values must be one of {sorted(_HOST_VALUES)}")
+        cq, keep_q = _host_csr(queries, host_values)
+        ci, keep_i = _host_csr(items, host_values)
+        self._check(self._lib.ss_set_host_values(self._h, _HOST_VALUES[host_values]), "ss_set_host_values")
         out_ptr, ld = ctypes.c_void_p(0), 0
         if out is not None:
             if isinstance(out, torch.Tensor):
@@ -336,22 +351,24 @@ def library_path() -> str:
     return _abi.library_path()
 
 
-def plan_host_pass(q_indptr, i_indptr, chunk_rows: int, device_limit: int, direct_output: bool = False):
+def plan_host_pass(q_indptr, i_indptr, chunk_rows: int, device_limit: int, direct_output: bool = False,
+                   host_values: str = "f32"):
     """Query-tile and item-batch boundaries of a bulk_cosine_host pass under
     a device limit (host only: runs without a GPU)."""
     lib = _abi.load()
     qp = np.ascontiguousarray(q_indptr, dtype=np.int64)
     ip = np.ascontiguousarray(i_indptr, dtype=np.int64)
+    vt = _HOST_VALUES[host_values]
     nq, ni = ctypes.c_int64(0), ctypes.c_int64(0)
     st = lib.ss_plan_host_pass(qp.ctypes.data, len(qp) - 1, ip.ctypes.data, len(ip) - 1, int(chunk_rows),
-                               int(device_limit), int(bool(direct_output)), None, 0, ctypes.byref(nq),
+                               int(device_limit), int(bool(direct_output)), vt, None, 0, ctypes.byref(nq),
                                None, 0, ctypes.byref(ni))
     if st != _abi.SS_OK:
         raise _abi.SparseCosError(st, "ss_plan_host_pass: " + lib.ss_status_string(st).decode())
     qb = np.zeros(nq.value + 1, dtype=np.int64)
     ib = np.zeros(ni.value + 1, dtype=np.int64)
     st = lib.ss_plan_host_pass(qp.ctypes.data, len(qp) - 1, ip.ctypes.data, len(ip) - 1, int(chunk_rows),
-                               int(device_limit), int(bool(direct_output)), qb.ctypes.data, len(qb),
+                               int(device_limit), int(bool(direct_output)), vt, qb.ctypes.data, len(qb),
                                ctypes.byref(nq), ib.ctypes.data, len(ib), ctypes.byref(ni))
     if st != _abi.SS_OK:
         raise _abi.SparseCosError(st, "ss_plan_host_pass: " + lib.ss_status_string(st).decode())

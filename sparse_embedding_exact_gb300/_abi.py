@@ -26,6 +26,9 @@ SS_ALGO_POSTING_LISTS = 0x2
 SS_ALGO_TILES = 0x8
 SS_ALGO_TENSOR = 0x10
 SS_MAX_CHUNK_ROWS = 65536
+SS_VALUES_F32 = 0
+SS_VALUES_BF16 = 1
+SS_VALUES_F16 = 2
 
 
 class ss_csr(ctypes.Structure):
@@ -65,7 +68,8 @@ SIGNATURES = {
     "ss_stream_checksum": (_I32, [_P, _I64, _P, _P]),
     "ss_bulk_cosine_host": (_I32, [_P, _CSR, _CSR, _P, _I64, ss_chunk_consumer, _P, _I32, _I32]),
     "ss_set_device_limit": (_I32, [_P, _I64]),
-    "ss_plan_host_pass": (_I32, [_P, _I64, _P, _I64, _I32, _I64, _I32, _P, _I64,
+    "ss_set_host_values": (_I32, [_P, _I32]),
+    "ss_plan_host_pass": (_I32, [_P, _I64, _P, _I64, _I32, _I64, _I32, _I32, _P, _I64,
                                  ctypes.POINTER(_I64), _P, _I64, ctypes.POINTER(_I64)]),
     "ss_validate_csr": (_I32, [_P, _CSR, _P]),
     "ss_check_device": (_I32, [_P, _P]),

@@ -153,8 +153,9 @@ struct ss_topk {
 struct ss_host_pass {
   // Device buffers: the query tile (indptr, indices, values, inverse norms),
   // two item batch slots (the same four each), two output tiles.
+  // With 16-bit host values, their staging copies (query tile, item slots).
   enum { kQPtr, kQIdx, kQVal, kInvQ, kIPtr0, kIIdx0, kIVal0, kInvI0, kIPtr1, kIIdx1, kIVal1, kInvI1,
-         kOut0, kOut1, kBuffers };
+         kOut0, kOut1, kQHalf, kIHalf0, kIHalf1, kBuffers };
   static constexpr int kSlotRoles = 4;  // kIPtr1 - kIPtr0
   // comp: norms, builds, scoring; copy: results to the host ring; up: item
   // batches to the device (the next batch while the current one is scored).
@@ -163,6 +164,8 @@ struct ss_host_pass {
   cudaEvent_t batch_ready[2] = {nullptr, nullptr}, batch_free[2] = {nullptr, nullptr};
   // Device bytes the pass may hold for its buffers above (0: no limit).
   int64_t device_limit = 0;
+  // Type of the host CSRs' values (SS_VALUES_F32, _BF16, _F16).
+  int32_t value_type = 0;
   std::vector<cudaEvent_t> copied;  // one per ring slot
   void *buf[kBuffers] = {};
   size_t cap[kBuffers] = {};

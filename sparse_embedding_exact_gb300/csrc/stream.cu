@@ -15,6 +15,7 @@
 // to the caller's consumer.  Events order buffer and slot reuse; every host
 // wait polls its event with a deadline.  Streams, events and buffers stay
 // with the handle between calls.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdarg.h>
 #include <stdio.h>
@@ -123,14 +124,27 @@ __global__ void k_rebase_indptr(int64_t *ptr, int64_t n, int64_t first) {
     ptr[i] -= first;
 }
 
+// 16-bit values widened to float32 (both conversions are exact).
+__global__ void k_widen_values(const uint16_t *__restrict__ src, float *__restrict__ dst, int64_t n,
+                               int32_t type) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint16_t b = src[i];
+    dst[i] = type == SS_VALUES_BF16 ? __uint_as_float((uint32_t)b << 16) : __half2float(__ushort_as_half(b));
+  }
+}
+
 // Bytes the pass holds on the device for a row range of a CSR matrix: indptr
-// (int64), indices and values (4 bytes each), inverse norms (float).
-int64_t range_bytes(int64_t rows, int64_t nnz) { return 8 * (rows + 1) + 8 * nnz + 4 * rows; }
+// (int64), indices and values (4 bytes each), inverse norms (float), and
+// with 16-bit host values their 2-byte staging copy.
+int64_t range_bytes(int64_t rows, int64_t nnz, bool half) {
+  return 8 * (rows + 1) + (half ? 10 : 8) * nnz + 4 * rows;
+}
 
 // Copies rows [r0, r1) of the host CSR m into the buffers of roles
-// base .. base + 2 (grown beforehand) on stream s, and describes the copy.
-ss_status upload_rows(ss_handle *h, const ss_csr *m, int64_t r0, int64_t r1, int base, cudaStream_t s,
-                      ss_csr *view) {
+// base .. base + 2 (grown beforehand; 16-bit values through the staging
+// buffer of role `stage`, then widened) on stream s, and describes the copy.
+ss_status upload_rows(ss_handle *h, const ss_csr *m, int64_t r0, int64_t r1, int base, int stage,
+                      cudaStream_t s, ss_csr *view) {
   ss_host_pass &hp = h->host;
   const int64_t n = r1 - r0, p0 = m->indptr[r0], nnz = m->indptr[r1] - p0;
   int64_t *ptr = static_cast<int64_t *>(hp.buf[base]);
@@ -139,7 +153,16 @@ ss_status upload_rows(ss_handle *h, const ss_csr *m, int64_t r0, int64_t r1, int
   S_CUDA(cudaMemcpyAsync(ptr, m->indptr + r0, sizeof(int64_t) * (size_t)(n + 1), cudaMemcpyHostToDevice, s));
   if (nnz > 0) {
     S_CUDA(cudaMemcpyAsync(idx, m->indices + p0, sizeof(int32_t) * (size_t)nnz, cudaMemcpyHostToDevice, s));
-    S_CUDA(cudaMemcpyAsync(val, m->values + p0, sizeof(float) * (size_t)nnz, cudaMemcpyHostToDevice, s));
+    if (hp.value_type == SS_VALUES_F32) {
+      S_CUDA(cudaMemcpyAsync(val, m->values + p0, sizeof(float) * (size_t)nnz, cudaMemcpyHostToDevice, s));
+    } else {
+      uint16_t *half = static_cast<uint16_t *>(hp.buf[stage]);
+      const uint16_t *src = reinterpret_cast<const uint16_t *>(m->values) + p0;
+      S_CUDA(cudaMemcpyAsync(half, src, sizeof(uint16_t) * (size_t)nnz, cudaMemcpyHostToDevice, s));
+      const int blocks = (int)std::min<int64_t>((nnz + 255) / 256, 8 * (int64_t)h->sm_count);
+      k_widen_values<<<blocks, 256, 0, s>>>(half, val, nnz, hp.value_type);
+      SS_CUDA_LAUNCH(cudaGetLastError());
+    }
   }
   if (p0 != 0) {
     const int blocks = (int)std::min<int64_t>((n + 1 + 255) / 256, 4 * (int64_t)h->sm_count);
@@ -155,13 +178,13 @@ ss_status upload_rows(ss_handle *h, const ss_csr *m, int64_t r0, int64_t r1, int
 // a range of `align` rows or more ends on a multiple of `align` rows after
 // its start, the last one excepted.  bounds = {0, ..., n}.  False when one
 // row alone does not fit.
-bool split_rows(const int64_t *ptr, int64_t n, int64_t cap, int64_t max_rows, int64_t align,
+bool split_rows(const int64_t *ptr, int64_t n, int64_t cap, int64_t max_rows, int64_t align, bool half,
                 std::vector<int64_t> &bounds) {
   bounds.assign(1, 0);
   int64_t r0 = 0;
   auto fits = [&](int64_t r1) {
     const int64_t nnz = ptr[r1] - ptr[r0];
-    return nnz < ((int64_t)1 << 31) && range_bytes(r1 - r0, nnz) <= cap;
+    return nnz < ((int64_t)1 << 31) && range_bytes(r1 - r0, nnz, half) <= cap;
   };
   while (r0 < n) {
     int64_t lo = r0, hi = std::min(n, r0 + max_rows);
@@ -189,7 +212,7 @@ bool split_rows(const int64_t *ptr, int64_t n, int64_t cap, int64_t max_rows, in
 // (one being scored, the next being copied) and are whole multiples of the
 // chunk when a chunk fits.  `why` says what did not fit.
 ss_status plan_pass(const int64_t *qptr, int64_t n_q, const int64_t *iptr, int64_t n_i, int64_t C,
-                    int64_t limit, bool direct, std::vector<int64_t> &qb, std::vector<int64_t> &ib,
+                    int64_t limit, bool direct, bool half, std::vector<int64_t> &qb, std::vector<int64_t> &ib,
                     std::string &why) {
   qb = {0, n_q};
   ib = {0, n_i};
@@ -197,8 +220,8 @@ ss_status plan_pass(const int64_t *qptr, int64_t n_q, const int64_t *iptr, int64
   const int64_t W = std::min(C, n_i);
   auto out_bytes = [&](int64_t rows) { return direct ? (int64_t)0 : 2 * 4 * rows * W; };
   const int64_t nnz_q = qptr[n_q], nnz_i = iptr[n_i], big = (int64_t)1 << 31;
-  const int64_t q_all = range_bytes(n_q, nnz_q) + out_bytes(n_q);
-  if (nnz_q < big && nnz_i < big && q_all + range_bytes(n_i, nnz_i) <= limit) return SS_OK;
+  const int64_t q_all = range_bytes(n_q, nnz_q, half) + out_bytes(n_q);
+  if (nnz_q < big && nnz_i < big && q_all + range_bytes(n_i, nnz_i, half) <= limit) return SS_OK;
   int64_t q_used = q_all;
   if (nnz_q >= big || q_all > limit / 2) {
     const int64_t max_rows = direct ? n_q : (limit / 4) / (8 * W);
@@ -206,18 +229,18 @@ ss_status plan_pass(const int64_t *qptr, int64_t n_q, const int64_t *iptr, int64
       why = "the output tiles of one query row exceed a quarter of the device limit";
       return SS_ERR_LIMIT;
     }
-    if (!split_rows(qptr, n_q, limit / 4, max_rows, 1, qb)) {
+    if (!split_rows(qptr, n_q, limit / 4, max_rows, 1, half, qb)) {
       why = "one query row exceeds a quarter of the device limit";
       return SS_ERR_LIMIT;
     }
     int64_t worst = 0, rows = 0;
     for (size_t t = 0; t + 1 < qb.size(); ++t) {
-      worst = std::max(worst, range_bytes(qb[t + 1] - qb[t], qptr[qb[t + 1]] - qptr[qb[t]]));
+      worst = std::max(worst, range_bytes(qb[t + 1] - qb[t], qptr[qb[t + 1]] - qptr[qb[t]], half));
       rows = std::max(rows, qb[t + 1] - qb[t]);
     }
     q_used = worst + out_bytes(rows);
   }
-  if (!split_rows(iptr, n_i, (limit - q_used) / 2, n_i, C, ib)) {
+  if (!split_rows(iptr, n_i, (limit - q_used) / 2, n_i, C, half, ib)) {
     why = "one item row exceeds half of what the query tiles leave of the device limit";
     return SS_ERR_LIMIT;
   }
@@ -318,18 +341,26 @@ extern "C" ss_status ss_set_device_limit(ss_handle *h, int64_t bytes) {
   return SS_OK;
 }
 
+extern "C" ss_status ss_set_host_values(ss_handle *h, int32_t value_type) {
+  if (!h || (value_type != SS_VALUES_F32 && value_type != SS_VALUES_BF16 && value_type != SS_VALUES_F16))
+    return SS_ERR_INVALID_ARG;
+  h->host.value_type = value_type;
+  return SS_OK;
+}
+
 extern "C" ss_status ss_plan_host_pass(const int64_t *q_indptr, int64_t n_q, const int64_t *i_indptr,
                                        int64_t n_i, int32_t chunk_rows, int64_t device_limit,
-                                       int32_t direct_output, int64_t *q_bounds, int64_t q_cap,
-                                       int64_t *n_q_tiles, int64_t *i_bounds, int64_t i_cap,
+                                       int32_t direct_output, int32_t value_type, int64_t *q_bounds,
+                                       int64_t q_cap, int64_t *n_q_tiles, int64_t *i_bounds, int64_t i_cap,
                                        int64_t *n_i_batches) {
   if (!q_indptr || !i_indptr || n_q < 0 || n_i < 0 || chunk_rows < 1 || device_limit < 0 ||
-      !n_q_tiles || !n_i_batches)
+      !n_q_tiles || !n_i_batches ||
+      (value_type != SS_VALUES_F32 && value_type != SS_VALUES_BF16 && value_type != SS_VALUES_F16))
     return SS_ERR_INVALID_ARG;
   std::vector<int64_t> qb, ib;
   std::string why;
   const ss_status st = plan_pass(q_indptr, n_q, i_indptr, n_i, chunk_rows, device_limit, direct_output != 0,
-                                 qb, ib, why);
+                                 value_type != SS_VALUES_F32, qb, ib, why);
   if (st != SS_OK) return st;
   *n_q_tiles = (int64_t)qb.size() - 1;
   *n_i_batches = (int64_t)ib.size() - 1;
@@ -377,10 +408,11 @@ extern "C" ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *qh, const s
   }
 
   // Query tiles x item batches (one of each unless the device limit says otherwise).
+  const bool half = hp.value_type != SS_VALUES_F32;
   std::vector<int64_t> qb, ib;
   {
     std::string why;
-    st = plan_pass(qh->indptr, n_q, ih->indptr, n_i, C, hp.device_limit, out_dev != nullptr, qb, ib, why);
+    st = plan_pass(qh->indptr, n_q, ih->indptr, n_i, C, hp.device_limit, out_dev != nullptr, half, qb, ib, why);
     if (st != SS_OK)
       return sfail(h, st, "ss_bulk_cosine_host: device limit of %lld bytes: %s", (long long)hp.device_limit,
                    why.c_str());
@@ -395,7 +427,7 @@ extern "C" ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *qh, const s
   // Buffers at their largest size over the tiles and batches, allocated
   // before anything is queued (growing one later would synchronise).
   using HP = ss_host_pass;
-  auto grow_for = [&](const ss_csr *m, const std::vector<int64_t> &bnd, int base, int inv) -> ss_status {
+  auto grow_for = [&](const ss_csr *m, const std::vector<int64_t> &bnd, int base, int inv, int stage) -> ss_status {
     int64_t rows = 0, nnz = 0;
     for (size_t t = 0; t + 1 < bnd.size(); ++t) {
       rows = std::max(rows, bnd[t + 1] - bnd[t]);
@@ -405,11 +437,13 @@ extern "C" ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *qh, const s
     if (s2 == SS_OK) s2 = ensure_buf(h, base + 1, sizeof(int32_t) * (size_t)nnz);
     if (s2 == SS_OK) s2 = ensure_buf(h, base + 2, sizeof(float) * (size_t)nnz);
     if (s2 == SS_OK) s2 = ensure_buf(h, inv, sizeof(float) * (size_t)rows);
+    if (s2 == SS_OK && half) s2 = ensure_buf(h, stage, sizeof(uint16_t) * (size_t)nnz);
     return s2;
   };
-  if ((st = grow_for(qh, qb, HP::kQPtr, HP::kInvQ)) != SS_OK) return st;
+  if ((st = grow_for(qh, qb, HP::kQPtr, HP::kInvQ, HP::kQHalf)) != SS_OK) return st;
   for (int s = 0; s < (n_batches > 1 ? 2 : 1); ++s)
-    if ((st = grow_for(ih, ib, HP::kIPtr0 + s * HP::kSlotRoles, HP::kInvI0 + s * HP::kSlotRoles)) != SS_OK)
+    if ((st = grow_for(ih, ib, HP::kIPtr0 + s * HP::kSlotRoles, HP::kInvI0 + s * HP::kSlotRoles,
+                       HP::kIHalf0 + s)) != SS_OK)
       return st;
   int64_t tile_rows = 0;
   for (int64_t t = 0; t < n_tiles; ++t) tile_rows = std::max(tile_rows, qb[t + 1] - qb[t]);
@@ -510,7 +544,8 @@ extern "C" ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *qh, const s
   auto upload_batch = [&](int64_t k) -> ss_status {
     const int s = (int)(k & 1);
     if (k >= 2) S_CUDA(cudaStreamWaitEvent(hp.up, hp.batch_free[s], 0));
-    ss_status s2 = upload_rows(h, ih, ib[k], ib[k + 1], HP::kIPtr0 + s * HP::kSlotRoles, hp.up, &iv[s]);
+    ss_status s2 = upload_rows(h, ih, ib[k], ib[k + 1], HP::kIPtr0 + s * HP::kSlotRoles, HP::kIHalf0 + s, hp.up,
+                               &iv[s]);
     if (s2 != SS_OK) return s2;
     S_CUDA(cudaEventRecord(hp.batch_ready[s], hp.up));
     return SS_OK;
@@ -534,7 +569,7 @@ extern "C" ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *qh, const s
     for (int64_t t = 0; t < n_tiles; ++t) {
       if (k == 0 || n_tiles > 1) {
         // The tile's buffers were last read by scoring calls queued earlier on comp.
-        if ((st = upload_rows(h, qh, qb[t], qb[t + 1], HP::kQPtr, hp.comp, &qv)) != SS_OK) return st;
+        if ((st = upload_rows(h, qh, qb[t], qb[t + 1], HP::kQPtr, HP::kQHalf, hp.comp, &qv)) != SS_OK) return st;
         invalidate_queries(h);
         if ((st = ss_row_norms(h, &qv, inv_q, vs)) != SS_OK) return st;
       }

@@ -723,6 +723,52 @@ def test_bulk_cosine_host_limit_with_consumer_and_checksums(sec):
         assert bits == int(t.view(np.uint32).astype(np.uint64).sum(dtype=np.uint64))
 
 
+# --------------------------------------------- reduced-precision host values
+@pytest.mark.parametrize("kind", ["bf16", "f16"])
+@pytest.mark.parametrize("limit", [0, 32 * 100 * 512])
+def test_bulk_cosine_host_with_16_bit_values(sec, kind, limit):
+    # The 16-bit values are widened exactly on the device, so without a limit
+    # the pass equals the float32 pass on the widened values bit for bit;
+    # against the unrounded values the input rounding costs at most 2 asin(u).
+    import math
+
+    from workload.generate import CsrBatch
+    from workload.halfprec import (UNIT_ROUNDOFF, bf16_bits_to_f32, f16_bits_to_f32, to_bf16_bits,
+                                   to_f16_bits)
+
+    cfg, Q, I, ref = _limit_case(sec)
+
+    def halves(m):
+        if kind == "bf16":
+            bits = to_bf16_bits(m.values)
+            return CsrBatch(m.indptr, m.indices, bits, m.dim), CsrBatch(m.indptr, m.indices,
+                                                                       bf16_bits_to_f32(bits), m.dim)
+        bits = to_f16_bits(m.values)  # given as float16, the numpy type
+        return (CsrBatch(m.indptr, m.indices, bits.view(np.float16), m.dim),
+                CsrBatch(m.indptr, m.indices, f16_bits_to_f32(bits), m.dim))
+
+    (Qh, Qw), (Ih, Iw) = halves(Q), halves(I)
+    with sec.SparseCosine(cfg.dim, chunk_rows=512) as h:
+        h.set_device_limit(limit)
+        got = np.full((Q.n_rows, I.n_rows), np.nan, np.float32)
+        h.bulk_cosine_host(Qh, Ih, out=got, ring_depth=3, host_values=kind)
+        wide = np.full_like(got, np.nan)
+        h.bulk_cosine_host(Qw, Iw, out=wide, ring_depth=3)
+        pinned = torch.full((Q.n_rows, I.n_rows), float("nan"), dtype=torch.float32).pin_memory()
+        h.bulk_cosine_host(Qh, Ih, out=pinned, ring_depth=2, host_values=kind)
+        with pytest.raises(TypeError):  # float32 arrays are not 16-bit values
+            h.bulk_cosine_host(Q, I, out=got, host_values=kind)
+    if limit == 0:
+        assert np.array_equal(got.view(np.int32), wide.view(np.int32))
+        assert np.array_equal(pinned.numpy().view(np.int32), wide.view(np.int32))
+    # (under a limit the 2-byte staging copies change the batches, and each
+    # batch takes its own hot set: equal within the accuracy bar, not bitwise)
+    ref_wide = oracle.cosine(Qw, Iw)
+    for res in (got, wide, pinned.numpy()):
+        assert _max_err(res, ref_wide) <= TOL
+    assert _max_err(got, ref) <= 2 * math.asin(UNIT_ROUNDOFF[kind]) + TOL
+
+
 # ------------------------------------------------------------- checksums
 def test_device_checksum_matches_host_checksum(sec):
     rng = np.random.default_rng(9)
