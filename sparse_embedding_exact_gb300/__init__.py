@@ -8,8 +8,12 @@ and raises if the library is missing.
     S[q, i] = (Q_q . I_i) / (|Q_q|_2 |I_i|_2)
 
 The calls mirror the C ABI: ``row_norms``, ``build_item_index``,
-``score_chunk``, ``score_all`` (the device-resident chunk loop) and
-``bulk_cosine_host`` (host buffers in, result streamed back chunk by chunk).
+``score_chunk``, ``score_all`` (the device-resident chunk loop),
+``topk_all`` / ``score_chunk_topk`` (the k best items per query row instead
+of the matrix) and ``bulk_cosine_host`` (host buffers in, result streamed
+back chunk by chunk; ``set_device_limit`` bounds its device memory, with
+item batches streamed and queries tiled, see ``plan_host_pass``; 16-bit
+host values with ``host_values="bf16"`` or ``"f16"``).
 """
 from __future__ import annotations
 

@@ -7,6 +7,8 @@
 
 #include <algorithm>
 #include <chrono>
+#include <map>
+#include <mutex>
 #include <new>
 #include <string>
 #include <thread>
@@ -330,6 +332,20 @@ bool owns_index(const ss_handle *h, const ss_index *idx) {
 }
 
 }  // namespace
+
+cudaError_t ensure_dyn_smem(const void *kernel, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void *, int>, size_t> raised;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t &have = raised[{kernel, dev}];
+  if (have >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
 
 void prof_mark(ss_handle *h, cudaStream_t s) {
   if (!h->prof_on) return;

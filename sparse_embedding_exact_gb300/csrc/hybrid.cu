@@ -1658,15 +1658,10 @@ cudaError_t launch_hot_select(ss_handle *h, const ss_csr &items, cudaStream_t s,
     if (e != cudaSuccess) return e;
   } else {
     const size_t smem = sizeof(int) * 2 * kSelSlots;
-    static bool configured = false;
-    if (!configured) {
-      cudaError_t e = cudaFuncSetAttribute(k_hot_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
-      if (e != cudaSuccess) return e;
-      configured = true;
-    }
+    cudaError_t e = ensure_dyn_smem(k_hot_select, smem);
+    if (e != cudaSuccess) return e;
     k_hot_select<<<1, kSelThreads, smem, s>>>(items.indptr, items.indices, n, n_sample, h->hot);
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     *queued = 1;
   }
@@ -1690,12 +1685,7 @@ cudaError_t launch_build_hybrid(ss_handle *h, const ss_csr &items, int64_t row_b
   if (n_chunks < 1 || n_chunks > h->build_batch || n_tiles > h->max_tiles) return cudaErrorInvalidValue;
   cudaError_t e = cudaMemsetAsync(h->counters, 0, sizeof(int32_t) * (1 + (size_t)n_chunks * (1 + T)), s);
   if (e != cudaSuccess) return e;
-  static bool configured = false;
-  if (!configured) {
-    e = cudaFuncSetAttribute(k_build_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize, kBuildSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  if ((e = ensure_dyn_smem(k_build_tiles, kBuildSmem)) != cudaSuccess) return e;
   k_build_tiles<<<n_tiles, kBThreads, kBuildSmem, s>>>(
       items.indptr, items.indices, items.values, row_begin, row_end, h->hot, h->slab, h->ell,
       h->meta, h->heavy_k, h->heavy_v, h->heavy_item, h->counters, h->heavy_cap, h->image,
@@ -1788,19 +1778,12 @@ cudaError_t launch_score_hybrid(ss_handle *h, const ss_csr &queries, const float
                                 int64_t ld_out, cudaStream_t s, int *queued, const ss_topk *topk) {
   *queued = 0;
   if (queries.n_rows == 0 || idx.n_items == 0) return cudaSuccess;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_score_hybrid, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kScoreSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_score_tiles<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFastSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_score_tiles<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFastSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_dyn_smem(k_score_hybrid, kScoreSmem);
+  if (e == cudaSuccess) e = ensure_dyn_smem(k_score_tiles<false>, kFastSmem);
+  if (e == cudaSuccess) e = ensure_dyn_smem(k_score_tiles<true>, kFastSmem);
+  if (e != cudaSuccess) return e;
   int prep = 0;
-  cudaError_t e = prepare_queries(h, queries, s, &prep);
+  e = prepare_queries(h, queries, s, &prep);
   if (e != cudaSuccess) return e;
   const int64_t n_qtiles = (queries.n_rows + kTQ - 1) / kTQ;
   const int vec_ok = ((reinterpret_cast<uintptr_t>(out) % 16) == 0) && (ld_out % 4 == 0);

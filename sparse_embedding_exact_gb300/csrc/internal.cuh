@@ -316,6 +316,14 @@ void invalidate_queries(ss_handle *h);
 // (called just before and just after each scoring-kernel launch).
 void prof_mark(ss_handle *h, cudaStream_t s);
 
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device, once per kernel and device; callable from several threads.
+cudaError_t ensure_dyn_smem(const void *kernel, size_t bytes);
+template <typename K>
+cudaError_t ensure_dyn_smem(K *kernel, size_t bytes) {
+  return ensure_dyn_smem(reinterpret_cast<const void *>(kernel), bytes);
+}
+
 // Launchers (all asynchronous on `s`).
 cudaError_t launch_row_norms(const ss_csr &m, float *inv_norms, int sm_count, cudaStream_t s);
 cudaError_t launch_validate_csr(const ss_csr &m, int32_t *d_status, int sm_count, cudaStream_t s);

@@ -739,12 +739,7 @@ cudaError_t launch_score_lists(ss_handle *h, const ss_csr &queries, const float 
   // One window covers the chunk unless it is wider than kWindowMax items.
   const bool windowed = a.n_items > a.window;
   auto kernel = windowed ? k_score_lists<true> : k_score_lists<false>;
-  static size_t configured[2] = {0, 0};
-  if (configured[windowed] < smem) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured[windowed] = smem;
-  }
+  if ((e = ensure_dyn_smem(kernel, smem)) != cudaSuccess) return e;
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kPThreads, smem);
   if (e != cudaSuccess) return e;

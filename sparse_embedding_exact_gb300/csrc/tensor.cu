@@ -1356,14 +1356,7 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     ld_dst = n_items;
   }
   {
-    static bool configured = false;
-    const size_t smem = score_smem_bytes(kHotMax);
-    if (!configured) {
-      if ((e = cudaFuncSetAttribute(k_tc_score, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-          cudaSuccess)
-        return e;
-      configured = true;
-    }
+    if ((e = ensure_dyn_smem(k_tc_score, score_smem_bytes(kHotMax))) != cudaSuccess) return e;
     ScoreArgs sa;
     sa.A = h->tc_A;
     sa.B = h->tc_B;
