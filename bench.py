@@ -60,6 +60,8 @@ def parse_args():
                         "in place of storing the full matrix; reported under 'topk'")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target seconds of oracle work for the CPU baseline sample")
+    p.add_argument("--ref-seconds", type=float, default=10.0,
+                   help="target seconds of oracle work per step of the reference arm")
     p.add_argument("--n-queries", type=int, default=0,
                    help="use only the first N query rows (small profiling captures)")
     p.add_argument("--n-items", type=int, default=0,
@@ -227,12 +229,12 @@ def run_reference(args):
 
     oracle.build()
     cores = host_cores()
-    # each step ~10 s of oracle work on all cores, so K + W steps end in minutes
+    # each step ~ref_seconds (10 s) of oracle work on all cores, so K + W steps end in minutes
     probe_rows = sample_query_rows(cfg.n_q, 2, cfg.seed + 1)
     t0 = time.perf_counter()
     oracle.cosine(Q, I, q_rows=probe_rows, threads=2)
     per_row = max(time.perf_counter() - t0, 1e-4)
-    k = int(max(1, min(cfg.n_q, 10.0 * cores / per_row)))
+    k = int(max(1, min(cfg.n_q, args.ref_seconds * cores / per_row)))
     rows = sample_query_rows(cfg.n_q, min(cfg.n_q, 4 * k), cfg.seed)
     times = []
     for s in range(args.warmup + args.steps):
