@@ -57,3 +57,23 @@ def test_input_rounding_stays_within_the_bound(kind):
     err = float(np.abs(rounded - exact).max())
     assert err <= bound
     assert err > 0.0  # the rounding does change the scores
+
+
+def test_binding_takes_16_bit_values_only_as_declared():
+    sec = pytest.importorskip("sparse_embedding_exact_gb300")
+    from sparse_embedding_exact_gb300 import _host_csr
+
+    cfg = CONFIGS["d65k_q1k_i10k"]
+    m = generate_rows(cfg, 0, 0, 20)
+    _, keep = _host_csr(m)  # float32 by default
+    assert keep[2].dtype == np.float32
+    bits = to_bf16_bits(m.values)
+    _, keep = _host_csr(CsrBatch(m.indptr, m.indices, bits, m.dim), "bf16")
+    assert keep[2].dtype == np.uint16 and np.array_equal(keep[2], bits)  # passed through untouched
+    h16 = m.values.astype(np.float16)
+    _, keep = _host_csr(CsrBatch(m.indptr, m.indices, h16, m.dim), "f16")
+    assert np.array_equal(keep[2], h16.view(np.uint16))
+    for kind, vals in (("bf16", m.values), ("bf16", h16), ("f16", m.values)):
+        with pytest.raises(TypeError):
+            _host_csr(CsrBatch(m.indptr, m.indices, vals, m.dim), kind)
+    assert sec._HOST_VALUES == {"f32": 0, "bf16": 1, "f16": 2}
