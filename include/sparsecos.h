@@ -198,7 +198,10 @@ ss_status ss_build_item_indexes(ss_handle *h, const ss_csr *items, int64_t row_b
  *   out[q * ld_out + i], i in [0, items->n_rows).
  * inv_q / inv_i: device norms from ss_row_norms.  out: device float32 with
  * ld_out >= items->n_rows.  Equivalent to calling ss_build_item_index and
- * ss_score_chunk per chunk in order on `stream`.
+ * ss_score_chunk per chunk in order on `stream`.  No rows: SS_OK, no work.
+ * Errors: SS_ERR_INVALID_ARG (null or mismatched arguments, ld_out too
+ * small), and those of ss_build_item_index and ss_score_chunk; device-side
+ * checks surface at the next ss_check_device.
  */
 ss_status ss_score_all(ss_handle *h, const ss_csr *queries, const float *inv_q,
                        const ss_csr *items, const float *inv_i, float *out, int64_t ld_out,
@@ -389,19 +392,25 @@ ss_status ss_check_device(ss_handle *h, void *stream);
  * chosen for an item matrix and the prepared query matrix.  The handle keys
  * both on the arrays' addresses and sizes, so call this after changing the
  * contents of a matrix in place; the next calls recompute them.  No GPU work.
+ * Errors: SS_ERR_INVALID_ARG (null handle).
  */
 ss_status ss_invalidate(ss_handle *h);
 
 /*
  * Diagnostics for an index built by ss_build_item_index.  Synchronises
  * `stream` and writes stats[0..7]:
- *   [0] algorithm (0 = hybrid, 1 = posting lists)  [1] items in the chunk
- *   [2] item tiles (hybrid)                         [3] hot dimensions H (posting
- *                                                       lists: those split off)
+ *   [0] algorithm (0 = item tiles,                  [1] items in the chunk
+ *       1 = posting lists, 2 = tensor path)
+ *   [2] item tiles (item tiles)                     [3] hot dimensions H (posting
+ *                                                       lists: those split off;
+ *                                                       tensor: on the tensor cores)
  *   [4] entries in the heavy-item list              [5] widest ELL column
  *   [6] ELL entries stored, padding included        [7] item tiles without an
- *       (posting lists: entries in the chunk)           inverted-index image
- * Fields that do not apply to the algorithm are 0.
+ *       (posting lists: entries in the chunk;           inverted-index image
+ *       tensor: cold entries in the chunk)
+ * Fields that do not apply to the algorithm are 0.  Errors:
+ * SS_ERR_INVALID_ARG (null handle or stats, an index that is not one of the
+ * handle's current ones), SS_ERR_CUDA.
  */
 ss_status ss_index_stats(ss_handle *h, const ss_index *idx, int64_t *stats, void *stream);
 
@@ -441,7 +450,8 @@ ss_status ss_cosine_chunk_noalloc(const ss_csr *queries, const ss_csr *items, in
                                   void *stream);
 
 /* Number of kernels this handle has launched so far (every call that
- * queues kernels adds the number it queued).  Host-side count; no sync. */
+ * queues kernels adds the number it queued).  Host-side count; no sync; 0
+ * for a null handle. */
 uint64_t ss_kernel_launches(const ss_handle *h);
 
 /* Timing of the scoring kernel itself (k_tc_score, k_score_tiles or
@@ -449,17 +459,21 @@ uint64_t ss_kernel_launches(const ss_handle *h);
  * records a CUDA event just before and just after its scoring kernel, on
  * the caller's stream; the other kernels of the call (operand preparation,
  * cold records, query preparation) fall outside the pair.  Turning it on or
- * off forgets the pairs recorded so far.  No synchronisation. */
+ * off forgets the pairs recorded so far.  No synchronisation.  Errors:
+ * SS_ERR_INVALID_ARG (null handle). */
 ss_status ss_profile_scorer(ss_handle *h, int32_t on);
 
 /* Sum of the recorded pairs' elapsed times in milliseconds and their count,
- * then forgets them.  Synchronises on the last recorded event. */
+ * then forgets them.  Synchronises on the last recorded event.  Errors:
+ * SS_ERR_INVALID_ARG (null pointers), SS_ERR_CUDA. */
 ss_status ss_scorer_time(ss_handle *h, double *total_ms, int64_t *launches);
 
-/* Frees the handle and its device workspace (synchronises the device). */
+/* Frees the handle and its device workspace (synchronises the device).
+ * Errors: SS_ERR_INVALID_ARG (null handle). */
 ss_status ss_destroy(ss_handle *h);
 
-/* Static text for a status code. */
+/* Static text for a status code ("unknown status" for other values; never
+ * NULL). */
 const char *ss_status_string(ss_status s);
 
 /* Message of the last error on the handle ("" if none); valid until the
