@@ -84,3 +84,42 @@ def test_product_does_not_import_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"\b(import|from)\s+oracle\b", text), f
                 assert "cosine_oracle" not in text, f
+
+
+def test_header_is_plain_c_and_every_call_links(lib, tmp_path):
+    # A C99 program (no C++ anywhere) that takes the address of every declared
+    # call, links against the library and runs the calls that need no device.
+    import shutil
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    from sparse_embedding_exact_gb300 import _abi
+
+    names = declared_functions()
+    src = tmp_path / "abi_check.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <string.h>\n#include "sparsecos.h"\n'
+        "typedef void (*fn)(void);\n"
+        "static const fn calls[] = {\n" + "".join(f"  (fn){n},\n" for n in names) + "};\n"
+        "int main(void) {\n"
+        "  size_t i;\n"
+        "  for (i = 0; i < sizeof(calls) / sizeof(calls[0]); ++i) if (!calls[i]) return 2;\n"
+        "  for (i = 0; i <= 9; ++i) if (!ss_status_string((ss_status)i)) return 3;\n"
+        "  if (ss_destroy(NULL) != SS_ERR_INVALID_ARG) return 4;\n"
+        "  if (ss_invalidate(NULL) != SS_ERR_INVALID_ARG) return 5;\n"
+        "  if (ss_kernel_launches(NULL) != 0) return 6;\n"
+        "  if (strcmp(ss_last_error(NULL), \"\") != 0) return 7;\n"
+        "  if (ss_set_device_limit(NULL, 0) != SS_ERR_INVALID_ARG) return 8;\n"
+        "  printf(\"%d calls\\n\", (int)(sizeof(calls) / sizeof(calls[0])));\n"
+        "  return 0;\n}\n")
+    exe = tmp_path / "abi_check"
+    libdir = os.path.dirname(_abi.library_path())
+    libname = os.path.basename(_abi.library_path())[3:-3]  # libX.so -> X
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I", os.path.join(ROOT, "include"), str(src), "-L", libdir, "-l" + libname,
+                        "-Wl,-rpath," + libdir, "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert r.stdout.strip() == f"{len(names)} calls"
