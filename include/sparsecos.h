@@ -67,12 +67,15 @@ typedef int32_t ss_status;
  *    rows.  Needs inverse norms whose products bound the scores by 1 (those
  *    of ss_row_norms); larger normalised products end the call with
  *    SS_ERR_DEVICE_CHECK.
- * With neither flag the handle chooses per item matrix: its first build is a
- * tiled one, and if more than half of the item tiles found no room for their
- * inverted index the matrix is rebuilt, and afterwards always built, as
- * posting lists (one synchronisation per item matrix).  Both give the
- * cosines within a few float32 roundings; each is bitwise deterministic.
- * Setting both flags is SS_ERR_INVALID_ARG. */
+ * With no algorithm flag the handle chooses per item matrix, once (one
+ * synchronisation per item matrix): the tensor path (SS_ALGO_TENSOR below)
+ * when a row sample of the matrix has at least 64 frequent ("hot")
+ * dimensions and leaves at most 0.25 expected shared dimensions per pair
+ * outside them; otherwise posting lists when more than half of the first
+ * build's item tiles found no room for their inverted index, else item
+ * tiles.  Every algorithm gives the cosines within 2e-6 of the exact ones
+ * and is bitwise deterministic.  Setting more than one flag is
+ * SS_ERR_INVALID_ARG. */
 #define SS_ALGO_POSTING_LISTS 0x2
 #define SS_ALGO_TILES 0x8
 /* Tensor-core path: the (at most 128) dimensions held by the largest share of
@@ -85,10 +88,7 @@ typedef int32_t ss_status;
  * for any chunking.  Best when the rows share a Zipf-like head of frequent
  * dimensions (BM25/TF-IDF text).  Needs inverse norms of the rows (those of
  * ss_row_norms): a normalised value above 1 + 2^-10 or a normalised row whose
- * squares sum above 1 + 2^-6 ends the call with SS_ERR_DEVICE_CHECK.  The
- * cold products of one scoring call are kept on the device in a buffer
- * sized from the row sample (2.5 times the estimated count plus 4M); a call
- * that needs more reports SS_ERR_DEVICE_CHECK at the next status read.
+ * squares sum above 1 + 2^-6 ends the call with SS_ERR_DEVICE_CHECK.
  * The query side is prepared once per query matrix, inverse-norm array and
  * item matrix: changing the contents of either array under the same
  * pointers needs ss_invalidate.  Exclusive with the two flags above. */
@@ -160,9 +160,11 @@ ss_status ss_build_item_index(ss_handle *h, const ss_csr *items, int64_t row_beg
  * queries: device CSR; inv_q: device float32[n_q] from ss_row_norms;
  * inv_i: device float32 pointer to the chunk's first item norm (the item
  * norm array + row_begin); out: device float32, row-major with leading
- * dimension ld_out >= chunk width.  Tiled indexes: float32 products and
- * sums; posting-list indexes: exact fixed-point sums of float32 products of
- * the normalised values (see SS_ALGO_POSTING_LISTS).
+ * dimension ld_out >= chunk width.  Item tiles: float32 products and sums;
+ * posting lists: exact fixed-point sums of float32 products of the
+ * normalised values (see SS_ALGO_POSTING_LISTS); tensor path: split-fp16
+ * tensor-core product of the hot dimensions plus exact fixed-point sums of
+ * the others (see SS_ALGO_TENSOR).  All within 2e-6 of the exact cosine.
  * Errors: SS_ERR_INVALID_ARG, SS_ERR_CUDA.
  */
 ss_status ss_score_chunk(ss_handle *h, const ss_csr *queries, const float *inv_q,
@@ -300,7 +302,12 @@ ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *queries_host,
  * one the 2-byte staging copies can change the item batches, and each batch
  * takes its own hot dimensions: equal within 2e-6 then).  Against the cosines of the unrounded values the
  * input rounding adds at most 2 asin(u) (u = 2^-9 for bfloat16, 2^-11 for
- * binary16, round-to-nearest inputs).  Values must be finite.  The setting
+ * binary16, round-to-nearest inputs).  The post allows 16-bit data where an
+ * error below 1e-3 is acceptable (section 5.3): binary16 meets that bar
+ * (at most 9.8e-4, measured 2.3e-4); bfloat16 is OUTSIDE it (measured up
+ * to 1.8e-3 on the 1.2M-dimension workload) and is offered only for data
+ * already stored as bfloat16, whose scores are then exact for the values as
+ * stored.  Neither is ever a default.  Values must be finite.  The setting
  * stays with the handle; SS_VALUES_F32 (the default) restores float32.
  * Errors: SS_ERR_INVALID_ARG (null handle, unknown type).
  */
@@ -381,9 +388,11 @@ ss_status ss_stream_checksum(const ss_handle *h, int64_t chunk, uint64_t *bits_s
 ss_status ss_validate_csr(ss_handle *h, const ss_csr *m, void *stream);
 
 /*
- * Synchronises `stream` and reports whether a kernel of this handle flagged
- * an input it could not use (SS_ERR_DEVICE_CHECK, e.g. a chunk whose nnz
- * exceeds the index capacity), then clears the flag.
+ * Synchronises `stream` (and the streams of the handle's host pass, which
+ * may still run work of a pass that returned early, e.g. on SS_ERR_TIMEOUT)
+ * and reports whether a kernel of this handle flagged an input it could not
+ * use (SS_ERR_DEVICE_CHECK, e.g. a chunk whose nnz exceeds the index
+ * capacity), then clears the flag.
  */
 ss_status ss_check_device(ss_handle *h, void *stream);
 
@@ -414,45 +423,109 @@ ss_status ss_invalidate(ss_handle *h);
  */
 ss_status ss_index_stats(ss_handle *h, const ss_index *idx, int64_t *stats, void *stream);
 
+/*
+ * Reads a chunk index built as posting lists or for the tensor path back
+ * into host memory, in one form for both: the chunk's CSR (item rows
+ * [row_begin, row_end) of the item matrix) turned into lists by dimension
+ * (a CSC of the chunk), with the frequent ("hot") dimensions that the index
+ * holds dense instead of in lists given apart.  For tests and inspection;
+ * synchronises `stream`.  Outputs (host memory; any may be NULL):
+ *   *n_hot, hot[0 .. *n_hot): the dense dimensions, ascending
+ *     (*n_hot <= SS_EXPORT_HOT_MAX; 0 when the index keeps every dimension
+ *     in lists);
+ *   hot_values[i * SS_EXPORT_HOT_MAX + j] = value of dimension hot[j] in
+ *     chunk item i (0 where the item lacks it), i < row_end - row_begin;
+ *     the rest of each row of SS_EXPORT_HOT_MAX is 0;
+ *   col_ptr[0 .. dim]: the list of dimension k is entries
+ *     [col_ptr[k], col_ptr[k + 1]) (col_ptr[0] = 0; hot dimensions have
+ *     empty lists);
+ *   item[e], value[e], e < *n_entries: chunk item (0-based) and stored value
+ *     of entry e; inside a list the items ascend (the device keeps them in
+ *     no particular order, which none of its sums depends on; they are
+ *     sorted here).  item and value need capacity >= *n_entries.
+ * Errors: SS_ERR_INVALID_ARG (not an index of this handle, an item-tile
+ * index, negative capacity), SS_ERR_LIMIT (capacity too small; *n_entries
+ * is still written), SS_ERR_DEVICE_CHECK (list offsets outside the index),
+ * SS_ERR_CUDA.
+ */
+#define SS_EXPORT_HOT_MAX 128
+ss_status ss_index_export(ss_handle *h, const ss_index *idx, int32_t *n_hot, int32_t *hot,
+                          float *hot_values, int32_t *col_ptr, int32_t *item, float *value,
+                          int64_t capacity, int64_t *n_entries, void *stream);
+
 /* Size of the fixed scratch array behind ss_cosine_chunk_noalloc. */
 #define SS_NOALLOC_SCRATCH_BYTES (32u << 20)
 
+/* Codes a kernel leaves in a device status word (the first problem found
+ * wins; 0 = none).  ss_check_device reads the handle's own word and turns a
+ * nonzero code into SS_ERR_DEVICE_CHECK; ss_cosine_chunk_noalloc hands its
+ * word to the caller. */
+#define SS_DEVICE_OK 0
+#define SS_DEVICE_UNSORTED 1     /* indices not strictly increasing in a row */
+#define SS_DEVICE_OUT_OF_RANGE 2 /* an index outside [0, dim) */
+#define SS_DEVICE_CAPACITY 3     /* more list entries than the space given for them */
+#define SS_DEVICE_STALL 4        /* a bounded wait inside a kernel ran out */
+#define SS_DEVICE_RANGE 5        /* inverse norms that are not the rows' own */
+
 /*
- * For callers that cannot allocate device memory (a host whose memory pool
- * owns the whole GPU, a CUDA graph capture in progress, a plug-in with a
- * fixed memory budget).  The paper has no counterpart: it is a packaging of
- * the same computation.
+ * Scores one item chunk for callers that cannot allocate device memory.
+ * Such callers exist: code running inside a host whose memory pool owns the
+ * whole GPU (a serving runtime or framework allocator that forbids foreign
+ * cudaMalloc calls), code called while a CUDA graph is being captured (an
+ * allocation then fails or breaks the capture), and plug-ins given a fixed
+ * memory budget up front.  The paper has no counterpart: this is a
+ * packaging of the same computation.
  *
  *   out[q * ld_out + c] = cos(Q_q, I_{row_begin + c}),  c < row_end - row_begin
  *
- * for every query row, computed with the posting-list kernels.  Needs no
- * handle and calls no cudaMalloc, cudaFree or allocating library routine:
- * all scratch (both norm vectors, the chunk's per-dimension counters and
- * list offsets, the posting lists) comes from one static device array of
- * SS_NOALLOC_SCRATCH_BYTES that every GPU loading this library holds until
- * the process exits.  The caller passes the inputs and the output, all in
- * device memory of the current device; `stream` as in the other calls.
+ * for every query row, computed with the posting-list kernels (see
+ * SS_ALGO_POSTING_LISTS for the arithmetic).  Needs no handle and calls no
+ * cudaMalloc, cudaFree or allocating library routine: all scratch (both norm
+ * vectors, the chunk's per-dimension counters and list offsets, the posting
+ * lists) comes from one static device array of SS_NOALLOC_SCRATCH_BYTES that
+ * every GPU loading this library holds until the process exits.  The caller
+ * passes the inputs and the output, all in device memory of the current
+ * device; `stream` as in the other calls.
  *   chunk_nnz: the number of nonzeros in item rows [row_begin, row_end)
  *   (indptr[row_end] - indptr[row_begin]), known to the caller; the lists
- *   are sized by it (a smaller value truncates them on the device).
- * Returns SS_ERR_LIMIT, without queueing work, when the scratch needed
- * (about 8 * (dim + 1) + 14 * chunk_nnz + 4 * (n_q + chunk rows) bytes)
- * exceeds SS_NOALLOC_SCRATCH_BYTES or the chunk exceeds SS_MAX_CHUNK_ROWS.
- * The first call on a device looks up the array's device address (no
- * allocation); make that first call before any stream capture.  Every call
- * shares the one array and it keeps the last call's contents (each call
- * clears what must start at zero): calls that overlap on the GPU, on
- * different streams or host threads, race and corrupt each other's results;
- * order them on one stream.
+ *   are sized by it.
+ *   device_status: device int32 or NULL.  The call sets it to SS_DEVICE_OK
+ *   on `stream`, and its kernels then leave there the first problem they
+ *   find: SS_DEVICE_CAPACITY when chunk_nnz is below the chunk's real count
+ *   (the lists were cut short and the scores are wrong),
+ *   SS_DEVICE_OUT_OF_RANGE for an index outside [0, dim).  Read it once
+ *   `stream` has run the call's work.  With NULL such problems go unreported.
+ * Returns SS_ERR_INVALID_ARG or SS_ERR_LIMIT without queueing work: the
+ * latter when the scratch needed (about 8 * (dim + 1) + 14 * chunk_nnz +
+ * 4 * (n_q + chunk rows) bytes) exceeds SS_NOALLOC_SCRATCH_BYTES or the
+ * chunk exceeds SS_MAX_CHUNK_ROWS.  The first call on a device looks up the
+ * array's device address (no allocation) and keeps it for the life of the
+ * process: make that first call before any stream capture, use the device's
+ * primary context (the runtime's default), and do not call it again after a
+ * cudaDeviceReset.  Every call shares the one array and it keeps the last
+ * call's contents (each call clears what must start at zero): calls that
+ * overlap on the GPU, on different streams or host threads, race and corrupt
+ * each other's results; order them on one stream.
  */
 ss_status ss_cosine_chunk_noalloc(const ss_csr *queries, const ss_csr *items, int64_t row_begin,
                                   int64_t row_end, int64_t chunk_nnz, float *out, int64_t ld_out,
-                                  void *stream);
+                                  int32_t *device_status, void *stream);
 
 /* Number of kernels this handle has launched so far (every call that
  * queues kernels adds the number it queued).  Host-side count; no sync; 0
  * for a null handle. */
 uint64_t ss_kernel_launches(const ss_handle *h);
+
+/* Testing hook for failure handling: makes the nth device or page-locked
+ * host allocation that the library makes from now on (counting every
+ * handle and thread; nth >= 1) fail as if the memory were exhausted, once;
+ * nth <= 0 disarms it.  The call that meets the failure returns
+ * SS_ERR_OOM, after which the handle has waited for its device and freed
+ * every buffer it allocates on demand: it stays usable and allocates them
+ * again on its next call.  Returns how many allocations were still to go
+ * before the previous arming fired (0: none was armed, or it has fired).
+ * Host only; no synchronisation. */
+int64_t ss_inject_alloc_failure(int64_t nth);
 
 /* Timing of the scoring kernel itself (k_tc_score, k_score_tiles or
  * k_score_lists, whichever the index uses).  While on, every scoring call

@@ -339,6 +339,32 @@ class SparseCosine:
                 "ell_entries", "tiles_without_image")
         return {k: int(out[j]) for j, k in enumerate(keys)}
 
+    def index_export(self, index, stream=None) -> dict:
+        """The chunk index read back as host arrays (posting lists or tensor
+        path; synchronises): "hot" (dense dimensions, ascending),
+        "hot_values" (items x len(hot)), and the lists of the other
+        dimensions as a CSC of the chunk: "col_ptr" (dim + 1), "item" and
+        "value" (items ascending inside each list)."""
+        lib = self._lib
+        n_hot = ctypes.c_int32(0)
+        n = ctypes.c_int64(0)
+        self._check(lib.ss_index_export(self._h, index, None, None, None, None, None, None, 0,
+                                        ctypes.byref(n), _stream_ptr(stream)), "ss_index_export")
+        stats = self.index_stats(index, stream)
+        n_items = stats["items"]
+        hot = np.zeros(_abi.SS_EXPORT_HOT_MAX, np.int32)
+        hot_values = np.zeros((n_items, _abi.SS_EXPORT_HOT_MAX), np.float32)
+        col_ptr = np.zeros(self.dim + 1, np.int32)
+        item = np.zeros(max(1, n.value), np.int32)
+        value = np.zeros(max(1, n.value), np.float32)
+        self._check(lib.ss_index_export(self._h, index, ctypes.byref(n_hot), hot.ctypes.data,
+                                        hot_values.ctypes.data, col_ptr.ctypes.data, item.ctypes.data,
+                                        value.ctypes.data, int(item.shape[0]), ctypes.byref(n),
+                                        _stream_ptr(stream)), "ss_index_export")
+        H = n_hot.value
+        return {"hot": hot[:H], "hot_values": hot_values[:, :H], "col_ptr": col_ptr,
+                "item": item[: n.value], "value": value[: n.value]}
+
     def invalidate(self):
         """Forget the hot set and the prepared queries (after in-place edits)."""
         self._check(self._lib.ss_invalidate(self._h), "ss_invalidate")

@@ -29,6 +29,13 @@ SS_MAX_CHUNK_ROWS = 65536
 SS_VALUES_F32 = 0
 SS_VALUES_BF16 = 1
 SS_VALUES_F16 = 2
+SS_EXPORT_HOT_MAX = 128
+SS_DEVICE_OK = 0
+SS_DEVICE_UNSORTED = 1
+SS_DEVICE_OUT_OF_RANGE = 2
+SS_DEVICE_CAPACITY = 3
+SS_DEVICE_STALL = 4
+SS_DEVICE_RANGE = 5
 
 
 class ss_csr(ctypes.Structure):
@@ -75,8 +82,10 @@ SIGNATURES = {
     "ss_check_device": (_I32, [_P, _P]),
     "ss_invalidate": (_I32, [_P]),
     "ss_index_stats": (_I32, [_P, _P, ctypes.POINTER(ctypes.c_int64), _P]),
-    "ss_cosine_chunk_noalloc": (_I32, [_CSR, _CSR, _I64, _I64, _I64, _P, _I64, _P]),
+    "ss_index_export": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, ctypes.POINTER(_I64), _P]),
+    "ss_cosine_chunk_noalloc": (_I32, [_CSR, _CSR, _I64, _I64, _I64, _P, _I64, _P, _P]),
     "ss_kernel_launches": (ctypes.c_uint64, [_P]),
+    "ss_inject_alloc_failure": (_I64, [_I64]),
     "ss_profile_scorer": (_I32, [_P, _I32]),
     "ss_scorer_time": (_I32, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I64)]),
     "ss_destroy": (_I32, [_P]),

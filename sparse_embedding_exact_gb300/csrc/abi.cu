@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <chrono>
 #include <map>
 #include <mutex>
@@ -32,7 +33,20 @@ ss_status fail(ss_handle *h, ss_status st, const char *fmt, ...) {
 
 ss_status cuda_fail(ss_handle *h, cudaError_t e, const char *what) {
   const ss_status st = (e == cudaErrorMemoryAllocation) ? SS_ERR_OOM : SS_ERR_CUDA;
+  if (h && st == SS_ERR_OOM) reset_after_oom(h);
   return fail(h, st, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Allocations left before the injected failure (0: none armed).
+std::atomic<int64_t> g_alloc_countdown{0};
+
+// True when this allocation is the one ss_inject_alloc_failure armed.
+bool injected_failure() {
+  int64_t left = g_alloc_countdown.load();
+  while (left > 0) {
+    if (g_alloc_countdown.compare_exchange_weak(left, left - 1)) return left == 1;
+  }
+  return false;
 }
 
 #define SS_CUDA(h, call)                                  \
@@ -102,15 +116,15 @@ ss_status validate(ss_handle *h, const ss_csr &m, cudaStream_t s, const char *wh
 // Posting-list workspace (column counters and pointers for a build batch,
 // the scorer's row counter); allocated on first use.
 ss_status ensure_posting_workspace(ss_handle *h) {
-  if (h->col_ptr) return SS_OK;
+  if (h->col_ptr) return SS_OK;  // the four exist together or not at all (reset_after_oom)
   const size_t n = (size_t)h->build_batch * (size_t)(h->dim + 1);
   h->scan_tiles = scan_tile_count((int64_t)n);
   SS_CUDA(h, cudaDeviceSynchronize());
-  SS_CUDA(h, cudaMalloc(&h->col_cnt, sizeof(int32_t) * n));
-  SS_CUDA(h, cudaMalloc(&h->scan_part, sizeof(int32_t) * (size_t)(h->scan_tiles + 1)));
-  SS_CUDA(h, cudaMalloc(&h->slab_post, sizeof(float) * (size_t)h->build_batch * hyb::kHotMax *
+  SS_CUDA(h, dev_alloc(&h->col_cnt, sizeof(int32_t) * n));
+  SS_CUDA(h, dev_alloc(&h->scan_part, sizeof(int32_t) * (size_t)(h->scan_tiles + 1)));
+  SS_CUDA(h, dev_alloc(&h->slab_post, sizeof(float) * (size_t)h->build_batch * hyb::kHotMax *
                                            (size_t)h->chunk_rows));
-  SS_CUDA(h, cudaMalloc(&h->col_ptr, sizeof(int32_t) * n));
+  SS_CUDA(h, dev_alloc(&h->col_ptr, sizeof(int32_t) * n));
   return SS_OK;
 }
 
@@ -129,9 +143,9 @@ ss_status ensure_capacity(ss_handle *h, int32_t algo, int64_t need) {
     h->post_val = nullptr;
     h->post_hat = nullptr;
     h->post_cap = 0;
-    SS_CUDA(h, cudaMalloc(&h->post_item, sizeof(uint16_t) * (size_t)cap));
-    SS_CUDA(h, cudaMalloc(&h->post_val, sizeof(float) * (size_t)cap));
-    SS_CUDA(h, cudaMalloc(&h->post_hat, sizeof(int2) * (size_t)cap));
+    SS_CUDA(h, dev_alloc(&h->post_item, sizeof(uint16_t) * (size_t)cap));
+    SS_CUDA(h, dev_alloc(&h->post_val, sizeof(float) * (size_t)cap));
+    SS_CUDA(h, dev_alloc(&h->post_hat, sizeof(int2) * (size_t)cap));
     h->post_cap = cap;
     return SS_OK;
   }
@@ -145,9 +159,9 @@ ss_status ensure_capacity(ss_handle *h, int32_t algo, int64_t need) {
   h->heavy_v = nullptr;
   h->heavy_item = nullptr;
   h->heavy_cap = 0;
-  SS_CUDA(h, cudaMalloc(&h->heavy_k, sizeof(int32_t) * (size_t)cap));
-  SS_CUDA(h, cudaMalloc(&h->heavy_v, sizeof(float) * (size_t)cap));
-  SS_CUDA(h, cudaMalloc(&h->heavy_item, (size_t)cap));
+  SS_CUDA(h, dev_alloc(&h->heavy_k, sizeof(int32_t) * (size_t)cap));
+  SS_CUDA(h, dev_alloc(&h->heavy_v, sizeof(float) * (size_t)cap));
+  SS_CUDA(h, dev_alloc(&h->heavy_item, (size_t)cap));
   h->heavy_cap = cap;
   return SS_OK;
 }
@@ -235,12 +249,15 @@ bool same_auto_source(const ss_handle *h, const ss_csr &m) {
          h->auto_src_rows == m.n_rows && h->auto_src_nnz == m.nnz;
 }
 
-// Builds the chunk indexes of [rb, re).  MODE_AUTO: for a new item matrix,
-// the hot set is chosen and every item tile of this first build is probed:
-// when more than kAutoOverflowShare of them hold more cold entries than a
-// shared-memory image takes (rows too long or too spread for item tiles),
-// the matrix is built as posting lists from then on, else as item tiles.
-// Reading the probe synchronises the stream once per item matrix.
+// Builds the chunk indexes of [rb, re).  MODE_AUTO, for a new item matrix:
+// the tensor path when a row sample shows a strong head (at least
+// kAutoMinHot hot dimensions leaving at most kAutoMaxCold expected shared
+// cold dimensions per pair); otherwise the hybrid hot set is chosen and
+// every item tile of this first build is probed: when more than
+// kAutoOverflowShare of them hold more cold entries than a shared-memory
+// image takes (rows too long or too spread for item tiles), posting lists,
+// else item tiles.  Reading the sample statistics (and the probe)
+// synchronises the stream once per item matrix.
 ss_status build_chunk(ss_handle *h, const ss_csr &items, int64_t rb, int64_t re, cudaStream_t s) {
   ss_status st = SS_OK;
   if (h->mode == MODE_POSTING) return build_algo(h, ALGO_POSTING, items, rb, re, s);
@@ -248,21 +265,19 @@ ss_status build_chunk(ss_handle *h, const ss_csr &items, int64_t rb, int64_t re,
   if (h->mode == MODE_TENSOR) return build_algo(h, ALGO_TENSOR, items, rb, re, s);
   if (!same_auto_source(h, items)) {
     int queued = 0;
-    SS_CUDA(h, launch_hot_select(h, items, s, &queued));
-    SS_CUDA(h, launch_auto_probe(h, items, rb, re, h->probe, s));
-    h->launches += queued + 1;
-    int32_t counts[2] = {0, 0};
-    SS_CUDA(h, cudaMemcpyAsync(counts, h->probe, sizeof(counts), cudaMemcpyDeviceToHost, s));
-    SS_CUDA(h, cudaStreamSynchronize(s));
-    h->auto_algo = ((double)counts[1] > kAutoOverflowShare * (double)counts[0]) ? ALGO_POSTING : ALGO_HYBRID;
-    if (h->auto_algo == ALGO_HYBRID) {
-      // Rows short enough for item tiles: the tensor path when the matrix
-      // has a strong head (at least kAutoMinHot hot dimensions leaving at
-      // most kAutoMaxCold expected shared cold dimensions per pair).
-      if ((st = ensure_posting_workspace(h)) != SS_OK) return st;
-      SS_CUDA(h, launch_tc_hot_select(h, items, s, &queued));
-      h->launches += queued;
-      if (h->tc_H >= tcp::kAutoMinHot && h->tc_est_cold <= tcp::kAutoMaxCold) h->auto_algo = ALGO_TENSOR;
+    if ((st = ensure_posting_workspace(h)) != SS_OK) return st;
+    SS_CUDA(h, launch_tc_hot_select(h, items, s, &queued));
+    h->launches += queued;
+    if (h->tc_H >= tcp::kAutoMinHot && h->tc_est_cold <= tcp::kAutoMaxCold) {
+      h->auto_algo = ALGO_TENSOR;
+    } else {
+      SS_CUDA(h, launch_hot_select(h, items, s, &queued));
+      SS_CUDA(h, launch_auto_probe(h, items, rb, re, h->probe, s));
+      h->launches += queued + 1;
+      int32_t counts[2] = {0, 0};
+      SS_CUDA(h, cudaMemcpyAsync(counts, h->probe, sizeof(counts), cudaMemcpyDeviceToHost, s));
+      SS_CUDA(h, cudaStreamSynchronize(s));
+      h->auto_algo = ((double)counts[1] > kAutoOverflowShare * (double)counts[0]) ? ALGO_POSTING : ALGO_HYBRID;
     }
     h->auto_src[0] = items.indptr;
     h->auto_src[1] = items.indices;
@@ -305,9 +320,9 @@ ss_status ensure_topk_space(ss_handle *h, int64_t n_q, int64_t cap) {
   h->cand_item = nullptr;
   h->cand_n = nullptr;
   h->cand_elems = h->cand_rows = 0;
-  SS_CUDA(h, cudaMalloc(&h->cand_val, sizeof(float) * (size_t)elems));
-  SS_CUDA(h, cudaMalloc(&h->cand_item, sizeof(int32_t) * (size_t)elems));
-  SS_CUDA(h, cudaMalloc(&h->cand_n, sizeof(int32_t) * (size_t)std::max<int64_t>(1, n_q)));
+  SS_CUDA(h, dev_alloc(&h->cand_val, sizeof(float) * (size_t)elems));
+  SS_CUDA(h, dev_alloc(&h->cand_item, sizeof(int32_t) * (size_t)elems));
+  SS_CUDA(h, dev_alloc(&h->cand_n, sizeof(int32_t) * (size_t)std::max<int64_t>(1, n_q)));
   SS_CUDA(h, cudaMemset(h->cand_n, 0, sizeof(int32_t) * (size_t)std::max<int64_t>(1, n_q)));
   h->cand_elems = elems;
   h->cand_rows = n_q;
@@ -332,6 +347,60 @@ bool owns_index(const ss_handle *h, const ss_index *idx) {
 }
 
 }  // namespace
+
+cudaError_t dev_alloc(void **p, size_t bytes) {
+  if (injected_failure()) {
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  return cudaMalloc(p, bytes);
+}
+
+cudaError_t host_alloc(void **p, size_t bytes) {
+  if (injected_failure()) {
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  return cudaHostAlloc(p, bytes, cudaHostAllocDefault);
+}
+
+void reset_after_oom(ss_handle *h) {
+  cudaDeviceSynchronize();
+  cudaGetLastError();
+  void *lazy[] = {h->col_cnt, h->col_ptr, h->scan_part, h->slab_post, h->post_item, h->post_val,
+                  h->post_hat, h->heavy_k, h->heavy_v, h->heavy_item, h->cand_val, h->cand_item,
+                  h->cand_n, h->qhot, h->qcold, h->qcold_n, h->qhot_dense, h->hot_scratch,
+                  h->tc_hot, h->tc_sel, h->tc_stats, h->tc_A, h->tc_qcold, h->tc_qcold_n, h->tc_B,
+                  h->tc_rec, h->tc_rec_off, h->tc_slab, h->tc_sq};
+  for (void *p : lazy) cudaFree(p);
+  h->col_cnt = h->col_ptr = h->scan_part = nullptr;
+  h->scan_tiles = 0;
+  h->slab_post = nullptr;
+  h->post_item = nullptr;
+  h->post_val = nullptr;
+  h->post_hat = nullptr;
+  h->post_cap = 0;
+  h->heavy_k = nullptr;
+  h->heavy_v = nullptr;
+  h->heavy_item = nullptr;
+  h->heavy_cap = 0;
+  h->cand_val = nullptr;
+  h->cand_item = h->cand_n = nullptr;
+  h->cand_elems = h->cand_rows = 0;
+  h->qhot = nullptr;
+  h->qcold = nullptr;
+  h->qcold_n = nullptr;
+  h->qhot_cap = h->qcold_cap = h->qcold_n_cap = 0;
+  h->qhot_dense = h->hot_scratch = nullptr;
+  h->qhot_dense_cap = h->hot_scratch_cap = 0;
+  h->tc_hot = h->tc_sel = h->tc_qcold_n = h->tc_rec_off = nullptr;
+  h->tc_stats = h->tc_slab = h->tc_sq = nullptr;
+  h->tc_A = h->tc_B = nullptr;
+  h->tc_qcold = h->tc_rec = nullptr;
+  h->tc_A_cap = h->tc_qcold_cap = h->tc_qcold_n_cap = h->tc_B_cap = h->tc_rec_cap = h->tc_rec_off_cap = 0;
+  h->n_views = 0;
+  ss_invalidate(h);
+}
 
 cudaError_t ensure_dyn_smem(const void *kernel, size_t bytes) {
   static std::mutex mu;
@@ -380,6 +449,8 @@ const char *ss_status_string(ss_status s) {
 const char *ss_last_error(const ss_handle *h) { return h ? h->last_error.c_str() : ""; }
 
 uint64_t ss_kernel_launches(const ss_handle *h) { return h ? h->launches : 0; }
+
+int64_t ss_inject_alloc_failure(int64_t nth) { return g_alloc_countdown.exchange(nth > 0 ? nth : 0); }
 
 ss_status ss_profile_scorer(ss_handle *h, int32_t on) {
   if (!h) return SS_ERR_INVALID_ARG;
@@ -430,12 +501,12 @@ ss_status ss_create(ss_handle **out, int device, int64_t dim, int32_t chunk_rows
   h->algo = (h->mode == MODE_POSTING) ? ALGO_POSTING : (h->mode == MODE_TENSOR) ? ALGO_TENSOR : ALGO_HYBRID;
   cudaError_t e = cudaSetDevice(device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, device);
-  if (e == cudaSuccess) e = cudaMalloc(&h->d_status, sizeof(int32_t));
+  if (e == cudaSuccess) e = dev_alloc(&h->d_status, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int32_t));
-  if (e == cudaSuccess) e = cudaMalloc(&h->row_next, 2 * sizeof(int32_t));
+  if (e == cudaSuccess) e = dev_alloc(&h->row_next, 2 * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(h->row_next, 0, 2 * sizeof(int32_t));
-  if (e == cudaSuccess) e = cudaMalloc(&h->probe, 2 * sizeof(int32_t));
-  if (e == cudaSuccess) e = cudaMalloc(&h->hot, sizeof(int32_t) * (1 + hyb::kHotMax));
+  if (e == cudaSuccess) e = dev_alloc(&h->probe, 2 * sizeof(int32_t));
+  if (e == cudaSuccess) e = dev_alloc(&h->hot, sizeof(int32_t) * (1 + hyb::kHotMax));
   if (e == cudaSuccess) e = cudaMemset(h->hot, 0, sizeof(int32_t) * (1 + hyb::kHotMax));
   {
     using namespace hyb;
@@ -451,14 +522,14 @@ ss_status ss_create(ss_handle **out, int device, int64_t dim, int32_t chunk_rows
   if (e == cudaSuccess && h->mode != MODE_POSTING && h->mode != MODE_TENSOR) {
     using namespace hyb;
     const size_t tiles = (size_t)h->max_tiles;
-    if (e == cudaSuccess) e = cudaMalloc(&h->slab, sizeof(float) * tiles * kHotMax * kTI);
-    if (e == cudaSuccess) e = cudaMalloc(&h->ell, sizeof(int2) * tiles * kEllMaxW * kTI);
-    if (e == cudaSuccess) e = cudaMalloc(&h->meta, sizeof(int32_t) * tiles * kMetaInts);
-    if (e == cudaSuccess) e = cudaMalloc(&h->heavy_tbl, sizeof(int4) * tiles * kTI);
+    if (e == cudaSuccess) e = dev_alloc(&h->slab, sizeof(float) * tiles * kHotMax * kTI);
+    if (e == cudaSuccess) e = dev_alloc(&h->ell, sizeof(int2) * tiles * kEllMaxW * kTI);
+    if (e == cudaSuccess) e = dev_alloc(&h->meta, sizeof(int32_t) * tiles * kMetaInts);
+    if (e == cudaSuccess) e = dev_alloc(&h->heavy_tbl, sizeof(int4) * tiles * kTI);
     const size_t n_counters = 1 + (size_t)h->build_batch * (1 + h->chunk_tiles);
-    if (e == cudaSuccess) e = cudaMalloc(&h->counters, sizeof(int32_t) * n_counters);
+    if (e == cudaSuccess) e = dev_alloc(&h->counters, sizeof(int32_t) * n_counters);
     if (e == cudaSuccess) e = cudaMemset(h->counters, 0, sizeof(int32_t) * n_counters);
-    if (e == cudaSuccess) e = cudaMalloc(&h->image, (size_t)kImgBytes * tiles);
+    if (e == cudaSuccess) e = dev_alloc(&h->image, (size_t)kImgBytes * tiles);
   }
   if (e != cudaSuccess) {
     const ss_status st = (e == cudaErrorMemoryAllocation) ? SS_ERR_OOM : SS_ERR_CUDA;
@@ -549,10 +620,95 @@ ss_status ss_index_stats(ss_handle *h, const ss_index *idx, int64_t *stats, void
   return SS_OK;
 }
 
+static_assert(tcp::kHotMax <= SS_EXPORT_HOT_MAX && hyb::kHotMax <= SS_EXPORT_HOT_MAX,
+              "every hot set fits the export's rows");
+
+ss_status ss_index_export(ss_handle *h, const ss_index *idx, int32_t *n_hot, int32_t *hot,
+                          float *hot_values, int32_t *col_ptr, int32_t *item, float *value,
+                          int64_t capacity, int64_t *n_entries, void *stream) {
+  if (!h) return SS_ERR_INVALID_ARG;
+  if (!idx || !owns_index(h, idx))
+    return fail(h, SS_ERR_INVALID_ARG, "ss_index_export: index does not belong to this handle");
+  if (idx->algo != ALGO_POSTING && idx->algo != ALGO_TENSOR)
+    return fail(h, SS_ERR_INVALID_ARG, "ss_index_export: item-tile indexes have no list form");
+  if (capacity < 0) return fail(h, SS_ERR_INVALID_ARG, "ss_index_export: negative capacity");
+  ss_status st = set_device(h);
+  if (st != SS_OK) return st;
+  SS_CUDA(h, cudaStreamSynchronize(as_stream(stream)));
+  const int64_t n_items = idx->n_items, dim = idx->dim;
+
+  // The dimensions held dense, and their values per item.
+  std::vector<int32_t> hot_set;
+  if (idx->hot) {
+    const int hmax = idx->algo == ALGO_TENSOR ? tcp::kHotMax : hyb::kHotMax;
+    std::vector<int32_t> raw(1 + (size_t)hmax);
+    SS_CUDA(h, cudaMemcpy(raw.data(), idx->hot, sizeof(int32_t) * raw.size(), cudaMemcpyDeviceToHost));
+    const int H = std::max(0, std::min(raw[0], hmax));
+    // Posting lists keep every dimension in the lists below kSplitMinHot.
+    if (idx->algo == ALGO_TENSOR || H >= kSplitMinHot) hot_set.assign(raw.begin() + 1, raw.begin() + 1 + H);
+  }
+  const int H = (int)hot_set.size();
+  if (n_hot) *n_hot = H;
+  if (hot) std::copy(hot_set.begin(), hot_set.end(), hot);
+  if (hot_values) {
+    std::fill(hot_values, hot_values + (size_t)n_items * SS_EXPORT_HOT_MAX, 0.f);
+    if (H > 0) {
+      if (idx->algo == ALGO_TENSOR) {  // slab [item][kHotMax]
+        std::vector<float> slab((size_t)n_items * tcp::kHotMax);
+        SS_CUDA(h, cudaMemcpy(slab.data(), idx->slab, sizeof(float) * slab.size(), cudaMemcpyDeviceToHost));
+        for (int64_t i = 0; i < n_items; ++i)
+          for (int j = 0; j < H; ++j) hot_values[i * SS_EXPORT_HOT_MAX + j] = slab[(size_t)i * tcp::kHotMax + j];
+      } else {  // slab [hot dim][slab_ld]
+        std::vector<float> slab((size_t)hyb::kHotMax * idx->slab_ld);
+        SS_CUDA(h, cudaMemcpy(slab.data(), idx->slab, sizeof(float) * slab.size(), cudaMemcpyDeviceToHost));
+        for (int64_t i = 0; i < n_items; ++i)
+          for (int j = 0; j < H; ++j) hot_values[i * SS_EXPORT_HOT_MAX + j] = slab[(size_t)j * idx->slab_ld + i];
+      }
+    }
+  }
+
+  // The lists, positions made relative to the chunk's first entry and each
+  // list put in ascending item order (the device leaves it unspecified).
+  std::vector<int32_t> ptr((size_t)dim + 1);
+  SS_CUDA(h, cudaMemcpy(ptr.data(), idx->col_ptr, sizeof(int32_t) * ptr.size(), cudaMemcpyDeviceToHost));
+  const int64_t base = ptr[0], n = (int64_t)ptr[dim] - base;
+  if (n < 0 || base < 0 || base + n > idx->capacity)
+    return fail(h, SS_ERR_DEVICE_CHECK, "ss_index_export: list offsets outside the index");
+  if (n_entries) *n_entries = n;
+  if (col_ptr)
+    for (int64_t k = 0; k <= dim; ++k) col_ptr[k] = (int32_t)(ptr[k] - base);
+  if (item || value) {
+    if (capacity < n) return fail(h, SS_ERR_LIMIT, "ss_index_export: %lld entries exceed capacity %lld",
+                                  (long long)n, (long long)capacity);
+    std::vector<uint16_t> it((size_t)n);
+    std::vector<float> val((size_t)n);
+    if (n > 0) {
+      SS_CUDA(h, cudaMemcpy(it.data(), idx->post_item + base, sizeof(uint16_t) * (size_t)n, cudaMemcpyDeviceToHost));
+      SS_CUDA(h, cudaMemcpy(val.data(), idx->post_val + base, sizeof(float) * (size_t)n, cudaMemcpyDeviceToHost));
+    }
+    std::vector<int64_t> order;
+    for (int64_t k = 0; k < dim; ++k) {
+      const int64_t b = ptr[k] - base, e = ptr[k + 1] - base;
+      order.resize((size_t)(e - b));
+      for (int64_t p = b; p < e; ++p) order[(size_t)(p - b)] = p;
+      std::sort(order.begin(), order.end(), [&](int64_t x, int64_t y) { return it[(size_t)x] < it[(size_t)y]; });
+      for (int64_t p = b; p < e; ++p) {
+        if (item) item[p] = it[(size_t)order[(size_t)(p - b)]];
+        if (value) value[p] = val[(size_t)order[(size_t)(p - b)]];
+      }
+    }
+  }
+  return SS_OK;
+}
+
 ss_status ss_check_device(ss_handle *h, void *stream) {
   if (!h) return SS_ERR_INVALID_ARG;
   ss_status st = set_device(h);
   if (st != SS_OK) return st;
+  // Work of a host pass that returned early (a timeout, a stopped consumer)
+  // may still be queued on the pass's own streams.
+  for (cudaStream_t ps : {h->host.comp, h->host.copy, h->host.up})
+    if (ps) SS_CUDA(h, cudaStreamSynchronize(ps));
   int32_t code = 0;
   if ((st = read_status(h, as_stream(stream), &code)) != SS_OK) return st;
   return status_from_device(h, code, "ss_check_device");

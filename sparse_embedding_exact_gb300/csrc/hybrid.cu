@@ -1735,7 +1735,7 @@ static cudaError_t prepare_queries(ss_handle *h, const ss_csr &q, cudaStream_t s
       cudaFree(h->qhot);
       h->qhot = nullptr;
       h->qhot_cap = 0;
-      e = cudaMalloc(&h->qhot, sizeof(float) * (size_t)need_hot);
+      e = dev_alloc(&h->qhot, sizeof(float) * (size_t)need_hot);
       if (e != cudaSuccess) return e;
       h->qhot_cap = need_hot;
     }
@@ -1743,7 +1743,7 @@ static cudaError_t prepare_queries(ss_handle *h, const ss_csr &q, cudaStream_t s
       cudaFree(h->qcold);
       h->qcold = nullptr;
       h->qcold_cap = 0;
-      e = cudaMalloc(&h->qcold, sizeof(int2) * (size_t)need_cold);
+      e = dev_alloc(&h->qcold, sizeof(int2) * (size_t)need_cold);
       if (e != cudaSuccess) return e;
       h->qcold_cap = need_cold;
     }
@@ -1751,7 +1751,7 @@ static cudaError_t prepare_queries(ss_handle *h, const ss_csr &q, cudaStream_t s
       cudaFree(h->qcold_n);
       h->qcold_n = nullptr;
       h->qcold_n_cap = 0;
-      e = cudaMalloc(&h->qcold_n, sizeof(int32_t) * (size_t)need_n);
+      e = dev_alloc(&h->qcold_n, sizeof(int32_t) * (size_t)need_n);
       if (e != cudaSuccess) return e;
       h->qcold_n_cap = need_n;
     }

@@ -18,6 +18,10 @@ enum : int32_t {
   DEV_STALL = 4,  // a bounded loop ran out of iterations
   DEV_RANGE = 5,  // a normalised product above 1: inverse norms that are not the rows' own
 };
+static_assert(DEV_OK == SS_DEVICE_OK && DEV_UNSORTED == SS_DEVICE_UNSORTED &&
+                  DEV_OUT_OF_RANGE == SS_DEVICE_OUT_OF_RANGE && DEV_CAPACITY == SS_DEVICE_CAPACITY &&
+                  DEV_STALL == SS_DEVICE_STALL && DEV_RANGE == SS_DEVICE_RANGE,
+              "device status codes are part of the C ABI");
 
 // Scoring algorithms.
 enum : int32_t {
@@ -307,6 +311,27 @@ struct ss_handle {
   int32_t *cand_n = nullptr;
   int64_t cand_elems = 0, cand_rows = 0;
 };
+
+// Every device and page-locked host allocation of the library goes through
+// these two, so that a test can make the n-th one fail
+// (ss_inject_alloc_failure); they return what cudaMalloc / cudaHostAlloc
+// return.
+cudaError_t dev_alloc(void **p, size_t bytes);
+cudaError_t host_alloc(void **p, size_t bytes);
+template <typename T>
+cudaError_t dev_alloc(T **p, size_t bytes) {
+  return dev_alloc(reinterpret_cast<void **>(p), bytes);
+}
+template <typename T>
+cudaError_t host_alloc(T **p, size_t bytes) {
+  return host_alloc(reinterpret_cast<void **>(p), bytes);
+}
+
+// After a failed allocation: waits for the device, frees every buffer the
+// handle allocates on demand (they are then all absent, never half made) and
+// forgets what was derived from earlier inputs, so the next call starts from
+// a clean workspace.
+void reset_after_oom(ss_handle *h);
 
 // Forgets what was prepared from the current query matrix (its caches are
 // keyed on the arrays' addresses, which a host pass reuses for new contents).

@@ -30,8 +30,11 @@ int g_sm_count[kMaxDevices] = {};
 size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
 // Device address of the scratch array on `device` (which must be current),
-// looked up once per device.  In host code the array's name is only a
-// stand-in for the symbol, never an address a kernel may use.
+// looked up once per device and kept for the life of the process.  In host
+// code the array's name is only a stand-in for the symbol, never an address
+// a kernel may use.  The address kept is the one of the context current at
+// the first call (the device's primary context, as the runtime uses); after
+// cudaDeviceReset, or from another context on the same device, it is stale.
 ss_status scratch_for_device(int device, void **addr, int *sm_count) {
   if (device < 0 || device >= kMaxDevices) return SS_ERR_LIMIT;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
@@ -59,7 +62,7 @@ bool csr_ok(const ss_csr *m) {
 extern "C" ss_status ss_cosine_chunk_noalloc(const ss_csr *queries, const ss_csr *items,
                                              int64_t row_begin, int64_t row_end,
                                              int64_t chunk_nnz, float *out, int64_t ld_out,
-                                             void *stream) {
+                                             int32_t *device_status, void *stream) {
   if (!csr_ok(queries) || !csr_ok(items) || queries->dim != items->dim) return SS_ERR_INVALID_ARG;
   if (row_begin < 0 || row_end <= row_begin || row_end > items->n_rows) return SS_ERR_INVALID_ARG;
   if (chunk_nnz < 0 || chunk_nnz > items->nnz) return SS_ERR_INVALID_ARG;
@@ -103,7 +106,9 @@ extern "C" ss_status ss_cosine_chunk_noalloc(const ss_csr *queries, const ss_csr
   view.mode = MODE_POSTING;
   view.build_batch = 1;
   view.sm_count = sm_count;
-  view.d_status = reinterpret_cast<int32_t *>(b + o_status);
+  // The kernels report what they find in the caller's status word when one
+  // is given, else in the scratch's own (which nobody reads).
+  view.d_status = device_status ? device_status : reinterpret_cast<int32_t *>(b + o_status);
   view.col_cnt = reinterpret_cast<int32_t *>(b + o_cnt);
   view.col_ptr = reinterpret_cast<int32_t *>(b + o_ptr);
   view.scan_part = reinterpret_cast<int32_t *>(b + o_part);

@@ -646,7 +646,7 @@ static cudaError_t prepare_hot_dense(ss_handle *h, const ss_csr &q, cudaStream_t
     cudaFree(h->qhot_dense);
     h->qhot_dense = nullptr;
     h->qhot_dense_cap = 0;
-    if ((e = cudaMalloc(&h->qhot_dense, sizeof(float) * (size_t)need)) != cudaSuccess) return e;
+    if ((e = dev_alloc(&h->qhot_dense, sizeof(float) * (size_t)need)) != cudaSuccess) return e;
     h->qhot_dense_cap = need;
   }
   const int64_t blocks = (rows_padded + 7) / 8;
@@ -721,7 +721,7 @@ cudaError_t launch_score_lists(ss_handle *h, const ss_csr &queries, const float 
         cudaFree(h->hot_scratch);
         h->hot_scratch = nullptr;
         h->hot_scratch_cap = 0;
-        if ((e = cudaMalloc(&h->hot_scratch, sizeof(float) * (size_t)need)) != cudaSuccess) return e;
+        if ((e = dev_alloc(&h->hot_scratch, sizeof(float) * (size_t)need)) != cudaSuccess) return e;
         h->hot_scratch_cap = need;
       }
       dst = h->hot_scratch;

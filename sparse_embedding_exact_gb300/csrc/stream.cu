@@ -43,6 +43,7 @@ ss_status sfail(ss_handle *h, ss_status st, const char *fmt, ...) {
 
 ss_status scuda(ss_handle *h, cudaError_t e, const char *what) {
   const ss_status st = (e == cudaErrorMemoryAllocation) ? SS_ERR_OOM : SS_ERR_CUDA;
+  if (st == SS_ERR_OOM) reset_after_oom(h);
   return sfail(h, st, "%s: %s", what, cudaGetErrorString(e));
 }
 
@@ -113,7 +114,7 @@ ss_status ensure_buf(ss_handle *h, int role, size_t bytes) {
   cudaFree(hp.buf[role]);
   hp.buf[role] = nullptr;
   hp.cap[role] = 0;
-  S_CUDA(cudaMalloc(&hp.buf[role], bytes));
+  S_CUDA(dev_alloc(&hp.buf[role], bytes));
   hp.cap[role] = bytes;
   return SS_OK;
 }
@@ -287,7 +288,7 @@ ss_status ensure_ring(ss_handle *h, int ring, size_t bytes) {
   }
   while ((int)hp.slots.size() < ring) {
     float *p = nullptr;
-    S_CUDA(cudaHostAlloc(&p, hp.slot_bytes, cudaHostAllocDefault));
+    S_CUDA(host_alloc(&p, hp.slot_bytes));
     hp.slots.push_back(p);
   }
   return SS_OK;
@@ -461,8 +462,8 @@ extern "C" ss_status ss_bulk_cosine_host(ss_handle *h, const ss_csr *qh, const s
       cudaFreeHost(hp.host_sums);
       hp.dev_sums = hp.host_sums = nullptr;
       hp.sums_slots = 0;
-      S_CUDA(cudaMalloc(&hp.dev_sums, 16 * (size_t)R));
-      S_CUDA(cudaHostAlloc(&hp.host_sums, 16 * (size_t)R, cudaHostAllocDefault));
+      S_CUDA(dev_alloc(&hp.dev_sums, 16 * (size_t)R));
+      S_CUDA(host_alloc(&hp.host_sums, 16 * (size_t)R));
       hp.sums_slots = R;
     }
   }

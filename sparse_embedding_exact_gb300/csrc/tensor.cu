@@ -31,12 +31,13 @@
 // same bit for bit for any launch shape and chunking), adds that to the
 // tensor result and stores the tile.
 //
-// Scorer (k_tc_score): persistent, one block per SM, 6 warps.  Warp 0 loads
-// operand tiles with bulk asynchronous copies (an item tile's operand stays
-// while the block works through its query tiles); warp 1 allocates tensor
-// memory and one of its threads issues the MMAs into one of two
-// accumulators; warps 2-5 each own a quarter of the 128 accumulator lanes
-// and run the epilogue of one tile pair while the MMAs of the next run.
+// Scorer (k_tc_score): persistent, one block per SM, 10 warps.  Warp 0
+// loads operand tiles with bulk asynchronous copies (an item tile's operand
+// stays while the block works through its query tiles); warp 1 allocates
+// tensor memory and one of its threads issues the MMAs into one of two
+// accumulators; warps 2-9 run the epilogue, two per quarter of the 128
+// accumulator lanes (one takes the even 32-column blocks, the other the
+// odd ones), on one tile pair while the MMAs of the next run.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -814,7 +815,7 @@ __device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[32]) {
 __global__ void __launch_bounds__(kSThreads, 1)
     k_tc_score(const ScoreArgs a) {
   extern __shared__ __align__(1024) unsigned char sm[];
-  __shared__ __align__(8) uint64_t bars[10];
+  __shared__ __align__(8) uint64_t bars[11];
   __shared__ uint32_t tmem_slot;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hp = a.Hp;
@@ -831,8 +832,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
   // read out (one arrival per epilogue warp).
   const uint32_t acc_full0 = smem_u32(&bars[6]), acc_full1 = smem_u32(&bars[7]);
   const uint32_t acc_free0 = smem_u32(&bars[8]), acc_free1 = smem_u32(&bars[9]);
+  const uint32_t drain = smem_u32(&bars[10]);  // the MMA thread's last commit
   if (tid == 0) {
     for (int i = 0; i < 8; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    mbar_init(drain, 1);
     mbar_init(acc_free0, kEpiWarps);
     mbar_init(acc_free1, kEpiWarps);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -857,33 +860,33 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // tile's lo part and hi part, each once the MMAs have released it.
     if (lane == 0) {
       int64_t prev_t = -1;
-      int nb = 0;
-      bool ok = true;
-      for (int64_t j = 0; j < nj && ok; ++j) {
+      int nb = 0;             // item tile copies issued
+      int64_t n_lo = 0, n_hi = 0;  // query part copies issued
+      for (int64_t j = 0; j < nj; ++j) {
         const int64_t u = u0 + j, t = u / a.n_qtiles, g = u % a.n_qtiles;
         if (t != prev_t) {
-          if (nb > 0) ok = mbar_wait(b_free, (uint32_t)((nb - 1) & 1), a.status);
-          if (!ok) break;
+          if (nb > 0 && !mbar_wait(b_free, (uint32_t)((nb - 1) & 1), a.status)) break;
           mbar_expect_tx(b_full, bytesB);
           bulk_g2s(smem_u32(sB), a.B + (size_t)t * (bytesB / 2), bytesB, b_full);
           ++nb;
           prev_t = t;
         }
         const uint16_t *At = a.A + (size_t)g * (bytesApart);  // tile: hi part, lo part (halves)
-        if (j > 0) ok = mbar_wait(lo_free, (uint32_t)((j - 1) & 1), a.status);
-        if (!ok) break;
+        if (j > 0 && !mbar_wait(lo_free, (uint32_t)((j - 1) & 1), a.status)) break;
         mbar_expect_tx(lo_full, bytesApart);
         bulk_g2s(smem_u32(sAlo), At + bytesApart / 2, bytesApart, lo_full);
-        if (j > 0) ok = mbar_wait(hi_free, (uint32_t)((j - 1) & 1), a.status);
-        if (!ok) break;
+        ++n_lo;
+        if (j > 0 && !mbar_wait(hi_free, (uint32_t)((j - 1) & 1), a.status)) break;
         mbar_expect_tx(hi_full, bytesApart);
         bulk_g2s(smem_u32(sAhi), At, bytesApart, hi_full);
+        ++n_hi;
       }
-      // Copies still in flight land before the block exits.
-      if (nj > 0) {
-        mbar_wait(lo_full, (uint32_t)((nj - 1) & 1), a.status);
-        mbar_wait(hi_full, (uint32_t)((nj - 1) & 1), a.status);
-      }
+      // Every copy issued lands before the block exits, also when a wait
+      // above gave up: copy k into a buffer is issued only after the phase
+      // of copy k - 1 completed, so the phase of the last copy issued is the
+      // one still open, and a bulk copy completes by itself.
+      if (n_lo > 0) mbar_wait(lo_full, (uint32_t)((n_lo - 1) & 1), a.status);
+      if (n_hi > 0) mbar_wait(hi_full, (uint32_t)((n_hi - 1) & 1), a.status);
       if (nb > 0) mbar_wait(b_full, (uint32_t)((nb - 1) & 1), a.status);
     }
   } else if (warp == 1) {
@@ -926,8 +929,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
         mma_commit(hi_free);
         mma_commit(b ? acc_full1 : acc_full0);
       }
-      // Every MMA has completed before the accumulators are freed.
-      if (nj > 0) mbar_wait((nj - 1) & 1 ? acc_full1 : acc_full0, (uint32_t)(((nj - 1) >> 1) & 1), a.status);
+      // Every MMA this thread issued has completed before the tensor memory
+      // is freed, also when a wait above gave up: a commit arrives once all
+      // of the thread's earlier MMAs are done, and an MMA completes by itself.
+      mma_commit(drain);
+      mbar_wait(drain, 0u, a.status);
     }
   } else {
     // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31, i.e. the
@@ -1089,6 +1095,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
       if (lane == 0) mbar_arrive(b ? acc_free1 : acc_free0);
     }
   }
+  // Tensor-memory reads of every warp are ordered before the release.
+  tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -1133,7 +1141,7 @@ cudaError_t grow(T **p, int64_t *cap, int64_t need, cudaStream_t s) {
   *p = nullptr;
   *cap = 0;
   const int64_t n = std::max<int64_t>(need, *cap + *cap / 2);
-  e = cudaMalloc(p, sizeof(T) * (size_t)n);
+  e = dev_alloc(p, sizeof(T) * (size_t)n);
   if (e != cudaSuccess) return e;
   *cap = n;
   return cudaSuccess;
@@ -1151,9 +1159,9 @@ cudaError_t launch_tc_hot_select(ss_handle *h, const ss_csr &items, cudaStream_t
   cudaError_t e = cudaSuccess;
   if (!h->tc_hot) {
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
-    if ((e = cudaMalloc(&h->tc_hot, sizeof(int32_t) * (1 + kHotMax))) != cudaSuccess) return e;
-    if ((e = cudaMalloc(&h->tc_sel, sizeof(int32_t) * 2 * kSelSlots)) != cudaSuccess) return e;
-    if ((e = cudaMalloc(&h->tc_stats, sizeof(float) * 2)) != cudaSuccess) return e;
+    if ((e = dev_alloc(&h->tc_hot, sizeof(int32_t) * (1 + kHotMax))) != cudaSuccess) return e;
+    if ((e = dev_alloc(&h->tc_sel, sizeof(int32_t) * 2 * kSelSlots)) != cudaSuccess) return e;
+    if ((e = dev_alloc(&h->tc_stats, sizeof(float) * 2)) != cudaSuccess) return e;
   }
   const int64_t n = items.n_rows;
   int64_t n_sample = 0;
@@ -1198,9 +1206,9 @@ cudaError_t launch_build_tc(ss_handle *h, const ss_csr &items, int64_t row_begin
   cudaError_t e = cudaSuccess;
   if (!h->tc_slab) {
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
-    if ((e = cudaMalloc(&h->tc_slab, sizeof(float) * (size_t)h->build_batch * C * kHotMax)) != cudaSuccess)
+    if ((e = dev_alloc(&h->tc_slab, sizeof(float) * (size_t)h->build_batch * C * kHotMax)) != cudaSuccess)
       return e;
-    if ((e = cudaMalloc(&h->tc_sq, sizeof(float) * (size_t)h->build_batch * C)) != cudaSuccess) return e;
+    if ((e = dev_alloc(&h->tc_sq, sizeof(float) * (size_t)h->build_batch * C)) != cudaSuccess) return e;
   }
   const int64_t stride = h->dim + 1;
   const int64_t n = stride * n_chunks;

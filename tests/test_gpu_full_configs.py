@@ -2,11 +2,15 @@
 times (8,192-item chunks).
 
 Every chunk is scored on the device.  The oracle checks 256 sampled query
-rows against every item (or the full matrix where it is small enough), and
-properties that hold at any size are checked on every entry: finite values
-and |S| <= 1 + tolerance.  One workload also goes through the host ring,
-where each chunk's checksum (the sum of the float32 bit patterns) must be the
-same on the device and on the host.
+rows against every item (the full matrix of the 1.2M-dimension workload is
+checked in test_gpu_exactness.py), and properties that hold at any size are
+checked on every entry: finite values and |S| <= 1 + tolerance.  The three
+workloads too large to keep (100, 400 and 80 GB of scores) are also streamed
+chunk by chunk into the page-locked host ring with stream verification on:
+each chunk's checksum (the sum of the float32 bit patterns) is taken on the
+device before its copy and must equal the host copy's, the sampled rows are
+collected from the ring, and every entry of every delivered chunk is checked
+for range.
 """
 import numpy as np
 import pytest
@@ -20,6 +24,18 @@ pytestmark = pytest.mark.gpu
 
 TOL = 2e-6
 CHUNK = 8192
+
+
+_DATA = {}
+
+
+def _workload(name):
+    """(Q, I) of a workload, generated once per test module."""
+    if name not in _DATA:
+        _DATA.clear()  # keep one workload in host memory at a time
+        cfg = CONFIGS[name]
+        _DATA[name] = (generate_side(cfg, 0), generate_side(cfg, 1))
+    return _DATA[name]
 
 
 @pytest.fixture(scope="module")
@@ -69,7 +85,7 @@ def _device_pass(sec, cfg, Q, I, rows):
                                   "d1.2m_q20k_i1m_heavy"])
 def test_full_workload_sampled_rows(sec, name):
     cfg = CONFIGS[name]
-    Q, I = generate_side(cfg, 0), generate_side(cfg, 1)
+    Q, I = _workload(name)
     rows = sample_query_rows(cfg.n_q, 256, cfg.seed)
     sampled, max_abs, finite, sums = _device_pass(sec, cfg, Q, I, rows)
     assert finite
@@ -77,6 +93,38 @@ def test_full_workload_sampled_rows(sec, name):
     assert len(sums) == -(-cfg.n_i // CHUNK)
     ref = oracle.cosine(Q, I, q_rows=rows)
     err = float(np.abs(sampled.astype(np.float64) - ref).max())
+    assert err <= TOL, f"{name}: max abs error {err:.3e}"
+
+
+@pytest.mark.parametrize("name", ["d500k_q50k_i500k_uniform", "d1.2m_q50k_i2m", "d1.2m_q20k_i1m_heavy"])
+def test_streamed_workload_through_the_host_ring(sec, name):
+    cfg = CONFIGS[name]
+    Q, I = _workload(name)
+    rows = sample_query_rows(cfg.n_q, 256, cfg.seed)
+    sampled = np.full((len(rows), I.n_rows), np.nan, np.float32)
+    seen, worst = [], [0.0]
+    torch.set_num_threads(max(1, min(16, torch.get_num_threads())))
+
+    def consume(c, b, e, tile):
+        seen.append((c, b, e))
+        sampled[:, b:e] = tile[rows]
+        m = float(torch.from_numpy(tile).abs().max())  # NaN if any entry is NaN
+        if not m == m:
+            worst[0] = float("nan")
+        elif worst[0] == worst[0]:
+            worst[0] = max(worst[0], m)
+
+    with sec.SparseCosine(cfg.dim, chunk_rows=CHUNK, verify_stream=True) as h:
+        h.bulk_cosine_host(Q, I, consumer=consume, ring_depth=3)
+        sums = h.stream_checksums()
+    n_chunks = -(-cfg.n_i // CHUNK)
+    assert [c for c, _, _ in seen] == list(range(n_chunks))
+    assert [(b, e) for _, b, e in seen] == [(b, min(b + CHUNK, cfg.n_i)) for b in range(0, cfg.n_i, CHUNK)]
+    assert len(sums) == n_chunks  # one verified checksum per chunk (device == host copy)
+    assert worst[0] <= 1.0 + TOL  # every entry finite and in range
+    ref = oracle.cosine(Q, I, q_rows=rows)
+    err = float(np.abs(sampled.astype(np.float64) - ref).max())
+    print(f"{name}: {n_chunks} chunks through the ring, sampled rows max |error| {err:.3e}")
     assert err <= TOL, f"{name}: max abs error {err:.3e}"
 
 

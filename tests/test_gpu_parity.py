@@ -411,14 +411,16 @@ def test_two_gpu_algorithms_agree(sec, name):
 
 # ------------------------------------------------------------- posting lists
 def test_auto_choice_follows_tile_overflow(sec):
-    """Without an algorithm flag the handle probes an item matrix's first
-    batch: posting lists when most item tiles overflow (the uniform workload,
-    500 nonzeros a row), else the tensor path when the matrix has a strong
-    head (the Zipf workloads: 128 hot dimensions leave about 0.11 shared cold
-    dimensions per pair).  Either way the result is that of the chosen
-    algorithm, bit for bit."""
+    """Without an algorithm flag the handle takes the tensor path when the
+    item matrix has a strong head (the Zipf(1.1) workloads: 128 hot
+    dimensions leave about 0.11 shared cold dimensions per pair), else
+    probes the first batch: posting lists when most item tiles overflow (the
+    uniform workload, 500 nonzeros a row; the heavy-tailed Zipf(1.3) one,
+    whose 128 hot dimensions still leave about 0.5 per pair).  Either way
+    the result is that of the chosen algorithm, bit for bit."""
     names = {0: "hybrid", 1: "posting", 2: "tensor"}
-    for name, want in (("d500k_q50k_i500k_uniform", 1), ("d1.2m_q5k_i200k", 2), ("d65k_q1k_i10k", 2)):
+    for name, want in (("d500k_q50k_i500k_uniform", 1), ("d1.2m_q5k_i200k", 2), ("d65k_q1k_i10k", 2),
+                       ("d1.2m_q20k_i1m_heavy", 1)):
         cfg = CONFIGS[name]
         Q, I = generate_rows(cfg, 0, 0, 50), generate_rows(cfg, 1, 0, 9000)
         with sec.SparseCosine(cfg.dim) as h:
@@ -765,8 +767,15 @@ def test_bulk_cosine_host_with_16_bit_values(sec, kind, limit):
     # batch takes its own hot set: equal within the accuracy bar, not bitwise)
     ref_wide = oracle.cosine(Qw, Iw)
     for res in (got, wide, pinned.numpy()):
-        assert _max_err(res, ref_wide) <= TOL
-    assert _max_err(got, ref) <= 2 * math.asin(UNIT_ROUNDOFF[kind]) + TOL
+        assert _max_err(res, ref_wide) <= TOL  # exact for the values as rounded
+    if kind == "f16":
+        # against the unrounded values: within the post's bar for 16-bit data
+        # (section 5.3: error below 1e-3), and within the derived 2 asin(u)
+        assert _max_err(got, ref) < 1e-3
+        assert _max_err(got, ref) <= 2 * math.asin(UNIT_ROUNDOFF[kind]) + TOL
+    # bfloat16 input rounding is outside that bar (its 8-bit significand gives
+    # errors above 1e-3 on these workloads: tests/test_half_values_cpu.py);
+    # the variant only guarantees exact scores of the rounded values.
 
 
 # ------------------------------------------------------------- checksums

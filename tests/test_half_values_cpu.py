@@ -57,6 +57,13 @@ def test_input_rounding_stays_within_the_bound(kind):
     err = float(np.abs(rounded - exact).max())
     assert err <= bound
     assert err > 0.0  # the rounding does change the scores
+    # The post allows 16-bit data where an error below 1e-3 is acceptable
+    # (section 5.3): binary16 meets it; bfloat16 does not on this workload,
+    # which is why the bfloat16 variant is documented as outside that bar.
+    if kind == "f16":
+        assert err < 1e-3
+    else:
+        assert err > 1e-3
 
 
 def test_binding_takes_16_bit_values_only_as_declared():

@@ -1,8 +1,9 @@
 """ss_cosine_chunk_noalloc: the entry point for callers that cannot allocate
 device memory (a host whose pool owns the GPU, a graph capture in progress, a
 plug-in with a fixed budget).  It is called through the C ABI and must match
-the handle-based entry points on two different chunks in a row, since the
-static scratch it works in keeps the previous call's contents.
+the CPU oracle and the handle-based entry points on two different chunks in a
+row, since the static scratch it works in keeps the previous call's contents;
+its device status word must report a chunk_nnz that is too small.
 
 This file is collected last on purpose: a run that stops at the first failure
 has already run every other test by the time it gets here.
@@ -13,6 +14,8 @@ import numpy as np
 import pytest
 
 torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
 
 from workload import CONFIGS, generate_rows  # noqa: E402
 
@@ -33,13 +36,14 @@ def sec():
     return sec
 
 
-def _noalloc(sec, q, i, row_begin, row_end, chunk_nnz, out):
+def _noalloc(sec, q, i, row_begin, row_end, chunk_nnz, out, status=None):
     lib = sec._abi.load()
     cq, ci = q.abi(), i.abi()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    st_ptr = ctypes.c_void_p(0 if status is None else status.data_ptr())
     return lib.ss_cosine_chunk_noalloc(ctypes.byref(cq), ctypes.byref(ci), row_begin, row_end,
                                        chunk_nnz, ctypes.c_void_p(out.data_ptr()), out.stride(0),
-                                       stream)
+                                       st_ptr, stream)
 
 
 def test_noalloc_matches_handle_entry_points_twice(sec):
@@ -54,12 +58,38 @@ def test_noalloc_matches_handle_entry_points_twice(sec):
             idx = h.build_item_index(i, rb, re)
             h.score_chunk(q, inv_q, idx, inv_i[rb:], ref, width)
             out = torch.full((Q.n_rows, width), float("nan"), dtype=torch.float32, device="cuda")
+            status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
             nnz = int(I.indptr[re] - I.indptr[rb])
-            assert _noalloc(sec, q, i, rb, re, nnz, out) == sec._abi.SS_OK
+            assert _noalloc(sec, q, i, rb, re, nnz, out, status) == sec._abi.SS_OK
             torch.cuda.synchronize()
-            got, want = out.cpu().numpy(), ref.cpu().numpy()
+            assert int(status.item()) == sec._abi.SS_DEVICE_OK
+            got, want = out.cpu().numpy().astype(np.float64), ref.cpu().numpy()
             assert np.isfinite(got).all()
-            assert float(np.abs(got.astype(np.float64) - want).max()) <= TOL
+            # against the CPU oracle (the definition), then against the handle path
+            exact = oracle.cosine(Q, I, i_begin=rb, i_end=re)
+            assert float(np.abs(got - exact).max()) <= TOL
+            assert float(np.abs(got - want).max()) <= 2 * TOL
+
+
+def test_noalloc_status_reports_a_short_chunk_nnz(sec):
+    """chunk_nnz one below the chunk's nonzeros: the lists are cut short, and
+    the status word the caller passed says so (SS_DEVICE_CAPACITY)."""
+    cfg = CONFIGS["d65k_q1k_i10k"]
+    Q, I = generate_rows(cfg, 0, 0, 64), generate_rows(cfg, 1, 0, 700)
+    q, i = sec.DeviceCsr.from_host(Q, "cuda"), sec.DeviceCsr.from_host(I, "cuda")
+    rb, re = 100, 700
+    nnz = int(I.indptr[re] - I.indptr[rb])
+    out = torch.empty((Q.n_rows, re - rb), dtype=torch.float32, device="cuda")
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    assert _noalloc(sec, q, i, rb, re, nnz - 1, out, status) == sec._abi.SS_OK
+    torch.cuda.synchronize()
+    assert int(status.item()) == sec._abi.SS_DEVICE_CAPACITY
+    # the exact count clears the word again and gives the oracle's cosines
+    assert _noalloc(sec, q, i, rb, re, nnz, out, status) == sec._abi.SS_OK
+    torch.cuda.synchronize()
+    assert int(status.item()) == sec._abi.SS_DEVICE_OK
+    exact = oracle.cosine(Q, I, i_begin=rb, i_end=re)
+    assert float(np.abs(out.cpu().numpy().astype(np.float64) - exact).max()) <= TOL
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(sec):
