@@ -453,6 +453,27 @@ ss_status ss_index_export(ss_handle *h, const ss_index *idx, int32_t *n_hot, int
                           float *hot_values, int32_t *col_ptr, int32_t *item, float *value,
                           int64_t capacity, int64_t *n_entries, void *stream);
 
+/*
+ * Reads back the tensor path's query-side inverted index into host memory;
+ * for tests and inspection; synchronises `stream`.  On the tensor path the
+ * lists by dimension are built on the query side, once per query matrix
+ * (at its first scoring call), and every chunk's items are walked against
+ * them.  The queries are cut into windows of *win_rows rows (*n_windows of
+ * them); window `window` holds, for every dimension outside the hot set,
+ * the list of its query rows in [window * win_rows, (window + 1) * win_rows):
+ *   col_ptr[0 .. dim]: list k is entries [col_ptr[k], col_ptr[k + 1]);
+ *   row[e]: the query row minus window * win_rows, ascending inside a list
+ *     (sorted here; the device keeps no order, which no sum depends on);
+ *   value[e]: the normalised value q_k * inv_q[row] (float32 product).
+ * Any output may be NULL; row and value need capacity >= *n_entries.
+ * Errors: SS_ERR_INVALID_ARG (no query matrix prepared for the tensor path,
+ * a window out of range), SS_ERR_LIMIT (capacity too small; *n_entries is
+ * still written), SS_ERR_DEVICE_CHECK, SS_ERR_CUDA.
+ */
+ss_status ss_query_index_export(ss_handle *h, int64_t window, int32_t *win_rows, int64_t *n_windows,
+                                int32_t *col_ptr, int32_t *row, float *value, int64_t capacity,
+                                int64_t *n_entries, void *stream);
+
 /* Size of the fixed scratch array behind ss_cosine_chunk_noalloc. */
 #define SS_NOALLOC_SCRATCH_BYTES (32u << 20)
 

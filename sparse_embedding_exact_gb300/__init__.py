@@ -365,6 +365,25 @@ class SparseCosine:
         return {"hot": hot[:H], "hot_values": hot_values[:, :H], "col_ptr": col_ptr,
                 "item": item[: n.value], "value": value[: n.value]}
 
+    def query_index_export(self, window: int = 0, stream=None) -> dict:
+        """The tensor path's query-side lists of one window, as host arrays
+        (after a scoring call prepared the queries; synchronises):
+        "win_rows", "n_windows", "col_ptr" (dim + 1), "row" (within the
+        window, ascending inside each list) and "value" (normalised)."""
+        lib = self._lib
+        wr, nw, n = ctypes.c_int32(0), ctypes.c_int64(0), ctypes.c_int64(0)
+        self._check(lib.ss_query_index_export(self._h, int(window), ctypes.byref(wr), ctypes.byref(nw), None,
+                                              None, None, 0, ctypes.byref(n), _stream_ptr(stream)),
+                    "ss_query_index_export")
+        col_ptr = np.zeros(self.dim + 1, np.int32)
+        row = np.zeros(max(1, n.value), np.int32)
+        value = np.zeros(max(1, n.value), np.float32)
+        self._check(lib.ss_query_index_export(self._h, int(window), None, None, col_ptr.ctypes.data,
+                                              row.ctypes.data, value.ctypes.data, int(row.shape[0]),
+                                              ctypes.byref(n), _stream_ptr(stream)), "ss_query_index_export")
+        return {"win_rows": wr.value, "n_windows": nw.value, "col_ptr": col_ptr, "row": row[: n.value],
+                "value": value[: n.value]}
+
     def invalidate(self):
         """Forget the hot set and the prepared queries (after in-place edits)."""
         self._check(self._lib.ss_invalidate(self._h), "ss_invalidate")

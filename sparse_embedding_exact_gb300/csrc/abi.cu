@@ -166,55 +166,79 @@ ss_status ensure_capacity(ss_handle *h, int32_t algo, int64_t need) {
   return SS_OK;
 }
 
+// Frees every buffer a handle allocates on demand and leaves them absent
+// (null, no capacity): each is then made again, whole, when next needed.
+void free_lazy_buffers(ss_handle *h) {
+  cudaFree(h->col_cnt);
+  cudaFree(h->col_ptr);
+  cudaFree(h->scan_part);
+  cudaFree(h->slab_post);
+  h->col_cnt = h->col_ptr = h->scan_part = nullptr;
+  h->scan_tiles = 0;
+  h->slab_post = nullptr;
+  cudaFree(h->post_item);
+  cudaFree(h->post_val);
+  cudaFree(h->post_hat);
+  h->post_item = nullptr;
+  h->post_val = nullptr;
+  h->post_hat = nullptr;
+  h->post_cap = 0;
+  cudaFree(h->heavy_k);
+  cudaFree(h->heavy_v);
+  cudaFree(h->heavy_item);
+  h->heavy_k = nullptr;
+  h->heavy_v = nullptr;
+  h->heavy_item = nullptr;
+  h->heavy_cap = 0;
+  cudaFree(h->cand_val);
+  cudaFree(h->cand_item);
+  cudaFree(h->cand_n);
+  h->cand_val = nullptr;
+  h->cand_item = h->cand_n = nullptr;
+  h->cand_elems = h->cand_rows = 0;
+  cudaFree(h->qhot);
+  cudaFree(h->qcold);
+  cudaFree(h->qcold_n);
+  h->qhot = nullptr;
+  h->qcold = nullptr;
+  h->qcold_n = nullptr;
+  h->qhot_cap = h->qcold_cap = h->qcold_n_cap = 0;
+  cudaFree(h->qhot_dense);
+  cudaFree(h->hot_scratch);
+  h->qhot_dense = h->hot_scratch = nullptr;
+  h->qhot_dense_cap = h->hot_scratch_cap = 0;
+  void *tc[] = {h->tc_hot, h->tc_sel, h->tc_stats, h->tc_A, h->tc_qcold, h->tc_qcold_n, h->tc_qcnt,
+                h->tc_qptr, h->tc_qpart, h->tc_qpost, h->tc_slab, h->tc_sq, h->tc_icold_rng, h->tc_B,
+                h->tc_rec, h->tc_seg, h->tc_cursor};
+  for (void *p : tc) cudaFree(p);
+  h->tc_hot = h->tc_sel = h->tc_qcold_n = h->tc_seg = nullptr;
+  h->tc_qcnt = h->tc_qptr = h->tc_qpart = nullptr;
+  h->tc_stats = h->tc_slab = h->tc_sq = nullptr;
+  h->tc_A = h->tc_B = nullptr;
+  h->tc_qcold = h->tc_rec = h->tc_qpost = h->tc_icold_rng = nullptr;
+  h->tc_cursor = nullptr;
+  h->tc_A_cap = h->tc_qcold_cap = h->tc_qcold_n_cap = h->tc_B_cap = h->tc_rec_cap = h->tc_seg_cap = 0;
+  h->tc_qcnt_cap = h->tc_qptr_cap = h->tc_qpart_cap = h->tc_qpost_cap = h->tc_cursor_cap = 0;
+  h->n_views = 0;
+}
+
 void free_workspace(ss_handle *h) {
   free_host_pass(h->host);
   for (cudaEvent_t e : h->prof_ev) cudaEventDestroy(e);
   h->prof_ev.clear();
   h->prof_used = 0;
-  cudaFree(h->cand_val);
-  cudaFree(h->cand_item);
-  cudaFree(h->cand_n);
-  h->cand_val = nullptr;
-  h->cand_item = nullptr;
-  h->cand_n = nullptr;
-  h->cand_elems = h->cand_rows = 0;
-  void *ptrs[] = {h->d_status, h->col_cnt, h->col_ptr, h->scan_part, h->post_item, h->post_val,
-                  h->post_hat, h->row_next, h->probe, h->slab_post, h->qhot_dense,
-                  h->hot_scratch, h->hot, h->slab, h->ell, h->meta, h->heavy_k,
-                  h->heavy_v, h->heavy_item, h->counters, h->image, h->qhot, h->qcold,
-                  h->qcold_n, h->heavy_tbl, h->tc_hot, h->tc_sel, h->tc_stats, h->tc_A,
-                  h->tc_qcold, h->tc_qcold_n, h->tc_B, h->tc_rec, h->tc_rec_off,
-                  h->tc_slab, h->tc_sq};
+  free_lazy_buffers(h);
+  void *ptrs[] = {h->d_status, h->row_next, h->probe, h->hot, h->slab, h->ell, h->meta,
+                  h->counters, h->image, h->heavy_tbl};
   for (void *p : ptrs) cudaFree(p);
-  h->tc_hot = h->tc_sel = h->tc_qcold_n = h->tc_rec_off = nullptr;
-  h->tc_stats = h->tc_slab = h->tc_sq = nullptr;
-  h->tc_A = h->tc_B = nullptr;
-  h->tc_qcold = h->tc_rec = nullptr;
-  h->tc_A_cap = h->tc_qcold_cap = h->tc_qcold_n_cap = h->tc_B_cap = h->tc_rec_cap = h->tc_rec_off_cap = 0;
-  h->post_hat = nullptr;
+  h->d_status = nullptr;
   h->row_next = nullptr;
   h->probe = nullptr;
-  h->slab_post = nullptr;
-  h->qhot_dense = nullptr;
-  h->hot_scratch = nullptr;
-  h->qhot_dense_cap = h->hot_scratch_cap = 0;
-  h->counters = nullptr;
-  h->heavy_tbl = nullptr;
-  h->image = nullptr;
-  h->qhot = nullptr;
-  h->qcold = nullptr;
-  h->qcold_n = nullptr;
-  h->qhot_cap = h->qcold_cap = h->qcold_n_cap = 0;
-  h->d_status = nullptr;
-  h->col_cnt = h->col_ptr = h->scan_part = nullptr;
-  h->post_item = nullptr;
-  h->post_val = nullptr;
-  h->post_cap = 0;
-  h->hot = h->meta = h->heavy_k = nullptr;
-  h->slab = h->heavy_v = nullptr;
+  h->hot = h->meta = h->counters = nullptr;
+  h->slab = nullptr;
   h->ell = nullptr;
-  h->heavy_item = nullptr;
-  h->heavy_cap = 0;
+  h->image = nullptr;
+  h->heavy_tbl = nullptr;
 }
 
 ss_status build_algo(ss_handle *h, int32_t algo, const ss_csr &items, int64_t rb, int64_t re,
@@ -225,7 +249,6 @@ ss_status build_algo(ss_handle *h, int32_t algo, const ss_csr &items, int64_t rb
   h->algo = algo;
   int queued = 0;
   if (algo == ALGO_TENSOR) {
-    if ((st = ensure_posting_workspace(h)) != SS_OK) return st;
     SS_CUDA(h, launch_tc_hot_select(h, items, s, &queued));
     h->launches += queued;
     SS_CUDA(h, launch_build_tc(h, items, rb, re, s, &queued));
@@ -265,7 +288,6 @@ ss_status build_chunk(ss_handle *h, const ss_csr &items, int64_t rb, int64_t re,
   if (h->mode == MODE_TENSOR) return build_algo(h, ALGO_TENSOR, items, rb, re, s);
   if (!same_auto_source(h, items)) {
     int queued = 0;
-    if ((st = ensure_posting_workspace(h)) != SS_OK) return st;
     SS_CUDA(h, launch_tc_hot_select(h, items, s, &queued));
     h->launches += queued;
     if (h->tc_H >= tcp::kAutoMinHot && h->tc_est_cold <= tcp::kAutoMaxCold) {
@@ -367,38 +389,7 @@ cudaError_t host_alloc(void **p, size_t bytes) {
 void reset_after_oom(ss_handle *h) {
   cudaDeviceSynchronize();
   cudaGetLastError();
-  void *lazy[] = {h->col_cnt, h->col_ptr, h->scan_part, h->slab_post, h->post_item, h->post_val,
-                  h->post_hat, h->heavy_k, h->heavy_v, h->heavy_item, h->cand_val, h->cand_item,
-                  h->cand_n, h->qhot, h->qcold, h->qcold_n, h->qhot_dense, h->hot_scratch,
-                  h->tc_hot, h->tc_sel, h->tc_stats, h->tc_A, h->tc_qcold, h->tc_qcold_n, h->tc_B,
-                  h->tc_rec, h->tc_rec_off, h->tc_slab, h->tc_sq};
-  for (void *p : lazy) cudaFree(p);
-  h->col_cnt = h->col_ptr = h->scan_part = nullptr;
-  h->scan_tiles = 0;
-  h->slab_post = nullptr;
-  h->post_item = nullptr;
-  h->post_val = nullptr;
-  h->post_hat = nullptr;
-  h->post_cap = 0;
-  h->heavy_k = nullptr;
-  h->heavy_v = nullptr;
-  h->heavy_item = nullptr;
-  h->heavy_cap = 0;
-  h->cand_val = nullptr;
-  h->cand_item = h->cand_n = nullptr;
-  h->cand_elems = h->cand_rows = 0;
-  h->qhot = nullptr;
-  h->qcold = nullptr;
-  h->qcold_n = nullptr;
-  h->qhot_cap = h->qcold_cap = h->qcold_n_cap = 0;
-  h->qhot_dense = h->hot_scratch = nullptr;
-  h->qhot_dense_cap = h->hot_scratch_cap = 0;
-  h->tc_hot = h->tc_sel = h->tc_qcold_n = h->tc_rec_off = nullptr;
-  h->tc_stats = h->tc_slab = h->tc_sq = nullptr;
-  h->tc_A = h->tc_B = nullptr;
-  h->tc_qcold = h->tc_rec = nullptr;
-  h->tc_A_cap = h->tc_qcold_cap = h->tc_qcold_n_cap = h->tc_B_cap = h->tc_rec_cap = h->tc_rec_off_cap = 0;
-  h->n_views = 0;
+  free_lazy_buffers(h);
   ss_invalidate(h);
 }
 
@@ -578,10 +569,9 @@ ss_status ss_index_stats(ss_handle *h, const ss_index *idx, int64_t *stats, void
   stats[1] = idx->n_items;
   SS_CUDA(h, cudaStreamSynchronize(as_stream(stream)));
   if (idx->algo == ALGO_TENSOR) {
-    int32_t ends[2] = {0, 0};
-    SS_CUDA(h, cudaMemcpy(&ends[0], idx->col_ptr, sizeof(int32_t), cudaMemcpyDeviceToHost));
-    SS_CUDA(h, cudaMemcpy(&ends[1], idx->col_ptr + idx->dim, sizeof(int32_t), cudaMemcpyDeviceToHost));
-    stats[6] = ends[1] - ends[0];
+    std::vector<int2> rng((size_t)idx->n_items);
+    SS_CUDA(h, cudaMemcpy(rng.data(), idx->icold_rng, sizeof(int2) * rng.size(), cudaMemcpyDeviceToHost));
+    for (const int2 &r : rng) stats[6] += r.y;
     int32_t hcount = 0;
     SS_CUDA(h, cudaMemcpy(&hcount, idx->hot, sizeof(int32_t), cudaMemcpyDeviceToHost));
     stats[3] = hcount;
@@ -667,6 +657,48 @@ ss_status ss_index_export(ss_handle *h, const ss_index *idx, int32_t *n_hot, int
     }
   }
 
+  if (idx->algo == ALGO_TENSOR) {
+    // The tensor path keeps each item's cold entries (CSR order); their
+    // lists by dimension, items ascending, are made here.
+    std::vector<int2> rng((size_t)n_items);
+    SS_CUDA(h, cudaMemcpy(rng.data(), idx->icold_rng, sizeof(int2) * rng.size(), cudaMemcpyDeviceToHost));
+    int64_t lo = INT64_MAX, hi = 0, n = 0;
+    for (const int2 &r : rng) {
+      if (r.x < 0 || r.y < 0) return fail(h, SS_ERR_DEVICE_CHECK, "ss_index_export: bad cold entry range");
+      if (r.y > 0) {
+        lo = std::min<int64_t>(lo, r.x);
+        hi = std::max<int64_t>(hi, (int64_t)r.x + r.y);
+      }
+      n += r.y;
+    }
+    if (n > 0 && hi > idx->capacity) return fail(h, SS_ERR_DEVICE_CHECK, "ss_index_export: entries outside the index");
+    if (n_entries) *n_entries = n;
+    std::vector<int2> ent(n > 0 ? (size_t)(hi - lo) : 0);
+    if (n > 0) SS_CUDA(h, cudaMemcpy(ent.data(), idx->icold + lo, sizeof(int2) * ent.size(), cudaMemcpyDeviceToHost));
+    std::vector<int64_t> ptr((size_t)dim + 2, 0);
+    for (int64_t i = 0; i < n_items; ++i)
+      for (int j = 0; j < rng[(size_t)i].y; ++j) {
+        const int32_t k = ent[(size_t)(rng[(size_t)i].x - lo + j)].x;
+        if (k < 0 || k >= dim) return fail(h, SS_ERR_DEVICE_CHECK, "ss_index_export: dimension out of range");
+        ++ptr[(size_t)k + 2];
+      }
+    for (int64_t k = 0; k < dim; ++k) ptr[(size_t)k + 2] += ptr[(size_t)k + 1];
+    if (col_ptr)
+      for (int64_t k = 0; k <= dim; ++k) col_ptr[k] = (int32_t)ptr[(size_t)k + 1];
+    if (item || value) {
+      if (capacity < n) return fail(h, SS_ERR_LIMIT, "ss_index_export: %lld entries exceed capacity %lld",
+                                    (long long)n, (long long)capacity);
+      for (int64_t i = 0; i < n_items; ++i)  // items in order: each list ascends
+        for (int j = 0; j < rng[(size_t)i].y; ++j) {
+          const int2 e = ent[(size_t)(rng[(size_t)i].x - lo + j)];
+          const int64_t at = ptr[(size_t)e.x + 1]++;
+          if (item) item[at] = (int32_t)i;
+          if (value) memcpy(value + at, &e.y, sizeof(float));
+        }
+    }
+    return SS_OK;
+  }
+
   // The lists, positions made relative to the chunk's first entry and each
   // list put in ascending item order (the device leaves it unspecified).
   std::vector<int32_t> ptr((size_t)dim + 1);
@@ -696,6 +728,48 @@ ss_status ss_index_export(ss_handle *h, const ss_index *idx, int32_t *n_hot, int
         if (item) item[p] = it[(size_t)order[(size_t)(p - b)]];
         if (value) value[p] = val[(size_t)order[(size_t)(p - b)]];
       }
+    }
+  }
+  return SS_OK;
+}
+
+ss_status ss_query_index_export(ss_handle *h, int64_t window, int32_t *win_rows, int64_t *n_windows,
+                                int32_t *col_ptr, int32_t *row, float *value, int64_t capacity,
+                                int64_t *n_entries, void *stream) {
+  if (!h) return SS_ERR_INVALID_ARG;
+  if (!h->tc_qptr || h->tcq_rows < 0 || h->tc_n_win <= 0)
+    return fail(h, SS_ERR_INVALID_ARG, "ss_query_index_export: no query matrix prepared for the tensor path");
+  if (window < 0 || window >= h->tc_n_win || capacity < 0)
+    return fail(h, SS_ERR_INVALID_ARG, "ss_query_index_export: window %lld outside [0, %lld)",
+                (long long)window, (long long)h->tc_n_win);
+  ss_status st = set_device(h);
+  if (st != SS_OK) return st;
+  SS_CUDA(h, cudaStreamSynchronize(as_stream(stream)));
+  if (win_rows) *win_rows = h->tc_win_rows;
+  if (n_windows) *n_windows = h->tc_n_win;
+  const int64_t dim = h->dim;
+  std::vector<int32_t> ptr((size_t)dim + 1);
+  SS_CUDA(h, cudaMemcpy(ptr.data(), h->tc_qptr + window * (dim + 1), sizeof(int32_t) * ptr.size(),
+                        cudaMemcpyDeviceToHost));
+  const int64_t base = ptr[0], n = (int64_t)ptr[dim] - base;
+  if (n < 0 || base < 0 || base + n > h->tc_qpost_cap)
+    return fail(h, SS_ERR_DEVICE_CHECK, "ss_query_index_export: list offsets outside the index");
+  if (n_entries) *n_entries = n;
+  if (col_ptr)
+    for (int64_t k = 0; k <= dim; ++k) col_ptr[k] = (int32_t)(ptr[k] - base);
+  if (row || value) {
+    if (capacity < n) return fail(h, SS_ERR_LIMIT, "ss_query_index_export: %lld entries exceed capacity %lld",
+                                  (long long)n, (long long)capacity);
+    std::vector<int2> ent((size_t)n);
+    if (n > 0)
+      SS_CUDA(h, cudaMemcpy(ent.data(), h->tc_qpost + base, sizeof(int2) * (size_t)n, cudaMemcpyDeviceToHost));
+    for (int64_t k = 0; k < dim; ++k) {  // each list by ascending row (the device order is unspecified)
+      const int64_t b = ptr[k] - base, e = ptr[k + 1] - base;
+      std::sort(ent.begin() + b, ent.begin() + e, [](const int2 &x, const int2 &y) { return x.x < y.x; });
+    }
+    for (int64_t p = 0; p < n; ++p) {
+      if (row) row[p] = ent[(size_t)p].x;
+      if (value) memcpy(value + p, &ent[(size_t)p].y, sizeof(float));
     }
   }
   return SS_OK;

@@ -30,6 +30,7 @@ __device__ __forceinline__ void hot_insert(int *keys, int8_t *vals, int32_t k, i
   }
 }
 __device__ __forceinline__ int hot_find(const int *keys, const int8_t *vals, int32_t k) {
+  if (k < 0) return -1;  // empty slots hold -1; no hot dimension is negative
   uint32_t s = hash_a(k, 7);
   for (int n = 0; n < kHotSlots; ++n) {
     const int key = keys[s];

@@ -112,10 +112,11 @@ struct ss_index {
   const int4 *heavy_tbl = nullptr;     // [tile][kTI]: heavy items {item, first entry - tile's heavy base, count, 0}
   const unsigned char *image = nullptr; // [tile][kImgBytes]
   const int32_t *counters = nullptr;   // [1] tiles without an image, [2..] their ids ([0] unused)
-  // ALGO_TENSOR (also col_ptr / post_item / post_val / capacity: the cold
-  // dimensions' lists; hot: the tensor hot set; slab: [item][tcp::kHotMax]
+  // ALGO_TENSOR (also hot: the tensor hot set; slab: [item][tcp::kHotMax]
   // raw hot values, 0 if absent)
   const float *sq = nullptr;           // [n_items]: each item's raw sum of squares
+  const int2 *icold = nullptr;         // the build's cold entries {dim, raw value bits}, rows in CSR order
+  const int2 *icold_rng = nullptr;     // [n_items]: {first entry in icold, count}
 };
 
 // Tensor-core path (see tensor.cu).
@@ -287,19 +288,34 @@ struct ss_handle {
   const void *tcq_src[4] = {nullptr, nullptr, nullptr, nullptr};
   int64_t tcq_rows = -1, tcq_nnz = -1;
   uint64_t tcq_generation = ~0ull;
-  // Per chunk of a build: raw hot values [chunk_rows][kHotMax] and sums of
-  // squares [chunk_rows].
+  // The query side's inverted index, per window of tc_win_rows query rows
+  // (tc_n_win of them): counters and list offsets [n_win][dim + 1], the
+  // scan's tile sums, and the entries {row within the window, normalised
+  // value bits}.
+  int32_t *tc_qcnt = nullptr, *tc_qptr = nullptr, *tc_qpart = nullptr;
+  int64_t tc_qcnt_cap = 0, tc_qptr_cap = 0, tc_qpart_cap = 0;
+  int2 *tc_qpost = nullptr;
+  int64_t tc_qpost_cap = 0;
+  int32_t tc_win_rows = 0;
+  int64_t tc_n_win = 0;
+  // Per chunk of a build: raw hot values [chunk_rows][kHotMax], sums of
+  // squares and {first cold entry, count} per item [chunk_rows] (the cold
+  // entries themselves go to post_hat).
   float *tc_slab = nullptr;
   float *tc_sq = nullptr;
+  int2 *tc_icold_rng = nullptr;
   // Item operand of the chunk being scored ([item tiles][kN x 2Hp] fp16).
   uint16_t *tc_B = nullptr;
   int64_t tc_B_cap = 0;
-  // Cold records of one scoring call: fixed-size buckets per (32 query
-  // rows, 32 items) and their counts (-1: the bucket did not fit).
+  // Cold records of one scoring call, segment by segment; per (query
+  // window, column block) the segment's start and its quarters' offsets;
+  // the records placed so far.
   int2 *tc_rec = nullptr;
   int64_t tc_rec_cap = 0;
-  int32_t *tc_rec_off = nullptr;
-  int64_t tc_rec_off_cap = 0;
+  int32_t *tc_seg = nullptr;
+  int64_t tc_seg_cap = 0;
+  unsigned long long *tc_cursor = nullptr;
+  int64_t tc_cursor_cap = 0;
 
   // The last build's chunk indexes (views into the workspace above).
   ss_index views[kMaxBuildBatch];

@@ -38,6 +38,8 @@
 // accumulators; warps 2-9 run the epilogue, two per quarter of the 128
 // accumulator lanes (one takes the even 32-column blocks, the other the
 // odd ones), on one tile pair while the MMAs of the next run.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -48,6 +50,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "internal.cuh"
 #include "topk.cuh"
@@ -69,7 +72,7 @@ constexpr float kMaxSquareSum = 1.0f + 1.0f / 64.0f;     // sum of x^2 of a norm
 constexpr int kStgInts = 32 * 32;              // one staging tile: 32 rows x 32 ints, 128-byte swizzle
 constexpr int kEpiWarps = 8;                   // two per quarter of the accumulator lanes
 constexpr int kSThreads = 64 + 32 * kEpiWarps; // producer, MMA, epilogue warps
-constexpr int kStgBytes = kEpiWarps * kStgInts * 4 + 1024;  // one tile per warp, 1024-byte aligned
+constexpr int kStgBytes = 2 * kEpiWarps * kStgInts * 4 + 1024;  // two tiles per warp, 1024-byte aligned
 constexpr int kRThreads = 1024;         // records: one warp per query row of the block
 constexpr int kPrepThreads = 256;
 constexpr int kWalkUnroll = 8;          // list entries per lane loaded before use
@@ -180,6 +183,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Shared-memory writes of this thread made visible to the asynchronous
+// (bulk copy) proxy.
+__device__ __forceinline__ void fence_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Bulk tensor store of a box (the tensor map's 32 x 32 floats, 128-byte
+// swizzle) from shared memory to the tile at element (x, y), added to this
+// thread's bulk group.  Parts of the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Until all but the most recent of this thread's bulk store groups have
+// read their shared-memory source.
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// Until this thread's bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Read-only loads issued exactly where they are written: the compiler may
 // otherwise sink a plain load to its first use, which defeats a prefetch.
 __device__ __forceinline__ int2 ld_keep_int2(const int2 *p) {
@@ -217,6 +242,7 @@ __device__ __forceinline__ int load_hot(const int32_t *hot, int *keys, uint8_t *
   return H;
 }
 __device__ __forceinline__ int find_hot(const int *keys, const uint8_t *vals, int32_t k) {
+  if (k < 0) return -1;  // empty slots hold -1; no hot dimension is negative
   uint32_t s = hot_hash(k);
   for (int n = 0; n < kHotSlots; ++n) {
     const int key = keys[s];
@@ -404,80 +430,105 @@ __global__ void __launch_bounds__(kSelThreads)
 }
 
 // ---------------------------------------------------------------- build
-// Posting lists of the cold dimensions (the hot ones are left out): the
-// histogram and scatter of a counting sort by dimension, per chunk of the
-// build, as the posting-list path builds them.
+// The item side of a chunk needs no inverted index: one pass over its CSR
+// rows (a warp per row, no atomics) writes each item's raw hot values into
+// the dense slab (0 where absent), its sum of squares, and its cold entries
+// {dim, raw value bits} packed in CSR order (dims ascending) at the row's
+// own positions relative to the build's first nonzero, with {first, count}
+// per item.  The inverted index is built once on the query side instead
+// (k_tc_qhist / k_tc_qscatter below), where it serves every chunk.
 __global__ void __launch_bounds__(256)
-    k_tc_hist(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
-              int64_t row_begin, int64_t row_end, int64_t chunk_rows, int n_chunks, int64_t dim,
-              const int32_t *__restrict__ hot, int32_t *__restrict__ count, int32_t *status) {
-  __shared__ int64_t bound[kMaxBuildBatch + 1];
-  __shared__ int hkeys[kHotSlots];
-  __shared__ uint8_t hvals[kHotSlots];
-  load_hot(hot, hkeys, hvals);
-  if (threadIdx.x <= n_chunks) {
-    const int64_t r = min(row_begin + (int64_t)threadIdx.x * chunk_rows, row_end);
-    bound[threadIdx.x] = indptr[r];
-  }
-  __syncthreads();
-  const int64_t p0 = bound[0], p1 = bound[n_chunks];
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t p = p0 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < p1; p += stride) {
-    const int32_t k = __ldg(indices + p);
-    int c = 0;
-    while (c + 1 < n_chunks && p >= bound[c + 1]) ++c;
-    if (k >= 0 && (int64_t)k < dim) {
-      if (find_hot(hkeys, hvals, k) >= 0) continue;
-      atomicAdd(count + (int64_t)c * (dim + 1) + k, 1);
-    } else {
-      flag(status, DEV_OUT_OF_RANGE);
-    }
-  }
-}
-
-__global__ void __launch_bounds__(256)
-    k_tc_scatter(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
-                 const float *__restrict__ values, int64_t row_begin, int64_t row_end,
-                 int64_t chunk_rows, int64_t dim, const int32_t *__restrict__ hot,
-                 int32_t *__restrict__ cursor, uint16_t *__restrict__ post_item,
-                 float *__restrict__ post_val, int64_t capacity, float *__restrict__ slab,
-                 float *__restrict__ sq, int32_t *status) {
+    k_tc_build(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
+               const float *__restrict__ values, int64_t row_begin, int64_t row_end, int64_t chunk_rows,
+               int64_t dim, const int32_t *__restrict__ hot, float *__restrict__ slab,
+               float *__restrict__ sq, int2 *__restrict__ icold, int2 *__restrict__ icold_rng,
+               int32_t *status) {
   __shared__ int hkeys[kHotSlots];
   __shared__ uint8_t hvals[kHotSlots];
   load_hot(hot, hkeys, hvals);
   const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  const int64_t p_base = indptr[row_begin];
   const int64_t warps = (int64_t)gridDim.x * 8;
+  bool bad = false;
   for (int64_t r = row_begin + (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < row_end; r += warps) {
     const int64_t b = indptr[r], e = indptr[r + 1];
     const int64_t c = (r - row_begin) / chunk_rows;
-    int32_t *cur = cursor + c * (dim + 1);
     const int64_t item = r - row_begin - c * chunk_rows;
     float *srow = slab + (c * chunk_rows + item) * kHotMax;  // this item's hot values, zero if absent
     static_assert(kHotMax == 128, "one float4 per lane clears an item's hot values");
     *reinterpret_cast<float4 *>(srow + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
     __syncwarp();
     float ss = 0.f;
-    for (int64_t j = b + lane; j < e; j += 32) {
-      const int32_t k = __ldg(indices + j);
-      const float v = __ldg(values + j);
-      ss = fmaf(v, v, ss);
-      if (k < 0 || (int64_t)k >= dim) continue;  // flagged by the histogram
-      const int h = find_hot(hkeys, hvals, k);
-      if (h >= 0) {
-        srow[h] = v;
-        continue;
+    int nc = 0;
+    for (int64_t j0 = b; j0 < e; j0 += 32) {
+      const int64_t j = j0 + lane;
+      bool cold = false;
+      int32_t k = 0;
+      float v = 0.f;
+      if (j < e) {
+        k = __ldg(indices + j);
+        v = __ldg(values + j);
+        ss = fmaf(v, v, ss);
+        if (k >= 0 && (int64_t)k < dim) {
+          const int h = find_hot(hkeys, hvals, k);
+          if (h >= 0) srow[h] = v;
+          else cold = true;
+        } else {
+          bad = true;
+        }
       }
-      const int32_t pos = atomicAdd(cur + k, 1);
-      if (pos >= 0 && (int64_t)pos < capacity) {
-        post_item[pos] = (uint16_t)item;
-        post_val[pos] = v;
-      } else {
-        flag(status, DEV_CAPACITY);
-      }
+      const unsigned m = __ballot_sync(0xffffffffu, cold);
+      if (cold) icold[(b - p_base) + nc + __popc(m & lt)] = make_int2(k, __float_as_int(v));
+      nc += __popc(m);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) sq[c * chunk_rows + item] = ss;
+    if (lane == 0) {
+      sq[c * chunk_rows + item] = ss;
+      icold_rng[c * chunk_rows + item] = make_int2((int)(b - p_base), nc);
+    }
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) flag(status, DEV_OUT_OF_RANGE);
+}
+
+// The query side's inverted index, once per query matrix, inverse norms and
+// hot set: the queries are cut into windows of `win_rows` rows, and per
+// window each cold dimension gets the list of its query rows (row within
+// the window, normalised value), a counting sort by (window, dimension):
+// the histogram here, a scan of the n_win x (dim + 1) counters
+// (launch_count_scan), then the scatter.  A list's order is unspecified:
+// the records it produces are summed as integers.
+__global__ void __launch_bounds__(256)
+    k_tc_qhist(const int64_t *__restrict__ q_indptr, const int2 *__restrict__ qcold,
+               const int32_t *__restrict__ qcold_n, int64_t n_q, int32_t win_rows, int64_t dim,
+               int32_t *__restrict__ count) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * 8;
+  for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < n_q; r += warps) {
+    const int64_t b = q_indptr[r];
+    const int n = qcold_n[r];
+    int32_t *cnt = count + (r / win_rows) * (dim + 1);
+    for (int j = lane; j < n; j += 32) atomicAdd(cnt + __ldg(qcold + b + j).x, 1);
+  }
+}
+
+__global__ void __launch_bounds__(256)
+    k_tc_qscatter(const int64_t *__restrict__ q_indptr, const int2 *__restrict__ qcold,
+                  const int32_t *__restrict__ qcold_n, int64_t n_q, int32_t win_rows, int64_t dim,
+                  int32_t *__restrict__ cursor, int2 *__restrict__ qpost) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * 8;
+  for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < n_q; r += warps) {
+    const int64_t b = q_indptr[r];
+    const int n = qcold_n[r];
+    const int64_t w = r / win_rows;
+    int32_t *cur = cursor + w * (dim + 1);
+    const int row = (int)(r - w * win_rows);
+    for (int j = lane; j < n; j += 32) {
+      const int2 e = __ldg(qcold + b + j);
+      qpost[atomicAdd(cur + e.x, 1)] = make_int2(row, e.y);
+    }
   }
 }
 
@@ -504,6 +555,7 @@ struct PrepArgs {
   uint16_t *op;           // operand tiles (hi part, lo part)
   int2 *qcold;            // queries: {dim, normalised value bits} at the row's CSR positions
   int32_t *qcold_n;       // queries: cold entries per row
+  int64_t dim;            // queries: indices outside [0, dim) are left out and reported
   int32_t *status;
 };
 
@@ -543,7 +595,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_tc_prep_queries(const PrepArgs
   const unsigned lt = (1u << lane) - 1u;
   const int Hp = a.Hp, G = 16 * Hp;  // halves per group
   uint16_t *gs = grp[warp];
-  bool bad = false;
+  bool bad = false, outside = false;
   for (int64_t g = (int64_t)blockIdx.x * (kPrepThreads / 32) + warp; g < a.n_groups;
        g += (int64_t)gridDim.x * (kPrepThreads / 32)) {
     for (int o = lane * 8; o < G; o += 256) *reinterpret_cast<uint4 *>(gs + o) = make_uint4(0u, 0u, 0u, 0u);
@@ -566,10 +618,15 @@ __global__ void __launch_bounds__(kPrepThreads) k_tc_prep_queries(const PrepArgs
           x = __ldg(a.val + p) * iv;
           ss = fmaf(x, x, ss);
           bad |= !(fabsf(x) <= kMaxNormalised);
-          h = find_hot(hkeys, hvals, k);
-          if (h >= 0) put_split(gs, rr, h, Hp, x);
+          if (k < 0 || (int64_t)k >= a.dim) {
+            outside = true;
+            h = -2;  // neither hot nor a cold entry (and never looked up: -1 marks empty slots)
+          } else {
+            h = find_hot(hkeys, hvals, k);
+            if (h >= 0) put_split(gs, rr, h, Hp, x);
+          }
         }
-        const bool cold = have && h < 0;
+        const bool cold = have && h == -1;
         const unsigned m = __ballot_sync(0xffffffffu, cold);
         if (cold) a.qcold[b + nc + __popc(m & lt)] = make_int2(k, __float_as_int(x));
         nc += __popc(m);
@@ -583,38 +640,15 @@ __global__ void __launch_bounds__(kPrepThreads) k_tc_prep_queries(const PrepArgs
     store_group(a.op, gs, g, a.gpt, Hp, lane);
     __syncwarp();
   }
+  if (__any_sync(0xffffffffu, outside) && lane == 0) flag(a.status, DEV_OUT_OF_RANGE);
   if (__any_sync(0xffffffffu, bad) && lane == 0) flag(a.status, DEV_RANGE);
 }
 
-// The item operand of a chunk from its hot slab, and the normalised copy
-// of the chunk's list entries, in one launch: the first `prep_blocks`
-// blocks take groups of 8 items (one warp a group; lane l reads row l / 4,
-// hot columns 32 (l % 4) .. + 31 as eight float4 loads issued together;
-// every K column written, zeros past the chunk; the inverse norms are
-// checked against the items' sums of squares), the other blocks rewrite the
-// list entries as {item, v * inv_i[item]}.
-struct ItemPrepArgs {
-  PrepArgs p;
-  int64_t prep_blocks;
-  const int32_t *col_ptr;  // the chunk's [dim + 1]
-  int32_t dim;
-  int64_t capacity;
-  const uint16_t *post_item;
-  const float *post_val;
-  int2 *post_hat;
-};
-
-__global__ void __launch_bounds__(kPrepThreads) k_tc_prep_items(const ItemPrepArgs ia) {
-  const PrepArgs &a = ia.p;
-  if ((int64_t)blockIdx.x >= ia.prep_blocks) {
-    const int64_t nb = gridDim.x - ia.prep_blocks, b = blockIdx.x - ia.prep_blocks;
-    const int64_t p0 = __ldg(ia.col_ptr), p1 = min((int64_t)__ldg(ia.col_ptr + ia.dim), ia.capacity);
-    for (int64_t p = p0 + b * kPrepThreads + threadIdx.x; p < p1; p += nb * kPrepThreads) {
-      const int it = ia.post_item[p];
-      ia.post_hat[p] = make_int2(it, __float_as_int(ia.post_val[p] * __ldg(a.inv + it)));
-    }
-    return;
-  }
+// The item operand of a chunk from its hot slab: one warp per group of 8
+// items (lane l reads row l / 4, hot columns 32 (l % 4) .. + 31 as eight
+// float4 loads issued together); every K column written, zeros past the
+// chunk; the inverse norms are checked against the items' sums of squares.
+__global__ void __launch_bounds__(kPrepThreads) k_tc_prep_items(const PrepArgs a) {
   __shared__ __align__(16) uint16_t grp[kPrepThreads / 32][8 * 2 * kHotMax];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int Hp = a.Hp;
@@ -622,7 +656,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_tc_prep_items(const ItemPrepAr
   uint16_t *gs = grp[warp];
   bool bad = false;
   for (int64_t g = (int64_t)blockIdx.x * (kPrepThreads / 32) + warp; g < a.n_groups;
-       g += ia.prep_blocks * (kPrepThreads / 32)) {
+       g += (int64_t)gridDim.x * (kPrepThreads / 32)) {
     const int64_t r = g * 8 + rr;
     const bool in = r < a.n_rows;
     const float iv = in ? __ldg(a.inv + r) : 0.f;
@@ -652,52 +686,80 @@ __global__ void __launch_bounds__(kPrepThreads) k_tc_prep_items(const ItemPrepAr
 }
 
 // ---------------------------------------------------------------- records
+// The cold products of one scoring call, as records {position in the
+// 32 x 32 swizzled staging tile of a bucket, fixed-point product}, a bucket
+// being (32 query rows, 32 items).  One block per (32-item column block,
+// query window): each of its warps takes one item and walks the item's cold
+// entries against the window's query lists (CSC by dimension, built once
+// per query matrix), laid end to end 32 entries at a time.  Records go to a
+// shared-memory buffer as they come, with a count per quarter (32 rows) of
+// the window; the block then sorts them by quarter in shared memory (a
+// counting sort) and writes them out as one contiguous segment of the
+// call's record array, at a place taken from a global cursor, with the
+// quarters' offsets beside it.  A bucket's records are then one contiguous
+// run, and every store is a coalesced one.  Blocks with more records than
+// the buffer holds walk their lists a second time and store each record
+// straight at its sorted place; blocks whose records do not fit the array
+// are marked (start -1) and the scorer computes their buckets from the
+// lists itself.  The order inside a bucket does not matter: the epilogue
+// sums integers.
+constexpr int kRecCap = 12288;        // records a block sorts in shared memory
+constexpr int kMaxQpw = 256;          // quarters of 32 rows in one query window, at most
+constexpr int kRecSmem = 2 * kRecCap * 8 + 3 * (kMaxQpw + 1) * 4;
+
 struct RecArgs {
-  const int64_t *q_indptr;
-  const int2 *qcold;
-  const int32_t *qcold_n;
+  const int2 *icold;       // items' cold entries {dim, raw value bits}
+  const int2 *icold_rng;   // per item of the chunk: {first entry, count}
+  const float *inv_i;      // the chunk's inverse norms
+  int32_t n_items;
+  const int32_t *qcol_ptr; // [n_win][dim + 1]: positions into qpost
+  const int2 *qpost;       // {row within the window, normalised value bits}
+  int64_t dim;
   int64_t n_q;
-  const int32_t *col_ptr;  // the chunk's [dim + 1]
-  const int2 *post_hat;
+  int32_t win_rows;        // query rows per window (a multiple of 32)
+  int32_t qpw;             // win_rows / 32
   int32_t n_cb;            // column blocks of the chunk
-  int32_t bucket_cap;      // records a bucket holds
-  int2 *rec;               // [quarter][column block][bucket_cap]: {position in the 32 x 32
-                           // swizzled staging tile, fixed-point product}
-  int32_t *rec_n;          // [quarter][column block]: records in the bucket, -1 if they did not fit
+  int2 *rec;               // the call's records, segment by segment
+  int64_t rec_cap;
+  unsigned long long *cursor;  // records placed so far (zeroed per call)
+  int32_t *seg;            // per block (w * n_cb + cb): [0] segment start or -1,
+                           // [1 + j] offset of quarter j in the segment, j <= qpw
   int32_t *status;
 };
 
-// Calls f(item, product) for every cold product of query row r with the
-// chunk: one warp takes the row's cold entries 32 at a time, and their
-// posting lists, laid end to end, 32 entries at a time (lane -> list by a
-// binary search over the lists' running lengths).
+// Calls f(row in window, product) for every cold product of chunk item
+// `item` (k-th item of its column block) with the query rows of window w:
+// the warp takes the item's cold entries 32 at a time, and their query
+// lists, laid end to end, 32 entries at a time (lane -> list by an OR of
+// the lists' start bits).
 template <typename F>
-__device__ __forceinline__ void walk_row(const RecArgs &a, int64_t r, int lane, int4 *slots, F f) {
-  const int64_t qb = a.q_indptr[r];
-  const int cn = a.qcold_n[r];
+__device__ __forceinline__ void walk_item(const RecArgs &a, int item, int w, int lane, int4 *slots, F f) {
+  const int2 rng = __ldg(a.icold_rng + item);
+  const float inv = __ldg(a.inv_i + item);
+  const int32_t *qptr = a.qcol_ptr + (int64_t)w * (a.dim + 1);
   const unsigned lt = (1u << lane) - 1u;
-  for (int b0 = 0; b0 < cn; b0 += 32) {
+  for (int b0 = 0; b0 < rng.y; b0 += 32) {
     int s = 0, len = 0;
-    float qv = 0.f;
-    if (b0 + lane < cn) {
-      const int2 e = __ldg(a.qcold + qb + b0 + lane);
-      qv = __int_as_float(e.y);
-      s = __ldg(a.col_ptr + e.x);
-      len = __ldg(a.col_ptr + e.x + 1) - s;
+    float vv = 0.f;
+    if (b0 + lane < rng.y) {
+      const int2 e = __ldg(a.icold + rng.x + b0 + lane);
+      vv = __int_as_float(e.y) * inv;
+      s = __ldg(qptr + e.x);
+      len = __ldg(qptr + e.x + 1) - s;
     }
     // The non-empty lists move to the first lanes, in order.
     const unsigned nz = __ballot_sync(0xffffffffu, len > 0);
-    if (len > 0) slots[__popc(nz & lt)] = make_int4(s, len, __float_as_int(qv), 0);
+    if (len > 0) slots[__popc(nz & lt)] = make_int4(s, len, __float_as_int(vv), 0);
     __syncwarp();
     if (lane < __popc(nz)) {
       const int4 v = slots[lane];
       s = v.x;
       len = v.y;
-      qv = __int_as_float(v.z);
+      vv = __int_as_float(v.z);
     } else {
       s = 0;
       len = 0;
-      qv = 0.f;
+      vv = 0.f;
     }
     __syncwarp();
     const int incl = warp_incl_scan(len, lane);
@@ -708,10 +770,15 @@ __device__ __forceinline__ void walk_row(const RecArgs &a, int64_t r, int lane, 
     const unsigned lt_eq = (2u << lane) - 1u;
     for (int f0 = 0; f0 < L; f0 += 32 * kWalkUnroll) {
       int pos[kWalkUnroll];
-      float pq[kWalkUnroll];
+      float pv[kWalkUnroll];
       bool ok[kWalkUnroll];
+      const int nu = min(kWalkUnroll, (L - f0 + 31) >> 5);  // windows of 32 entries left (warp-uniform)
 #pragma unroll
       for (int u = 0; u < kWalkUnroll; ++u) {
+        ok[u] = false;
+        pos[u] = 0;
+        pv[u] = 0.f;
+        if (u >= nu) continue;
         const int w0 = f0 + 32 * u, fi = w0 + lane;
         const unsigned before = __ballot_sync(0xffffffffu, incl <= w0);  // lists ending at or before w0
         const bool starts = len > 0 && excl >= w0 && excl < w0 + 32;
@@ -723,7 +790,7 @@ __device__ __forceinline__ void walk_row(const RecArgs &a, int64_t r, int lane, 
         const int jj = j < 31 ? j : 31;
         const int sj = __shfl_sync(0xffffffffu, s, jj);
         const int ej = __shfl_sync(0xffffffffu, excl, jj);
-        pq[u] = __shfl_sync(0xffffffffu, qv, jj);
+        pv[u] = __shfl_sync(0xffffffffu, vv, jj);
         ok[u] = fi < L;
         pos[u] = sj + (fi - ej);
       }
@@ -731,60 +798,159 @@ __device__ __forceinline__ void walk_row(const RecArgs &a, int64_t r, int lane, 
 #pragma unroll
       for (int u = 0; u < kWalkUnroll; ++u) {
         ph[u] = make_int2(0, 0);
-        if (ok[u]) ph[u] = ld_keep_int2(a.post_hat + pos[u]);
+        if (ok[u]) ph[u] = ld_keep_int2(a.qpost + pos[u]);
       }
 #pragma unroll
       for (int u = 0; u < kWalkUnroll; ++u)
-        if (ok[u]) f(ph[u].x, cold_fix(pq[u], __int_as_float(ph[u].y)));
+        if (u < nu) f(ok[u], ph[u].x, ok[u] ? cold_fix(__int_as_float(ph[u].y), pv[u]) : 0);
     }
   }
 }
 
-// One block per 32 query rows (one warp per row): every cold product of
-// the rows with the chunk becomes a record in the bucket of its 32-item
-// column block, in a slot taken from the block's own counter (the order
-// inside a bucket does not matter: the epilogue sums integers).  A bucket
-// that fills up is marked (count -1); the scorer then takes that block's
-// cold products straight from the lists.
 __global__ void __launch_bounds__(kRThreads, 1) k_tc_records(const RecArgs a) {
-  extern __shared__ int rsm[];
-  int *cnt = rsm;  // [n_cb]
+  extern __shared__ __align__(16) unsigned char rsm[];
+  int2 *buf = reinterpret_cast<int2 *>(rsm);            // records as they come: {quarter << 10 | pos, p}
+  int2 *sorted = buf + kRecCap;                         // the same, by quarter: {pos, p}
+  int *cnt = reinterpret_cast<int *>(sorted + kRecCap); // [kMaxQpw + 1] per quarter, then offsets
+  int *off = cnt + (kMaxQpw + 1);
+  int *cur = off + (kMaxQpw + 1);
+  constexpr int kChunks = kRecCap / 32;                 // the buffer is handed out 32 slots at a time
   __shared__ int4 slots_all[kRThreads / 32][32];
+  __shared__ int fill[kChunks];                         // records in each chunk of the buffer
+  __shared__ int n_chunks, seg_start;
   int4 *slots = slots_all[threadIdx.x >> 5];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t Q = blockIdx.x;
-  const int64_t row0 = Q * 32;
-  const int nrows = (int)(a.n_q - row0 < 32 ? a.n_q - row0 : 32);
-  const int ncb = a.n_cb, cap = a.bucket_cap;
-  for (int c = tid; c < ncb; c += kRThreads) cnt[c] = 0;
+  const unsigned lt = (1u << lane) - 1u;
+  const int cb = blockIdx.x, w = blockIdx.y;
+  const int qpw = a.qpw;
+  for (int j = tid; j <= kMaxQpw; j += kRThreads) cnt[j] = 0;
+  if (tid == 0) n_chunks = 0;
   __syncthreads();
-  int2 *rq = a.rec + Q * ncb * (int64_t)cap;
-  for (int rl = warp; rl < nrows; rl += kRThreads / 32)
-    walk_row(a, row0 + rl, lane, slots, [&](int item, int p) {
-      const int cb = item >> 5;
-      const int slot = atomicAdd(&cnt[cb], 1);
-      if (slot < cap) rq[(int64_t)cb * cap + slot] = make_int2(stg_index(rl, item & 31), p);
+  const int item = cb * 32 + warp;
+  const bool have_item = item < a.n_items;
+  // The warp appends to its current chunk of 32 slots and takes a new one
+  // (one shared atomic) when the records of a step do not fit it.
+  int my_chunk = -1, my_fill = 32;
+  if (have_item)
+    walk_item(a, item, w, lane, slots, [&](bool ok, int row, int p) {
+      const unsigned m = __ballot_sync(0xffffffffu, ok);
+      if (!m) return;
+      const int n = __popc(m), rank = __popc(m & lt), room = 32 - my_fill;
+      int next = my_chunk;
+      if (n > room) {
+        if (lane == 0) {
+          next = atomicAdd(&n_chunks, 1);
+          if (my_chunk >= 0 && my_chunk < kChunks) fill[my_chunk] = 32;
+        }
+        next = __shfl_sync(0xffffffffu, next, 0);
+      }
+      if (ok) {
+        // {row << 5 | item within the block, product}: the quarter is
+        // key >> 10; counting and placing are left to the sort below.
+        const int c = rank < room ? my_chunk : next;
+        const int at = rank < room ? my_fill + rank : rank - room;
+        if (c < kChunks) buf[c * 32 + at] = make_int2((row << 5) | warp, p);
+      }
+      if (n > room) {
+        my_chunk = next;
+        my_fill = n - room;
+      } else {
+        my_fill += n;
+      }
     });
+  if (lane == 0 && my_chunk >= 0 && my_chunk < kChunks) fill[my_chunk] = my_fill;
   __syncthreads();
-  for (int c = tid; c < ncb; c += kRThreads) a.rec_n[Q * ncb + c] = cnt[c] <= cap ? cnt[c] : -1;
+  // Records per quarter (a warp per chunk of the buffer); when the buffer
+  // overflowed, the walk is repeated to count.
+  const int used = min(n_chunks, kChunks);
+  if (n_chunks <= kChunks) {
+    for (int c = warp; c < used; c += kRThreads / 32)
+      if (lane < fill[c]) atomicAdd(&cnt[buf[c * 32 + lane].x >> 10], 1);
+  } else if (have_item) {
+    walk_item(a, item, w, lane, slots, [&](bool ok, int row, int) {
+      if (ok) atomicAdd(&cnt[row >> 5], 1);
+    });
+  }
+  __syncthreads();
+  __shared__ int n_total;
+  if (warp == 0) {
+    // Offsets of the quarters: lane l scans quarters 8 l .. 8 l + 7.
+    static_assert(kMaxQpw == 256, "eight quarters per lane");
+    int v[8], sum = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[k] = cnt[8 * lane + k];
+      sum += v[k];
+    }
+    int run = warp_incl_scan(sum, lane) - sum;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      off[8 * lane + k] = run;
+      cur[8 * lane + k] = run;
+      run += v[k];
+    }
+    if (lane == 31) {
+      off[kMaxQpw] = run;
+      n_total = run;
+    }
+    const int total = __shfl_sync(0xffffffffu, run, 31);
+    if (lane == 0) {
+      int start = -1;
+      if (total > 0) {
+        const unsigned long long at = atomicAdd(a.cursor, (unsigned long long)total);
+        // When the array is full the scorer computes these buckets itself.
+        if (at + (unsigned long long)total <= (unsigned long long)a.rec_cap) start = (int)at;
+      }
+      seg_start = start;
+    }
+  }
+  __syncthreads();
+  const int start = seg_start, total = n_total;
+  int32_t *seg = a.seg + ((int64_t)w * a.n_cb + cb) * (qpw + 2);
+  for (int j = tid; j <= qpw; j += kRThreads) seg[1 + j] = off[j];
+  if (tid == 0) seg[0] = total > 0 ? start : 0;
+  if (total == 0 || start < 0) return;
+  int2 *dst = a.rec + start;
+  if (n_chunks <= kChunks) {
+    // Counting sort by quarter in shared memory (a warp per chunk of the
+    // buffer), then one coalesced copy.
+    for (int c = warp; c < used; c += kRThreads / 32) {
+      if (lane < fill[c]) {
+        const int2 r = buf[c * 32 + lane];
+        const int row = r.x >> 5;
+        sorted[atomicAdd(&cur[row >> 5], 1)] = make_int2(stg_index(row & 31, r.x & 31), r.y);
+      }
+    }
+    __syncthreads();
+    for (int j = tid; j < total; j += kRThreads) dst[j] = sorted[j];
+  } else {
+    // Too many to sort on chip: walk again and store each record at its place.
+    if (have_item)
+      walk_item(a, item, w, lane, slots, [&](bool ok, int row, int p) {
+        if (ok) dst[atomicAdd(&cur[row >> 5], 1)] = make_int2(stg_index(row & 31, warp), p);
+      });
+  }
 }
 
 // ---------------------------------------------------------------- scorer
 struct ScoreArgs {
+  CUtensorMap out_map;     // the output tile for bulk tensor stores (when use_tma)
+  int32_t use_tma;         // device-memory output with 16-byte rows: stores by the tensor map
   const uint16_t *A;       // query operand tiles
   const uint16_t *B;       // item operand tiles
-  const int2 *rec;
-  const int32_t *rec_n;
-  // For buckets that did not fit: the queries' cold entries and the chunk's
-  // normalised lists.
-  const int64_t *q_indptr;
-  const int2 *qcold;
-  const int32_t *qcold_n;
-  const int32_t *col_ptr;
-  const int2 *post_hat;
+  const int2 *rec;         // the call's records (k_tc_records)
+  const int32_t *seg;      // per (query window, column block): segment start, quarter offsets
+  int32_t qpw;             // quarters per query window
+  // For segments that did not fit: the items' cold entries, the chunk's
+  // inverse norms and the windows' query lists.
+  const int2 *icold;
+  const int2 *icold_rng;
+  const float *inv_i;
+  const int32_t *qcol_ptr;
+  const int2 *qpost;
+  int64_t dim;
   int64_t n_quarters;
   int32_t n_cb;
-  int32_t bucket_cap;
   float *out;
   int64_t ld_out;
   int64_t n_q;
@@ -797,9 +963,10 @@ struct ScoreArgs {
 };
 
 // Bytes of the scorer's dynamic shared memory for Hp hot columns: the item
-// tile (hi, lo: 1024 Hp), the query tile's lo and hi parts (256 Hp each,
-// separate so one can load while the other is read), the epilogue staging.
-size_t score_smem_bytes(int Hp) { return (size_t)1536 * Hp + kStgBytes; }
+// tile (hi, lo: 1024 Hp), one query part (256 Hp: the lo part, then the hi
+// part of each query tile), the epilogue staging (two tiles per warp, so a
+// tile's bulk store reads it while the warp fills the other).
+size_t score_smem_bytes(int Hp) { return (size_t)1280 * Hp + kStgBytes; }
 
 // Ties registers just loaded from tensor memory to the wait that completes
 // the load, so that no use of them is scheduled before it.
@@ -813,7 +980,7 @@ __device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[32]) {
 }
 
 __global__ void __launch_bounds__(kSThreads, 1)
-    k_tc_score(const ScoreArgs a) {
+    k_tc_score(const __grid_constant__ ScoreArgs a) {
   extern __shared__ __align__(1024) unsigned char sm[];
   __shared__ __align__(8) uint64_t bars[11];
   __shared__ uint32_t tmem_slot;
@@ -821,13 +988,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int Hp = a.Hp;
   const uint32_t bytesB = 1024u * (uint32_t)Hp, bytesApart = 256u * (uint32_t)Hp;
   unsigned char *sB = sm;                          // hi part, then lo part
-  unsigned char *sAlo = sm + bytesB;
-  unsigned char *sAhi = sAlo + bytesApart;
+  unsigned char *sA = sm + bytesB;                 // the query tile's lo part, then its hi part
   int *stg_all = reinterpret_cast<int *>(
-      (reinterpret_cast<uintptr_t>(sAhi + bytesApart) + 1023) & ~static_cast<uintptr_t>(1023));
+      (reinterpret_cast<uintptr_t>(sA + bytesApart) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t b_full = smem_u32(&bars[0]), b_free = smem_u32(&bars[1]);
-  const uint32_t lo_full = smem_u32(&bars[2]), lo_free = smem_u32(&bars[3]);
-  const uint32_t hi_full = smem_u32(&bars[4]), hi_free = smem_u32(&bars[5]);
+  // bars[2..3]: a query part landed / read by the MMAs (two phases per unit:
+  // the lo part, then the hi part).  bars[4..5] unused.
+  const uint32_t a_full = smem_u32(&bars[2]), a_free = smem_u32(&bars[3]);
   // bars[6..7]: accumulator b written (MMA commit); bars[8..9]: accumulator b
   // read out (one arrival per epilogue warp).
   const uint32_t acc_full0 = smem_u32(&bars[6]), acc_full1 = smem_u32(&bars[7]);
@@ -857,11 +1024,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
   if (warp == 0) {
     // ---- producer: the item tile when it changes, then per unit the query
-    // tile's lo part and hi part, each once the MMAs have released it.
+    // tile's lo part and hi part into the one query buffer, each once the
+    // MMAs have released it (copy k of the buffer: the lo part of unit k / 2
+    // for even k, its hi part for odd k).
     if (lane == 0) {
       int64_t prev_t = -1;
-      int nb = 0;             // item tile copies issued
-      int64_t n_lo = 0, n_hi = 0;  // query part copies issued
+      int nb = 0;         // item tile copies issued
+      int64_t na = 0;     // query part copies issued
       for (int64_t j = 0; j < nj; ++j) {
         const int64_t u = u0 + j, t = u / a.n_qtiles, g = u % a.n_qtiles;
         if (t != prev_t) {
@@ -872,21 +1041,20 @@ __global__ void __launch_bounds__(kSThreads, 1)
           prev_t = t;
         }
         const uint16_t *At = a.A + (size_t)g * (bytesApart);  // tile: hi part, lo part (halves)
-        if (j > 0 && !mbar_wait(lo_free, (uint32_t)((j - 1) & 1), a.status)) break;
-        mbar_expect_tx(lo_full, bytesApart);
-        bulk_g2s(smem_u32(sAlo), At + bytesApart / 2, bytesApart, lo_full);
-        ++n_lo;
-        if (j > 0 && !mbar_wait(hi_free, (uint32_t)((j - 1) & 1), a.status)) break;
-        mbar_expect_tx(hi_full, bytesApart);
-        bulk_g2s(smem_u32(sAhi), At, bytesApart, hi_full);
-        ++n_hi;
+        if (na > 0 && !mbar_wait(a_free, (uint32_t)((na - 1) & 1), a.status)) break;
+        mbar_expect_tx(a_full, bytesApart);
+        bulk_g2s(smem_u32(sA), At + bytesApart / 2, bytesApart, a_full);
+        ++na;
+        if (!mbar_wait(a_free, (uint32_t)((na - 1) & 1), a.status)) break;
+        mbar_expect_tx(a_full, bytesApart);
+        bulk_g2s(smem_u32(sA), At, bytesApart, a_full);
+        ++na;
       }
       // Every copy issued lands before the block exits, also when a wait
       // above gave up: copy k into a buffer is issued only after the phase
       // of copy k - 1 completed, so the phase of the last copy issued is the
       // one still open, and a bulk copy completes by itself.
-      if (n_lo > 0) mbar_wait(lo_full, (uint32_t)((n_lo - 1) & 1), a.status);
-      if (n_hi > 0) mbar_wait(hi_full, (uint32_t)((n_hi - 1) & 1), a.status);
+      if (na > 0) mbar_wait(a_full, (uint32_t)((na - 1) & 1), a.status);
       if (nb > 0) mbar_wait(b_full, (uint32_t)((nb - 1) & 1), a.status);
     }
   } else if (warp == 1) {
@@ -896,7 +1064,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       const uint32_t idesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
       const uint32_t sbo = 16u * (uint32_t)Hp, lbo = 128u;
       const uint32_t bhi = smem_u32(sB), blo = bhi + bytesB / 2;
-      const uint32_t alo = smem_u32(sAlo), ahi = smem_u32(sAhi);
+      const uint32_t aq = smem_u32(sA);
       int64_t prev_t = -1;
       int nb = 0;
       bool ok = true;
@@ -910,23 +1078,23 @@ __global__ void __launch_bounds__(kSThreads, 1)
         }
         const int b = (int)(j & 1);
         if (ok && j >= 2) ok = mbar_wait(b ? acc_free1 : acc_free0, (uint32_t)(((j - 2) >> 1) & 1), a.status);
-        if (ok) ok = mbar_wait(lo_full, (uint32_t)(j & 1), a.status);
+        if (ok) ok = mbar_wait(a_full, 0u, a.status);  // phase 2 j: the lo part
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(b * kN);
         for (int k = 0; k < Hp; k += 16)
-          mma_f16(d, smem_desc(alo + (uint32_t)(k / 8) * 128u, lbo, sbo),
+          mma_f16(d, smem_desc(aq + (uint32_t)(k / 8) * 128u, lbo, sbo),
                   smem_desc(bhi + (uint32_t)(k / 8) * 128u, lbo, sbo), idesc, k > 0 ? 1u : 0u);
-        mma_commit(lo_free);
-        if (!mbar_wait(hi_full, (uint32_t)(j & 1), a.status)) break;
+        mma_commit(a_free);
+        if (!mbar_wait(a_full, 1u, a.status)) break;  // phase 2 j + 1: the hi part
         tc_fence_after();
         for (int k = 0; k < Hp; k += 16)
-          mma_f16(d, smem_desc(ahi + (uint32_t)(k / 8) * 128u, lbo, sbo),
+          mma_f16(d, smem_desc(aq + (uint32_t)(k / 8) * 128u, lbo, sbo),
                   smem_desc(blo + (uint32_t)(k / 8) * 128u, lbo, sbo), idesc, 1u);
         for (int k = 0; k < Hp; k += 16)
-          mma_f16(d, smem_desc(ahi + (uint32_t)(k / 8) * 128u, lbo, sbo),
+          mma_f16(d, smem_desc(aq + (uint32_t)(k / 8) * 128u, lbo, sbo),
                   smem_desc(bhi + (uint32_t)(k / 8) * 128u, lbo, sbo), idesc, 1u);
-        mma_commit(hi_free);
+        mma_commit(a_free);
         mma_commit(b ? acc_full1 : acc_full0);
       }
       // Every MMA this thread issued has completed before the tensor memory
@@ -942,29 +1110,34 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // next block's accumulator columns one block ahead.
     const int qd = warp & 3;
     const int half = (warp - 2) >> 2;                 // 0: even column blocks, 1: odd ones
-    int *stg = stg_all + (warp - 2) * kStgInts;       // this warp's staging tile (swizzled)
+    int *stg_mine = stg_all + 2 * (warp - 2) * kStgInts;  // this warp's two staging tiles (swizzled)
     const bool vec = a.vec_ok != 0;
+    const bool tma = a.use_tma != 0;
     const int sw = lane & 7;
-    int *row = stg + lane * 32;
-    // Lanes 0..7: record counts of the unit's 8 column blocks (0 past the
-    // chunk or the queries).
-    auto load_bnd = [&](int64_t u) -> int {
+    int n_blocks = 0;                                 // blocks this warp has done (tile n_blocks % 2 next)
+    // Lanes 0..7: where the records of the unit's 8 column blocks start in
+    // the record array and how many there are (0 past the chunk or the
+    // queries; -1 when their segment did not fit and the bucket is computed
+    // from the lists here).
+    auto load_bnd = [&](int64_t u, int &beg) -> int {
       const int64_t t = u / a.n_qtiles, g = u % a.n_qtiles;
       const int64_t Q = g * 4 + qd;
       const int cb = (int)t * 8 + lane;
-      int v = 0;
-      if (Q < a.n_quarters && lane < 8 && cb < a.n_cb) v = ld_keep_int(a.rec_n + Q * a.n_cb + cb);
-      return v;
+      int n = 0;
+      beg = 0;
+      if (Q < a.n_quarters && lane < 8 && cb < a.n_cb) {
+        const int64_t w = Q / a.qpw;
+        const int ql = (int)(Q - w * a.qpw);
+        const int32_t *sg = a.seg + (w * a.n_cb + cb) * (int64_t)(a.qpw + 2);
+        const int st = ld_keep_int(sg), o0 = ld_keep_int(sg + 1 + ql), o1 = ld_keep_int(sg + 2 + ql);
+        n = st < 0 ? -1 : o1 - o0;
+        beg = st + o0;
+      }
+      return n;
     };
-    // Bucket of column block 0 of unit u (block c follows at c * bucket_cap).
-    auto bucket0 = [&](int64_t u) -> const int2 * {
-      const int64_t t = u / a.n_qtiles, g = u % a.n_qtiles;
-      const int64_t Q = g * 4 + qd;
-      return a.rec + (Q * a.n_cb + t * 8) * (int64_t)a.bucket_cap;
-    };
-    const int bcap = a.bucket_cap;
-    auto fetch = [&](int bnd, const int2 *bk, int c, int2(&dst)[kRecPerLane]) {
+    auto fetch = [&](int bnd, int bbeg, int c, int2(&dst)[kRecPerLane]) {
       const int n = __shfl_sync(0xffffffffu, bnd, c);
+      const int2 *bk = a.rec + __shfl_sync(0xffffffffu, bbeg, c);
 #pragma unroll
       for (int m = 0; m < kRecPerLane; ++m) {
         const int p = 32 * m + lane;
@@ -976,12 +1149,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // block live in register slot i, fetched two of its blocks ahead
     // (across units), so no copy waits on a load in flight.
     constexpr int kMine = kN / kColBlock / 2;
-    int bnd = nj > 0 ? load_bnd(u0) : 0, bnd_n = 0;
+    int bbeg = 0, bbeg_n = 0;
+    int bnd = nj > 0 ? load_bnd(u0, bbeg) : 0, bnd_n = 0;
     int2 R[kMine][kRecPerLane];
-    const int2 *bk = nj > 0 ? bucket0(u0) : a.rec, *bk_n = bk;
     if (nj > 0) {
-      fetch(bnd, bk + half * bcap, half, R[0]);
-      fetch(bnd, bk + (2 + half) * bcap, 2 + half, R[1]);
+      fetch(bnd, bbeg, half, R[0]);
+      fetch(bnd, bbeg, 2 + half, R[1]);
     }
     for (int64_t j = 0; j < nj; ++j) {
       const int64_t u = u0 + j, t = u / a.n_qtiles, g = u % a.n_qtiles;
@@ -992,10 +1165,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       __syncwarp();
       if (!ok) break;
       tc_fence_after();
-      if (j + 1 < nj) {
-        bnd_n = load_bnd(u + 1);
-        bk_n = bucket0(u + 1);
-      }
+      if (j + 1 < nj) bnd_n = load_bnd(u + 1, bbeg_n);
       const int64_t qrow0 = (g * 4 + qd) * 32;
       const int item0 = (int)t * kN;
       // Lane l stores items 4 (l % 8) .. + 3 of rows 4 s + l / 8 of each block.
@@ -1005,10 +1175,17 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
       for (int i = 0; i < kMine; ++i) {
         const int c = 2 * i + half;
+        int *stg = stg_mine + (n_blocks & 1) * kStgInts;
+        int *row = stg + lane * 32;
+        ++n_blocks;
         uint32_t rc[32];
         tmem_ld32(tbase + (uint32_t)(c * kColBlock), rc);  // lands during the record phase
-        if (i + 2 < kMine) fetch(bnd, bk + (c + 4) * bcap, c + 4, R[(i + 2) & 3]);
-        else if (j + 1 < nj) fetch(bnd_n, bk_n + (c + 4 - 2 * kMine) * bcap, c + 4 - 2 * kMine, R[(i + 2) & 3]);
+        if (i + 2 < kMine) fetch(bnd, bbeg, c + 4, R[(i + 2) & 3]);
+        else if (j + 1 < nj) fetch(bnd_n, bbeg_n, c + 4 - 2 * kMine, R[(i + 2) & 3]);
+        if (tma) {  // the bulk store of two blocks ago has read this staging tile
+          if (lane == 0) bulk_wait_read1();
+          __syncwarp();
+        }
 #pragma unroll
         for (int k = 0; k < 8; ++k) *reinterpret_cast<int4 *>(row + 4 * (k ^ sw)) = make_int4(0, 0, 0, 0);
         __syncwarp();
@@ -1017,28 +1194,40 @@ __global__ void __launch_bounds__(kSThreads, 1)
           if (R[i & 3][m].y != 0) atomicAdd(stg + R[i & 3][m].x, R[i & 3][m].y);
         {
           const int n = __shfl_sync(0xffffffffu, bnd, c);
-          const int2 *bc = bk + c * bcap;
-          for (int p = 32 * kRecPerLane + lane; p < n; p += 32) {
-            const int2 rr = __ldg(bc + p);
-            atomicAdd(stg + rr.x, rr.y);
+          const int2 *bc = a.rec + __shfl_sync(0xffffffffu, bbeg, c);
+          // Records past those held in registers: loads in batches of four
+          // per lane, issued before any of their adds.
+          for (int p0 = 32 * kRecPerLane; p0 < n; p0 += 128) {
+            int2 t4[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const int p = p0 + 32 * m + lane;
+              t4[m] = p < n ? ld_keep_int2(bc + p) : make_int2(0, 0);
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+              if (t4[m].y != 0) atomicAdd(stg + t4[m].x, t4[m].y);
           }
           if (n < 0) {
-            // The bucket did not fit: each lane walks its row's cold lists
-            // and keeps the items of this block (rare; exact, same sums).
-            const int64_t q = qrow0 + lane;
-            const int lo = (int)t * kN + c * kColBlock;
-            if (q < a.n_q) {
-              const int64_t qb = a.q_indptr[q];
-              const int cn = a.qcold_n[q];
-              for (int e = 0; e < cn; ++e) {
-                const int2 qe = __ldg(a.qcold + qb + e);
-                const float qv = __int_as_float(qe.y);
-                const int p1 = __ldg(a.col_ptr + qe.x + 1);
-                for (int p = __ldg(a.col_ptr + qe.x); p < p1; ++p) {
-                  const int2 ph = __ldg(a.post_hat + p);
-                  const int d = ph.x - lo;
-                  if ((unsigned)d < (unsigned)kColBlock)
-                    atomicAdd(stg + stg_index(lane, d), cold_fix(qv, __int_as_float(ph.y)));
+            // The segment did not fit the record array: each lane walks its
+            // item's cold entries against the window's query lists and keeps
+            // the rows of this quarter (rare; exact, the same integers).
+            const int item = item0 + c * kColBlock + lane;
+            const int64_t Q = g * 4 + qd;
+            const int64_t w = Q / a.qpw;
+            const int ql = (int)(Q - w * a.qpw);
+            if (item < a.n_items) {
+              const int2 rng = __ldg(a.icold_rng + item);
+              const float inv = __ldg(a.inv_i + item);
+              const int32_t *qptr = a.qcol_ptr + w * (a.dim + 1);
+              for (int e = 0; e < rng.y; ++e) {
+                const int2 ie = __ldg(a.icold + rng.x + e);
+                const float vv = __int_as_float(ie.y) * inv;
+                const int p1 = __ldg(qptr + ie.x + 1);
+                for (int p = __ldg(qptr + ie.x); p < p1; ++p) {
+                  const int2 ph = __ldg(a.qpost + p);
+                  if ((ph.x >> 5) == ql)
+                    atomicAdd(stg + stg_index(ph.x & 31, lane), cold_fix(__int_as_float(ph.y), vv));
                 }
               }
             }
@@ -1059,10 +1248,21 @@ __global__ void __launch_bounds__(kSThreads, 1)
           *reinterpret_cast<float4 *>(chunk) = o;
         }
         __syncwarp();
-        // Row-contiguous stores: lane l writes items 4 (l % 8) .. + 3 of
-        // rows 4 s + l / 8 (chunk l % 8 of the row, found through the swizzle).
         const int it = item0 + c * kColBlock + 4 * (lane & 7);
-        if (vec && rows_whole && item0 + (c + 1) * kColBlock <= a.n_items) {
+        if (tma) {
+          // One bulk tensor store of the tile (its layout is the map's
+          // 128-byte swizzle); rows past the queries and columns past the
+          // chunk are left out by the map's bounds.
+          fence_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            if (qrow0 < a.n_q && item0 + c * kColBlock < a.n_items)
+              tma_store_2d(&a.out_map, smem_u32(stg), item0 + c * kColBlock, (int)qrow0);
+            bulk_commit();  // one group per block, empty or not, so the wait above counts blocks
+          }
+        } else if (vec && rows_whole && item0 + (c + 1) * kColBlock <= a.n_items) {
+          // Row-contiguous stores: lane l writes items 4 (l % 8) .. + 3 of
+          // rows 4 s + l / 8 (chunk l % 8 of the row, found through the swizzle).
 #pragma unroll
           for (int sidx = 0; sidx < 8; ++sidx) {
             const int rl = 4 * sidx + (lane >> 3);
@@ -1089,11 +1289,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
         __syncwarp();
       }
       bnd = bnd_n;
-      bk = bk_n;
+      bbeg = bbeg_n;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b ? acc_free1 : acc_free0);
     }
+    // The bulk stores this warp issued complete before the block exits
+    // (also after a wait above gave up: a bulk store completes by itself).
+    if (tma && lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   // Tensor-memory reads of every warp are ordered before the release.
   tc_fence_before();
@@ -1204,24 +1408,20 @@ cudaError_t launch_build_tc(ss_handle *h, const ss_csr &items, int64_t row_begin
   h->n_views = 0;
   if (n_chunks < 1 || n_chunks > h->build_batch) return cudaErrorInvalidValue;
   cudaError_t e = cudaSuccess;
-  if (!h->tc_slab) {
+  if (!h->tc_slab) {  // the three exist together or not at all (reset_after_oom)
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
-    if ((e = dev_alloc(&h->tc_slab, sizeof(float) * (size_t)h->build_batch * C * kHotMax)) != cudaSuccess)
-      return e;
-    if ((e = dev_alloc(&h->tc_sq, sizeof(float) * (size_t)h->build_batch * C)) != cudaSuccess) return e;
+    const size_t rows = (size_t)h->build_batch * C;
+    if ((e = dev_alloc(&h->tc_slab, sizeof(float) * rows * kHotMax)) != cudaSuccess) return e;
+    if ((e = dev_alloc(&h->tc_sq, sizeof(float) * rows)) != cudaSuccess) return e;
+    if ((e = dev_alloc(&h->tc_icold_rng, sizeof(int2) * rows)) != cudaSuccess) return e;
   }
-  const int64_t stride = h->dim + 1;
-  const int64_t n = stride * n_chunks;
-  if ((e = cudaMemsetAsync(h->col_cnt, 0, sizeof(int32_t) * (size_t)n, s)) != cudaSuccess) return e;
   const int grid = (h->sm_count > 0 ? h->sm_count : 148) * 8;
-  k_tc_hist<<<grid, 256, 0, s>>>(items.indptr, items.indices, row_begin, row_end, C, n_chunks, h->dim,
-                                 h->tc_hot, h->col_cnt, h->d_status);
-  if ((e = launch_count_scan(h->col_cnt, n, h->scan_part, h->col_ptr, s)) != cudaSuccess) return e;
-  k_tc_scatter<<<grid, 256, 0, s>>>(items.indptr, items.indices, items.values, row_begin, row_end, C,
-                                    h->dim, h->tc_hot, h->col_cnt, h->post_item, h->post_val,
-                                    h->post_cap, h->tc_slab, h->tc_sq, h->d_status);
+  // The build's cold entries go to the entry array sized for the matrix
+  // (post_hat, post_cap >= items.nnz), at the rows' own positions.
+  k_tc_build<<<grid, 256, 0, s>>>(items.indptr, items.indices, items.values, row_begin, row_end, C, h->dim,
+                                  h->tc_hot, h->tc_slab, h->tc_sq, h->post_hat, h->tc_icold_rng, h->d_status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  *queued = 5;
+  *queued = 1;
   for (int k = 0; k < n_chunks; ++k) {
     ss_index &ix = h->views[k];
     ix = ss_index();
@@ -1230,17 +1430,69 @@ cudaError_t launch_build_tc(ss_handle *h, const ss_csr &items, int64_t row_begin
     ix.row_end = std::min<int64_t>(ix.row_begin + C, row_end);
     ix.n_items = (int32_t)(ix.row_end - ix.row_begin);
     ix.dim = h->dim;
-    ix.col_ptr = h->col_ptr + (size_t)k * stride;
-    ix.post_item = h->post_item;
-    ix.post_val = h->post_val;
     ix.capacity = h->post_cap;
     ix.hot = h->tc_hot;
     ix.slab = h->tc_slab + (size_t)k * C * kHotMax;
     ix.slab_ld = kHotMax;
     ix.sq = h->tc_sq + (size_t)k * C;
+    ix.icold = h->post_hat;
+    ix.icold_rng = h->tc_icold_rng + (size_t)k * C;
   }
   h->n_views = n_chunks;
   return cudaSuccess;
+}
+
+// The driver's tensor-map encoder, looked up once (null when unavailable).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// A tensor map of the output tile (n_q rows x n_items floats, row stride
+// ld floats) in boxes of 32 x 32 with the 128-byte swizzle of the scorer's
+// staging tiles.  Only for device memory (not page-locked host memory
+// mapped into the device); false when the map cannot be made, and the
+// scorer then stores with plain instructions.
+static bool encode_out_map(CUtensorMap *map, float *out, int64_t n_q, int64_t n_items, int64_t ld) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode || n_q <= 0 || n_items <= 0 || (reinterpret_cast<uintptr_t>(out) & 15) != 0 || (ld & 3) != 0)
+    return false;
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, out) != cudaSuccess || attr.type != cudaMemoryTypeDevice) {
+    cudaGetLastError();
+    return false;
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)n_items, (cuuint64_t)n_q};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * sizeof(float)};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t elem[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, out, dims, strides, box, elem,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Query rows per window of the query side's inverted index: as many as keep
+// a records block (32 items x the window) near three quarters of kRecCap
+// records on the sample's estimate of shared cold dimensions per pair (the
+// blocks' records spread about 25% above their mean on Zipf data), a
+// multiple of 32, at most kMaxQpw quarters; windows as equal as that allows.
+static int window_rows(int64_t n_q, double est_cold) {
+  const double per_row = 32.0 * std::max(est_cold, 1e-9);
+  int64_t cap = (int64_t)std::floor(0.75 * kRecCap / per_row);
+  cap = std::max<int64_t>(32, std::min<int64_t>(32 * kMaxQpw, cap / 32 * 32));
+  const int64_t n_win = std::max<int64_t>(1, (n_q + cap - 1) / cap);
+  const int64_t rows = (n_q + n_win - 1) / n_win;
+  return (int)std::min<int64_t>(cap, (rows + 31) / 32 * 32);
 }
 
 cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, const ss_index &idx,
@@ -1254,16 +1506,25 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
   const int64_t n_qtiles = (n_q + kM - 1) / kM;
   const int32_t n_items = idx.n_items;
   const int64_t n_tiles = (n_items + kN - 1) / kN;
+  const int64_t dim = idx.dim;
   cudaError_t e = cudaSuccess;
   int nq = 0;
 
-  // Query operand and cold entries, once per query matrix, inverse norms and hot set.
+  // Query operand, cold entries and the windows' inverted index, once per
+  // query matrix, inverse norms and hot set.
   if (!(h->tcq_src[0] == q.indptr && h->tcq_src[1] == q.indices && h->tcq_src[2] == q.values &&
         h->tcq_src[3] == inv_q && h->tcq_rows == q.n_rows && h->tcq_nnz == q.nnz &&
         h->tcq_generation == h->tc_hot_generation)) {
+    const int win = window_rows(n_q, h->tc_est_cold);
+    const int64_t n_win = (n_q + win - 1) / win;
+    const int64_t n_cnt = n_win * (dim + 1);
     if ((e = grow(&h->tc_A, &h->tc_A_cap, n_qtiles * kM * 2 * Hp, s)) != cudaSuccess) return e;
     if ((e = grow(&h->tc_qcold, &h->tc_qcold_cap, std::max<int64_t>(1, q.nnz), s)) != cudaSuccess) return e;
     if ((e = grow(&h->tc_qcold_n, &h->tc_qcold_n_cap, n_q, s)) != cudaSuccess) return e;
+    if ((e = grow(&h->tc_qpost, &h->tc_qpost_cap, std::max<int64_t>(1, q.nnz), s)) != cudaSuccess) return e;
+    if ((e = grow(&h->tc_qcnt, &h->tc_qcnt_cap, n_cnt, s)) != cudaSuccess) return e;
+    if ((e = grow(&h->tc_qptr, &h->tc_qptr_cap, n_cnt, s)) != cudaSuccess) return e;
+    if ((e = grow(&h->tc_qpart, &h->tc_qpart_cap, scan_tile_count(n_cnt) + 1, s)) != cudaSuccess) return e;
     PrepArgs pa;
     pa.indptr = q.indptr;
     pa.idx = q.indices;
@@ -1279,11 +1540,21 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     pa.op = h->tc_A;
     pa.qcold = h->tc_qcold;
     pa.qcold_n = h->tc_qcold_n;
+    pa.dim = dim;
     pa.status = h->d_status;
     const int64_t blocks = std::min<int64_t>((pa.n_groups + 7) / 8, (int64_t)sms * 8);
     k_tc_prep_queries<<<(unsigned)blocks, kPrepThreads, 0, s>>>(pa);
+    if ((e = cudaMemsetAsync(h->tc_qcnt, 0, sizeof(int32_t) * (size_t)n_cnt, s)) != cudaSuccess) return e;
+    const int64_t row_blocks = std::min<int64_t>((n_q + 7) / 8, (int64_t)sms * 8);
+    k_tc_qhist<<<(unsigned)row_blocks, 256, 0, s>>>(q.indptr, h->tc_qcold, h->tc_qcold_n, n_q, win, dim,
+                                                    h->tc_qcnt);
+    if ((e = launch_count_scan(h->tc_qcnt, n_cnt, h->tc_qpart, h->tc_qptr, s)) != cudaSuccess) return e;
+    k_tc_qscatter<<<(unsigned)row_blocks, 256, 0, s>>>(q.indptr, h->tc_qcold, h->tc_qcold_n, n_q, win, dim,
+                                                       h->tc_qcnt, h->tc_qpost);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    ++nq;
+    nq += 6;
+    h->tc_win_rows = win;
+    h->tc_n_win = n_win;
     h->tcq_src[0] = q.indptr;
     h->tcq_src[1] = q.indices;
     h->tcq_src[2] = q.values;
@@ -1292,8 +1563,11 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     h->tcq_nnz = q.nnz;
     h->tcq_generation = h->tc_hot_generation;
   }
+  const int win = h->tc_win_rows;
+  const int64_t n_win = h->tc_n_win;
+  const int qpw = win / 32;
 
-  // Item operand and the normalised posting entries of this chunk.
+  // Item operand of this chunk.
   if ((e = grow(&h->tc_B, &h->tc_B_cap, n_tiles * kN * 2 * Hp, s)) != cudaSuccess) return e;
   {
     PrepArgs pa;
@@ -1311,46 +1585,46 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     pa.op = h->tc_B;
     pa.qcold = nullptr;
     pa.qcold_n = nullptr;
+    pa.dim = dim;
     pa.status = h->d_status;
-    ItemPrepArgs ia;
-    ia.p = pa;
-    ia.prep_blocks = std::min<int64_t>((pa.n_groups + 7) / 8, (int64_t)sms * 8);
-    ia.col_ptr = idx.col_ptr;
-    ia.dim = (int32_t)idx.dim;
-    ia.capacity = idx.capacity;
-    ia.post_item = idx.post_item;
-    ia.post_val = idx.post_val;
-    ia.post_hat = h->post_hat;
-    const int64_t norm_blocks = (int64_t)sms * 2;
-    k_tc_prep_items<<<(unsigned)(ia.prep_blocks + norm_blocks), kPrepThreads, 0, s>>>(ia);
+    const int64_t blocks = std::min<int64_t>((pa.n_groups + 7) / 8, (int64_t)sms * 8);
+    k_tc_prep_items<<<(unsigned)blocks, kPrepThreads, 0, s>>>(pa);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ++nq;
   }
 
-  // Cold records: a bucket per (32 query rows, 32 items) holding 3 times
-  // the sample's estimate of its records (at least 64, at most 1024); the
-  // scorer computes the blocks of fuller buckets from the lists.
+  // Cold records, a segment per (query window, 32-item column block), in an
+  // array sized at three times the sample's estimate (blocks past it are
+  // computed by the scorer from the lists).
   const int64_t n_quarters = (n_q + 31) / 32;
   const int32_t n_cb = (n_items + kColBlock - 1) / kColBlock;
   const double est = std::max(0.0, h->tc_est_cold);
-  const int32_t cap = (int32_t)std::min<double>(1024.0, std::max<double>(64.0, std::ceil((3.0 * est * 1024.0 + 64.0) / 32.0) * 32.0));
-  if ((e = grow(&h->tc_rec_off, &h->tc_rec_off_cap, n_quarters * n_cb, s)) != cudaSuccess) return e;
-  if ((e = grow(&h->tc_rec, &h->tc_rec_cap, n_quarters * n_cb * (int64_t)cap, s)) != cudaSuccess) return e;
+  const int64_t rec_cap = (int64_t)std::min<double>((double)INT32_MAX,
+                                                     3.0 * est * (double)n_q * (double)n_items + (double)(1 << 20));
+  if ((e = grow(&h->tc_seg, &h->tc_seg_cap, n_win * n_cb * (int64_t)(qpw + 2), s)) != cudaSuccess) return e;
+  if ((e = grow(&h->tc_rec, &h->tc_rec_cap, rec_cap, s)) != cudaSuccess) return e;
+  if ((e = grow(&h->tc_cursor, &h->tc_cursor_cap, 1, s)) != cudaSuccess) return e;
   {
     RecArgs ra;
-    ra.q_indptr = q.indptr;
-    ra.qcold = h->tc_qcold;
-    ra.qcold_n = h->tc_qcold_n;
+    ra.icold = idx.icold;
+    ra.icold_rng = idx.icold_rng;
+    ra.inv_i = inv_i;
+    ra.n_items = n_items;
+    ra.qcol_ptr = h->tc_qptr;
+    ra.qpost = h->tc_qpost;
+    ra.dim = dim;
     ra.n_q = n_q;
-    ra.col_ptr = idx.col_ptr;
-    ra.post_hat = h->post_hat;
+    ra.win_rows = win;
+    ra.qpw = qpw;
     ra.n_cb = n_cb;
-    ra.bucket_cap = cap;
     ra.rec = h->tc_rec;
-    ra.rec_n = h->tc_rec_off;
+    ra.rec_cap = rec_cap;
+    ra.cursor = h->tc_cursor;
+    ra.seg = h->tc_seg;
     ra.status = h->d_status;
-    const size_t smem = sizeof(int) * (size_t)n_cb;
-    k_tc_records<<<(unsigned)n_quarters, kRThreads, smem, s>>>(ra);
+    if ((e = ensure_dyn_smem(k_tc_records, kRecSmem)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(h->tc_cursor, 0, sizeof(unsigned long long), s)) != cudaSuccess) return e;
+    k_tc_records<<<dim3((unsigned)n_cb, (unsigned)n_win), kRThreads, kRecSmem, s>>>(ra);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ++nq;
   }
@@ -1369,15 +1643,16 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     sa.A = h->tc_A;
     sa.B = h->tc_B;
     sa.rec = h->tc_rec;
-    sa.rec_n = h->tc_rec_off;
-    sa.q_indptr = q.indptr;
-    sa.qcold = h->tc_qcold;
-    sa.qcold_n = h->tc_qcold_n;
-    sa.col_ptr = idx.col_ptr;
-    sa.post_hat = h->post_hat;
+    sa.seg = h->tc_seg;
+    sa.qpw = qpw;
+    sa.icold = idx.icold;
+    sa.icold_rng = idx.icold_rng;
+    sa.inv_i = inv_i;
+    sa.qcol_ptr = h->tc_qptr;
+    sa.qpost = h->tc_qpost;
+    sa.dim = dim;
     sa.n_quarters = n_quarters;
     sa.n_cb = n_cb;
-    sa.bucket_cap = cap;
     sa.out = dst;
     sa.ld_out = ld_dst;
     sa.n_q = n_q;
@@ -1386,6 +1661,7 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     sa.n_units = n_tiles * n_qtiles;
     sa.Hp = Hp;
     sa.vec_ok = ((reinterpret_cast<uintptr_t>(dst) % 16) == 0) && (ld_dst % 4 == 0);
+    sa.use_tma = sa.vec_ok && encode_out_map(&sa.out_map, dst, n_q, n_items, ld_dst) ? 1 : 0;
     sa.status = h->d_status;
     const int64_t grid = std::min<int64_t>(sms, sa.n_units);
     prof_mark(h, s);

@@ -112,6 +112,43 @@ def test_index_is_the_chunks_csc(sec, algorithm, name, n_i, rb, re):
     assert ex["item"].size + int((want_hot != 0).sum()) == chunk.nnz - int((coo.data[~keep] == 0).sum())
 
 
+@pytest.mark.parametrize("name,n_q", [("d1.2m_q5k_i200k", 5000), ("d65k_q1k_i10k", 1000),
+                                      ("d1.2m_q20k_i1m_heavy", 3000)])
+def test_query_side_index_is_each_windows_csc(sec, name, n_q):
+    """The tensor path's lists by dimension live on the query side (built
+    once per query matrix, in windows of query rows): each window's lists
+    must be the CSC of those query rows' cold nonzeros, normalised by the
+    rows' inverse norms (float32 products), bit for bit."""
+    cfg = CONFIGS[name]
+    Q, I = generate_rows(cfg, 0, 0, n_q), generate_rows(cfg, 1, 0, 9000)
+    with sec.SparseCosine(cfg.dim, chunk_rows=8192, algorithm="tensor") as h:
+        q, i = _dev(sec, Q), _dev(sec, I)
+        inv_q, inv_i = h.row_norms(q), h.row_norms(i)
+        idx = h.build_item_index(i, 0, 8192)
+        hot = h.index_export(idx)["hot"]
+        out = torch.empty((n_q, 8192), dtype=torch.float32, device="cuda")
+        h.score_chunk(q, inv_q, idx, inv_i, out, 8192)  # prepares the query side
+        h.check_device()
+        first = h.query_index_export(0)
+        windows = [h.query_index_export(w) for w in range(first["n_windows"])]
+        inv = inv_q.cpu().numpy()
+    W = first["win_rows"]
+    assert W % 32 == 0 and first["n_windows"] == -(-n_q // W)
+    rows = np.repeat(np.arange(n_q), np.diff(Q.indptr))
+    normed = (Q.values * inv[rows]).astype(np.float32)
+    for w, ex in enumerate(windows):
+        r0, r1 = w * W, min((w + 1) * W, n_q)
+        lo, hi = int(Q.indptr[r0]), int(Q.indptr[r1])
+        sub = sp.csr_matrix((normed[lo:hi], Q.indices[lo:hi], Q.indptr[r0:r1 + 1] - lo), shape=(r1 - r0, cfg.dim))
+        coo = sub.tocoo()
+        keep = ~np.isin(coo.col, hot)
+        csc = sp.csr_matrix((coo.data[keep], (coo.row[keep], coo.col[keep])), shape=sub.shape).tocsc()
+        csc.sort_indices()
+        assert np.array_equal(ex["col_ptr"].astype(np.int64), csc.indptr.astype(np.int64)), w
+        assert np.array_equal(ex["row"], csc.indices.astype(np.int32)), w
+        assert np.array_equal(ex["value"].view(np.uint32), csc.data.astype(np.float32).view(np.uint32)), w
+
+
 def test_index_export_rejects_item_tiles(sec):
     from sparse_embedding_exact_gb300 import SparseCosError, _abi
 
@@ -244,3 +281,26 @@ def test_full_matrix_of_the_1_2m_workload(sec):
             worst = max(worst, float(np.abs(got - ref).max()))
     print(f"full 5,000 x 200,000 matrix (algorithm {algo}): max |error| {worst:.3e}")
     assert worst <= TOL
+
+
+# ------------------------------------------------------------------ record overflow paths
+def test_tensor_records_beyond_every_buffer(sec):
+    """Queries far denser in the items' cold dimensions than the item sample
+    suggests: a block's records exceed its shared-memory sort (it walks its
+    lists a second time and stores each record at its place), and the call's
+    records exceed the array sized from the sample (the scorer computes those
+    buckets from the lists itself).  Every entry still matches the oracle."""
+    rng = np.random.default_rng(41)
+    d = 50_000
+    items = [(np.sort(rng.choice(d, 40, replace=False)), rng.lognormal(0, 1, 40)) for _ in range(8192)]
+    queries = [(np.sort(rng.choice(d, 400, replace=False)), rng.standard_normal(400)) for _ in range(2048)]
+    I, Q = csr_from_rows(items, d), csr_from_rows(queries, d)
+    with sec.SparseCosine(d, chunk_rows=8192, algorithm="tensor") as h:
+        q, i = _dev(sec, Q), _dev(sec, I)
+        inv_q, inv_i = h.row_norms(q), h.row_norms(i)
+        S = h.score_all(q, inv_q, i, inv_i)
+        h.check_device()
+        got = S.cpu().numpy().astype(np.float64)
+    err = float(np.abs(got - oracle.cosine(Q, I, f64=True)).max())
+    print(f"tensor path, records past every buffer: max |error| {err:.3e}")
+    assert err <= TOL
