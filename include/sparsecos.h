@@ -454,25 +454,28 @@ ss_status ss_index_export(ss_handle *h, const ss_index *idx, int32_t *n_hot, int
                           int64_t capacity, int64_t *n_entries, void *stream);
 
 /*
- * Reads back the tensor path's query-side inverted index into host memory;
- * for tests and inspection; synchronises `stream`.  On the tensor path the
- * lists by dimension are built on the query side, once per query matrix
- * (at its first scoring call), and every chunk's items are walked against
- * them.  The queries are cut into windows of *win_rows rows (*n_windows of
- * them); window `window` holds, for every dimension outside the hot set,
- * the list of its query rows in [window * win_rows, (window + 1) * win_rows):
- *   col_ptr[0 .. dim]: list k is entries [col_ptr[k], col_ptr[k + 1]);
- *   row[e]: the query row minus window * win_rows, ascending inside a list
+ * Reads back the lists that the tensor path's last scoring call used for
+ * its chunk, into host memory; for tests and inspection; synchronises
+ * `stream`.  The first call for a query matrix numbers the dimensions that
+ * some query row holds outside the hot set (n_dims of them, ascending); the
+ * first call after a build sorts the nonzeros of each of the build's
+ * chunks in those dimensions by number; the other nonzeros make no cold
+ * product and are left out:
+ *   dims[0 .. n_dims - 1]: the numbered dimensions, ascending;
+ *   col_ptr[0 .. n_dims]: list k (dimension dims[k]) is entries
+ *     [col_ptr[k], col_ptr[k + 1]);
+ *   item[e]: the item's row within the chunk, ascending inside a list
  *     (sorted here; the device keeps no order, which no sum depends on);
- *   value[e]: the normalised value q_k * inv_q[row] (float32 product).
- * Any output may be NULL; row and value need capacity >= *n_entries.
- * Errors: SS_ERR_INVALID_ARG (no query matrix prepared for the tensor path,
- * a window out of range), SS_ERR_LIMIT (capacity too small; *n_entries is
- * still written), SS_ERR_DEVICE_CHECK, SS_ERR_CUDA.
+ *   value[e]: the item's stored value (the inverse norms are applied by
+ *     each scoring call).
+ * Any output may be NULL; dims and col_ptr need room for dim + 1 entries,
+ * item and value capacity >= *n_entries.
+ * Errors: SS_ERR_INVALID_ARG (no tensor-path scoring call made yet),
+ * SS_ERR_LIMIT (capacity too small; *n_entries is still written),
+ * SS_ERR_DEVICE_CHECK, SS_ERR_CUDA.
  */
-ss_status ss_query_index_export(ss_handle *h, int64_t window, int32_t *win_rows, int64_t *n_windows,
-                                int32_t *col_ptr, int32_t *row, float *value, int64_t capacity,
-                                int64_t *n_entries, void *stream);
+ss_status ss_lists_export(ss_handle *h, int64_t *n_dims, int32_t *dims, int32_t *col_ptr, int32_t *item,
+                          float *value, int64_t capacity, int64_t *n_entries, void *stream);
 
 /* Size of the fixed scratch array behind ss_cosine_chunk_noalloc. */
 #define SS_NOALLOC_SCRATCH_BYTES (32u << 20)

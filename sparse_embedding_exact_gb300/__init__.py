@@ -365,24 +365,24 @@ class SparseCosine:
         return {"hot": hot[:H], "hot_values": hot_values[:, :H], "col_ptr": col_ptr,
                 "item": item[: n.value], "value": value[: n.value]}
 
-    def query_index_export(self, window: int = 0, stream=None) -> dict:
-        """The tensor path's query-side lists of one window, as host arrays
-        (after a scoring call prepared the queries; synchronises):
-        "win_rows", "n_windows", "col_ptr" (dim + 1), "row" (within the
-        window, ascending inside each list) and "value" (normalised)."""
+    def lists_export(self, stream=None) -> dict:
+        """The lists the tensor path's last scoring call used for its chunk,
+        as host arrays (synchronises): "dims" (the queries' cold dimensions,
+        ascending), "col_ptr" (len(dims) + 1), "item" (ascending inside each
+        list) and "value" (the items' stored values)."""
         lib = self._lib
-        wr, nw, n = ctypes.c_int32(0), ctypes.c_int64(0), ctypes.c_int64(0)
-        self._check(lib.ss_query_index_export(self._h, int(window), ctypes.byref(wr), ctypes.byref(nw), None,
-                                              None, None, 0, ctypes.byref(n), _stream_ptr(stream)),
-                    "ss_query_index_export")
+        nd, n = ctypes.c_int64(0), ctypes.c_int64(0)
+        self._check(lib.ss_lists_export(self._h, ctypes.byref(nd), None, None, None, None, 0, ctypes.byref(n),
+                                        _stream_ptr(stream)), "ss_lists_export")
+        dims = np.zeros(self.dim + 1, np.int32)
         col_ptr = np.zeros(self.dim + 1, np.int32)
-        row = np.zeros(max(1, n.value), np.int32)
+        item = np.zeros(max(1, n.value), np.int32)
         value = np.zeros(max(1, n.value), np.float32)
-        self._check(lib.ss_query_index_export(self._h, int(window), None, None, col_ptr.ctypes.data,
-                                              row.ctypes.data, value.ctypes.data, int(row.shape[0]),
-                                              ctypes.byref(n), _stream_ptr(stream)), "ss_query_index_export")
-        return {"win_rows": wr.value, "n_windows": nw.value, "col_ptr": col_ptr, "row": row[: n.value],
-                "value": value[: n.value]}
+        self._check(lib.ss_lists_export(self._h, ctypes.byref(nd), dims.ctypes.data, col_ptr.ctypes.data,
+                                        item.ctypes.data, value.ctypes.data, int(item.shape[0]), ctypes.byref(n),
+                                        _stream_ptr(stream)), "ss_lists_export")
+        k = nd.value
+        return {"dims": dims[:k], "col_ptr": col_ptr[: k + 1], "item": item[: n.value], "value": value[: n.value]}
 
     def invalidate(self):
         """Forget the hot set and the prepared queries (after in-place edits)."""

@@ -83,8 +83,7 @@ SIGNATURES = {
     "ss_invalidate": (_I32, [_P]),
     "ss_index_stats": (_I32, [_P, _P, ctypes.POINTER(ctypes.c_int64), _P]),
     "ss_index_export": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, ctypes.POINTER(_I64), _P]),
-    "ss_query_index_export": (_I32, [_P, _I64, ctypes.POINTER(_I32), ctypes.POINTER(_I64), _P, _P, _P, _I64,
-                                     ctypes.POINTER(_I64), _P]),
+    "ss_lists_export": (_I32, [_P, ctypes.POINTER(_I64), _P, _P, _P, _P, _I64, ctypes.POINTER(_I64), _P]),
     "ss_cosine_chunk_noalloc": (_I32, [_CSR, _CSR, _I64, _I64, _I64, _P, _I64, _P, _P]),
     "ss_kernel_launches": (ctypes.c_uint64, [_P]),
     "ss_inject_alloc_failure": (_I64, [_I64]),

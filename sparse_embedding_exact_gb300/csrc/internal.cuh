@@ -276,9 +276,10 @@ struct ss_handle {
   const void *tc_hot_src[3] = {nullptr, nullptr, nullptr};
   int64_t tc_hot_rows = -1, tc_hot_nnz = -1;
   uint64_t tc_hot_generation = 0;
-  // Query operand ([query tiles][kM x 2Hp] fp16) and cold entries ({dim,
-  // normalised value bits} at the row's own CSR positions; counts per row),
-  // for the query matrix, inverse norms and hot set they were made for.
+  // Query operand ([query tiles][kM x 2Hp] fp16) and cold entries ({cold
+  // number, normalised value bits} at the row's own CSR positions; counts
+  // per row), for the query matrix, inverse norms and hot set they were
+  // made for.
   uint16_t *tc_A = nullptr;
   int64_t tc_A_cap = 0;
   int2 *tc_qcold = nullptr;
@@ -288,16 +289,13 @@ struct ss_handle {
   const void *tcq_src[4] = {nullptr, nullptr, nullptr, nullptr};
   int64_t tcq_rows = -1, tcq_nnz = -1;
   uint64_t tcq_generation = ~0ull;
-  // The query side's inverted index, per window of tc_win_rows query rows
-  // (tc_n_win of them): counters and list offsets [n_win][dim + 1], the
-  // scan's tile sums, and the entries {row within the window, normalised
-  // value bits}.
+  // The numbering of the queries' cold dimensions: marks [dim + 1], their
+  // exclusive scan (the cold number of dimension d; d is held by some query
+  // iff entry d + 1 > entry d), the scan's tile sums; the count of numbers.
   int32_t *tc_qcnt = nullptr, *tc_qptr = nullptr, *tc_qpart = nullptr;
   int64_t tc_qcnt_cap = 0, tc_qptr_cap = 0, tc_qpart_cap = 0;
-  int2 *tc_qpost = nullptr;
-  int64_t tc_qpost_cap = 0;
-  int32_t tc_win_rows = 0;
-  int64_t tc_n_win = 0;
+  int64_t tc_n_cid = 0;
+  uint64_t tcq_serial = 0;  // counts query preparations
   // Per chunk of a build: raw hot values [chunk_rows][kHotMax], sums of
   // squares and {first cold entry, count} per item [chunk_rows] (the cold
   // entries themselves go to post_hat).
@@ -307,15 +305,24 @@ struct ss_handle {
   // Item operand of the chunk being scored ([item tiles][kN x 2Hp] fp16).
   uint16_t *tc_B = nullptr;
   int64_t tc_B_cap = 0;
-  // Cold records of one scoring call, segment by segment; per (query
-  // window, column block) the segment's start and its quarters' offsets;
-  // the records placed so far.
+  // The lists by cold number of every chunk of the last build, made at the
+  // first scoring call after the build or after a new query preparation:
+  // counters (then cursors) and offsets [n_chunks][n_cid + 1], the scan's
+  // tile sums, the entries {item within its chunk, raw value bits}; which
+  // build and queries they were made for, how many chunks, the chunk of the
+  // last scoring call.
+  int32_t *tc_ccnt = nullptr, *tc_cptr = nullptr, *tc_cpart = nullptr;
+  int64_t tc_ccnt_cap = 0, tc_cptr_cap = 0, tc_cpart_cap = 0;
+  int2 *tc_chat = nullptr;
+  int64_t tc_chat_cap = 0;
+  uint64_t tc_build_serial = 0, tc_lists_build = 0, tc_lists_queries = 0;
+  int32_t tc_lists_chunks = 0, tc_lists_last = 0;
+  // Cold records of one scoring call: sub-buckets of (8 query rows, 32
+  // items) and their counts (-1: did not fit).
   int2 *tc_rec = nullptr;
   int64_t tc_rec_cap = 0;
-  int32_t *tc_seg = nullptr;
-  int64_t tc_seg_cap = 0;
-  unsigned long long *tc_cursor = nullptr;
-  int64_t tc_cursor_cap = 0;
+  int32_t *tc_rec_n = nullptr;
+  int64_t tc_rec_n_cap = 0;
 
   // The last build's chunk indexes (views into the workspace above).
   ss_index views[kMaxBuildBatch];

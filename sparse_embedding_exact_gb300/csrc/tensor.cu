@@ -21,23 +21,26 @@
 // (2^-25 absolute for values in fp16's subnormal range).
 //
 // The remaining ("cold") dimensions are few per pair (0.11 expected on the
-// 1.2M-word workload).  A records kernel walks, for every block of 32 query
-// rows, each row's cold nonzeros against the chunk's posting lists (CSC by
-// dimension, the cold dimensions only) and writes one record per product,
-// bucketed by (32 query rows, 32 items): the position inside the bucket and
-// the product rounded to a fixed-point integer of resolution 2^-28.  The
-// scorer's epilogue adds a bucket's records into a 32 x 32 integer tile in
-// shared memory (integer sums do not depend on order, so the result is the
-// same bit for bit for any launch shape and chunking), adds that to the
-// tensor result and stores the tile.
+// 1.2M-word workload).  Once per query matrix the dimensions the queries
+// hold cold are numbered; each scoring call sorts the chunk's nonzeros in
+// those dimensions into lists by number (a counting sort: the chunk's
+// other nonzeros make no product), and a records kernel walks, for every
+// block of 8 query rows, each row's cold nonzeros against those lists and
+// writes one record per product, bucketed by (32 query rows, 32 items):
+// the position inside the bucket and the product rounded to a fixed-point
+// integer of resolution 2^-28.  The scorer's epilogue adds a bucket's
+// records into a 32 x 32 integer tile in shared memory (integer sums do not
+// depend on order, so the result is the same bit for bit for any launch
+// shape and chunking), adds that to the tensor result and stores the tile.
 //
-// Scorer (k_tc_score): persistent, one block per SM, 10 warps.  Warp 0
+// Scorer (k_tc_score): persistent, one block per SM, 18 warps.  Warp 0
 // loads operand tiles with bulk asynchronous copies (an item tile's operand
 // stays while the block works through its query tiles); warp 1 allocates
 // tensor memory and one of its threads issues the MMAs into one of two
-// accumulators; warps 2-9 run the epilogue, two per quarter of the 128
-// accumulator lanes (one takes the even 32-column blocks, the other the
-// odd ones), on one tile pair while the MMAs of the next run.
+// accumulators; warps 2-17 run the epilogue, four per quarter of the 128
+// accumulator lanes (each takes two of the eight 32-column blocks), on one
+// tile pair while the MMAs of the next run, and store each 32 x 32 tile
+// with one bulk tensor copy.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -70,13 +73,17 @@ constexpr float kFixInv = 1.0f / 268435456.0f;
 constexpr float kMaxNormalised = 1.0f + 1.0f / 1024.0f;  // |x| of a normalised value
 constexpr float kMaxSquareSum = 1.0f + 1.0f / 64.0f;     // sum of x^2 of a normalised row
 constexpr int kStgInts = 32 * 32;              // one staging tile: 32 rows x 32 ints, 128-byte swizzle
-constexpr int kEpiWarps = 8;                   // two per quarter of the accumulator lanes
+constexpr int kEpiWarps = 16;                  // four per quarter of the accumulator lanes
+constexpr int kWarpsPerQ = kEpiWarps / 4;      // epilogue warps per quarter
+constexpr int kMine = 8 / kWarpsPerQ;          // 32-column blocks per warp and tile pair
 constexpr int kSThreads = 64 + 32 * kEpiWarps; // producer, MMA, epilogue warps
-constexpr int kStgBytes = 2 * kEpiWarps * kStgInts * 4 + 1024;  // two tiles per warp, 1024-byte aligned
-constexpr int kRThreads = 1024;         // records: one warp per query row of the block
+constexpr int kStgTiles = kEpiWarps <= 8 ? 2 : 1;  // staging tiles per epilogue warp
+constexpr int kStgBytes = kEpiWarps * kStgTiles * kStgInts * 4 + 1024;  // 1024-byte aligned
+static_assert(kEpiWarps % 4 == 0 && 8 % kWarpsPerQ == 0, "whole blocks per epilogue warp");
+constexpr int kRThreads = 1024;         // records: one warp per query row of a 32-row block
 constexpr int kPrepThreads = 256;
 constexpr int kWalkUnroll = 8;          // list entries per lane loaded before use
-constexpr int kRecPerLane = 4;          // epilogue: records of a block held per lane (128 per block)
+constexpr int kRecPerLane = 4;          // epilogue: a block's first records per lane (128), fetched two blocks ahead
 constexpr long long kWaitNs = 2000000000ll;    // bounded waits: 2 s
 
 __device__ __forceinline__ void flag(int32_t *status, int32_t code) { atomicCAS(status, DEV_OK, code); }
@@ -125,11 +132,20 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 // Bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16),
-// completing as transaction bytes on `bar`.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+// completing as transaction bytes on `bar`, with an L2 policy for the
+// source lines.
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                              uint64_t policy) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
                : "memory");
+}
+// An L2 policy that keeps the lines it marks last: the operand tiles, read
+// again by the blocks that score their other tile pairs.
+__device__ __forceinline__ uint64_t evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 // Shared-memory matrix descriptor: K-major operand without swizzle, made of
 // core matrices of 8 rows x 16 bytes (128 contiguous bytes); lbo = bytes
@@ -191,12 +207,25 @@ __device__ __forceinline__ void fence_async_shared() {
 // Bulk tensor store of a box (the tensor map's 32 x 32 floats, 128-byte
 // swizzle) from shared memory to the tile at element (x, y), added to this
 // thread's bulk group.  Parts of the box outside the tensor are not written.
-__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int x, int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
-               "r"(src), "r"(x), "r"(y)
+__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int x, int y, uint64_t policy) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;"
+               ::"l"(tmap), "r"(src), "r"(x), "r"(y), "l"(policy)
                : "memory");
 }
+// An L2 policy that evicts the lines it marks first: the output, written
+// once and never read back here, should not push the operands and records
+// that the block still reads out of the cache.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Until all of this thread's bulk store groups have read their
+// shared-memory source.
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 // Until all but the most recent of this thread's bulk store groups have
 // read their shared-memory source.
 __device__ __forceinline__ void bulk_wait_read1() {
@@ -430,13 +459,13 @@ __global__ void __launch_bounds__(kSelThreads)
 }
 
 // ---------------------------------------------------------------- build
-// The item side of a chunk needs no inverted index: one pass over its CSR
+// The build does not depend on the queries: one pass over the chunk's CSR
 // rows (a warp per row, no atomics) writes each item's raw hot values into
 // the dense slab (0 where absent), its sum of squares, and its cold entries
 // {dim, raw value bits} packed in CSR order (dims ascending) at the row's
 // own positions relative to the build's first nonzero, with {first, count}
-// per item.  The inverted index is built once on the query side instead
-// (k_tc_qhist / k_tc_qscatter below), where it serves every chunk.
+// per item.  Each scoring call sorts these entries into lists over the
+// dimensions its queries hold (k_tc_chist / k_tc_cscatter below).
 __global__ void __launch_bounds__(256)
     k_tc_build(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
                const float *__restrict__ values, int64_t row_begin, int64_t row_end, int64_t chunk_rows,
@@ -492,42 +521,84 @@ __global__ void __launch_bounds__(256)
   if (__any_sync(0xffffffffu, bad) && lane == 0) flag(status, DEV_OUT_OF_RANGE);
 }
 
-// The query side's inverted index, once per query matrix, inverse norms and
-// hot set: the queries are cut into windows of `win_rows` rows, and per
-// window each cold dimension gets the list of its query rows (row within
-// the window, normalised value), a counting sort by (window, dimension):
-// the histogram here, a scan of the n_win x (dim + 1) counters
-// (launch_count_scan), then the scatter.  A list's order is unspecified:
-// the records it produces are summed as integers.
+// The query side's numbering of cold dimensions, once per query matrix,
+// inverse norms and hot set: every dimension that some query row holds as
+// a cold nonzero is marked (mark[d] = 1, the same value from every writer),
+// an exclusive scan of the marks (launch_count_scan) numbers the marked
+// dimensions 0, 1, ... in ascending order (cid[d]; cid[d + 1] > cid[d]
+// exactly for the marked ones), and the queries' cold entries then carry
+// that number in place of the dimension.  A chunk's lists are made over
+// these numbers only: a dimension no query row holds cold makes no product.
 __global__ void __launch_bounds__(256)
-    k_tc_qhist(const int64_t *__restrict__ q_indptr, const int2 *__restrict__ qcold,
-               const int32_t *__restrict__ qcold_n, int64_t n_q, int32_t win_rows, int64_t dim,
-               int32_t *__restrict__ count) {
+    k_tc_qmark(const int64_t *__restrict__ q_indptr, const int2 *__restrict__ qcold,
+               const int32_t *__restrict__ qcold_n, int64_t n_q, int32_t *__restrict__ mark) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * 8;
   for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < n_q; r += warps) {
     const int64_t b = q_indptr[r];
     const int n = qcold_n[r];
-    int32_t *cnt = count + (r / win_rows) * (dim + 1);
-    for (int j = lane; j < n; j += 32) atomicAdd(cnt + __ldg(qcold + b + j).x, 1);
+    for (int j = lane; j < n; j += 32) mark[__ldg(qcold + b + j).x] = 1;
   }
 }
 
 __global__ void __launch_bounds__(256)
-    k_tc_qscatter(const int64_t *__restrict__ q_indptr, const int2 *__restrict__ qcold,
-                  const int32_t *__restrict__ qcold_n, int64_t n_q, int32_t win_rows, int64_t dim,
-                  int32_t *__restrict__ cursor, int2 *__restrict__ qpost) {
+    k_tc_qcid(const int64_t *__restrict__ q_indptr, int2 *__restrict__ qcold, const int32_t *__restrict__ qcold_n,
+              int64_t n_q, const int32_t *__restrict__ cid) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * 8;
   for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < n_q; r += warps) {
     const int64_t b = q_indptr[r];
     const int n = qcold_n[r];
-    const int64_t w = r / win_rows;
-    int32_t *cur = cursor + w * (dim + 1);
-    const int row = (int)(r - w * win_rows);
-    for (int j = lane; j < n; j += 32) {
-      const int2 e = __ldg(qcold + b + j);
-      qpost[atomicAdd(cur + e.x, 1)] = make_int2(row, e.y);
+    for (int j = lane; j < n; j += 32) qcold[b + j].x = __ldg(cid + qcold[b + j].x);
+  }
+}
+
+// The lists of every chunk of a build (CSC by query cold number, one set
+// per chunk), made at the first scoring call that needs them: a counting
+// sort of the build's per-item cold entries by (chunk, cid), the entries of
+// dimensions no query holds cold left out.  The histogram here (a warp per
+// item), launch_count_scan over the n_chunks x (n_cid + 1) counters, then
+// the scatter, which writes {item within its chunk, raw value bits} (each
+// call's records kernel multiplies by that call's inverse norms).  A
+// list's order is unspecified: the records it makes are summed as
+// integers.  Items are numbered across the build: item `it` is row
+// it % chunk_rows of chunk it / chunk_rows.
+__global__ void __launch_bounds__(256)
+    k_tc_chist(const int2 *__restrict__ icold, const int2 *__restrict__ icold_rng, int64_t n_items,
+               int64_t chunk_rows, const int32_t *__restrict__ cid, int64_t n_ccnt, int32_t *__restrict__ count) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * 8;
+  for (int64_t it = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); it < n_items; it += warps) {
+    const int2 rng = __ldg(icold_rng + it);
+    int32_t *cnt = count + (it / chunk_rows) * n_ccnt;
+    for (int j = lane; j < rng.y; j += 32) {
+      const int d = __ldg(icold + rng.x + j).x;
+      const int c0 = __ldg(cid + d), c1 = __ldg(cid + d + 1);
+      if (c1 > c0) atomicAdd(cnt + c0, 1);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256)
+    k_tc_cscatter(const int2 *__restrict__ icold, const int2 *__restrict__ icold_rng, int64_t n_items,
+                  int64_t chunk_rows, const int32_t *__restrict__ cid, int64_t n_ccnt,
+                  int32_t *__restrict__ cursor, int2 *__restrict__ chat, int64_t capacity, int32_t *status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * 8;
+  for (int64_t it = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); it < n_items; it += warps) {
+    const int2 rng = __ldg(icold_rng + it);
+    const int64_t c = it / chunk_rows;
+    int32_t *cur = cursor + c * n_ccnt;
+    const int item = (int)(it - c * chunk_rows);
+    for (int j = lane; j < rng.y; j += 32) {
+      const int2 e = __ldg(icold + rng.x + j);
+      const int c0 = __ldg(cid + e.x), c1 = __ldg(cid + e.x + 1);
+      if (c1 <= c0) continue;
+      const int32_t pos = atomicAdd(cur + c0, 1);
+      if (pos >= 0 && (int64_t)pos < capacity)
+        chat[pos] = make_int2(item, e.y);
+      else
+        flag(status, DEV_CAPACITY);
     }
   }
 }
@@ -580,6 +651,24 @@ __device__ __forceinline__ void store_group(uint16_t *op, const uint16_t *gs, in
     *reinterpret_cast<uint4 *>(hi + o) = *reinterpret_cast<const uint4 *>(gs + o);
     *reinterpret_cast<uint4 *>(lo + o) = *reinterpret_cast<const uint4 *>(gs + P + o);
   }
+}
+
+// Writes a group buffer to group g of the query operand, whose tiles hold
+// four sub-parts in the order the MMAs read them: lo part K columns
+// [0, Hp/2), lo part [Hp/2, Hp), hi part [0, Hp/2), hi part [Hp/2, Hp); each
+// sub-part is `gpt` groups of 8 rows x Hp/2 halves in the same no-swizzle
+// K-major layout (in the group buffer a part's two halves are already
+// contiguous: core matrices of K columns >= Hp/2 follow those below).
+__device__ __forceinline__ void store_group_q(uint16_t *op, const uint16_t *gs, int64_t g, int gpt, int Hp,
+                                              int lane) {
+  const int64_t t = g / gpt, gl = g % gpt;
+  const int P = 4 * Hp;  // halves of one group sub-part (8 rows x Hp / 2)
+  uint16_t *tile = op + t * 4 * gpt * P + gl * P;
+  const int src[4] = {2 * P, 3 * P, 0, P};  // lo K0, lo K1, hi K0, hi K1 in the group buffer
+#pragma unroll
+  for (int sp = 0; sp < 4; ++sp)
+    for (int o = lane * 8; o < P; o += 256)
+      *reinterpret_cast<uint4 *>(tile + (int64_t)sp * gpt * P + o) = *reinterpret_cast<const uint4 *>(gs + src[sp] + o);
 }
 
 // One warp per group of 8 query rows: the rows' normalised hot values split
@@ -637,7 +726,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_tc_prep_queries(const PrepArgs
       if (lane == 0) a.qcold_n[r] = nc;
     }
     __syncwarp();
-    store_group(a.op, gs, g, a.gpt, Hp, lane);
+    store_group_q(a.op, gs, g, a.gpt, Hp, lane);
     __syncwarp();
   }
   if (__any_sync(0xffffffffu, outside) && lane == 0) flag(a.status, DEV_OUT_OF_RANGE);
@@ -686,111 +775,80 @@ __global__ void __launch_bounds__(kPrepThreads) k_tc_prep_items(const PrepArgs a
 }
 
 // ---------------------------------------------------------------- records
-// The cold products of one scoring call, as records {position in the
-// 32 x 32 swizzled staging tile of a bucket, fixed-point product}, a bucket
-// being (32 query rows, 32 items).  One block per (32-item column block,
-// query window): each of its warps takes one item and walks the item's cold
-// entries against the window's query lists (CSC by dimension, built once
-// per query matrix), laid end to end 32 entries at a time.  Records go to a
-// shared-memory buffer as they come, with a count per quarter (32 rows) of
-// the window; the block then sorts them by quarter in shared memory (a
-// counting sort) and writes them out as one contiguous segment of the
-// call's record array, at a place taken from a global cursor, with the
-// quarters' offsets beside it.  A bucket's records are then one contiguous
-// run, and every store is a coalesced one.  Blocks with more records than
-// the buffer holds walk their lists a second time and store each record
-// straight at its sorted place; blocks whose records do not fit the array
-// are marked (start -1) and the scorer computes their buckets from the
-// lists itself.  The order inside a bucket does not matter: the epilogue
-// sums integers.
-constexpr int kRecCap = 12288;        // records a block sorts in shared memory
-constexpr int kMaxQpw = 256;          // quarters of 32 rows in one query window, at most
-constexpr int kRecSmem = 2 * kRecCap * 8 + 3 * (kMaxQpw + 1) * 4;
-
+// The cold products of one scoring call become records {position in the
+// 32 x 32 swizzled staging tile of their bucket, fixed-point product}, a
+// bucket being (32 query rows, 32 items) with room for bucket_cap records
+// and a count (-1 when its records did not fit; the scorer then computes
+// the bucket from the lists).
 struct RecArgs {
-  const int2 *icold;       // items' cold entries {dim, raw value bits}
-  const int2 *icold_rng;   // per item of the chunk: {first entry, count}
-  const float *inv_i;      // the chunk's inverse norms
-  int32_t n_items;
-  const int32_t *qcol_ptr; // [n_win][dim + 1]: positions into qpost
-  const int2 *qpost;       // {row within the window, normalised value bits}
-  int64_t dim;
+  const int64_t *q_indptr;
+  const int2 *qcold;       // queries' cold entries {cid, normalised value bits}
+  const int32_t *qcold_n;
   int64_t n_q;
-  int32_t win_rows;        // query rows per window (a multiple of 32)
-  int32_t qpw;             // win_rows / 32
-  int32_t n_cb;            // column blocks of the chunk
-  int2 *rec;               // the call's records, segment by segment
-  int64_t rec_cap;
-  unsigned long long *cursor;  // records placed so far (zeroed per call)
-  int32_t *seg;            // per block (w * n_cb + cb): [0] segment start or -1,
-                           // [1 + j] offset of quarter j in the segment, j <= qpw
+  const int32_t *col_ptr;  // the chunk's lists: [n_cid + 1] offsets into chat
+  const int2 *chat;        // {item, raw value bits}
+  const float *inv_i;      // the chunk's inverse norms
+  int32_t n_cb;            // 32-item column blocks of the chunk
+  int32_t bucket_cap;      // records a bucket holds
+  int2 *rec;               // [quarter][column block][bucket_cap]
+  int32_t *rec_n;          // [quarter][column block]
   int32_t *status;
 };
 
-// Calls f(row in window, product) for every cold product of chunk item
-// `item` (k-th item of its column block) with the query rows of window w:
-// the warp takes the item's cold entries 32 at a time, and their query
-// lists, laid end to end, 32 entries at a time (lane -> list by an OR of
-// the lists' start bits).
+// Calls f(item, product) for every cold product of query row r with the
+// chunk.  One warp takes the row's cold entries 32 at a time and lays their
+// lists end to end; each lane then takes one list entry of every window of
+// 32, finding its list from the bits that mark where lists start inside
+// the window (a lane's list is the last one that starts at or before it).
 template <typename F>
-__device__ __forceinline__ void walk_item(const RecArgs &a, int item, int w, int lane, int4 *slots, F f) {
-  const int2 rng = __ldg(a.icold_rng + item);
-  const float inv = __ldg(a.inv_i + item);
-  const int32_t *qptr = a.qcol_ptr + (int64_t)w * (a.dim + 1);
-  const unsigned lt = (1u << lane) - 1u;
-  for (int b0 = 0; b0 < rng.y; b0 += 32) {
+__device__ __forceinline__ void walk_row(const RecArgs &a, int64_t r, int lane, int4 *slots, F f) {
+  const int64_t qb = a.q_indptr[r];
+  const int cn = a.qcold_n[r];
+  const unsigned lt = (1u << lane) - 1u, lt_eq = (2u << lane) - 1u;
+  for (int b0 = 0; b0 < cn; b0 += 32) {
     int s = 0, len = 0;
-    float vv = 0.f;
-    if (b0 + lane < rng.y) {
-      const int2 e = __ldg(a.icold + rng.x + b0 + lane);
-      vv = __int_as_float(e.y) * inv;
-      s = __ldg(qptr + e.x);
-      len = __ldg(qptr + e.x + 1) - s;
+    float qv = 0.f;
+    if (b0 + lane < cn) {
+      const int2 e = __ldg(a.qcold + qb + b0 + lane);
+      qv = __int_as_float(e.y);
+      s = __ldg(a.col_ptr + e.x);
+      len = __ldg(a.col_ptr + e.x + 1) - s;
     }
     // The non-empty lists move to the first lanes, in order.
     const unsigned nz = __ballot_sync(0xffffffffu, len > 0);
-    if (len > 0) slots[__popc(nz & lt)] = make_int4(s, len, __float_as_int(vv), 0);
+    if (len > 0) slots[__popc(nz & lt)] = make_int4(s, len, __float_as_int(qv), 0);
     __syncwarp();
     if (lane < __popc(nz)) {
       const int4 v = slots[lane];
       s = v.x;
       len = v.y;
-      vv = __int_as_float(v.z);
+      qv = __int_as_float(v.z);
     } else {
       s = 0;
       len = 0;
-      vv = 0.f;
+      qv = 0.f;
     }
     __syncwarp();
     const int incl = warp_incl_scan(len, lane);
     const int excl = incl - len;
     const int L = __shfl_sync(0xffffffffu, incl, 31);
-    // Lists that start inside a window of 32 entries set their start bit;
-    // a lane's list is the last one starting at or before it.
-    const unsigned lt_eq = (2u << lane) - 1u;
     for (int f0 = 0; f0 < L; f0 += 32 * kWalkUnroll) {
       int pos[kWalkUnroll];
-      float pv[kWalkUnroll];
+      float pq[kWalkUnroll];
       bool ok[kWalkUnroll];
-      const int nu = min(kWalkUnroll, (L - f0 + 31) >> 5);  // windows of 32 entries left (warp-uniform)
 #pragma unroll
       for (int u = 0; u < kWalkUnroll; ++u) {
-        ok[u] = false;
-        pos[u] = 0;
-        pv[u] = 0.f;
-        if (u >= nu) continue;
         const int w0 = f0 + 32 * u, fi = w0 + lane;
         const unsigned before = __ballot_sync(0xffffffffu, incl <= w0);  // lists ending at or before w0
         const bool starts = len > 0 && excl >= w0 && excl < w0 + 32;
         const unsigned m = __reduce_or_sync(0xffffffffu, starts ? (1u << ((excl - w0) & 31)) : 0u);
         const int first = __popc(before);  // the list holding entry w0 (if any entry is left)
-        const int starts_before = __popc(m & lt_eq);
         // If no list starts at w0 itself, entry w0 continues list `first`.
-        const int j = first + starts_before - ((m & 1u) ? 1 : 0);
+        const int j = first + __popc(m & lt_eq) - ((m & 1u) ? 1 : 0);
         const int jj = j < 31 ? j : 31;
         const int sj = __shfl_sync(0xffffffffu, s, jj);
         const int ej = __shfl_sync(0xffffffffu, excl, jj);
-        pv[u] = __shfl_sync(0xffffffffu, vv, jj);
+        pq[u] = __shfl_sync(0xffffffffu, qv, jj);
         ok[u] = fi < L;
         pos[u] = sj + (fi - ej);
       }
@@ -798,138 +856,41 @@ __device__ __forceinline__ void walk_item(const RecArgs &a, int item, int w, int
 #pragma unroll
       for (int u = 0; u < kWalkUnroll; ++u) {
         ph[u] = make_int2(0, 0);
-        if (ok[u]) ph[u] = ld_keep_int2(a.qpost + pos[u]);
+        if (ok[u]) ph[u] = ld_keep_int2(a.chat + pos[u]);
       }
+      float iv[kWalkUnroll];
+#pragma unroll
+      for (int u = 0; u < kWalkUnroll; ++u) iv[u] = ok[u] ? __ldg(a.inv_i + ph[u].x) : 0.f;
 #pragma unroll
       for (int u = 0; u < kWalkUnroll; ++u)
-        if (u < nu) f(ok[u], ph[u].x, ok[u] ? cold_fix(__int_as_float(ph[u].y), pv[u]) : 0);
+        if (ok[u]) f(ph[u].x, cold_fix(pq[u], __int_as_float(ph[u].y) * iv[u]));
     }
   }
 }
 
-__global__ void __launch_bounds__(kRThreads, 1) k_tc_records(const RecArgs a) {
-  extern __shared__ __align__(16) unsigned char rsm[];
-  int2 *buf = reinterpret_cast<int2 *>(rsm);            // records as they come: {quarter << 10 | pos, p}
-  int2 *sorted = buf + kRecCap;                         // the same, by quarter: {pos, p}
-  int *cnt = reinterpret_cast<int *>(sorted + kRecCap); // [kMaxQpw + 1] per quarter, then offsets
-  int *off = cnt + (kMaxQpw + 1);
-  int *cur = off + (kMaxQpw + 1);
-  constexpr int kChunks = kRecCap / 32;                 // the buffer is handed out 32 slots at a time
+// One block per 32 query rows (one warp per row): every cold product of
+// the rows with the chunk becomes a record in the bucket of its column
+// block, at a slot taken from the block's own counter (the order inside a
+// bucket does not matter: the epilogue sums integers).
+__global__ void __launch_bounds__(kRThreads) k_tc_records(const RecArgs a) {
+  extern __shared__ int rcnt[];  // [n_cb]
   __shared__ int4 slots_all[kRThreads / 32][32];
-  __shared__ int fill[kChunks];                         // records in each chunk of the buffer
-  __shared__ int n_chunks, seg_start;
-  int4 *slots = slots_all[threadIdx.x >> 5];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const unsigned lt = (1u << lane) - 1u;
-  const int cb = blockIdx.x, w = blockIdx.y;
-  const int qpw = a.qpw;
-  for (int j = tid; j <= kMaxQpw; j += kRThreads) cnt[j] = 0;
-  if (tid == 0) n_chunks = 0;
+  int4 *slots = slots_all[warp];
+  const int64_t Q = blockIdx.x;
+  const int ncb = a.n_cb, cap = a.bucket_cap;
+  for (int c = tid; c < ncb; c += kRThreads) rcnt[c] = 0;
   __syncthreads();
-  const int item = cb * 32 + warp;
-  const bool have_item = item < a.n_items;
-  // The warp appends to its current chunk of 32 slots and takes a new one
-  // (one shared atomic) when the records of a step do not fit it.
-  int my_chunk = -1, my_fill = 32;
-  if (have_item)
-    walk_item(a, item, w, lane, slots, [&](bool ok, int row, int p) {
-      const unsigned m = __ballot_sync(0xffffffffu, ok);
-      if (!m) return;
-      const int n = __popc(m), rank = __popc(m & lt), room = 32 - my_fill;
-      int next = my_chunk;
-      if (n > room) {
-        if (lane == 0) {
-          next = atomicAdd(&n_chunks, 1);
-          if (my_chunk >= 0 && my_chunk < kChunks) fill[my_chunk] = 32;
-        }
-        next = __shfl_sync(0xffffffffu, next, 0);
-      }
-      if (ok) {
-        // {row << 5 | item within the block, product}: the quarter is
-        // key >> 10; counting and placing are left to the sort below.
-        const int c = rank < room ? my_chunk : next;
-        const int at = rank < room ? my_fill + rank : rank - room;
-        if (c < kChunks) buf[c * 32 + at] = make_int2((row << 5) | warp, p);
-      }
-      if (n > room) {
-        my_chunk = next;
-        my_fill = n - room;
-      } else {
-        my_fill += n;
-      }
+  int2 *rq = a.rec + Q * ncb * (int64_t)cap;
+  const int64_t r = Q * 32 + warp;
+  if (r < a.n_q)
+    walk_row(a, r, lane, slots, [&](int item, int p) {
+      const int cb = item >> 5;
+      const int slot = atomicAdd(&rcnt[cb], 1);
+      if (slot < cap) rq[(int64_t)cb * cap + slot] = make_int2(stg_index(warp, item & 31), p);
     });
-  if (lane == 0 && my_chunk >= 0 && my_chunk < kChunks) fill[my_chunk] = my_fill;
   __syncthreads();
-  // Records per quarter (a warp per chunk of the buffer); when the buffer
-  // overflowed, the walk is repeated to count.
-  const int used = min(n_chunks, kChunks);
-  if (n_chunks <= kChunks) {
-    for (int c = warp; c < used; c += kRThreads / 32)
-      if (lane < fill[c]) atomicAdd(&cnt[buf[c * 32 + lane].x >> 10], 1);
-  } else if (have_item) {
-    walk_item(a, item, w, lane, slots, [&](bool ok, int row, int) {
-      if (ok) atomicAdd(&cnt[row >> 5], 1);
-    });
-  }
-  __syncthreads();
-  __shared__ int n_total;
-  if (warp == 0) {
-    // Offsets of the quarters: lane l scans quarters 8 l .. 8 l + 7.
-    static_assert(kMaxQpw == 256, "eight quarters per lane");
-    int v[8], sum = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      v[k] = cnt[8 * lane + k];
-      sum += v[k];
-    }
-    int run = warp_incl_scan(sum, lane) - sum;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      off[8 * lane + k] = run;
-      cur[8 * lane + k] = run;
-      run += v[k];
-    }
-    if (lane == 31) {
-      off[kMaxQpw] = run;
-      n_total = run;
-    }
-    const int total = __shfl_sync(0xffffffffu, run, 31);
-    if (lane == 0) {
-      int start = -1;
-      if (total > 0) {
-        const unsigned long long at = atomicAdd(a.cursor, (unsigned long long)total);
-        // When the array is full the scorer computes these buckets itself.
-        if (at + (unsigned long long)total <= (unsigned long long)a.rec_cap) start = (int)at;
-      }
-      seg_start = start;
-    }
-  }
-  __syncthreads();
-  const int start = seg_start, total = n_total;
-  int32_t *seg = a.seg + ((int64_t)w * a.n_cb + cb) * (qpw + 2);
-  for (int j = tid; j <= qpw; j += kRThreads) seg[1 + j] = off[j];
-  if (tid == 0) seg[0] = total > 0 ? start : 0;
-  if (total == 0 || start < 0) return;
-  int2 *dst = a.rec + start;
-  if (n_chunks <= kChunks) {
-    // Counting sort by quarter in shared memory (a warp per chunk of the
-    // buffer), then one coalesced copy.
-    for (int c = warp; c < used; c += kRThreads / 32) {
-      if (lane < fill[c]) {
-        const int2 r = buf[c * 32 + lane];
-        const int row = r.x >> 5;
-        sorted[atomicAdd(&cur[row >> 5], 1)] = make_int2(stg_index(row & 31, r.x & 31), r.y);
-      }
-    }
-    __syncthreads();
-    for (int j = tid; j < total; j += kRThreads) dst[j] = sorted[j];
-  } else {
-    // Too many to sort on chip: walk again and store each record at its place.
-    if (have_item)
-      walk_item(a, item, w, lane, slots, [&](bool ok, int row, int p) {
-        if (ok) dst[atomicAdd(&cur[row >> 5], 1)] = make_int2(stg_index(row & 31, warp), p);
-      });
-  }
+  for (int c = tid; c < ncb; c += kRThreads) a.rec_n[Q * ncb + c] = rcnt[c] <= cap ? rcnt[c] : -1;
 }
 
 // ---------------------------------------------------------------- scorer
@@ -939,16 +900,16 @@ struct ScoreArgs {
   const uint16_t *A;       // query operand tiles
   const uint16_t *B;       // item operand tiles
   const int2 *rec;         // the call's records (k_tc_records)
-  const int32_t *seg;      // per (query window, column block): segment start, quarter offsets
-  int32_t qpw;             // quarters per query window
-  // For segments that did not fit: the items' cold entries, the chunk's
-  // inverse norms and the windows' query lists.
-  const int2 *icold;
-  const int2 *icold_rng;
+  const int32_t *rec_n;    // their counts per bucket (-1: did not fit)
+  int32_t bucket_cap;
+  // For buckets that did not fit: the queries' cold entries and the call's
+  // lists of the chunk.
+  const int64_t *q_indptr;
+  const int2 *qcold;
+  const int32_t *qcold_n;
+  const int32_t *col_ptr;
+  const int2 *chat;
   const float *inv_i;
-  const int32_t *qcol_ptr;
-  const int2 *qpost;
-  int64_t dim;
   int64_t n_quarters;
   int32_t n_cb;
   float *out;
@@ -963,9 +924,8 @@ struct ScoreArgs {
 };
 
 // Bytes of the scorer's dynamic shared memory for Hp hot columns: the item
-// tile (hi, lo: 1024 Hp), one query part (256 Hp: the lo part, then the hi
-// part of each query tile), the epilogue staging (two tiles per warp, so a
-// tile's bulk store reads it while the warp fills the other).
+// tile (hi, lo: 1024 Hp), two buffers of one query sub-part (128 Hp each),
+// the epilogue staging (one 32 x 32 tile per epilogue warp).
 size_t score_smem_bytes(int Hp) { return (size_t)1280 * Hp + kStgBytes; }
 
 // Ties registers just loaded from tensor memory to the wait that completes
@@ -988,20 +948,22 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int Hp = a.Hp;
   const uint32_t bytesB = 1024u * (uint32_t)Hp, bytesApart = 256u * (uint32_t)Hp;
   unsigned char *sB = sm;                          // hi part, then lo part
-  unsigned char *sA = sm + bytesB;                 // the query tile's lo part, then its hi part
+  unsigned char *sA = sm + bytesB;                 // two buffers of one query sub-part (a K half of a part)
   int *stg_all = reinterpret_cast<int *>(
       (reinterpret_cast<uintptr_t>(sA + bytesApart) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t b_full = smem_u32(&bars[0]), b_free = smem_u32(&bars[1]);
-  // bars[2..3]: a query part landed / read by the MMAs (two phases per unit:
-  // the lo part, then the hi part).  bars[4..5] unused.
-  const uint32_t a_full = smem_u32(&bars[2]), a_free = smem_u32(&bars[3]);
+  // bars[2..3]: query sub-part buffer 0 / 1 landed; bars[4..5]: buffer 0 / 1
+  // read by the MMAs (two phases of each per unit).
+  const uint32_t a_full[2] = {smem_u32(&bars[2]), smem_u32(&bars[3])};
+  const uint32_t a_free[2] = {smem_u32(&bars[4]), smem_u32(&bars[5])};
+  const uint32_t bytesAsub = bytesApart / 2;       // one sub-part: 128 rows x Hp / 2 halves
   // bars[6..7]: accumulator b written (MMA commit); bars[8..9]: accumulator b
   // read out (one arrival per epilogue warp).
   const uint32_t acc_full0 = smem_u32(&bars[6]), acc_full1 = smem_u32(&bars[7]);
   const uint32_t acc_free0 = smem_u32(&bars[8]), acc_free1 = smem_u32(&bars[9]);
   const uint32_t drain = smem_u32(&bars[10]);  // the MMA thread's last commit
   if (tid == 0) {
-    for (int i = 0; i < 8; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    for (int i = 0; i < 8; ++i) mbar_init(smem_u32(&bars[i]), 1);  // b, query buffers, accumulators
     mbar_init(drain, 1);
     mbar_init(acc_free0, kEpiWarps);
     mbar_init(acc_free1, kEpiWarps);
@@ -1024,37 +986,44 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
   if (warp == 0) {
     // ---- producer: the item tile when it changes, then per unit the query
-    // tile's lo part and hi part into the one query buffer, each once the
-    // MMAs have released it (copy k of the buffer: the lo part of unit k / 2
-    // for even k, its hi part for odd k).
+    // tile's four sub-parts (lo K0, lo K1, hi K0, hi K1), copy k into buffer
+    // k % 2 once the MMAs have released that buffer's previous sub-part.
     if (lane == 0) {
+      const uint64_t keep = evict_last_policy();
       int64_t prev_t = -1;
       int nb = 0;         // item tile copies issued
-      int64_t na = 0;     // query part copies issued
+      int64_t na = 0;     // query sub-part copies issued
       for (int64_t j = 0; j < nj; ++j) {
         const int64_t u = u0 + j, t = u / a.n_qtiles, g = u % a.n_qtiles;
         if (t != prev_t) {
           if (nb > 0 && !mbar_wait(b_free, (uint32_t)((nb - 1) & 1), a.status)) break;
           mbar_expect_tx(b_full, bytesB);
-          bulk_g2s(smem_u32(sB), a.B + (size_t)t * (bytesB / 2), bytesB, b_full);
+          bulk_g2s_hint(smem_u32(sB), a.B + (size_t)t * (bytesB / 2), bytesB, b_full, keep);
           ++nb;
           prev_t = t;
         }
-        const uint16_t *At = a.A + (size_t)g * (bytesApart);  // tile: hi part, lo part (halves)
-        if (na > 0 && !mbar_wait(a_free, (uint32_t)((na - 1) & 1), a.status)) break;
-        mbar_expect_tx(a_full, bytesApart);
-        bulk_g2s(smem_u32(sA), At + bytesApart / 2, bytesApart, a_full);
-        ++na;
-        if (!mbar_wait(a_free, (uint32_t)((na - 1) & 1), a.status)) break;
-        mbar_expect_tx(a_full, bytesApart);
-        bulk_g2s(smem_u32(sA), At, bytesApart, a_full);
-        ++na;
+        const uint16_t *At = a.A + (size_t)g * (bytesApart);  // a tile: four sub-parts of bytesAsub bytes
+        bool ok = true;
+        for (int sp = 0; sp < 4 && ok; ++sp) {
+          const int buf = (int)(na & 1);
+          const int64_t k = na >> 1;  // copies into this buffer before this one
+          if (k > 0) ok = mbar_wait(a_free[buf], (uint32_t)((k - 1) & 1), a.status);
+          if (!ok) break;
+          mbar_expect_tx(a_full[buf], bytesAsub);
+          bulk_g2s_hint(smem_u32(sA) + (uint32_t)buf * bytesAsub, At + (size_t)sp * (bytesAsub / 2), bytesAsub,
+                        a_full[buf], keep);
+          ++na;
+        }
+        if (!ok) break;
       }
       // Every copy issued lands before the block exits, also when a wait
       // above gave up: copy k into a buffer is issued only after the phase
       // of copy k - 1 completed, so the phase of the last copy issued is the
       // one still open, and a bulk copy completes by itself.
-      if (na > 0) mbar_wait(a_full, (uint32_t)((na - 1) & 1), a.status);
+      for (int buf = 0; buf < 2; ++buf) {
+        const int64_t n_buf = (na + 1 - buf) >> 1;  // copies issued into this buffer
+        if (n_buf > 0) mbar_wait(a_full[buf], (uint32_t)((n_buf - 1) & 1), a.status);
+      }
       if (nb > 0) mbar_wait(b_full, (uint32_t)((nb - 1) & 1), a.status);
     }
   } else if (warp == 1) {
@@ -1062,9 +1031,20 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // hi_q x lo_v and hi_q x hi_v.
     if (lane == 0) {
       const uint32_t idesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
-      const uint32_t sbo = 16u * (uint32_t)Hp, lbo = 128u;
+      const int Kp = Hp / 2;
+      const uint32_t sboA = 16u * (uint32_t)Kp, sboB = 16u * (uint32_t)Hp, lbo = 128u;
       const uint32_t bhi = smem_u32(sB), blo = bhi + bytesB / 2;
-      const uint32_t aq = smem_u32(sA);
+      const uint32_t abuf[2] = {smem_u32(sA), smem_u32(sA) + bytesAsub};
+      // Sub-part s of unit j is copy 4 j + s, in buffer s % 2, at that
+      // buffer's phase 2 j + s / 2.
+      auto wait_part = [&](int s) { return mbar_wait(a_full[s & 1], (uint32_t)((s >> 1) & 1), a.status); };
+      // The Kp-column product of a sub-part buffer with K half h of item part bp.
+      auto mma_half = [&](uint32_t d, int buf, uint32_t bp, int h, bool first) {
+        for (int kk = 0; kk < Kp; kk += 16)
+          mma_f16(d, smem_desc(abuf[buf] + (uint32_t)(kk / 8) * 128u, lbo, sboA),
+                  smem_desc(bp + (uint32_t)((h * Kp + kk) / 8) * 128u, lbo, sboB), idesc,
+                  (first && kk == 0) ? 0u : 1u);
+      };
       int64_t prev_t = -1;
       int nb = 0;
       bool ok = true;
@@ -1078,23 +1058,28 @@ __global__ void __launch_bounds__(kSThreads, 1)
         }
         const int b = (int)(j & 1);
         if (ok && j >= 2) ok = mbar_wait(b ? acc_free1 : acc_free0, (uint32_t)(((j - 2) >> 1) & 1), a.status);
-        if (ok) ok = mbar_wait(a_full, 0u, a.status);  // phase 2 j: the lo part
         if (!ok) break;
-        tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(b * kN);
-        for (int k = 0; k < Hp; k += 16)
-          mma_f16(d, smem_desc(aq + (uint32_t)(k / 8) * 128u, lbo, sbo),
-                  smem_desc(bhi + (uint32_t)(k / 8) * 128u, lbo, sbo), idesc, k > 0 ? 1u : 0u);
-        mma_commit(a_free);
-        if (!mbar_wait(a_full, 1u, a.status)) break;  // phase 2 j + 1: the hi part
+        // lo_q x hi_v over both K halves, then hi_q x lo_v, then hi_q x hi_v
+        // (the cross terms first, while the sum is small).
+        if (!(ok = wait_part(0))) break;
         tc_fence_after();
-        for (int k = 0; k < Hp; k += 16)
-          mma_f16(d, smem_desc(aq + (uint32_t)(k / 8) * 128u, lbo, sbo),
-                  smem_desc(blo + (uint32_t)(k / 8) * 128u, lbo, sbo), idesc, 1u);
-        for (int k = 0; k < Hp; k += 16)
-          mma_f16(d, smem_desc(aq + (uint32_t)(k / 8) * 128u, lbo, sbo),
-                  smem_desc(bhi + (uint32_t)(k / 8) * 128u, lbo, sbo), idesc, 1u);
-        mma_commit(a_free);
+        mma_half(d, 0, bhi, 0, true);
+        mma_commit(a_free[0]);
+        if (!(ok = wait_part(1))) break;
+        tc_fence_after();
+        mma_half(d, 1, bhi, 1, false);
+        mma_commit(a_free[1]);
+        if (!(ok = wait_part(2))) break;
+        tc_fence_after();
+        mma_half(d, 0, blo, 0, false);
+        if (!(ok = wait_part(3))) break;
+        tc_fence_after();
+        mma_half(d, 1, blo, 1, false);
+        mma_half(d, 0, bhi, 0, false);
+        mma_commit(a_free[0]);
+        mma_half(d, 1, bhi, 1, false);
+        mma_commit(a_free[1]);
         mma_commit(b ? acc_full1 : acc_full0);
       }
       // Every MMA this thread issued has completed before the tensor memory
@@ -1105,56 +1090,56 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
   } else {
     // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31, i.e. the
-    // unit's query rows 32 (w % 4) .. + 31, in 8 blocks of 32 columns.  The
-    // records of a block are fetched two blocks ahead (across units), the
-    // next block's accumulator columns one block ahead.
+    // unit's query rows 32 (w % 4) .. + 31; the kWarpsPerQ warps of a
+    // quarter share its eight 32-column blocks (warp `sub` takes blocks
+    // sub, sub + kWarpsPerQ, ...).  A block's records are fetched one block
+    // ahead (across units); its accumulator columns are loaded while they
+    // land.
     const int qd = warp & 3;
-    const int half = (warp - 2) >> 2;                 // 0: even column blocks, 1: odd ones
-    int *stg_mine = stg_all + 2 * (warp - 2) * kStgInts;  // this warp's two staging tiles (swizzled)
+    const int sub = (warp - 2) >> 2;
+    int *stg_mine = stg_all + (warp - 2) * kStgTiles * kStgInts;  // this warp's staging tiles (swizzled)
+    int n_blocks = 0;                                              // blocks done (tile n_blocks % kStgTiles next)
     const bool vec = a.vec_ok != 0;
     const bool tma = a.use_tma != 0;
+    const uint64_t out_policy = evict_first_policy();
     const int sw = lane & 7;
-    int n_blocks = 0;                                 // blocks this warp has done (tile n_blocks % 2 next)
-    // Lanes 0..7: where the records of the unit's 8 column blocks start in
-    // the record array and how many there are (0 past the chunk or the
-    // queries; -1 when their segment did not fit and the bucket is computed
-    // from the lists here).
-    auto load_bnd = [&](int64_t u, int &beg) -> int {
+    const int cap = a.bucket_cap;
+    // Lanes 0..7: the record counts of the unit's 8 column blocks (0 past
+    // the chunk or the queries).
+    auto load_cnt = [&](int64_t u) -> int {
       const int64_t t = u / a.n_qtiles, g = u % a.n_qtiles;
       const int64_t Q = g * 4 + qd;
       const int cb = (int)t * 8 + lane;
-      int n = 0;
-      beg = 0;
-      if (Q < a.n_quarters && lane < 8 && cb < a.n_cb) {
-        const int64_t w = Q / a.qpw;
-        const int ql = (int)(Q - w * a.qpw);
-        const int32_t *sg = a.seg + (w * a.n_cb + cb) * (int64_t)(a.qpw + 2);
-        const int st = ld_keep_int(sg), o0 = ld_keep_int(sg + 1 + ql), o1 = ld_keep_int(sg + 2 + ql);
-        n = st < 0 ? -1 : o1 - o0;
-        beg = st + o0;
-      }
-      return n;
+      return (Q < a.n_quarters && lane < 8 && cb < a.n_cb) ? ld_keep_int(a.rec_n + Q * a.n_cb + cb) : 0;
     };
-    auto fetch = [&](int bnd, int bbeg, int c, int2(&dst)[kRecPerLane]) {
-      const int n = __shfl_sync(0xffffffffu, bnd, c);
-      const int2 *bk = a.rec + __shfl_sync(0xffffffffu, bbeg, c);
+    // The bucket of the unit's column block 0 (block c's follows at c * cap).
+    auto bucket0 = [&](int64_t u) -> const int2 * {
+      const int64_t t = u / a.n_qtiles, g = u % a.n_qtiles;
+      const int64_t Q = g * 4 + qd;
+      return a.rec + (Q * a.n_cb + t * 8) * (int64_t)cap;
+    };
+    auto fetch = [&](int counts, const int2 *bucket, int c, int2(&dst)[kRecPerLane]) {
+      const int n = __shfl_sync(0xffffffffu, counts, c);
+      const int2 *bc = bucket + (int64_t)c * cap;
 #pragma unroll
       for (int m = 0; m < kRecPerLane; ++m) {
         const int p = 32 * m + lane;
-        dst[m] = make_int2(0, 0);
-        if (p < n) dst[m] = ld_keep_int2(bk + p);
+        dst[m] = make_int2(0, 0);  // no record
+        if (p < n) dst[m] = ld_keep_int2(bc + p);
       }
     };
-    // This warp's blocks c = 2 i + half, i = 0..3; the records of its i-th
-    // block live in register slot i, fetched two of its blocks ahead
-    // (across units), so no copy waits on a load in flight.
-    constexpr int kMine = kN / kColBlock / 2;
-    int bbeg = 0, bbeg_n = 0;
-    int bnd = nj > 0 ? load_bnd(u0, bbeg) : 0, bnd_n = 0;
-    int2 R[kMine][kRecPerLane];
+    // The warp's blocks in order: block kMine j + i is column block
+    // sub + kWarpsPerQ i of unit j.  Its records sit in register set i % 2;
+    // those of the block two later are loaded into the same set once its
+    // records are added, so that each load has about two blocks of work to
+    // land in.  Record counts are read two units ahead.
+    static_assert(kMine >= 2 && kMine % 2 == 0, "two register sets of records");
+    int cnt = nj > 0 ? load_cnt(u0) : 0, cnt_n = nj > 1 ? load_cnt(u0 + 1) : 0, cnt_nn = 0;
+    const int2 *bk = nj > 0 ? bucket0(u0) : a.rec, *bk_n = nj > 1 ? bucket0(u0 + 1) : a.rec, *bk_nn = a.rec;
+    int2 R[2][kRecPerLane];
     if (nj > 0) {
-      fetch(bnd, bbeg, half, R[0]);
-      fetch(bnd, bbeg, 2 + half, R[1]);
+      fetch(cnt, bk, sub, R[0]);
+      fetch(cnt, bk, sub + kWarpsPerQ, R[1]);
     }
     for (int64_t j = 0; j < nj; ++j) {
       const int64_t u = u0 + j, t = u / a.n_qtiles, g = u % a.n_qtiles;
@@ -1165,87 +1150,95 @@ __global__ void __launch_bounds__(kSThreads, 1)
       __syncwarp();
       if (!ok) break;
       tc_fence_after();
-      if (j + 1 < nj) bnd_n = load_bnd(u + 1, bbeg_n);
+      if (j + 2 < nj) {
+        cnt_nn = load_cnt(u + 2);
+        bk_nn = bucket0(u + 2);
+      }
       const int64_t qrow0 = (g * 4 + qd) * 32;
       const int item0 = (int)t * kN;
-      // Lane l stores items 4 (l % 8) .. + 3 of rows 4 s + l / 8 of each block.
-      float *my_row = a.out + (qrow0 + (lane >> 3)) * a.ld_out + item0 + 4 * (lane & 7);
-      const bool rows_whole = qrow0 + 32 <= a.n_q;
       const uint32_t tbase = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(b * kN);
 #pragma unroll
       for (int i = 0; i < kMine; ++i) {
-        const int c = 2 * i + half;
-        int *stg = stg_mine + (n_blocks & 1) * kStgInts;
+        const int c = sub + kWarpsPerQ * i;
+        int2(&Rc)[kRecPerLane] = R[i & 1];
+        int *stg = stg_mine + (kStgTiles > 1 ? (n_blocks % kStgTiles) * kStgInts : 0);
         int *row = stg + lane * 32;
         ++n_blocks;
         uint32_t rc[32];
-        tmem_ld32(tbase + (uint32_t)(c * kColBlock), rc);  // lands during the record phase
-        if (i + 2 < kMine) fetch(bnd, bbeg, c + 4, R[(i + 2) & 3]);
-        else if (j + 1 < nj) fetch(bnd_n, bbeg_n, c + 4 - 2 * kMine, R[(i + 2) & 3]);
-        if (tma) {  // the bulk store of two blocks ago has read this staging tile
-          if (lane == 0) bulk_wait_read1();
+        tmem_ld32(tbase + (uint32_t)(c * kColBlock), rc);  // lands while the records are added
+        const int n = __shfl_sync(0xffffffffu, cnt, c);
+        // The records of the block two later, into the set just used.
+        auto prefetch = [&]() {
+          if (i + 2 < kMine) fetch(cnt, bk, c + 2 * kWarpsPerQ, Rc);
+          else if (j + 1 < nj) fetch(cnt_n, bk_n, sub + kWarpsPerQ * (i + 2 - kMine), Rc);
+        };
+        if (tma) {  // the bulk store that last read this staging tile is done reading it
+          if (lane == 0) {
+            if (kStgTiles > 1) bulk_wait_read1();
+            else bulk_wait_read0();
+          }
           __syncwarp();
         }
+        if (n != 0) {
+          // The records, summed as integers in the tile (lane = row, chunk
+          // k of the row at chunk k ^ (row % 8)), then added to the
+          // accumulator with one rounding.
 #pragma unroll
-        for (int k = 0; k < 8; ++k) *reinterpret_cast<int4 *>(row + 4 * (k ^ sw)) = make_int4(0, 0, 0, 0);
-        __syncwarp();
+          for (int k = 0; k < 8; ++k) *reinterpret_cast<int4 *>(row + 4 * (k ^ sw)) = make_int4(0, 0, 0, 0);
+          __syncwarp();
 #pragma unroll
-        for (int m = 0; m < kRecPerLane; ++m)
-          if (R[i & 3][m].y != 0) atomicAdd(stg + R[i & 3][m].x, R[i & 3][m].y);
-        {
-          const int n = __shfl_sync(0xffffffffu, bnd, c);
-          const int2 *bc = a.rec + __shfl_sync(0xffffffffu, bbeg, c);
-          // Records past those held in registers: loads in batches of four
-          // per lane, issued before any of their adds.
-          for (int p0 = 32 * kRecPerLane; p0 < n; p0 += 128) {
-            int2 t4[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const int p = p0 + 32 * m + lane;
-              t4[m] = p < n ? ld_keep_int2(bc + p) : make_int2(0, 0);
-            }
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-              if (t4[m].y != 0) atomicAdd(stg + t4[m].x, t4[m].y);
+          for (int m = 0; m < kRecPerLane; ++m)
+            if (Rc[m].y != 0) atomicAdd(stg + Rc[m].x, Rc[m].y);
+          prefetch();
+          const int2 *bc = bk + (int64_t)c * cap;
+          for (int p = 32 * kRecPerLane + lane; p < n; p += 32) {  // past the first 32 kRecPerLane (rare)
+            const int2 rr = ld_keep_int2(bc + p);
+            atomicAdd(stg + rr.x, rr.y);
           }
           if (n < 0) {
-            // The segment did not fit the record array: each lane walks its
-            // item's cold entries against the window's query lists and keeps
-            // the rows of this quarter (rare; exact, the same integers).
-            const int item = item0 + c * kColBlock + lane;
-            const int64_t Q = g * 4 + qd;
-            const int64_t w = Q / a.qpw;
-            const int ql = (int)(Q - w * a.qpw);
-            if (item < a.n_items) {
-              const int2 rng = __ldg(a.icold_rng + item);
-              const float inv = __ldg(a.inv_i + item);
-              const int32_t *qptr = a.qcol_ptr + w * (a.dim + 1);
-              for (int e = 0; e < rng.y; ++e) {
-                const int2 ie = __ldg(a.icold + rng.x + e);
-                const float vv = __int_as_float(ie.y) * inv;
-                const int p1 = __ldg(qptr + ie.x + 1);
-                for (int p = __ldg(qptr + ie.x); p < p1; ++p) {
-                  const int2 ph = __ldg(a.qpost + p);
-                  if ((ph.x >> 5) == ql)
-                    atomicAdd(stg + stg_index(ph.x & 31, lane), cold_fix(__int_as_float(ph.y), vv));
+            // The bucket did not fit: each lane walks its row's cold lists
+            // and keeps the items of this block (rare; exact, the same sums).
+            const int64_t q = qrow0 + lane;
+            const int lo = item0 + c * kColBlock;
+            if (q < a.n_q) {
+              const int64_t qb = a.q_indptr[q];
+              const int cn = a.qcold_n[q];
+              for (int e = 0; e < cn; ++e) {
+                const int2 qe = __ldg(a.qcold + qb + e);
+                const float qv = __int_as_float(qe.y);
+                const int p1 = __ldg(a.col_ptr + qe.x + 1);
+                for (int p = __ldg(a.col_ptr + qe.x); p < p1; ++p) {
+                  const int2 ph = __ldg(a.chat + p);
+                  const int d = ph.x - lo;
+                  if ((unsigned)d < (unsigned)kColBlock)
+                    atomicAdd(stg + stg_index(lane, d), cold_fix(qv, __int_as_float(ph.y) * __ldg(a.inv_i + ph.x)));
                 }
               }
             }
           }
-        }
-        __syncwarp();
-        tmem_wait_ld();
-        tmem_regs_ready(rc);
+          __syncwarp();
+          tmem_wait_ld();
+          tmem_regs_ready(rc);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          int *chunk = row + 4 * (k ^ sw);
-          const int4 ci = *reinterpret_cast<const int4 *>(chunk);
-          float4 o;
-          o.x = fmaf((float)ci.x, kFixInv, __uint_as_float(rc[4 * k + 0]));
-          o.y = fmaf((float)ci.y, kFixInv, __uint_as_float(rc[4 * k + 1]));
-          o.z = fmaf((float)ci.z, kFixInv, __uint_as_float(rc[4 * k + 2]));
-          o.w = fmaf((float)ci.w, kFixInv, __uint_as_float(rc[4 * k + 3]));
-          *reinterpret_cast<float4 *>(chunk) = o;
+          for (int k = 0; k < 8; ++k) {
+            int *chunk = row + 4 * (k ^ sw);
+            const int4 ci = *reinterpret_cast<const int4 *>(chunk);
+            float4 o;
+            o.x = fmaf((float)ci.x, kFixInv, __uint_as_float(rc[4 * k + 0]));
+            o.y = fmaf((float)ci.y, kFixInv, __uint_as_float(rc[4 * k + 1]));
+            o.z = fmaf((float)ci.z, kFixInv, __uint_as_float(rc[4 * k + 2]));
+            o.w = fmaf((float)ci.w, kFixInv, __uint_as_float(rc[4 * k + 3]));
+            *reinterpret_cast<float4 *>(chunk) = o;
+          }
+        } else {
+          prefetch();
+          tmem_wait_ld();
+          tmem_regs_ready(rc);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<float4 *>(row + 4 * (k ^ sw)) =
+                make_float4(__uint_as_float(rc[4 * k + 0]), __uint_as_float(rc[4 * k + 1]),
+                            __uint_as_float(rc[4 * k + 2]), __uint_as_float(rc[4 * k + 3]));
         }
         __syncwarp();
         const int it = item0 + c * kColBlock + 4 * (lane & 7);
@@ -1257,12 +1250,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
           __syncwarp();
           if (lane == 0) {
             if (qrow0 < a.n_q && item0 + c * kColBlock < a.n_items)
-              tma_store_2d(&a.out_map, smem_u32(stg), item0 + c * kColBlock, (int)qrow0);
-            bulk_commit();  // one group per block, empty or not, so the wait above counts blocks
+              tma_store_2d(&a.out_map, smem_u32(stg), item0 + c * kColBlock, (int)qrow0, out_policy);
+            bulk_commit();
           }
-        } else if (vec && rows_whole && item0 + (c + 1) * kColBlock <= a.n_items) {
+        } else if (vec && qrow0 + 32 <= a.n_q && item0 + (c + 1) * kColBlock <= a.n_items) {
           // Row-contiguous stores: lane l writes items 4 (l % 8) .. + 3 of
           // rows 4 s + l / 8 (chunk l % 8 of the row, found through the swizzle).
+          float *my_row = a.out + (qrow0 + (lane >> 3)) * a.ld_out + item0 + 4 * (lane & 7);
 #pragma unroll
           for (int sidx = 0; sidx < 8; ++sidx) {
             const int rl = 4 * sidx + (lane >> 3);
@@ -1288,8 +1282,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
         }
         __syncwarp();
       }
-      bnd = bnd_n;
-      bbeg = bbeg_n;
+      cnt = cnt_n;
+      bk = bk_n;
+      cnt_n = cnt_nn;
+      bk_n = bk_nn;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b ? acc_free1 : acc_free0);
@@ -1351,7 +1347,9 @@ cudaError_t grow(T **p, int64_t *cap, int64_t need, cudaStream_t s) {
   return cudaSuccess;
 }
 
-int padded_hot(int H) { return std::max(16, (H + 15) / 16 * 16); }
+// Hot columns rounded up to a multiple of 32: each K half of the query
+// operand then holds whole MMA steps of 16.
+int padded_hot(int H) { return std::max(32, (H + 31) / 32 * 32); }
 
 }  // namespace
 
@@ -1415,6 +1413,7 @@ cudaError_t launch_build_tc(ss_handle *h, const ss_csr &items, int64_t row_begin
     if ((e = dev_alloc(&h->tc_sq, sizeof(float) * rows)) != cudaSuccess) return e;
     if ((e = dev_alloc(&h->tc_icold_rng, sizeof(int2) * rows)) != cudaSuccess) return e;
   }
+  ++h->tc_build_serial;  // the lists made for the previous build's chunks are stale
   const int grid = (h->sm_count > 0 ? h->sm_count : 148) * 8;
   // The build's cold entries go to the entry array sized for the matrix
   // (post_hat, post_cap >= items.nnz), at the rows' own positions.
@@ -1481,20 +1480,6 @@ static bool encode_out_map(CUtensorMap *map, float *out, int64_t n_q, int64_t n_
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Query rows per window of the query side's inverted index: as many as keep
-// a records block (32 items x the window) near three quarters of kRecCap
-// records on the sample's estimate of shared cold dimensions per pair (the
-// blocks' records spread about 25% above their mean on Zipf data), a
-// multiple of 32, at most kMaxQpw quarters; windows as equal as that allows.
-static int window_rows(int64_t n_q, double est_cold) {
-  const double per_row = 32.0 * std::max(est_cold, 1e-9);
-  int64_t cap = (int64_t)std::floor(0.75 * kRecCap / per_row);
-  cap = std::max<int64_t>(32, std::min<int64_t>(32 * kMaxQpw, cap / 32 * 32));
-  const int64_t n_win = std::max<int64_t>(1, (n_q + cap - 1) / cap);
-  const int64_t rows = (n_q + n_win - 1) / n_win;
-  return (int)std::min<int64_t>(cap, (rows + 31) / 32 * 32);
-}
-
 cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, const ss_index &idx,
                             const float *inv_i, float *out, int64_t ld_out, cudaStream_t s,
                             int *queued, const ss_topk *topk) {
@@ -1510,18 +1495,16 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
   cudaError_t e = cudaSuccess;
   int nq = 0;
 
-  // Query operand, cold entries and the windows' inverted index, once per
-  // query matrix, inverse norms and hot set.
+  // Query operand, cold entries and the numbering of the queries' cold
+  // dimensions, once per query matrix, inverse norms and hot set.
   if (!(h->tcq_src[0] == q.indptr && h->tcq_src[1] == q.indices && h->tcq_src[2] == q.values &&
         h->tcq_src[3] == inv_q && h->tcq_rows == q.n_rows && h->tcq_nnz == q.nnz &&
         h->tcq_generation == h->tc_hot_generation)) {
-    const int win = window_rows(n_q, h->tc_est_cold);
-    const int64_t n_win = (n_q + win - 1) / win;
-    const int64_t n_cnt = n_win * (dim + 1);
+    h->tcq_rows = -1;  // not prepared until the end of this block
+    const int64_t n_cnt = dim + 1;
     if ((e = grow(&h->tc_A, &h->tc_A_cap, n_qtiles * kM * 2 * Hp, s)) != cudaSuccess) return e;
     if ((e = grow(&h->tc_qcold, &h->tc_qcold_cap, std::max<int64_t>(1, q.nnz), s)) != cudaSuccess) return e;
     if ((e = grow(&h->tc_qcold_n, &h->tc_qcold_n_cap, n_q, s)) != cudaSuccess) return e;
-    if ((e = grow(&h->tc_qpost, &h->tc_qpost_cap, std::max<int64_t>(1, q.nnz), s)) != cudaSuccess) return e;
     if ((e = grow(&h->tc_qcnt, &h->tc_qcnt_cap, n_cnt, s)) != cudaSuccess) return e;
     if ((e = grow(&h->tc_qptr, &h->tc_qptr_cap, n_cnt, s)) != cudaSuccess) return e;
     if ((e = grow(&h->tc_qpart, &h->tc_qpart_cap, scan_tile_count(n_cnt) + 1, s)) != cudaSuccess) return e;
@@ -1546,15 +1529,19 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     k_tc_prep_queries<<<(unsigned)blocks, kPrepThreads, 0, s>>>(pa);
     if ((e = cudaMemsetAsync(h->tc_qcnt, 0, sizeof(int32_t) * (size_t)n_cnt, s)) != cudaSuccess) return e;
     const int64_t row_blocks = std::min<int64_t>((n_q + 7) / 8, (int64_t)sms * 8);
-    k_tc_qhist<<<(unsigned)row_blocks, 256, 0, s>>>(q.indptr, h->tc_qcold, h->tc_qcold_n, n_q, win, dim,
-                                                    h->tc_qcnt);
+    k_tc_qmark<<<(unsigned)row_blocks, 256, 0, s>>>(q.indptr, h->tc_qcold, h->tc_qcold_n, n_q, h->tc_qcnt);
     if ((e = launch_count_scan(h->tc_qcnt, n_cnt, h->tc_qpart, h->tc_qptr, s)) != cudaSuccess) return e;
-    k_tc_qscatter<<<(unsigned)row_blocks, 256, 0, s>>>(q.indptr, h->tc_qcold, h->tc_qcold_n, n_q, win, dim,
-                                                       h->tc_qcnt, h->tc_qpost);
+    k_tc_qcid<<<(unsigned)row_blocks, 256, 0, s>>>(q.indptr, h->tc_qcold, h->tc_qcold_n, n_q, h->tc_qptr);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     nq += 6;
-    h->tc_win_rows = win;
-    h->tc_n_win = n_win;
+    // The number of cold dimensions the queries hold sizes every call's
+    // lists: read once here.
+    int32_t n_cid = 0;
+    if ((e = cudaMemcpyAsync(&n_cid, h->tc_qptr + dim, sizeof(int32_t), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+      return e;
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
+    if (n_cid < 0 || (int64_t)n_cid > dim) return cudaErrorIllegalState;
+    h->tc_n_cid = n_cid;
     h->tcq_src[0] = q.indptr;
     h->tcq_src[1] = q.indices;
     h->tcq_src[2] = q.values;
@@ -1562,10 +1549,9 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     h->tcq_rows = q.n_rows;
     h->tcq_nnz = q.nnz;
     h->tcq_generation = h->tc_hot_generation;
+    ++h->tcq_serial;
   }
-  const int win = h->tc_win_rows;
-  const int64_t n_win = h->tc_n_win;
-  const int qpw = win / 32;
+  const int64_t n_cid = h->tc_n_cid;
 
   // Item operand of this chunk.
   if ((e = grow(&h->tc_B, &h->tc_B_cap, n_tiles * kN * 2 * Hp, s)) != cudaSuccess) return e;
@@ -1593,38 +1579,72 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     ++nq;
   }
 
-  // Cold records, a segment per (query window, 32-item column block), in an
-  // array sized at three times the sample's estimate (blocks past it are
-  // computed by the scorer from the lists).
+  // The lists over the queries' cold dimensions, for every chunk of the
+  // index's build at once, at the first call that needs them.
+  const int64_t n_ccnt = n_cid + 1;
+  const bool is_view = &idx >= h->views && &idx < h->views + h->n_views;
+  const ss_index *first = is_view ? h->views : &idx;
+  const int n_chunks = is_view ? h->n_views : 1;
+  const int kpos = is_view ? (int)(&idx - h->views) : 0;
+  if (!(is_view && h->tc_lists_build == h->tc_build_serial && h->tc_lists_queries == h->tcq_serial)) {
+    const int64_t C = h->chunk_rows;
+    const int64_t items_all = (int64_t)(n_chunks - 1) * C + first[n_chunks - 1].n_items;
+    if (n_chunks > 1 && (first[1].icold_rng != first[0].icold_rng + C || first[1].icold != first[0].icold))
+      return cudaErrorInvalidValue;  // a build's chunks share one entry array, rows C apart
+    if ((e = grow(&h->tc_ccnt, &h->tc_ccnt_cap, n_chunks * n_ccnt, s)) != cudaSuccess) return e;
+    if ((e = grow(&h->tc_cptr, &h->tc_cptr_cap, n_chunks * n_ccnt, s)) != cudaSuccess) return e;
+    if ((e = grow(&h->tc_cpart, &h->tc_cpart_cap, scan_tile_count(n_chunks * n_ccnt) + 1, s)) != cudaSuccess)
+      return e;
+    if ((e = grow(&h->tc_chat, &h->tc_chat_cap, std::max<int64_t>(1, idx.capacity), s)) != cudaSuccess) return e;
+    h->tc_lists_build = 0;
+    const int64_t item_blocks = std::min<int64_t>((items_all + 7) / 8, (int64_t)sms * 8);
+    if ((e = cudaMemsetAsync(h->tc_ccnt, 0, sizeof(int32_t) * (size_t)(n_chunks * n_ccnt), s)) != cudaSuccess)
+      return e;
+    k_tc_chist<<<(unsigned)item_blocks, 256, 0, s>>>(first->icold, first->icold_rng, items_all, C, h->tc_qptr,
+                                                     n_ccnt, h->tc_ccnt);
+    if ((e = launch_count_scan(h->tc_ccnt, n_chunks * n_ccnt, h->tc_cpart, h->tc_cptr, s)) != cudaSuccess) return e;
+    k_tc_cscatter<<<(unsigned)item_blocks, 256, 0, s>>>(first->icold, first->icold_rng, items_all, C, h->tc_qptr,
+                                                        n_ccnt, h->tc_ccnt, h->tc_chat, h->tc_chat_cap,
+                                                        h->d_status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    nq += 5;
+    if (is_view) {
+      h->tc_lists_build = h->tc_build_serial;
+      h->tc_lists_queries = h->tcq_serial;
+    }
+    h->tc_lists_chunks = n_chunks;
+  }
+  const int32_t *col_ptr = h->tc_cptr + (int64_t)kpos * n_ccnt;
+  h->tc_lists_last = kpos;
+
+  // Cold records: a bucket per (32 query rows, 32 items) holding three
+  // times the sample's estimate of its records plus 64 (at least 64, at
+  // most 1024); the scorer computes the blocks of fuller buckets from the
+  // lists.
   const int64_t n_quarters = (n_q + 31) / 32;
   const int32_t n_cb = (n_items + kColBlock - 1) / kColBlock;
   const double est = std::max(0.0, h->tc_est_cold);
-  const int64_t rec_cap = (int64_t)std::min<double>((double)INT32_MAX,
-                                                     3.0 * est * (double)n_q * (double)n_items + (double)(1 << 20));
-  if ((e = grow(&h->tc_seg, &h->tc_seg_cap, n_win * n_cb * (int64_t)(qpw + 2), s)) != cudaSuccess) return e;
-  if ((e = grow(&h->tc_rec, &h->tc_rec_cap, rec_cap, s)) != cudaSuccess) return e;
-  if ((e = grow(&h->tc_cursor, &h->tc_cursor_cap, 1, s)) != cudaSuccess) return e;
+  const int32_t cap = (int32_t)std::min<double>(
+      1024.0, std::max<double>(64.0, std::ceil((3.0 * est * 1024.0 + 64.0) / 32.0) * 32.0));
+  if ((e = grow(&h->tc_rec_n, &h->tc_rec_n_cap, n_quarters * n_cb, s)) != cudaSuccess) return e;
+  if ((e = grow(&h->tc_rec, &h->tc_rec_cap, n_quarters * n_cb * (int64_t)cap, s)) != cudaSuccess) return e;
   {
     RecArgs ra;
-    ra.icold = idx.icold;
-    ra.icold_rng = idx.icold_rng;
-    ra.inv_i = inv_i;
-    ra.n_items = n_items;
-    ra.qcol_ptr = h->tc_qptr;
-    ra.qpost = h->tc_qpost;
-    ra.dim = dim;
+    ra.q_indptr = q.indptr;
+    ra.qcold = h->tc_qcold;
+    ra.qcold_n = h->tc_qcold_n;
     ra.n_q = n_q;
-    ra.win_rows = win;
-    ra.qpw = qpw;
+    ra.col_ptr = col_ptr;
+    ra.chat = h->tc_chat;
+    ra.inv_i = inv_i;
     ra.n_cb = n_cb;
+    ra.bucket_cap = cap;
     ra.rec = h->tc_rec;
-    ra.rec_cap = rec_cap;
-    ra.cursor = h->tc_cursor;
-    ra.seg = h->tc_seg;
+    ra.rec_n = h->tc_rec_n;
     ra.status = h->d_status;
-    if ((e = ensure_dyn_smem(k_tc_records, kRecSmem)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(h->tc_cursor, 0, sizeof(unsigned long long), s)) != cudaSuccess) return e;
-    k_tc_records<<<dim3((unsigned)n_cb, (unsigned)n_win), kRThreads, kRecSmem, s>>>(ra);
+    const size_t smem = sizeof(int) * (size_t)n_cb;
+    if ((e = ensure_dyn_smem(k_tc_records, smem)) != cudaSuccess) return e;
+    k_tc_records<<<(unsigned)n_quarters, kRThreads, smem, s>>>(ra);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ++nq;
   }
@@ -1643,14 +1663,14 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     sa.A = h->tc_A;
     sa.B = h->tc_B;
     sa.rec = h->tc_rec;
-    sa.seg = h->tc_seg;
-    sa.qpw = qpw;
-    sa.icold = idx.icold;
-    sa.icold_rng = idx.icold_rng;
+    sa.rec_n = h->tc_rec_n;
+    sa.bucket_cap = cap;
+    sa.q_indptr = q.indptr;
+    sa.qcold = h->tc_qcold;
+    sa.qcold_n = h->tc_qcold_n;
+    sa.col_ptr = col_ptr;
+    sa.chat = h->tc_chat;
     sa.inv_i = inv_i;
-    sa.qcol_ptr = h->tc_qptr;
-    sa.qpost = h->tc_qpost;
-    sa.dim = dim;
     sa.n_quarters = n_quarters;
     sa.n_cb = n_cb;
     sa.out = dst;

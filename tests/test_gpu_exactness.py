@@ -114,39 +114,48 @@ def test_index_is_the_chunks_csc(sec, algorithm, name, n_i, rb, re):
 
 @pytest.mark.parametrize("name,n_q", [("d1.2m_q5k_i200k", 5000), ("d65k_q1k_i10k", 1000),
                                       ("d1.2m_q20k_i1m_heavy", 3000)])
-def test_query_side_index_is_each_windows_csc(sec, name, n_q):
-    """The tensor path's lists by dimension live on the query side (built
-    once per query matrix, in windows of query rows): each window's lists
-    must be the CSC of those query rows' cold nonzeros, normalised by the
-    rows' inverse norms (float32 products), bit for bit."""
+def test_call_lists_are_the_chunks_csc_over_the_queries_cold_dims(sec, name, n_q):
+    """The tensor path sorts each chunk's nonzeros by the dimensions the
+    queries hold outside the hot set: a call's lists must be the CSC of its
+    chunk restricted to exactly those dimensions, with the stored values,
+    bit for bit; two builds in a row reuse the queries' numbering, and the
+    last chunk of a two-chunk build gets its own lists."""
     cfg = CONFIGS[name]
     Q, I = generate_rows(cfg, 0, 0, n_q), generate_rows(cfg, 1, 0, 9000)
     with sec.SparseCosine(cfg.dim, chunk_rows=8192, algorithm="tensor") as h:
         q, i = _dev(sec, Q), _dev(sec, I)
         inv_q, inv_i = h.row_norms(q), h.row_norms(i)
-        idx = h.build_item_index(i, 0, 8192)
-        hot = h.index_export(idx)["hot"]
-        out = torch.empty((n_q, 8192), dtype=torch.float32, device="cuda")
-        h.score_chunk(q, inv_q, idx, inv_i, out, 8192)  # prepares the query side
-        h.check_device()
-        first = h.query_index_export(0)
-        windows = [h.query_index_export(w) for w in range(first["n_windows"])]
-        inv = inv_q.cpu().numpy()
-    W = first["win_rows"]
-    assert W % 32 == 0 and first["n_windows"] == -(-n_q // W)
-    rows = np.repeat(np.arange(n_q), np.diff(Q.indptr))
-    normed = (Q.values * inv[rows]).astype(np.float32)
-    for w, ex in enumerate(windows):
-        r0, r1 = w * W, min((w + 1) * W, n_q)
-        lo, hi = int(Q.indptr[r0]), int(Q.indptr[r1])
-        sub = sp.csr_matrix((normed[lo:hi], Q.indices[lo:hi], Q.indptr[r0:r1 + 1] - lo), shape=(r1 - r0, cfg.dim))
-        coo = sub.tocoo()
-        keep = ~np.isin(coo.col, hot)
-        csc = sp.csr_matrix((coo.data[keep], (coo.row[keep], coo.col[keep])), shape=sub.shape).tocsc()
+        exports = []
+        for rb, re in ((0, 8192), (8192, 9000)):
+            idx = h.build_item_index(i, rb, re)
+            hot = h.index_export(idx)["hot"]
+            out = torch.empty((n_q, re - rb), dtype=torch.float32, device="cuda")
+            h.score_chunk(q, inv_q, idx, inv_i[rb:], out, re - rb)
+            h.check_device()
+            exports.append((rb, re, hot, h.lists_export()))
+        # one build of two chunks: the second chunk's lists
+        h2 = sec.SparseCosine(cfg.dim, chunk_rows=4500, algorithm="tensor")
+        try:
+            inv2, invq2 = h2.row_norms(i), h2.row_norms(q)
+            views = h2.build_item_indexes(i, 0, 9000)
+            assert len(views) == 2
+            for b, e, vw in views:
+                out = torch.empty((n_q, e - b), dtype=torch.float32, device="cuda")
+                h2.score_chunk(q, invq2, vw, inv2[b:], out, e - b)
+            h2.check_device()
+            hot2 = h2.index_export(views[1][2])["hot"]
+            exports.append((4500, 9000, hot2, h2.lists_export()))
+        finally:
+            h2.close()
+    for rb, re, hot_c, ex in exports:
+        qcold = np.setdiff1d(np.unique(Q.indices), hot_c)  # the queries' cold dimensions
+        assert np.array_equal(ex["dims"], qcold.astype(np.int32))
+        chunk = _scipy(I, rb, re)
+        csc = chunk[:, qcold].tocsc()
         csc.sort_indices()
-        assert np.array_equal(ex["col_ptr"].astype(np.int64), csc.indptr.astype(np.int64)), w
-        assert np.array_equal(ex["row"], csc.indices.astype(np.int32)), w
-        assert np.array_equal(ex["value"].view(np.uint32), csc.data.astype(np.float32).view(np.uint32)), w
+        assert np.array_equal(ex["col_ptr"].astype(np.int64), csc.indptr.astype(np.int64)), rb
+        assert np.array_equal(ex["item"], csc.indices.astype(np.int32)), rb
+        assert np.array_equal(ex["value"].view(np.uint32), csc.data.astype(np.float32).view(np.uint32)), rb
 
 
 def test_index_export_rejects_item_tiles(sec):
