@@ -34,8 +34,9 @@
 // shape and chunking), adds that to the tensor result and stores the tile.
 //
 // Scorer (k_tc_score): persistent, one block per SM, 18 warps.  Warp 0
-// loads operand tiles with bulk asynchronous copies (an item tile's operand
-// stays while the block works through its query tiles); warp 1 allocates
+// loads operand tiles with bulk asynchronous copies (a query tile's operand
+// stays while the block works through its item tiles, whose four K-half
+// sub-parts stream through three buffers); warp 1 allocates
 // tensor memory and one of its threads issues the MMAs into one of two
 // accumulators; warps 2-17 run the epilogue, four per quarter of the 128
 // accumulator lanes (each takes two of the eight 32-column blocks), on one
@@ -73,6 +74,7 @@ constexpr float kFixInv = 1.0f / 268435456.0f;
 constexpr float kMaxNormalised = 1.0f + 1.0f / 1024.0f;  // |x| of a normalised value
 constexpr float kMaxSquareSum = 1.0f + 1.0f / 64.0f;     // sum of x^2 of a normalised row
 constexpr int kStgInts = 32 * 32;              // one staging tile: 32 rows x 32 ints, 128-byte swizzle
+constexpr int kBBufs = 3;                      // scorer: item sub-part buffers
 constexpr int kEpiWarps = 16;                  // four per quarter of the accumulator lanes
 constexpr int kWarpsPerQ = kEpiWarps / 4;      // epilogue warps per quarter
 constexpr int kMine = 8 / kWarpsPerQ;          // 32-column blocks per warp and tile pair
@@ -405,20 +407,31 @@ __global__ void __launch_bounds__(kSelThreads)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) my_pairs += __shfl_xor_sync(0xffffffffu, my_pairs, o);
   if ((tid & 31) == 0) atomicAdd(&pairs_all, my_pairs);
-  __syncthreads();
   if (tid == 0) {
-    // Largest bin t where the dimensions in bins > t are fewer than kHotMax
-    // and those in bins >= t reach it; -1 when all of them fit.
-    int above = 0, thr = -1;
-    for (int c = kCountBins - 1; c >= floor_c; --c) {
-      if (above + hist[c] >= kHotMax) {
-        thr = c;
-        break;
-      }
-      above += hist[c];
+    thr_sh = -1;
+    take_ties = 0;
+  }
+  __syncthreads();
+  {
+    // The threshold: the largest bin t where the dimensions in bins > t are
+    // fewer than kHotMax and those in bins >= t reach it (-1 when all of
+    // them fit).  Thread i takes bin kCountBins - 1 - i, so a scan over the
+    // threads gives each bin the count of the bins at or above it.
+    static_assert(kCountBins == kSelThreads, "one count bin per thread");
+    __shared__ int wsum[kSelThreads / 32];
+    const int lane = tid & 31, w = tid >> 5;
+    const int c = kCountBins - 1 - tid;
+    const int hc = hist[c];
+    const int inc = warp_incl_scan(hc, lane);
+    if (lane == 31) wsum[w] = inc;
+    __syncthreads();
+    int before = 0;
+    for (int k = 0; k < w; ++k) before += wsum[k];
+    const int at_or_above = before + inc, above = at_or_above - hc;
+    if (c >= floor_c && at_or_above >= kHotMax && above < kHotMax) {
+      thr_sh = c;  // one bin at most: the counts only grow as c falls
+      take_ties = hc <= kTieCap;
     }
-    thr_sh = thr;
-    take_ties = thr >= 0 && hist[thr] <= kTieCap;
   }
   __syncthreads();
   const int thr = thr_sh;
@@ -639,22 +652,8 @@ __device__ __forceinline__ void put_split(uint16_t *gs, int rr, int h, int Hp, f
   gs[8 * Hp + core_off(rr, h)] = __half_as_ushort(lo);
 }
 
-// Writes a group buffer (hi and lo parts, 8 Hp halves each) to group g of an
-// operand whose tiles hold `gpt` groups.
-__device__ __forceinline__ void store_group(uint16_t *op, const uint16_t *gs, int64_t g, int gpt, int Hp,
-                                            int lane) {
-  const int64_t t = g / gpt, gl = g % gpt;
-  const int P = 8 * Hp;  // halves of one group part
-  uint16_t *hi = op + (t * 2 * gpt + gl) * P;
-  uint16_t *lo = hi + (int64_t)gpt * P;
-  for (int o = lane * 8; o < P; o += 256) {
-    *reinterpret_cast<uint4 *>(hi + o) = *reinterpret_cast<const uint4 *>(gs + o);
-    *reinterpret_cast<uint4 *>(lo + o) = *reinterpret_cast<const uint4 *>(gs + P + o);
-  }
-}
-
-// Writes a group buffer to group g of the query operand, whose tiles hold
-// four sub-parts in the order the MMAs read them: lo part K columns
+// Writes a group buffer to group g of an operand (queries or items) whose
+// tiles hold four sub-parts in the order the MMAs read them: lo part K columns
 // [0, Hp/2), lo part [Hp/2, Hp), hi part [0, Hp/2), hi part [Hp/2, Hp); each
 // sub-part is `gpt` groups of 8 rows x Hp/2 halves in the same no-swizzle
 // K-major layout (in the group buffer a part's two halves are already
@@ -768,7 +767,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_tc_prep_items(const PrepArgs a
       }
     }
     __syncwarp();
-    store_group(a.op, gs, g, a.gpt, Hp, lane);
+    store_group_q(a.op, gs, g, a.gpt, Hp, lane);
     __syncwarp();
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) flag(a.status, DEV_RANGE);
@@ -917,16 +916,17 @@ struct ScoreArgs {
   int64_t n_q;
   int32_t n_items;
   int64_t n_qtiles;
-  int64_t n_units;         // item tiles x query tiles
+  int64_t n_tiles;         // item tiles
+  int64_t n_units;         // query tiles x item tiles
   int32_t Hp;
   int32_t vec_ok;          // 16-byte aligned output rows: vector stores
   int32_t *status;
 };
 
-// Bytes of the scorer's dynamic shared memory for Hp hot columns: the item
-// tile (hi, lo: 1024 Hp), two buffers of one query sub-part (128 Hp each),
-// the epilogue staging (one 32 x 32 tile per epilogue warp).
-size_t score_smem_bytes(int Hp) { return (size_t)1280 * Hp + kStgBytes; }
+// Bytes of the scorer's dynamic shared memory for Hp hot columns: the query
+// tile (hi, lo: 512 Hp), kBBufs buffers of one item sub-part (256 Hp each),
+// the epilogue staging.
+size_t score_smem_bytes(int Hp) { return (size_t)(512 + 256 * kBBufs) * Hp + kStgBytes; }
 
 // Ties registers just loaded from tensor memory to the wait that completes
 // the load, so that no use of them is scheduled before it.
@@ -942,29 +942,32 @@ __device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[32]) {
 __global__ void __launch_bounds__(kSThreads, 1)
     k_tc_score(const __grid_constant__ ScoreArgs a) {
   extern __shared__ __align__(1024) unsigned char sm[];
-  __shared__ __align__(8) uint64_t bars[11];
+  __shared__ __align__(8) uint64_t bars[7 + 2 * kBBufs];
   __shared__ uint32_t tmem_slot;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hp = a.Hp;
-  const uint32_t bytesB = 1024u * (uint32_t)Hp, bytesApart = 256u * (uint32_t)Hp;
-  unsigned char *sB = sm;                          // hi part, then lo part
-  unsigned char *sA = sm + bytesB;                 // two buffers of one query sub-part (a K half of a part)
+  // The query tile (four sub-parts of 128 rows x Hp / 2 halves: lo K0,
+  // lo K1, hi K0, hi K1) stays while the block works through its item
+  // tiles; each item tile's four sub-parts (256 items x Hp / 2 halves, the
+  // same order) stream through kBBufs buffers.
+  const uint32_t bytesAsub = 128u * (uint32_t)Hp, bytesA = 4u * bytesAsub;
+  const uint32_t bytesBsub = 256u * (uint32_t)Hp;
+  unsigned char *sA = sm;
+  unsigned char *sB = sm + bytesA;
   int *stg_all = reinterpret_cast<int *>(
-      (reinterpret_cast<uintptr_t>(sA + bytesApart) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t b_full = smem_u32(&bars[0]), b_free = smem_u32(&bars[1]);
-  // bars[2..3]: query sub-part buffer 0 / 1 landed; bars[4..5]: buffer 0 / 1
-  // read by the MMAs (two phases of each per unit).
-  const uint32_t a_full[2] = {smem_u32(&bars[2]), smem_u32(&bars[3])};
-  const uint32_t a_free[2] = {smem_u32(&bars[4]), smem_u32(&bars[5])};
-  const uint32_t bytesAsub = bytesApart / 2;       // one sub-part: 128 rows x Hp / 2 halves
-  // bars[6..7]: accumulator b written (MMA commit); bars[8..9]: accumulator b
-  // read out (one arrival per epilogue warp).
-  const uint32_t acc_full0 = smem_u32(&bars[6]), acc_full1 = smem_u32(&bars[7]);
-  const uint32_t acc_free0 = smem_u32(&bars[8]), acc_free1 = smem_u32(&bars[9]);
-  const uint32_t drain = smem_u32(&bars[10]);  // the MMA thread's last commit
+      (reinterpret_cast<uintptr_t>(sB + kBBufs * bytesBsub) + 1023) & ~static_cast<uintptr_t>(1023));
+  // bars[0]: query tile landed; bars[1]: query tile read by the MMAs;
+  // bars[2..3]: accumulator b written (MMA commit); bars[4..5]: accumulator
+  // b read out (one arrival per epilogue warp); bars[6]: the MMA thread's
+  // last commit; then per item buffer: landed, read by the MMAs.
+  const uint32_t a_full = smem_u32(&bars[0]), a_free = smem_u32(&bars[1]);
+  const uint32_t acc_full0 = smem_u32(&bars[2]), acc_full1 = smem_u32(&bars[3]);
+  const uint32_t acc_free0 = smem_u32(&bars[4]), acc_free1 = smem_u32(&bars[5]);
+  const uint32_t drain = smem_u32(&bars[6]);
+  auto b_full = [&](int buf) { return smem_u32(&bars[7 + buf]); };
+  auto b_free = [&](int buf) { return smem_u32(&bars[7 + kBBufs + buf]); };
   if (tid == 0) {
-    for (int i = 0; i < 8; ++i) mbar_init(smem_u32(&bars[i]), 1);  // b, query buffers, accumulators
-    mbar_init(drain, 1);
+    for (int i = 0; i < 7 + 2 * kBBufs; ++i) mbar_init(smem_u32(&bars[i]), 1);
     mbar_init(acc_free0, kEpiWarps);
     mbar_init(acc_free1, kEpiWarps);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -980,107 +983,114 @@ __global__ void __launch_bounds__(kSThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
+  // Units are (query tile g, item tile t) pairs, u = g * n_tiles + t; each
+  // block takes a contiguous range, so its query tile rarely changes.
   const int64_t u0 = (int64_t)blockIdx.x * a.n_units / gridDim.x;
   const int64_t u1 = (int64_t)(blockIdx.x + 1) * a.n_units / gridDim.x;
   const int64_t nj = u1 - u0;
 
   if (warp == 0) {
-    // ---- producer: the item tile when it changes, then per unit the query
-    // tile's four sub-parts (lo K0, lo K1, hi K0, hi K1), copy k into buffer
-    // k % 2 once the MMAs have released that buffer's previous sub-part.
+    // ---- producer: the query tile when it changes (once the MMAs have
+    // released the previous one), then per unit the item tile's four
+    // sub-parts, copy n into buffer n % kBBufs once the MMAs have released
+    // that buffer's previous copy.
     if (lane == 0) {
       const uint64_t keep = evict_last_policy();
-      int64_t prev_t = -1;
-      int nb = 0;         // item tile copies issued
-      int64_t na = 0;     // query sub-part copies issued
-      for (int64_t j = 0; j < nj; ++j) {
-        const int64_t u = u0 + j, t = u / a.n_qtiles, g = u % a.n_qtiles;
-        if (t != prev_t) {
-          if (nb > 0 && !mbar_wait(b_free, (uint32_t)((nb - 1) & 1), a.status)) break;
-          mbar_expect_tx(b_full, bytesB);
-          bulk_g2s_hint(smem_u32(sB), a.B + (size_t)t * (bytesB / 2), bytesB, b_full, keep);
-          ++nb;
-          prev_t = t;
-        }
-        const uint16_t *At = a.A + (size_t)g * (bytesApart);  // a tile: four sub-parts of bytesAsub bytes
-        bool ok = true;
-        for (int sp = 0; sp < 4 && ok; ++sp) {
-          const int buf = (int)(na & 1);
-          const int64_t k = na >> 1;  // copies into this buffer before this one
-          if (k > 0) ok = mbar_wait(a_free[buf], (uint32_t)((k - 1) & 1), a.status);
-          if (!ok) break;
-          mbar_expect_tx(a_full[buf], bytesAsub);
-          bulk_g2s_hint(smem_u32(sA) + (uint32_t)buf * bytesAsub, At + (size_t)sp * (bytesAsub / 2), bytesAsub,
-                        a_full[buf], keep);
+      int64_t prev_g = -1;
+      int na = 0;        // query tile copies issued
+      int64_t nbc = 0;   // item sub-part copies issued
+      bool ok = true;
+      for (int64_t j = 0; j < nj && ok; ++j) {
+        const int64_t u = u0 + j, g = u / a.n_tiles, t = u % a.n_tiles;
+        if (g != prev_g) {
+          if (na > 0 && !(ok = mbar_wait(a_free, (uint32_t)((na - 1) & 1), a.status))) break;
+          mbar_expect_tx(a_full, bytesA);
+          bulk_g2s_hint(smem_u32(sA), a.A + (size_t)g * (bytesA / 2), bytesA, a_full, keep);
           ++na;
+          prev_g = g;
         }
-        if (!ok) break;
+        const uint16_t *Bt = a.B + (size_t)t * (2 * (size_t)bytesBsub);  // 4 sub-parts of bytesBsub bytes
+        for (int sp = 0; sp < 4; ++sp) {
+          const int buf = (int)(nbc % kBBufs);
+          const int64_t k = nbc / kBBufs;  // copies into this buffer before this one
+          if (k > 0 && !(ok = mbar_wait(b_free(buf), (uint32_t)((k - 1) & 1), a.status))) break;
+          mbar_expect_tx(b_full(buf), bytesBsub);
+          bulk_g2s_hint(smem_u32(sB) + (uint32_t)buf * bytesBsub, Bt + (size_t)sp * (bytesBsub / 2), bytesBsub,
+                        b_full(buf), keep);
+          ++nbc;
+        }
       }
       // Every copy issued lands before the block exits, also when a wait
-      // above gave up: copy k into a buffer is issued only after the phase
-      // of copy k - 1 completed, so the phase of the last copy issued is the
-      // one still open, and a bulk copy completes by itself.
-      for (int buf = 0; buf < 2; ++buf) {
-        const int64_t n_buf = (na + 1 - buf) >> 1;  // copies issued into this buffer
-        if (n_buf > 0) mbar_wait(a_full[buf], (uint32_t)((n_buf - 1) & 1), a.status);
+      // above gave up: copy k into a buffer is issued only after the MMAs
+      // released copy k - 1 (which had landed), so at most the last copy of
+      // each buffer is in flight, and a bulk copy completes by itself.
+      for (int buf = 0; buf < kBBufs; ++buf) {
+        const int64_t n_buf = (nbc + kBBufs - 1 - buf) / kBBufs;  // copies issued into this buffer
+        if (n_buf > 0) mbar_wait(b_full(buf), (uint32_t)((n_buf - 1) & 1), a.status);
       }
-      if (nb > 0) mbar_wait(b_full, (uint32_t)((nb - 1) & 1), a.status);
+      if (na > 0) mbar_wait(a_full, (uint32_t)((na - 1) & 1), a.status);
     }
   } else if (warp == 1) {
-    // ---- MMA issue: lo_q x hi_v (as soon as the lo part is in), then
-    // hi_q x lo_v and hi_q x hi_v.
+    // ---- MMA issue, per unit: the cross terms hi_q x lo_v and lo_q x hi_v
+    // first (while the sum is small), then hi_q x hi_v.
     if (lane == 0) {
       const uint32_t idesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
       const int Kp = Hp / 2;
-      const uint32_t sboA = 16u * (uint32_t)Kp, sboB = 16u * (uint32_t)Hp, lbo = 128u;
-      const uint32_t bhi = smem_u32(sB), blo = bhi + bytesB / 2;
-      const uint32_t abuf[2] = {smem_u32(sA), smem_u32(sA) + bytesAsub};
-      // Sub-part s of unit j is copy 4 j + s, in buffer s % 2, at that
-      // buffer's phase 2 j + s / 2.
-      auto wait_part = [&](int s) { return mbar_wait(a_full[s & 1], (uint32_t)((s >> 1) & 1), a.status); };
-      // The Kp-column product of a sub-part buffer with K half h of item part bp.
-      auto mma_half = [&](uint32_t d, int buf, uint32_t bp, int h, bool first) {
+      const uint32_t sbo = 16u * (uint32_t)Kp, lbo = 128u;
+      const uint32_t aa = smem_u32(sA);
+      const uint32_t a_lo0 = aa, a_lo1 = aa + bytesAsub, a_hi0 = aa + 2 * bytesAsub, a_hi1 = aa + 3 * bytesAsub;
+      // The Kp-column product of a query sub-part with an item sub-part.
+      auto mma_sub = [&](uint32_t d, uint32_t a_addr, uint32_t b_addr, bool first) {
         for (int kk = 0; kk < Kp; kk += 16)
-          mma_f16(d, smem_desc(abuf[buf] + (uint32_t)(kk / 8) * 128u, lbo, sboA),
-                  smem_desc(bp + (uint32_t)((h * Kp + kk) / 8) * 128u, lbo, sboB), idesc,
-                  (first && kk == 0) ? 0u : 1u);
+          mma_f16(d, smem_desc(a_addr + (uint32_t)(kk / 8) * 128u, lbo, sbo),
+                  smem_desc(b_addr + (uint32_t)(kk / 8) * 128u, lbo, sbo), idesc, (first && kk == 0) ? 0u : 1u);
       };
-      int64_t prev_t = -1;
-      int nb = 0;
+      int64_t prev_g = -1;
+      int na = 0;
+      int64_t nbc = 0;
       bool ok = true;
+      uint32_t bb[4];
+      int bufs[4];
+      // Waits for item sub-part s of the current unit (copy nbc + s).
+      auto wait_sub = [&](int s) -> bool {
+        const int64_t n = nbc + s;
+        const int buf = (int)(n % kBBufs);
+        bufs[s] = buf;
+        bb[s] = smem_u32(sB) + (uint32_t)buf * bytesBsub;
+        return mbar_wait(b_full(buf), (uint32_t)((n / kBBufs) & 1), a.status);
+      };
       for (int64_t j = 0; j < nj && ok; ++j) {
-        const int64_t t = (u0 + j) / a.n_qtiles;
-        if (t != prev_t) {
-          if (prev_t >= 0) mma_commit(b_free);  // the previous item tile is no longer read
-          ok = mbar_wait(b_full, (uint32_t)(nb & 1), a.status);
-          ++nb;
-          prev_t = t;
+        const int64_t g = (u0 + j) / a.n_tiles;
+        if (g != prev_g) {
+          if (prev_g >= 0) mma_commit(a_free);  // the previous query tile is no longer read
+          ok = mbar_wait(a_full, (uint32_t)(na & 1), a.status);
+          ++na;
+          prev_g = g;
+          if (!ok) break;
         }
         const int b = (int)(j & 1);
-        if (ok && j >= 2) ok = mbar_wait(b ? acc_free1 : acc_free0, (uint32_t)(((j - 2) >> 1) & 1), a.status);
-        if (!ok) break;
+        if (j >= 2 && !(ok = mbar_wait(b ? acc_free1 : acc_free0, (uint32_t)(((j - 2) >> 1) & 1), a.status))) break;
         const uint32_t d = tmem + (uint32_t)(b * kN);
-        // lo_q x hi_v over both K halves, then hi_q x lo_v, then hi_q x hi_v
-        // (the cross terms first, while the sum is small).
-        if (!(ok = wait_part(0))) break;
+        if (!(ok = wait_sub(0))) break;
         tc_fence_after();
-        mma_half(d, 0, bhi, 0, true);
-        mma_commit(a_free[0]);
-        if (!(ok = wait_part(1))) break;
+        mma_sub(d, a_hi0, bb[0], true);   // hi_q x lo_v, K half 0
+        mma_commit(b_free(bufs[0]));
+        if (!(ok = wait_sub(1))) break;
         tc_fence_after();
-        mma_half(d, 1, bhi, 1, false);
-        mma_commit(a_free[1]);
-        if (!(ok = wait_part(2))) break;
+        mma_sub(d, a_hi1, bb[1], false);  // hi_q x lo_v, K half 1
+        mma_commit(b_free(bufs[1]));
+        if (!(ok = wait_sub(2))) break;
         tc_fence_after();
-        mma_half(d, 0, blo, 0, false);
-        if (!(ok = wait_part(3))) break;
+        mma_sub(d, a_lo0, bb[2], false);  // lo_q x hi_v, K half 0
+        if (!(ok = wait_sub(3))) break;
         tc_fence_after();
-        mma_half(d, 1, blo, 1, false);
-        mma_half(d, 0, bhi, 0, false);
-        mma_commit(a_free[0]);
-        mma_half(d, 1, bhi, 1, false);
-        mma_commit(a_free[1]);
+        mma_sub(d, a_lo1, bb[3], false);  // lo_q x hi_v, K half 1
+        mma_sub(d, a_hi0, bb[2], false);  // hi_q x hi_v, K half 0
+        mma_commit(b_free(bufs[2]));
+        mma_sub(d, a_hi1, bb[3], false);  // hi_q x hi_v, K half 1
+        mma_commit(b_free(bufs[3]));
         mma_commit(b ? acc_full1 : acc_full0);
+        nbc += 4;
       }
       // Every MMA this thread issued has completed before the tensor memory
       // is freed, also when a wait above gave up: a commit arrives once all
@@ -1107,14 +1117,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // Lanes 0..7: the record counts of the unit's 8 column blocks (0 past
     // the chunk or the queries).
     auto load_cnt = [&](int64_t u) -> int {
-      const int64_t t = u / a.n_qtiles, g = u % a.n_qtiles;
+      const int64_t g = u / a.n_tiles, t = u % a.n_tiles;
       const int64_t Q = g * 4 + qd;
       const int cb = (int)t * 8 + lane;
       return (Q < a.n_quarters && lane < 8 && cb < a.n_cb) ? ld_keep_int(a.rec_n + Q * a.n_cb + cb) : 0;
     };
     // The bucket of the unit's column block 0 (block c's follows at c * cap).
     auto bucket0 = [&](int64_t u) -> const int2 * {
-      const int64_t t = u / a.n_qtiles, g = u % a.n_qtiles;
+      const int64_t g = u / a.n_tiles, t = u % a.n_tiles;
       const int64_t Q = g * 4 + qd;
       return a.rec + (Q * a.n_cb + t * 8) * (int64_t)cap;
     };
@@ -1142,7 +1152,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       fetch(cnt, bk, sub + kWarpsPerQ, R[1]);
     }
     for (int64_t j = 0; j < nj; ++j) {
-      const int64_t u = u0 + j, t = u / a.n_qtiles, g = u % a.n_qtiles;
+      const int64_t u = u0 + j, g = u / a.n_tiles, t = u % a.n_tiles;
       const int b = (int)(j & 1);
       int ok = 1;
       if (lane == 0) ok = mbar_wait(b ? acc_full1 : acc_full0, (uint32_t)((j >> 1) & 1), a.status);
@@ -1678,6 +1688,7 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     sa.n_q = n_q;
     sa.n_items = n_items;
     sa.n_qtiles = n_qtiles;
+    sa.n_tiles = n_tiles;
     sa.n_units = n_tiles * n_qtiles;
     sa.Hp = Hp;
     sa.vec_ok = ((reinterpret_cast<uintptr_t>(dst) % 16) == 0) && (ld_dst % 4 == 0);
