@@ -209,7 +209,7 @@ void free_lazy_buffers(ss_handle *h) {
   h->qhot_dense_cap = h->hot_scratch_cap = 0;
   void *tc[] = {h->tc_hot, h->tc_sel, h->tc_stats, h->tc_A, h->tc_qcold, h->tc_qcold_n, h->tc_qcnt,
                 h->tc_qptr, h->tc_qpart, h->tc_slab, h->tc_sq, h->tc_icold_rng, h->tc_B, h->tc_ccnt,
-                h->tc_cptr, h->tc_cpart, h->tc_chat, h->tc_rec, h->tc_rec_n};
+                h->tc_cptr, h->tc_cpart, h->tc_chat, h->tc_icid, h->tc_rec, h->tc_rec_n};
   for (void *p : tc) cudaFree(p);
   h->tc_hot = h->tc_sel = h->tc_qcold_n = nullptr;
   h->tc_qcnt = h->tc_qptr = h->tc_qpart = nullptr;
@@ -220,6 +220,8 @@ void free_lazy_buffers(ss_handle *h) {
   h->tc_A_cap = h->tc_qcold_cap = h->tc_qcold_n_cap = h->tc_B_cap = h->tc_rec_cap = h->tc_rec_n_cap = 0;
   h->tc_qcnt_cap = h->tc_qptr_cap = h->tc_qpart_cap = 0;
   h->tc_ccnt_cap = h->tc_cptr_cap = h->tc_cpart_cap = h->tc_chat_cap = 0;
+  h->tc_icid = nullptr;
+  h->tc_icid_cap = 0;
   h->tc_n_cid = 0;
   h->tcq_rows = -1;  // the query side is made again, whole
   h->tc_lists_build = 0;

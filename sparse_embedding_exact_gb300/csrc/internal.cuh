@@ -315,6 +315,8 @@ struct ss_handle {
   int64_t tc_ccnt_cap = 0, tc_cptr_cap = 0, tc_cpart_cap = 0;
   int2 *tc_chat = nullptr;
   int64_t tc_chat_cap = 0;
+  int32_t *tc_icid = nullptr;  // per build entry (as the build's cold entries): its cold number or -1
+  int64_t tc_icid_cap = 0;
   uint64_t tc_build_serial = 0, tc_lists_build = 0, tc_lists_queries = 0;
   int32_t tc_lists_chunks = 0, tc_lists_last = 0;
   // Cold records of one scoring call: sub-buckets of (8 query rows, 32

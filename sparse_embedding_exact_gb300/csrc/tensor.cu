@@ -222,6 +222,8 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
+// Brings the 128-byte line holding p into this SM's L1 (no register).
+__device__ __forceinline__ void prefetch_l1(const void *p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Until all of this thread's bulk store groups have read their
 // shared-memory source.
@@ -570,15 +572,18 @@ __global__ void __launch_bounds__(256)
 // per chunk), made at the first scoring call that needs them: a counting
 // sort of the build's per-item cold entries by (chunk, cid), the entries of
 // dimensions no query holds cold left out.  The histogram here (a warp per
-// item), launch_count_scan over the n_chunks x (n_cid + 1) counters, then
-// the scatter, which writes {item within its chunk, raw value bits} (each
+// item; each entry's number, or -1, is kept beside it so that the scatter
+// reads it back in order instead of looking it up again),
+// launch_count_scan over the n_chunks x (n_cid + 1) counters, then the
+// scatter, which writes {item within its chunk, raw value bits} (each
 // call's records kernel multiplies by that call's inverse norms).  A
 // list's order is unspecified: the records it makes are summed as
 // integers.  Items are numbered across the build: item `it` is row
 // it % chunk_rows of chunk it / chunk_rows.
 __global__ void __launch_bounds__(256)
     k_tc_chist(const int2 *__restrict__ icold, const int2 *__restrict__ icold_rng, int64_t n_items,
-               int64_t chunk_rows, const int32_t *__restrict__ cid, int64_t n_ccnt, int32_t *__restrict__ count) {
+               int64_t chunk_rows, const int32_t *__restrict__ cid, int64_t n_ccnt, int32_t *__restrict__ count,
+               int32_t *__restrict__ icid) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * 8;
   for (int64_t it = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); it < n_items; it += warps) {
@@ -587,6 +592,7 @@ __global__ void __launch_bounds__(256)
     for (int j = lane; j < rng.y; j += 32) {
       const int d = __ldg(icold + rng.x + j).x;
       const int c0 = __ldg(cid + d), c1 = __ldg(cid + d + 1);
+      icid[rng.x + j] = c1 > c0 ? c0 : -1;
       if (c1 > c0) atomicAdd(cnt + c0, 1);
     }
   }
@@ -594,7 +600,7 @@ __global__ void __launch_bounds__(256)
 
 __global__ void __launch_bounds__(256)
     k_tc_cscatter(const int2 *__restrict__ icold, const int2 *__restrict__ icold_rng, int64_t n_items,
-                  int64_t chunk_rows, const int32_t *__restrict__ cid, int64_t n_ccnt,
+                  int64_t chunk_rows, const int32_t *__restrict__ icid, int64_t n_ccnt,
                   int32_t *__restrict__ cursor, int2 *__restrict__ chat, int64_t capacity, int32_t *status) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * 8;
@@ -604,12 +610,11 @@ __global__ void __launch_bounds__(256)
     int32_t *cur = cursor + c * n_ccnt;
     const int item = (int)(it - c * chunk_rows);
     for (int j = lane; j < rng.y; j += 32) {
-      const int2 e = __ldg(icold + rng.x + j);
-      const int c0 = __ldg(cid + e.x), c1 = __ldg(cid + e.x + 1);
-      if (c1 <= c0) continue;
+      const int c0 = __ldg(icid + rng.x + j);
+      if (c0 < 0) continue;
       const int32_t pos = atomicAdd(cur + c0, 1);
       if (pos >= 0 && (int64_t)pos < capacity)
-        chat[pos] = make_int2(item, e.y);
+        chat[pos] = make_int2(item, __ldg(icold + rng.x + j).y);
       else
         flag(status, DEV_CAPACITY);
     }
@@ -1116,18 +1121,27 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int cap = a.bucket_cap;
     // Lanes 0..7: the record counts of the unit's 8 column blocks (0 past
     // the chunk or the queries).
-    auto load_cnt = [&](int64_t u) -> int {
-      const int64_t g = u / a.n_tiles, t = u % a.n_tiles;
-      const int64_t Q = g * 4 + qd;
-      const int cb = (int)t * 8 + lane;
-      return (Q < a.n_quarters && lane < 8 && cb < a.n_cb) ? ld_keep_int(a.rec_n + Q * a.n_cb + cb) : 0;
+    const int n_tiles = (int)a.n_tiles, n_quarters = (int)a.n_quarters, n_cb = a.n_cb;
+    // Units are numbered (g, t): query tile g, item tile t; next(g, t)
+    // steps to the following unit without a division.
+    auto next_unit = [&](int &g, int &t) {
+      if (++t == n_tiles) {
+        t = 0;
+        ++g;
+      }
+    };
+    auto load_cnt = [&](int g, int t) -> int {
+      const int Q = g * 4 + qd;
+      const int cb = t * 8 + lane;
+      return (Q < n_quarters && lane < 8 && cb < n_cb) ? ld_keep_int(a.rec_n + (int64_t)Q * n_cb + cb) : 0;
     };
     // The bucket of the unit's column block 0 (block c's follows at c * cap).
-    auto bucket0 = [&](int64_t u) -> const int2 * {
-      const int64_t g = u / a.n_tiles, t = u % a.n_tiles;
-      const int64_t Q = g * 4 + qd;
-      return a.rec + (Q * a.n_cb + t * 8) * (int64_t)cap;
+    auto bucket0 = [&](int g, int t) -> const int2 * {
+      const int Q = g * 4 + qd;
+      return a.rec + ((int64_t)Q * n_cb + t * 8) * cap;
     };
+    // Block c's first 32 kRecPerLane records into dst; the lines of the
+    // rest (if any) into L1, for the loop that adds them.
     auto fetch = [&](int counts, const int2 *bucket, int c, int2(&dst)[kRecPerLane]) {
       const int n = __shfl_sync(0xffffffffu, counts, c);
       const int2 *bc = bucket + (int64_t)c * cap;
@@ -1137,6 +1151,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
         dst[m] = make_int2(0, 0);  // no record
         if (p < n) dst[m] = ld_keep_int2(bc + p);
       }
+      const int p = 32 * kRecPerLane + 16 * lane;  // 16 records (one line) per lane
+      if (p < n) prefetch_l1(bc + p);
     };
     // The warp's blocks in order: block kMine j + i is column block
     // sub + kWarpsPerQ i of unit j.  Its records sit in register set i % 2;
@@ -1144,28 +1160,29 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // records are added, so that each load has about two blocks of work to
     // land in.  Record counts are read two units ahead.
     static_assert(kMine >= 2 && kMine % 2 == 0, "two register sets of records");
-    int cnt = nj > 0 ? load_cnt(u0) : 0, cnt_n = nj > 1 ? load_cnt(u0 + 1) : 0, cnt_nn = 0;
-    const int2 *bk = nj > 0 ? bucket0(u0) : a.rec, *bk_n = nj > 1 ? bucket0(u0 + 1) : a.rec, *bk_nn = a.rec;
+    const int nv = (int)nj;  // units fit 32 bits (checked at launch)
+    int g = (int)(u0 / n_tiles), t = (int)(u0 - (int64_t)g * n_tiles);  // the current unit
+    int g1 = g, t1 = t;
+    next_unit(g1, t1);  // the next one
+    int g2 = g1, t2 = t1;
+    next_unit(g2, t2);  // the one after
+    int cnt = nv > 0 ? load_cnt(g, t) : 0, cnt_n = nv > 1 ? load_cnt(g1, t1) : 0, cnt_nn = 0;
     int2 R[2][kRecPerLane];
-    if (nj > 0) {
-      fetch(cnt, bk, sub, R[0]);
-      fetch(cnt, bk, sub + kWarpsPerQ, R[1]);
+    if (nv > 0) {
+      fetch(cnt, bucket0(g, t), sub, R[0]);
+      fetch(cnt, bucket0(g, t), sub + kWarpsPerQ, R[1]);
     }
-    for (int64_t j = 0; j < nj; ++j) {
-      const int64_t u = u0 + j, g = u / a.n_tiles, t = u % a.n_tiles;
-      const int b = (int)(j & 1);
+    for (int j = 0; j < nv; ++j) {
+      const int b = j & 1;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(b ? acc_full1 : acc_full0, (uint32_t)((j >> 1) & 1), a.status);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       __syncwarp();
       if (!ok) break;
       tc_fence_after();
-      if (j + 2 < nj) {
-        cnt_nn = load_cnt(u + 2);
-        bk_nn = bucket0(u + 2);
-      }
-      const int64_t qrow0 = (g * 4 + qd) * 32;
-      const int item0 = (int)t * kN;
+      if (j + 2 < nv) cnt_nn = load_cnt(g2, t2);
+      const int qrow0 = (g * 4 + qd) * 32;
+      const int item0 = t * kN;
       const uint32_t tbase = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(b * kN);
 #pragma unroll
       for (int i = 0; i < kMine; ++i) {
@@ -1179,8 +1196,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const int n = __shfl_sync(0xffffffffu, cnt, c);
         // The records of the block two later, into the set just used.
         auto prefetch = [&]() {
-          if (i + 2 < kMine) fetch(cnt, bk, c + 2 * kWarpsPerQ, Rc);
-          else if (j + 1 < nj) fetch(cnt_n, bk_n, sub + kWarpsPerQ * (i + 2 - kMine), Rc);
+          if (i + 2 < kMine) fetch(cnt, bucket0(g, t), c + 2 * kWarpsPerQ, Rc);
+          else if (j + 1 < nv) fetch(cnt_n, bucket0(g1, t1), sub + kWarpsPerQ * (i + 2 - kMine), Rc);
         };
         if (tma) {  // the bulk store that last read this staging tile is done reading it
           if (lane == 0) {
@@ -1200,7 +1217,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
           for (int m = 0; m < kRecPerLane; ++m)
             if (Rc[m].y != 0) atomicAdd(stg + Rc[m].x, Rc[m].y);
           prefetch();
-          const int2 *bc = bk + (int64_t)c * cap;
+          const int2 *bc = bucket0(g, t) + (int64_t)c * cap;
           for (int p = 32 * kRecPerLane + lane; p < n; p += 32) {  // past the first 32 kRecPerLane (rare)
             const int2 rr = ld_keep_int2(bc + p);
             atomicAdd(stg + rr.x, rr.y);
@@ -1208,7 +1225,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
           if (n < 0) {
             // The bucket did not fit: each lane walks its row's cold lists
             // and keeps the items of this block (rare; exact, the same sums).
-            const int64_t q = qrow0 + lane;
+            const int64_t q = (int64_t)qrow0 + lane;
             const int lo = item0 + c * kColBlock;
             if (q < a.n_q) {
               const int64_t qb = a.q_indptr[q];
@@ -1251,7 +1268,6 @@ __global__ void __launch_bounds__(kSThreads, 1)
                             __uint_as_float(rc[4 * k + 2]), __uint_as_float(rc[4 * k + 3]));
         }
         __syncwarp();
-        const int it = item0 + c * kColBlock + 4 * (lane & 7);
         if (tma) {
           // One bulk tensor store of the tile (its layout is the map's
           // 128-byte swizzle); rows past the queries and columns past the
@@ -1266,19 +1282,20 @@ __global__ void __launch_bounds__(kSThreads, 1)
         } else if (vec && qrow0 + 32 <= a.n_q && item0 + (c + 1) * kColBlock <= a.n_items) {
           // Row-contiguous stores: lane l writes items 4 (l % 8) .. + 3 of
           // rows 4 s + l / 8 (chunk l % 8 of the row, found through the swizzle).
-          float *my_row = a.out + (qrow0 + (lane >> 3)) * a.ld_out + item0 + 4 * (lane & 7);
+          float *my_row = a.out + ((int64_t)qrow0 + (lane >> 3)) * a.ld_out + item0 + c * kColBlock + 4 * (lane & 7);
 #pragma unroll
           for (int sidx = 0; sidx < 8; ++sidx) {
             const int rl = 4 * sidx + (lane >> 3);
             const float4 v = *reinterpret_cast<const float4 *>(stg + rl * 32 + 4 * ((lane & 7) ^ (rl & 7)));
-            __stcs(reinterpret_cast<float4 *>(my_row + (int64_t)(4 * sidx) * a.ld_out + c * kColBlock), v);
+            __stcs(reinterpret_cast<float4 *>(my_row + (int64_t)(4 * sidx) * a.ld_out), v);
           }
         } else {
+          const int it = item0 + c * kColBlock + 4 * (lane & 7);
 #pragma unroll
           for (int sidx = 0; sidx < 8; ++sidx) {
             const int rl = 4 * sidx + (lane >> 3);
             const float4 v = *reinterpret_cast<const float4 *>(stg + rl * 32 + 4 * ((lane & 7) ^ (rl & 7)));
-            const int64_t q = qrow0 + rl;
+            const int64_t q = (int64_t)qrow0 + rl;
             if (q < a.n_q && it < a.n_items) {
               float *dst = a.out + q * a.ld_out + it;
               if (vec && it + 4 <= a.n_items) {
@@ -1293,9 +1310,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
         __syncwarp();
       }
       cnt = cnt_n;
-      bk = bk_n;
       cnt_n = cnt_nn;
-      bk_n = bk_nn;
+      g = g1;
+      t = t1;
+      g1 = g2;
+      t1 = t2;
+      next_unit(g2, t2);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b ? acc_free1 : acc_free0);
@@ -1606,14 +1626,15 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     if ((e = grow(&h->tc_cpart, &h->tc_cpart_cap, scan_tile_count(n_chunks * n_ccnt) + 1, s)) != cudaSuccess)
       return e;
     if ((e = grow(&h->tc_chat, &h->tc_chat_cap, std::max<int64_t>(1, idx.capacity), s)) != cudaSuccess) return e;
+    if ((e = grow(&h->tc_icid, &h->tc_icid_cap, std::max<int64_t>(1, idx.capacity), s)) != cudaSuccess) return e;
     h->tc_lists_build = 0;
     const int64_t item_blocks = std::min<int64_t>((items_all + 7) / 8, (int64_t)sms * 8);
     if ((e = cudaMemsetAsync(h->tc_ccnt, 0, sizeof(int32_t) * (size_t)(n_chunks * n_ccnt), s)) != cudaSuccess)
       return e;
     k_tc_chist<<<(unsigned)item_blocks, 256, 0, s>>>(first->icold, first->icold_rng, items_all, C, h->tc_qptr,
-                                                     n_ccnt, h->tc_ccnt);
+                                                     n_ccnt, h->tc_ccnt, h->tc_icid);
     if ((e = launch_count_scan(h->tc_ccnt, n_chunks * n_ccnt, h->tc_cpart, h->tc_cptr, s)) != cudaSuccess) return e;
-    k_tc_cscatter<<<(unsigned)item_blocks, 256, 0, s>>>(first->icold, first->icold_rng, items_all, C, h->tc_qptr,
+    k_tc_cscatter<<<(unsigned)item_blocks, 256, 0, s>>>(first->icold, first->icold_rng, items_all, C, h->tc_icid,
                                                         n_ccnt, h->tc_ccnt, h->tc_chat, h->tc_chat_cap,
                                                         h->d_status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1694,6 +1715,7 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     sa.vec_ok = ((reinterpret_cast<uintptr_t>(dst) % 16) == 0) && (ld_dst % 4 == 0);
     sa.use_tma = sa.vec_ok && encode_out_map(&sa.out_map, dst, n_q, n_items, ld_dst) ? 1 : 0;
     sa.status = h->d_status;
+    if (sa.n_units > INT32_MAX || n_q > INT32_MAX - 256) return cudaErrorInvalidValue;  // 32-bit unit and row numbers
     const int64_t grid = std::min<int64_t>(sms, sa.n_units);
     prof_mark(h, s);
     k_tc_score<<<(unsigned)grid, kSThreads, score_smem_bytes(Hp), s>>>(sa);
