@@ -22,10 +22,11 @@
 //
 // The remaining ("cold") dimensions are few per pair (0.11 expected on the
 // 1.2M-word workload).  Once per query matrix the dimensions the queries
-// hold cold are numbered; each scoring call sorts the chunk's nonzeros in
-// those dimensions into lists by number (a counting sort: the chunk's
-// other nonzeros make no product), and a records kernel walks, for every
-// block of 8 query rows, each row's cold nonzeros against those lists and
+// hold cold are numbered; the first scoring call after a build sorts the
+// build's nonzeros in those dimensions into lists by number, per chunk (a
+// counting sort: the other nonzeros make no product), and a records kernel
+// walks, for every block of 32 query rows, each row's cold nonzeros against
+// the chunk's lists and
 // writes one record per product, bucketed by (32 query rows, 32 items):
 // the position inside the bucket and the product rounded to a fixed-point
 // integer of resolution 2^-28.  The scorer's epilogue adds a bucket's
@@ -737,43 +738,50 @@ __global__ void __launch_bounds__(kPrepThreads) k_tc_prep_queries(const PrepArgs
   if (__any_sync(0xffffffffu, bad) && lane == 0) flag(a.status, DEV_RANGE);
 }
 
-// The item operand of a chunk from its hot slab: one warp per group of 8
-// items (lane l reads row l / 4, hot columns 32 (l % 4) .. + 31 as eight
-// float4 loads issued together); every K column written, zeros past the
-// chunk; the inverse norms are checked against the items' sums of squares.
-__global__ void __launch_bounds__(kPrepThreads) k_tc_prep_items(const PrepArgs a) {
-  __shared__ __align__(16) uint16_t grp[kPrepThreads / 32][8 * 2 * kHotMax];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int Hp = a.Hp;
-  const int rr = lane >> 2, h0 = 32 * (lane & 3);
-  uint16_t *gs = grp[warp];
+// The item operand of a chunk from its hot slab, written without a shared
+// staging buffer: a warp takes a group of 8 items, and lane l the 16-byte
+// chunks (item l % 8, K columns 8 kc .. + 7) for kc = l / 8, l / 8 + 4, ...:
+// eight slab values, normalised and split, give one hi chunk and one lo
+// chunk, each stored whole at its place in the K-half sub-part (a warp's
+// 32 stores of a part are four 128-byte runs).  Every K column is written,
+// zeros past the chunk; the inverse norms are checked against the items'
+// sums of squares.  Runs as the trailing blocks of the records launch.
+__device__ void prep_item_groups(const PrepArgs &a, int64_t g0, int64_t stride, int lane) {
+  const int Hp = a.Hp, Kc = Hp / 8, halfKc = Kc / 2;  // 16-byte K chunks in all, in one K half
+  const int r8 = lane & 7, kq = lane >> 3;
+  const int P = 4 * Hp;  // halves of one group sub-part (8 rows x Hp / 2)
   bool bad = false;
-  for (int64_t g = (int64_t)blockIdx.x * (kPrepThreads / 32) + warp; g < a.n_groups;
-       g += (int64_t)gridDim.x * (kPrepThreads / 32)) {
-    const int64_t r = g * 8 + rr;
+  for (int64_t g = g0; g < a.n_groups; g += stride) {
+    const int64_t r = g * 8 + r8;
     const bool in = r < a.n_rows;
     const float iv = in ? __ldg(a.inv + r) : 0.f;
-    if (in && (lane & 3) == 0) bad |= !(__ldg(a.sq + r) * iv * iv <= kMaxSquareSum);
-    float4 v[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (in && h0 + 4 * q < Hp) v[q] = __ldg(reinterpret_cast<const float4 *>(a.slab + r * kHotMax + h0) + q);
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int h = h0 + 4 * q;
-      if (h >= Hp) continue;
-      const float x[4] = {v[q].x * iv, v[q].y * iv, v[q].z * iv, v[q].w * iv};
+    if (in && kq == 0) bad |= !(__ldg(a.sq + r) * iv * iv <= kMaxSquareSum);
+    const int64_t t = g / a.gpt, gl = g % a.gpt;
+    uint16_t *tile = a.op + t * 4 * a.gpt * P + gl * P;
+    for (int kc = kq; kc < Kc; kc += 4) {
+      float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+      if (in) {
+        const float4 *src = reinterpret_cast<const float4 *>(a.slab + r * kHotMax + 8 * kc);
+        v0 = __ldg(src);
+        v1 = __ldg(src + 1);
+      }
+      const float x[8] = {v0.x * iv, v0.y * iv, v0.z * iv, v0.w * iv, v1.x * iv, v1.y * iv, v1.z * iv, v1.w * iv};
+      uint32_t hi[4], lo[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        bad |= !(fabsf(x[e]) <= kMaxNormalised);
-        put_split(gs, rr, h + e, Hp, x[e]);
+        bad |= !(fabsf(x[2 * e]) <= kMaxNormalised) || !(fabsf(x[2 * e + 1]) <= kMaxNormalised);
+        const __half h0 = __float2half_rn(x[2 * e]), h1 = __float2half_rn(x[2 * e + 1]);
+        const __half l0 = __float2half_rn(x[2 * e] - __half2float(h0));
+        const __half l1 = __float2half_rn(x[2 * e + 1] - __half2float(h1));
+        hi[e] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+        lo[e] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
       }
+      const int khalf = kc >= halfKc ? 1 : 0, kk = kc - khalf * halfKc;
+      const int off = kk * 64 + r8 * 8;  // the chunk inside its group sub-part
+      // sub-parts: 0 lo K0, 1 lo K1, 2 hi K0, 3 hi K1
+      *reinterpret_cast<uint4 *>(tile + (int64_t)(0 + khalf) * a.gpt * P + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<uint4 *>(tile + (int64_t)(2 + khalf) * a.gpt * P + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
     }
-    __syncwarp();
-    store_group_q(a.op, gs, g, a.gpt, Hp, lane);
-    __syncwarp();
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) flag(a.status, DEV_RANGE);
 }
@@ -797,6 +805,8 @@ struct RecArgs {
   int2 *rec;               // [quarter][column block][bucket_cap]
   int32_t *rec_n;          // [quarter][column block]
   int32_t *status;
+  int64_t n_quarters;      // records blocks; the blocks past them write the item operand
+  PrepArgs prep;           // the chunk's item operand
 };
 
 // Calls f(item, product) for every cold product of query row r with the
@@ -877,6 +887,12 @@ __device__ __forceinline__ void walk_row(const RecArgs &a, int64_t r, int lane, 
 // block, at a slot taken from the block's own counter (the order inside a
 // bucket does not matter: the epilogue sums integers).
 __global__ void __launch_bounds__(kRThreads) k_tc_records(const RecArgs a) {
+  if ((int64_t)blockIdx.x >= a.n_quarters) {  // a trailing block: the item operand, a warp per group
+    const int64_t warps = (int64_t)(gridDim.x - a.n_quarters) * (kRThreads / 32);
+    prep_item_groups(a.prep, (int64_t)(blockIdx.x - a.n_quarters) * (kRThreads / 32) + (threadIdx.x >> 5), warps,
+                     threadIdx.x & 31);
+    return;
+  }
   extern __shared__ int rcnt[];  // [n_cb]
   __shared__ int4 slots_all[kRThreads / 32][32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1583,10 +1599,11 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
   }
   const int64_t n_cid = h->tc_n_cid;
 
-  // Item operand of this chunk.
+  // Item operand of this chunk (written by the records launch's trailing
+  // blocks).
   if ((e = grow(&h->tc_B, &h->tc_B_cap, n_tiles * kN * 2 * Hp, s)) != cudaSuccess) return e;
+  PrepArgs pa;
   {
-    PrepArgs pa;
     pa.indptr = nullptr;
     pa.idx = nullptr;
     pa.val = nullptr;
@@ -1603,10 +1620,6 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     pa.qcold_n = nullptr;
     pa.dim = dim;
     pa.status = h->d_status;
-    const int64_t blocks = std::min<int64_t>((pa.n_groups + 7) / 8, (int64_t)sms * 8);
-    k_tc_prep_items<<<(unsigned)blocks, kPrepThreads, 0, s>>>(pa);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    ++nq;
   }
 
   // The lists over the queries' cold dimensions, for every chunk of the
@@ -1673,9 +1686,14 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     ra.rec = h->tc_rec;
     ra.rec_n = h->tc_rec_n;
     ra.status = h->d_status;
+    ra.n_quarters = n_quarters;
+    ra.prep = pa;
+    // The operand's blocks (a warp per group of 8 items) come after the
+    // records blocks, in the launch's last wave, where most SMs are idle.
+    const int64_t prep_blocks = (pa.n_groups + kRThreads / 32 - 1) / (kRThreads / 32);
     const size_t smem = sizeof(int) * (size_t)n_cb;
     if ((e = ensure_dyn_smem(k_tc_records, smem)) != cudaSuccess) return e;
-    k_tc_records<<<(unsigned)n_quarters, kRThreads, smem, s>>>(ra);
+    k_tc_records<<<(unsigned)(n_quarters + prep_blocks), kRThreads, smem, s>>>(ra);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ++nq;
   }
