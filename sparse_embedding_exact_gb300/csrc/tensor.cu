@@ -805,8 +805,9 @@ struct RecArgs {
   int2 *rec;               // [quarter][column block][bucket_cap]
   int32_t *rec_n;          // [quarter][column block]
   int32_t *status;
-  int64_t n_quarters;      // records blocks; the blocks past them write the item operand
-  PrepArgs prep;           // the chunk's item operand
+  int64_t n_main;          // quarters with a block of their own (whole waves of blocks)
+  int64_t n_shared;        // blocks sharing the rows of the quarters after those
+  PrepArgs prep;           // the chunk's item operand (the blocks after all of these)
 };
 
 // Calls f(item, product) for every cold product of query row r with the
@@ -815,7 +816,8 @@ struct RecArgs {
 // 32, finding its list from the bits that mark where lists start inside
 // the window (a lane's list is the last one that starts at or before it).
 template <typename F>
-__device__ __forceinline__ void walk_row(const RecArgs &a, int64_t r, int lane, int4 *slots, F f) {
+__device__ __forceinline__ void walk_row(const RecArgs &a, int64_t r, int lane, int4 *slots, F f, int piece = 0,
+                                         int pieces = 1) {
   const int64_t qb = a.q_indptr[r];
   const int cn = a.qcold_n[r];
   const unsigned lt = (1u << lane) - 1u, lt_eq = (2u << lane) - 1u;
@@ -846,13 +848,15 @@ __device__ __forceinline__ void walk_row(const RecArgs &a, int64_t r, int lane, 
     const int incl = warp_incl_scan(len, lane);
     const int excl = incl - len;
     const int L = __shfl_sync(0xffffffffu, incl, 31);
-    for (int f0 = 0; f0 < L; f0 += 32 * kWalkUnroll) {
+    // Windows of 32 entries piece, piece + pieces, ... (all of them when
+    // the walk is not shared), kWalkUnroll at a time.
+    for (int base = piece; 32 * base < L; base += pieces * kWalkUnroll) {
       int pos[kWalkUnroll];
       float pq[kWalkUnroll];
       bool ok[kWalkUnroll];
 #pragma unroll
       for (int u = 0; u < kWalkUnroll; ++u) {
-        const int w0 = f0 + 32 * u, fi = w0 + lane;
+        const int w0 = 32 * (base + pieces * u), fi = w0 + lane;
         const unsigned before = __ballot_sync(0xffffffffu, incl <= w0);  // lists ending at or before w0
         const bool starts = len > 0 && excl >= w0 && excl < w0 + 32;
         const unsigned m = __reduce_or_sync(0xffffffffu, starts ? (1u << ((excl - w0) & 31)) : 0u);
@@ -882,23 +886,56 @@ __device__ __forceinline__ void walk_row(const RecArgs &a, int64_t r, int lane, 
   }
 }
 
-// One block per 32 query rows (one warp per row): every cold product of
-// the rows with the chunk becomes a record in the bucket of its column
-// block, at a slot taken from the block's own counter (the order inside a
-// bucket does not matter: the epilogue sums integers).
+// Every cold product of a query row with the chunk becomes a record in the
+// bucket of its (32 rows, 32 items), at a slot taken from the bucket's
+// counter (the order inside a bucket does not matter: the epilogue sums
+// integers).  The quarters that fill whole waves of blocks get a block each
+// (one warp per row, counters in shared memory); the rows of the quarters
+// left over, which would run as a short last wave of whole blocks, are
+// shared by all warps of one more wave of blocks (several warps per row,
+// counters in global memory).  Blocks after those write the item operand.
 __global__ void __launch_bounds__(kRThreads) k_tc_records(const RecArgs a) {
-  if ((int64_t)blockIdx.x >= a.n_quarters) {  // a trailing block: the item operand, a warp per group
-    const int64_t warps = (int64_t)(gridDim.x - a.n_quarters) * (kRThreads / 32);
-    prep_item_groups(a.prep, (int64_t)(blockIdx.x - a.n_quarters) * (kRThreads / 32) + (threadIdx.x >> 5), warps,
-                     threadIdx.x & 31);
+  const int64_t bid = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ncb = a.n_cb, cap = a.bucket_cap;
+  if (bid >= a.n_main + a.n_shared) {  // a trailing block: the item operand, a warp per group
+    const int64_t warps = (int64_t)(gridDim.x - a.n_main - a.n_shared) * (kRThreads / 32);
+    prep_item_groups(a.prep, (bid - a.n_main - a.n_shared) * (kRThreads / 32) + warp, warps, lane);
+    return;
+  }
+  __shared__ int4 slots_all[kRThreads / 32][32];
+  int4 *slots = slots_all[warp];
+  if (bid >= a.n_main) {
+    // The rows of the quarters past the main ones, shared by every warp of
+    // these blocks: row e gets `pieces` warps, warp k of them walking the
+    // windows k, k + pieces, ... of its lists.  Their buckets are counted
+    // in global memory (zeroed before the launch): a count above the
+    // bucket's room marks it as not fitting.
+    const int64_t row0 = a.n_main * 32, rows = a.n_q - row0;
+    const int64_t warps = a.n_shared * (kRThreads / 32);
+    const int64_t w = (bid - a.n_main) * (kRThreads / 32) + warp;
+    const int64_t per_row = warps / (rows > 0 ? rows : 1);
+    const int pieces = (int)(per_row > 1 ? per_row : 1);
+    if (w >= rows * pieces) return;
+    const int64_t r = row0 + w % rows;
+    const int piece = (int)(w / rows);
+    const int64_t Q = r / 32;
+    const int rl = (int)(r - Q * 32);
+    int2 *rq = a.rec + Q * ncb * (int64_t)cap;
+    int32_t *cnt = a.rec_n + Q * ncb;
+    walk_row(
+        a, r, lane, slots,
+        [&](int item, int p) {
+          const int cb = item >> 5;
+          const int slot = atomicAdd(cnt + cb, 1);
+          if (slot < cap) rq[(int64_t)cb * cap + slot] = make_int2(stg_index(rl, item & 31), p);
+        },
+        piece, pieces);
     return;
   }
   extern __shared__ int rcnt[];  // [n_cb]
-  __shared__ int4 slots_all[kRThreads / 32][32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int4 *slots = slots_all[warp];
-  const int64_t Q = blockIdx.x;
-  const int ncb = a.n_cb, cap = a.bucket_cap;
+  const int tid = threadIdx.x;
+  const int64_t Q = bid;
   for (int c = tid; c < ncb; c += kRThreads) rcnt[c] = 0;
   __syncthreads();
   int2 *rq = a.rec + Q * ncb * (int64_t)cap;
@@ -1149,7 +1186,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     auto load_cnt = [&](int g, int t) -> int {
       const int Q = g * 4 + qd;
       const int cb = t * 8 + lane;
-      return (Q < n_quarters && lane < 8 && cb < n_cb) ? ld_keep_int(a.rec_n + (int64_t)Q * n_cb + cb) : 0;
+      const int v = (Q < n_quarters && lane < 8 && cb < n_cb) ? ld_keep_int(a.rec_n + (int64_t)Q * n_cb + cb) : 0;
+      return v > cap ? -1 : v;  // a shared count above the room: the bucket did not fit
     };
     // The bucket of the unit's column block 0 (block c's follows at c * cap).
     auto bucket0 = [&](int g, int t) -> const int2 * {
@@ -1686,14 +1724,26 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     ra.rec = h->tc_rec;
     ra.rec_n = h->tc_rec_n;
     ra.status = h->d_status;
-    ra.n_quarters = n_quarters;
     ra.prep = pa;
-    // The operand's blocks (a warp per group of 8 items) come after the
-    // records blocks, in the launch's last wave, where most SMs are idle.
-    const int64_t prep_blocks = (pa.n_groups + kRThreads / 32 - 1) / (kRThreads / 32);
     const size_t smem = sizeof(int) * (size_t)n_cb;
     if ((e = ensure_dyn_smem(k_tc_records, smem)) != cudaSuccess) return e;
-    k_tc_records<<<(unsigned)(n_quarters + prep_blocks), kRThreads, smem, s>>>(ra);
+    // Whole waves of quarter blocks, then one wave sharing the rest.
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_tc_records, kRThreads, smem) != cudaSuccess ||
+        per_sm < 1) {
+      cudaGetLastError();
+      per_sm = 1;
+    }
+    const int64_t wave = (int64_t)sms * per_sm;
+    ra.n_main = n_quarters / wave * wave;
+    ra.n_shared = ra.n_main < n_quarters ? wave : 0;
+    if (ra.n_shared > 0 &&
+        (e = cudaMemsetAsync(h->tc_rec_n + ra.n_main * n_cb, 0,
+                             sizeof(int32_t) * (size_t)((n_quarters - ra.n_main) * n_cb), s)) != cudaSuccess)
+      return e;
+    // The operand's blocks (a warp per group of 8 items) come last.
+    const int64_t prep_blocks = (pa.n_groups + kRThreads / 32 - 1) / (kRThreads / 32);
+    k_tc_records<<<(unsigned)(ra.n_main + ra.n_shared + prep_blocks), kRThreads, smem, s>>>(ra);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ++nq;
   }
