@@ -75,13 +75,16 @@ constexpr float kFixInv = 1.0f / 268435456.0f;
 constexpr float kMaxNormalised = 1.0f + 1.0f / 1024.0f;  // |x| of a normalised value
 constexpr float kMaxSquareSum = 1.0f + 1.0f / 64.0f;     // sum of x^2 of a normalised row
 constexpr int kStgInts = 32 * 32;              // one staging tile: 32 rows x 32 ints, 128-byte swizzle
-constexpr int kBBufs = 3;                      // scorer: item sub-part buffers
+constexpr int kBBufs = 2;                      // scorer: item sub-part buffers
 constexpr int kEpiWarps = 16;                  // four per quarter of the accumulator lanes
 constexpr int kWarpsPerQ = kEpiWarps / 4;      // epilogue warps per quarter
 constexpr int kMine = 8 / kWarpsPerQ;          // 32-column blocks per warp and tile pair
 constexpr int kSThreads = 64 + 32 * kEpiWarps; // producer, MMA, epilogue warps
 constexpr int kStgTiles = kEpiWarps <= 8 ? 2 : 1;  // staging tiles per epilogue warp
 constexpr int kStgBytes = kEpiWarps * kStgTiles * kStgInts * 4 + 1024;  // 1024-byte aligned
+constexpr int kTailRecs = 128;                 // epilogue: a block's records past the register set staged in
+                                               // shared memory (two slots per warp)
+constexpr int kTailBytes = kEpiWarps * 2 * kTailRecs * 8;
 static_assert(kEpiWarps % 4 == 0 && 8 % kWarpsPerQ == 0, "whole blocks per epilogue warp");
 constexpr int kRThreads = 1024;         // records: one warp per query row of a 32-row block
 constexpr int kPrepThreads = 256;
@@ -223,8 +226,14 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
-// Brings the 128-byte line holding p into this SM's L1 (no register).
-__device__ __forceinline__ void prefetch_l1(const void *p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
+// Asynchronous 8-byte copy global -> shared memory by this thread (grouped
+// by cp_async_commit, waited for by cp_async_wait1).
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Until all but the most recent of this thread's copy groups have landed.
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Until all of this thread's bulk store groups have read their
 // shared-memory source.
@@ -983,8 +992,8 @@ struct ScoreArgs {
 
 // Bytes of the scorer's dynamic shared memory for Hp hot columns: the query
 // tile (hi, lo: 512 Hp), kBBufs buffers of one item sub-part (256 Hp each),
-// the epilogue staging.
-size_t score_smem_bytes(int Hp) { return (size_t)(512 + 256 * kBBufs) * Hp + kStgBytes; }
+// the staging tiles of the epilogue, its staged records (kTailBytes).
+size_t score_smem_bytes(int Hp) { return (size_t)(512 + 256 * kBBufs) * Hp + kStgBytes + kTailBytes; }
 
 // Ties registers just loaded from tensor memory to the wait that completes
 // the load, so that no use of them is scheduled before it.
@@ -1166,6 +1175,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int qd = warp & 3;
     const int sub = (warp - 2) >> 2;
     int *stg_mine = stg_all + (warp - 2) * kStgTiles * kStgInts;  // this warp's staging tiles (swizzled)
+    // This warp's two slots of staged records (a block's records
+    // 32 kRecPerLane .. + kTailRecs - 1), slot i % 2 for its block i of a unit.
+    int2 *tail_mine = reinterpret_cast<int2 *>(stg_all + kEpiWarps * kStgTiles * kStgInts) +
+                      (warp - 2) * 2 * kTailRecs;
     int n_blocks = 0;                                              // blocks done (tile n_blocks % kStgTiles next)
     const bool vec = a.vec_ok != 0;
     const bool tma = a.use_tma != 0;
@@ -1194,9 +1207,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
       const int Q = g * 4 + qd;
       return a.rec + ((int64_t)Q * n_cb + t * 8) * cap;
     };
-    // Block c's first 32 kRecPerLane records into dst; the lines of the
-    // rest (if any) into L1, for the loop that adds them.
-    auto fetch = [&](int counts, const int2 *bucket, int c, int2(&dst)[kRecPerLane]) {
+    // Block c's first 32 kRecPerLane records into dst; the next kTailRecs
+    // into shared-memory slot `slot` by asynchronous copies (each lane
+    // copies the records it will add), one copy group per call.
+    auto fetch = [&](int counts, const int2 *bucket, int c, int2(&dst)[kRecPerLane], int slot) {
       const int n = __shfl_sync(0xffffffffu, counts, c);
       const int2 *bc = bucket + (int64_t)c * cap;
 #pragma unroll
@@ -1205,8 +1219,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
         dst[m] = make_int2(0, 0);  // no record
         if (p < n) dst[m] = ld_keep_int2(bc + p);
       }
-      const int p = 32 * kRecPerLane + 16 * lane;  // 16 records (one line) per lane
-      if (p < n) prefetch_l1(bc + p);
+      const uint32_t ts = smem_u32(tail_mine + slot * kTailRecs);
+#pragma unroll
+      for (int m = 0; m < kTailRecs / 32; ++m) {
+        const int q = 32 * m + lane;
+        if (32 * kRecPerLane + q < n) cp_async8(ts + 8u * (uint32_t)q, bc + 32 * kRecPerLane + q);
+      }
+      cp_async_commit();
     };
     // The warp's blocks in order: block kMine j + i is column block
     // sub + kWarpsPerQ i of unit j.  Its records sit in register set i % 2;
@@ -1223,8 +1242,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     int cnt = nv > 0 ? load_cnt(g, t) : 0, cnt_n = nv > 1 ? load_cnt(g1, t1) : 0, cnt_nn = 0;
     int2 R[2][kRecPerLane];
     if (nv > 0) {
-      fetch(cnt, bucket0(g, t), sub, R[0]);
-      fetch(cnt, bucket0(g, t), sub + kWarpsPerQ, R[1]);
+      fetch(cnt, bucket0(g, t), sub, R[0], 0);
+      fetch(cnt, bucket0(g, t), sub + kWarpsPerQ, R[1], 1);
     }
     for (int j = 0; j < nv; ++j) {
       const int b = j & 1;
@@ -1250,8 +1269,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const int n = __shfl_sync(0xffffffffu, cnt, c);
         // The records of the block two later, into the set just used.
         auto prefetch = [&]() {
-          if (i + 2 < kMine) fetch(cnt, bucket0(g, t), c + 2 * kWarpsPerQ, Rc);
-          else if (j + 1 < nv) fetch(cnt_n, bucket0(g1, t1), sub + kWarpsPerQ * (i + 2 - kMine), Rc);
+          if (i + 2 < kMine) fetch(cnt, bucket0(g, t), c + 2 * kWarpsPerQ, Rc, i & 1);
+          else if (j + 1 < nv) fetch(cnt_n, bucket0(g1, t1), sub + kWarpsPerQ * (i + 2 - kMine), Rc, i & 1);
+          else cp_async_commit();  // an empty group keeps one group per block
         };
         if (tma) {  // the bulk store that last read this staging tile is done reading it
           if (lane == 0) {
@@ -1270,12 +1290,22 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
           for (int m = 0; m < kRecPerLane; ++m)
             if (Rc[m].y != 0) atomicAdd(stg + Rc[m].x, Rc[m].y);
-          prefetch();
-          const int2 *bc = bucket0(g, t) + (int64_t)c * cap;
-          for (int p = 32 * kRecPerLane + lane; p < n; p += 32) {  // past the first 32 kRecPerLane (rare)
-            const int2 rr = ld_keep_int2(bc + p);
-            atomicAdd(stg + rr.x, rr.y);
+          if (n > 32 * kRecPerLane) {
+            // The staged records (this block's group is complete once at
+            // most the next block's group is pending), then any past them.
+            cp_async_wait1();
+            const int2 *ts = tail_mine + (i & 1) * kTailRecs;
+            for (int q = lane; q < kTailRecs && 32 * kRecPerLane + q < n; q += 32) {
+              const int2 rr = ts[q];
+              atomicAdd(stg + rr.x, rr.y);
+            }
+            const int2 *bc = bucket0(g, t) + (int64_t)c * cap;
+            for (int p = 32 * kRecPerLane + kTailRecs + lane; p < n; p += 32) {  // rare
+              const int2 rr = ld_keep_int2(bc + p);
+              atomicAdd(stg + rr.x, rr.y);
+            }
           }
+          prefetch();
           if (n < 0) {
             // The bucket did not fit: each lane walks its row's cold lists
             // and keeps the items of this block (rare; exact, the same sums).
@@ -1375,7 +1405,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
       if (lane == 0) mbar_arrive(b ? acc_free1 : acc_free0);
     }
     // The bulk stores this warp issued complete before the block exits
-    // (also after a wait above gave up: a bulk store completes by itself).
+    // (also after a wait above gave up: a bulk store completes by itself),
+    // and so do its staged-record copies.
+    asm volatile("cp.async.wait_all;" ::: "memory");
     if (tma && lane == 0) bulk_wait_all();
     __syncwarp();
   }
