@@ -37,7 +37,7 @@
 // Scorer (k_tc_score): persistent, one block per SM, 18 warps.  Warp 0
 // loads operand tiles with bulk asynchronous copies (a query tile's operand
 // stays while the block works through its item tiles, whose four K-half
-// sub-parts stream through three buffers); warp 1 allocates
+// sub-parts stream through two buffers); warp 1 allocates
 // tensor memory and one of its threads issues the MMAs into one of two
 // accumulators; warps 2-17 run the epilogue, four per quarter of the 128
 // accumulator lanes (each takes two of the eight 32-column blocks), on one
