@@ -78,7 +78,7 @@ typedef int32_t ss_status;
  * SS_ERR_INVALID_ARG. */
 #define SS_ALGO_POSTING_LISTS 0x2
 #define SS_ALGO_TILES 0x8
-/* Tensor-core path: the (at most 128) dimensions held by the largest share of
+/* Tensor-core path: the (at most 160) dimensions held by the largest share of
  * a row sample of the item matrix are multiplied on the tensor cores as a
  * dense product of the normalised values, each split into two fp16 parts
  * (hi = fp16(x), lo = fp16(x - hi)) so that hi*hi + hi*lo + lo*hi carries
@@ -448,7 +448,7 @@ ss_status ss_index_stats(ss_handle *h, const ss_index *idx, int64_t *stats, void
  * is still written), SS_ERR_DEVICE_CHECK (list offsets outside the index),
  * SS_ERR_CUDA.
  */
-#define SS_EXPORT_HOT_MAX 128
+#define SS_EXPORT_HOT_MAX 160
 ss_status ss_index_export(ss_handle *h, const ss_index *idx, int32_t *n_hot, int32_t *hot,
                           float *hot_values, int32_t *col_ptr, int32_t *item, float *value,
                           int64_t capacity, int64_t *n_entries, void *stream);

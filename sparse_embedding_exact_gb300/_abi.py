@@ -29,7 +29,7 @@ SS_MAX_CHUNK_ROWS = 65536
 SS_VALUES_F32 = 0
 SS_VALUES_BF16 = 1
 SS_VALUES_F16 = 2
-SS_EXPORT_HOT_MAX = 128
+SS_EXPORT_HOT_MAX = 160
 SS_DEVICE_OK = 0
 SS_DEVICE_UNSORTED = 1
 SS_DEVICE_OUT_OF_RANGE = 2

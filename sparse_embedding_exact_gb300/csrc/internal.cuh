@@ -121,7 +121,7 @@ struct ss_index {
 
 // Tensor-core path (see tensor.cu).
 namespace tcp {
-constexpr int kHotMax = 128;   // hot dimensions multiplied on the tensor cores
+constexpr int kHotMax = 160;   // hot dimensions multiplied on the tensor cores
 constexpr int kM = 128;        // query rows per tile (MMA M)
 constexpr int kN = 256;        // items per tile (MMA N)
 constexpr int kColBlock = 32;  // items per cold-record bucket

@@ -9,8 +9,8 @@
 // is the same cosine and keeps every operand in [-1, 1]).
 //
 // In BM25/TF-IDF data the head of the dictionary (section 3.2) is held by a
-// large share of the rows: on a Zipf(1.1) law over 1.2M words, the 128 most
-// frequent dimensions carry 98% of the expected 6.8 shared dimensions of a
+// large share of the rows: on a Zipf(1.1) law over 1.2M words, the 160 most
+// frequent dimensions carry 98.7% of the expected 6.8 shared dimensions of a
 // pair.  Those dimensions are multiplied as a dense [128 queries x 256 items
 // x H] product per tile pair.  The tensor cores take 16-bit operands, so
 // each normalised value x (|x| <= 1) is split as x = hi + lo with hi =
@@ -65,7 +65,10 @@ namespace {
 using namespace tcp;
 
 constexpr int kHotSlotsBits = 9;
-constexpr int kHotSlots = 1 << kHotSlotsBits;  // <= 128 keys: load <= 1/4
+constexpr int kHotSlots = 1 << kHotSlotsBits;  // <= kHotMax keys: load <= 0.31
+static_assert(kHotMax <= kHotSlots / 3, "the hot table stays sparse");
+constexpr int kSelSort = 256;                  // the chosen dims, sorted (a power of two >= kHotMax)
+static_assert(kSelSort >= kHotMax && (kSelSort & (kSelSort - 1)) == 0, "bitonic sort size");
 constexpr int kSelSlotsBits = 16;
 constexpr int kSelSlots = 1 << kSelSlotsBits;  // selection table (global memory)
 constexpr int64_t kSampleEntries = 32768;      // nonzeros sampled to choose the hot set
@@ -393,12 +396,12 @@ __global__ void __launch_bounds__(kSelThreads)
   const int32_t *keys = tab, *cnts = tab + kSelSlots;
   __shared__ int hist[kCountBins];
   __shared__ unsigned long long ties[kTieCap];
-  __shared__ unsigned long long sel[2 * kHotMax];
+  __shared__ unsigned long long sel[kSelSort];
   __shared__ int n_above, n_ties, thr_sh, take_ties;
   __shared__ unsigned long long pairs_all, pairs_hot;
   const int tid = threadIdx.x;
   for (int j = tid; j < kCountBins; j += kSelThreads) hist[j] = 0;
-  for (int j = tid; j < 2 * kHotMax; j += kSelThreads) sel[j] = ~0ull;
+  for (int j = tid; j < kSelSort; j += kSelThreads) sel[j] = ~0ull;
   for (int j = tid; j < kTieCap; j += kSelThreads) ties[j] = ~0ull;
   if (tid == 0) {
     n_above = n_ties = 0;
@@ -465,7 +468,7 @@ __global__ void __launch_bounds__(kSelThreads)
   const int need = min(kHotMax - above, n_ties);
   for (int j = tid; j < need; j += kSelThreads) sel[above + j] = ties[j];
   __syncthreads();
-  block_sort(sel, 2 * kHotMax);
+  block_sort(sel, kSelSort);
   const int H = above + max(need, 0);
   unsigned long long hp = 0;
   for (int j = tid; j < H; j += kSelThreads) {
@@ -510,8 +513,8 @@ __global__ void __launch_bounds__(256)
     const int64_t c = (r - row_begin) / chunk_rows;
     const int64_t item = r - row_begin - c * chunk_rows;
     float *srow = slab + (c * chunk_rows + item) * kHotMax;  // this item's hot values, zero if absent
-    static_assert(kHotMax == 128, "one float4 per lane clears an item's hot values");
-    *reinterpret_cast<float4 *>(srow + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
+    static_assert(kHotMax % 4 == 0, "an item's hot values are cleared as float4s");
+    for (int h = 4 * lane; h < kHotMax; h += 128) *reinterpret_cast<float4 *>(srow + h) = make_float4(0.f, 0.f, 0.f, 0.f);
     __syncwarp();
     float ss = 0.f;
     int nc = 0;
@@ -987,13 +990,20 @@ struct ScoreArgs {
   int64_t n_units;         // query tiles x item tiles
   int32_t Hp;
   int32_t vec_ok;          // 16-byte aligned output rows: vector stores
+  int32_t use_tail;        // records past the register set staged in shared memory
   int32_t *status;
 };
 
 // Bytes of the scorer's dynamic shared memory for Hp hot columns: the query
 // tile (hi, lo: 512 Hp), kBBufs buffers of one item sub-part (256 Hp each),
-// the staging tiles of the epilogue, its staged records (kTailBytes).
-size_t score_smem_bytes(int Hp) { return (size_t)(512 + 256 * kBBufs) * Hp + kStgBytes + kTailBytes; }
+// the staging tiles of the epilogue, its staged records (kTailBytes, when
+// they fit: at Hp = 128, not at Hp = 160).
+size_t score_smem_bytes(int Hp, bool tail) {
+  return (size_t)(512 + 256 * kBBufs) * Hp + kStgBytes + (tail ? kTailBytes : 0);
+}
+constexpr size_t kMaxDynSmem = 232448;  // shared memory a block may take
+// Whether the staged records fit beside the operands at Hp hot columns.
+bool score_tail_fits(int Hp) { return score_smem_bytes(Hp, true) <= kMaxDynSmem; }
 
 // Ties registers just loaded from tensor memory to the wait that completes
 // the load, so that no use of them is scheduled before it.
@@ -1182,6 +1192,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     int n_blocks = 0;                                              // blocks done (tile n_blocks % kStgTiles next)
     const bool vec = a.vec_ok != 0;
     const bool tma = a.use_tma != 0;
+    const bool tail_on = a.use_tail != 0;
     const uint64_t out_policy = evict_first_policy();
     const int sw = lane & 7;
     const int cap = a.bucket_cap;
@@ -1219,11 +1230,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
         dst[m] = make_int2(0, 0);  // no record
         if (p < n) dst[m] = ld_keep_int2(bc + p);
       }
-      const uint32_t ts = smem_u32(tail_mine + slot * kTailRecs);
+      if (tail_on) {
+        const uint32_t ts = smem_u32(tail_mine + slot * kTailRecs);
 #pragma unroll
-      for (int m = 0; m < kTailRecs / 32; ++m) {
-        const int q = 32 * m + lane;
-        if (32 * kRecPerLane + q < n) cp_async8(ts + 8u * (uint32_t)q, bc + 32 * kRecPerLane + q);
+        for (int m = 0; m < kTailRecs / 32; ++m) {
+          const int q = 32 * m + lane;
+          if (32 * kRecPerLane + q < n) cp_async8(ts + 8u * (uint32_t)q, bc + 32 * kRecPerLane + q);
+        }
       }
       cp_async_commit();
     };
@@ -1293,14 +1306,18 @@ __global__ void __launch_bounds__(kSThreads, 1)
           if (n > 32 * kRecPerLane) {
             // The staged records (this block's group is complete once at
             // most the next block's group is pending), then any past them.
-            cp_async_wait1();
-            const int2 *ts = tail_mine + (i & 1) * kTailRecs;
-            for (int q = lane; q < kTailRecs && 32 * kRecPerLane + q < n; q += 32) {
-              const int2 rr = ts[q];
-              atomicAdd(stg + rr.x, rr.y);
+            int p0 = 32 * kRecPerLane;
+            if (tail_on) {
+              cp_async_wait1();
+              const int2 *ts = tail_mine + (i & 1) * kTailRecs;
+              for (int q = lane; q < kTailRecs && 32 * kRecPerLane + q < n; q += 32) {
+                const int2 rr = ts[q];
+                atomicAdd(stg + rr.x, rr.y);
+              }
+              p0 += kTailRecs;
             }
             const int2 *bc = bucket0(g, t) + (int64_t)c * cap;
-            for (int p = 32 * kRecPerLane + kTailRecs + lane; p < n; p += 32) {  // rare
+            for (int p = p0 + lane; p < n; p += 32) {  // rare
               const int2 rr = ld_keep_int2(bc + p);
               atomicAdd(stg + rr.x, rr.y);
             }
@@ -1789,7 +1806,9 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     ld_dst = n_items;
   }
   {
-    if ((e = ensure_dyn_smem(k_tc_score, score_smem_bytes(kHotMax))) != cudaSuccess) return e;
+    if ((e = ensure_dyn_smem(k_tc_score, std::max(score_smem_bytes(kHotMax, false), score_smem_bytes(128, true)))) !=
+        cudaSuccess)
+      return e;
     ScoreArgs sa;
     sa.A = h->tc_A;
     sa.B = h->tc_B;
@@ -1814,11 +1833,12 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     sa.Hp = Hp;
     sa.vec_ok = ((reinterpret_cast<uintptr_t>(dst) % 16) == 0) && (ld_dst % 4 == 0);
     sa.use_tma = sa.vec_ok && encode_out_map(&sa.out_map, dst, n_q, n_items, ld_dst) ? 1 : 0;
+    sa.use_tail = score_tail_fits(Hp) ? 1 : 0;
     sa.status = h->d_status;
     if (sa.n_units > INT32_MAX || n_q > INT32_MAX - 256) return cudaErrorInvalidValue;  // 32-bit unit and row numbers
     const int64_t grid = std::min<int64_t>(sms, sa.n_units);
     prof_mark(h, s);
-    k_tc_score<<<(unsigned)grid, kSThreads, score_smem_bytes(Hp), s>>>(sa);
+    k_tc_score<<<(unsigned)grid, kSThreads, score_smem_bytes(Hp, sa.use_tail != 0), s>>>(sa);
     prof_mark(h, s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ++nq;

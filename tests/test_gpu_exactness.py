@@ -50,11 +50,14 @@ def _scipy(batch, begin=0, end=None):
                          shape=(end - begin, batch.dim))
 
 
-def tensor_hot_set(I):
+TENSOR_HOT_MAX = 160  # the tensor path's largest hot set (the header's SS_EXPORT_HOT_MAX)
+
+
+def tensor_hot_set(I, k=TENSOR_HOT_MAX):
     """The tensor path's hot set, by its stated rule, on the host: the rows
     j * n / n_s (j < n_s, n_s = 32768 * n / nnz clamped to [16, n]) are
     sampled; a dimension qualifies when at least max(2, ceil(0.2% of n_s))
-    sampled rows hold it; the 128 with the most sampled rows are taken
+    sampled rows hold it; the k (160) with the most sampled rows are taken
     (counts of 1,023 or more count as equal), ties to the lower dimension,
     and none of a tie larger than 4,096 dimensions."""
     n, nnz = I.n_rows, I.nnz
@@ -66,15 +69,15 @@ def tensor_hot_set(I):
     floor_c = min(1023, max(2, (n_s * 2 + 999) // 1000))
     cand = np.nonzero(counts >= floor_c)[0]
     cc = np.minimum(counts[cand], 1023)
-    if cand.size <= 128:
+    if cand.size <= k:
         return np.sort(cand)
     order = np.lexsort((cand, -cc))
-    t = cc[order[127]]
+    t = cc[order[k - 1]]
     above = cand[cc > t]
     ties = np.sort(cand[cc == t])
     if ties.size > 4096:
         return np.sort(above)
-    return np.sort(np.concatenate([above, ties[: 128 - above.size]]))
+    return np.sort(np.concatenate([above, ties[: k - above.size]]))
 
 
 # ------------------------------------------------------------------ index vs scipy
@@ -212,7 +215,7 @@ def test_split_with_subnormal_low_parts(sec):
     Q = csr_from_rows(_head_rows(rng, 48, qh, d), d)
     I = csr_from_rows(_head_rows(rng, 160, ih, d), d)
     got, st = _tensor_scores(sec, Q, I)
-    assert st["algorithm"] == 2 and st["hot_dims"] == 128
+    assert st["algorithm"] == 2 and st["hot_dims"] >= 128  # the head (and any extra dim sampled twice)
     err = float(np.abs(got.astype(np.float64) - oracle.cosine(Q, I, f64=True)).max())
     print(f"split fp16, subnormal low parts: max |error| {err:.3e}")
     assert err <= TOL
@@ -233,7 +236,7 @@ def test_split_with_cancelling_equal_magnitudes(sec):
     Q = csr_from_rows(_head_rows(rng, 64, qh, d, cold_per_row=1), d)
     I = csr_from_rows(_head_rows(rng, 192, ih, d, cold_per_row=1), d)
     got, st = _tensor_scores(sec, Q, I)
-    assert st["algorithm"] == 2 and st["hot_dims"] == 128
+    assert st["algorithm"] == 2 and st["hot_dims"] >= 128  # the head (and any extra dim sampled twice)
     err = float(np.abs(got.astype(np.float64) - oracle.cosine(Q, I, f64=True)).max())
     print(f"split fp16, cancelling equal magnitudes: max |error| {err:.3e}")
     assert err <= TOL
@@ -295,10 +298,10 @@ def test_full_matrix_of_the_1_2m_workload(sec):
 # ------------------------------------------------------------------ record overflow paths
 def test_tensor_records_beyond_every_buffer(sec):
     """Queries far denser in the items' cold dimensions than the item sample
-    suggests: a block's records exceed its shared-memory sort (it walks its
-    lists a second time and stores each record at its place), and the call's
-    records exceed the array sized from the sample (the scorer computes those
-    buckets from the lists itself).  Every entry still matches the oracle."""
+    suggests: buckets hold more records than the epilogue keeps in registers
+    and in shared memory (it reads the rest from the bucket), and more than
+    the buckets' room, sized from the sample (the scorer computes those
+    blocks from the lists itself).  Every entry still matches the oracle."""
     rng = np.random.default_rng(41)
     d = 50_000
     items = [(np.sort(rng.choice(d, 40, replace=False)), rng.lognormal(0, 1, 40)) for _ in range(8192)]

@@ -412,11 +412,11 @@ def test_two_gpu_algorithms_agree(sec, name):
 # ------------------------------------------------------------- posting lists
 def test_auto_choice_follows_tile_overflow(sec):
     """Without an algorithm flag the handle takes the tensor path when the
-    item matrix has a strong head (the Zipf(1.1) workloads: 128 hot
-    dimensions leave about 0.11 shared cold dimensions per pair), else
+    item matrix has a strong head (the Zipf(1.1) workloads: 160 hot
+    dimensions leave about 0.09 shared cold dimensions per pair), else
     probes the first batch: posting lists when most item tiles overflow (the
     uniform workload, 500 nonzeros a row; the heavy-tailed Zipf(1.3) one,
-    whose 128 hot dimensions still leave about 0.5 per pair).  Either way
+    whose 160 hot dimensions still leave about 0.4 per pair).  Either way
     the result is that of the chosen algorithm, bit for bit."""
     names = {0: "hybrid", 1: "posting", 2: "tensor"}
     for name, want in (("d500k_q50k_i500k_uniform", 1), ("d1.2m_q5k_i200k", 2), ("d65k_q1k_i10k", 2),
@@ -524,7 +524,7 @@ def test_tensor_path_spans_tiles_and_ragged_tails(sec, name, n_q, n_i, chunk):
         S = h.score_all(q, inv_q, i, inv_i)
         h.check_device()
         got = S.cpu().numpy()
-    assert st["algorithm"] == 2 and 0 < st["hot_dims"] <= 128
+    assert st["algorithm"] == 2 and 0 < st["hot_dims"] <= 160
     assert _max_err(got, oracle.cosine(Q, I)) <= TOL
 
 
