@@ -315,31 +315,40 @@ def run_ours(args):
           for _ in chunks]
     span = CHUNK * h.build_batch  # chunks whose indexes one build launch covers
     batches = [(b, min(b + span, n_i)) for b in range(0, n_i, span)]
+    batch_chunks = [[c for c, (b, _) in enumerate(chunks) if bb <= b < be] for bb, be in batches]
     ev_build = [torch.cuda.Event(enable_timing=True) for _ in batches]
 
-    def step(record):
+    def step(sampled=None):
         # Every step redoes the whole path: the hot set and the prepared
         # queries are derived again, not reused from the previous step.
+        # Events (around the scoring calls, around the scoring kernel inside
+        # them, before the build) go into the build batch `sampled` only:
+        # each event costs GPU time, so timing every launch would slow the
+        # step it measures.
         h.invalidate()
         h.row_norms(q, out=inv_q)
         h.row_norms(it, out=inv_i)
         c = 0
         for bi, (bb, be) in enumerate(batches):
-            if record:
+            rec = bi == sampled
+            if rec:
                 ev_build[bi].record(stream)
             for b, e, idx in h.build_item_indexes(it, bb, be):
-                if record:
+                if rec:
                     ev[c][0].record(stream)
+                    h.profile_scorer(True)
                 if resident:
                     h.score_chunk(q, inv_q, idx, inv_i[b:], out[:, b:], n_i)
                 else:
                     h.score_chunk(q, inv_q, idx, inv_i[b:], bufs[c & 1], CHUNK)
-                if record:
+                if rec:
+                    h.profile_scorer(False)
                     ev[c][1].record(stream)
                 c += 1
+        return batch_chunks[sampled] if sampled is not None else []
 
     for _ in range(args.warmup):
-        step(False)
+        step()
     torch.cuda.synchronize()
     h.check_device()
     index_stats = h.index_stats(h.build_item_index(it, *chunks[0]))
@@ -353,25 +362,25 @@ def run_ours(args):
     sampler = ClockSampler(local)
     sampler.start()
     launches0 = h.kernel_launches()
-    h.profile_scorer(True)  # events around each scoring-kernel launch, on its stream
-    step_ms, score_ms, build_ms = [], [], []
+    h.scorer_time()  # forget pairs recorded before the timed region
+    step_ms, score_ms, build_ms, timed_chunks = [], [], [], []
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for _ in range(args.steps):
+    for k in range(args.steps):
         flush.fill_(1.0)  # evict L2 between timed steps
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
+        sb = k % len(batches)  # the batches take turns carrying the events
         t_start.record(stream)
-        step(True)
+        cs = step(sb)
         t_end.record(stream)
         torch.cuda.synchronize()
         step_ms.append(t_start.elapsed_time(t_end))
-        score_ms.extend(a.elapsed_time(b) for a, b in ev)
-        first = [i * h.build_batch for i in range(len(batches))]  # each batch's first chunk
-        build_ms.extend(ev_build[i].elapsed_time(ev[f][0]) for i, f in enumerate(first))
+        score_ms.extend(ev[c][0].elapsed_time(ev[c][1]) for c in cs)
+        timed_chunks.extend(cs)
+        build_ms.append(ev_build[sb].elapsed_time(ev[cs[0]][0]))
     launches = h.kernel_launches() - launches0
     kernel_ms_total, kernel_launches = h.scorer_time()
-    h.profile_scorer(False)
     clocks = sampler.stop()
     h.check_device()
 
@@ -388,7 +397,7 @@ def run_ours(args):
     # library's own events around each of its launches; the whole scoring
     # call (with its preparation kernels) is reported beside it.
     alg = chunk_algorithmic_bytes(Q, I)
-    per_launch_bytes = statistics.mean(alg)
+    per_launch_bytes = statistics.mean(alg[c] for c in timed_chunks)
     call_s = statistics.mean(score_ms) / 1e3
     per_launch_s = (kernel_ms_total / kernel_launches / 1e3) if kernel_launches else call_s
     achieved = per_launch_bytes / per_launch_s / 1e9
@@ -406,7 +415,9 @@ def run_ours(args):
             "bytes_per_launch": per_launch_bytes, "launch_ms": 1e3 * per_launch_s,
             "launches_timed": kernel_launches,
             "call_ms": 1e3 * call_s, "call_frac": per_launch_bytes / call_s / 1e9 / peak,
-            "score_share_of_step": sum(score_ms) / max(sum(step_ms), 1e-9),
+            "timing_sample": "events around one build batch of chunks per timed step (the batches "
+                             "in turn); the other batches run without events",
+            "score_share_of_step": statistics.mean(score_ms) * len(chunks) / max(statistics.mean(step_ms), 1e-9),
             "index_build_ms_per_launch": statistics.mean(build_ms),
             "index_build_chunks_per_launch": h.build_batch}
 

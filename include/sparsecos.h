@@ -556,8 +556,9 @@ int64_t ss_inject_alloc_failure(int64_t nth);
  * records a CUDA event just before and just after its scoring kernel, on
  * the caller's stream; the other kernels of the call (operand preparation,
  * cold records, query preparation) fall outside the pair.  Turning it on or
- * off forgets the pairs recorded so far.  No synchronisation.  Errors:
- * SS_ERR_INVALID_ARG (null handle). */
+ * off keeps the pairs recorded so far (so a caller can time a sample of its
+ * calls); ss_scorer_time reads and forgets them.  No synchronisation.
+ * Errors: SS_ERR_INVALID_ARG (null handle). */
 ss_status ss_profile_scorer(ss_handle *h, int32_t on);
 
 /* Sum of the recorded pairs' elapsed times in milliseconds and their count,

@@ -321,7 +321,7 @@ class SparseCosine:
 
     def scorer_time(self):
         """(total milliseconds, launches) of the scoring-kernel launches
-        recorded since profiling was turned on or last read; synchronises."""
+        recorded since the last read; synchronises."""
         ms = ctypes.c_double()
         n = ctypes.c_int64()
         self._check(self._lib.ss_scorer_time(self._h, ctypes.byref(ms), ctypes.byref(n)), "ss_scorer_time")

@@ -451,8 +451,7 @@ int64_t ss_inject_alloc_failure(int64_t nth) { return g_alloc_countdown.exchange
 
 ss_status ss_profile_scorer(ss_handle *h, int32_t on) {
   if (!h) return SS_ERR_INVALID_ARG;
-  h->prof_on = on != 0;
-  h->prof_used = 0;
+  h->prof_on = on != 0;  // the pairs recorded so far stay until ss_scorer_time reads them
   return SS_OK;
 }
 

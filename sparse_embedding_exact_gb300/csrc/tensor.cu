@@ -229,6 +229,8 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
+// Brings the 128-byte line holding p into this SM's L1 (no register).
+__device__ __forceinline__ void prefetch_l1(const void *p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
 // Asynchronous 8-byte copy global -> shared memory by this thread (grouped
 // by cp_async_commit, waited for by cp_async_wait1).
 __device__ __forceinline__ void cp_async8(uint32_t dst, const void *src) {
@@ -1237,6 +1239,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
           const int q = 32 * m + lane;
           if (32 * kRecPerLane + q < n) cp_async8(ts + 8u * (uint32_t)q, bc + 32 * kRecPerLane + q);
         }
+      } else {  // the lines of the rest into L1 instead (16 records a lane)
+        const int p = 32 * kRecPerLane + 16 * lane;
+        if (p < n) prefetch_l1(bc + p);
       }
       cp_async_commit();
     };
