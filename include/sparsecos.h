@@ -454,27 +454,26 @@ ss_status ss_index_export(ss_handle *h, const ss_index *idx, int32_t *n_hot, int
                           int64_t capacity, int64_t *n_entries, void *stream);
 
 /*
- * Reads back the lists that the tensor path's last scoring call used for
- * its chunk, into host memory; for tests and inspection; synchronises
- * `stream`.  The first call for a query matrix numbers the dimensions that
- * some query row holds outside the hot set (n_dims of them, ascending); the
- * first call after a build sorts the nonzeros of each of the build's
- * chunks in those dimensions by number; the other nonzeros make no cold
- * product and are left out:
- *   dims[0 .. n_dims - 1]: the numbered dimensions, ascending;
+ * Reads back the queries' lists that the tensor path's scoring calls walk,
+ * into host memory; for tests and inspection; synchronises `stream`.  The
+ * first call for a query matrix (with its inverse norms and the hot set)
+ * sorts the queries' nonzeros outside the hot set by dimension; every
+ * later call walks each item's nonzeros outside the hot set into the list
+ * of its dimension (the other item nonzeros make no cold product):
+ *   dims[0 .. n_dims - 1]: the dimensions some query row holds outside the
+ *     hot set, ascending;
  *   col_ptr[0 .. n_dims]: list k (dimension dims[k]) is entries
  *     [col_ptr[k], col_ptr[k + 1]);
- *   item[e]: the item's row within the chunk, ascending inside a list
- *     (sorted here; the device keeps no order, which no sum depends on);
- *   value[e]: the item's stored value (the inverse norms are applied by
- *     each scoring call).
+ *   query[e]: the query row, ascending inside a list (sorted here; the
+ *     device keeps no order, which no sum depends on);
+ *   value[e]: the query's value times its row's inverse norm (float32).
  * Any output may be NULL; dims and col_ptr need room for dim + 1 entries,
- * item and value capacity >= *n_entries.
+ * query and value capacity >= *n_entries.
  * Errors: SS_ERR_INVALID_ARG (no tensor-path scoring call made yet),
  * SS_ERR_LIMIT (capacity too small; *n_entries is still written),
  * SS_ERR_DEVICE_CHECK, SS_ERR_CUDA.
  */
-ss_status ss_lists_export(ss_handle *h, int64_t *n_dims, int32_t *dims, int32_t *col_ptr, int32_t *item,
+ss_status ss_lists_export(ss_handle *h, int64_t *n_dims, int32_t *dims, int32_t *col_ptr, int32_t *query,
                           float *value, int64_t capacity, int64_t *n_entries, void *stream);
 
 /* Size of the fixed scratch array behind ss_cosine_chunk_noalloc. */

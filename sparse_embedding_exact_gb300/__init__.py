@@ -366,23 +366,24 @@ class SparseCosine:
                 "item": item[: n.value], "value": value[: n.value]}
 
     def lists_export(self, stream=None) -> dict:
-        """The lists the tensor path's last scoring call used for its chunk,
-        as host arrays (synchronises): "dims" (the queries' cold dimensions,
-        ascending), "col_ptr" (len(dims) + 1), "item" (ascending inside each
-        list) and "value" (the items' stored values)."""
+        """The queries' lists the tensor path's scoring calls walk, as host
+        arrays (synchronises): "dims" (the dimensions some query holds
+        outside the hot set, ascending), "col_ptr" (len(dims) + 1), "query"
+        (ascending inside each list) and "value" (the query's value times
+        its row's inverse norm)."""
         lib = self._lib
         nd, n = ctypes.c_int64(0), ctypes.c_int64(0)
         self._check(lib.ss_lists_export(self._h, ctypes.byref(nd), None, None, None, None, 0, ctypes.byref(n),
                                         _stream_ptr(stream)), "ss_lists_export")
         dims = np.zeros(self.dim + 1, np.int32)
         col_ptr = np.zeros(self.dim + 1, np.int32)
-        item = np.zeros(max(1, n.value), np.int32)
+        query = np.zeros(max(1, n.value), np.int32)
         value = np.zeros(max(1, n.value), np.float32)
         self._check(lib.ss_lists_export(self._h, ctypes.byref(nd), dims.ctypes.data, col_ptr.ctypes.data,
-                                        item.ctypes.data, value.ctypes.data, int(item.shape[0]), ctypes.byref(n),
+                                        query.ctypes.data, value.ctypes.data, int(query.shape[0]), ctypes.byref(n),
                                         _stream_ptr(stream)), "ss_lists_export")
         k = nd.value
-        return {"dims": dims[:k], "col_ptr": col_ptr[: k + 1], "item": item[: n.value], "value": value[: n.value]}
+        return {"dims": dims[:k], "col_ptr": col_ptr[: k + 1], "query": query[: n.value], "value": value[: n.value]}
 
     def invalidate(self):
         """Forget the hot set and the prepared queries (after in-place edits)."""

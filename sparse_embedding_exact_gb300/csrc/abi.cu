@@ -208,23 +208,17 @@ void free_lazy_buffers(ss_handle *h) {
   h->qhot_dense = h->hot_scratch = nullptr;
   h->qhot_dense_cap = h->hot_scratch_cap = 0;
   void *tc[] = {h->tc_hot, h->tc_sel, h->tc_stats, h->tc_A, h->tc_qcold, h->tc_qcold_n, h->tc_qcnt,
-                h->tc_qptr, h->tc_qpart, h->tc_slab, h->tc_sq, h->tc_icold_rng, h->tc_B, h->tc_ccnt,
-                h->tc_cptr, h->tc_cpart, h->tc_chat, h->tc_icid, h->tc_rec, h->tc_rec_n};
+                h->tc_qptr, h->tc_qpart, h->tc_qlist, h->tc_slab, h->tc_sq, h->tc_icold_rng, h->tc_B,
+                h->tc_rec, h->tc_rec_n};
   for (void *p : tc) cudaFree(p);
   h->tc_hot = h->tc_sel = h->tc_qcold_n = nullptr;
-  h->tc_qcnt = h->tc_qptr = h->tc_qpart = nullptr;
-  h->tc_ccnt = h->tc_cptr = h->tc_cpart = h->tc_rec_n = nullptr;
+  h->tc_qcnt = h->tc_qptr = h->tc_qpart = h->tc_rec_n = nullptr;
   h->tc_stats = h->tc_slab = h->tc_sq = nullptr;
   h->tc_A = h->tc_B = nullptr;
-  h->tc_qcold = h->tc_rec = h->tc_chat = h->tc_icold_rng = nullptr;
+  h->tc_qcold = h->tc_qlist = h->tc_rec = h->tc_icold_rng = nullptr;
   h->tc_A_cap = h->tc_qcold_cap = h->tc_qcold_n_cap = h->tc_B_cap = h->tc_rec_cap = h->tc_rec_n_cap = 0;
-  h->tc_qcnt_cap = h->tc_qptr_cap = h->tc_qpart_cap = 0;
-  h->tc_ccnt_cap = h->tc_cptr_cap = h->tc_cpart_cap = h->tc_chat_cap = 0;
-  h->tc_icid = nullptr;
-  h->tc_icid_cap = 0;
-  h->tc_n_cid = 0;
+  h->tc_qcnt_cap = h->tc_qptr_cap = h->tc_qpart_cap = h->tc_qlist_cap = 0;
   h->tcq_rows = -1;  // the query side is made again, whole
-  h->tc_lists_build = 0;
   h->n_views = 0;
 }
 
@@ -738,47 +732,46 @@ ss_status ss_index_export(ss_handle *h, const ss_index *idx, int32_t *n_hot, int
   return SS_OK;
 }
 
-ss_status ss_lists_export(ss_handle *h, int64_t *n_dims, int32_t *dims, int32_t *col_ptr, int32_t *item,
+ss_status ss_lists_export(ss_handle *h, int64_t *n_dims, int32_t *dims, int32_t *col_ptr, int32_t *query,
                           float *value, int64_t capacity, int64_t *n_entries, void *stream) {
   if (!h) return SS_ERR_INVALID_ARG;
-  if (!h->tc_qptr || !h->tc_cptr || !h->tc_chat || h->tcq_rows < 0 || capacity < 0)
+  if (!h->tc_qptr || !h->tc_qlist || h->tcq_rows < 0 || capacity < 0)
     return fail(h, SS_ERR_INVALID_ARG, "ss_lists_export: no tensor-path scoring call made yet");
   ss_status st = set_device(h);
   if (st != SS_OK) return st;
   SS_CUDA(h, cudaStreamSynchronize(as_stream(stream)));
-  const int64_t dim = h->dim, nd = h->tc_n_cid;
-  if (h->tc_lists_last < 0 || h->tc_lists_last >= std::max(1, h->tc_lists_chunks))
-    return fail(h, SS_ERR_INVALID_ARG, "ss_lists_export: no tensor-path scoring call made yet");
-  std::vector<int32_t> cid((size_t)dim + 1), ptr((size_t)nd + 1);
-  SS_CUDA(h, cudaMemcpy(cid.data(), h->tc_qptr, sizeof(int32_t) * cid.size(), cudaMemcpyDeviceToHost));
-  SS_CUDA(h, cudaMemcpy(ptr.data(), h->tc_cptr + (int64_t)h->tc_lists_last * (nd + 1), sizeof(int32_t) * ptr.size(),
-                        cudaMemcpyDeviceToHost));
-  if (cid[0] != 0 || cid[(size_t)dim] != nd)
-    return fail(h, SS_ERR_DEVICE_CHECK, "ss_lists_export: numbering inconsistent");
-  const int64_t base = ptr[0], n = (int64_t)ptr[(size_t)nd] - base;
-  if (base < 0 || n < 0 || base + n > h->tc_chat_cap)
+  const int64_t dim = h->dim;
+  std::vector<int32_t> off((size_t)dim + 1);
+  SS_CUDA(h, cudaMemcpy(off.data(), h->tc_qptr, sizeof(int32_t) * off.size(), cudaMemcpyDeviceToHost));
+  const int64_t n = off[(size_t)dim];
+  if (off[0] != 0 || n < 0 || n > h->tc_qlist_cap)
     return fail(h, SS_ERR_DEVICE_CHECK, "ss_lists_export: offsets outside the lists");
-  for (int32_t &x : ptr) x -= (int32_t)base;
+  std::vector<int32_t> ptr(1, 0);
+  std::vector<int32_t> held;
+  for (int64_t d = 0; d < dim; ++d) {
+    if (off[(size_t)d + 1] < off[(size_t)d])
+      return fail(h, SS_ERR_DEVICE_CHECK, "ss_lists_export: offsets not ascending");
+    if (off[(size_t)d + 1] > off[(size_t)d]) {
+      held.push_back((int32_t)d);
+      ptr.push_back(off[(size_t)d + 1]);
+    }
+  }
+  const int64_t nd = (int64_t)held.size();
   if (n_dims) *n_dims = nd;
   if (n_entries) *n_entries = n;
-  if (dims) {
-    int64_t k = 0;
-    for (int64_t d = 0; d < dim; ++d)
-      if (cid[(size_t)d + 1] > cid[(size_t)d]) dims[k++] = (int32_t)d;
-  }
+  if (dims && nd > 0) memcpy(dims, held.data(), sizeof(int32_t) * held.size());
   if (col_ptr) memcpy(col_ptr, ptr.data(), sizeof(int32_t) * ptr.size());
-  if (item || value) {
+  if (query || value) {
     if (capacity < n)
       return fail(h, SS_ERR_LIMIT, "ss_lists_export: %lld entries exceed capacity %lld", (long long)n,
                   (long long)capacity);
     std::vector<int2> ent((size_t)n);
-    if (n > 0)
-      SS_CUDA(h, cudaMemcpy(ent.data(), h->tc_chat + base, sizeof(int2) * (size_t)n, cudaMemcpyDeviceToHost));
-    for (int64_t k = 0; k < nd; ++k)  // each list by ascending item (the device order is unspecified)
+    if (n > 0) SS_CUDA(h, cudaMemcpy(ent.data(), h->tc_qlist, sizeof(int2) * (size_t)n, cudaMemcpyDeviceToHost));
+    for (int64_t k = 0; k < nd; ++k)  // each list by ascending query row (the device order is unspecified)
       std::sort(ent.begin() + ptr[(size_t)k], ent.begin() + ptr[(size_t)k + 1],
                 [](const int2 &x, const int2 &y) { return x.x < y.x; });
     for (int64_t p = 0; p < n; ++p) {
-      if (item) item[p] = ent[(size_t)p].x;
+      if (query) query[p] = ent[(size_t)p].x;
       if (value) memcpy(value + p, &ent[(size_t)p].y, sizeof(float));
     }
   }

@@ -276,10 +276,9 @@ struct ss_handle {
   const void *tc_hot_src[3] = {nullptr, nullptr, nullptr};
   int64_t tc_hot_rows = -1, tc_hot_nnz = -1;
   uint64_t tc_hot_generation = 0;
-  // Query operand ([query tiles][kM x 2Hp] fp16) and cold entries ({cold
-  // number, normalised value bits} at the row's own CSR positions; counts
-  // per row), for the query matrix, inverse norms and hot set they were
-  // made for.
+  // Query operand ([query tiles][kM x 2Hp] fp16) and cold entries ({dim,
+  // normalised value bits} at the row's own CSR positions; counts per row),
+  // for the query matrix, inverse norms and hot set they were made for.
   uint16_t *tc_A = nullptr;
   int64_t tc_A_cap = 0;
   int2 *tc_qcold = nullptr;
@@ -289,13 +288,13 @@ struct ss_handle {
   const void *tcq_src[4] = {nullptr, nullptr, nullptr, nullptr};
   int64_t tcq_rows = -1, tcq_nnz = -1;
   uint64_t tcq_generation = ~0ull;
-  // The numbering of the queries' cold dimensions: marks [dim + 1], their
-  // exclusive scan (the cold number of dimension d; d is held by some query
-  // iff entry d + 1 > entry d), the scan's tile sums; the count of numbers.
+  // The queries' lists by dimension (CSC of their cold entries): counters
+  // (then cursors) [dim + 1], offsets [dim + 1], the scan's tile sums, the
+  // entries {query row, normalised value bits} [nnz of the queries].
   int32_t *tc_qcnt = nullptr, *tc_qptr = nullptr, *tc_qpart = nullptr;
   int64_t tc_qcnt_cap = 0, tc_qptr_cap = 0, tc_qpart_cap = 0;
-  int64_t tc_n_cid = 0;
-  uint64_t tcq_serial = 0;  // counts query preparations
+  int2 *tc_qlist = nullptr;
+  int64_t tc_qlist_cap = 0;
   // Per chunk of a build: raw hot values [chunk_rows][kHotMax], sums of
   // squares and {first cold entry, count} per item [chunk_rows] (the cold
   // entries themselves go to post_hat).
@@ -305,22 +304,8 @@ struct ss_handle {
   // Item operand of the chunk being scored ([item tiles][kN x 2Hp] fp16).
   uint16_t *tc_B = nullptr;
   int64_t tc_B_cap = 0;
-  // The lists by cold number of every chunk of the last build, made at the
-  // first scoring call after the build or after a new query preparation:
-  // counters (then cursors) and offsets [n_chunks][n_cid + 1], the scan's
-  // tile sums, the entries {item within its chunk, raw value bits}; which
-  // build and queries they were made for, how many chunks, the chunk of the
-  // last scoring call.
-  int32_t *tc_ccnt = nullptr, *tc_cptr = nullptr, *tc_cpart = nullptr;
-  int64_t tc_ccnt_cap = 0, tc_cptr_cap = 0, tc_cpart_cap = 0;
-  int2 *tc_chat = nullptr;
-  int64_t tc_chat_cap = 0;
-  int32_t *tc_icid = nullptr;  // per build entry (as the build's cold entries): its cold number or -1
-  int64_t tc_icid_cap = 0;
-  uint64_t tc_build_serial = 0, tc_lists_build = 0, tc_lists_queries = 0;
-  int32_t tc_lists_chunks = 0, tc_lists_last = 0;
-  // Cold records of one scoring call: sub-buckets of (8 query rows, 32
-  // items) and their counts (-1: did not fit).
+  // Cold records of one scoring call: buckets of (32 query rows, 32 items)
+  // and their counts (-1: did not fit).
   int2 *tc_rec = nullptr;
   int64_t tc_rec_cap = 0;
   int32_t *tc_rec_n = nullptr;

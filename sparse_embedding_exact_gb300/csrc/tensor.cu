@@ -89,7 +89,8 @@ constexpr int kTailRecs = 128;                 // epilogue: a block's records pa
                                                // shared memory (two slots per warp)
 constexpr int kTailBytes = kEpiWarps * 2 * kTailRecs * 8;
 static_assert(kEpiWarps % 4 == 0 && 8 % kWarpsPerQ == 0, "whole blocks per epilogue warp");
-constexpr int kRThreads = 1024;         // records: one warp per query row of a 32-row block
+constexpr int kRThreads = 512;          // records: a block per 32-item column block, two per SM
+constexpr int64_t kRecMaxQuarters = 16384;  // records: bucket counters in shared memory up to this many
 constexpr int kPrepThreads = 256;
 constexpr int kWalkUnroll = 8;          // list entries per lane loaded before use
 constexpr int kRecPerLane = 4;          // epilogue: a block's first records per lane (128), fetched two blocks ahead
@@ -494,8 +495,8 @@ __global__ void __launch_bounds__(kSelThreads)
 // the dense slab (0 where absent), its sum of squares, and its cold entries
 // {dim, raw value bits} packed in CSR order (dims ascending) at the row's
 // own positions relative to the build's first nonzero, with {first, count}
-// per item.  Each scoring call sorts these entries into lists over the
-// dimensions its queries hold (k_tc_chist / k_tc_cscatter below).
+// per item.  Each scoring call's records kernel walks these entries item by
+// item, each into the queries' list of its dimension.
 __global__ void __launch_bounds__(256)
     k_tc_build(const int64_t *__restrict__ indptr, const int32_t *__restrict__ indices,
                const float *__restrict__ values, int64_t row_begin, int64_t row_end, int64_t chunk_rows,
@@ -551,87 +552,39 @@ __global__ void __launch_bounds__(256)
   if (__any_sync(0xffffffffu, bad) && lane == 0) flag(status, DEV_OUT_OF_RANGE);
 }
 
-// The query side's numbering of cold dimensions, once per query matrix,
-// inverse norms and hot set: every dimension that some query row holds as
-// a cold nonzero is marked (mark[d] = 1, the same value from every writer),
-// an exclusive scan of the marks (launch_count_scan) numbers the marked
-// dimensions 0, 1, ... in ascending order (cid[d]; cid[d + 1] > cid[d]
-// exactly for the marked ones), and the queries' cold entries then carry
-// that number in place of the dimension.  A chunk's lists are made over
-// these numbers only: a dimension no query row holds cold makes no product.
+// The queries' lists, once per query matrix, inverse norms and hot set: a
+// counting sort of the queries' cold entries by dimension.  The counts per
+// dimension (k_tc_qcount), their exclusive scan (launch_count_scan: list d
+// is entries [qptr[d], qptr[d + 1]) and is empty for a dimension no query
+// row holds cold; the scan leaves each counter at its list's start), then
+// the scatter (k_tc_qscatter), which takes each entry's place from its
+// dimension's counter and writes {query row, normalised value bits}.  A list's order is unspecified:
+// the records it makes are summed as integers.  Every scoring call walks
+// the same lists from its chunk's items, so nothing is sorted per chunk.
 __global__ void __launch_bounds__(256)
-    k_tc_qmark(const int64_t *__restrict__ q_indptr, const int2 *__restrict__ qcold,
-               const int32_t *__restrict__ qcold_n, int64_t n_q, int32_t *__restrict__ mark) {
+    k_tc_qcount(const int64_t *__restrict__ q_indptr, const int2 *__restrict__ qcold,
+                const int32_t *__restrict__ qcold_n, int64_t n_q, int32_t *__restrict__ count) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * 8;
   for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < n_q; r += warps) {
     const int64_t b = q_indptr[r];
     const int n = qcold_n[r];
-    for (int j = lane; j < n; j += 32) mark[__ldg(qcold + b + j).x] = 1;
+    for (int j = lane; j < n; j += 32) atomicAdd(count + __ldg(qcold + b + j).x, 1);
   }
 }
 
 __global__ void __launch_bounds__(256)
-    k_tc_qcid(const int64_t *__restrict__ q_indptr, int2 *__restrict__ qcold, const int32_t *__restrict__ qcold_n,
-              int64_t n_q, const int32_t *__restrict__ cid) {
+    k_tc_qscatter(const int64_t *__restrict__ q_indptr, const int2 *__restrict__ qcold,
+                  const int32_t *__restrict__ qcold_n, int64_t n_q, int32_t *__restrict__ cursor,
+                  int2 *__restrict__ qlist) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * 8;
   for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < n_q; r += warps) {
     const int64_t b = q_indptr[r];
     const int n = qcold_n[r];
-    for (int j = lane; j < n; j += 32) qcold[b + j].x = __ldg(cid + qcold[b + j].x);
-  }
-}
-
-// The lists of every chunk of a build (CSC by query cold number, one set
-// per chunk), made at the first scoring call that needs them: a counting
-// sort of the build's per-item cold entries by (chunk, cid), the entries of
-// dimensions no query holds cold left out.  The histogram here (a warp per
-// item; each entry's number, or -1, is kept beside it so that the scatter
-// reads it back in order instead of looking it up again),
-// launch_count_scan over the n_chunks x (n_cid + 1) counters, then the
-// scatter, which writes {item within its chunk, raw value bits} (each
-// call's records kernel multiplies by that call's inverse norms).  A
-// list's order is unspecified: the records it makes are summed as
-// integers.  Items are numbered across the build: item `it` is row
-// it % chunk_rows of chunk it / chunk_rows.
-__global__ void __launch_bounds__(256)
-    k_tc_chist(const int2 *__restrict__ icold, const int2 *__restrict__ icold_rng, int64_t n_items,
-               int64_t chunk_rows, const int32_t *__restrict__ cid, int64_t n_ccnt, int32_t *__restrict__ count,
-               int32_t *__restrict__ icid) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warps = (int64_t)gridDim.x * 8;
-  for (int64_t it = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); it < n_items; it += warps) {
-    const int2 rng = __ldg(icold_rng + it);
-    int32_t *cnt = count + (it / chunk_rows) * n_ccnt;
-    for (int j = lane; j < rng.y; j += 32) {
-      const int d = __ldg(icold + rng.x + j).x;
-      const int c0 = __ldg(cid + d), c1 = __ldg(cid + d + 1);
-      icid[rng.x + j] = c1 > c0 ? c0 : -1;
-      if (c1 > c0) atomicAdd(cnt + c0, 1);
-    }
-  }
-}
-
-__global__ void __launch_bounds__(256)
-    k_tc_cscatter(const int2 *__restrict__ icold, const int2 *__restrict__ icold_rng, int64_t n_items,
-                  int64_t chunk_rows, const int32_t *__restrict__ icid, int64_t n_ccnt,
-                  int32_t *__restrict__ cursor, int2 *__restrict__ chat, int64_t capacity, int32_t *status) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warps = (int64_t)gridDim.x * 8;
-  for (int64_t it = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); it < n_items; it += warps) {
-    const int2 rng = __ldg(icold_rng + it);
-    const int64_t c = it / chunk_rows;
-    int32_t *cur = cursor + c * n_ccnt;
-    const int item = (int)(it - c * chunk_rows);
-    for (int j = lane; j < rng.y; j += 32) {
-      const int c0 = __ldg(icid + rng.x + j);
-      if (c0 < 0) continue;
-      const int32_t pos = atomicAdd(cur + c0, 1);
-      if (pos >= 0 && (int64_t)pos < capacity)
-        chat[pos] = make_int2(item, __ldg(icold + rng.x + j).y);
-      else
-        flag(status, DEV_CAPACITY);
+    for (int j = lane; j < n; j += 32) {
+      const int2 e = __ldg(qcold + b + j);
+      qlist[atomicAdd(cursor + e.x, 1)] = make_int2((int)r, e.y);
     }
   }
 }
@@ -807,56 +760,59 @@ __device__ void prep_item_groups(const PrepArgs &a, int64_t g0, int64_t stride, 
 // and a count (-1 when its records did not fit; the scorer then computes
 // the bucket from the lists).
 struct RecArgs {
-  const int64_t *q_indptr;
-  const int2 *qcold;       // queries' cold entries {cid, normalised value bits}
-  const int32_t *qcold_n;
-  int64_t n_q;
-  const int32_t *col_ptr;  // the chunk's lists: [n_cid + 1] offsets into chat
-  const int2 *chat;        // {item, raw value bits}
+  const int2 *icold;       // the chunk's items' cold entries {dim, raw value bits}
+  const int2 *icold_rng;   // per item of the chunk: {first entry, count}
+  int32_t n_items;
   const float *inv_i;      // the chunk's inverse norms
+  const int32_t *qptr;     // the queries' lists: [dim + 1] offsets into qlist
+  const int2 *qlist;       // {query row, normalised value bits}
+  int64_t n_quarters;      // 32-row groups of queries
   int32_t n_cb;            // 32-item column blocks of the chunk
   int32_t bucket_cap;      // records a bucket holds
   int2 *rec;               // [quarter][column block][bucket_cap]
   int32_t *rec_n;          // [quarter][column block]
   int32_t *status;
-  int64_t n_main;          // quarters with a block of their own (whole waves of blocks)
-  int64_t n_shared;        // blocks sharing the rows of the quarters after those
+  int64_t n_main;          // column blocks with a block of their own (whole waves of blocks)
+  int64_t n_shared;        // blocks sharing the items of the column blocks after those
   PrepArgs prep;           // the chunk's item operand (the blocks after all of these)
 };
 
-// Calls f(item, product) for every cold product of query row r with the
-// chunk.  One warp takes the row's cold entries 32 at a time and lays their
-// lists end to end; each lane then takes one list entry of every window of
-// 32, finding its list from the bits that mark where lists start inside
-// the window (a lane's list is the last one that starts at or before it).
+// Calls f(query row, product) for every cold product of item `it` with the
+// queries.  One warp takes the item's cold entries 32 at a time and lays
+// the queries' lists of their dimensions end to end; each lane then takes
+// one list entry of every window of 32, finding its list from the bits
+// that mark where lists start inside the window (a lane's list is the last
+// one that starts at or before it).  The item's value is normalised once
+// per entry; the product is the same fp32 product of the two normalised
+// values, whichever side is walked.
 template <typename F>
-__device__ __forceinline__ void walk_row(const RecArgs &a, int64_t r, int lane, int4 *slots, F f, int piece = 0,
-                                         int pieces = 1) {
-  const int64_t qb = a.q_indptr[r];
-  const int cn = a.qcold_n[r];
+__device__ __forceinline__ void walk_item(const RecArgs &a, int it, int lane, int4 *slots, F f, int piece = 0,
+                                          int pieces = 1) {
+  const int2 rng = __ldg(a.icold_rng + it);
+  const float ivi = __ldg(a.inv_i + it);
   const unsigned lt = (1u << lane) - 1u, lt_eq = (2u << lane) - 1u;
-  for (int b0 = 0; b0 < cn; b0 += 32) {
+  for (int b0 = 0; b0 < rng.y; b0 += 32) {
     int s = 0, len = 0;
-    float qv = 0.f;
-    if (b0 + lane < cn) {
-      const int2 e = __ldg(a.qcold + qb + b0 + lane);
-      qv = __int_as_float(e.y);
-      s = __ldg(a.col_ptr + e.x);
-      len = __ldg(a.col_ptr + e.x + 1) - s;
+    float iv = 0.f;
+    if (b0 + lane < rng.y) {
+      const int2 e = __ldg(a.icold + rng.x + b0 + lane);
+      iv = __int_as_float(e.y) * ivi;
+      s = __ldg(a.qptr + e.x);
+      len = __ldg(a.qptr + e.x + 1) - s;
     }
     // The non-empty lists move to the first lanes, in order.
     const unsigned nz = __ballot_sync(0xffffffffu, len > 0);
-    if (len > 0) slots[__popc(nz & lt)] = make_int4(s, len, __float_as_int(qv), 0);
+    if (len > 0) slots[__popc(nz & lt)] = make_int4(s, len, __float_as_int(iv), 0);
     __syncwarp();
     if (lane < __popc(nz)) {
       const int4 v = slots[lane];
       s = v.x;
       len = v.y;
-      qv = __int_as_float(v.z);
+      iv = __int_as_float(v.z);
     } else {
       s = 0;
       len = 0;
-      qv = 0.f;
+      iv = 0.f;
     }
     __syncwarp();
     const int incl = warp_incl_scan(len, lane);
@@ -866,7 +822,7 @@ __device__ __forceinline__ void walk_row(const RecArgs &a, int64_t r, int lane, 
     // the walk is not shared), kWalkUnroll at a time.
     for (int base = piece; 32 * base < L; base += pieces * kWalkUnroll) {
       int pos[kWalkUnroll];
-      float pq[kWalkUnroll];
+      float pv[kWalkUnroll];
       bool ok[kWalkUnroll];
 #pragma unroll
       for (int u = 0; u < kWalkUnroll; ++u) {
@@ -880,35 +836,34 @@ __device__ __forceinline__ void walk_row(const RecArgs &a, int64_t r, int lane, 
         const int jj = j < 31 ? j : 31;
         const int sj = __shfl_sync(0xffffffffu, s, jj);
         const int ej = __shfl_sync(0xffffffffu, excl, jj);
-        pq[u] = __shfl_sync(0xffffffffu, qv, jj);
+        pv[u] = __shfl_sync(0xffffffffu, iv, jj);
         ok[u] = fi < L;
         pos[u] = sj + (fi - ej);
       }
-      int2 ph[kWalkUnroll];
+      int2 qe[kWalkUnroll];
 #pragma unroll
       for (int u = 0; u < kWalkUnroll; ++u) {
-        ph[u] = make_int2(0, 0);
-        if (ok[u]) ph[u] = ld_keep_int2(a.chat + pos[u]);
+        qe[u] = make_int2(0, 0);
+        if (ok[u]) qe[u] = ld_keep_int2(a.qlist + pos[u]);
       }
-      float iv[kWalkUnroll];
-#pragma unroll
-      for (int u = 0; u < kWalkUnroll; ++u) iv[u] = ok[u] ? __ldg(a.inv_i + ph[u].x) : 0.f;
 #pragma unroll
       for (int u = 0; u < kWalkUnroll; ++u)
-        if (ok[u]) f(ph[u].x, cold_fix(pq[u], __int_as_float(ph[u].y) * iv[u]));
+        if (ok[u]) f(qe[u].x, cold_fix(__int_as_float(qe[u].y), pv[u]));
     }
   }
 }
 
-// Every cold product of a query row with the chunk becomes a record in the
+// Every cold product of an item with the queries becomes a record in the
 // bucket of its (32 rows, 32 items), at a slot taken from the bucket's
 // counter (the order inside a bucket does not matter: the epilogue sums
-// integers).  The quarters that fill whole waves of blocks get a block each
-// (one warp per row, counters in shared memory); the rows of the quarters
-// left over, which would run as a short last wave of whole blocks, are
-// shared by all warps of one more wave of blocks (several warps per row,
-// counters in global memory).  Blocks after those write the item operand.
-__global__ void __launch_bounds__(kRThreads) k_tc_records(const RecArgs a) {
+// integers).  A column block gets a block of its own (its 32 items taken a
+// warp at a time, a counter per quarter in shared memory) when the column
+// blocks fill whole waves of blocks, or one wave that gives every SM a
+// block; otherwise the items of the column blocks past the whole waves are
+// shared by all warps of one more wave of blocks (several warps per item
+// when there are few, counters in global memory).  Blocks after those
+// write the item operand.
+__global__ void __launch_bounds__(kRThreads, 2) k_tc_records(const RecArgs a) {
   const int64_t bid = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ncb = a.n_cb, cap = a.bucket_cap;
@@ -920,48 +875,48 @@ __global__ void __launch_bounds__(kRThreads) k_tc_records(const RecArgs a) {
   __shared__ int4 slots_all[kRThreads / 32][32];
   int4 *slots = slots_all[warp];
   if (bid >= a.n_main) {
-    // The rows of the quarters past the main ones, shared by every warp of
-    // these blocks: row e gets `pieces` warps, warp k of them walking the
-    // windows k, k + pieces, ... of its lists.  Their buckets are counted
-    // in global memory (zeroed before the launch): a count above the
-    // bucket's room marks it as not fitting.
-    const int64_t row0 = a.n_main * 32, rows = a.n_q - row0;
+    // The items past the main column blocks, shared by every warp of these
+    // blocks: item e gets `pieces` warps, warp k of them walking the windows
+    // k, k + pieces, ... of its lists (when the items outnumber the warps,
+    // each warp takes every warps-th item).  Their buckets are counted in
+    // global memory (zeroed before the launch): a count above the bucket's
+    // room marks it as not fitting.
+    const int64_t item0 = a.n_main * 32, items = a.n_items - item0;
     const int64_t warps = a.n_shared * (kRThreads / 32);
-    const int64_t w = (bid - a.n_main) * (kRThreads / 32) + warp;
-    const int64_t per_row = warps / (rows > 0 ? rows : 1);
-    const int pieces = (int)(per_row > 1 ? per_row : 1);
-    if (w >= rows * pieces) return;
-    const int64_t r = row0 + w % rows;
-    const int piece = (int)(w / rows);
-    const int64_t Q = r / 32;
-    const int rl = (int)(r - Q * 32);
-    int2 *rq = a.rec + Q * ncb * (int64_t)cap;
-    int32_t *cnt = a.rec_n + Q * ncb;
-    walk_row(
-        a, r, lane, slots,
-        [&](int item, int p) {
-          const int cb = item >> 5;
-          const int slot = atomicAdd(cnt + cb, 1);
-          if (slot < cap) rq[(int64_t)cb * cap + slot] = make_int2(stg_index(rl, item & 31), p);
-        },
-        piece, pieces);
+    const int64_t per_item = warps / (items > 0 ? items : 1);
+    const int pieces = (int)(per_item > 1 ? per_item : 1);
+    for (int64_t w = (bid - a.n_main) * (kRThreads / 32) + warp; w < items * pieces; w += warps) {
+      const int it = (int)(item0 + w % items);
+      const int piece = (int)(w / items);
+      const int cb = it >> 5, il = it & 31;
+      walk_item(
+          a, it, lane, slots,
+          [&](int q, int p) {
+            const int64_t Q = q >> 5;
+            const int slot = atomicAdd(a.rec_n + Q * ncb + cb, 1);
+            if (slot < cap) a.rec[(Q * ncb + cb) * cap + slot] = make_int2(stg_index(q & 31, il), p);
+          },
+          piece, pieces);
+    }
     return;
   }
-  extern __shared__ int rcnt[];  // [n_cb]
+  extern __shared__ int rcnt[];  // [n_quarters]
   const int tid = threadIdx.x;
-  const int64_t Q = bid;
-  for (int c = tid; c < ncb; c += kRThreads) rcnt[c] = 0;
+  const int64_t cb = bid;
+  const int nqt = (int)a.n_quarters;
+  for (int c = tid; c < nqt; c += kRThreads) rcnt[c] = 0;
   __syncthreads();
-  int2 *rq = a.rec + Q * ncb * (int64_t)cap;
-  const int64_t r = Q * 32 + warp;
-  if (r < a.n_q)
-    walk_row(a, r, lane, slots, [&](int item, int p) {
-      const int cb = item >> 5;
-      const int slot = atomicAdd(&rcnt[cb], 1);
-      if (slot < cap) rq[(int64_t)cb * cap + slot] = make_int2(stg_index(warp, item & 31), p);
-    });
+  for (int il = warp; il < 32; il += kRThreads / 32) {  // the block's items, a warp to each in turn
+    const int it = (int)(cb * 32 + il);
+    if (it < a.n_items)
+      walk_item(a, it, lane, slots, [&](int q, int p) {
+        const int Q = q >> 5;
+        const int slot = atomicAdd(&rcnt[Q], 1);
+        if (slot < cap) a.rec[((int64_t)Q * ncb + cb) * cap + slot] = make_int2(stg_index(q & 31, il), p);
+      });
+  }
   __syncthreads();
-  for (int c = tid; c < ncb; c += kRThreads) a.rec_n[Q * ncb + c] = rcnt[c] <= cap ? rcnt[c] : -1;
+  for (int c = tid; c < nqt; c += kRThreads) a.rec_n[(int64_t)c * ncb + cb] = rcnt[c] <= cap ? rcnt[c] : -1;
 }
 
 // ---------------------------------------------------------------- scorer
@@ -973,13 +928,12 @@ struct ScoreArgs {
   const int2 *rec;         // the call's records (k_tc_records)
   const int32_t *rec_n;    // their counts per bucket (-1: did not fit)
   int32_t bucket_cap;
-  // For buckets that did not fit: the queries' cold entries and the call's
-  // lists of the chunk.
-  const int64_t *q_indptr;
-  const int2 *qcold;
-  const int32_t *qcold_n;
-  const int32_t *col_ptr;
-  const int2 *chat;
+  // For buckets that did not fit: the chunk's items' cold entries and the
+  // queries' lists.
+  const int2 *icold;
+  const int2 *icold_rng;
+  const int32_t *qptr;
+  const int2 *qlist;
   const float *inv_i;
   int64_t n_quarters;
   int32_t n_cb;
@@ -1329,22 +1283,21 @@ __global__ void __launch_bounds__(kSThreads, 1)
           }
           prefetch();
           if (n < 0) {
-            // The bucket did not fit: each lane walks its row's cold lists
-            // and keeps the items of this block (rare; exact, the same sums).
-            const int64_t q = (int64_t)qrow0 + lane;
-            const int lo = item0 + c * kColBlock;
-            if (q < a.n_q) {
-              const int64_t qb = a.q_indptr[q];
-              const int cn = a.qcold_n[q];
-              for (int e = 0; e < cn; ++e) {
-                const int2 qe = __ldg(a.qcold + qb + e);
-                const float qv = __int_as_float(qe.y);
-                const int p1 = __ldg(a.col_ptr + qe.x + 1);
-                for (int p = __ldg(a.col_ptr + qe.x); p < p1; ++p) {
-                  const int2 ph = __ldg(a.chat + p);
-                  const int d = ph.x - lo;
-                  if ((unsigned)d < (unsigned)kColBlock)
-                    atomicAdd(stg + stg_index(lane, d), cold_fix(qv, __int_as_float(ph.y) * __ldg(a.inv_i + ph.x)));
+            // The bucket did not fit: each lane walks its item's cold
+            // entries through the queries' lists and keeps the rows of this
+            // block (rare; exact, the same sums).
+            const int it = item0 + c * kColBlock + lane;
+            if (it < a.n_items) {
+              const int2 rng = __ldg(a.icold_rng + it);
+              const float ivi = __ldg(a.inv_i + it);
+              for (int e = 0; e < rng.y; ++e) {
+                const int2 ie = __ldg(a.icold + rng.x + e);
+                const float iv = __int_as_float(ie.y) * ivi;
+                const int p1 = __ldg(a.qptr + ie.x + 1);
+                for (int p = __ldg(a.qptr + ie.x); p < p1; ++p) {
+                  const int2 qe = __ldg(a.qlist + p);
+                  const int d = qe.x - (int)qrow0;
+                  if ((unsigned)d < 32u) atomicAdd(stg + stg_index(d, lane), cold_fix(__int_as_float(qe.y), iv));
                 }
               }
             }
@@ -1551,7 +1504,6 @@ cudaError_t launch_build_tc(ss_handle *h, const ss_csr &items, int64_t row_begin
     if ((e = dev_alloc(&h->tc_sq, sizeof(float) * rows)) != cudaSuccess) return e;
     if ((e = dev_alloc(&h->tc_icold_rng, sizeof(int2) * rows)) != cudaSuccess) return e;
   }
-  ++h->tc_build_serial;  // the lists made for the previous build's chunks are stale
   const int grid = (h->sm_count > 0 ? h->sm_count : 148) * 8;
   // The build's cold entries go to the entry array sized for the matrix
   // (post_hat, post_cap >= items.nnz), at the rows' own positions.
@@ -1633,8 +1585,8 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
   cudaError_t e = cudaSuccess;
   int nq = 0;
 
-  // Query operand, cold entries and the numbering of the queries' cold
-  // dimensions, once per query matrix, inverse norms and hot set.
+  // Query operand, cold entries and the queries' lists, once per query
+  // matrix, inverse norms and hot set.
   if (!(h->tcq_src[0] == q.indptr && h->tcq_src[1] == q.indices && h->tcq_src[2] == q.values &&
         h->tcq_src[3] == inv_q && h->tcq_rows == q.n_rows && h->tcq_nnz == q.nnz &&
         h->tcq_generation == h->tc_hot_generation)) {
@@ -1646,6 +1598,7 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     if ((e = grow(&h->tc_qcnt, &h->tc_qcnt_cap, n_cnt, s)) != cudaSuccess) return e;
     if ((e = grow(&h->tc_qptr, &h->tc_qptr_cap, n_cnt, s)) != cudaSuccess) return e;
     if ((e = grow(&h->tc_qpart, &h->tc_qpart_cap, scan_tile_count(n_cnt) + 1, s)) != cudaSuccess) return e;
+    if ((e = grow(&h->tc_qlist, &h->tc_qlist_cap, std::max<int64_t>(1, q.nnz), s)) != cudaSuccess) return e;
     PrepArgs pa;
     pa.indptr = q.indptr;
     pa.idx = q.indices;
@@ -1667,19 +1620,12 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     k_tc_prep_queries<<<(unsigned)blocks, kPrepThreads, 0, s>>>(pa);
     if ((e = cudaMemsetAsync(h->tc_qcnt, 0, sizeof(int32_t) * (size_t)n_cnt, s)) != cudaSuccess) return e;
     const int64_t row_blocks = std::min<int64_t>((n_q + 7) / 8, (int64_t)sms * 8);
-    k_tc_qmark<<<(unsigned)row_blocks, 256, 0, s>>>(q.indptr, h->tc_qcold, h->tc_qcold_n, n_q, h->tc_qcnt);
+    k_tc_qcount<<<(unsigned)row_blocks, 256, 0, s>>>(q.indptr, h->tc_qcold, h->tc_qcold_n, n_q, h->tc_qcnt);
     if ((e = launch_count_scan(h->tc_qcnt, n_cnt, h->tc_qpart, h->tc_qptr, s)) != cudaSuccess) return e;
-    k_tc_qcid<<<(unsigned)row_blocks, 256, 0, s>>>(q.indptr, h->tc_qcold, h->tc_qcold_n, n_q, h->tc_qptr);
+    k_tc_qscatter<<<(unsigned)row_blocks, 256, 0, s>>>(q.indptr, h->tc_qcold, h->tc_qcold_n, n_q, h->tc_qcnt,
+                                                       h->tc_qlist);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     nq += 6;
-    // The number of cold dimensions the queries hold sizes every call's
-    // lists: read once here.
-    int32_t n_cid = 0;
-    if ((e = cudaMemcpyAsync(&n_cid, h->tc_qptr + dim, sizeof(int32_t), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
-      return e;
-    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
-    if (n_cid < 0 || (int64_t)n_cid > dim) return cudaErrorIllegalState;
-    h->tc_n_cid = n_cid;
     h->tcq_src[0] = q.indptr;
     h->tcq_src[1] = q.indices;
     h->tcq_src[2] = q.values;
@@ -1687,9 +1633,7 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     h->tcq_rows = q.n_rows;
     h->tcq_nnz = q.nnz;
     h->tcq_generation = h->tc_hot_generation;
-    ++h->tcq_serial;
   }
-  const int64_t n_cid = h->tc_n_cid;
 
   // Item operand of this chunk (written by the records launch's trailing
   // blocks).
@@ -1714,45 +1658,6 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     pa.status = h->d_status;
   }
 
-  // The lists over the queries' cold dimensions, for every chunk of the
-  // index's build at once, at the first call that needs them.
-  const int64_t n_ccnt = n_cid + 1;
-  const bool is_view = &idx >= h->views && &idx < h->views + h->n_views;
-  const ss_index *first = is_view ? h->views : &idx;
-  const int n_chunks = is_view ? h->n_views : 1;
-  const int kpos = is_view ? (int)(&idx - h->views) : 0;
-  if (!(is_view && h->tc_lists_build == h->tc_build_serial && h->tc_lists_queries == h->tcq_serial)) {
-    const int64_t C = h->chunk_rows;
-    const int64_t items_all = (int64_t)(n_chunks - 1) * C + first[n_chunks - 1].n_items;
-    if (n_chunks > 1 && (first[1].icold_rng != first[0].icold_rng + C || first[1].icold != first[0].icold))
-      return cudaErrorInvalidValue;  // a build's chunks share one entry array, rows C apart
-    if ((e = grow(&h->tc_ccnt, &h->tc_ccnt_cap, n_chunks * n_ccnt, s)) != cudaSuccess) return e;
-    if ((e = grow(&h->tc_cptr, &h->tc_cptr_cap, n_chunks * n_ccnt, s)) != cudaSuccess) return e;
-    if ((e = grow(&h->tc_cpart, &h->tc_cpart_cap, scan_tile_count(n_chunks * n_ccnt) + 1, s)) != cudaSuccess)
-      return e;
-    if ((e = grow(&h->tc_chat, &h->tc_chat_cap, std::max<int64_t>(1, idx.capacity), s)) != cudaSuccess) return e;
-    if ((e = grow(&h->tc_icid, &h->tc_icid_cap, std::max<int64_t>(1, idx.capacity), s)) != cudaSuccess) return e;
-    h->tc_lists_build = 0;
-    const int64_t item_blocks = std::min<int64_t>((items_all + 7) / 8, (int64_t)sms * 8);
-    if ((e = cudaMemsetAsync(h->tc_ccnt, 0, sizeof(int32_t) * (size_t)(n_chunks * n_ccnt), s)) != cudaSuccess)
-      return e;
-    k_tc_chist<<<(unsigned)item_blocks, 256, 0, s>>>(first->icold, first->icold_rng, items_all, C, h->tc_qptr,
-                                                     n_ccnt, h->tc_ccnt, h->tc_icid);
-    if ((e = launch_count_scan(h->tc_ccnt, n_chunks * n_ccnt, h->tc_cpart, h->tc_cptr, s)) != cudaSuccess) return e;
-    k_tc_cscatter<<<(unsigned)item_blocks, 256, 0, s>>>(first->icold, first->icold_rng, items_all, C, h->tc_icid,
-                                                        n_ccnt, h->tc_ccnt, h->tc_chat, h->tc_chat_cap,
-                                                        h->d_status);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    nq += 5;
-    if (is_view) {
-      h->tc_lists_build = h->tc_build_serial;
-      h->tc_lists_queries = h->tcq_serial;
-    }
-    h->tc_lists_chunks = n_chunks;
-  }
-  const int32_t *col_ptr = h->tc_cptr + (int64_t)kpos * n_ccnt;
-  h->tc_lists_last = kpos;
-
   // Cold records: a bucket per (32 query rows, 32 items) holding three
   // times the sample's estimate of its records plus 64 (at least 64, at
   // most 1024); the scorer computes the blocks of fuller buckets from the
@@ -1766,22 +1671,25 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
   if ((e = grow(&h->tc_rec, &h->tc_rec_cap, n_quarters * n_cb * (int64_t)cap, s)) != cudaSuccess) return e;
   {
     RecArgs ra;
-    ra.q_indptr = q.indptr;
-    ra.qcold = h->tc_qcold;
-    ra.qcold_n = h->tc_qcold_n;
-    ra.n_q = n_q;
-    ra.col_ptr = col_ptr;
-    ra.chat = h->tc_chat;
+    ra.icold = idx.icold;
+    ra.icold_rng = idx.icold_rng;
+    ra.n_items = n_items;
     ra.inv_i = inv_i;
+    ra.qptr = h->tc_qptr;
+    ra.qlist = h->tc_qlist;
+    ra.n_quarters = n_quarters;
     ra.n_cb = n_cb;
     ra.bucket_cap = cap;
     ra.rec = h->tc_rec;
     ra.rec_n = h->tc_rec_n;
     ra.status = h->d_status;
     ra.prep = pa;
-    const size_t smem = sizeof(int) * (size_t)n_cb;
+    // A main block counts its buckets in shared memory (one counter per
+    // quarter); past kRecMaxQuarters every item goes the shared way.
+    const bool own = n_quarters <= kRecMaxQuarters;
+    const size_t smem = own ? sizeof(int) * (size_t)n_quarters : 0;
     if ((e = ensure_dyn_smem(k_tc_records, smem)) != cudaSuccess) return e;
-    // Whole waves of quarter blocks, then one wave sharing the rest.
+    // Whole waves of column blocks, then one wave sharing the rest.
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_tc_records, kRThreads, smem) != cudaSuccess ||
         per_sm < 1) {
@@ -1789,11 +1697,14 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
       per_sm = 1;
     }
     const int64_t wave = (int64_t)sms * per_sm;
-    ra.n_main = n_quarters / wave * wave;
-    ra.n_shared = ra.n_main < n_quarters ? wave : 0;
+    // A chunk of at most one wave of column blocks that still gives every
+    // SM one runs as main blocks only; a smaller one is shared out.
+    ra.n_main = !own ? 0 : (n_cb <= wave && 2 * n_cb >= wave) ? n_cb : n_cb / wave * wave;
+    ra.n_shared = ra.n_main < n_cb ? wave : 0;
+    // The shared column blocks' counters: [n_main, n_cb) of every quarter.
     if (ra.n_shared > 0 &&
-        (e = cudaMemsetAsync(h->tc_rec_n + ra.n_main * n_cb, 0,
-                             sizeof(int32_t) * (size_t)((n_quarters - ra.n_main) * n_cb), s)) != cudaSuccess)
+        (e = cudaMemset2DAsync(h->tc_rec_n + ra.n_main, sizeof(int32_t) * (size_t)n_cb, 0,
+                               sizeof(int32_t) * (size_t)(n_cb - ra.n_main), (size_t)n_quarters, s)) != cudaSuccess)
       return e;
     // The operand's blocks (a warp per group of 8 items) come last.
     const int64_t prep_blocks = (pa.n_groups + kRThreads / 32 - 1) / (kRThreads / 32);
@@ -1820,11 +1731,10 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     sa.rec = h->tc_rec;
     sa.rec_n = h->tc_rec_n;
     sa.bucket_cap = cap;
-    sa.q_indptr = q.indptr;
-    sa.qcold = h->tc_qcold;
-    sa.qcold_n = h->tc_qcold_n;
-    sa.col_ptr = col_ptr;
-    sa.chat = h->tc_chat;
+    sa.icold = idx.icold;
+    sa.icold_rng = idx.icold_rng;
+    sa.qptr = h->tc_qptr;
+    sa.qlist = h->tc_qlist;
     sa.inv_i = inv_i;
     sa.n_quarters = n_quarters;
     sa.n_cb = n_cb;

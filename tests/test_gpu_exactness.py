@@ -117,48 +117,44 @@ def test_index_is_the_chunks_csc(sec, algorithm, name, n_i, rb, re):
 
 @pytest.mark.parametrize("name,n_q", [("d1.2m_q5k_i200k", 5000), ("d65k_q1k_i10k", 1000),
                                       ("d1.2m_q20k_i1m_heavy", 3000)])
-def test_call_lists_are_the_chunks_csc_over_the_queries_cold_dims(sec, name, n_q):
-    """The tensor path sorts each chunk's nonzeros by the dimensions the
-    queries hold outside the hot set: a call's lists must be the CSC of its
-    chunk restricted to exactly those dimensions, with the stored values,
-    bit for bit; two builds in a row reuse the queries' numbering, and the
-    last chunk of a two-chunk build gets its own lists."""
+def test_query_lists_are_the_normalised_queries_csc_over_their_cold_dims(sec, name, n_q):
+    """The tensor path sorts the queries' nonzeros outside the hot set by
+    dimension, once per query matrix: its lists must be the CSC of the
+    normalised queries restricted to exactly those dimensions, bit for bit
+    (each value the float32 product of the stored value and its row's
+    inverse norm), the same for every chunk of a build and for a second
+    build scored with them."""
     cfg = CONFIGS[name]
     Q, I = generate_rows(cfg, 0, 0, n_q), generate_rows(cfg, 1, 0, 9000)
-    with sec.SparseCosine(cfg.dim, chunk_rows=8192, algorithm="tensor") as h:
+    with sec.SparseCosine(cfg.dim, chunk_rows=4500, algorithm="tensor") as h:
         q, i = _dev(sec, Q), _dev(sec, I)
         inv_q, inv_i = h.row_norms(q), h.row_norms(i)
         exports = []
-        for rb, re in ((0, 8192), (8192, 9000)):
-            idx = h.build_item_index(i, rb, re)
-            hot = h.index_export(idx)["hot"]
-            out = torch.empty((n_q, re - rb), dtype=torch.float32, device="cuda")
-            h.score_chunk(q, inv_q, idx, inv_i[rb:], out, re - rb)
+        views = h.build_item_indexes(i, 0, 9000)
+        assert len(views) == 2
+        hot = h.index_export(views[0][2])["hot"]
+        for b, e, vw in views:
+            out = torch.empty((n_q, e - b), dtype=torch.float32, device="cuda")
+            h.score_chunk(q, inv_q, vw, inv_i[b:], out, e - b)
             h.check_device()
-            exports.append((rb, re, hot, h.lists_export()))
-        # one build of two chunks: the second chunk's lists
-        h2 = sec.SparseCosine(cfg.dim, chunk_rows=4500, algorithm="tensor")
-        try:
-            inv2, invq2 = h2.row_norms(i), h2.row_norms(q)
-            views = h2.build_item_indexes(i, 0, 9000)
-            assert len(views) == 2
-            for b, e, vw in views:
-                out = torch.empty((n_q, e - b), dtype=torch.float32, device="cuda")
-                h2.score_chunk(q, invq2, vw, inv2[b:], out, e - b)
-            h2.check_device()
-            hot2 = h2.index_export(views[1][2])["hot"]
-            exports.append((4500, 9000, hot2, h2.lists_export()))
-        finally:
-            h2.close()
-    for rb, re, hot_c, ex in exports:
-        qcold = np.setdiff1d(np.unique(Q.indices), hot_c)  # the queries' cold dimensions
-        assert np.array_equal(ex["dims"], qcold.astype(np.int32))
-        chunk = _scipy(I, rb, re)
-        csc = chunk[:, qcold].tocsc()
-        csc.sort_indices()
-        assert np.array_equal(ex["col_ptr"].astype(np.int64), csc.indptr.astype(np.int64)), rb
-        assert np.array_equal(ex["item"], csc.indices.astype(np.int32)), rb
-        assert np.array_equal(ex["value"].view(np.uint32), csc.data.astype(np.float32).view(np.uint32)), rb
+            exports.append(h.lists_export())
+        idx = h.build_item_index(i, 0, 4500)  # a second build with the same queries
+        out = torch.empty((n_q, 4500), dtype=torch.float32, device="cuda")
+        h.score_chunk(q, inv_q, idx, inv_i, out, 4500)
+        h.check_device()
+        exports.append(h.lists_export())
+        invq = inv_q.cpu().numpy()
+    qs = _scipy(Q)
+    rows = np.repeat(np.arange(n_q), np.diff(qs.indptr))
+    norm = sp.csr_matrix((qs.data.astype(np.float32) * invq[rows], qs.indices, qs.indptr), shape=qs.shape)
+    qcold = np.setdiff1d(np.unique(Q.indices), hot)  # the queries' cold dimensions
+    csc = norm[:, qcold].tocsc()
+    csc.sort_indices()
+    for k, ex in enumerate(exports):
+        assert np.array_equal(ex["dims"], qcold.astype(np.int32)), k
+        assert np.array_equal(ex["col_ptr"].astype(np.int64), csc.indptr.astype(np.int64)), k
+        assert np.array_equal(ex["query"], csc.indices.astype(np.int32)), k
+        assert np.array_equal(ex["value"].view(np.uint32), csc.data.astype(np.float32).view(np.uint32)), k
 
 
 def test_index_export_rejects_item_tiles(sec):
