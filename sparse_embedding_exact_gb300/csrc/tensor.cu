@@ -774,6 +774,7 @@ struct RecArgs {
   int32_t *status;
   int64_t n_main;          // column blocks with a block of their own (whole waves of blocks)
   int64_t n_shared;        // blocks sharing the items of the column blocks after those
+  int32_t pieces;          // main blocks: the parts each item's walk is cut into
   PrepArgs prep;           // the chunk's item operand (the blocks after all of these)
 };
 
@@ -904,16 +905,30 @@ __global__ void __launch_bounds__(kRThreads, 2) k_tc_records(const RecArgs a) {
   const int tid = threadIdx.x;
   const int64_t cb = bid;
   const int nqt = (int)a.n_quarters;
+  __shared__ int next_part;
+  if (tid == 0) next_part = 0;
   for (int c = tid; c < nqt; c += kRThreads) rcnt[c] = 0;
   __syncthreads();
-  for (int il = warp; il < 32; il += kRThreads / 32) {  // the block's items, a warp to each in turn
+  // The block's 32 items, each cut into `pieces` parts (part k walks the
+  // windows k, k + pieces, ... of the item's lists): a warp takes the next
+  // part as it finishes one, so items of unequal length even out.
+  const int parts = 32 * a.pieces;
+  for (;;) {
+    int u = 0;
+    if (lane == 0) u = atomicAdd(&next_part, 1);
+    u = __shfl_sync(0xffffffffu, u, 0);
+    if (u >= parts) break;
+    const int il = u & 31, piece = u >> 5;
     const int it = (int)(cb * 32 + il);
     if (it < a.n_items)
-      walk_item(a, it, lane, slots, [&](int q, int p) {
-        const int Q = q >> 5;
-        const int slot = atomicAdd(&rcnt[Q], 1);
-        if (slot < cap) a.rec[((int64_t)Q * ncb + cb) * cap + slot] = make_int2(stg_index(q & 31, il), p);
-      });
+      walk_item(
+          a, it, lane, slots,
+          [&](int q, int p) {
+            const int Q = q >> 5;
+            const int slot = atomicAdd(&rcnt[Q], 1);
+            if (slot < cap) a.rec[((int64_t)Q * ncb + cb) * cap + slot] = make_int2(stg_index(q & 31, il), p);
+          },
+          piece, a.pieces);
   }
   __syncthreads();
   for (int c = tid; c < nqt; c += kRThreads) a.rec_n[(int64_t)c * ncb + cb] = rcnt[c] <= cap ? rcnt[c] : -1;
@@ -1701,6 +1716,9 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     // SM one runs as main blocks only; a smaller one is shared out.
     ra.n_main = !own ? 0 : (n_cb <= wave && 2 * n_cb >= wave) ? n_cb : n_cb / wave * wave;
     ra.n_shared = ra.n_main < n_cb ? wave : 0;
+    // An item's walk is cut into parts of about 32 windows of 32 records
+    // (the sample's estimate of its records: est x n_q), at most 8.
+    ra.pieces = (int32_t)std::max<double>(1.0, std::min<double>(8.0, std::floor(est * (double)n_q / 1024.0)));
     // The shared column blocks' counters: [n_main, n_cb) of every quarter.
     if (ra.n_shared > 0 &&
         (e = cudaMemset2DAsync(h->tc_rec_n + ra.n_main, sizeof(int32_t) * (size_t)n_cb, 0,
