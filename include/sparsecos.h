@@ -465,7 +465,8 @@ ss_status ss_index_export(ss_handle *h, const ss_index *idx, int32_t *n_hot, int
  *   col_ptr[0 .. n_dims]: list k (dimension dims[k]) is entries
  *     [col_ptr[k], col_ptr[k + 1]);
  *   query[e]: the query row, ascending inside a list (sorted here; the
- *     device keeps no order, which no sum depends on);
+ *     device keeps no order, which no sum depends on, and one set of lists
+ *     per slice of query rows, merged here);
  *   value[e]: the query's value times its row's inverse norm (float32).
  * Any output may be NULL; dims and col_ptr need room for dim + 1 entries,
  * query and value capacity >= *n_entries.

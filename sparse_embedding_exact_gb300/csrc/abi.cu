@@ -740,23 +740,26 @@ ss_status ss_lists_export(ss_handle *h, int64_t *n_dims, int32_t *dims, int32_t 
   ss_status st = set_device(h);
   if (st != SS_OK) return st;
   SS_CUDA(h, cudaStreamSynchronize(as_stream(stream)));
-  const int64_t dim = h->dim;
-  std::vector<int32_t> off((size_t)dim + 1);
+  const int64_t dim = h->dim, S = h->tcq_slices, stride = dim + 1;
+  std::vector<int32_t> off((size_t)(S * stride));
   SS_CUDA(h, cudaMemcpy(off.data(), h->tc_qptr, sizeof(int32_t) * off.size(), cudaMemcpyDeviceToHost));
-  const int64_t n = off[(size_t)dim];
-  if (off[0] != 0 || n < 0 || n > h->tc_qlist_cap)
+  const int64_t n = S > 0 ? off[(size_t)(S * stride - 1)] : 0;
+  if (S < 1 || off[0] != 0 || n < 0 || n > h->tc_qlist_cap)
     return fail(h, SS_ERR_DEVICE_CHECK, "ss_lists_export: offsets outside the lists");
-  std::vector<int32_t> ptr(1, 0);
-  std::vector<int32_t> held;
+  for (int64_t k = 1; k < S * stride; ++k)
+    if (off[(size_t)k] < off[(size_t)k - 1]) return fail(h, SS_ERR_DEVICE_CHECK, "ss_lists_export: offsets not ascending");
+  // The slices' lists of each dimension, merged.
+  std::vector<int32_t> ptr(1, 0), held;
   for (int64_t d = 0; d < dim; ++d) {
-    if (off[(size_t)d + 1] < off[(size_t)d])
-      return fail(h, SS_ERR_DEVICE_CHECK, "ss_lists_export: offsets not ascending");
-    if (off[(size_t)d + 1] > off[(size_t)d]) {
+    int64_t len = 0;
+    for (int64_t sl = 0; sl < S; ++sl) len += off[(size_t)(sl * stride + d + 1)] - off[(size_t)(sl * stride + d)];
+    if (len > 0) {
       held.push_back((int32_t)d);
-      ptr.push_back(off[(size_t)d + 1]);
+      ptr.push_back(ptr.back() + (int32_t)len);
     }
   }
   const int64_t nd = (int64_t)held.size();
+  if (ptr.back() != n) return fail(h, SS_ERR_DEVICE_CHECK, "ss_lists_export: slices inconsistent");
   if (n_dims) *n_dims = nd;
   if (n_entries) *n_entries = n;
   if (dims && nd > 0) memcpy(dims, held.data(), sizeof(int32_t) * held.size());
@@ -765,11 +768,16 @@ ss_status ss_lists_export(ss_handle *h, int64_t *n_dims, int32_t *dims, int32_t 
     if (capacity < n)
       return fail(h, SS_ERR_LIMIT, "ss_lists_export: %lld entries exceed capacity %lld", (long long)n,
                   (long long)capacity);
-    std::vector<int2> ent((size_t)n);
-    if (n > 0) SS_CUDA(h, cudaMemcpy(ent.data(), h->tc_qlist, sizeof(int2) * (size_t)n, cudaMemcpyDeviceToHost));
-    for (int64_t k = 0; k < nd; ++k)  // each list by ascending query row (the device order is unspecified)
-      std::sort(ent.begin() + ptr[(size_t)k], ent.begin() + ptr[(size_t)k + 1],
-                [](const int2 &x, const int2 &y) { return x.x < y.x; });
+    std::vector<int2> raw((size_t)n), ent;
+    ent.reserve((size_t)n);
+    if (n > 0) SS_CUDA(h, cudaMemcpy(raw.data(), h->tc_qlist, sizeof(int2) * (size_t)n, cudaMemcpyDeviceToHost));
+    for (int64_t k = 0; k < nd; ++k) {
+      const int64_t d = held[(size_t)k];
+      for (int64_t sl = 0; sl < S; ++sl)
+        ent.insert(ent.end(), raw.begin() + off[(size_t)(sl * stride + d)], raw.begin() + off[(size_t)(sl * stride + d + 1)]);
+      // each list by ascending query row (the device order is unspecified)
+      std::sort(ent.begin() + ptr[(size_t)k], ent.end(), [](const int2 &x, const int2 &y) { return x.x < y.x; });
+    }
     for (int64_t p = 0; p < n; ++p) {
       if (query) query[p] = ent[(size_t)p].x;
       if (value) memcpy(value + p, &ent[(size_t)p].y, sizeof(float));

@@ -288,9 +288,11 @@ struct ss_handle {
   const void *tcq_src[4] = {nullptr, nullptr, nullptr, nullptr};
   int64_t tcq_rows = -1, tcq_nnz = -1;
   uint64_t tcq_generation = ~0ull;
-  // The queries' lists by dimension (CSC of their cold entries): counters
-  // (then cursors) [dim + 1], offsets [dim + 1], the scan's tile sums, the
-  // entries {query row, normalised value bits} [nnz of the queries].
+  // The queries' lists by dimension (CSC of their cold entries), one set
+  // per slice of tcq_slice_rows query rows: counters (then cursors) and
+  // offsets [slices][dim + 1], the scan's tile sums, the entries {query
+  // row, normalised value bits} [nnz of the queries].
+  int64_t tcq_slice_rows = 1, tcq_slices = 0;
   int32_t *tc_qcnt = nullptr, *tc_qptr = nullptr, *tc_qpart = nullptr;
   int64_t tc_qcnt_cap = 0, tc_qptr_cap = 0, tc_qpart_cap = 0;
   int2 *tc_qlist = nullptr;

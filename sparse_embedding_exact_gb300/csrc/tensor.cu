@@ -91,6 +91,7 @@ constexpr int kTailBytes = kEpiWarps * 2 * kTailRecs * 8;
 static_assert(kEpiWarps % 4 == 0 && 8 % kWarpsPerQ == 0, "whole blocks per epilogue warp");
 constexpr int kRThreads = 512;          // records: a block per 32-item column block, two per SM
 constexpr int64_t kRecMaxQuarters = 16384;  // records: bucket counters in shared memory up to this many
+constexpr double kRecSliceBytes = 48.0 * (1 << 20);  // records: expected bytes of one launch's buckets
 constexpr int kPrepThreads = 256;
 constexpr int kWalkUnroll = 8;          // list entries per lane loaded before use
 constexpr int kRecPerLane = 4;          // epilogue: a block's first records per lane (128), fetched two blocks ahead
@@ -553,7 +554,10 @@ __global__ void __launch_bounds__(256)
 }
 
 // The queries' lists, once per query matrix, inverse norms and hot set: a
-// counting sort of the queries' cold entries by dimension.  The counts per
+// counting sort of the queries' cold entries by (slice of query rows,
+// dimension), each slice holding its own set of d + 1 offsets.  A records
+// launch walks one slice's lists, so that the buckets it fills at once
+// stay few enough for their partly written lines to remain in L2.  The counts per
 // dimension (k_tc_qcount), their exclusive scan (launch_count_scan: list d
 // is entries [qptr[d], qptr[d + 1]) and is empty for a dimension no query
 // row holds cold; the scan leaves each counter at its list's start), then
@@ -563,28 +567,31 @@ __global__ void __launch_bounds__(256)
 // the same lists from its chunk's items, so nothing is sorted per chunk.
 __global__ void __launch_bounds__(256)
     k_tc_qcount(const int64_t *__restrict__ q_indptr, const int2 *__restrict__ qcold,
-                const int32_t *__restrict__ qcold_n, int64_t n_q, int32_t *__restrict__ count) {
+                const int32_t *__restrict__ qcold_n, int64_t n_q, int64_t slice_rows, int64_t stride,
+                int32_t *__restrict__ count) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * 8;
   for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < n_q; r += warps) {
     const int64_t b = q_indptr[r];
     const int n = qcold_n[r];
-    for (int j = lane; j < n; j += 32) atomicAdd(count + __ldg(qcold + b + j).x, 1);
+    int32_t *cnt = count + (r / slice_rows) * stride;
+    for (int j = lane; j < n; j += 32) atomicAdd(cnt + __ldg(qcold + b + j).x, 1);
   }
 }
 
 __global__ void __launch_bounds__(256)
     k_tc_qscatter(const int64_t *__restrict__ q_indptr, const int2 *__restrict__ qcold,
-                  const int32_t *__restrict__ qcold_n, int64_t n_q, int32_t *__restrict__ cursor,
-                  int2 *__restrict__ qlist) {
+                  const int32_t *__restrict__ qcold_n, int64_t n_q, int64_t slice_rows, int64_t stride,
+                  int32_t *__restrict__ cursor, int2 *__restrict__ qlist) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * 8;
   for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < n_q; r += warps) {
     const int64_t b = q_indptr[r];
     const int n = qcold_n[r];
+    int32_t *cur = cursor + (r / slice_rows) * stride;
     for (int j = lane; j < n; j += 32) {
       const int2 e = __ldg(qcold + b + j);
-      qlist[atomicAdd(cursor + e.x, 1)] = make_int2((int)r, e.y);
+      qlist[atomicAdd(cur + e.x, 1)] = make_int2((int)r, e.y);
     }
   }
 }
@@ -764,9 +771,10 @@ struct RecArgs {
   const int2 *icold_rng;   // per item of the chunk: {first entry, count}
   int32_t n_items;
   const float *inv_i;      // the chunk's inverse norms
-  const int32_t *qptr;     // the queries' lists: [dim + 1] offsets into qlist
+  const int32_t *qptr;     // the slice's lists: [dim + 1] offsets into qlist
   const int2 *qlist;       // {query row, normalised value bits}
-  int64_t n_quarters;      // 32-row groups of queries
+  int64_t q0;              // the slice's first quarter (32-row group of queries)
+  int64_t n_quarters;      // the slice's quarters
   int32_t n_cb;            // 32-item column blocks of the chunk
   int32_t bucket_cap;      // records a bucket holds
   int2 *rec;               // [quarter][column block][bucket_cap]
@@ -901,7 +909,7 @@ __global__ void __launch_bounds__(kRThreads, 2) k_tc_records(const RecArgs a) {
     }
     return;
   }
-  extern __shared__ int rcnt[];  // [n_quarters]
+  extern __shared__ int rcnt[];  // [n_quarters] from q0
   const int tid = threadIdx.x;
   const int64_t cb = bid;
   const int nqt = (int)a.n_quarters;
@@ -925,13 +933,13 @@ __global__ void __launch_bounds__(kRThreads, 2) k_tc_records(const RecArgs a) {
           a, it, lane, slots,
           [&](int q, int p) {
             const int Q = q >> 5;
-            const int slot = atomicAdd(&rcnt[Q], 1);
+            const int slot = atomicAdd(&rcnt[Q - a.q0], 1);
             if (slot < cap) a.rec[((int64_t)Q * ncb + cb) * cap + slot] = make_int2(stg_index(q & 31, il), p);
           },
           piece, a.pieces);
   }
   __syncthreads();
-  for (int c = tid; c < nqt; c += kRThreads) a.rec_n[(int64_t)c * ncb + cb] = rcnt[c] <= cap ? rcnt[c] : -1;
+  for (int c = tid; c < nqt; c += kRThreads) a.rec_n[(a.q0 + c) * ncb + cb] = rcnt[c] <= cap ? rcnt[c] : -1;
 }
 
 // ---------------------------------------------------------------- scorer
@@ -947,7 +955,9 @@ struct ScoreArgs {
   // queries' lists.
   const int2 *icold;
   const int2 *icold_rng;
-  const int32_t *qptr;
+  const int32_t *qptr;     // slice s's offsets at qptr + s * qptr_stride
+  int64_t qptr_stride;
+  int64_t slice_rows;
   const int2 *qlist;
   const float *inv_i;
   int64_t n_quarters;
@@ -1305,11 +1315,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
             if (it < a.n_items) {
               const int2 rng = __ldg(a.icold_rng + it);
               const float ivi = __ldg(a.inv_i + it);
+              const int32_t *qp = a.qptr + (int64_t)qrow0 / a.slice_rows * a.qptr_stride;  // the rows' slice
               for (int e = 0; e < rng.y; ++e) {
                 const int2 ie = __ldg(a.icold + rng.x + e);
                 const float iv = __int_as_float(ie.y) * ivi;
-                const int p1 = __ldg(a.qptr + ie.x + 1);
-                for (int p = __ldg(a.qptr + ie.x); p < p1; ++p) {
+                const int p1 = __ldg(qp + ie.x + 1);
+                for (int p = __ldg(qp + ie.x); p < p1; ++p) {
                   const int2 qe = __ldg(a.qlist + p);
                   const int d = qe.x - (int)qrow0;
                   if ((unsigned)d < 32u) atomicAdd(stg + stg_index(d, lane), cold_fix(__int_as_float(qe.y), iv));
@@ -1606,7 +1617,14 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
         h->tcq_src[3] == inv_q && h->tcq_rows == q.n_rows && h->tcq_nnz == q.nnz &&
         h->tcq_generation == h->tc_hot_generation)) {
     h->tcq_rows = -1;  // not prepared until the end of this block
-    const int64_t n_cnt = dim + 1;
+    // Slices of whole query tiles whose records in one chunk (the sample's
+    // estimate) take about kRecSliceBytes: one records launch each.
+    const double quarter_bytes =
+        8.0 * std::max(1e-3, h->tc_est_cold) * 1024.0 * (double)((h->chunk_rows + kColBlock - 1) / kColBlock);
+    const int64_t tiles_per_slice = std::max<int64_t>(1, (int64_t)((double)kRecSliceBytes / quarter_bytes) / (kM / 32));
+    const int64_t slice_rows = std::min<int64_t>(n_qtiles, tiles_per_slice) * kM;
+    const int64_t n_slices = (n_q + slice_rows - 1) / slice_rows;
+    const int64_t n_cnt = n_slices * (dim + 1);
     if ((e = grow(&h->tc_A, &h->tc_A_cap, n_qtiles * kM * 2 * Hp, s)) != cudaSuccess) return e;
     if ((e = grow(&h->tc_qcold, &h->tc_qcold_cap, std::max<int64_t>(1, q.nnz), s)) != cudaSuccess) return e;
     if ((e = grow(&h->tc_qcold_n, &h->tc_qcold_n_cap, n_q, s)) != cudaSuccess) return e;
@@ -1635,10 +1653,11 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     k_tc_prep_queries<<<(unsigned)blocks, kPrepThreads, 0, s>>>(pa);
     if ((e = cudaMemsetAsync(h->tc_qcnt, 0, sizeof(int32_t) * (size_t)n_cnt, s)) != cudaSuccess) return e;
     const int64_t row_blocks = std::min<int64_t>((n_q + 7) / 8, (int64_t)sms * 8);
-    k_tc_qcount<<<(unsigned)row_blocks, 256, 0, s>>>(q.indptr, h->tc_qcold, h->tc_qcold_n, n_q, h->tc_qcnt);
+    k_tc_qcount<<<(unsigned)row_blocks, 256, 0, s>>>(q.indptr, h->tc_qcold, h->tc_qcold_n, n_q, slice_rows, dim + 1,
+                                                     h->tc_qcnt);
     if ((e = launch_count_scan(h->tc_qcnt, n_cnt, h->tc_qpart, h->tc_qptr, s)) != cudaSuccess) return e;
-    k_tc_qscatter<<<(unsigned)row_blocks, 256, 0, s>>>(q.indptr, h->tc_qcold, h->tc_qcold_n, n_q, h->tc_qcnt,
-                                                       h->tc_qlist);
+    k_tc_qscatter<<<(unsigned)row_blocks, 256, 0, s>>>(q.indptr, h->tc_qcold, h->tc_qcold_n, n_q, slice_rows,
+                                                       dim + 1, h->tc_qcnt, h->tc_qlist);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     nq += 6;
     h->tcq_src[0] = q.indptr;
@@ -1648,7 +1667,10 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     h->tcq_rows = q.n_rows;
     h->tcq_nnz = q.nnz;
     h->tcq_generation = h->tc_hot_generation;
+    h->tcq_slice_rows = slice_rows;
+    h->tcq_slices = n_slices;
   }
+  const int64_t slice_rows = h->tcq_slice_rows, n_slices = h->tcq_slices;
 
   // Item operand of this chunk (written by the records launch's trailing
   // blocks).
@@ -1684,15 +1706,20 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
       1024.0, std::max<double>(64.0, std::ceil((3.0 * est * 1024.0 + 64.0) / 32.0) * 32.0));
   if ((e = grow(&h->tc_rec_n, &h->tc_rec_n_cap, n_quarters * n_cb, s)) != cudaSuccess) return e;
   if ((e = grow(&h->tc_rec, &h->tc_rec_cap, n_quarters * n_cb * (int64_t)cap, s)) != cudaSuccess) return e;
-  {
+  // One records launch per slice of query rows; the first also writes the
+  // item operand (its trailing blocks).
+  for (int64_t sl = 0; sl < n_slices; ++sl) {
+    const int64_t q_lo = sl * slice_rows, q_hi = std::min<int64_t>(n_q, q_lo + slice_rows);
+    const int64_t q0 = q_lo / 32, nqs = (q_hi + 31) / 32 - q0;  // the slice's quarters
     RecArgs ra;
     ra.icold = idx.icold;
     ra.icold_rng = idx.icold_rng;
     ra.n_items = n_items;
     ra.inv_i = inv_i;
-    ra.qptr = h->tc_qptr;
+    ra.qptr = h->tc_qptr + sl * (dim + 1);
     ra.qlist = h->tc_qlist;
-    ra.n_quarters = n_quarters;
+    ra.q0 = q0;
+    ra.n_quarters = nqs;
     ra.n_cb = n_cb;
     ra.bucket_cap = cap;
     ra.rec = h->tc_rec;
@@ -1701,8 +1728,8 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     ra.prep = pa;
     // A main block counts its buckets in shared memory (one counter per
     // quarter); past kRecMaxQuarters every item goes the shared way.
-    const bool own = n_quarters <= kRecMaxQuarters;
-    const size_t smem = own ? sizeof(int) * (size_t)n_quarters : 0;
+    const bool own = nqs <= kRecMaxQuarters;
+    const size_t smem = own ? sizeof(int) * (size_t)nqs : 0;
     if ((e = ensure_dyn_smem(k_tc_records, smem)) != cudaSuccess) return e;
     // Whole waves of column blocks, then one wave sharing the rest.
     int per_sm = 0;
@@ -1717,15 +1744,16 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     ra.n_main = !own ? 0 : (n_cb <= wave && 2 * n_cb >= wave) ? n_cb : n_cb / wave * wave;
     ra.n_shared = ra.n_main < n_cb ? wave : 0;
     // An item's walk is cut into parts of about 32 windows of 32 records
-    // (the sample's estimate of its records: est x n_q), at most 8.
-    ra.pieces = (int32_t)std::max<double>(1.0, std::min<double>(8.0, std::floor(est * (double)n_q / 1024.0)));
-    // The shared column blocks' counters: [n_main, n_cb) of every quarter.
+    // (the sample's estimate of its records in the slice: est x rows), at
+    // most 8.
+    ra.pieces = (int32_t)std::max<double>(1.0, std::min<double>(8.0, std::floor(est * (double)(q_hi - q_lo) / 1024.0)));
+    // The shared column blocks' counters: [n_main, n_cb) of the slice's quarters.
     if (ra.n_shared > 0 &&
-        (e = cudaMemset2DAsync(h->tc_rec_n + ra.n_main, sizeof(int32_t) * (size_t)n_cb, 0,
-                               sizeof(int32_t) * (size_t)(n_cb - ra.n_main), (size_t)n_quarters, s)) != cudaSuccess)
+        (e = cudaMemset2DAsync(h->tc_rec_n + q0 * n_cb + ra.n_main, sizeof(int32_t) * (size_t)n_cb, 0,
+                               sizeof(int32_t) * (size_t)(n_cb - ra.n_main), (size_t)nqs, s)) != cudaSuccess)
       return e;
     // The operand's blocks (a warp per group of 8 items) come last.
-    const int64_t prep_blocks = (pa.n_groups + kRThreads / 32 - 1) / (kRThreads / 32);
+    const int64_t prep_blocks = sl == 0 ? (pa.n_groups + kRThreads / 32 - 1) / (kRThreads / 32) : 0;
     k_tc_records<<<(unsigned)(ra.n_main + ra.n_shared + prep_blocks), kRThreads, smem, s>>>(ra);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ++nq;
@@ -1752,6 +1780,8 @@ cudaError_t launch_score_tc(ss_handle *h, const ss_csr &q, const float *inv_q, c
     sa.icold = idx.icold;
     sa.icold_rng = idx.icold_rng;
     sa.qptr = h->tc_qptr;
+    sa.qptr_stride = dim + 1;
+    sa.slice_rows = slice_rows;
     sa.qlist = h->tc_qlist;
     sa.inv_i = inv_i;
     sa.n_quarters = n_quarters;

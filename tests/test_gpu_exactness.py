@@ -291,6 +291,41 @@ def test_full_matrix_of_the_1_2m_workload(sec):
     assert worst <= TOL
 
 
+def test_query_slices_of_the_1_2m_workload(sec):
+    """24,000 queries: the queries' lists come in several slices of rows
+    (one records launch each); sampled rows of every slice, the slices'
+    first and last rows among them, match the oracle over a whole chunk,
+    and the exported lists merge the slices into the queries' CSC."""
+    from workload import sample_query_rows
+
+    cfg = CONFIGS["d1.2m_q5k_i200k"].scaled(24_000, 8192)
+    Q, I = generate_side(cfg, 0), generate_side(cfg, 1)
+    with sec.SparseCosine(cfg.dim, chunk_rows=8192, algorithm="tensor") as h:
+        q, i = _dev(sec, Q), _dev(sec, I)
+        inv_q, inv_i = h.row_norms(q), h.row_norms(i)
+        S = h.score_all(q, inv_q, i, inv_i)
+        h.check_device()
+        ex = h.lists_export()
+        hot = h.index_export(h.build_item_index(i, 0, 8192))["hot"]
+        rows = np.unique(np.concatenate([sample_query_rows(Q.n_rows, 192), np.arange(0, Q.n_rows, 2560),
+                                         np.arange(2559, Q.n_rows, 2560), [Q.n_rows - 1]])).astype(np.int64)
+        got = S[torch.as_tensor(rows, device=S.device)].cpu().numpy().astype(np.float64)
+        invq = inv_q.cpu().numpy()
+    err = float(np.abs(got - oracle.cosine(Q, I, q_rows=rows, f64=True)).max())
+    print(f"24,000 x 8,192 in query slices: max |error| {err:.3e}")
+    assert err <= TOL
+    qs = _scipy(Q)
+    norm = sp.csr_matrix((qs.data.astype(np.float32) * invq[np.repeat(np.arange(Q.n_rows), np.diff(qs.indptr))],
+                          qs.indices, qs.indptr), shape=qs.shape)
+    qcold = np.setdiff1d(np.unique(Q.indices), hot)
+    csc = norm[:, qcold].tocsc()
+    csc.sort_indices()
+    assert np.array_equal(ex["dims"], qcold.astype(np.int32))
+    assert np.array_equal(ex["col_ptr"].astype(np.int64), csc.indptr.astype(np.int64))
+    assert np.array_equal(ex["query"], csc.indices.astype(np.int32))
+    assert np.array_equal(ex["value"].view(np.uint32), csc.data.astype(np.float32).view(np.uint32))
+
+
 # ------------------------------------------------------------------ record overflow paths
 def test_tensor_records_beyond_every_buffer(sec):
     """Queries far denser in the items' cold dimensions than the item sample
