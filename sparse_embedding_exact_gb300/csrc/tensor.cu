@@ -20,13 +20,12 @@
 // FP32: the dropped lo_q lo_v and the splitting error are below 2^-22 |x|
 // (2^-25 absolute for values in fp16's subnormal range).
 //
-// The remaining ("cold") dimensions are few per pair (0.11 expected on the
-// 1.2M-word workload).  Once per query matrix the dimensions the queries
-// hold cold are numbered; the first scoring call after a build sorts the
-// build's nonzeros in those dimensions into lists by number, per chunk (a
-// counting sort: the other nonzeros make no product), and a records kernel
-// walks, for every block of 32 query rows, each row's cold nonzeros against
-// the chunk's lists and
+// The remaining ("cold") dimensions are few per pair (0.09 expected on the
+// 1.2M-word workload with 160 hot dimensions).  Once per query matrix the
+// queries' cold nonzeros are sorted into lists by dimension (a counting
+// sort, one set of lists per slice of query rows), and for each chunk a
+// records kernel walks every item's cold nonzeros against the lists of
+// their dimensions (a dimension no query holds cold has an empty list) and
 // writes one record per product, bucketed by (32 query rows, 32 items):
 // the position inside the bucket and the product rounded to a fixed-point
 // integer of resolution 2^-28.  The scorer's epilogue adds a bucket's
